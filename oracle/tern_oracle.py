@@ -1,0 +1,408 @@
+"""CPU oracle for the ternary-weight linear layer.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plain reference that the
+CUDA library is checked against.  Only the test suite, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import it; the
+product path never does.  It shares no code with the CUDA kernels.
+
+Source of the method: the page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM
+TP=2" (qiita.com/nakanokensetsu/items/ecc183fae033565af7cb):
+
+* "前提" (premises): weights are codes in {-1,0,+1} stored at 2 bits with one
+  scale per 128 elements of a row, and a block-wise Hadamard rotation is
+  applied on the input side;
+* section 1 "TP=2 への移植": the rotation is a Sylvester Hadamard of block 1024
+  with the split identity H1024[a;b] = [H512 a + H512 b ; H512 a - H512 b],
+  which is the last butterfly stage of the kernel;
+* section 4 "効いた高速化", int8 prefill: q[n,g] = round(127 s[n,g] / smax[n]),
+  W_int8[n,k] = code[n,k] q[n,k/128] fits int8 exactly, activations are
+  quantised to int8 per token after the rotation, one int8 GEMM, then a
+  per-row and per-token rescale.
+
+Two references live here:
+
+O1 (exact, fp64)        rotate_f64 / dequant_f64 / linear_f64
+O2 (int8 path, spec-exact fp32 operation sequence)
+                        fwht_f32 / quant_tokens / decompose_scales /
+                        w_int8 / acc_int8 / y_int8 / linear_int8
+
+plus the 2-bit storage format (pack_codes / unpack_codes / pack_scales), which
+the pages leave open and this library defines (see ``include/tern.h``).
+
+Readings of the pages taken here (each is also listed in the design notes):
+* natural (Sylvester) order H, not sequency order; normalised by 1/32 per block;
+* the butterfly stages run with stride 1, 2, 4, ..., 512, so the stride-512
+  stage (the printed split identity) is the last one;
+* the optional "rotation sign table" is a +-1 vector applied to x before H;
+* group index g = floor(k/128) within the row;
+* smax[n] = max_g |s[n,g]|; q = rint((127*s)/smax) in fp32, left to right as
+  printed, round half to even; rscale = smax/127; a zero row gives q = 0,
+  rscale = 0;
+* per-token symmetric absmax quantisation over the whole row of K:
+  tscale = absmax/127, xq = clamp(rint(xr / tscale), -127, 127); a zero token
+  gives xq = 0, tscale = 0;
+* y = bf16_rn(((float)acc * tscale[m]) * rscale[n]), fp32 left to right.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+HBLOCK = 1024          # Hadamard block width (page 1, section 1)
+GROUP = 128            # elements per scale group (page 1, premises)
+INV_SQRT_BLOCK = 1.0 / 32.0
+
+
+# --------------------------------------------------------------------------
+# Hadamard rotation
+# --------------------------------------------------------------------------
+
+def hadamard_dense(n: int) -> np.ndarray:
+    """Natural-order Sylvester Hadamard matrix of size n (fp64, entries +-1).
+
+    H_1 = [1];  H_2m = [[H_m, H_m], [H_m, -H_m]]  (page 1, section 1: the
+    recursive Sylvester structure behind the split identity).
+    """
+    if n < 1 or (n & (n - 1)) != 0:
+        raise ValueError("n must be a power of two")
+    h = np.ones((1, 1), dtype=np.float64)
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+_H1024 = None
+
+
+def _h1024() -> np.ndarray:
+    global _H1024
+    if _H1024 is None:
+        _H1024 = hadamard_dense(HBLOCK)
+    return _H1024
+
+
+def rotate_f64(x, sign=None) -> np.ndarray:
+    """O1 rotation: xr = (I_B kron H1024/32) (sign * x), exactly, in fp64.
+
+    Computed as a dense matrix product per 1024-block (page 1, premises and
+    section 1), deliberately not as butterflies.
+    x: [M, K] (any float dtype), K a multiple of 1024.  sign: None or [K] of +-1.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, k = x.shape
+    if k % HBLOCK:
+        raise ValueError("K must be a multiple of 1024")
+    if sign is not None:
+        x = x * np.asarray(sign, dtype=np.float64)[None, :]
+    h = _h1024()
+    out = np.empty_like(x)
+    for b in range(k // HBLOCK):
+        blk = x[:, b * HBLOCK:(b + 1) * HBLOCK]
+        out[:, b * HBLOCK:(b + 1) * HBLOCK] = (blk @ h.T) * INV_SQRT_BLOCK
+    return out
+
+
+def fwht_f32(x, sign=None) -> np.ndarray:
+    """O2 rotation: the canonical fast Walsh-Hadamard transform in fp32.
+
+    Per 1024-block, butterfly stages with stride h = 1, 2, 4, ..., 512 in that
+    order; each butterfly maps (u, v) -> (u + v, u - v) with u the lower index.
+    The last stage (h = 512) is the split identity printed on page 1,
+    section 1.  Then every element is multiplied by 1/32 (exact).  Every
+    operation is one correctly rounded fp32 add, subtract or multiply.
+    x: [M, K]; bf16 inputs must be passed already widened to fp32 (exact).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    m, k = x.shape
+    if k % HBLOCK:
+        raise ValueError("K must be a multiple of 1024")
+    if sign is not None:
+        x = x * np.asarray(sign, dtype=np.float32)[None, :]
+    v = x.reshape(m, k // HBLOCK, HBLOCK).copy()
+    h = 1
+    while h < HBLOCK:
+        w = v.reshape(m, k // HBLOCK, HBLOCK // (2 * h), 2, h)
+        lo = w[:, :, :, 0, :]
+        hi = w[:, :, :, 1, :]
+        s = lo + hi
+        d = lo - hi
+        v = np.stack([s, d], axis=3).reshape(m, k // HBLOCK, HBLOCK)
+        h *= 2
+    v = v * np.float32(INV_SQRT_BLOCK)
+    return v.reshape(m, k).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# Weights: dequantisation (O1) and the scale decomposition (O2)
+# --------------------------------------------------------------------------
+
+def dequant_f64(codes, scales) -> np.ndarray:
+    """O1 weight: W[n,k] = code[n,k] * s[n, k // 128] in fp64 (page 1, premises)."""
+    codes = np.asarray(codes)
+    s = np.asarray(scales).astype(np.float64)
+    return codes.astype(np.float64) * np.repeat(s, GROUP, axis=1)
+
+
+def decompose_scales(scales):
+    """Scale decomposition of page 1, section 4 (int8 prefill).
+
+    smax[n] = max_g |s[n,g]| (fp32, exact from fp16),
+    q[n,g]  = rint((127 * s[n,g]) / smax[n]) with both operations in fp32,
+              round half to even (127*s is exact in fp32 for fp16 s),
+    rscale[n] = smax[n] / 127 (fp32).
+    A row whose scales are all zero gets q = 0 and rscale = 0.
+    Returns (q int8 [N,G], rscale fp32 [N], smax fp32 [N]).
+    """
+    s = np.asarray(scales).astype(np.float32)
+    smax = np.max(np.abs(s), axis=1).astype(np.float32)
+    q = np.zeros(s.shape, dtype=np.float32)
+    nz = smax > 0
+    num = (np.float32(127.0) * s[nz]).astype(np.float32)
+    q[nz] = np.rint((num / smax[nz, None]).astype(np.float32))
+    rscale = np.zeros_like(smax)
+    rscale[nz] = (smax[nz] / np.float32(127.0)).astype(np.float32)
+    if np.any(np.abs(q) > 127):
+        raise AssertionError("|q| > 127")
+    return q.astype(np.int8), rscale, smax
+
+
+def w_int8(codes, q) -> np.ndarray:
+    """W_int8[n,k] = code[n,k] * q[n, k // 128]  (page 1, section 4).  int16 result."""
+    codes = np.asarray(codes).astype(np.int16)
+    qq = np.repeat(np.asarray(q).astype(np.int16), GROUP, axis=1)
+    return codes * qq
+
+
+# --------------------------------------------------------------------------
+# Activations: per-token int8 quantisation (O2)
+# --------------------------------------------------------------------------
+
+def quant_tokens(xr):
+    """Per-token symmetric int8 quantisation of the rotated activations.
+
+    Page 1, section 4: activations are quantised to int8 per token after the
+    Hadamard rotation.  a[m] = max_k |xr[m,k]| (fp32), tscale[m] = a[m]/127
+    (fp32), xq = clamp(rint(xr / tscale), -127, 127) with the division and the
+    rounding in fp32 (half to even).  A zero token gives xq = 0, tscale = 0.
+    Returns (xq int8 [M,K], tscale fp32 [M]).
+    """
+    xr = np.asarray(xr, dtype=np.float32)
+    a = np.max(np.abs(xr), axis=1).astype(np.float32) if xr.shape[1] else \
+        np.zeros(xr.shape[0], np.float32)
+    tscale = (a / np.float32(127.0)).astype(np.float32)
+    xq = np.zeros(xr.shape, dtype=np.float32)
+    nz = tscale > 0
+    xq[nz] = np.rint((xr[nz] / tscale[nz, None]).astype(np.float32))
+    xq = np.clip(xq, -127, 127)
+    tscale = np.where(nz, tscale, np.float32(0)).astype(np.float32)
+    return xq.astype(np.int8), tscale
+
+
+# --------------------------------------------------------------------------
+# The int8 GEMM and its rescale (O2)
+# --------------------------------------------------------------------------
+
+INT32_MAX = 2 ** 31 - 1
+
+
+def acc_int8(xq, w) -> np.ndarray:
+    """acc[m,n] = sum_k xq[m,k] * W_int8[n,k], exact.
+
+    The products and all partial sums are integers of magnitude below 2^53,
+    so an fp64 matrix product is exact in any summation order.  The result
+    is checked to fit int32.  Returns int64 [M,N].
+    """
+    a = np.asarray(xq).astype(np.float64)
+    b = np.asarray(w).astype(np.float64)
+    k = a.shape[1]
+    if k and 127.0 * 127.0 * k >= 2.0 ** 53:
+        raise ValueError("K too large for exact fp64 accumulation")
+    acc = a @ b.T
+    acc_i = np.rint(acc).astype(np.int64)
+    if np.any(np.abs(acc_i) > INT32_MAX):
+        raise AssertionError("accumulator exceeds int32")
+    return acc_i
+
+
+def bf16_round(x32) -> np.ndarray:
+    """Round fp32 values to bf16 (round to nearest, ties to even).
+
+    Returned as fp32 values that are exactly representable in bf16.  NaN is
+    kept quiet; infinities pass through.
+    """
+    x32 = np.ascontiguousarray(x32, dtype=np.float32)
+    u = x32.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = (u + 0x7FFF + lsb) & 0xFFFF0000
+    r = r.astype(np.uint32)
+    nan = np.isnan(x32)
+    r[nan] = 0x7FC00000
+    return r.view(np.float32)
+
+
+def bf16_bits(x32) -> np.ndarray:
+    """bf16 bit patterns (uint16) of bf16_round(x32)."""
+    return (bf16_round(x32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def y_int8(acc, tscale, rscale) -> np.ndarray:
+    """y[m,n] = bf16_rn(((float)acc[m,n] * tscale[m]) * rscale[n]).
+
+    Every step is one fp32 operation (the int32 -> fp32 conversion rounds to
+    nearest even), evaluated left to right.  Returns fp32 values on the bf16
+    grid.
+    """
+    a = np.asarray(acc).astype(np.float32)
+    t = np.asarray(tscale, dtype=np.float32)[:, None]
+    r = np.asarray(rscale, dtype=np.float32)[None, :]
+    y = ((a * t).astype(np.float32) * r).astype(np.float32)
+    return bf16_round(y)
+
+
+# --------------------------------------------------------------------------
+# Whole layer, both references
+# --------------------------------------------------------------------------
+
+def linear_f64(x, codes, scales, sign=None) -> np.ndarray:
+    """O1: y = (H_blk (sign*x)) W^T in fp64, W = code * s (page 1, premises)."""
+    return rotate_f64(x, sign) @ dequant_f64(codes, scales).T
+
+
+def linear_int8(x, codes, scales, sign=None):
+    """O2: the whole int8 prefill path of page 1, section 4.
+
+    Returns a dict with xr (fp32), xq, tscale, q, rscale, w (int16 holding the
+    int8 weights), acc (int64) and y (fp32 on the bf16 grid).
+    """
+    xr = fwht_f32(np.asarray(x, dtype=np.float32), sign)
+    xq, tscale = quant_tokens(xr)
+    q, rscale, _ = decompose_scales(scales)
+    w = w_int8(codes, q)
+    acc = acc_int8(xq, w)
+    y = y_int8(acc, tscale, rscale)
+    return dict(xr=xr, xq=xq, tscale=tscale, q=q, rscale=rscale, w=w, acc=acc, y=y)
+
+
+def rel_frobenius(y, yref) -> float:
+    """||y - yref||_F / ||yref||_F in fp64 (0 when both are zero)."""
+    y = np.asarray(y, dtype=np.float64)
+    yref = np.asarray(yref, dtype=np.float64)
+    den = np.linalg.norm(yref)
+    num = np.linalg.norm(y - yref)
+    if den == 0.0:
+        return 0.0 if num == 0.0 else float("inf")
+    return float(num / den)
+
+
+# --------------------------------------------------------------------------
+# 2-bit storage format (defined by this library; the pages leave it open)
+# --------------------------------------------------------------------------
+#
+# A 2-bit field holds one code: bit 0 = "nonzero", bit 1 = "negative".
+#   +1 -> 0b01, -1 -> 0b11, 0 -> 0b00 (0b10 also reads as 0 and is never written).
+#
+# Rows are padded with zero codes to a multiple of 16 (a "row tile").  The
+# packed array is a sequence of 512-byte chunks, one per (row tile t, group g),
+# chunk index t * G + g, G = K/128.  Inside a chunk, 32 slots of 16 bytes
+# (slot L = bytes 16L..16L+15) hold four little-endian 32-bit words w_0..w_3.
+# For slot L let r = L // 4 and c = L % 4.  Word i, field e (0..7):
+#   jj = e // 4, p = e % 4, j = 2*i + jj            (16-wide k step in the group)
+#   row  = 16 t + r + 8 * (p % 2)
+#   k    = 128 g + 16 j + 2 c + 8 * (p // 2)
+#   bits 2e, 2e+1        hold the code at (row, k)
+#   bits 16+2e, 16+2e+1  hold the code at (row, k + 1)
+
+
+def _field(code):
+    code = np.asarray(code).astype(np.int64)
+    return np.where(code == 1, 1, np.where(code == -1, 3, 0)).astype(np.uint64)
+
+
+def _field_value(f):
+    f = np.asarray(f).astype(np.int64)
+    return np.where((f & 1) == 0, 0, np.where((f & 2) != 0, -1, 1)).astype(np.int8)
+
+
+def padded_rows(n: int) -> int:
+    return (n + 15) // 16 * 16
+
+
+def pack_codes(codes) -> np.ndarray:
+    """Pack int8 codes [N,K] into the 2-bit tile format above.  Returns uint8."""
+    codes = np.asarray(codes)
+    n, k = codes.shape
+    if k % GROUP:
+        raise ValueError("K must be a multiple of 128")
+    npad = padded_rows(n)
+    full = np.zeros((npad, k), dtype=np.int8)
+    full[:n] = codes
+    t_count, g_count = npad // 16, k // GROUP
+    words = np.zeros((t_count, g_count, 32, 4), dtype=np.uint64)
+    for lane in range(32):
+        r, c = lane // 4, lane % 4
+        for i in range(4):
+            acc = np.zeros((t_count, g_count), dtype=np.uint64)
+            for e in range(8):
+                jj, p = e // 4, e % 4
+                j = 2 * i + jj
+                rows = np.arange(t_count) * 16 + r + 8 * (p % 2)
+                kk = np.arange(g_count) * GROUP + 16 * j + 2 * c + 8 * (p // 2)
+                lo = _field(full[rows[:, None], kk[None, :]])
+                hi = _field(full[rows[:, None], kk[None, :] + 1])
+                acc |= lo << np.uint64(2 * e)
+                acc |= hi << np.uint64(16 + 2 * e)
+            words[:, :, lane, i] = acc
+    return words.astype("<u4").reshape(-1).view(np.uint8).copy()
+
+
+def unpack_codes(packed, n: int, k: int) -> np.ndarray:
+    """Inverse of pack_codes: uint8 packed -> int8 codes [n, k]."""
+    npad = padded_rows(n)
+    t_count, g_count = npad // 16, k // GROUP
+    words = np.frombuffer(np.ascontiguousarray(packed).tobytes(), dtype="<u4")
+    words = words.reshape(t_count, g_count, 32, 4).astype(np.uint64)
+    out = np.zeros((npad, k), dtype=np.int8)
+    for lane in range(32):
+        r, c = lane // 4, lane % 4
+        for i in range(4):
+            w = words[:, :, lane, i]
+            for e in range(8):
+                jj, p = e // 4, e % 4
+                j = 2 * i + jj
+                rows = np.arange(t_count) * 16 + r + 8 * (p % 2)
+                kk = np.arange(g_count) * GROUP + 16 * j + 2 * c + 8 * (p // 2)
+                out[rows[:, None], kk[None, :]] = _field_value((w >> np.uint64(2 * e)) & np.uint64(3))
+                out[rows[:, None], kk[None, :] + 1] = _field_value((w >> np.uint64(16 + 2 * e)) & np.uint64(3))
+    return out[:n]
+
+
+def pack_scales(scales) -> np.ndarray:
+    """Permute fp16 scales [N,G] to the tile order used next to pack_codes.
+
+    Rows padded with zeros to a multiple of 16.  For row tile t and group g,
+    32 bytes at element offset (t*G + g)*16 hold 8 pairs; pair r (r = 0..7)
+    is (s[16t+r, g], s[16t+r+8, g]).  Returns a flat float16 array.
+    """
+    s = np.asarray(scales, dtype=np.float16)
+    n, g_count = s.shape
+    npad = padded_rows(n)
+    full = np.zeros((npad, g_count), dtype=np.float16)
+    full[:n] = s
+    t_count = npad // 16
+    out = np.zeros((t_count, g_count, 8, 2), dtype=np.float16)
+    for r in range(8):
+        out[:, :, r, 0] = full[np.arange(t_count) * 16 + r, :]
+        out[:, :, r, 1] = full[np.arange(t_count) * 16 + r + 8, :]
+    return out.reshape(-1)
+
+
+def unpack_scales(sp, n: int, g_count: int) -> np.ndarray:
+    """Inverse of pack_scales."""
+    npad = padded_rows(n)
+    t_count = npad // 16
+    a = np.asarray(sp, dtype=np.float16).reshape(t_count, g_count, 8, 2)
+    full = np.zeros((npad, g_count), dtype=np.float16)
+    for r in range(8):
+        full[np.arange(t_count) * 16 + r, :] = a[:, :, r, 0]
+        full[np.arange(t_count) * 16 + r + 8, :] = a[:, :, r, 1]
+    return full[:n]

@@ -1,0 +1,351 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test ties an oracle function to a fact fixed by the pages or by the
+mathematics: textbook matrices, closed forms, invariants, hand-computed
+worked examples (tests/golden/), brute force on tiny inputs, and library
+routines where a special case reduces to one.  A planted-mistake test shows
+that the pins catch plausible errors.
+"""
+
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tern_oracle as O
+from ternary_weight_linear_block_gb300 import inputs as I
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+def _walsh_popcount(n):
+    """Closed form of natural-order Hadamard: H[i,j] = (-1)^popcount(i & j)."""
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    bits = np.vectorize(lambda v: bin(int(v)).count("1"))(i & j)
+    return np.where(bits % 2 == 0, 1.0, -1.0)
+
+
+# ---------------------------------------------------------------- Hadamard
+
+def test_h8_matches_textbook_golden():
+    h8 = np.array([[float(v) for v in r.split()] for r in _rows("hadamard8_natural.txt")])
+    assert np.array_equal(O.hadamard_dense(8), h8)
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 16, 64, 1024])
+def test_hadamard_closed_form_and_orthogonality(n):
+    h = O.hadamard_dense(n)
+    assert np.array_equal(h, _walsh_popcount(n))
+    assert np.array_equal(h, h.T)
+    assert np.array_equal(h @ h.T, n * np.eye(n))
+
+
+def test_normalised_rotation_is_an_involution_and_orthonormal():
+    # (H/32)(H/32) = I exactly in fp64 (entries +-1/32, sums of 1024 terms).
+    h = O.hadamard_dense(1024) / 32.0
+    assert np.array_equal(h @ h, np.eye(1024))
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((3, 2048))
+    xr = O.rotate_f64(x)
+    assert np.allclose(O.rotate_f64(xr), x, rtol=0, atol=1e-12)
+    assert np.allclose(np.linalg.norm(xr, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+
+
+def test_split_identity_of_the_page():
+    # H1024 [a; b] = [H512 a + H512 b ; H512 a - H512 b]   (page 1, section 1)
+    rng = np.random.default_rng(2)
+    a = rng.integers(-50, 50, 512).astype(np.float64)
+    b = rng.integers(-50, 50, 512).astype(np.float64)
+    h512 = _walsh_popcount(512)
+    lhs = O.rotate_f64(np.concatenate([a, b])[None, :])[0] * 32.0
+    rhs = np.concatenate([h512 @ a + h512 @ b, h512 @ a - h512 @ b])
+    assert np.array_equal(lhs, rhs)
+    # negative control: swapping the halves (the swapped-rank mistake the
+    # page's CPU mock detects) must not satisfy the identity
+    bad = np.concatenate([h512 @ a - h512 @ b, h512 @ a + h512 @ b])
+    assert O.rel_frobenius(bad, lhs) > 0.5
+
+
+def test_fwht_f32_exact_on_integers_and_matches_closed_form():
+    rng = np.random.default_rng(3)
+    x = rng.integers(-1000, 1000, (4, 3072)).astype(np.float32)
+    got = O.fwht_f32(x)
+    ref = np.concatenate([x[:, b * 1024:(b + 1) * 1024].astype(np.float64)
+                          @ _walsh_popcount(1024).T / 32.0 for b in range(3)], axis=1)
+    assert np.array_equal(got.astype(np.float64), ref)
+
+
+def test_fwht_f32_special_cases():
+    k = 2048
+    x = np.zeros((3, k), np.float32)
+    x[0, :1024] = 3.0                     # constant block -> 32c at index 0
+    x[1, 1024 + 37] = 1.0                 # one-hot -> column of H / 32
+    x[2, 5] = -2.0
+    y = O.fwht_f32(x)
+    e0 = np.zeros(1024, np.float32)
+    e0[0] = 96.0
+    assert np.array_equal(y[0, :1024], e0) and not y[0, 1024:].any()
+    col = _walsh_popcount(1024)[:, 37] / 32.0
+    assert np.array_equal(y[1, 1024:].astype(np.float64), col) and not y[1, :1024].any()
+    assert np.array_equal(y[2, :1024].astype(np.float64), -2.0 * _walsh_popcount(1024)[:, 5] / 32.0)
+
+
+def test_fwht_f32_close_to_exact_on_random_and_sign_vector():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((5, 2048)).astype(np.float32)
+    sign = rng.choice([-1.0, 1.0], 2048)
+    got = O.fwht_f32(x, sign).astype(np.float64)
+    ref = _walsh_popcount(1024)
+    exact = np.concatenate([(x[:, b * 1024:(b + 1) * 1024] * sign[b * 1024:(b + 1) * 1024])
+                            .astype(np.float64) @ ref.T / 32.0 for b in range(2)], axis=1)
+    assert O.rel_frobenius(got, exact) < 1e-6
+    assert O.rel_frobenius(O.rotate_f64(x, sign), exact) < 1e-14
+
+
+def test_planted_mistakes_are_caught():
+    """Mutants of the butterfly (sign swap, wrong stage set) fail the pins."""
+    def fwht_mutant(x, swap_sign=False, skip_last=False):
+        v = np.asarray(x, np.float32).reshape(x.shape[0], -1, 1024).copy()
+        h = 1
+        while h < 1024:
+            if skip_last and h == 512:
+                break
+            w = v.reshape(v.shape[0], v.shape[1], 1024 // (2 * h), 2, h)
+            lo, hi = w[:, :, :, 0, :], w[:, :, :, 1, :]
+            d = (hi - lo) if swap_sign else (lo - hi)
+            v = np.stack([lo + hi, d], axis=3).reshape(v.shape)
+            h *= 2
+        return (v * np.float32(1 / 32)).reshape(x.shape)
+
+    rng = np.random.default_rng(5)
+    x = rng.integers(-9, 9, (2, 1024)).astype(np.float32)
+    exact = x.astype(np.float64) @ _walsh_popcount(1024).T / 32.0
+    assert np.array_equal(O.fwht_f32(x).astype(np.float64), exact)
+    for kw in ({"swap_sign": True}, {"skip_last": True}):
+        assert not np.array_equal(fwht_mutant(x, **kw).astype(np.float64), exact)
+
+
+# ---------------------------------------------------------------- scales
+
+def test_scale_decomposition_golden():
+    for r in _rows("scale_decomposition.txt"):
+        s_txt, q_txt, smax_txt = [p.strip() for p in r.split("|")]
+        s = np.array([[float(v) for v in s_txt.split()]], dtype=np.float16)
+        q, rscale, smax = O.decompose_scales(s)
+        assert q[0].tolist() == [int(v) for v in q_txt.split()]
+        assert smax[0] == np.float32(np.float16(float(smax_txt)))
+        assert rscale[0] == np.float32(smax[0] / np.float32(127.0))
+
+
+def test_scale_decomposition_exact_rational_and_invariants():
+    rng = np.random.default_rng(6)
+    s = (0.02 * np.abs(rng.standard_normal((64, 40))) + 1e-3).astype(np.float16)
+    s[3] = 0
+    s[5, ::3] *= -1
+    q, rscale, smax = O.decompose_scales(s)
+    for n in range(s.shape[0]):
+        sm = max(abs(Fraction(float(v))) for v in s[n])
+        for g in range(s.shape[1]):
+            if sm == 0:
+                want = 0
+            else:
+                want = round(127 * Fraction(float(s[n, g])) / sm)   # exact, half to even
+            assert q[n, g] == want
+    assert np.all(np.abs(q.astype(int)) <= 127)
+    nz = smax > 0
+    am = np.argmax(np.abs(s.astype(np.float32)), axis=1)
+    assert np.all(np.abs(q[np.arange(64), am][nz]) == 127)
+    assert q[3].max() == 0 and rscale[3] == 0
+
+
+def test_int8_weight_fits_and_approximates_dequant():
+    d = I.make_layer(I.TINY, m=1, seed=0, n=64)
+    q, rscale, _ = O.decompose_scales(d.scales)
+    w = O.w_int8(d.codes, q)
+    assert np.abs(w).max() <= 127                     # "fits int8 exactly"
+    wd = O.dequant_f64(d.codes, d.scales)
+    err = np.abs(w * rscale[:, None].astype(np.float64) - wd)
+    assert np.all(err <= 0.5 * rscale[:, None] * (1 + 1e-6) + 1e-12)
+
+
+# ---------------------------------------------------------------- activations
+
+def test_token_quant_golden():
+    for r in _rows("token_quant.txt"):
+        x_txt, q_txt, t_txt = [p.strip() for p in r.split("|")]
+        xr = np.array([[float(v) for v in x_txt.split()]], np.float32)
+        xq, t = O.quant_tokens(xr)
+        assert xq[0].tolist() == [int(v) for v in q_txt.split()]
+        assert t[0] == np.float32(float(t_txt))
+
+
+def test_token_quant_rational_and_invariants():
+    rng = np.random.default_rng(7)
+    xr = rng.standard_normal((16, 1024)).astype(np.float32)
+    xr[4] = 0
+    xq, t = O.quant_tokens(xr)
+    assert np.all(np.abs(xq.astype(int)) <= 127)
+    am = np.argmax(np.abs(xr), axis=1)
+    for m in range(16):
+        if m == 4:
+            assert t[m] == 0 and not xq[m].any()
+            continue
+        assert abs(int(xq[m, am[m]])) == 127
+        tm = Fraction(float(t[m]))
+        for k in range(0, 1024, 7):
+            exact = Fraction(float(xr[m, k])) / tm
+            want = max(-127, min(127, round(exact)))
+            if xq[m, k] != want:     # only a quotient rounded onto a tie may differ
+                assert abs(abs(exact - int(exact)) - Fraction(1, 2)) < Fraction(1, 1 << 19)
+    err = np.abs(xq.astype(np.float64) * t[:, None] - xr)
+    assert np.all(err <= 0.5 * t[:, None] * (1 + 1e-5) + 1e-30)
+
+
+# ---------------------------------------------------------------- int8 GEMM
+
+def test_acc_int8_brute_force_tiny():
+    rng = np.random.default_rng(8)
+    xq = rng.integers(-127, 128, (3, 256)).astype(np.int8)
+    w = rng.integers(-127, 128, (5, 256)).astype(np.int16)
+    acc = O.acc_int8(xq, w)
+    for m in range(3):
+        for n in range(5):
+            assert acc[m, n] == sum(int(a) * int(b) for a, b in zip(xq[m], w[n]))
+
+
+def test_acc_int8_extreme_magnitude_exact():
+    k = 17408
+    xq = np.full((2, k), 127, np.int8)
+    xq[1] = -127
+    w = np.full((2, k), 127, np.int16)
+    acc = O.acc_int8(xq, w)
+    assert acc[0, 0] == 127 * 127 * k and acc[1, 1] == -127 * 127 * k
+    assert 127 * 127 * k < 2 ** 31
+
+
+def test_equal_scales_reduce_to_plain_integer_gemm():
+    # all s equal -> q = 127 everywhere -> W_int8 = 127 * code: a textbook
+    # integer matrix product, checked with pure Python loops
+    rng = np.random.default_rng(9)
+    codes = rng.integers(-1, 2, (4, 1024)).astype(np.int8)
+    s = np.full((4, 8), 0.0137, np.float16)
+    q, rscale, _ = O.decompose_scales(s)
+    assert np.all(q == 127)
+    xq = rng.integers(-127, 128, (2, 1024)).astype(np.int8)
+    acc = O.acc_int8(xq, O.w_int8(codes, q))
+    for m in range(2):
+        for n in range(4):
+            assert acc[m, n] == 127 * sum(int(a) * int(c) for a, c in zip(xq[m], codes[n]))
+
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(10)
+    v = np.concatenate([rng.standard_normal(10000).astype(np.float32) * 1e3,
+                        np.array([0.0, -0.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1e-40,
+                                  3.0e38, -1.5, np.inf, -np.inf], np.float32)])
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(O.bf16_round(v).view(np.uint32), ref.view(np.uint32))
+
+
+def test_y_rescale_order_and_rounding():
+    acc = np.array([[16777217, -3, 0]], np.int64)     # 2^24+1 rounds in the cast
+    t = np.array([0.5], np.float32)
+    r = np.array([2.0, 0.1, 7.0], np.float32)
+    y = O.y_int8(acc, t, r)
+    assert y[0, 0] == np.float32(16777216.0)
+    assert y[0, 1] == O.bf16_round(np.array([np.float32(-1.5) * np.float32(0.1)]))[0]
+    assert y[0, 2] == 0.0
+
+
+# ---------------------------------------------------------------- whole layer
+
+def test_linear_f64_two_formulations_agree():
+    d = I.make_layer(I.TINY, m=8, seed=0)
+    y1 = O.linear_f64(d.x, d.codes, d.scales)
+    wh = O.dequant_f64(d.codes, d.scales) @ (O.hadamard_dense(1024) / 32.0)   # (W H) x
+    y2 = d.x.astype(np.float64) @ wh.T
+    assert O.rel_frobenius(y1, y2) < 1e-12
+
+
+def test_linear_f64_special_cases():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((2, 2048))
+    codes = np.zeros((6, 2048), np.int8)
+    s = (np.abs(rng.standard_normal((6, 16))) * 0.02 + 1e-3).astype(np.float16)
+    assert not O.linear_f64(x, codes, s).any()
+    codes[1, 1500] = -1
+    y = O.linear_f64(x, codes, s)
+    xr = O.rotate_f64(x)
+    assert np.allclose(y[:, 1], -float(s[1, 1500 // 128]) * xr[:, 1500], rtol=1e-15, atol=0)
+    codes = rng.integers(-1, 2, (6, 2048)).astype(np.int8)
+    s_eq = np.full((6, 16), 0.25, np.float16)
+    y = O.linear_f64(x, codes, s_eq)
+    assert np.allclose(y, 0.25 * (xr @ codes.T.astype(np.float64)), rtol=1e-13, atol=1e-13)
+
+
+def test_int8_path_error_against_exact_tiny_config():
+    # expected: activation quant + scale quant give about 1e-2 relative
+    # error; the page reports 9.5e-3 per layer on real weights
+    d = I.make_layer(I.TINY, m=8, seed=0)
+    r = O.linear_int8(d.x, d.codes, d.scales)
+    exact = O.linear_f64(d.x, d.codes, d.scales)
+    e = O.rel_frobenius(r["y"], exact)
+    assert 1e-3 < e < 2e-2
+
+
+# ---------------------------------------------------------------- 2-bit format
+
+def test_pack_format_golden():
+    codes = np.zeros((16, 128), np.int8)
+    expect = []
+    for r in _rows("packed_format.txt"):
+        left, off, word = [p.strip() for p in r.split("|")]
+        row, k, c = [int(v) for v in left.split()]
+        codes[row, k] = c
+        expect.append((int(off), int(word, 16)))
+    p = O.pack_codes(codes)
+    assert p.size == 512
+    words = p.view("<u4")
+    nonzero = {i * 4: int(w) for i, w in enumerate(words) if w}
+    assert nonzero == dict(expect)
+
+
+@pytest.mark.parametrize("n,k", [(16, 128), (40, 1024), (7, 256), (256, 1024)])
+def test_pack_roundtrip(n, k):
+    rng = np.random.default_rng(n * 7 + k)
+    codes = rng.integers(-1, 2, (n, k)).astype(np.int8)
+    p = O.pack_codes(codes)
+    assert p.size == O.padded_rows(n) * k // 4
+    assert np.array_equal(O.unpack_codes(p, n, k), codes)
+    s = rng.standard_normal((n, k // 128)).astype(np.float16)
+    sp = O.pack_scales(s)
+    assert sp.size == O.padded_rows(n) * (k // 128)
+    assert np.array_equal(O.unpack_scales(sp, n, k // 128), s)
+
+
+def test_pack_halfword_reading_gives_two_times_code():
+    # The fp16 reading of the format: (word << (14 - 2e)) & 0xC000C000 is a
+    # pair of fp16 values 2*code (0x4000 = 2.0, 0xC000 = -2.0, 0 / -0).
+    rng = np.random.default_rng(12)
+    codes = rng.integers(-1, 2, (16, 128)).astype(np.int8)
+    words = O.pack_codes(codes).view("<u4").reshape(32, 4)
+    for lane in range(32):
+        r, c = lane // 4, lane % 4
+        for i in range(4):
+            for e in range(8):
+                v = (int(words[lane, i]) << (14 - 2 * e)) & 0xC000C000
+                lo = np.array([v & 0xFFFF], np.uint16).view(np.float16)[0]
+                hi = np.array([v >> 16], np.uint16).view(np.float16)[0]
+                jj, p = e // 4, e % 4
+                row = r + 8 * (p % 2)
+                k = 16 * (2 * i + jj) + 2 * c + 8 * (p // 2)
+                assert float(lo) == 2.0 * codes[row, k]
+                assert float(hi) == 2.0 * codes[row, k + 1]
