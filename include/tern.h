@@ -1,0 +1,211 @@
+/*
+ * tern.h -- C ABI of the GB300 (sm_103a) ternary-weight linear layer.
+ *
+ * The layer (page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2",
+ * qiita.com/nakanokensetsu/items/ecc183fae033565af7cb):
+ *   - weights are codes in {-1, 0, +1} stored at 2 bits, with one fp16 scale
+ *     per 128 consecutive elements of each output row (section "前提");
+ *   - a block-wise Sylvester Hadamard rotation of width 1024, normalised by
+ *     1/sqrt(1024) = 1/32, is applied to the input activations (section
+ *     "前提" and section 1, split identity H1024[a;b] = [H512 a + H512 b ;
+ *     H512 a - H512 b]);
+ *   - decode: y[m,n] = sum_k code[n,k] s[n,k/128] xr[m,k] for M <= 16 tokens;
+ *   - prefill (section 4): q[n,g] = round(127 s[n,g] / smax[n]),
+ *     W_int8[n,k] = code[n,k] q[n,k/128] (exactly int8), per-token int8
+ *     activations after the rotation, one int8 GEMM with int32 accumulation,
+ *     then a per-row and per-token rescale to bf16.
+ *
+ * Notation: M tokens, N output rows, K input width (a multiple of 1024),
+ * G = K/128 scale groups, B = K/1024 Hadamard blocks, Np = N rounded up to a
+ * multiple of 16.
+ *
+ * Conventions for every entry point:
+ *   - all data pointers are DEVICE pointers unless stated; the caller
+ *     allocates and owns every buffer; the library allocates nothing and
+ *     keeps no state besides a per-translation-unit device error word;
+ *   - fp16 and bf16 data are passed as uint16_t bit patterns;
+ *   - every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns after enqueueing its kernels;
+ *   - argument errors are detected on the host before anything is enqueued
+ *     and nothing is written; launch errors are reported as TERN_ERR_CUDA;
+ *   - M == 0 (or N == 0) is a valid no-op returning TERN_OK;
+ *   - buffers must be 16-byte aligned unless stated; rows are dense
+ *     (leading dimension = the row length);
+ *   - the kernels require a compute capability 10.3 device (GB300); on any
+ *     other device the calls return TERN_ERR_UNSUPPORTED.
+ */
+#ifndef TERN_H_
+#define TERN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TERN_OK = 0,
+  TERN_ERR_INVALID_ARG = 1, /* null pointer for a required buffer, bad mode, negative size */
+  TERN_ERR_SHAPE = 2,       /* K not a multiple of 1024, M out of range, sizes too large */
+  TERN_ERR_ALIGN = 3,       /* a buffer is not 16-byte aligned */
+  TERN_ERR_UNSUPPORTED = 4, /* no sm_103 device current */
+  TERN_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  TERN_ERR_WORKSPACE = 6,   /* workspace missing or smaller than tern_workspace_bytes() */
+  TERN_ERR_TIMEOUT = 7      /* a bounded device-side wait gave up (see tern_check) */
+} tern_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* tern_status_str(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int tern_version(void);
+
+/* ------------------------------------------------------------------------
+ * Packed weight format (defined by this library; the page does not give one)
+ *
+ * 2-bit field: bit 0 = nonzero, bit 1 = negative.  +1 -> 0b01, -1 -> 0b11,
+ * 0 -> 0b00 (0b10 also reads as 0 and is never written).
+ *
+ * Rows are padded with zero codes to Np.  `packed` is a sequence of 512-byte
+ * chunks, chunk (t * G + g) for row tile t (rows 16t..16t+15) and group g
+ * (k = 128g..128g+127).  In a chunk, slot L (bytes 16L..16L+15, L = 0..31)
+ * holds four little-endian 32-bit words w_0..w_3.  With r = L / 4, c = L % 4,
+ * word i and field e (0..7), jj = e / 4, p = e % 4, j = 2i + jj:
+ *     row = 16t + r + 8 (p % 2),   k = 128g + 16j + 2c + 8 (p / 2);
+ *     bits 2e..2e+1 of w_i hold code(row, k), bits 16+2e..17+2e code(row, k+1).
+ * Read as fp16 pairs, (w_i << (14 - 2e)) & 0xC000C000 is (2 code(row,k),
+ * 2 code(row,k+1)) -- the A fragment of an m16n8k16 tensor-core MMA.
+ *
+ * `scales_packed` (fp16): for tile t and group g, 16 values at element
+ * offset (t * G + g) * 16, pair r = (s[16t + r][g], s[16t + r + 8][g]).
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of `packed` for an N x K weight: Np * K / 4. */
+size_t tern_packed_bytes(int64_t N, int64_t K);
+/* Bytes of `scales_packed`: Np * (K / 128) * 2. */
+size_t tern_packed_scale_bytes(int64_t N, int64_t K);
+
+/*
+ * tern_pack -- load-time conversion of one layer's weights (page section
+ * "前提" for the format; section 4 for the scale decomposition).
+ *
+ *   codes   int8 [N][K], values in {-1,0,+1} (other values: undefined result)
+ *   scales  fp16 [N][G]
+ * outputs (any of q, rscale, w_q may be NULL; packed and scales_packed may be
+ * NULL together when only the prefill operands are wanted):
+ *   packed         uint8, tern_packed_bytes(N,K) bytes, format above
+ *   scales_packed  fp16, tern_packed_scale_bytes(N,K) bytes, format above
+ *   q              int8 [N][G]: rint((127*s)/smax) in fp32, half to even,
+ *                  smax[n] = max_g |s[n,g]|; a zero row gives q = 0
+ *   rscale         fp32 [N]: smax/127 (0 for a zero row)
+ *   w_q            fp16 [N][K]: the exact int8 weight code*q[n,k/128], held in
+ *                  fp16 (every integer in [-127,127] is exact in fp16) because
+ *                  the sm_103a tensor cores multiply it exactly on the f16 path
+ *                  and offer no fast int8 path; needs q and rscale non-NULL.
+ *                  q and rscale must be both NULL or both non-NULL.
+ * Requirements: K % 1024 == 0, 1 <= K <= 65536, N >= 0.
+ */
+tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                      uint8_t* packed, uint16_t* scales_packed, int8_t* q, float* rscale,
+                      uint16_t* w_q, void* stream);
+
+/* ------------------------------------------------------------------------
+ * tern_fwht_quant -- block Hadamard rotation of the activations (page
+ * section "前提", section 1) and, in TERN_FWHT_I8 mode, the per-token int8
+ * quantisation of section 4.
+ *
+ * The rotation: per token and per 1024-block, butterfly stages with stride
+ * 1, 2, 4, ..., 512 (in that order; the last one is the page's split
+ * identity), each (u, v) -> (u + v, u - v) in fp32, then * (1/32).  If
+ * `sign` (int8 [K] of +-1) is given, x is multiplied by it first (the
+ * optional "rotation sign table"); NULL means all +1.
+ *
+ *   x      bf16 [M][K]
+ *   mode   TERN_FWHT_F32:    out = float xr[M][K]; out_scale unused (may be NULL)
+ *          TERN_FWHT_DECODE: out = fp16 decode operand, layout [K/32][M][32]:
+ *                 element (m, k) sits at chunk k/32, position
+ *                 8c + 4 j2 + 2 (o8 / 8) + (o8 % 2)  where o = k % 32,
+ *                 j2 = o / 16, o8 = o % 16, c = (o8 % 8) / 2;
+ *                 value fp16_rn(xr[m,k] * F[m,b]) with the power of two
+ *                 F[m,b] = 2^min(14 - E, 126), E = (biased exponent field
+ *                 of the fp32 value max_{k in block b} |xr[m,k]|) - 127,
+ *                 i.e. floor(log2(absmax)) for a normal absmax, so the
+ *                 block's largest magnitude lands in [2^14, 2^15) and no
+ *                 fp16 overflow is possible; out_scale = float [M][B]
+ *                 holding 1 / F[m,b] (exact)
+ *          TERN_FWHT_I8:     out = fp16 [M][K] holding xq in [-127,127];
+ *                 out_scale = float tscale[M]:
+ *                 a = max_k |xr[m,k]|, tscale = a/127 (fp32),
+ *                 xq = clamp(rint(xr / tscale), -127, 127) (fp32 division,
+ *                 half to even); a == 0 gives xq = 0 and tscale = 0.
+ * Requirements: K % 1024 == 0, K <= 65536 (K <= 32768 in TERN_FWHT_I8 mode),
+ * M >= 0; `sign` may be unaligned.
+ * ---------------------------------------------------------------------- */
+#define TERN_FWHT_F32 0
+#define TERN_FWHT_DECODE 1
+#define TERN_FWHT_I8 2
+tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign,
+                            int mode, void* out, float* out_scale, void* stream);
+
+/* ------------------------------------------------------------------------
+ * tern_gemv_decode -- decode GEMV for 1 <= M <= 16 tokens:
+ *     y[m,n] = bf16_rn( sum_g s[n,g] * sum_{k in g} code[n,k] * xr[m,k] )
+ * computed from the packed weights and the TERN_FWHT_DECODE operand, with
+ * fp16 tensor-core products and fp32 accumulation.  Every weight byte is
+ * read once for all M tokens.
+ *
+ *   packed, scales_packed   from tern_pack (N, K of this layer)
+ *   xh, xs                  from tern_fwht_quant(mode = TERN_FWHT_DECODE)
+ *   y                       bf16 [M][N]
+ *   ws, ws_bytes            workspace of at least
+ *                           tern_workspace_bytes(TERN_OP_GEMV, M, N, K) bytes,
+ *                           16-byte aligned, ZERO-FILLED before its first use
+ *                           (tern_workspace_init); every call leaves it
+ *                           zero-filled again on completion.  Calls that share
+ *                           a workspace must not run concurrently.
+ * Requirements: 1 <= M <= 16 (M == 0 is a no-op), K % 1024 == 0, K <= 65536.
+ * ---------------------------------------------------------------------- */
+tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* scales_packed,
+                             const uint16_t* xh, const float* xs, int64_t M, int64_t N,
+                             int64_t K, uint16_t* y, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * tern_gemm_prefill_int8 -- the int8 prefill GEMM of page section 4:
+ *     acc[m,n] = sum_k xq[m,k] * W_int8[n,k]            (exact int32)
+ *     y[m,n]   = bf16_rn(((float)acc[m,n] * tscale[m]) * rscale[n])
+ * The operands hold int8 values in fp16 (see tern_pack / tern_fwht_quant);
+ * the tcgen05 tensor cores multiply them exactly and the kernel keeps every
+ * fp32 partial sum below 2^24 (1024-wide chunks, then int32), so acc is
+ * bit-exact.
+ *
+ *   xq      fp16 [M][K] (TERN_FWHT_I8 output), tscale fp32 [M]
+ *   w_q     fp16 [N][K] (tern_pack output),    rscale fp32 [N]
+ *   y       bf16 [M][N]
+ *   acc     int32 [M][N] or NULL
+ *   ws      unused by this version (pass NULL, 0)
+ * Requirements: K % 1024 == 0, K <= 65536, M >= 0, N % 16 == 0, N >= 0.
+ * Device-side waits are bounded; a wait that gives up makes the call's
+ * outputs undefined and is reported by tern_check().
+ * ---------------------------------------------------------------------- */
+tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
+                                   const float* rscale, int64_t M, int64_t N, int64_t K,
+                                   uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* Workspace sizing and initialisation. */
+#define TERN_OP_GEMV 1
+#define TERN_OP_GEMM 2
+size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+/* Zero-fill `bytes` of device memory at ws on `stream` (asynchronous). */
+tern_status tern_workspace_init(void* ws, size_t bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the device error words.
+ * Returns TERN_ERR_TIMEOUT if a bounded device-side wait gave up since the
+ * last check, TERN_ERR_CUDA on a sticky CUDA error, else TERN_OK. */
+tern_status tern_check(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TERN_H_ */

@@ -406,3 +406,36 @@ def unpack_scales(sp, n: int, g_count: int) -> np.ndarray:
         full[np.arange(t_count) * 16 + r, :] = a[:, :, r, 0]
         full[np.arange(t_count) * 16 + r + 8, :] = a[:, :, r, 1]
     return full[:n]
+
+
+# --------------------------------------------------------------------------
+# fp16 decode operand (the GEMV's activation format, defined in include/tern.h)
+# --------------------------------------------------------------------------
+
+def decode_operand(xr):
+    """fp16 copy of the rotated activations, one power-of-two factor per block.
+
+    For token m and 1024-block b: E = (biased exponent field of the fp32
+    absmax of the block) - 127, F = 2^min(14 - E, 126); values
+    fp16_rn(xr * F) (the fp32 product is exact), stored in the layout
+    [K/32][M][32] where element k of a 32-chunk sits at position
+    8c + 4 j2 + 2 (o8 // 8) + (o8 % 2), o = k % 32, j2 = o // 16,
+    o8 = o % 16, c = (o8 % 8) // 2.  Returns (flat fp16 array, inv [M,B]
+    with inv = 1/F, and the natural-order fp16 values [M,K]).
+    """
+    xr = np.asarray(xr, dtype=np.float32)
+    m, k = xr.shape
+    nb = k // HBLOCK
+    blocks = np.abs(xr).reshape(m, nb, HBLOCK).max(axis=2).astype(np.float32)
+    e = ((blocks.view(np.uint32) >> 23) & 0xFF).astype(np.int64) - 127
+    sh = np.minimum(14 - e, 126)
+    f = np.ldexp(np.float32(1.0), sh).astype(np.float32)
+    inv = np.ldexp(np.float32(1.0), -sh).astype(np.float32)
+    scaled = (xr.reshape(m, nb, HBLOCK) * f[:, :, None]).astype(np.float32).reshape(m, k)
+    vals = scaled.astype(np.float16)
+    o = np.arange(32)
+    j2, o8 = o // 16, o % 16
+    pos = 8 * ((o8 % 8) // 2) + 4 * j2 + 2 * (o8 // 8) + (o8 % 2)
+    out = np.zeros((k // 32, m, 32), dtype=np.float16)
+    out[:, :, pos] = vals.reshape(m, k // 32, 32).transpose(1, 0, 2)
+    return out.reshape(-1), inv, vals

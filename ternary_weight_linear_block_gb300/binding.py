@@ -1,0 +1,258 @@
+"""Thin ctypes binding over libtern.so (include/tern.h).
+
+The functions named ``tern_*`` mirror the C entry points one to one and only
+marshal arguments: torch tensors supply device memory (their data pointers)
+and the current CUDA stream supplies ``stream``.  Every step of the layer runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and a
+missing library raises.
+
+``pack_layer`` / ``decode`` / ``prefill`` are conveniences that allocate the
+outputs with torch and call the entry points in order.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtern.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "tern.h")
+
+TERN_OK = 0
+TERN_FWHT_F32 = 0
+TERN_FWHT_DECODE = 1
+TERN_FWHT_I8 = 2
+TERN_OP_GEMV = 1
+TERN_OP_GEMM = 2
+STATUS_NAMES = {0: "TERN_OK", 1: "TERN_ERR_INVALID_ARG", 2: "TERN_ERR_SHAPE", 3: "TERN_ERR_ALIGN",
+                4: "TERN_ERR_UNSUPPORTED", 5: "TERN_ERR_CUDA", 6: "TERN_ERR_WORKSPACE",
+                7: "TERN_ERR_TIMEOUT"}
+
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_SIGS = {
+    "tern_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "tern_version": (ctypes.c_int, []),
+    "tern_packed_bytes": (_sz, [_i64, _i64]),
+    "tern_packed_scale_bytes": (_sz, [_i64, _i64]),
+    "tern_workspace_bytes": (_sz, [ctypes.c_int, _i64, _i64, _i64]),
+    "tern_workspace_init": (ctypes.c_int, [_p, _sz, _p]),
+    "tern_pack": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _p]),
+    "tern_fwht_quant": (ctypes.c_int, [_p, _i64, _i64, _p, ctypes.c_int, _p, _p, _p]),
+    "tern_gemv_decode": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
+    "tern_gemm_prefill_int8": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _p, _sz,
+                                              _p]),
+    "tern_check": (ctypes.c_int, [_p]),
+}
+
+_lib = None
+
+
+class TernError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libtern.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libtern.so not built ({LIB_PATH}); run "
+                               "ternary_weight_linear_block_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/tern.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(tern_\w+)\s*\(", text, re.M)))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return stream
+
+
+def _call(name, *args):
+    st = getattr(lib(), name)(*args)
+    if st != TERN_OK:
+        raise TernError(name, st)
+    return st
+
+
+# ---------------------------------------------------------------- C mirrors
+
+def tern_status_str(status: int) -> str:
+    return lib().tern_status_str(status).decode()
+
+
+def tern_version() -> int:
+    return lib().tern_version()
+
+
+def tern_packed_bytes(n: int, k: int) -> int:
+    return lib().tern_packed_bytes(n, k)
+
+
+def tern_packed_scale_bytes(n: int, k: int) -> int:
+    return lib().tern_packed_scale_bytes(n, k)
+
+
+def tern_workspace_bytes(op: int, m: int, n: int, k: int) -> int:
+    return lib().tern_workspace_bytes(op, m, n, k)
+
+
+def tern_workspace_init(ws, nbytes: int | None = None, stream=None):
+    nb = ws.numel() * ws.element_size() if nbytes is None else nbytes
+    return _call("tern_workspace_init", _ptr(ws), nb, _stream(stream))
+
+
+def tern_pack(codes, scales, n, k, packed, scales_packed, q, rscale, w_q, stream=None):
+    return _call("tern_pack", _ptr(codes), _ptr(scales), n, k, _ptr(packed), _ptr(scales_packed),
+                 _ptr(q), _ptr(rscale), _ptr(w_q), _stream(stream))
+
+
+def tern_fwht_quant(x, m, k, sign, mode, out, out_scale, stream=None):
+    return _call("tern_fwht_quant", _ptr(x), m, k, _ptr(sign), mode, _ptr(out), _ptr(out_scale),
+                 _stream(stream))
+
+
+def tern_gemv_decode(packed, scales_packed, xh, xs, m, n, k, y, ws, ws_bytes, stream=None):
+    return _call("tern_gemv_decode", _ptr(packed), _ptr(scales_packed), _ptr(xh), _ptr(xs), m, n,
+                 k, _ptr(y), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def tern_gemm_prefill_int8(xq, tscale, w_q, rscale, m, n, k, y, acc=None, ws=None, ws_bytes=0,
+                           stream=None):
+    return _call("tern_gemm_prefill_int8", _ptr(xq), _ptr(tscale), _ptr(w_q), _ptr(rscale), m, n,
+                 k, _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def tern_check(stream=None):
+    return _call("tern_check", _stream(stream))
+
+
+# ---------------------------------------------------------------- conveniences
+
+def _need(t, dtype, name):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name}: expected a contiguous CUDA tensor of {dtype}")
+
+
+@dataclass
+class PackedLayer:
+    n: int
+    k: int
+    packed: torch.Tensor | None         # uint8
+    scales_packed: torch.Tensor | None  # float16
+    q: torch.Tensor | None              # int8 [N, G]
+    rscale: torch.Tensor | None         # float32 [N]
+    w_q: torch.Tensor | None            # float16 [N, K]
+
+    @property
+    def weight_bytes(self) -> int:
+        """Algorithmic bytes of the decode weights: 2-bit codes + fp16 scales."""
+        return self.n * self.k // 4 + self.n * (self.k // 128) * 2
+
+
+def pack_layer(codes: torch.Tensor, scales: torch.Tensor, decode: bool = True,
+               prefill: bool = True, stream=None) -> PackedLayer:
+    """Run tern_pack on device codes (int8 [N,K]) and scales (fp16 [N,G])."""
+    _need(codes, torch.int8, "codes")
+    _need(scales, torch.float16, "scales")
+    n, k = codes.shape
+    dev = codes.device
+    packed = sp = q = rs = wq = None
+    if decode:
+        packed = torch.empty(tern_packed_bytes(n, k), dtype=torch.uint8, device=dev)
+        sp = torch.empty(tern_packed_scale_bytes(n, k) // 2, dtype=torch.float16, device=dev)
+    if prefill:
+        q = torch.empty((n, k // 128), dtype=torch.int8, device=dev)
+        rs = torch.empty(n, dtype=torch.float32, device=dev)
+        wq = torch.empty((n, k), dtype=torch.float16, device=dev)
+    tern_pack(codes, scales, n, k, packed, sp, q, rs, wq, stream)
+    return PackedLayer(n, k, packed, sp, q, rs, wq)
+
+
+def fwht(x: torch.Tensor, mode: int, sign: torch.Tensor | None = None, stream=None):
+    """Rotation (+ quantisation) of bf16 activations [M,K]; returns (out, out_scale)."""
+    _need(x, torch.bfloat16, "x")
+    m, k = x.shape
+    dev = x.device
+    if mode == TERN_FWHT_F32:
+        out, sc = torch.empty((m, k), dtype=torch.float32, device=dev), None
+    elif mode == TERN_FWHT_DECODE:
+        out = torch.empty(m * k, dtype=torch.float16, device=dev)
+        sc = torch.empty((m, k // 1024), dtype=torch.float32, device=dev)
+    else:
+        out = torch.empty((m, k), dtype=torch.float16, device=dev)
+        sc = torch.empty(m, dtype=torch.float32, device=dev)
+    tern_fwht_quant(x, m, k, sign, mode, out, sc, stream)
+    return out, sc
+
+
+class Workspace:
+    """A zero-initialised device workspace, grown on demand."""
+
+    def __init__(self, device="cuda"):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int, stream=None) -> torch.Tensor:
+        nbytes = max(int(nbytes), 256)
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            tern_workspace_init(self.buf, nbytes, stream)
+        return self.buf
+
+
+def decode(layer: PackedLayer, x: torch.Tensor, ws: Workspace, y: torch.Tensor | None = None,
+           sign=None, stream=None) -> torch.Tensor:
+    """Decode forward for M <= 16 bf16 tokens: rotation, then the GEMV."""
+    m = x.shape[0]
+    xh, xs = fwht(x, TERN_FWHT_DECODE, sign, stream)
+    if y is None:
+        y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=x.device)
+    nb = tern_workspace_bytes(TERN_OP_GEMV, m, layer.n, layer.k)
+    buf = ws.get(nb, stream)
+    tern_gemv_decode(layer.packed, layer.scales_packed, xh, xs, m, layer.n, layer.k, y, buf,
+                     buf.numel(), stream)
+    return y
+
+
+def prefill(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,
+            acc: torch.Tensor | None = None, sign=None, stream=None) -> torch.Tensor:
+    """Prefill forward: rotation + per-token int8 quantisation, then the GEMM."""
+    m = x.shape[0]
+    xq, ts = fwht(x, TERN_FWHT_I8, sign, stream)
+    if y is None:
+        y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=x.device)
+    tern_gemm_prefill_int8(xq, ts, layer.w_q, layer.rscale, m, layer.n, layer.k, y, acc,
+                           stream=stream)
+    return y

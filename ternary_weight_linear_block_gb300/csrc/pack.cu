@@ -1,0 +1,154 @@
+// Load-time weight conversion: 2-bit tile packing of the codes, the tile
+// order of the group scales, and the scale decomposition of the int8 path.
+//
+// Page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2": section "前提"
+// (codes in {-1,0,+1} at 2 bits, one scale per 128 elements of a row) and
+// section 4 (q[n,g] = round(127 s[n,g] / smax[n]); W_int8[n,k] =
+// code[n,k] q[n,k/128] fits int8 exactly).  Expanding the weights to int8
+// once here, instead of on every prefill step, removes the run-time weight
+// expansion that section 6 measures at 31 of 83 ms of ternary-linear time.
+// The packed tile format is defined in include/tern.h.
+#include <cuda_fp16.h>
+
+#include "tern_internal.cuh"
+
+namespace tern {
+namespace {
+
+__device__ __forceinline__ uint32_t field_of(int8_t c) {
+  return c == 1 ? 1u : (c == -1 ? 3u : 0u);
+}
+
+// One thread per 32-bit word of the packed codes.
+__global__ void pack_codes_kernel(const int8_t* __restrict__ codes, int N, int K,
+                                  uint32_t* __restrict__ packed, long n_words) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int G = K / kGroup;
+  for (long wi = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; wi < n_words;
+       wi += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(wi & 3);
+    const int lane = static_cast<int>((wi >> 2) & 31);
+    const long tg = wi >> 7;
+    const long t = tg / G;
+    const int g = static_cast<int>(tg % G);
+    const int r = lane >> 2, c = lane & 3;
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int jj = e >> 2, p = e & 3;
+      const int j = 2 * i + jj;
+      const long row = 16 * t + r + 8 * (p & 1);
+      const int k = kGroup * g + 16 * j + 2 * c + 8 * (p >> 1);
+      if (row < N) {
+        const int8_t* src = codes + row * K + k;
+        w |= field_of(src[0]) << (2 * e);
+        w |= field_of(src[1]) << (16 + 2 * e);
+      }
+    }
+    packed[wi] = w;
+  }
+}
+
+// One thread per (tile, group, pair r): 32 bits = (s[16t+r][g], s[16t+r+8][g]).
+__global__ void pack_scales_kernel(const uint16_t* __restrict__ scales, int N, int G,
+                                   uint32_t* __restrict__ out, long n_pairs) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (long pi = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; pi < n_pairs;
+       pi += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(pi & 7);
+    const long tg = pi >> 3;
+    const long t = tg / G;
+    const int g = static_cast<int>(tg % G);
+    const long r0 = 16 * t + r, r1 = r0 + 8;
+    const uint32_t lo = r0 < N ? scales[r0 * G + g] : 0u;
+    const uint32_t hi = r1 < N ? scales[r1 * G + g] : 0u;
+    out[pi] = lo | (hi << 16);
+  }
+}
+
+// One warp per row: smax, q, rscale.
+__global__ void scale_decomp_kernel(const uint16_t* __restrict__ scales, int N, int G,
+                                    int8_t* __restrict__ q, float* __restrict__ rscale) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const long row = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= N) return;
+  const __half* s = reinterpret_cast<const __half*>(scales) + row * G;
+  float smax = 0.f;
+  for (int g = lane; g < G; g += 32) smax = fmaxf(smax, fabsf(__half2float(s[g])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+  for (int g = lane; g < G; g += 32) {
+    float v = 0.f;
+    if (smax > 0.f) v = rintf(__fdiv_rn(__fmul_rn(127.0f, __half2float(s[g])), smax));
+    q[row * G + g] = static_cast<int8_t>(static_cast<int>(v));
+  }
+  if (lane == 0) rscale[row] = smax > 0.f ? __fdiv_rn(smax, 127.0f) : 0.f;
+}
+
+// One thread per 8 consecutive elements of a row: w_q = code * q (exact in fp16).
+__global__ void wq_kernel(const int8_t* __restrict__ codes, const int8_t* __restrict__ q, int N,
+                          int K, __half* __restrict__ wq, long n_vec) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int G = K / kGroup;
+  for (long vi = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; vi < n_vec;
+       vi += static_cast<long>(gridDim.x) * blockDim.x) {
+    const long e0 = vi * 8;
+    const long row = e0 / K;
+    const int k = static_cast<int>(e0 % K);
+    const float qq = static_cast<float>(q[row * G + k / kGroup]);
+    const uint2 cw = *reinterpret_cast<const uint2*>(codes + e0);
+    const int8_t* cb = reinterpret_cast<const int8_t*>(&cw);
+    uint32_t w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      __half2 h = __floats2half2_rn(static_cast<float>(cb[2 * t]) * qq,
+                                    static_cast<float>(cb[2 * t + 1]) * qq);
+      w[t] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(wq + e0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+unsigned grid_for(long items, int threads) {
+  long b = (items + threads - 1) / threads;
+  if (b > 152L * 32) b = 152L * 32;
+  return static_cast<unsigned>(b < 1 ? 1 : b);
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                        uint8_t* packed, uint16_t* scales_packed, int8_t* q, float* rscale,
+                        uint16_t* w_q, cudaStream_t st) {
+  const int n = static_cast<int>(N), k = static_cast<int>(K), G = static_cast<int>(K / kGroup);
+  const long np = pad16(N);
+  cudaError_t e = cudaSuccess;
+  if (packed != nullptr) {
+    const long n_words = np * K / 16;
+    e = launch(pack_codes_kernel, dim3(grid_for(n_words, 256)), dim3(256), 0, st, codes, n, k,
+               reinterpret_cast<uint32_t*>(packed), n_words);
+    if (e != cudaSuccess) return e;
+    const long n_pairs = np / 16 * G * 8;
+    e = launch(pack_scales_kernel, dim3(grid_for(n_pairs, 256)), dim3(256), 0, st, scales, n, G,
+               reinterpret_cast<uint32_t*>(scales_packed), n_pairs);
+    if (e != cudaSuccess) return e;
+  }
+  if (q != nullptr) {
+    e = launch(scale_decomp_kernel, dim3(static_cast<unsigned>((N + 7) / 8)), dim3(256), 0, st,
+               scales, n, G, q, rscale);
+    if (e != cudaSuccess) return e;
+    if (w_q != nullptr) {
+      const long n_vec = N * K / 8;
+      e = launch(wq_kernel, dim3(grid_for(n_vec, 256)), dim3(256), 0, st, codes,
+                 static_cast<const int8_t*>(q), n, k, reinterpret_cast<__half*>(w_q), n_vec);
+    }
+  }
+  return e;
+}
+
+}  // namespace tern

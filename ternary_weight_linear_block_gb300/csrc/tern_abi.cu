@@ -1,0 +1,164 @@
+// extern "C" entry points of libtern: argument validation, then the
+// launchers of the kernel translation units.  The contract of every entry
+// point is stated in include/tern.h.
+#include <cstdio>
+
+#include "tern_internal.cuh"
+
+using namespace tern;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_dev_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+
+bool device_supported() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+  if (dev < kMaxDevices && g_dev_ok[dev] != 0) return g_dev_ok[dev] > 0;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return false;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev < kMaxDevices) g_dev_ok[dev] = ok ? 1 : -1;
+  return ok;
+}
+
+tern_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA; }
+
+bool k_ok(int64_t K, int64_t kmax) { return K > 0 && K % kHBlock == 0 && K <= kmax; }
+
+}  // namespace
+
+extern "C" {
+
+const char* tern_status_str(int status) {
+  switch (status) {
+    case TERN_OK: return "TERN_OK";
+    case TERN_ERR_INVALID_ARG: return "TERN_ERR_INVALID_ARG";
+    case TERN_ERR_SHAPE: return "TERN_ERR_SHAPE";
+    case TERN_ERR_ALIGN: return "TERN_ERR_ALIGN";
+    case TERN_ERR_UNSUPPORTED: return "TERN_ERR_UNSUPPORTED";
+    case TERN_ERR_CUDA: return "TERN_ERR_CUDA";
+    case TERN_ERR_WORKSPACE: return "TERN_ERR_WORKSPACE";
+    case TERN_ERR_TIMEOUT: return "TERN_ERR_TIMEOUT";
+    default: return "TERN_ERR_UNKNOWN";
+  }
+}
+
+int tern_version(void) { return 100; }
+
+size_t tern_packed_bytes(int64_t N, int64_t K) {
+  if (N < 0 || K < 0) return 0;
+  return static_cast<size_t>(pad16(N)) * static_cast<size_t>(K) / 4;
+}
+
+size_t tern_packed_scale_bytes(int64_t N, int64_t K) {
+  if (N < 0 || K < 0) return 0;
+  return static_cast<size_t>(pad16(N)) * static_cast<size_t>(K / kGroup) * 2;
+}
+
+size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (op == TERN_OP_GEMV) return gemv_workspace_bytes(M, N, K);
+  return 0;
+}
+
+tern_status tern_workspace_init(void* ws, size_t bytes, void* stream) {
+  if (bytes == 0) return TERN_OK;
+  if (ws == nullptr) return TERN_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                      uint8_t* packed, uint16_t* scales_packed, int8_t* q, float* rscale,
+                      uint16_t* w_q, void* stream) {
+  if (N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
+  if ((packed == nullptr) != (scales_packed == nullptr)) return TERN_ERR_INVALID_ARG;
+  if ((q == nullptr) != (rscale == nullptr)) return TERN_ERR_INVALID_ARG;
+  if (w_q != nullptr && q == nullptr) return TERN_ERR_INVALID_ARG;
+  if (N == 0) return TERN_OK;
+  if (codes == nullptr || scales == nullptr) return TERN_ERR_INVALID_ARG;
+  if (packed == nullptr && q == nullptr) return TERN_OK;
+  if (!aligned16(codes) || !aligned16(scales) || (packed && !aligned16(packed)) ||
+      (scales_packed && !aligned16(scales_packed)) || (q && !aligned16(q)) ||
+      (rscale && !aligned16(rscale)) || (w_q && !aligned16(w_q)))
+    return TERN_ERR_ALIGN;
+  if (N > (int64_t(1) << 30) / (K / 16)) return TERN_ERR_SHAPE;  // keeps int32 row math safe
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_pack(codes, scales, N, K, packed, scales_packed, q, rscale, w_q,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign,
+                            int mode, void* out, float* out_scale, void* stream) {
+  if (M < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (mode != TERN_FWHT_F32 && mode != TERN_FWHT_DECODE && mode != TERN_FWHT_I8)
+    return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, mode == TERN_FWHT_I8 ? 32768 : kMaxK)) return TERN_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) / K) return TERN_ERR_SHAPE;
+  if (M == 0) return TERN_OK;
+  if (x == nullptr || out == nullptr) return TERN_ERR_INVALID_ARG;
+  if (mode != TERN_FWHT_F32 && out_scale == nullptr) return TERN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || (mode != TERN_FWHT_F32 && !aligned16(out_scale)))
+    return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(
+      launch_fwht(x, M, K, sign, mode, out, out_scale, static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* scales_packed,
+                             const uint16_t* xh, const float* xs, int64_t M, int64_t N,
+                             int64_t K, uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
+  if (M > 16) return TERN_ERR_SHAPE;
+  if (N > (int64_t(1) << 30) / (K / 16)) return TERN_ERR_SHAPE;
+  if (M == 0 || N == 0) return TERN_OK;
+  if (packed == nullptr || scales_packed == nullptr || xh == nullptr || xs == nullptr ||
+      y == nullptr)
+    return TERN_ERR_INVALID_ARG;
+  if (!aligned16(packed) || !aligned16(scales_packed) || !aligned16(xh) || !aligned16(xs) ||
+      !aligned16(y))
+    return TERN_ERR_ALIGN;
+  const size_t need = gemv_workspace_bytes(M, N, K);
+  if (ws == nullptr || ws_bytes < need) return TERN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_gemv(packed, scales_packed, xh, xs, M, N, K, y, ws,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
+                                   const float* rscale, int64_t M, int64_t N, int64_t K,
+                                   uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
+  if (N % 16 != 0) return TERN_ERR_SHAPE;
+  if (M > (int64_t(1) << 24) || N > (int64_t(1) << 24)) return TERN_ERR_SHAPE;
+  if (M == 0 || N == 0) return TERN_OK;
+  if (xq == nullptr || tscale == nullptr || w_q == nullptr || rscale == nullptr || y == nullptr)
+    return TERN_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(tscale) || !aligned16(w_q) || !aligned16(rscale) ||
+      !aligned16(y) || (acc && !aligned16(acc)))
+    return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_gemm(xq, tscale, w_q, rscale, M, N, K, y, acc,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_check(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return TERN_ERR_CUDA;
+  unsigned int err = 0;
+  e = gemm_read_clear_error(&err);
+  if (e != cudaSuccess) return TERN_ERR_CUDA;
+  return err ? TERN_ERR_TIMEOUT : TERN_OK;
+}
+
+}  // extern "C"

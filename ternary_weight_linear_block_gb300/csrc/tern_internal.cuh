@@ -1,0 +1,58 @@
+// Internal helpers shared by the kernels of libtern (device side and launch side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tern.h"
+
+namespace tern {
+
+constexpr int kHBlock = 1024;   // Hadamard block width
+constexpr int kGroup = 128;     // elements per scale group
+constexpr int kMaxK = 65536;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t pad16(int64_t n) { return (n + 15) / 16 * 16; }
+
+// Programmatic dependent launch: every kernel waits for its predecessor
+// grid before touching data a previous kernel may have written, and lets its
+// successor launch early so the successor's independent prologue overlaps.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                   Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Launchers (one per translation unit); they assume validated arguments.
+cudaError_t launch_fwht(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign, int mode,
+                        void* out, float* out_scale, cudaStream_t st);
+cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                        uint8_t* packed, uint16_t* scales_packed, int8_t* q, float* rscale,
+                        uint16_t* w_q, cudaStream_t st);
+size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* scales_packed, const uint16_t* xh,
+                        const float* xs, int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                        cudaStream_t st);
+cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
+                        const float* rscale, int64_t M, int64_t N, int64_t K, uint16_t* y,
+                        int32_t* acc, cudaStream_t st);
+// Reads and clears the GEMM translation unit's device error word.
+cudaError_t gemm_read_clear_error(unsigned int* err);
+
+}  // namespace tern

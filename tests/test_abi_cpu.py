@@ -1,0 +1,107 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library must load, export every function that include/tern.h declares,
+and reject bad arguments on the host before any CUDA call.
+"""
+
+import ctypes
+import os
+
+import pytest
+import torch
+
+from ternary_weight_linear_block_gb300 import binding as B
+from ternary_weight_linear_block_gb300 import build as BUILD
+
+
+@pytest.fixture(scope="session")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        BUILD.build()
+    return B.lib()
+
+
+def test_every_header_function_is_exported(lib):
+    names = B.header_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(B._SIGS), "binding and header disagree"
+
+
+def test_status_strings_and_version(lib):
+    assert B.tern_version() == 100
+    for code, name in B.STATUS_NAMES.items():
+        assert B.tern_status_str(code) == name
+    assert B.tern_status_str(99) == "TERN_ERR_UNKNOWN"
+
+
+def test_sizes(lib):
+    assert B.tern_packed_bytes(34816, 5120) == 34816 * 5120 // 4
+    assert B.tern_packed_scale_bytes(34816, 5120) == 34816 * 40 * 2
+    assert B.tern_packed_bytes(100, 1024) == 112 * 256          # rows padded to 16
+    assert B.tern_packed_bytes(-1, 1024) == 0
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMV, 0, 10, 1024) == 0
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMV, 4, 34816, 5120) > 0
+
+
+FAKE = 1 << 20          # an aligned, never dereferenced address
+
+
+def _st(fn, *args):
+    return getattr(B.lib(), fn)(*args)
+
+
+def test_pack_argument_errors(lib):
+    assert _st("tern_pack", FAKE, FAKE, 16, 1000, FAKE, FAKE, None, None, None, None) == 2
+    assert _st("tern_pack", FAKE, FAKE, -1, 1024, FAKE, FAKE, None, None, None, None) == 1
+    assert _st("tern_pack", FAKE, FAKE, 16, 1024, FAKE, None, None, None, None, None) == 1
+    assert _st("tern_pack", FAKE, FAKE, 16, 1024, None, None, None, None, FAKE, None) == 1
+    assert _st("tern_pack", None, FAKE, 16, 1024, FAKE, FAKE, None, None, None, None) == 1
+    assert _st("tern_pack", FAKE + 4, FAKE, 16, 1024, FAKE, FAKE, None, None, None, None) == 3
+    assert _st("tern_pack", FAKE, FAKE, 0, 1024, FAKE, FAKE, None, None, None, None) == 0
+    assert _st("tern_pack", FAKE, FAKE, 16, 1024 * 65, FAKE, FAKE, None, None, None, None) == 2
+
+
+def test_fwht_argument_errors(lib):
+    assert _st("tern_fwht_quant", FAKE, 4, 1000, None, 0, FAKE, None, None) == 2
+    assert _st("tern_fwht_quant", FAKE, 4, 1024, None, 7, FAKE, None, None) == 1
+    assert _st("tern_fwht_quant", FAKE, 4, 1024, None, 1, FAKE, None, None) == 1   # no scale out
+    assert _st("tern_fwht_quant", FAKE, 4, 1024 * 33, None, 2, FAKE, FAKE, None) == 2
+    assert _st("tern_fwht_quant", FAKE + 2, 4, 1024, None, 0, FAKE, None, None) == 3
+    assert _st("tern_fwht_quant", None, 4, 1024, None, 0, FAKE, None, None) == 1
+    assert _st("tern_fwht_quant", FAKE, 0, 1024, None, 0, FAKE, None, None) == 0
+    assert _st("tern_fwht_quant", FAKE, -3, 1024, None, 0, FAKE, None, None) == 1
+
+
+def test_gemv_argument_errors(lib):
+    ws = B.tern_workspace_bytes(B.TERN_OP_GEMV, 4, 256, 1024)
+    args = lambda m=4, n=256, k=1024, ws_ptr=FAKE, ws_b=ws, y=FAKE: (
+        FAKE, FAKE, FAKE, FAKE, m, n, k, y, ws_ptr, ws_b, None)
+    assert _st("tern_gemv_decode", *args(m=17)) == 2
+    assert _st("tern_gemv_decode", *args(k=1536)) == 2
+    assert _st("tern_gemv_decode", *args(y=None)) == 1
+    assert _st("tern_gemv_decode", *args(y=FAKE + 8)) == 3
+    assert _st("tern_gemv_decode", *args(ws_b=ws - 1)) == 6
+    assert _st("tern_gemv_decode", *args(ws_ptr=None)) == 6
+    assert _st("tern_gemv_decode", *args(m=0)) == 0
+
+
+def test_gemm_argument_errors(lib):
+    a = lambda m=64, n=256, k=1024, y=FAKE: (FAKE, FAKE, FAKE, FAKE, m, n, k, y, None, None, 0, None)
+    assert _st("tern_gemm_prefill_int8", *a(n=250)) == 2
+    assert _st("tern_gemm_prefill_int8", *a(k=100)) == 2
+    assert _st("tern_gemm_prefill_int8", *a(y=None)) == 1
+    assert _st("tern_gemm_prefill_int8", *a(y=FAKE + 2)) == 3
+    assert _st("tern_gemm_prefill_int8", *a(m=0)) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_call_without_gpu_is_unsupported(lib):
+    assert _st("tern_fwht_quant", FAKE, 4, 1024, None, 0, FAKE, None, None) == 4
+
+
+def test_binding_raises_named_error(lib):
+    with pytest.raises(B.TernError) as ei:
+        B.tern_fwht_quant(FAKE, 4, 1000, None, 0, FAKE, None, stream=0)
+    assert ei.value.status == 2 and "TERN_ERR_SHAPE" in str(ei.value)

@@ -1,0 +1,117 @@
+"""GPU parity of tern_fwht_quant against the oracle (bitwise)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tern_oracle as O
+from ternary_weight_linear_block_gb300 import binding as B
+from ternary_weight_linear_block_gb300 import inputs as I
+from tests.gpu_helpers import bf16_to_f32, ensure_lib, f16_bits, poison, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+CASES = [  # (M, K, outlier fraction, factor): the workloads' activation mixes
+    (1, 1024, 0.01, 20.0), (8, 1024, 0.01, 20.0), (1, 5120, 0.001, 50.0), (4, 5120, 0.001, 50.0),
+    (3, 17408, 0.001, 50.0), (16, 17408, 0.001, 50.0), (13, 2048, 0.01, 20.0),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def _run(xd, m, k, mode, sign=None):
+    dev = "cuda"
+    if mode == B.TERN_FWHT_F32:
+        out, sc = poison(torch.empty((m, k), dtype=torch.float32, device=dev)), None
+    elif mode == B.TERN_FWHT_DECODE:
+        out = poison(torch.empty(m * k, dtype=torch.float16, device=dev))
+        sc = poison(torch.empty((m, k // 1024), dtype=torch.float32, device=dev))
+    else:
+        out = poison(torch.empty((m, k), dtype=torch.float16, device=dev))
+        sc = poison(torch.empty(m, dtype=torch.float32, device=dev))
+    B.tern_fwht_quant(xd, m, k, sign, mode, out, sc)
+    torch.cuda.synchronize()
+    return out, sc
+
+
+@pytest.mark.parametrize("m,k,frac,mult", CASES)
+def test_fwht_f32_bitwise(m, k, frac, mult):
+    bits, x = I.make_activations(1, m, k, frac, mult)
+    out, _ = _run(to_dev_bf16(bits), m, k, B.TERN_FWHT_F32)
+    ref = O.fwht_f32(x)
+    got = out.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("m,k,frac,mult", CASES)
+def test_fwht_decode_operand_bitwise(m, k, frac, mult):
+    bits, x = I.make_activations(2, m, k, frac, mult)
+    out, sc = _run(to_dev_bf16(bits), m, k, B.TERN_FWHT_DECODE)
+    flat, inv, _ = O.decode_operand(O.fwht_f32(x))
+    assert np.array_equal(f16_bits(out), flat.view(np.uint16))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), inv.view(np.uint32))
+
+
+@pytest.mark.parametrize("m,k,frac,mult", CASES + [(64, 17408, 0.001, 50.0), (37, 5120, 0.001, 50.0)])
+def test_fwht_i8_bitwise(m, k, frac, mult):
+    bits, x = I.make_activations(3, m, k, frac, mult)
+    out, sc = _run(to_dev_bf16(bits), m, k, B.TERN_FWHT_I8)
+    xq, ts = O.quant_tokens(O.fwht_f32(x))
+    got = out.cpu().float().numpy()
+    assert np.array_equal(got, xq.astype(np.float32))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), ts.view(np.uint32))
+
+
+def test_sign_vector_all_modes():
+    m, k = 5, 3072
+    bits, x = I.make_activations(4, m, k, 0.01, 20.0)
+    rng = np.random.default_rng(44)
+    sign = rng.choice(np.array([-1, 1], np.int8), k)
+    sd = to_dev(sign)
+    xd = to_dev_bf16(bits)
+    out, _ = _run(xd, m, k, B.TERN_FWHT_F32, sd)
+    ref = O.fwht_f32(x, sign.astype(np.float32))
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    out, sc = _run(xd, m, k, B.TERN_FWHT_I8, sd)
+    xq, ts = O.quant_tokens(ref)
+    assert np.array_equal(out.cpu().float().numpy(), xq.astype(np.float32))
+    # unaligned sign pointer (the header allows it)
+    buf = torch.zeros(k + 1, dtype=torch.int8, device="cuda")
+    buf[1:] = sd
+    out2, _ = _run(xd, m, k, B.TERN_FWHT_F32, buf[1:])
+    assert np.array_equal(out2.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_degenerate_inputs():
+    k = 2048
+    x = np.zeros((4, k), np.float32)
+    x[1] = 3.0e30                      # huge, same sign everywhere
+    x[2, 7] = -1.0e-30                 # one tiny value
+    x[3, ::2] = 1.0
+    x[3, 1::2] = -1.0
+    from ternary_weight_linear_block_gb300.inputs import to_bf16_bits, bf16_bits_to_f32
+    bits = to_bf16_bits(x)
+    xf = bf16_bits_to_f32(bits)
+    xd = to_dev_bf16(bits)
+    out, _ = _run(xd, 4, k, B.TERN_FWHT_F32)
+    ref = O.fwht_f32(xf)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    out, sc = _run(xd, 4, k, B.TERN_FWHT_DECODE)
+    flat, inv, _ = O.decode_operand(ref)
+    assert np.array_equal(f16_bits(out), flat.view(np.uint16))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), inv.view(np.uint32))
+    out, sc = _run(xd, 4, k, B.TERN_FWHT_I8)
+    xq, ts = O.quant_tokens(ref)
+    assert np.array_equal(out.cpu().float().numpy(), xq.astype(np.float32))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), ts.view(np.uint32))
+    assert ts[0] == 0 and not xq[0].any()
+
+
+def test_m_zero_is_a_noop():
+    out = poison(torch.empty(16, dtype=torch.float32, device="cuda"))
+    B.tern_fwht_quant(out, 0, 1024, None, B.TERN_FWHT_F32, out, None)
+    torch.cuda.synchronize()
+    assert (out.view(torch.int32) == -1).all()

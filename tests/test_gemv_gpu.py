@@ -1,0 +1,93 @@
+"""GPU parity of the decode path (rotation + tern_gemv_decode) against the
+fp64 oracle: relative Frobenius error <= 4e-3 on bf16 outputs."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tern_oracle as O
+from ternary_weight_linear_block_gb300 import binding as B
+from ternary_weight_linear_block_gb300 import inputs as I
+from tests.gpu_helpers import bf16_to_f32, ensure_lib, poison, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+TOL = 4e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def _layer(codes, scales):
+    return B.pack_layer(to_dev(codes), to_dev(scales), decode=True, prefill=False)
+
+
+def _decode(layer, bits, m, ws=None):
+    ws = ws or B.Workspace()
+    y = poison(torch.empty((m, layer.n), dtype=torch.bfloat16, device="cuda"))
+    B.decode(layer, to_dev_bf16(bits), ws, y=y)
+    torch.cuda.synchronize()
+    return bf16_to_f32(y)
+
+
+@pytest.mark.parametrize("m", [1, 2, 8, 9, 16])
+def test_tiny_layer(m):
+    d = I.make_layer(I.TINY, m, seed=0)
+    y = _decode(_layer(d.codes, d.scales), d.x_bits, m)
+    ref = O.linear_f64(d.x, d.codes, d.scales)
+    assert np.isfinite(y).all()
+    e = O.rel_frobenius(y, ref)
+    assert e <= TOL, e
+    assert e > 0   # an exact match against fp64 would be suspicious for bf16 outputs
+
+
+@pytest.mark.parametrize("n,k,m", [(100, 2048, 3), (272, 3072, 13), (16, 1024, 1), (4112, 4096, 5),
+                                   (1040, 8192, 16)])
+def test_ragged_shapes(n, k, m):
+    codes = I.make_codes(7, n, k)
+    scales = I.make_scales(7, n, k)
+    bits, x = I.make_activations(7, m, k, 0.01, 20.0)
+    y = _decode(_layer(codes, scales), bits, m)
+    e = O.rel_frobenius(y, O.linear_f64(x, codes, scales))
+    assert e <= TOL, e
+
+
+@pytest.mark.parametrize("layer,m", [(I.GATE_UP, 1), (I.GATE_UP, 4), (I.GATE_UP, 16), (I.DOWN, 1),
+                                     (I.DOWN, 4), (I.DOWN, 8), (I.DOWN, 16), (I.QKV, 1),
+                                     (I.QKV, 8), (I.QKV, 16), (I.O_PROJ, 4)])
+def test_full_size_sampled_rows(layer, m):
+    """Full workload shapes in the benchmarked launch; the oracle computes a
+    seeded sample of 512 output rows for all tokens."""
+    d = I.make_layer(layer, m, seed=0)
+    y = _decode(_layer(d.codes, d.scales), d.x_bits, m)
+    rows = np.sort(np.random.default_rng(1).choice(layer.n, 512, replace=False))
+    ref = O.linear_f64(d.x, d.codes[rows], d.scales[rows])
+    e = O.rel_frobenius(y[:, rows], ref)
+    assert e <= TOL, e
+    assert np.isfinite(y).all()
+
+
+def test_repeat_calls_reuse_workspace():
+    d = I.make_layer(I.QKV, 4, seed=3)
+    layer = _layer(d.codes, d.scales)
+    ws = B.Workspace()
+    y1 = _decode(layer, d.x_bits, 4, ws)
+    y2 = _decode(layer, d.x_bits, 4, ws)
+    assert np.array_equal(y1, y2)          # deterministic; counters were reset
+
+
+def test_special_weights():
+    k, n, m = 2048, 64, 3
+    bits, x = I.make_activations(9, m, k, 0.0, 1.0)
+    scales = I.make_scales(9, n, k)
+    codes = np.zeros((n, k), np.int8)
+    y = _decode(_layer(codes, scales), bits, m)
+    assert not y.any()                      # all-zero codes -> exact zeros
+    codes[5, 1300] = -1                     # a single nonzero code
+    y = _decode(_layer(codes, scales), bits, m)
+    xr = O.rotate_f64(x)
+    want = -float(scales[5, 1300 // 128]) * xr[:, 1300]
+    assert np.allclose(y[:, 5], want, rtol=2 ** -8, atol=0)
+    assert not np.delete(y, 5, axis=1).any()

@@ -349,3 +349,36 @@ def test_pack_halfword_reading_gives_two_times_code():
                 k = 16 * (2 * i + jj) + 2 * c + 8 * (p // 2)
                 assert float(lo) == 2.0 * codes[row, k]
                 assert float(hi) == 2.0 * codes[row, k + 1]
+
+
+# ---------------------------------------------------------------- decode operand
+
+def test_decode_operand_range_precision_and_layout():
+    rng = np.random.default_rng(13)
+    xr = (rng.standard_normal((3, 2048)) * np.array([[1e-3], [1.0], [3e4]])).astype(np.float32)
+    xr[1, 1024:] = 0.0                                  # an all-zero block
+    flat, inv, vals = O.decode_operand(xr)
+    # fp16 cast matches torch's (library) round-to-nearest-even cast
+    f = (1.0 / inv).astype(np.float32)
+    scaled = (xr.reshape(3, 2, 1024) * f[:, :, None]).reshape(3, 2048).astype(np.float32)
+    ref = torch.from_numpy(scaled).to(torch.float16).numpy()
+    assert np.array_equal(vals.view(np.uint16), ref.view(np.uint16))
+    # each nonzero block's largest magnitude lands in [2^14, 2^15)
+    bm = np.abs(vals.astype(np.float32)).reshape(3, 2, 1024).max(axis=2)
+    for m in range(3):
+        for b in range(2):
+            if np.abs(xr[m, b * 1024:(b + 1) * 1024]).max() > 0:
+                assert 2 ** 14 <= bm[m, b] < 2 ** 15
+    back = vals.astype(np.float64) * np.repeat(inv, 1024, axis=1)
+    assert np.all(np.abs(back - xr) <= np.abs(xr) * 2.0 ** -11 + 1e-30)
+    # layout: the B-fragment reading (lane c gets k = 2c, 2c+1, 2c+8, 2c+9 of
+    # each 16-wide step) recovers the natural order
+    chunks = flat.reshape(2048 // 32, 3, 4, 8)
+    for ch in range(0, 64, 7):
+        for m in range(3):
+            for c in range(4):
+                for j2 in range(2):
+                    kb = ch * 32 + 16 * j2
+                    got = chunks[ch, m, c, 4 * j2:4 * j2 + 4]
+                    want = vals[m, [kb + 2 * c, kb + 2 * c + 1, kb + 2 * c + 8, kb + 2 * c + 9]]
+                    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
