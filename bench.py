@@ -1,0 +1,418 @@
+"""Benchmark of the ternary-weight linear layer on GB300.
+
+Workload (default): decode through the fused gate/up projection,
+K = 5120 -> N = 34816, one batch of M = 1 and one of M = 4 tokens per step.
+A step is one pass of the decode hot path for each batch: the block-Hadamard
+rotation into the fp16 decode operand, then the 2-bit GEMV.  Weights rotate
+through independent synthetic copies totalling more than 4x L2 (129 MB), so
+every step streams its weights from HBM.  Metric: decode weight GB/s =
+(2-bit code bytes + fp16 scale bytes) per step / step time.
+
+The JSON line also carries the prefill int8 path (M = 2048 through the same
+layer) as its own object, the roofline of the dominant kernel, the end-to-end
+number through the public API with host buffers, clocks sampled during the
+timed region, and the CPU oracle timed on a bounded sample.
+
+Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
+weights (independent layers, no collective in the data path; weak scaling);
+value = bytes processed by all ranks / max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ternary_weight_linear_block_gb300 import binding as B  # noqa: E402
+from ternary_weight_linear_block_gb300 import inputs as I  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "ternary linear: decode weight GB/s (% HBM peak); prefill int8 TOPS (% peak)"
+DECODE_MS = (1, 4)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------- distributed
+
+def _dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, ws, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v: float, ws: int) -> float:
+    if ws <= 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        # "under load": samples within 80% of the highest seen
+        hi = max(sm)
+        loaded = [v for v in sm if v >= 0.8 * hi] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+
+def _make_layers(layer: I.Layer, copies: int, seed: int, prefill: bool):
+    """Synthetic weights drawn on the device (seeded), packed by tern_pack."""
+    g = torch.Generator(device="cuda")
+    out = []
+    for c in range(copies):
+        g.manual_seed(seed * 1000 + c)
+        codes = (torch.randint(0, 3, (layer.n, layer.k), dtype=torch.int8, device="cuda",
+                               generator=g) - 1).to(torch.int8)
+        scales = (0.02 * torch.randn((layer.n, layer.k // 128), device="cuda", generator=g).abs()
+                  + 1e-3).to(torch.float16)
+        out.append(B.pack_layer(codes, scales, decode=True, prefill=prefill))
+        del codes, scales
+    torch.cuda.synchronize()
+    return out
+
+
+def _activations(layer: I.Layer, m: int, seed: int) -> torch.Tensor:
+    bits, _ = I.make_activations(seed, m, layer.k, layer.outlier_frac, layer.outlier_mult)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+
+
+class DecodeRunner:
+    """Preallocated buffers for the decode step over a rotation of layers."""
+
+    def __init__(self, layers, xs_host, stream):
+        self.layers = layers
+        self.stream = stream
+        self.n, self.k = layers[0].n, layers[0].k
+        self.ms = [x.shape[0] for x in xs_host]
+        self.x = [x.cuda() for x in xs_host]
+        self.xh = [torch.empty(m * self.k, dtype=torch.float16, device="cuda") for m in self.ms]
+        self.xs = [torch.empty((m, self.k // 1024), dtype=torch.float32, device="cuda")
+                   for m in self.ms]
+        self.y = [torch.empty((m, self.n), dtype=torch.bfloat16, device="cuda") for m in self.ms]
+        self.ws = []
+        for m in self.ms:
+            nb = max(B.tern_workspace_bytes(B.TERN_OP_GEMV, m, self.n, self.k), 256)
+            w = torch.empty(nb, dtype=torch.uint8, device="cuda")
+            B.tern_workspace_init(w, nb, stream)
+            self.ws.append(w)
+        self.i = 0
+
+    def step(self):
+        """One decode pass per batch; each batch streams the next weight copy."""
+        st = self.stream.cuda_stream
+        for b, m in enumerate(self.ms):
+            layer = self.layers[self.i % len(self.layers)]
+            self.i += 1
+            B.tern_fwht_quant(self.x[b], m, self.k, None, B.TERN_FWHT_DECODE, self.xh[b],
+                              self.xs[b], st)
+            B.tern_gemv_decode(layer.packed, layer.scales_packed, self.xh[b], self.xs[b], m,
+                               self.n, self.k, self.y[b], self.ws[b], self.ws[b].numel(), st)
+
+    def gemv_only(self, b):
+        st = self.stream.cuda_stream
+        m = self.ms[b]
+        layer = self.layers[self.i % len(self.layers)]
+        self.i += 1
+        B.tern_gemv_decode(layer.packed, layer.scales_packed, self.xh[b], self.xs[b], m, self.n,
+                           self.k, self.y[b], self.ws[b], self.ws[b].numel(), st)
+
+    def launches_per_step(self):
+        return 2 * len(self.ms)
+
+    def bytes_per_step(self):
+        return sum(self.layers[0].weight_bytes for _ in self.ms)
+
+
+def _time_region(fn, steps, stream, ws):
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    return e0.elapsed_time(e1) / 1e3   # seconds
+
+
+def _gemv_algorithmic_bytes(m, n, k):
+    """Bytes one GEMV launch must move: codes + scales + fp16 operand + per-block
+    factors + bf16 output."""
+    return n * k // 4 + n * (k // 128) * 2 + m * k * 2 + m * (k // 1024) * 4 + m * n * 2
+
+
+def run_decode(args, rank, ws, local):
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    layer = I.GATE_UP
+    per_copy = layer.n * layer.k // 4
+    copies = max(4, int(np.ceil(4 * L2_BYTES / per_copy)) + 1)
+    hbm_peak, tc_peak, peak_kind = _peaks()
+    with torch.cuda.stream(stream):
+        layers = _make_layers(layer, copies, seed=rank, prefill=False)
+        xs_host = [_activations(layer, m, seed=rank * 10 + m) for m in DECODE_MS]
+        run = DecodeRunner(layers, xs_host, stream)
+        for _ in range(args.warmup):
+            run.step()
+        torch.cuda.synchronize()
+
+        with ClockSampler(local) as clk:
+            t = _time_region(run.step, args.steps, stream, ws)
+        clocks = clk.summary()
+        t = _max_over_ranks(t, ws)
+
+        # dominant kernel alone (same launch configuration), M = 4 batch
+        kb = DECODE_MS.index(4) if 4 in DECODE_MS else 0
+        kernel_launches = max(200, args.steps)
+        tk = _time_region(lambda: run.gemv_only(kb), kernel_launches, stream, 1)
+        gemv_us = tk / kernel_launches * 1e6
+
+        # end to end through the public API: pinned host x in, host y out
+        x_pin = [x.pin_memory() for x in xs_host]
+        y_pin = [torch.empty((m, layer.n), dtype=torch.bfloat16).pin_memory() for m in DECODE_MS]
+        wsp = [B.Workspace() for _ in DECODE_MS]
+
+        def e2e_step():
+            for b, m in enumerate(DECODE_MS):
+                lay = layers[run.i % len(layers)]
+                run.i += 1
+                xd = x_pin[b].to("cuda", non_blocking=True)
+                y = B.decode(lay, xd, wsp[b], stream=stream.cuda_stream)
+                y_pin[b].copy_(y, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(args.warmup):
+            e2e_step()
+        e2e_steps = max(50, args.steps // 20)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        te2e = time.perf_counter() - t0
+        te2e = _max_over_ranks(te2e, ws)
+
+    bytes_step = run.bytes_per_step()
+    value = bytes_step * args.steps * ws / t / 1e9
+    m = DECODE_MS[kb]
+    alg = _gemv_algorithmic_bytes(m, layer.n, layer.k)
+    achieved = alg / (gemv_us * 1e-6) / 1e9
+    h2d = sum(m * layer.k * 2 for m in DECODE_MS)
+    d2h = sum(m * layer.n * 2 for m in DECODE_MS)
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded uniform ternary codes, |N(0,1)|-based fp16 g128 scales, "
+                "bf16 N(0,1) activations with 0.1% outlier channels x50)",
+        "config": {"workload": "decode gate/up 5120->34816", "K": layer.k, "N": layer.n,
+                   "M": list(DECODE_MS), "weight_copies": copies,
+                   "weight_bytes_per_copy": layers[0].weight_bytes,
+                   "l2": "inputs larger than L2: weights rotate over "
+                         f"{copies} copies ({copies * layers[0].weight_bytes / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{ws} (independent layers per GPU)"},
+        "pct_hbm_peak": round(100 * value / ws / hbm_peak, 1),
+        "roofline": {"bound": "hbm", "kernel": "tern_gemv_decode (M=%d)" % m,
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "algorithmic_bytes": alg, "avg_launch_us": round(gemv_us, 3),
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"},
+        "e2e": {"value": round(bytes_step * e2e_steps * ws / te2e / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(te2e / e2e_steps * 1e3, 4)},
+        "gpu_launches": run.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    return out, layers
+
+
+def run_cpu_baseline(args, budget_s=15.0):
+    """The oracle (fp64 dense reference) timed on a bounded sample of the workload."""
+    from oracle import tern_oracle as O
+    layer = I.GATE_UP
+    rows = 2048
+    d = I.make_layer(layer, 4, seed=0, n=rows)
+    xs = {m: d.x[:m] for m in DECODE_MS}
+    O.linear_f64(xs[1], d.codes[:16], d.scales[:16])     # warm the H matrix cache
+    done_bytes = 0
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        for m in DECODE_MS:
+            O.linear_f64(xs[m], d.codes, d.scales)
+            done_bytes += rows * layer.k // 4 + rows * (layer.k // 128) * 2
+        reps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        blas = max((i.get("num_threads", 1) for i in threadpool_info()), default=cores)
+        cores = min(cores, blas)
+    except ImportError:
+        pass
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"fp64 dense oracle on {rows} of {layer.n} rows of gate/up 5120->34816, "
+                      f"M=1 and M=4, {reps} repetitions in {dt:.1f} s"}
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return None
+    steps = args.steps
+    per = max(1.0, min(20.0, 60.0 / max(1, steps + args.warmup)))
+    for _ in range(args.warmup):
+        run_cpu_baseline(args, budget_s=per / 4)
+    vals = []
+    t0 = time.perf_counter()
+    base = None
+    for _ in range(min(steps, 10)):
+        base = run_cpu_baseline(args, budget_s=per)
+        vals.append(base["value"])
+    dt = time.perf_counter() - t0
+    v = statistics.median(vals)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws,
+            "steps": min(steps, 10), "warmup": args.warmup,
+            "ms_per_step": round(dt / max(1, len(vals)) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode gate/up 5120->34816", "K": 5120, "N": 34816,
+                       "M": list(DECODE_MS)},
+            "cpu_baseline": dict(base, value=v),
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, ws, local = _dist_init()
+    if args.impl == "reference":
+        line = run_reference(args, rank, ws)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    from ternary_weight_linear_block_gb300 import build as BUILD
+    if not os.path.exists(B.LIB_PATH):
+        if rank == 0:
+            BUILD.build()
+        _barrier(ws)
+    line, layers = run_decode(args, rank, ws, local)
+    del layers
+    torch.cuda.empty_cache()
+    if rank == 0:
+        if not args.no_cpu_baseline and ws == 1:
+            line["cpu_baseline"] = run_cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -40,7 +40,7 @@ constexpr int kPF = 3;              // units of weights in flight per warp
 constexpr int kCtasPerSm = 2;
 
 struct GemvPlan {
-  long U;        // units = row blocks * G
+  int U;         // units = row blocks * G
   int C;         // CTAs
   int RBn;       // row blocks
   int S;         // partial slots per row block
@@ -76,8 +76,19 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 }
 
 template <int NT>
-struct Acc {
-  float v[kTW][NT][4];
+__device__ __forceinline__ void zero_acc(float (&acc)[kTW][NT][4]) {
+#pragma unroll
+  for (int tt = 0; tt < kTW; ++tt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[tt][nt][i] = 0.f;
+}
+
+// Weights of one unit for one warp: codes of its 16-row tiles and their scales.
+struct Slot {
+  uint4 c[kTW];
+  uint32_t s[kTW];
 };
 
 template <int NT>
@@ -85,85 +96,107 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     gemv_decode_kernel(const uint4* __restrict__ packed, const uint32_t* __restrict__ sp,
                        const uint4* __restrict__ xh, const float* __restrict__ xs, int M, int N,
                        int K, __nv_bfloat16* __restrict__ y, unsigned int* __restrict__ counters,
-                       float* __restrict__ partials, long U, int S) {
+                       float* __restrict__ partials, int U, int S) {
+  // Activation fragments are prefetched one unit ahead when registers allow.
+  constexpr bool kXPrefetch = (NT == 1);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int G = K / kGroup;
   const int B = K / kHBlock;
   const int n_tiles = (N + 15) / 16;
-  const long C = gridDim.x;
-  const long c = blockIdx.x;
-  const long u0 = unit_begin(c, U, C);
-  const long u1 = unit_begin(c + 1, U, C);
+  const int C = gridDim.x;
+  const int c = blockIdx.x;
+  const int u0 = static_cast<int>(unit_begin(c, U, C));
+  const int u1 = static_cast<int>(unit_begin(c + 1, U, C));
   const int r = lane >> 2;   // fragment row group
   const int cq = lane & 3;   // fragment column pair
+  const int tile_in_rb = warp * kTW;
 
   __shared__ int s_last;
 
-  // weight loads for unit u into a register slot
-  auto load_unit = [&](long u, uint4 (&cv)[kTW]) {
-    const long rb = u / G;
-    const int g = static_cast<int>(u % G);
+  // ---- weight prefetch cursor (rows of the warp, group) -------------------
+  int pf_u = u0, pf_rb = u0 / G, pf_g = u0 % G;
+  auto load_slot = [&](Slot& sl) {
 #pragma unroll
     for (int tt = 0; tt < kTW; ++tt) {
-      const long tile = rb * (kRB / 16) + warp * kTW + tt;
-      if (tile < n_tiles)
-        cv[tt] = ldg_stream(packed + (tile * G + g) * 32 + lane);
-      else
-        cv[tt] = make_uint4(0, 0, 0, 0);
+      const int tile = pf_rb * (kRB / 16) + tile_in_rb + tt;
+      if (tile < n_tiles) {
+        const long chunk = static_cast<long>(tile) * G + pf_g;
+        sl.c[tt] = ldg_stream(packed + chunk * 32 + lane);
+        sl.s[tt] = __ldg(sp + chunk * 8 + r);
+      } else {
+        sl.c[tt] = make_uint4(0, 0, 0, 0);
+        sl.s[tt] = 0u;
+      }
+    }
+    ++pf_u;
+    if (++pf_g == G) {
+      pf_g = 0;
+      ++pf_rb;
     }
   };
 
-  uint4 ring[kPF][kTW];
+  Slot ring[kPF];
 #pragma unroll
   for (int s = 0; s < kPF; ++s)
-    if (u0 + s < u1) load_unit(u0 + s, ring[s]);
+    if (pf_u < u1) load_slot(ring[s]);
 
   pdl_wait();
   pdl_launch_dependents();
 
-  Acc<NT> acc;
+  auto load_x = [&](int gg, uint4 (&xo)[4][NT], float (&xso)[NT][2]) {
 #pragma unroll
-  for (int tt = 0; tt < kTW; ++tt)
+    for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int tok = nt * 8 + r;
+        xo[ch][nt] = tok < M ? __ldg(xh + ((static_cast<long>(gg) * 4 + ch) * M + tok) * 4 + cq)
+                             : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc.v[tt][nt][i] = 0.f;
+      for (int h = 0; h < 2; ++h) {
+        const int tok = nt * 8 + 2 * cq + h;
+        xso[nt][h] = tok < M ? __ldg(xs + static_cast<long>(tok) * B + (gg >> 3)) : 0.f;
+      }
+  };
 
-  long seg_begin = u0;  // first unit of the current row block segment
+  float acc[kTW][NT][4];
+  zero_acc<NT>(acc);
 
-  auto flush = [&](long rb, long ga, long gb) {
-    const bool whole = (ga == 0 && gb == G);
-    if (whole) {
+  auto flush = [&](int rb, int ga, int gb) {
+    if (ga == 0 && gb == G) {   // the whole row block is ours: write y directly
 #pragma unroll
       for (int tt = 0; tt < kTW; ++tt) {
-        const long row0 = (rb * (kRB / 16) + warp * kTW + tt) * 16 + r;
+        const int row0 = (rb * (kRB / 16) + tile_in_rb + tt) * 16 + r;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const long row = row0 + 8 * (i >> 1);
+            const int row = row0 + 8 * (i >> 1);
             const int tok = nt * 8 + 2 * cq + (i & 1);
-            if (row < N && tok < M) y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(acc.v[tt][nt][i]);
+            if (row < N && tok < M)
+              y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(acc[tt][nt][i]);
           }
       }
       return;
     }
-    // partial: slot = c - first owner of the row block
-    const long first = owner_of(rb * G, U, C);
-    const long last_owner = owner_of(rb * G + G - 1, U, C);
+    // a piece of the row block: store it in our slot, last arriver reduces
+    const long first = owner_of(static_cast<long>(rb) * G, U, C);
+    const long last_owner = owner_of(static_cast<long>(rb) * G + G - 1, U, C);
     const long slot = c - first;
-    float* base = partials + (rb * S + slot) * static_cast<long>(M) * kRB;
+    float* base = partials + (static_cast<long>(rb) * S + slot) * static_cast<long>(M) * kRB;
 #pragma unroll
     for (int tt = 0; tt < kTW; ++tt) {
-      const int rowin0 = (warp * kTW + tt) * 16 + r;
+      const int rowin0 = (tile_in_rb + tt) * 16 + r;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int rowin = rowin0 + 8 * (i >> 1);
           const int tok = nt * 8 + 2 * cq + (i & 1);
-          if (tok < M) __stcg(base + static_cast<long>(tok) * kRB + rowin, acc.v[tt][nt][i]);
+          if (tok < M) __stcg(base + static_cast<long>(tok) * kRB + rowin, acc[tt][nt][i]);
         }
     }
     __threadfence();
@@ -179,18 +212,18 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
       const long nslots = last_owner - first + 1;
 #pragma unroll
       for (int tt = 0; tt < kTW; ++tt) {
-        const int rowin0 = (warp * kTW + tt) * 16 + r;
+        const int rowin0 = (tile_in_rb + tt) * 16 + r;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int rowin = rowin0 + 8 * (i >> 1);
             const int tok = nt * 8 + 2 * cq + (i & 1);
-            const long row = rb * kRB + rowin;
+            const int row = rb * kRB + rowin;
             if (tok < M && row < N) {
               float sum = 0.f;
               for (long sl = 0; sl < nslots; ++sl)
-                sum += __ldcg(partials + ((rb * S + sl) * M + tok) * static_cast<long>(kRB) + rowin);
+                sum += __ldcg(partials + ((static_cast<long>(rb) * S + sl) * M + tok) * kRB + rowin);
               y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum);
             }
           }
@@ -200,48 +233,37 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     __syncthreads();
   };
 
-  for (long ub = u0; ub < u1; ub += kPF) {
+  int rb = u0 / G, g = u0 % G;
+  int seg_g0 = g;   // first group of the current row-block segment
+  uint4 xv[4][NT];
+  float xsv[NT][2];
+  if (kXPrefetch && u0 < u1) load_x(g, xv, xsv);
+
+  for (int ub = u0; ub < u1; ub += kPF) {
 #pragma unroll
     for (int s = 0; s < kPF; ++s) {
-      const long u = ub + s;
+      const int u = ub + s;
       if (u < u1) {
-        const long rb = u / G;
-        const int g = static_cast<int>(u % G);
-        const int blk = g >> 3;
-        // activation fragments for the group: 4 chunks of 32 k, NT token tiles
-        uint4 xv[4][NT];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const int tok = nt * 8 + r;
-            if (tok < M)
-              xv[ch][nt] = __ldg(xh + ((static_cast<long>(g) * 4 + ch) * M + tok) * 4 + cq);
-            else
-              xv[ch][nt] = make_uint4(0, 0, 0, 0);
-          }
-        float xsv[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int tok = nt * 8 + 2 * cq + h;
-            xsv[nt][h] = tok < M ? __ldg(xs + static_cast<long>(tok) * B + blk) : 0.f;
-          }
-        float sc[kTW][2];
-#pragma unroll
-        for (int tt = 0; tt < kTW; ++tt) {
-          const long tile = rb * (kRB / 16) + warp * kTW + tt;
-          uint32_t s2 = tile < n_tiles ? __ldg(sp + (tile * G + g) * 8 + r) : 0u;
-          __half2 h2 = *reinterpret_cast<__half2*>(&s2);
-          float2 f2 = __half22float2(h2);
-          sc[tt][0] = f2.x * 0.5f;   // rows r, r+8; 1/2 undoes the 2*code reading
-          sc[tt][1] = f2.y * 0.5f;
+        int nrb = rb, ng = g + 1;
+        if (ng == G) {
+          ng = 0;
+          ++nrb;
+        }
+        uint4 xn[4][NT];
+        float xsn[NT][2];
+        if (kXPrefetch) {
+          if (u + 1 < u1) load_x(ng, xn, xsn);
+        } else {
+          load_x(g, xv, xsv);
         }
 #pragma unroll
         for (int tt = 0; tt < kTW; ++tt) {
+          uint32_t s2 = ring[s].s[tt];
+          const float2 f2 = __half22float2(*reinterpret_cast<__half2*>(&s2));
+          const float sr = f2.x * 0.5f, sr8 = f2.y * 0.5f;   // 1/2 undoes the 2*code reading
+          const uint32_t w4[4] = {ring[s].c[tt].x, ring[s].c[tt].y, ring[s].c[tt].z,
+                                  ring[s].c[tt].w};
           float d[NT][4];
-          const uint32_t w4[4] = {ring[s][tt].x, ring[s][tt].y, ring[s][tt].z, ring[s][tt].w};
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t w = w4[j >> 1];
@@ -252,34 +274,35 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               const uint4 xq = xv[j >> 1][nt];
-              const uint32_t b0 = (j & 1) ? xq.z : xq.x;
-              const uint32_t b1 = (j & 1) ? xq.w : xq.y;
-              mma16816(d[nt], a, b0, b1, j == 0);
+              mma16816(d[nt], a, (j & 1) ? xq.z : xq.x, (j & 1) ? xq.w : xq.y, j == 0);
             }
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            acc.v[tt][nt][0] = fmaf(d[nt][0], sc[tt][0] * xsv[nt][0], acc.v[tt][nt][0]);
-            acc.v[tt][nt][1] = fmaf(d[nt][1], sc[tt][0] * xsv[nt][1], acc.v[tt][nt][1]);
-            acc.v[tt][nt][2] = fmaf(d[nt][2], sc[tt][1] * xsv[nt][0], acc.v[tt][nt][2]);
-            acc.v[tt][nt][3] = fmaf(d[nt][3], sc[tt][1] * xsv[nt][1], acc.v[tt][nt][3]);
+            acc[tt][nt][0] = fmaf(d[nt][0], sr * xsv[nt][0], acc[tt][nt][0]);
+            acc[tt][nt][1] = fmaf(d[nt][1], sr * xsv[nt][1], acc[tt][nt][1]);
+            acc[tt][nt][2] = fmaf(d[nt][2], sr8 * xsv[nt][0], acc[tt][nt][2]);
+            acc[tt][nt][3] = fmaf(d[nt][3], sr8 * xsv[nt][1], acc[tt][nt][3]);
           }
         }
-        // refill this ring slot
-        if (u + kPF < u1) load_unit(u + kPF, ring[s]);
-        // end of a row block segment?
-        const bool seg_end = (u + 1 == u1) || ((u + 1) / G != rb);
-        if (seg_end) {
-          const long ga = seg_begin - rb * G;
-          const long gb = u + 1 - rb * G;
-          flush(rb, ga, gb);
+        if (pf_u < u1) load_slot(ring[s]);
+        if (u + 1 == u1 || nrb != rb) {
+          flush(rb, seg_g0, g + 1);
+          zero_acc<NT>(acc);
+          seg_g0 = 0;
+        }
+        rb = nrb;
+        g = ng;
+        if (kXPrefetch) {
 #pragma unroll
-          for (int tt = 0; tt < kTW; ++tt)
+          for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt) xv[ch][nt] = xn[ch][nt];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) acc.v[tt][nt][i] = 0.f;
-          seg_begin = u + 1;
+          for (int nt = 0; nt < NT; ++nt) {
+            xsv[nt][0] = xsn[nt][0];
+            xsv[nt][1] = xsn[nt][1];
+          }
         }
       }
     }
@@ -290,7 +313,7 @@ GemvPlan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
   GemvPlan p;
   const long G = K / kGroup;
   p.RBn = static_cast<int>((N + kRB - 1) / kRB);
-  p.U = static_cast<long>(p.RBn) * G;
+  p.U = static_cast<int>(p.RBn * G);
   const long cmax = static_cast<long>(sms) * kCtasPerSm;
   p.C = static_cast<int>(p.U < cmax ? p.U : cmax);
   // slots: the most CTAs that touch one row block
