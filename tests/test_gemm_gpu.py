@@ -1,0 +1,118 @@
+"""GPU parity of the int8 prefill path against the oracle.
+
+acc (int32) must equal the integer oracle bit for bit; y must be within
+2e-3 (relative Frobenius) of the CPU int8-path oracle and within 2e-2 of
+the exact fp64 layer.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tern_oracle as O
+from ternary_weight_linear_block_gb300 import binding as B
+from ternary_weight_linear_block_gb300 import inputs as I
+from tests.gpu_helpers import bf16_to_f32, ensure_lib, poison, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def _gemm_raw(xq, ts, w, rs):
+    """Call the GEMM entry point directly on integer operands."""
+    m, k = xq.shape
+    n = w.shape[0]
+    xd = to_dev(xq.astype(np.float16))
+    wd = to_dev(w.astype(np.float16))
+    y = poison(torch.empty((m, n), dtype=torch.bfloat16, device="cuda"))
+    acc = poison(torch.empty((m, n), dtype=torch.int32, device="cuda"))
+    B.tern_gemm_prefill_int8(xd, to_dev(ts), wd, to_dev(rs), m, n, k, y, acc)
+    B.tern_check()
+    return acc.cpu().numpy().astype(np.int64), bf16_to_f32(y)
+
+
+def _prefill(codes, scales, bits, m):
+    layer = B.pack_layer(to_dev(codes), to_dev(scales), decode=False, prefill=True)
+    y = poison(torch.empty((m, layer.n), dtype=torch.bfloat16, device="cuda"))
+    acc = poison(torch.empty((m, layer.n), dtype=torch.int32, device="cuda"))
+    B.prefill(layer, to_dev_bf16(bits), y=y, acc=acc)
+    B.tern_check()
+    return acc, y
+
+
+@pytest.mark.parametrize("m", [1, 8, 128, 200])
+def test_tiny_layer(m):
+    d = I.make_layer(I.TINY, m, seed=0)
+    acc, y = _prefill(d.codes, d.scales, d.x_bits, m)
+    r = O.linear_int8(d.x, d.codes, d.scales)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), r["acc"])
+    yg = bf16_to_f32(y)
+    assert O.rel_frobenius(yg, r["y"]) <= 2e-3
+    assert np.array_equal(yg.view(np.uint32), r["y"].view(np.uint32))   # same fp32 steps
+    assert O.rel_frobenius(yg, O.linear_f64(d.x, d.codes, d.scales)) <= 2e-2
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 272, 2048), (129, 528, 3072), (64, 256, 1024),
+                                   (257, 1040, 5120)])
+def test_ragged_shapes(m, n, k):
+    codes = I.make_codes(11, n, k)
+    scales = I.make_scales(11, n, k)
+    bits, x = I.make_activations(11, m, k, 0.01, 20.0)
+    acc, y = _prefill(codes, scales, bits, m)
+    r = O.linear_int8(x, codes, scales)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), r["acc"])
+    assert np.array_equal(bf16_to_f32(y).view(np.uint32), r["y"].view(np.uint32))
+
+
+@pytest.mark.parametrize("k", [1024, 5120, 17408])
+def test_extreme_magnitudes_exact(k):
+    """|acc| up to 127*127*K: every fp32 chunk sum is at its largest."""
+    m, n = 130, 272
+    rng = np.random.default_rng(k)
+    xq = np.full((m, k), 127, np.int16)
+    xq[1] = -127
+    xq[2, ::2] = -127
+    xq[3:] = rng.integers(-127, 128, (m - 3, k))
+    w = np.full((n, k), 127, np.int16)
+    w[5] = -127
+    w[6, 1::3] = 0
+    w[7:] = rng.integers(-127, 128, (n - 7, k))
+    ts = np.full(m, 1e-3, np.float32)
+    rs = np.full(n, 2e-3, np.float32)
+    acc, y = _gemm_raw(xq, ts, w, rs)
+    ref = O.acc_int8(xq, w)
+    assert acc[0, 0] == 127 * 127 * k
+    assert np.array_equal(acc, ref)
+    assert np.array_equal(y.view(np.uint32), O.y_int8(ref, ts, rs).view(np.uint32))
+
+
+@pytest.mark.parametrize("layer,m", [(I.GATE_UP, 512), (I.DOWN, 512), (I.GATE_UP, 2048),
+                                     (I.DOWN, 2048)])
+def test_full_size_sampled(layer, m):
+    """Full prefill shapes; the oracle computes a seeded sample of rows."""
+    d = I.make_layer(layer, m, seed=0)
+    acc, y = _prefill(d.codes, d.scales, d.x_bits, m)
+    rows = np.sort(np.random.default_rng(2).choice(layer.n, 256, replace=False))
+    toks = np.sort(np.random.default_rng(3).choice(m, min(m, 256), replace=False))
+    r = O.linear_int8(d.x[toks], d.codes[rows], d.scales[rows])
+    # per-token quantisation sees the whole token, so the token sample is exact
+    rt = torch.from_numpy(rows).cuda()
+    tt = torch.from_numpy(toks).cuda()
+    acc_s = acc[tt][:, rt].cpu().numpy().astype(np.int64)
+    y_s = bf16_to_f32(y[tt][:, rt])
+    assert np.array_equal(acc_s, r["acc"])
+    assert np.array_equal(y_s.view(np.uint32), r["y"].view(np.uint32))
+    exact = O.linear_f64(d.x[toks], d.codes[rows], d.scales[rows])
+    assert O.rel_frobenius(y_s, exact) <= 2e-2
+    assert np.isfinite(bf16_to_f32(y)).all()
+
+
+def test_zero_operands():
+    m, n, k = 40, 256, 1024
+    acc, y = _gemm_raw(np.zeros((m, k), np.int16), np.zeros(m, np.float32),
+                       np.zeros((n, k), np.int16), np.zeros(n, np.float32))
+    assert not acc.any() and not y.any()
