@@ -177,7 +177,7 @@ class DecodeRunner:
         self.n, self.k = layers[0].n, layers[0].k
         self.ms = [x.shape[0] for x in xs_host]
         self.x = [x.cuda() for x in xs_host]
-        self.xh = [torch.empty(m * self.k, dtype=torch.float16, device="cuda") for m in self.ms]
+        self.xh = [torch.empty((m, self.k), dtype=torch.float16, device="cuda") for m in self.ms]
         self.xs = [torch.empty((m, self.k // 1024), dtype=torch.float32, device="cuda")
                    for m in self.ms]
         self.y = [torch.empty((m, self.n), dtype=torch.bfloat16, device="cuda") for m in self.ms]
@@ -197,16 +197,16 @@ class DecodeRunner:
             self.i += 1
             B.tern_fwht_quant(self.x[b], m, self.k, None, B.TERN_FWHT_DECODE, self.xh[b],
                               self.xs[b], st)
-            B.tern_gemv_decode(layer.packed, layer.scales_packed, self.xh[b], self.xs[b], m,
-                               self.n, self.k, self.y[b], self.ws[b], self.ws[b].numel(), st)
+            B.tern_gemv_decode(layer.packed, self.xh[b], self.xs[b], m, self.n, self.k, self.y[b],
+                               self.ws[b], self.ws[b].numel(), st)
 
     def gemv_only(self, b):
         st = self.stream.cuda_stream
         m = self.ms[b]
         layer = self.layers[self.i % len(self.layers)]
         self.i += 1
-        B.tern_gemv_decode(layer.packed, layer.scales_packed, self.xh[b], self.xs[b], m, self.n,
-                           self.k, self.y[b], self.ws[b], self.ws[b].numel(), st)
+        B.tern_gemv_decode(layer.packed, self.xh[b], self.xs[b], m, self.n, self.k, self.y[b],
+                           self.ws[b], self.ws[b].numel(), st)
 
     def launches_per_step(self):
         return 2 * len(self.ms)
@@ -230,16 +230,16 @@ def _time_region(fn, steps, stream, ws):
 
 
 def _gemv_algorithmic_bytes(m, n, k):
-    """Bytes one GEMV launch must move: codes + scales + fp16 operand + per-block
-    factors + bf16 output."""
-    return n * k // 4 + n * (k // 128) * 2 + m * k * 2 + m * (k // 1024) * 4 + m * n * 2
+    """Bytes one GEMV launch must move: codes + scales + the fp16 activation
+    operand + per-block factors + bf16 output."""
+    return n * k // 4 + n * (k // 128) * 2 + 2 * m * k + m * (k // 1024) * 4 + m * n * 2
 
 
 def run_decode(args, rank, ws, local):
     torch.cuda.set_device(local)
     stream = torch.cuda.Stream()
     layer = I.GATE_UP
-    per_copy = layer.n * layer.k // 4
+    per_copy = B.tern_packed_bytes(layer.n, layer.k)
     copies = max(4, int(np.ceil(4 * L2_BYTES / per_copy)) + 1)
     hbm_peak, tc_peak, peak_kind = _peaks()
     with torch.cuda.stream(stream):
@@ -295,7 +295,7 @@ def run_decode(args, rank, ws, local):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 products (2*code x fp16 activations), f32 accumulate",
         "data": "synthetic (seeded uniform ternary codes, |N(0,1)|-based fp16 g128 scales, "
                 "bf16 N(0,1) activations with 0.1% outlier channels x50)",
         "config": {"workload": "decode gate/up 5120->34816", "K": layer.k, "N": layer.n,

@@ -64,27 +64,31 @@ int tern_version(void);
 /* ------------------------------------------------------------------------
  * Packed weight format (defined by this library; the page does not give one)
  *
- * 2-bit field: bit 0 = nonzero, bit 1 = negative.  +1 -> 0b01, -1 -> 0b11,
- * 0 -> 0b00 (0b10 also reads as 0 and is never written).
+ * 2-bit field: high bit = negative, low bit = nonzero.  +1 -> 0b01,
+ * -1 -> 0b11, 0 -> 0b00 (0b10 also reads as 0 and is never written).
  *
- * Rows are padded with zero codes to Np.  `packed` is a sequence of 512-byte
- * chunks, chunk (t * G + g) for row tile t (rows 16t..16t+15) and group g
- * (k = 128g..128g+127).  In a chunk, slot L (bytes 16L..16L+15, L = 0..31)
- * holds four little-endian 32-bit words w_0..w_3.  With r = L / 4, c = L % 4,
- * word i and field e (0..7), jj = e / 4, p = e % 4, j = 2i + jj:
- *     row = 16t + r + 8 (p % 2),   k = 128g + 16j + 2c + 8 (p / 2);
- *     bits 2e..2e+1 of w_i hold code(row, k), bits 16+2e..17+2e code(row, k+1).
- * Read as fp16 pairs, (w_i << (14 - 2e)) & 0xC000C000 is (2 code(row,k),
- * 2 code(row,k+1)) -- the A fragment of an m16n8k16 tensor-core MMA.
- *
- * `scales_packed` (fp16): for tile t and group g, 16 values at element
- * offset (t * G + g) * 16, pair r = (s[16t + r][g], s[16t + r + 8][g]).
+ * Rows are padded with zero codes and zero scales to Np512 = N rounded up to
+ * a multiple of 512.  `packed` is a sequence of 17408-byte units, unit
+ * (rb * G + g) for row block rb (rows 512 rb .. 512 rb + 511) and group g
+ * (k = 128 g .. 128 g + 127).  A unit holds
+ *   bytes [0, 16384):      codes, 32 tiles of 16 rows.  Tile t (rows
+ *       512 rb + 16 t ..) starts at byte 512 t; slot L (0..31) of the tile,
+ *       bytes 512 t + 16 L .. + 15, holds four little-endian 32-bit words
+ *       w_0..w_3.  With r = L / 4, c = L % 4, word i and field e (0..7),
+ *       jj = e / 4, p = e % 4, j = 2 i + jj:
+ *         bits 2e..2e+1 of w_i:      code(row, k),
+ *         bits 16+2e..17+2e of w_i:  code(row, k + 1),
+ *       with row = 512 rb + 16 t + r + 8 (p % 2),
+ *            k   = 128 g + 16 j + 2 c + 8 (p / 2);
+ *   bytes [16384, 17408):  fp16 scales: tile t at 16384 + 32 t holds 8 pairs
+ *       (s[512 rb + 16 t + r][g], s[512 rb + 16 t + r + 8][g]), r = 0..7.
+ * Read as fp16 pairs, (w_i << (14 - 2e)) & 0xC000C000 is
+ * (2 code(row, k), 2 code(row, k + 1)) (0x4000 = 2.0, 0xC000 = -2.0): register
+ * p of the A fragment of an m16n8k16 tensor-core MMA for k16 step j.
  * ---------------------------------------------------------------------- */
 
-/* Bytes of `packed` for an N x K weight: Np * K / 4. */
+/* Bytes of `packed` for an N x K weight: ceil(N/512) * (K/128) * 17408. */
 size_t tern_packed_bytes(int64_t N, int64_t K);
-/* Bytes of `scales_packed`: Np * (K / 128) * 2. */
-size_t tern_packed_scale_bytes(int64_t N, int64_t K);
 
 /*
  * tern_pack -- load-time conversion of one layer's weights (page section
@@ -92,10 +96,9 @@ size_t tern_packed_scale_bytes(int64_t N, int64_t K);
  *
  *   codes   int8 [N][K], values in {-1,0,+1} (other values: undefined result)
  *   scales  fp16 [N][G]
- * outputs (any of q, rscale, w_q may be NULL; packed and scales_packed may be
- * NULL together when only the prefill operands are wanted):
+ * outputs (any may be NULL; packed is the decode operand, q / rscale / w_q
+ * the prefill operands):
  *   packed         uint8, tern_packed_bytes(N,K) bytes, format above
- *   scales_packed  fp16, tern_packed_scale_bytes(N,K) bytes, format above
  *   q              int8 [N][G]: rint((127*s)/smax) in fp32, half to even,
  *                  smax[n] = max_g |s[n,g]|; a zero row gives q = 0
  *   rscale         fp32 [N]: smax/127 (0 for a zero row)
@@ -107,8 +110,7 @@ size_t tern_packed_scale_bytes(int64_t N, int64_t K);
  * Requirements: K % 1024 == 0, 1 <= K <= 65536, N >= 0.
  */
 tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
-                      uint8_t* packed, uint16_t* scales_packed, int8_t* q, float* rscale,
-                      uint16_t* w_q, void* stream);
+                      uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q, void* stream);
 
 /* ------------------------------------------------------------------------
  * tern_fwht_quant -- block Hadamard rotation of the activations (page
@@ -123,11 +125,8 @@ tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, in
  *
  *   x      bf16 [M][K]
  *   mode   TERN_FWHT_F32:    out = float xr[M][K]; out_scale unused (may be NULL)
- *          TERN_FWHT_DECODE: out = fp16 decode operand, layout [K/32][M][32]:
- *                 element (m, k) sits at chunk k/32, position
- *                 8c + 4 j2 + 2 (o8 / 8) + (o8 % 2)  where o = k % 32,
- *                 j2 = o / 16, o8 = o % 16, c = (o8 % 8) / 2;
- *                 value fp16_rn(xr[m,k] * F[m,b]) with the power of two
+ *          TERN_FWHT_DECODE: out = fp16 [M][K], the decode operand:
+ *                 fp16_rn(xr[m,k] * F[m,b]) with the power of two
  *                 F[m,b] = 2^min(14 - E, 126), E = (biased exponent field
  *                 of the fp32 value max_{k in block b} |xr[m,k]|) - 127,
  *                 i.e. floor(log2(absmax)) for a normal absmax, so the
@@ -151,11 +150,11 @@ tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_
 /* ------------------------------------------------------------------------
  * tern_gemv_decode -- decode GEMV for 1 <= M <= 16 tokens:
  *     y[m,n] = bf16_rn( sum_g s[n,g] * sum_{k in g} code[n,k] * xr[m,k] )
- * computed from the packed weights and the TERN_FWHT_DECODE operand, with
- * fp16 tensor-core products and fp32 accumulation.  Every weight byte is
- * read once for all M tokens.
+ * computed from the packed weights and the TERN_FWHT_DECODE operand with fp16
+ * tensor-core products (2 code times the fp16 activation, exact) and fp32
+ * accumulation.  Every weight byte is read once for all M tokens.
  *
- *   packed, scales_packed   from tern_pack (N, K of this layer)
+ *   packed                  from tern_pack (this layer's N, K)
  *   xh, xs                  from tern_fwht_quant(mode = TERN_FWHT_DECODE)
  *   y                       bf16 [M][N]
  *   ws, ws_bytes            workspace of at least
@@ -165,10 +164,12 @@ tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_
  *                           zero-filled again on completion.  Calls that share
  *                           a workspace must not run concurrently.
  * Requirements: 1 <= M <= 16 (M == 0 is a no-op), K % 1024 == 0, K <= 65536.
+ * Device-side waits are bounded; a wait that gives up makes the call's
+ * outputs undefined and is reported by tern_check().
  * ---------------------------------------------------------------------- */
-tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* scales_packed,
-                             const uint16_t* xh, const float* xs, int64_t M, int64_t N,
-                             int64_t K, uint16_t* y, void* ws, size_t ws_bytes, void* stream);
+tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const float* xs,
+                             int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                             size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * tern_gemm_prefill_int8 -- the int8 prefill GEMM of page section 4:

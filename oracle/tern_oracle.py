@@ -26,8 +26,9 @@ O2 (int8 path, spec-exact fp32 operation sequence)
                         fwht_f32 / quant_tokens / decompose_scales /
                         w_int8 / acc_int8 / y_int8 / linear_int8
 
-plus the 2-bit storage format (pack_codes / unpack_codes / pack_scales), which
-the pages leave open and this library defines (see ``include/tern.h``).
+plus the 2-bit storage format (pack_weights / unpack_weights) and the fp16
+decode operand (decode_operand), which the pages leave open and this library
+defines (see ``include/tern.h``).
 
 Readings of the pages taken here (each is also listed in the design notes):
 * natural (Sylvester) order H, not sequency order; normalised by 1/32 per block;
@@ -298,19 +299,24 @@ def rel_frobenius(y, yref) -> float:
 # 2-bit storage format (defined by this library; the pages leave it open)
 # --------------------------------------------------------------------------
 #
-# A 2-bit field holds one code: bit 0 = "nonzero", bit 1 = "negative".
+# A 2-bit field holds one code: high bit = "negative", low bit = "nonzero".
 #   +1 -> 0b01, -1 -> 0b11, 0 -> 0b00 (0b10 also reads as 0 and is never written).
 #
-# Rows are padded with zero codes to a multiple of 16 (a "row tile").  The
-# packed array is a sequence of 512-byte chunks, one per (row tile t, group g),
-# chunk index t * G + g, G = K/128.  Inside a chunk, 32 slots of 16 bytes
-# (slot L = bytes 16L..16L+15) hold four little-endian 32-bit words w_0..w_3.
-# For slot L let r = L // 4 and c = L % 4.  Word i, field e (0..7):
-#   jj = e // 4, p = e % 4, j = 2*i + jj            (16-wide k step in the group)
-#   row  = 16 t + r + 8 * (p % 2)
-#   k    = 128 g + 16 j + 2 c + 8 * (p // 2)
-#   bits 2e, 2e+1        hold the code at (row, k)
-#   bits 16+2e, 16+2e+1  hold the code at (row, k + 1)
+# Rows are padded with zero codes and zero scales to a multiple of 512.  The
+# packed buffer is a sequence of 17408-byte units, unit rb * G + g for row
+# block rb (512 rows) and group g (128 k), G = K / 128.  In a unit:
+#   bytes [0, 16384): 32 tiles of 16 rows, tile t at byte 512 t; slot L
+#     (bytes 512 t + 16 L ..) holds four little-endian 32-bit words w_0..w_3;
+#     with r = L // 4, c = L % 4, word i, field e (0..7), jj = e // 4,
+#     p = e % 4, j = 2 i + jj:
+#       bits 2e..2e+1 of w_i:     code(row, k)
+#       bits 16+2e..17+2e of w_i: code(row, k + 1)
+#     with row = 512 rb + 16 t + r + 8 (p % 2), k = 128 g + 16 j + 2 c + 8 (p // 2);
+#   bytes [16384, 17408): fp16 scale pairs, tile t at 16384 + 32 t:
+#     (s[512 rb + 16 t + r, g], s[512 rb + 16 t + r + 8, g]) for r = 0..7.
+
+UNIT_ROWS = 512
+UNIT_BYTES = 17408
 
 
 def _field(code):
@@ -324,88 +330,61 @@ def _field_value(f):
 
 
 def padded_rows(n: int) -> int:
-    return (n + 15) // 16 * 16
+    return (n + UNIT_ROWS - 1) // UNIT_ROWS * UNIT_ROWS
 
 
-def pack_codes(codes) -> np.ndarray:
-    """Pack int8 codes [N,K] into the 2-bit tile format above.  Returns uint8."""
+def pack_weights(codes, scales) -> np.ndarray:
+    """Pack int8 codes [N,K] and fp16 scales [N,K/128] into the unit format."""
     codes = np.asarray(codes)
     n, k = codes.shape
     if k % GROUP:
         raise ValueError("K must be a multiple of 128")
+    g_count = k // GROUP
     npad = padded_rows(n)
     full = np.zeros((npad, k), dtype=np.int8)
     full[:n] = codes
-    t_count, g_count = npad // 16, k // GROUP
-    words = np.zeros((t_count, g_count, 32, 4), dtype=np.uint64)
-    for lane in range(32):
-        r, c = lane // 4, lane % 4
-        for i in range(4):
-            acc = np.zeros((t_count, g_count), dtype=np.uint64)
-            for e in range(8):
-                jj, p = e // 4, e % 4
-                j = 2 * i + jj
-                rows = np.arange(t_count) * 16 + r + 8 * (p % 2)
-                kk = np.arange(g_count) * GROUP + 16 * j + 2 * c + 8 * (p // 2)
-                lo = _field(full[rows[:, None], kk[None, :]])
-                hi = _field(full[rows[:, None], kk[None, :] + 1])
-                acc |= lo << np.uint64(2 * e)
-                acc |= hi << np.uint64(16 + 2 * e)
-            words[:, :, lane, i] = acc
-    return words.astype("<u4").reshape(-1).view(np.uint8).copy()
+    sfull = np.zeros((npad, g_count), dtype=np.float16)
+    sfull[:n] = np.asarray(scales, dtype=np.float16)
+    rbs = npad // UNIT_ROWS
+    # [rb, t, rh, r, g, i, jj, kh, c, lohi]: row = 512 rb + 16 t + 8 rh + r,
+    # k = 128 g + 32 i + 16 jj + 8 kh + 2 c + lohi
+    f = _field(full.reshape(rbs, 32, 2, 8, g_count, 4, 2, 2, 4, 2))
+    words = np.zeros((rbs, g_count, 32, 8, 4, 4), dtype=np.uint64)     # rb, g, t, r, c, i
+    for jj in range(2):
+        for kh in range(2):
+            for rh in range(2):
+                e = 4 * jj + 2 * kh + rh                                # p = 2 kh + rh
+                for lohi in range(2):
+                    part = f[:, :, rh, :, :, :, jj, kh, :, lohi]          # rb, t, r, g, i, c
+                    words |= part.transpose(0, 3, 1, 2, 5, 4) << np.uint64(16 * lohi + 2 * e)
+    code_bytes = words.astype("<u4").reshape(rbs, g_count, 4096).view(np.uint8)
+    sc = sfull.reshape(rbs, 32, 2, 8, g_count).transpose(0, 4, 1, 3, 2)  # rb, g, t, r, rh
+    scale_bytes = np.ascontiguousarray(sc).astype("<f2").view(np.uint8).reshape(rbs, g_count, 1024)
+    out = np.concatenate([code_bytes, scale_bytes], axis=2)
+    return out.reshape(-1).copy()
 
 
-def unpack_codes(packed, n: int, k: int) -> np.ndarray:
-    """Inverse of pack_codes: uint8 packed -> int8 codes [n, k]."""
+def unpack_weights(packed, n: int, k: int):
+    """Inverse of pack_weights: returns (codes int8 [n,k], scales fp16 [n,k/128])."""
+    g_count = k // GROUP
     npad = padded_rows(n)
-    t_count, g_count = npad // 16, k // GROUP
-    words = np.frombuffer(np.ascontiguousarray(packed).tobytes(), dtype="<u4")
-    words = words.reshape(t_count, g_count, 32, 4).astype(np.uint64)
-    out = np.zeros((npad, k), dtype=np.int8)
-    for lane in range(32):
-        r, c = lane // 4, lane % 4
-        for i in range(4):
-            w = words[:, :, lane, i]
-            for e in range(8):
-                jj, p = e // 4, e % 4
-                j = 2 * i + jj
-                rows = np.arange(t_count) * 16 + r + 8 * (p % 2)
-                kk = np.arange(g_count) * GROUP + 16 * j + 2 * c + 8 * (p // 2)
-                out[rows[:, None], kk[None, :]] = _field_value((w >> np.uint64(2 * e)) & np.uint64(3))
-                out[rows[:, None], kk[None, :] + 1] = _field_value((w >> np.uint64(16 + 2 * e)) & np.uint64(3))
-    return out[:n]
-
-
-def pack_scales(scales) -> np.ndarray:
-    """Permute fp16 scales [N,G] to the tile order used next to pack_codes.
-
-    Rows padded with zeros to a multiple of 16.  For row tile t and group g,
-    32 bytes at element offset (t*G + g)*16 hold 8 pairs; pair r (r = 0..7)
-    is (s[16t+r, g], s[16t+r+8, g]).  Returns a flat float16 array.
-    """
-    s = np.asarray(scales, dtype=np.float16)
-    n, g_count = s.shape
-    npad = padded_rows(n)
-    full = np.zeros((npad, g_count), dtype=np.float16)
-    full[:n] = s
-    t_count = npad // 16
-    out = np.zeros((t_count, g_count, 8, 2), dtype=np.float16)
-    for r in range(8):
-        out[:, :, r, 0] = full[np.arange(t_count) * 16 + r, :]
-        out[:, :, r, 1] = full[np.arange(t_count) * 16 + r + 8, :]
-    return out.reshape(-1)
-
-
-def unpack_scales(sp, n: int, g_count: int) -> np.ndarray:
-    """Inverse of pack_scales."""
-    npad = padded_rows(n)
-    t_count = npad // 16
-    a = np.asarray(sp, dtype=np.float16).reshape(t_count, g_count, 8, 2)
-    full = np.zeros((npad, g_count), dtype=np.float16)
-    for r in range(8):
-        full[np.arange(t_count) * 16 + r, :] = a[:, :, r, 0]
-        full[np.arange(t_count) * 16 + r + 8, :] = a[:, :, r, 1]
-    return full[:n]
+    rbs = npad // UNIT_ROWS
+    units = np.ascontiguousarray(packed, dtype=np.uint8).reshape(rbs, g_count, UNIT_BYTES)
+    words = units[:, :, :16384].copy().view("<u4").reshape(rbs, g_count, 32, 8, 4, 4)
+    words = words.astype(np.uint64)                                     # rb, g, t, r, c, i
+    out = np.zeros((rbs, 32, 2, 8, g_count, 4, 2, 2, 4, 2), dtype=np.int8)
+    for jj in range(2):
+        for kh in range(2):
+            for rh in range(2):
+                e = 4 * jj + 2 * kh + rh
+                for lohi in range(2):
+                    fld = (words >> np.uint64(16 * lohi + 2 * e)) & np.uint64(3)
+                    out[:, :, rh, :, :, :, jj, kh, :, lohi] = \
+                        _field_value(fld).transpose(0, 2, 3, 1, 5, 4)
+    codes = out.reshape(npad, k)
+    sc = units[:, :, 16384:].copy().view("<f2").reshape(rbs, g_count, 32, 8, 2)
+    scales = sc.transpose(0, 2, 4, 3, 1).reshape(npad, g_count)
+    return codes[:n], scales[:n].astype(np.float16)
 
 
 # --------------------------------------------------------------------------
@@ -417,11 +396,8 @@ def decode_operand(xr):
 
     For token m and 1024-block b: E = (biased exponent field of the fp32
     absmax of the block) - 127, F = 2^min(14 - E, 126); values
-    fp16_rn(xr * F) (the fp32 product is exact), stored in the layout
-    [K/32][M][32] where element k of a 32-chunk sits at position
-    8c + 4 j2 + 2 (o8 // 8) + (o8 % 2), o = k % 32, j2 = o // 16,
-    o8 = o % 16, c = (o8 % 8) // 2.  Returns (flat fp16 array, inv [M,B]
-    with inv = 1/F, and the natural-order fp16 values [M,K]).
+    fp16_rn(xr * F) (the fp32 product is exact), natural [M, K] order.
+    Returns (fp16 [M, K], inv [M, B] with inv = 1/F).
     """
     xr = np.asarray(xr, dtype=np.float32)
     m, k = xr.shape
@@ -432,10 +408,4 @@ def decode_operand(xr):
     f = np.ldexp(np.float32(1.0), sh).astype(np.float32)
     inv = np.ldexp(np.float32(1.0), -sh).astype(np.float32)
     scaled = (xr.reshape(m, nb, HBLOCK) * f[:, :, None]).astype(np.float32).reshape(m, k)
-    vals = scaled.astype(np.float16)
-    o = np.arange(32)
-    j2, o8 = o // 16, o % 16
-    pos = 8 * ((o8 % 8) // 2) + 4 * j2 + 2 * (o8 // 8) + (o8 % 2)
-    out = np.zeros((k // 32, m, 32), dtype=np.float16)
-    out[:, :, pos] = vals.reshape(m, k // 32, 32).transpose(1, 0, 2)
-    return out.reshape(-1), inv, vals
+    return scaled.astype(np.float16), inv

@@ -40,12 +40,11 @@ _SIGS = {
     "tern_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "tern_version": (ctypes.c_int, []),
     "tern_packed_bytes": (_sz, [_i64, _i64]),
-    "tern_packed_scale_bytes": (_sz, [_i64, _i64]),
     "tern_workspace_bytes": (_sz, [ctypes.c_int, _i64, _i64, _i64]),
     "tern_workspace_init": (ctypes.c_int, [_p, _sz, _p]),
-    "tern_pack": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _p]),
+    "tern_pack": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p]),
     "tern_fwht_quant": (ctypes.c_int, [_p, _i64, _i64, _p, ctypes.c_int, _p, _p, _p]),
-    "tern_gemv_decode": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
+    "tern_gemv_decode": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
     "tern_gemm_prefill_int8": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _p, _sz,
                                               _p]),
     "tern_check": (ctypes.c_int, [_p]),
@@ -120,10 +119,6 @@ def tern_packed_bytes(n: int, k: int) -> int:
     return lib().tern_packed_bytes(n, k)
 
 
-def tern_packed_scale_bytes(n: int, k: int) -> int:
-    return lib().tern_packed_scale_bytes(n, k)
-
-
 def tern_workspace_bytes(op: int, m: int, n: int, k: int) -> int:
     return lib().tern_workspace_bytes(op, m, n, k)
 
@@ -133,9 +128,9 @@ def tern_workspace_init(ws, nbytes: int | None = None, stream=None):
     return _call("tern_workspace_init", _ptr(ws), nb, _stream(stream))
 
 
-def tern_pack(codes, scales, n, k, packed, scales_packed, q, rscale, w_q, stream=None):
-    return _call("tern_pack", _ptr(codes), _ptr(scales), n, k, _ptr(packed), _ptr(scales_packed),
-                 _ptr(q), _ptr(rscale), _ptr(w_q), _stream(stream))
+def tern_pack(codes, scales, n, k, packed, q, rscale, w_q, stream=None):
+    return _call("tern_pack", _ptr(codes), _ptr(scales), n, k, _ptr(packed), _ptr(q),
+                 _ptr(rscale), _ptr(w_q), _stream(stream))
 
 
 def tern_fwht_quant(x, m, k, sign, mode, out, out_scale, stream=None):
@@ -143,9 +138,9 @@ def tern_fwht_quant(x, m, k, sign, mode, out, out_scale, stream=None):
                  _stream(stream))
 
 
-def tern_gemv_decode(packed, scales_packed, xh, xs, m, n, k, y, ws, ws_bytes, stream=None):
-    return _call("tern_gemv_decode", _ptr(packed), _ptr(scales_packed), _ptr(xh), _ptr(xs), m, n,
-                 k, _ptr(y), _ptr(ws), ws_bytes, _stream(stream))
+def tern_gemv_decode(packed, xh, xs, m, n, k, y, ws, ws_bytes, stream=None):
+    return _call("tern_gemv_decode", _ptr(packed), _ptr(xh), _ptr(xs), m, n, k, _ptr(y), _ptr(ws),
+                 ws_bytes, _stream(stream))
 
 
 def tern_gemm_prefill_int8(xq, tscale, w_q, rscale, m, n, k, y, acc=None, ws=None, ws_bytes=0,
@@ -169,8 +164,7 @@ def _need(t, dtype, name):
 class PackedLayer:
     n: int
     k: int
-    packed: torch.Tensor | None         # uint8
-    scales_packed: torch.Tensor | None  # float16
+    packed: torch.Tensor | None         # uint8, codes + scales in 17408-byte units
     q: torch.Tensor | None              # int8 [N, G]
     rscale: torch.Tensor | None         # float32 [N]
     w_q: torch.Tensor | None            # float16 [N, K]
@@ -188,16 +182,15 @@ def pack_layer(codes: torch.Tensor, scales: torch.Tensor, decode: bool = True,
     _need(scales, torch.float16, "scales")
     n, k = codes.shape
     dev = codes.device
-    packed = sp = q = rs = wq = None
+    packed = q = rs = wq = None
     if decode:
         packed = torch.empty(tern_packed_bytes(n, k), dtype=torch.uint8, device=dev)
-        sp = torch.empty(tern_packed_scale_bytes(n, k) // 2, dtype=torch.float16, device=dev)
     if prefill:
         q = torch.empty((n, k // 128), dtype=torch.int8, device=dev)
         rs = torch.empty(n, dtype=torch.float32, device=dev)
         wq = torch.empty((n, k), dtype=torch.float16, device=dev)
-    tern_pack(codes, scales, n, k, packed, sp, q, rs, wq, stream)
-    return PackedLayer(n, k, packed, sp, q, rs, wq)
+    tern_pack(codes, scales, n, k, packed, q, rs, wq, stream)
+    return PackedLayer(n, k, packed, q, rs, wq)
 
 
 def fwht(x: torch.Tensor, mode: int, sign: torch.Tensor | None = None, stream=None):
@@ -208,7 +201,7 @@ def fwht(x: torch.Tensor, mode: int, sign: torch.Tensor | None = None, stream=No
     if mode == TERN_FWHT_F32:
         out, sc = torch.empty((m, k), dtype=torch.float32, device=dev), None
     elif mode == TERN_FWHT_DECODE:
-        out = torch.empty(m * k, dtype=torch.float16, device=dev)
+        out = torch.empty((m, k), dtype=torch.float16, device=dev)
         sc = torch.empty((m, k // 1024), dtype=torch.float32, device=dev)
     else:
         out = torch.empty((m, k), dtype=torch.float16, device=dev)
@@ -241,8 +234,7 @@ def decode(layer: PackedLayer, x: torch.Tensor, ws: Workspace, y: torch.Tensor |
         y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=x.device)
     nb = tern_workspace_bytes(TERN_OP_GEMV, m, layer.n, layer.k)
     buf = ws.get(nb, stream)
-    tern_gemv_decode(layer.packed, layer.scales_packed, xh, xs, m, layer.n, layer.k, y, buf,
-                     buf.numel(), stream)
+    tern_gemv_decode(layer.packed, xh, xs, m, layer.n, layer.k, y, buf, buf.numel(), stream)
     return y
 
 

@@ -109,8 +109,8 @@ __global__ void __launch_bounds__(128) fwht_block_kernel(const uint16_t* __restr
   const int lane = threadIdx.x & 31;
   const int B = K / kHBlock;
   const long wid = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   if (wid >= static_cast<long>(M) * B) return;
   const int m = static_cast<int>(wid / B);
   const int b = static_cast<int>(wid % B);
@@ -137,19 +137,16 @@ __global__ void __launch_bounds__(128) fwht_block_kernel(const uint16_t* __restr
     const int sh = min(14 - e, 126);                 // >= -114, so 2^sh is a normal float
     const float f = __uint_as_float(static_cast<uint32_t>(sh + 127) << 23);
     const float finv = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
-    __half* o = static_cast<__half*>(out);
-    // element (ih, lane, il): chunk = b*32 + ih*8 + lane/4, k%32 = (lane%4)*8 + il
-    // position in chunk = 8*(il/2) + 4*((lane%4)/2) + 2*(lane%2) + il%2
-    const int lq = lane & 3;
+    __half* o = static_cast<__half*>(out) + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock;
 #pragma unroll
     for (int ih = 0; ih < 4; ++ih) {
-      const long chunk = static_cast<long>(b) * 32 + ih * 8 + (lane >> 2);
-      __half* base = o + (chunk * M + m) * 32 + 4 * (lq >> 1) + 2 * (lq & 1);
+      uint32_t w[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         __half2 h2 = __floats2half2_rn(__fmul_rn(v[ih][2 * t], f), __fmul_rn(v[ih][2 * t + 1], f));
-        *reinterpret_cast<__half2*>(base + 8 * t) = h2;
+        w[t] = *reinterpret_cast<uint32_t*>(&h2);
       }
+      *reinterpret_cast<uint4*>(o + ih * 256 + lane * 8) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     if (lane == 0) out_scale[static_cast<long>(m) * B + b] = finv;
   }
@@ -168,8 +165,8 @@ __global__ void __launch_bounds__(256) fwht_i8_kernel(const uint16_t* __restrict
   const int warp = threadIdx.x >> 5;
   const int m = blockIdx.x;
   const int B = K / kHBlock;
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   const uint16_t* xm = x + static_cast<long>(m) * K;
   float amax = 0.f;
   for (int b = warp; b < B; b += 8) {

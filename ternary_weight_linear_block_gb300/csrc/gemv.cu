@@ -1,329 +1,376 @@
 // Decode GEMV for M <= 16 tokens over 2-bit ternary weights.
 //
 // Page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2", section "前提":
-// y[m,n] = sum_g s[n,g] sum_{k in g} code[n,k] xr[m,k] with codes in
-// {-1,0,+1} at 2 bits and one fp16 scale per 128 elements of a row; xr is
-// the block-Hadamard-rotated activation.  Section 5 records that an int8
-// (dp4a) decode kernel added error and gained only 2% end to end, so the
-// activations stay in fp16 here.
+// y[m,n] = sum_g s[n,g] sum_{k in g} code[n,k] xr[m,k], codes in {-1,0,+1}
+// stored at 2 bits, one fp16 scale per 128 elements of a row, xr the
+// block-Hadamard-rotated activation.  Section 5 records that an int8 (dp4a)
+// decode kernel added error for a 2% end-to-end gain; here the activations
+// stay in fp16 (per-block power-of-two scaled, see tern_fwht_quant).
 //
-// Design (GB300):
-// * Each weight byte is read once for all M tokens: tokens are the n side of
-//   m16n8k16 tensor-core MMAs (one n8 tile for M <= 8, two for M <= 16), the
-//   weight rows are the m side.
-// * The packed format is laid out so that one 16-byte load per lane carries
-//   the A fragments of 8 MMAs (16 rows x 128 k), and two register
-//   instructions (shift, and) turn a 32-bit word into an fp16 pair 2*code.
-// * Per 128-wide group, the raw code products accumulate in a fresh fp32
-//   MMA accumulator; the group scale (times 1/2 for the 2*code reading, times
-//   the per-block power of two of the fp16 operand) is applied with one FMA.
-// * Work is split stream-K style: the units (256-row block, group) are cut
-//   into equal contiguous ranges, one per persistent CTA (two per SM).  A row
-//   block finished by one CTA is written directly; otherwise each
-//   contributing CTA stores its partial in a slot of the workspace and the
-//   last one to arrive (atomic counter, no waiting) sums the slots in fixed
-//   order, writes bf16 and resets the counter.
-// * The weights do not depend on the previous kernel, so each CTA issues its
-//   first weight loads before waiting on the programmatic launch dependency.
+// GB300 design.  The layer is one stream of weight bytes; everything else is
+// arranged so that stream runs at HBM speed with few instructions per byte:
+// * unit = 512 weight rows x one 128-wide group: 16384 bytes of codes and
+//   1024 bytes of scales, contiguous in the packed format, fetched by one
+//   bulk copy (L2 evict-first) into an 8-stage shared-memory ring; the
+//   activation tile of the group (16 token rows x 128 k, fp16) arrives by
+//   TMA (128-byte swizzle) into the same stage; token rows >= M are
+//   zero-filled by TMA and cost no memory traffic.
+// * 2 code is exact in fp16 and the packed format places each pair of
+//   2-bit fields so that a shift and an and give the fp16 pair
+//   (2 code(k), 2 code(k+1)): 16 codes become two m16n8k16 A fragments.
+//   Tokens are the n side of the MMA (one n8 tile for M <= 8, two for
+//   M <= 16), so every weight byte is read once for all M tokens.
+//   (On sm_103a the legacy fp8 mma.sync issues four FMA-pipe instructions
+//   per MMA and tcgen05 costs ~100 cycles per MMA even at N = 16, so the
+//   fp16 mma.sync pipe is the fastest tensor path at this shape.)
+// * sixteen consumer warps each own 32 rows (2 tiles) of a unit: B fragments
+//   come from ldmatrix, A fragments from the unpacked words; per group the
+//   fresh fp32 accumulators are scaled by the row's group scale, and per
+//   1024-block by the block's power-of-two activation factor.
+// * units are cut into equal contiguous ranges, one per persistent CTA
+//   (stream-K).  A 512-row block finished by one CTA is written directly;
+//   otherwise each contributing CTA stores its partial in a workspace slot
+//   and the last to arrive (atomic counter, no waiting) sums the slots in
+//   fixed order, writes bf16 y and resets the counter.
+// * the weight copies do not depend on the previous kernel, so the producer
+//   issues the first ring of them before the programmatic launch wait, and
+//   every CTA lets the next kernel launch as soon as it starts.
+// All barrier waits are bounded; a wait that gives up sets an error word that
+// tern_check() reports.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "sm100_ptx.cuh"
 #include "tern_internal.cuh"
 
 namespace tern {
+
+__device__ unsigned int g_gemv_error;
+
 namespace {
 
-constexpr int kWarps = 8;           // warps per CTA
-constexpr int kTW = 2;              // 16-row tiles per warp
-constexpr int kRB = kWarps * kTW * 16;  // rows per row block (256)
-constexpr int kPF = 3;              // units of weights in flight per warp
-constexpr int kCtasPerSm = 2;
+constexpr int RB = 512;                         // weight rows per unit
+constexpr int TILES = RB / 16;
+constexpr int UNIT_CODE_BYTES = RB * 32;        // 512 rows x 128 codes x 2 bits
+constexpr int UNIT_BYTES = UNIT_CODE_BYTES + TILES * 32;
+constexpr int XTILE_BYTES = 16 * kGroup * 2;    // 16 token rows x 128 k, fp16 (two 64-k boxes)
+constexpr int STAGE_BYTES = 24576;
+constexpr int STAGES = 8;
+constexpr int CONSUMERS = 16;                   // consumer warps
+constexpr int TPW = TILES / CONSUMERS;          // tiles per consumer warp (2)
+constexpr int NUM_THREADS = 32 * (1 + CONSUMERS);
+constexpr uint32_t WAIT_LIMIT = 1u << 26;
+constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
 
-struct GemvPlan {
-  int U;         // units = row blocks * G
-  int C;         // CTAs
-  int RBn;       // row blocks
-  int S;         // partial slots per row block
-};
+static_assert(XTILE_BYTES + UNIT_BYTES <= STAGE_BYTES, "stage too small");
+static_assert(STAGE_BYTES % 1024 == 0 && XTILE_BYTES % 16 == 0, "stage alignment");
+
+enum : unsigned int { ERR_PRODUCER = 1u, ERR_CONSUMER = 2u, ERR_DRAIN = 4u };
 
 __host__ __device__ inline long unit_begin(long c, long U, long C) { return c * U / C; }
-// CTA owning unit u
 __host__ __device__ inline long owner_of(long u, long U, long C) { return ((u + 1) * C - 1) / U; }
 
-__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+__device__ __forceinline__ void fail(volatile int* abort_flag, unsigned int code) {
+  *abort_flag = 1;
+  atomicOr(&g_gemv_error, code);
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1, bool zero_c) {
-  if (zero_c) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%10,%10,%10,%10};\n"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 template <int NT>
-__device__ __forceinline__ void zero_acc(float (&acc)[kTW][NT][4]) {
-#pragma unroll
-  for (int tt = 0; tt < kTW; ++tt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[tt][nt][i] = 0.f;
-}
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemv_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t* __restrict__ packed,
+                const float* __restrict__ xs, int M, int N, int K, __nv_bfloat16* __restrict__ y,
+                unsigned int* __restrict__ counters, float* __restrict__ partials, int U, int S) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
+  volatile int* s_last = abort_flag + 1;
 
-// Weights of one unit for one warp: codes of its 16-row tiles and their scales.
-struct Slot {
-  uint4 c[kTW];
-  uint32_t s[kTW];
-};
-
-template <int NT>
-__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
-    gemv_decode_kernel(const uint4* __restrict__ packed, const uint32_t* __restrict__ sp,
-                       const uint4* __restrict__ xh, const float* __restrict__ xs, int M, int N,
-                       int K, __nv_bfloat16* __restrict__ y, unsigned int* __restrict__ counters,
-                       float* __restrict__ partials, int U, int S) {
-  // Activation fragments are prefetched one unit ahead when registers allow.
-  constexpr bool kXPrefetch = (NT == 1);
-  const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int G = K / kGroup;
   const int B = K / kHBlock;
-  const int n_tiles = (N + 15) / 16;
   const int C = gridDim.x;
-  const int c = blockIdx.x;
-  const int u0 = static_cast<int>(unit_begin(c, U, C));
-  const int u1 = static_cast<int>(unit_begin(c + 1, U, C));
-  const int r = lane >> 2;   // fragment row group
-  const int cq = lane & 3;   // fragment column pair
-  const int tile_in_rb = warp * kTW;
+  const int u0 = static_cast<int>(unit_begin(blockIdx.x, U, C));
+  const int u1 = static_cast<int>(unit_begin(blockIdx.x + 1, U, C));
+  const int n_units = u1 - u0;
 
-  __shared__ int s_last;
-
-  // ---- weight prefetch cursor (rows of the warp, group) -------------------
-  int pf_u = u0, pf_rb = u0 / G, pf_g = u0 % G;
-  auto load_slot = [&](Slot& sl) {
-#pragma unroll
-    for (int tt = 0; tt < kTW; ++tt) {
-      const int tile = pf_rb * (kRB / 16) + tile_in_rb + tt;
-      if (tile < n_tiles) {
-        const long chunk = static_cast<long>(tile) * G + pf_g;
-        sl.c[tt] = ldg_stream(packed + chunk * 32 + lane);
-        sl.s[tt] = __ldg(sp + chunk * 8 + r);
-      } else {
-        sl.c[tt] = make_uint4(0, 0, 0, 0);
-        sl.s[tt] = 0u;
-      }
+  pdl_launch_dependents();   // the next kernel may start its own independent prologue
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], CONSUMERS);
     }
-    ++pf_u;
-    if (++pf_g == G) {
-      pf_g = 0;
-      ++pf_rb;
-    }
-  };
+    *abort_flag = 0;
+    ptx::mbar_fence_init();
+  }
+  __syncthreads();
 
-  Slot ring[kPF];
-#pragma unroll
-  for (int s = 0; s < kPF; ++s)
-    if (pf_u < u1) load_slot(ring[s]);
-
-  pdl_wait();
-  pdl_launch_dependents();
-
-  auto load_x = [&](int gg, uint4 (&xo)[4][NT], float (&xso)[NT][2]) {
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int tok = nt * 8 + r;
-        xo[ch][nt] = tok < M ? __ldg(xh + ((static_cast<long>(gg) * 4 + ch) * M + tok) * 4 + cq)
-                             : make_uint4(0, 0, 0, 0);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ producer
+      const uint64_t pol = ptx::l2_policy_evict_first();
+      ptx::prefetch_tmap(&tmX);
+      const int pre = n_units < STAGES ? n_units : STAGES;
+      for (int i = 0; i < pre; ++i) {
+        ptx::mbar_arrive_expect_tx(&full[i], UNIT_BYTES + XTILE_BYTES);
+        ptx::bulk_load_hint(smem + i * STAGE_BYTES + XTILE_BYTES,
+                            packed + static_cast<size_t>(u0 + i) * UNIT_BYTES, UNIT_BYTES, &full[i],
+                            pol);
       }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int tok = nt * 8 + 2 * cq + h;
-        xso[nt][h] = tok < M ? __ldg(xs + static_cast<long>(tok) * B + (gg >> 3)) : 0.f;
-      }
-  };
-
-  float acc[kTW][NT][4];
-  zero_acc<NT>(acc);
-
-  auto flush = [&](int rb, int ga, int gb) {
-    if (ga == 0 && gb == G) {   // the whole row block is ours: write y directly
-#pragma unroll
-      for (int tt = 0; tt < kTW; ++tt) {
-        const int row0 = (rb * (kRB / 16) + tile_in_rb + tt) * 16 + r;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int row = row0 + 8 * (i >> 1);
-            const int tok = nt * 8 + 2 * cq + (i & 1);
-            if (row < N && tok < M)
-              y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(acc[tt][nt][i]);
+      pdl_wait();   // the activations are written by the previous kernel
+      int g = u0 % G;
+      int issued = pre;
+      bool ok = true;
+      for (int i = 0; i < n_units; ++i) {
+        const int s = i % STAGES;
+        uint8_t* st = smem + s * STAGE_BYTES;
+        if (i >= STAGES) {
+          const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, WAIT_LIMIT)) {
+            if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
+            ok = false;
+            break;
           }
+          ptx::mbar_arrive_expect_tx(&full[s], UNIT_BYTES + XTILE_BYTES);
+          ptx::bulk_load_hint(st + XTILE_BYTES, packed + static_cast<size_t>(u0 + i) * UNIT_BYTES,
+                              UNIT_BYTES, &full[s], pol);
+          ++issued;
+        }
+        ptx::tma_load_2d(st, &tmX, &full[s], g * kGroup, 0);
+        ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[s], g * kGroup + 64, 0);
+        if (++g == G) g = 0;
       }
-      return;
+      if (!ok) {
+        // let every copy still in flight land before the CTA exits
+        for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i) {
+          const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
+          if (!ptx::mbar_wait_bounded(&full[i % STAGES], ph, WAIT_LIMIT))
+            atomicOr(&g_gemv_error, ERR_DRAIN);
+        }
+      }
     }
-    // a piece of the row block: store it in our slot, last arriver reduces
-    const long first = owner_of(static_cast<long>(rb) * G, U, C);
-    const long last_owner = owner_of(static_cast<long>(rb) * G + G - 1, U, C);
-    const long slot = c - first;
-    float* base = partials + (static_cast<long>(rb) * S + slot) * static_cast<long>(M) * kRB;
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ consumers
+    const int cw = warp - 1;          // owns tiles TPW*cw .. TPW*cw + TPW-1 of each unit
+    const int gq = lane >> 2, cq = lane & 3;
+    pdl_wait();   // xs is written by the previous kernel; y / ws may still be read by it
+
+    // ldmatrix source for this lane: matrix mi = lane / 8 covers (k16 step
+    // j0 + mi / 2, 8-wide k half mi % 2), token row 8 nt + lane % 8.
+    const int mi = lane >> 3, lrow = lane & 7;
+
+    float acc[TPW][NT][4], bacc[TPW][NT][4];
 #pragma unroll
-    for (int tt = 0; tt < kTW; ++tt) {
-      const int rowin0 = (tile_in_rb + tt) * 16 + r;
+    for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rowin = rowin0 + 8 * (i >> 1);
-          const int tok = nt * 8 + 2 * cq + (i & 1);
-          if (tok < M) __stcg(base + static_cast<long>(tok) * kRB + rowin, acc[tt][nt][i]);
-        }
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const unsigned add = static_cast<unsigned>(gb - ga);
-      const unsigned old = atomicAdd(counters + rb, add);
-      s_last = (old + add == static_cast<unsigned>(G)) ? 1 : 0;
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      const long nslots = last_owner - first + 1;
+        for (int i = 0; i < 4; ++i) acc[tt][nt][i] = bacc[tt][nt][i] = 0.f;
+
+    int rb = u0 / G, g = u0 % G, seg_g0 = g;
+
+    auto flush = [&](int ga, int gb) {
+      if (ga == 0 && gb == G) {
 #pragma unroll
-      for (int tt = 0; tt < kTW; ++tt) {
-        const int rowin0 = (tile_in_rb + tt) * 16 + r;
+        for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int row = rb * RB + 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+              const int tok = 8 * nt + 2 * cq + (i & 1);
+              if (row < N && tok < M)
+                y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(acc[tt][nt][i]);
+            }
+        return;
+      }
+      const long first = owner_of(static_cast<long>(rb) * G, U, C);
+      const long last_owner = owner_of(static_cast<long>(rb) * G + G - 1, U, C);
+      const long slot = blockIdx.x - first;
+      float* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
+#pragma unroll
+      for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int rowin = rowin0 + 8 * (i >> 1);
-            const int tok = nt * 8 + 2 * cq + (i & 1);
-            const int row = rb * kRB + rowin;
-            if (tok < M && row < N) {
-              float sum = 0.f;
-              for (long sl = 0; sl < nslots; ++sl)
-                sum += __ldcg(partials + ((static_cast<long>(rb) * S + sl) * M + tok) * kRB + rowin);
-              y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum);
-            }
+            const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+            const int tok = 8 * nt + 2 * cq + (i & 1);
+            if (tok < M) __stcg(base + tok * RB + rin, acc[tt][nt][i]);
           }
+      __threadfence();
+      ptx::named_sync(1, 32 * CONSUMERS);
+      if (cw == 0 && lane == 0) {
+        const unsigned add = static_cast<unsigned>(gb - ga);
+        const unsigned old = atomicAdd(counters + rb, add);
+        *s_last = (old + add == static_cast<unsigned>(G)) ? 1 : 0;
       }
-      if (threadIdx.x == 0) counters[rb] = 0u;
-    }
-    __syncthreads();
-  };
-
-  int rb = u0 / G, g = u0 % G;
-  int seg_g0 = g;   // first group of the current row-block segment
-  uint4 xv[4][NT];
-  float xsv[NT][2];
-  if (kXPrefetch && u0 < u1) load_x(g, xv, xsv);
-
-  for (int ub = u0; ub < u1; ub += kPF) {
+      ptx::named_sync(1, 32 * CONSUMERS);
+      if (*s_last) {
+        __threadfence();
+        const long nslots = last_owner - first + 1;
 #pragma unroll
-    for (int s = 0; s < kPF; ++s) {
-      const int u = ub + s;
-      if (u < u1) {
-        int nrb = rb, ng = g + 1;
-        if (ng == G) {
-          ng = 0;
-          ++nrb;
-        }
-        uint4 xn[4][NT];
-        float xsn[NT][2];
-        if (kXPrefetch) {
-          if (u + 1 < u1) load_x(ng, xn, xsn);
-        } else {
-          load_x(g, xv, xsv);
-        }
+        for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
-        for (int tt = 0; tt < kTW; ++tt) {
-          uint32_t s2 = ring[s].s[tt];
-          const float2 f2 = __half22float2(*reinterpret_cast<__half2*>(&s2));
-          const float sr = f2.x * 0.5f, sr8 = f2.y * 0.5f;   // 1/2 undoes the 2*code reading
-          const uint32_t w4[4] = {ring[s].c[tt].x, ring[s].c[tt].y, ring[s].c[tt].z,
-                                  ring[s].c[tt].w};
-          float d[NT][4];
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t w = w4[j >> 1];
-            const int e0 = (j & 1) * 4;
-            uint32_t a[4];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) a[p] = (w << (14 - 2 * (e0 + p))) & 0xC000C000u;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const uint4 xq = xv[j >> 1][nt];
-              mma16816(d[nt], a, (j & 1) ? xq.z : xq.x, (j & 1) ? xq.w : xq.y, j == 0);
+            for (int i = 0; i < 4; ++i) {
+              const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+              const int row = rb * RB + rin;
+              const int tok = 8 * nt + 2 * cq + (i & 1);
+              if (tok < M && row < N) {
+                float sum = 0.f;
+                for (long sl = 0; sl < nslots; ++sl)
+                  sum += __ldcg(partials + ((static_cast<long>(rb) * S + sl) * M + tok) * RB + rin);
+                y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum);
+              }
             }
-          }
+        if (cw == 0 && lane == 0) counters[rb] = 0u;
+      }
+      ptx::named_sync(1, 32 * CONSUMERS);
+    };
+
+    for (int i = 0; i < n_units; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
+      if (!ptx::mbar_wait(&full[s], ph, abort_flag, WAIT_LIMIT)) {
+        if (!*abort_flag) fail(abort_flag, ERR_CONSUMER);
+        break;
+      }
+      const uint8_t* st = smem + s * STAGE_BYTES;
+      const uint8_t* unit = st + XTILE_BYTES;
+      uint4 cv[TPW];
+      uint32_t sp[TPW];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            acc[tt][nt][0] = fmaf(d[nt][0], sr * xsv[nt][0], acc[tt][nt][0]);
-            acc[tt][nt][1] = fmaf(d[nt][1], sr * xsv[nt][1], acc[tt][nt][1]);
-            acc[tt][nt][2] = fmaf(d[nt][2], sr8 * xsv[nt][0], acc[tt][nt][2]);
-            acc[tt][nt][3] = fmaf(d[nt][3], sr8 * xsv[nt][1], acc[tt][nt][3]);
-          }
+      for (int tt = 0; tt < TPW; ++tt) {
+        cv[tt] = *reinterpret_cast<const uint4*>(unit + 512 * (TPW * cw + tt) + 16 * lane);
+        sp[tt] = *reinterpret_cast<const uint32_t*>(unit + UNIT_CODE_BYTES + 32 * (TPW * cw + tt) +
+                                                    4 * gq);
+      }
+      // B fragments: bf[nt][j][0..1] for the 8 k16 steps of the group
+      uint32_t bf[NT][8][2];
+      const uint32_t xb = ptx::smem_u32(st);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j0 = 0; j0 < 8; j0 += 2) {
+          const int j = j0 + (mi >> 1);
+          const int row = 8 * nt + lrow;
+          const int chunk = 2 * (j & 3) + (mi & 1);
+          const uint32_t addr = xb + (j >> 2) * (XTILE_BYTES / 2) + row * 128 +
+                                ((chunk ^ (row & 7)) << 4);
+          ldmatrix_x4(addr, bf[nt][j0][0], bf[nt][j0][1], bf[nt][j0 + 1][0], bf[nt][j0 + 1][1]);
         }
-        if (pf_u < u1) load_slot(ring[s]);
-        if (u + 1 == u1 || nrb != rb) {
-          flush(rb, seg_g0, g + 1);
-          zero_acc<NT>(acc);
-          seg_g0 = 0;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[s]);
+
+#pragma unroll
+      for (int tt = 0; tt < TPW; ++tt) {
+        float d[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d[nt][q] = 0.f;
+        const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t w = w4[j >> 1];
+          const int e0 = (j & 1) * 4;
+          uint32_t a[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) a[p] = (w << (14 - 2 * (e0 + p))) & 0xC000C000u;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
         }
-        rb = nrb;
-        g = ng;
-        if (kXPrefetch) {
+        __half2 s2h = *reinterpret_cast<__half2*>(&sp[tt]);
+        const float2 s2 = __half22float2(s2h);
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) xv[ch][nt] = xn[ch][nt];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            xsv[nt][0] = xsn[nt][0];
-            xsv[nt][1] = xsn[nt][1];
-          }
+        for (int nt = 0; nt < NT; ++nt) {
+          bacc[tt][nt][0] = fmaf(d[nt][0], s2.x, bacc[tt][nt][0]);
+          bacc[tt][nt][1] = fmaf(d[nt][1], s2.x, bacc[tt][nt][1]);
+          bacc[tt][nt][2] = fmaf(d[nt][2], s2.y, bacc[tt][nt][2]);
+          bacc[tt][nt][3] = fmaf(d[nt][3], s2.y, bacc[tt][nt][3]);
         }
       }
+      const bool seg_end = (i + 1 == n_units) || (g + 1 == G);
+      if (((g & 7) == 7) || seg_end) {
+        const int blk = g >> 3;
+        float f[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int tok = 8 * nt + 2 * cq + h;
+            // 1/2 undoes the 2*code reading of the weights
+            f[nt][h] = tok < M ? 0.5f * __ldg(xs + static_cast<long>(tok) * B + blk) : 0.f;
+          }
+#pragma unroll
+        for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[tt][nt][q] = fmaf(bacc[tt][nt][q], f[nt][q & 1], acc[tt][nt][q]);
+              bacc[tt][nt][q] = 0.f;
+            }
+      }
+      if (seg_end) {
+        flush(seg_g0, g + 1);
+#pragma unroll
+        for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[tt][nt][q] = 0.f;
+        seg_g0 = 0;
+      }
+      if (++g == G) {
+        g = 0;
+        ++rb;
+      }
     }
+    __syncwarp();
   }
+  __syncthreads();
 }
 
-GemvPlan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
+struct GemvPlan {
+  int U, C, RBn, S;
+};
+
+GemvPlan make_plan(int64_t N, int64_t K, int sms) {
   GemvPlan p;
   const long G = K / kGroup;
-  p.RBn = static_cast<int>((N + kRB - 1) / kRB);
+  p.RBn = static_cast<int>((N + RB - 1) / RB);
   p.U = static_cast<int>(p.RBn * G);
-  const long cmax = static_cast<long>(sms) * kCtasPerSm;
-  p.C = static_cast<int>(p.U < cmax ? p.U : cmax);
-  // slots: the most CTAs that touch one row block
+  p.C = p.U < sms ? p.U : sms;
   long s = 1;
   for (long rb = 0; rb < p.RBn; ++rb) {
     const long a = owner_of(rb * G, p.U, p.C), b = owner_of(rb * G + G - 1, p.U, p.C);
     if (b - a + 1 > s) s = b - a + 1;
   }
   p.S = static_cast<int>(s);
-  (void)M;
   return p;
 }
 
@@ -334,32 +381,82 @@ int sm_count() {
   return n;
 }
 
-}  // namespace
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Workspace: [RBn] counters (padded to 256 B), then partials [RBn][S][M][256] fp32.
-size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  const GemvPlan p = make_plan(M, N, K, sm_count());
-  const size_t cnt = (static_cast<size_t>(p.RBn) * 4 + 255) / 256 * 256;
-  return cnt + static_cast<size_t>(p.RBn) * p.S * M * kRB * sizeof(float);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
 }
 
-cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* scales_packed, const uint16_t* xh,
-                        const float* xs, int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
-                        cudaStream_t st) {
-  const GemvPlan p = make_plan(M, N, K, sm_count());
+template <int NT>
+cudaError_t launch_nt(const CUtensorMap& tm, const uint8_t* packed, const float* xs, int M, int N,
+                      int K, __nv_bfloat16* y, unsigned int* counters, float* partials,
+                      const GemvPlan& p, cudaStream_t st) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  return launch(gemv_kernel<NT>, dim3(p.C), dim3(NUM_THREADS), SMEM_BYTES, st, tm, packed, xs, M,
+                N, K, y, counters, partials, p.U, p.S);
+}
+
+}  // namespace
+
+size_t gemv_packed_bytes(int64_t N, int64_t K) {
+  return static_cast<size_t>((N + RB - 1) / RB) * static_cast<size_t>(K / kGroup) * UNIT_BYTES;
+}
+
+// Workspace: [RBn] counters (padded to 256 B), then partials [RBn][S][M][512] fp32.
+size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const GemvPlan p = make_plan(N, K, sm_count());
+  const size_t cnt = (static_cast<size_t>(p.RBn) * 4 + 255) / 256 * 256;
+  return cnt + static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(float);
+}
+
+cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* xs, int64_t M,
+                        int64_t N, int64_t K, uint16_t* y, void* ws, cudaStream_t st) {
+  const GemvPlan p = make_plan(N, K, sm_count());
   const size_t cnt = (static_cast<size_t>(p.RBn) * 4 + 255) / 256 * 256;
   unsigned int* counters = static_cast<unsigned int*>(ws);
   float* partials = reinterpret_cast<float*>(static_cast<char*>(ws) + cnt);
-  const auto* pk = reinterpret_cast<const uint4*>(packed);
-  const auto* spk = reinterpret_cast<const uint32_t*>(scales_packed);
-  const auto* xv = reinterpret_cast<const uint4*>(xh);
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // the fp16 activations [M][K]; boxes of 64 k x 16 token rows
+  CUtensorMap tm;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xh), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   auto* yy = reinterpret_cast<__nv_bfloat16*>(y);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  if (M <= 8)
-    return launch(gemv_decode_kernel<1>, dim3(p.C), dim3(kWarps * 32), 0, st, pk, spk, xv, xs, m,
-                  n, k, yy, counters, partials, p.U, p.S);
-  return launch(gemv_decode_kernel<2>, dim3(p.C), dim3(kWarps * 32), 0, st, pk, spk, xv, xs, m, n,
-                k, yy, counters, partials, p.U, p.S);
+  if (M <= 8) return launch_nt<1>(tm, packed, xs, m, n, k, yy, counters, partials, p, st);
+  return launch_nt<2>(tm, packed, xs, m, n, k, yy, counters, partials, p, st);
+}
+
+cudaError_t gemv_read_clear_error(unsigned int* err) {
+  cudaError_t e = cudaMemcpyFromSymbol(err, g_gemv_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace tern

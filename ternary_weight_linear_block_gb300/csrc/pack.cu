@@ -1,5 +1,6 @@
-// Load-time weight conversion: 2-bit tile packing of the codes, the tile
-// order of the group scales, and the scale decomposition of the int8 path.
+// Load-time weight conversion: packing of the 2-bit codes and their group
+// scales into the decode GEMV's units, and the scale decomposition of the
+// int8 path.
 //
 // Page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2": section "前提"
 // (codes in {-1,0,+1} at 2 bits, one scale per 128 elements of a row) and
@@ -7,7 +8,7 @@
 // code[n,k] q[n,k/128] fits int8 exactly).  Expanding the weights to int8
 // once here, instead of on every prefill step, removes the run-time weight
 // expansion that section 6 measures at 31 of 83 ms of ternary-linear time.
-// The packed tile format is defined in include/tern.h.
+// The packed unit format is defined in include/tern.h.
 #include <cuda_fp16.h>
 
 #include "tern_internal.cuh"
@@ -19,52 +20,46 @@ __device__ __forceinline__ uint32_t field_of(int8_t c) {
   return c == 1 ? 1u : (c == -1 ? 3u : 0u);
 }
 
-// One thread per 32-bit word of the packed codes.
-__global__ void pack_codes_kernel(const int8_t* __restrict__ codes, int N, int K,
+constexpr int kUnitRows = 512;
+constexpr int kUnitWords = 4352;       // 17408-byte unit: 4096 code words + 256 scale words
+
+// One thread per 32-bit word of the packed units (codes and scales).
+__global__ void pack_units_kernel(const int8_t* __restrict__ codes,
+                                  const uint16_t* __restrict__ scales, int N, int K,
                                   uint32_t* __restrict__ packed, long n_words) {
   pdl_wait();
   pdl_launch_dependents();
   const int G = K / kGroup;
   for (long wi = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; wi < n_words;
        wi += static_cast<long>(gridDim.x) * blockDim.x) {
-    const int i = static_cast<int>(wi & 3);
-    const int lane = static_cast<int>((wi >> 2) & 31);
-    const long tg = wi >> 7;
-    const long t = tg / G;
-    const int g = static_cast<int>(tg % G);
-    const int r = lane >> 2, c = lane & 3;
-    uint32_t w = 0;
+    const long unit = wi / kUnitWords;
+    const int w = static_cast<int>(wi % kUnitWords);
+    const long rb = unit / G;
+    const int g = static_cast<int>(unit % G);
+    uint32_t out = 0;
+    if (w < 4096) {
+      // tile t, slot L = 4 r + c, word i
+      const int t = w >> 7, lane = (w >> 2) & 31, i = w & 3;
+      const int r = lane >> 2, c = lane & 3;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int jj = e >> 2, p = e & 3;
-      const int j = 2 * i + jj;
-      const long row = 16 * t + r + 8 * (p & 1);
-      const int k = kGroup * g + 16 * j + 2 * c + 8 * (p >> 1);
-      if (row < N) {
+      for (int e = 0; e < 8; ++e) {
+        const int jj = e >> 2, p = e & 3;
+        const long row = rb * kUnitRows + 16 * t + r + 8 * (p & 1);
+        if (row >= N) continue;
+        const int k = kGroup * g + 16 * (2 * i + jj) + 2 * c + 8 * (p >> 1);
         const int8_t* src = codes + row * K + k;
-        w |= field_of(src[0]) << (2 * e);
-        w |= field_of(src[1]) << (16 + 2 * e);
+        out |= field_of(src[0]) << (2 * e);
+        out |= field_of(src[1]) << (16 + 2 * e);
       }
+    } else {
+      const int j = w - 4096;          // tile t = j / 8, pair gq = j % 8
+      const int t = j >> 3, gq = j & 7;
+      const long r0 = rb * kUnitRows + 16 * t + gq, r1 = r0 + 8;
+      const uint32_t lo = r0 < N ? scales[r0 * G + g] : 0u;
+      const uint32_t hi = r1 < N ? scales[r1 * G + g] : 0u;
+      out = lo | (hi << 16);
     }
-    packed[wi] = w;
-  }
-}
-
-// One thread per (tile, group, pair r): 32 bits = (s[16t+r][g], s[16t+r+8][g]).
-__global__ void pack_scales_kernel(const uint16_t* __restrict__ scales, int N, int G,
-                                   uint32_t* __restrict__ out, long n_pairs) {
-  pdl_wait();
-  pdl_launch_dependents();
-  for (long pi = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; pi < n_pairs;
-       pi += static_cast<long>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(pi & 7);
-    const long tg = pi >> 3;
-    const long t = tg / G;
-    const int g = static_cast<int>(tg % G);
-    const long r0 = 16 * t + r, r1 = r0 + 8;
-    const uint32_t lo = r0 < N ? scales[r0 * G + g] : 0u;
-    const uint32_t hi = r1 < N ? scales[r1 * G + g] : 0u;
-    out[pi] = lo | (hi << 16);
+    packed[wi] = out;
   }
 }
 
@@ -123,19 +118,14 @@ unsigned grid_for(long items, int threads) {
 }  // namespace
 
 cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
-                        uint8_t* packed, uint16_t* scales_packed, int8_t* q, float* rscale,
-                        uint16_t* w_q, cudaStream_t st) {
+                        uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q,
+                        cudaStream_t st) {
   const int n = static_cast<int>(N), k = static_cast<int>(K), G = static_cast<int>(K / kGroup);
-  const long np = pad16(N);
   cudaError_t e = cudaSuccess;
   if (packed != nullptr) {
-    const long n_words = np * K / 16;
-    e = launch(pack_codes_kernel, dim3(grid_for(n_words, 256)), dim3(256), 0, st, codes, n, k,
-               reinterpret_cast<uint32_t*>(packed), n_words);
-    if (e != cudaSuccess) return e;
-    const long n_pairs = np / 16 * G * 8;
-    e = launch(pack_scales_kernel, dim3(grid_for(n_pairs, 256)), dim3(256), 0, st, scales, n, G,
-               reinterpret_cast<uint32_t*>(scales_packed), n_pairs);
+    const long n_words = (N + kUnitRows - 1) / kUnitRows * G * kUnitWords;
+    e = launch(pack_units_kernel, dim3(grid_for(n_words, 256)), dim3(256), 0, st, codes, scales, n,
+               k, reinterpret_cast<uint32_t*>(packed), n_words);
     if (e != cudaSuccess) return e;
   }
   if (q != nullptr) {

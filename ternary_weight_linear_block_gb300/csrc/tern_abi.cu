@@ -50,13 +50,8 @@ const char* tern_status_str(int status) {
 int tern_version(void) { return 100; }
 
 size_t tern_packed_bytes(int64_t N, int64_t K) {
-  if (N < 0 || K < 0) return 0;
-  return static_cast<size_t>(pad16(N)) * static_cast<size_t>(K) / 4;
-}
-
-size_t tern_packed_scale_bytes(int64_t N, int64_t K) {
-  if (N < 0 || K < 0) return 0;
-  return static_cast<size_t>(pad16(N)) * static_cast<size_t>(K / kGroup) * 2;
+  if (N < 0 || K < 0 || K % kGroup != 0) return 0;
+  return gemv_packed_bytes(N, K);
 }
 
 size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
@@ -72,23 +67,20 @@ tern_status tern_workspace_init(void* ws, size_t bytes, void* stream) {
 }
 
 tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
-                      uint8_t* packed, uint16_t* scales_packed, int8_t* q, float* rscale,
-                      uint16_t* w_q, void* stream) {
+                      uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q, void* stream) {
   if (N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
   if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
-  if ((packed == nullptr) != (scales_packed == nullptr)) return TERN_ERR_INVALID_ARG;
   if ((q == nullptr) != (rscale == nullptr)) return TERN_ERR_INVALID_ARG;
   if (w_q != nullptr && q == nullptr) return TERN_ERR_INVALID_ARG;
   if (N == 0) return TERN_OK;
   if (codes == nullptr || scales == nullptr) return TERN_ERR_INVALID_ARG;
   if (packed == nullptr && q == nullptr) return TERN_OK;
   if (!aligned16(codes) || !aligned16(scales) || (packed && !aligned16(packed)) ||
-      (scales_packed && !aligned16(scales_packed)) || (q && !aligned16(q)) ||
-      (rscale && !aligned16(rscale)) || (w_q && !aligned16(w_q)))
+      (q && !aligned16(q)) || (rscale && !aligned16(rscale)) || (w_q && !aligned16(w_q)))
     return TERN_ERR_ALIGN;
   if (N > (int64_t(1) << 30) / (K / 16)) return TERN_ERR_SHAPE;  // keeps int32 row math safe
   if (!device_supported()) return TERN_ERR_UNSUPPORTED;
-  return from_cuda(launch_pack(codes, scales, N, K, packed, scales_packed, q, rscale, w_q,
+  return from_cuda(launch_pack(codes, scales, N, K, packed, q, rscale, w_q,
                                static_cast<cudaStream_t>(stream)));
 }
 
@@ -109,26 +101,23 @@ tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_
       launch_fwht(x, M, K, sign, mode, out, out_scale, static_cast<cudaStream_t>(stream)));
 }
 
-tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* scales_packed,
-                             const uint16_t* xh, const float* xs, int64_t M, int64_t N,
-                             int64_t K, uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const float* xs,
+                             int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                             size_t ws_bytes, void* stream) {
   if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
   if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
   if (M > 16) return TERN_ERR_SHAPE;
   if (N > (int64_t(1) << 30) / (K / 16)) return TERN_ERR_SHAPE;
   if (M == 0 || N == 0) return TERN_OK;
-  if (packed == nullptr || scales_packed == nullptr || xh == nullptr || xs == nullptr ||
-      y == nullptr)
+  if (packed == nullptr || xh == nullptr || xs == nullptr || y == nullptr)
     return TERN_ERR_INVALID_ARG;
-  if (!aligned16(packed) || !aligned16(scales_packed) || !aligned16(xh) || !aligned16(xs) ||
-      !aligned16(y))
+  if (!aligned16(packed) || !aligned16(xh) || !aligned16(xs) || !aligned16(y))
     return TERN_ERR_ALIGN;
   const size_t need = gemv_workspace_bytes(M, N, K);
   if (ws == nullptr || ws_bytes < need) return TERN_ERR_WORKSPACE;
   if (!aligned16(ws)) return TERN_ERR_ALIGN;
   if (!device_supported()) return TERN_ERR_UNSUPPORTED;
-  return from_cuda(launch_gemv(packed, scales_packed, xh, xs, M, N, K, y, ws,
-                               static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_gemv(packed, xh, xs, M, N, K, y, ws, static_cast<cudaStream_t>(stream)));
 }
 
 tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
@@ -155,10 +144,10 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
 tern_status tern_check(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return TERN_ERR_CUDA;
-  unsigned int err = 0;
-  e = gemm_read_clear_error(&err);
-  if (e != cudaSuccess) return TERN_ERR_CUDA;
-  return err ? TERN_ERR_TIMEOUT : TERN_OK;
+  unsigned int err_gemm = 0, err_gemv = 0;
+  if (gemm_read_clear_error(&err_gemm) != cudaSuccess) return TERN_ERR_CUDA;
+  if (gemv_read_clear_error(&err_gemv) != cudaSuccess) return TERN_ERR_CUDA;
+  return (err_gemm | err_gemv) ? TERN_ERR_TIMEOUT : TERN_OK;
 }
 
 }  // extern "C"

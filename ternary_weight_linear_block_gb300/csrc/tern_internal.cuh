@@ -43,16 +43,17 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
 cudaError_t launch_fwht(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign, int mode,
                         void* out, float* out_scale, cudaStream_t st);
 cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
-                        uint8_t* packed, uint16_t* scales_packed, int8_t* q, float* rscale,
-                        uint16_t* w_q, cudaStream_t st);
-size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
-cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* scales_packed, const uint16_t* xh,
-                        const float* xs, int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                        uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q,
                         cudaStream_t st);
+size_t gemv_packed_bytes(int64_t N, int64_t K);
+size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* xs, int64_t M,
+                        int64_t N, int64_t K, uint16_t* y, void* ws, cudaStream_t st);
 cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
                         const float* rscale, int64_t M, int64_t N, int64_t K, uint16_t* y,
                         int32_t* acc, cudaStream_t st);
-// Reads and clears the GEMM translation unit's device error word.
+// Read and clear the device error word of the GEMV / GEMM translation unit.
+cudaError_t gemv_read_clear_error(unsigned int* err);
 cudaError_t gemm_read_clear_error(unsigned int* err);
 
 }  // namespace tern

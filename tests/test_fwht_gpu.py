@@ -27,7 +27,7 @@ def _run(xd, m, k, mode, sign=None):
     if mode == B.TERN_FWHT_F32:
         out, sc = poison(torch.empty((m, k), dtype=torch.float32, device=dev)), None
     elif mode == B.TERN_FWHT_DECODE:
-        out = poison(torch.empty(m * k, dtype=torch.float16, device=dev))
+        out = poison(torch.empty((m, k), dtype=torch.float16, device=dev))
         sc = poison(torch.empty((m, k // 1024), dtype=torch.float32, device=dev))
     else:
         out = poison(torch.empty((m, k), dtype=torch.float16, device=dev))
@@ -50,8 +50,8 @@ def test_fwht_f32_bitwise(m, k, frac, mult):
 def test_fwht_decode_operand_bitwise(m, k, frac, mult):
     bits, x = I.make_activations(2, m, k, frac, mult)
     out, sc = _run(to_dev_bf16(bits), m, k, B.TERN_FWHT_DECODE)
-    flat, inv, _ = O.decode_operand(O.fwht_f32(x))
-    assert np.array_equal(f16_bits(out), flat.view(np.uint16))
+    vals, inv = O.decode_operand(O.fwht_f32(x))
+    assert np.array_equal(f16_bits(out), vals.view(np.uint16))
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), inv.view(np.uint32))
 
 
@@ -100,8 +100,8 @@ def test_degenerate_inputs():
     ref = O.fwht_f32(xf)
     assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
     out, sc = _run(xd, 4, k, B.TERN_FWHT_DECODE)
-    flat, inv, _ = O.decode_operand(ref)
-    assert np.array_equal(f16_bits(out), flat.view(np.uint16))
+    vals, inv = O.decode_operand(ref)
+    assert np.array_equal(f16_bits(out), vals.view(np.uint16))
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), inv.view(np.uint32))
     out, sc = _run(xd, 4, k, B.TERN_FWHT_I8)
     xq, ts = O.quant_tokens(ref)

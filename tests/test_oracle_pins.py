@@ -304,60 +304,71 @@ def test_int8_path_error_against_exact_tiny_config():
 # ---------------------------------------------------------------- 2-bit format
 
 def test_pack_format_golden():
-    codes = np.zeros((16, 128), np.int8)
-    expect = []
+    codes = np.zeros((512, 256), np.int8)
+    expect = {}
     for r in _rows("packed_format.txt"):
         left, off, word = [p.strip() for p in r.split("|")]
         row, k, c = [int(v) for v in left.split()]
         codes[row, k] = c
-        expect.append((int(off), int(word, 16)))
-    p = O.pack_codes(codes)
-    assert p.size == 512
-    words = p.view("<u4")
-    nonzero = {i * 4: int(w) for i, w in enumerate(words) if w}
-    assert nonzero == dict(expect)
+        expect[int(off)] = int(word, 16)
+    scales = np.zeros((512, 2), np.float16)
+    scales[3, 1] = 0.5      # unit 1, tile 0, pair r = 3, low half
+    scales[20, 0] = 0.25    # unit 0, tile 1, pair r = 4, low half
+    p = O.pack_weights(codes, scales)
+    assert p.size == 2 * 17408
+    code_words = {}
+    for unit in range(2):
+        w = p[unit * 17408:unit * 17408 + 16384].view("<u4")
+        code_words.update({unit * 17408 + 4 * i: int(v) for i, v in enumerate(w) if v})
+    assert code_words == expect
+    # scale pairs: s[3, 1] -> unit 1, tile 0, pair 3, low half; s[20, 0] -> tile 1, pair 4
+    assert p[17408 + 16384 + 12:17408 + 16384 + 14].view("<f2")[0] == np.float16(0.5)
+    assert p[16384 + 32 + 16:16384 + 32 + 18].view("<f2")[0] == np.float16(0.25)
+    assert np.count_nonzero(p[16384:17408]) == 1 and np.count_nonzero(p[17408 + 16384:]) == 1
 
 
-@pytest.mark.parametrize("n,k", [(16, 128), (40, 1024), (7, 256), (256, 1024)])
+@pytest.mark.parametrize("n,k", [(512, 128), (40, 1024), (7, 256), (700, 2048)])
 def test_pack_roundtrip(n, k):
     rng = np.random.default_rng(n * 7 + k)
     codes = rng.integers(-1, 2, (n, k)).astype(np.int8)
-    p = O.pack_codes(codes)
-    assert p.size == O.padded_rows(n) * k // 4
-    assert np.array_equal(O.unpack_codes(p, n, k), codes)
     s = rng.standard_normal((n, k // 128)).astype(np.float16)
-    sp = O.pack_scales(s)
-    assert sp.size == O.padded_rows(n) * (k // 128)
-    assert np.array_equal(O.unpack_scales(sp, n, k // 128), s)
+    p = O.pack_weights(codes, s)
+    assert p.size == O.padded_rows(n) // 512 * (k // 128) * 17408
+    c2, s2 = O.unpack_weights(p, n, k)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, s)
 
 
 def test_pack_halfword_reading_gives_two_times_code():
-    # The fp16 reading of the format: (word << (14 - 2e)) & 0xC000C000 is a
-    # pair of fp16 values 2*code (0x4000 = 2.0, 0xC000 = -2.0, 0 / -0).
+    # (w_i << (14 - 2e)) & 0xC000C000 read as an fp16 pair is
+    # (2 code(row, k), 2 code(row, k + 1)) with row = 16 t + r + 8 (p % 2),
+    # k = 16 j + 2 c + 8 (p // 2): register p of the A fragment of the
+    # m16n8k16 MMA for k16 step j (0x4000 = 2.0, 0xC000 = -2.0).
     rng = np.random.default_rng(12)
-    codes = rng.integers(-1, 2, (16, 128)).astype(np.int8)
-    words = O.pack_codes(codes).view("<u4").reshape(32, 4)
-    for lane in range(32):
-        r, c = lane // 4, lane % 4
-        for i in range(4):
-            for e in range(8):
-                v = (int(words[lane, i]) << (14 - 2 * e)) & 0xC000C000
-                lo = np.array([v & 0xFFFF], np.uint16).view(np.float16)[0]
-                hi = np.array([v >> 16], np.uint16).view(np.float16)[0]
-                jj, p = e // 4, e % 4
-                row = r + 8 * (p % 2)
-                k = 16 * (2 * i + jj) + 2 * c + 8 * (p // 2)
-                assert float(lo) == 2.0 * codes[row, k]
-                assert float(hi) == 2.0 * codes[row, k + 1]
+    codes = rng.integers(-1, 2, (512, 128)).astype(np.int8)
+    words = O.pack_weights(codes, np.zeros((512, 1), np.float16))[:16384].view("<u4")
+    words = words.reshape(32, 32, 4)                 # tile, slot, word
+    for t in range(0, 32, 7):
+        for lane in range(32):
+            r, c = lane // 4, lane % 4
+            for i in range(4):
+                for e in range(8):
+                    v = (int(words[t, lane, i]) << (14 - 2 * e)) & 0xC000C000
+                    lo = np.array([v & 0xFFFF], np.uint16).view(np.float16)[0]
+                    hi = np.array([v >> 16], np.uint16).view(np.float16)[0]
+                    jj, p = e // 4, e % 4
+                    row = 16 * t + r + 8 * (p % 2)
+                    k = 16 * (2 * i + jj) + 2 * c + 8 * (p // 2)
+                    assert float(lo) == 2.0 * codes[row, k]
+                    assert float(hi) == 2.0 * codes[row, k + 1]
 
 
 # ---------------------------------------------------------------- decode operand
 
-def test_decode_operand_range_precision_and_layout():
+def test_decode_operand_range_and_precision():
     rng = np.random.default_rng(13)
     xr = (rng.standard_normal((3, 2048)) * np.array([[1e-3], [1.0], [3e4]])).astype(np.float32)
     xr[1, 1024:] = 0.0                                  # an all-zero block
-    flat, inv, vals = O.decode_operand(xr)
+    vals, inv = O.decode_operand(xr)
     # fp16 cast matches torch's (library) round-to-nearest-even cast
     f = (1.0 / inv).astype(np.float32)
     scaled = (xr.reshape(3, 2, 1024) * f[:, :, None]).reshape(3, 2048).astype(np.float32)
@@ -371,14 +382,3 @@ def test_decode_operand_range_precision_and_layout():
                 assert 2 ** 14 <= bm[m, b] < 2 ** 15
     back = vals.astype(np.float64) * np.repeat(inv, 1024, axis=1)
     assert np.all(np.abs(back - xr) <= np.abs(xr) * 2.0 ** -11 + 1e-30)
-    # layout: the B-fragment reading (lane c gets k = 2c, 2c+1, 2c+8, 2c+9 of
-    # each 16-wide step) recovers the natural order
-    chunks = flat.reshape(2048 // 32, 3, 4, 8)
-    for ch in range(0, 64, 7):
-        for m in range(3):
-            for c in range(4):
-                for j2 in range(2):
-                    kb = ch * 32 + 16 * j2
-                    got = chunks[ch, m, c, 4 * j2:4 * j2 + 4]
-                    want = vals[m, [kb + 2 * c, kb + 2 * c + 1, kb + 2 * c + 8, kb + 2 * c + 9]]
-                    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))

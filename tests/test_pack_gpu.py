@@ -21,25 +21,23 @@ def _pack(codes, scales):
     n, k = codes.shape
     cd, sd = to_dev(codes), to_dev(scales)
     packed = poison(torch.empty(B.tern_packed_bytes(n, k), dtype=torch.uint8, device="cuda"))
-    sp = poison(torch.empty(B.tern_packed_scale_bytes(n, k) // 2, dtype=torch.float16, device="cuda"))
     q = poison(torch.empty((n, k // 128), dtype=torch.int8, device="cuda"))
     rs = poison(torch.empty(n, dtype=torch.float32, device="cuda"))
     wq = poison(torch.empty((n, k), dtype=torch.float16, device="cuda"))
-    B.tern_pack(cd, sd, n, k, packed, sp, q, rs, wq)
+    B.tern_pack(cd, sd, n, k, packed, q, rs, wq)
     torch.cuda.synchronize()
-    return packed, sp, q, rs, wq
+    return packed, q, rs, wq
 
 
-@pytest.mark.parametrize("n,k", [(256, 1024), (100, 2048), (16, 1024), (5120, 17408), (10240, 5120)])
+@pytest.mark.parametrize("n,k", [(256, 1024), (100, 2048), (16, 1024), (300, 3072), (5120, 17408), (10240, 5120)])
 def test_pack_bitwise(n, k):
     codes = I.make_codes(5, n, k)
     scales = I.make_scales(5, n, k)
     scales[3 % n] = 0                          # a zero row
     if n > 10:
         scales[7, ::2] = -scales[7, ::2]       # negative scales
-    packed, sp, q, rs, wq = _pack(codes, scales)
-    assert np.array_equal(packed.cpu().numpy(), O.pack_codes(codes))
-    assert np.array_equal(f16_bits(sp), O.pack_scales(scales).view(np.uint16))
+    packed, q, rs, wq = _pack(codes, scales)
+    assert np.array_equal(packed.cpu().numpy(), O.pack_weights(codes, scales))
     qo, ro, _ = O.decompose_scales(scales)
     assert np.array_equal(q.cpu().numpy(), qo)
     assert np.array_equal(rs.cpu().numpy().view(np.uint32), ro.view(np.uint32))
@@ -52,9 +50,8 @@ def test_pack_full_gate_up_shape():
     layer = I.GATE_UP
     codes = I.make_codes(0, layer.n, layer.k)
     scales = I.make_scales(0, layer.n, layer.k)
-    packed, sp, q, rs, wq = _pack(codes, scales)
-    assert np.array_equal(packed.cpu().numpy(), O.pack_codes(codes))
-    assert np.array_equal(f16_bits(sp), O.pack_scales(scales).view(np.uint16))
+    packed, q, rs, wq = _pack(codes, scales)
+    assert np.array_equal(packed.cpu().numpy(), O.pack_weights(codes, scales))
     qo, ro, _ = O.decompose_scales(scales)
     assert np.array_equal(q.cpu().numpy(), qo)
     rows = np.random.default_rng(0).choice(layer.n, 256, replace=False)
