@@ -74,12 +74,24 @@ def _barrier(ws):
 
 
 def _max_over_ranks(v: float, ws: int) -> float:
+    """The slowest rank's time (every rank gets it)."""
     if ws <= 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank streams its own weights (independent layers): weak scaling."""
+    return 1000 * rank
+
+
+def aggregate_value(bytes_per_step: int, steps: int, ws: int, t_max: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time."""
+    return bytes_per_step * steps * ws / t_max / 1e9
 
 
 # ---------------------------------------------------------------- clocks
@@ -243,7 +255,7 @@ def run_decode(args, rank, ws, local):
     copies = max(4, int(np.ceil(4 * L2_BYTES / per_copy)) + 1)
     hbm_peak, tc_peak, peak_kind = _peaks()
     with torch.cuda.stream(stream):
-        layers = _make_layers(layer, copies, seed=rank, prefill=False)
+        layers = _make_layers(layer, copies, seed=rank_seed(rank), prefill=False)
         xs_host = [_activations(layer, m, seed=rank * 10 + m) for m in DECODE_MS]
         run = DecodeRunner(layers, xs_host, stream)
         for _ in range(args.warmup):
@@ -285,7 +297,7 @@ def run_decode(args, rank, ws, local):
         te2e = _max_over_ranks(te2e, ws)
 
     bytes_step = run.bytes_per_step()
-    value = bytes_step * args.steps * ws / t / 1e9
+    value = aggregate_value(bytes_step, args.steps, ws, t)
     m = DECODE_MS[kb]
     alg = _gemv_algorithmic_bytes(m, layer.n, layer.k)
     achieved = alg / (gemv_us * 1e-6) / 1e9
@@ -317,6 +329,53 @@ def run_decode(args, rank, ws, local):
         "clocks": clocks,
     }
     return out, layers
+
+
+def run_prefill(args, local, m=2048):
+    """Prefill int8 path through gate/up 5120->34816 at M tokens: the rotation
+    with per-token int8 quantisation, then the exact int8 GEMM (int8 values,
+    fp16 tensor pipe) with its per-row / per-token rescale to bf16."""
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    layer = I.GATE_UP
+    _, tc_peak, peak_kind = _peaks()
+    with torch.cuda.stream(stream):
+        lay = _make_layers(layer, 1, seed=7, prefill=True)[0]
+        x = _activations(layer, m, seed=77).cuda()
+        xq = torch.empty((m, layer.k), dtype=torch.float16, device="cuda")
+        ts = torch.empty(m, dtype=torch.float32, device="cuda")
+        y = torch.empty((m, layer.n), dtype=torch.bfloat16, device="cuda")
+        st = stream.cuda_stream
+
+        def step():
+            B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_I8, xq, ts, st)
+            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y,
+                                     stream=st)
+
+        def gemm_only():
+            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y,
+                                     stream=st)
+
+        for _ in range(max(3, args.warmup // 4)):
+            step()
+        torch.cuda.synchronize()
+        n = 20
+        t = _time_region(step, n, stream, 1)
+        tg = _time_region(gemm_only, n, stream, 1)
+        B.tern_check(stream)
+    ops = 2.0 * m * layer.n * layer.k
+    del lay
+    torch.cuda.empty_cache()
+    return {"metric": "prefill int8 TOPS (2*M*N*K / step time)", "value": round(ops * n / t / 1e12, 1),
+            "unit": "TOPS", "workload": f"prefill gate/up 5120->34816, M={m}",
+            "ms_per_step": round(t / n * 1e3, 4),
+            "roofline": {"bound": "tensor", "kernel": "tern_gemm_prefill_int8",
+                         "achieved": round(ops * n / tg / 1e12, 1), "peak": tc_peak,
+                         "unit": "TFLOP/s", "frac": round(ops * n / tg / 1e12 / tc_peak, 4),
+                         "avg_launch_us": round(tg / n * 1e6, 2), "traffic": None,
+                         "peak_source": f"{peak_kind} bf16_tflops (MEASURED_PEAKS.json): the "
+                                        "int8 values run on the fp16/bf16 tensor pipe; "
+                                        "sm_103a has no tcgen05 int8 kind"}}
 
 
 def run_cpu_baseline(args, budget_s=15.0):
@@ -382,10 +441,11 @@ def run_reference(args, rank, ws):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -405,6 +465,8 @@ def main():
     line, layers = run_decode(args, rank, ws, local)
     del layers
     torch.cuda.empty_cache()
+    if not args.no_prefill:
+        line["prefill"] = run_prefill(args, local)
     if rank == 0:
         if not args.no_cpu_baseline and ws == 1:
             line["cpu_baseline"] = run_cpu_baseline(args)
