@@ -172,6 +172,33 @@ tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const fl
                              size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * tern_gemv_decode_noalloc -- the same decode GEMV as tern_gemv_decode, for
+ * callers that cannot allocate device memory.  The page has no counterpart.
+ *
+ * An application that embeds this layer and owns every byte of device memory
+ * through its own pool, handing the layer only its inputs and outputs, cannot
+ * give it a separate workspace, and a decode loop that must never stall
+ * cannot call cudaMalloc, which may synchronise the device.  This call takes
+ * no workspace and allocates nothing: its scratch (the per-row-block arrival
+ * counters and partial sums) lives in a static device array of
+ * TERN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.
+ *
+ *   packed, xh, xs, M, N, K, y, stream: as for tern_gemv_decode.
+ * Returns TERN_ERR_WORKSPACE when tern_workspace_bytes(TERN_OP_GEMV, M, N, K)
+ * exceeds TERN_NOALLOC_SCRATCH_BYTES (nothing is launched).  The first call
+ * on a device, with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  Every call shares the one array, which keeps the last
+ * call's contents: each call clears the counters on its stream first, and
+ * calls that overlap on the GPU race on the array.
+ * ---------------------------------------------------------------------- */
+#define TERN_NOALLOC_SCRATCH_BYTES (16u << 20)
+tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uint16_t* xh, const float* xs,
+                                     int64_t M, int64_t N, int64_t K, uint16_t* y,
+                                     void* stream);
+
+/* ------------------------------------------------------------------------
  * tern_gemm_prefill_int8 -- the int8 prefill GEMM of page section 4:
  *     acc[m,n] = sum_k xq[m,k] * W_int8[n,k]            (exact int32)
  *     y[m,n]   = bf16_rn(((float)acc[m,n] * tscale[m]) * rscale[n])

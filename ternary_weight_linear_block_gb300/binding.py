@@ -48,6 +48,7 @@ _SIGS = {
     "tern_gemm_prefill_int8": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _p, _sz,
                                               _p]),
     "tern_check": (ctypes.c_int, [_p]),
+    "tern_gemv_decode_noalloc": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
 }
 
 _lib = None
@@ -151,6 +152,13 @@ def tern_gemm_prefill_int8(xq, tscale, w_q, rscale, m, n, k, y, acc=None, ws=Non
 
 def tern_check(stream=None):
     return _call("tern_check", _stream(stream))
+
+
+def tern_gemv_decode_noalloc(packed, xh, xs, m, n, k, y, stream=None):
+    """Decode GEMV with the library's fixed scratch array (no workspace, no
+    allocation), for callers that cannot allocate device memory."""
+    return _call("tern_gemv_decode_noalloc", _ptr(packed), _ptr(xh), _ptr(xs), m, n, k, _ptr(y),
+                 _stream(stream))
 
 
 # ---------------------------------------------------------------- conveniences

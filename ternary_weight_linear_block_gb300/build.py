@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtern.so")
-SOURCES = ["tern_abi.cu", "fwht.cu", "pack.cu", "gemv.cu", "gemm.cu"]
+SOURCES = ["tern_abi.cu", "fwht.cu", "pack.cu", "gemv.cu", "gemm.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

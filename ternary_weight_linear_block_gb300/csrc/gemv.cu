@@ -421,6 +421,11 @@ size_t gemv_packed_bytes(int64_t N, int64_t K) {
   return static_cast<size_t>((N + RB - 1) / RB) * static_cast<size_t>(K / kGroup) * UNIT_BYTES;
 }
 
+// Bytes of the counter region at the start of the workspace.
+size_t gemv_counter_bytes(int64_t N) {
+  return (static_cast<size_t>((N + RB - 1) / RB) * 4 + 255) / 256 * 256;
+}
+
 // Workspace: [RBn] counters (padded to 256 B), then partials [RBn][S][M][512] fp32.
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const GemvPlan p = make_plan(N, K, sm_count());

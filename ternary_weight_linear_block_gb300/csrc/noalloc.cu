@@ -1,0 +1,76 @@
+// tern_gemv_decode_noalloc: the decode GEMV with its scratch memory in a
+// fixed, file-scope device array instead of a caller-provided workspace.
+//
+// Who needs it: an application that embeds this layer and owns all of its
+// device memory through its own pool (and hands the layer only its input and
+// output buffers) cannot let the library take a separate workspace, and a
+// decode loop that must never stall cannot call cudaMalloc, which may
+// synchronise the whole device.  This entry point allocates nothing: the
+// GEMV's per-row-block arrival counters and partial sums live in
+// g_noalloc_scratch, a static device array of TERN_NOALLOC_SCRATCH_BYTES that
+// every GPU loading the library keeps until the process exits.
+//
+// The first call on a device (with that device current) looks up the array's
+// device address with cudaGetSymbolAddress and caches it per device; that
+// first call should come before any stream capture.  All calls share the one
+// array and it keeps the last call's contents, so each call clears the
+// counter region on its stream before the kernel; calls that overlap on the
+// GPU (for example on two streams) race on the array.
+#include "tern_internal.cuh"
+
+namespace tern {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TERN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices];   // device address of g_noalloc_scratch, per device
+int g_dev_ok[kMaxDevices];           // 0 unknown, 1 sm_103, -1 other
+
+cudaError_t scratch_address(int dev, void** out) {
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+bool device_ok(int dev) {
+  if (g_dev_ok[dev] != 0) return g_dev_ok[dev] > 0;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return false;
+  g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  return g_dev_ok[dev] > 0;
+}
+
+}  // namespace
+}  // namespace tern
+
+extern "C" tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uint16_t* xh,
+                                                const float* xs, int64_t M, int64_t N, int64_t K,
+                                                uint16_t* y, void* stream) {
+  using namespace tern;
+  if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (K == 0 || K % kHBlock != 0 || K > kMaxK || M > 16) return TERN_ERR_SHAPE;
+  if (N > (int64_t(1) << 30) / (K / 16)) return TERN_ERR_SHAPE;
+  if (M == 0 || N == 0) return TERN_OK;
+  if (packed == nullptr || xh == nullptr || xs == nullptr || y == nullptr)
+    return TERN_ERR_INVALID_ARG;
+  if (!aligned16(packed) || !aligned16(xh) || !aligned16(xs) || !aligned16(y))
+    return TERN_ERR_ALIGN;
+  if (gemv_workspace_bytes(M, N, K) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ERR_WORKSPACE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || !device_ok(dev))
+    return TERN_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (scratch_address(dev, &scratch) != cudaSuccess) return TERN_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, gemv_counter_bytes(N), st) != cudaSuccess) return TERN_ERR_CUDA;
+  return launch_gemv(packed, xh, xs, M, N, K, y, scratch, st) == cudaSuccess ? TERN_OK
+                                                                           : TERN_ERR_CUDA;
+}
