@@ -103,7 +103,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
-  volatile int* s_last = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -176,9 +175,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int gq = lane >> 2, cq = lane & 3;
     pdl_wait();   // xs is written by the previous kernel; y / ws may still be read by it
 
-    // ldmatrix source for this lane: matrix mi = lane / 8 covers (k16 step
-    // j0 + mi / 2, 8-wide k half mi % 2), token row 8 nt + lane % 8.
+    // Per-lane shared-memory offsets, fixed for the whole kernel.  ldmatrix
+    // matrix mi = lane / 8 covers (k16 step j0 + mi / 2, 8-wide k half mi % 2),
+    // token row 8 nt + lane % 8, in the 128-byte-swizzled activation tile.
     const int mi = lane >> 3, lrow = lane & 7;
+    uint32_t bf_off[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = 2 * q + (mi >> 1);
+        const int row = 8 * nt + lrow;
+        const int chunk = 2 * (j & 3) + (mi & 1);
+        bf_off[nt][q] = (j >> 2) * (XTILE_BYTES / 2) + row * 128 + ((chunk ^ (row & 7)) << 4);
+      }
+    const uint32_t smem_base = ptx::smem_u32(smem);
 
     float acc[TPW][NT][4], bacc[TPW][NT][4];
 #pragma unroll
@@ -190,6 +201,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     int rb = u0 / G, g = u0 % G, seg_g0 = g;
 
+    // A segment of a row block ends here.  A row block finished by this CTA
+    // is written directly.  Otherwise each warp stores its 32 rows in this
+    // CTA's slot and bumps the arrival counter of (row block, warp slice); the
+    // warp whose add completes all G groups sums the slots in fixed order.
+    // No warp ever waits for another.
     auto flush = [&](int ga, int gb) {
       if (ga == 0 && gb == G) {
 #pragma unroll
@@ -220,14 +236,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (tok < M) __stcg(base + tok * RB + rin, acc[tt][nt][i]);
           }
       __threadfence();
-      ptx::named_sync(1, 32 * CONSUMERS);
-      if (cw == 0 && lane == 0) {
+      __syncwarp();
+      unsigned* cnt = counters + static_cast<long>(rb) * CONSUMERS + cw;
+      int last = 0;
+      if (lane == 0) {
         const unsigned add = static_cast<unsigned>(gb - ga);
-        const unsigned old = atomicAdd(counters + rb, add);
-        *s_last = (old + add == static_cast<unsigned>(G)) ? 1 : 0;
+        last = (atomicAdd(cnt, add) + add == static_cast<unsigned>(G)) ? 1 : 0;
       }
-      ptx::named_sync(1, 32 * CONSUMERS);
-      if (*s_last) {
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
         __threadfence();
         const long nslots = last_owner - first + 1;
 #pragma unroll
@@ -246,9 +263,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum);
               }
             }
-        if (cw == 0 && lane == 0) counters[rb] = 0u;
+        __syncwarp();
+        if (lane == 0) *cnt = 0u;
       }
-      ptx::named_sync(1, 32 * CONSUMERS);
     };
 
     for (int i = 0; i < n_units; ++i) {
@@ -270,18 +287,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // B fragments: bf[nt][j][0..1] for the 8 k16 steps of the group
       uint32_t bf[NT][8][2];
-      const uint32_t xb = ptx::smem_u32(st);
+      const uint32_t xb = smem_base + s * STAGE_BYTES;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j0 = 0; j0 < 8; j0 += 2) {
-          const int j = j0 + (mi >> 1);
-          const int row = 8 * nt + lrow;
-          const int chunk = 2 * (j & 3) + (mi & 1);
-          const uint32_t addr = xb + (j >> 2) * (XTILE_BYTES / 2) + row * 128 +
-                                ((chunk ^ (row & 7)) << 4);
-          ldmatrix_x4(addr, bf[nt][j0][0], bf[nt][j0][1], bf[nt][j0 + 1][0], bf[nt][j0 + 1][1]);
-        }
+        for (int q = 0; q < 4; ++q)
+          ldmatrix_x4(xb + bf_off[nt][q], bf[nt][2 * q][0], bf[nt][2 * q][1], bf[nt][2 * q + 1][0],
+                      bf[nt][2 * q + 1][1]);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[s]);
 
@@ -423,22 +435,21 @@ size_t gemv_packed_bytes(int64_t N, int64_t K) {
 
 // Bytes of the counter region at the start of the workspace.
 size_t gemv_counter_bytes(int64_t N) {
-  return (static_cast<size_t>((N + RB - 1) / RB) * 4 + 255) / 256 * 256;
+  return (static_cast<size_t>((N + RB - 1) / RB) * CONSUMERS * 4 + 255) / 256 * 256;
 }
 
-// Workspace: [RBn] counters (padded to 256 B), then partials [RBn][S][M][512] fp32.
+// Workspace: counters [RBn][16 warp slices] (padded to 256 B), then partials
+// [RBn][S][M][512] fp32.
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const GemvPlan p = make_plan(N, K, sm_count());
-  const size_t cnt = (static_cast<size_t>(p.RBn) * 4 + 255) / 256 * 256;
-  return cnt + static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(float);
+  return gemv_counter_bytes(N) + static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(float);
 }
 
 cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* xs, int64_t M,
                         int64_t N, int64_t K, uint16_t* y, void* ws, cudaStream_t st) {
   const GemvPlan p = make_plan(N, K, sm_count());
-  const size_t cnt = (static_cast<size_t>(p.RBn) * 4 + 255) / 256 * 256;
   unsigned int* counters = static_cast<unsigned int*>(ws);
-  float* partials = reinterpret_cast<float*>(static_cast<char*>(ws) + cnt);
+  float* partials = reinterpret_cast<float*>(static_cast<char*>(ws) + gemv_counter_bytes(N));
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   // the fp16 activations [M][K]; boxes of 64 k x 16 token rows
