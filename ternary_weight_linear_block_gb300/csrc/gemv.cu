@@ -92,6 +92,106 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+
+// A segment [ga, gb) of row block rb ends: write its partial sums.  A row block
+// finished by one CTA is written directly.  Otherwise each warp stores its 32
+// rows in this CTA's slot and bumps the arrival counter of (row block, warp
+// slice); the warp whose add completes all G groups sums the slots in fixed
+// order.  No warp ever waits for another.  Kept out of line: the hot loop must
+// not pay registers for this rarely taken path.
+template <int NT>
+__device__ __forceinline__ void flush_segment(const float (&acc)[TPW][NT][4], int ga, int gb, int rb,
+                                              int G, int U, int C, int S, int M, int N, int cw,
+                                              int lane, __nv_bfloat16* __restrict__ y,
+                                              unsigned int* __restrict__ counters,
+                                              float* __restrict__ partials) {
+  const int gq = lane >> 2, cq = lane & 3;
+  if (ga == 0 && gb == G) {
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = rb * RB + 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+          const int tok = 8 * nt + 2 * cq + (i & 1);
+          if (row < N && tok < M)
+            y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(acc[tt][nt][i]);
+        }
+    return;
+  }
+  const long first = owner_of(static_cast<long>(rb) * G, U, C);
+  const long last_owner = owner_of(static_cast<long>(rb) * G + G - 1, U, C);
+  const long slot = blockIdx.x - first;
+  float* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+        const int tok = 8 * nt + 2 * cq + (i & 1);
+        if (tok < M) __stcg(base + tok * RB + rin, acc[tt][nt][i]);
+      }
+  __threadfence();
+  __syncwarp();
+  unsigned* cnt = counters + static_cast<long>(rb) * CONSUMERS + cw;
+  int last = 0;
+  if (lane == 0) {
+    const unsigned add = static_cast<unsigned>(gb - ga);
+    last = (atomicAdd(cnt, add) + add == static_cast<unsigned>(G)) ? 1 : 0;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  const int nslots = static_cast<int>(last_owner - first + 1);
+  // all slots of a batch are loaded before any is added: one memory round
+  // trip per batch, and the adds keep their fixed slot order
+  constexpr int NV = TPW * NT * 4;
+  constexpr int SB = NT == 1 ? 4 : 2;
+  float sum[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) sum[v] = 0.f;
+  for (int sl0 = 0; sl0 < nslots; sl0 += SB) {
+    float part[SB][NV];
+#pragma unroll
+    for (int sb = 0; sb < SB; ++sb)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
+        const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+        const int tok = 8 * nt + 2 * cq + (i & 1);
+        part[sb][v] = (sl0 + sb < nslots && tok < M)
+                          ? __ldcg(partials + ((static_cast<long>(rb) * S + sl0 + sb) * M + tok) * RB + rin)
+                          : 0.f;
+      }
+#pragma unroll
+    for (int sb = 0; sb < SB; ++sb)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) sum[v] += part[sb][v];
+  }
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
+    const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+    const int row = rb * RB + rin;
+    const int tok = 8 * nt + 2 * cq + (i & 1);
+    if (tok < M && row < N) y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum[v]);
+  }
+  __syncwarp();
+  if (lane == 0) *cnt = 0u;
+}
+
+template <int NT>
+__device__ __noinline__ void flush_segment_ni(const float (&acc)[TPW][NT][4], int ga, int gb, int rb,
+                                              int G, int U, int C, int S, int M, int N, int cw,
+                                              int lane, __nv_bfloat16* __restrict__ y,
+                                              unsigned int* __restrict__ counters,
+                                              float* __restrict__ partials) {
+  flush_segment<NT>(acc, ga, gb, rb, G, U, C, S, M, N, cw, lane, y, counters, partials);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t* __restrict__ packed,
@@ -206,68 +306,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // CTA's slot and bumps the arrival counter of (row block, warp slice); the
     // warp whose add completes all G groups sums the slots in fixed order.
     // No warp ever waits for another.
-    auto flush = [&](int ga, int gb) {
-      if (ga == 0 && gb == G) {
-#pragma unroll
-        for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int row = rb * RB + 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
-              const int tok = 8 * nt + 2 * cq + (i & 1);
-              if (row < N && tok < M)
-                y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(acc[tt][nt][i]);
-            }
-        return;
-      }
-      const long first = owner_of(static_cast<long>(rb) * G, U, C);
-      const long last_owner = owner_of(static_cast<long>(rb) * G + G - 1, U, C);
-      const long slot = blockIdx.x - first;
-      float* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
-#pragma unroll
-      for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
-            const int tok = 8 * nt + 2 * cq + (i & 1);
-            if (tok < M) __stcg(base + tok * RB + rin, acc[tt][nt][i]);
-          }
-      __threadfence();
-      __syncwarp();
-      unsigned* cnt = counters + static_cast<long>(rb) * CONSUMERS + cw;
-      int last = 0;
-      if (lane == 0) {
-        const unsigned add = static_cast<unsigned>(gb - ga);
-        last = (atomicAdd(cnt, add) + add == static_cast<unsigned>(G)) ? 1 : 0;
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence();
-        const long nslots = last_owner - first + 1;
-#pragma unroll
-        for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
-              const int row = rb * RB + rin;
-              const int tok = 8 * nt + 2 * cq + (i & 1);
-              if (tok < M && row < N) {
-                float sum = 0.f;
-                for (long sl = 0; sl < nslots; ++sl)
-                  sum += __ldcg(partials + ((static_cast<long>(rb) * S + sl) * M + tok) * RB + rin);
-                y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum);
-              }
-            }
-        __syncwarp();
-        if (lane == 0) *cnt = 0u;
-      }
-    };
-
     for (int i = 0; i < n_units; ++i) {
       const int s = i % STAGES;
       const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
@@ -348,7 +386,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
       }
       if (seg_end) {
-        flush(seg_g0, g + 1);
+        flush_segment_ni<NT>(acc, seg_g0, g + 1, rb, G, U, C, S, M, N, cw, lane, y, counters, partials);
 #pragma unroll
         for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
