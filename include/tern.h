@@ -165,7 +165,8 @@ tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_
  *                           a workspace must not run concurrently.
  * Requirements: 1 <= M <= 16 (M == 0 is a no-op), K % 1024 == 0, K <= 65536.
  * Device-side waits are bounded; a wait that gives up makes the call's
- * outputs undefined and is reported by tern_check().
+ * outputs undefined and is reported by tern_check(); the workspace must then
+ * be zero-filled again (tern_workspace_init) before its next use.
  * ---------------------------------------------------------------------- */
 tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const float* xs,
                              int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
@@ -179,8 +180,8 @@ tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const fl
  * through its own pool, handing the layer only its inputs and outputs, cannot
  * give it a separate workspace, and a decode loop that must never stall
  * cannot call cudaMalloc, which may synchronise the device.  This call takes
- * no workspace and allocates nothing: its scratch (the per-row-block arrival
- * counters and partial sums) lives in a static device array of
+ * no workspace and allocates nothing: its scratch (the tagged partial sums
+ * of row blocks shared by several CTAs) lives in a static device array of
  * TERN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library holds until the process exits.
  *
@@ -189,9 +190,9 @@ tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const fl
  * exceeds TERN_NOALLOC_SCRATCH_BYTES (nothing is launched).  The first call
  * on a device, with that device current, looks up the array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture.  Every call shares the one array, which keeps the last
- * call's contents: each call clears the counters on its stream first, and
- * calls that overlap on the GPU race on the array.
+ * stream capture.  Every call shares the one array: each call zero-fills the
+ * part it uses on its stream first (so a call that gave up waiting leaves
+ * nothing behind), and calls that overlap on the GPU race on the array.
  * ---------------------------------------------------------------------- */
 #define TERN_NOALLOC_SCRATCH_BYTES (16u << 20)
 tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uint16_t* xh, const float* xs,

@@ -28,15 +28,19 @@
 //   fresh fp32 accumulators are scaled by the row's group scale, and per
 //   1024-block by the block's power-of-two activation factor.
 // * units are cut into equal contiguous ranges, one per persistent CTA
-//   (stream-K).  A 512-row block finished by one CTA is written directly;
-//   otherwise each contributing CTA stores its partial in a workspace slot
-//   and the last to arrive (atomic counter, no waiting) sums the slots in
-//   fixed order, writes bf16 y and resets the counter.
+//   (stream-K).  A 512-row block finished by one CTA is written directly.  A
+//   block shared by several CTAs is summed by its first owner, which in this
+//   order reaches the block last: the other owners publish their partial sums
+//   as tagged 64-bit words (no fence, no atomic), the first owner reads them
+//   in slot order, writes bf16 y and clears the tags.  Each warp's rows are
+//   independent, so the flags are per value and no warp waits for a CTA-wide
+//   event.  The segment's end runs outside the per-unit loop, which keeps the
+//   hot loop's registers for the hot loop.
 // * the weight copies do not depend on the previous kernel, so the producer
 //   issues the first ring of them before the programmatic launch wait, and
 //   every CTA lets the next kernel launch as soon as it starts.
-// All barrier waits are bounded; a wait that gives up sets an error word that
-// tern_check() reports.
+// All barrier and tag waits are bounded; a wait that gives up sets an error
+// word that tern_check() reports (the workspace must then be re-initialised).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -66,7 +70,7 @@ constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 +
 static_assert(XTILE_BYTES + UNIT_BYTES <= STAGE_BYTES, "stage too small");
 static_assert(STAGE_BYTES % 1024 == 0 && XTILE_BYTES % 16 == 0, "stage alignment");
 
-enum : unsigned int { ERR_PRODUCER = 1u, ERR_CONSUMER = 2u, ERR_DRAIN = 4u };
+enum : unsigned int { ERR_PRODUCER = 1u, ERR_CONSUMER = 2u, ERR_DRAIN = 4u, ERR_REDUCE = 8u };
 
 __host__ __device__ inline long unit_begin(long c, long U, long C) { return c * U / C; }
 __host__ __device__ inline long owner_of(long u, long U, long C) { return ((u + 1) * C - 1) / U; }
@@ -93,110 +97,125 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 }
 
 
-// A segment [ga, gb) of row block rb ends: write its partial sums.  A row block
-// finished by one CTA is written directly.  Otherwise each warp stores its 32
-// rows in this CTA's slot and bumps the arrival counter of (row block, warp
-// slice); the warp whose add completes all G groups sums the slots in fixed
-// order.  No warp ever waits for another.  Kept out of line: the hot loop must
-// not pay registers for this rarely taken path.
+__device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// A segment [ga, gb) of row block rb ends.  A row block finished by one CTA
+// is written directly.  Otherwise the first CTA owning part of the block sums
+// it: every other owner publishes its 32 rows per warp as tagged 64-bit words
+// (value | 1 << 32) in its slot, with no fence and no atomic (each word is
+// single-copy atomic, so a set tag vouches for the value beside it), and the
+// first owner, which in stream-K order finishes the block last, reads them,
+// adds them in slot order, writes y and clears the tags for the next call.
+// Out of line: the hot loop must not pay registers for this path.
 template <int NT>
-__device__ __forceinline__ void flush_segment(const float (&acc)[TPW][NT][4], int ga, int gb, int rb,
-                                              int G, int U, int C, int S, int M, int N, int cw,
-                                              int lane, __nv_bfloat16* __restrict__ y,
-                                              unsigned int* __restrict__ counters,
-                                              float* __restrict__ partials) {
+__device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int ga, int gb, int rb,
+                                         int G, int U, int C, int S, int M, int N, int cw,
+                                         int lane, __nv_bfloat16* __restrict__ y,
+                                         unsigned long long* __restrict__ partials,
+                                         volatile int* abort_flag) {
   const int gq = lane >> 2, cq = lane & 3;
+  constexpr int NV = TPW * NT * 4;
   if (ga == 0 && gb == G) {
 #pragma unroll
-    for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = rb * RB + 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
-          const int tok = 8 * nt + 2 * cq + (i & 1);
-          if (row < N && tok < M)
-            y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(acc[tt][nt][i]);
-        }
+    for (int v = 0; v < NV; ++v) {
+      const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
+      const int row = rb * RB + 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+      const int tok = 8 * nt + 2 * cq + (i & 1);
+      if (row < N && tok < M)
+        y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(acc[tt][nt][i]);
+    }
     return;
   }
   const long first = owner_of(static_cast<long>(rb) * G, U, C);
-  const long last_owner = owner_of(static_cast<long>(rb) * G + G - 1, U, C);
-  const long slot = blockIdx.x - first;
-  float* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
+  const int slot = static_cast<int>(blockIdx.x - first);
+  if (slot != 0) {
+    unsigned long long* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
 #pragma unroll
-  for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
-        const int tok = 8 * nt + 2 * cq + (i & 1);
-        if (tok < M) __stcg(base + tok * RB + rin, acc[tt][nt][i]);
-      }
-  __threadfence();
-  __syncwarp();
-  unsigned* cnt = counters + static_cast<long>(rb) * CONSUMERS + cw;
-  int last = 0;
-  if (lane == 0) {
-    const unsigned add = static_cast<unsigned>(gb - ga);
-    last = (atomicAdd(cnt, add) + add == static_cast<unsigned>(G)) ? 1 : 0;
+    for (int v = 0; v < NV; ++v) {
+      const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
+      const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+      const int tok = 8 * nt + 2 * cq + (i & 1);
+      if (tok < M)
+        st_tagged(base + tok * RB + rin,
+                  (1ull << 32) | __float_as_uint(acc[tt][nt][i]));
+    }
+    return;
   }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
-  const int nslots = static_cast<int>(last_owner - first + 1);
-  // all slots of a batch are loaded before any is added: one memory round
-  // trip per batch, and the adds keep their fixed slot order
-  constexpr int NV = TPW * NT * 4;
-  constexpr int SB = NT == 1 ? 4 : 2;
+  const int nslots = static_cast<int>(owner_of(static_cast<long>(rb) * G + G - 1, U, C) - first + 1);
   float sum[NV];
 #pragma unroll
-  for (int v = 0; v < NV; ++v) sum[v] = 0.f;
-  for (int sl0 = 0; sl0 < nslots; sl0 += SB) {
-    float part[SB][NV];
+  for (int v = 0; v < NV; ++v) sum[v] = acc[v / (NT * 4)][(v / 4) % NT][v % 4];
+  // the other slots in order: all words of a slot are loaded before any is
+  // checked, so a slot published long ago costs one memory round trip; a slot
+  // not yet complete is retried (bounded)
+  constexpr int SB = 1;
+  bool ok = true;
+  for (int sl0 = 1; sl0 < nslots && ok; sl0 += SB) {
+    unsigned long long w[SB][NV];
+    for (uint32_t tries = 0;; ++tries) {
+      bool ready = true;
 #pragma unroll
-    for (int sb = 0; sb < SB; ++sb)
+      for (int sb = 0; sb < SB; ++sb) {
+        const unsigned long long* base =
+            partials + (static_cast<long>(rb) * S + sl0 + sb) * M * RB;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
+          const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+          const int tok = 8 * nt + 2 * cq + (i & 1);
+          w[sb][v] = (sl0 + sb < nslots && tok < M) ? ld_tagged(base + tok * RB + rin) : (1ull << 32);
+        }
+      }
+#pragma unroll
+      for (int sb = 0; sb < SB; ++sb)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) ready = ready && (w[sb][v] >> 32) == 1ull;
+      if (__all_sync(0xffffffffu, ready)) break;
+      if (tries >= (WAIT_LIMIT >> 10) || *abort_flag) {
+        if (lane == 0) fail(abort_flag, ERR_REDUCE);
+        ok = false;
+        break;
+      }
+      __nanosleep(200);
+    }
+    if (!ok) break;
+#pragma unroll
+    for (int sb = 0; sb < SB; ++sb) {
+#pragma unroll
+      for (int v = 0; v < NV; ++v) sum[v] += __uint_as_float(static_cast<unsigned int>(w[sb][v]));
+      if (sl0 + sb >= nslots) continue;
+      unsigned long long* base = partials + (static_cast<long>(rb) * S + sl0 + sb) * M * RB;
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
         const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
         const int tok = 8 * nt + 2 * cq + (i & 1);
-        part[sb][v] = (sl0 + sb < nslots && tok < M)
-                          ? __ldcg(partials + ((static_cast<long>(rb) * S + sl0 + sb) * M + tok) * RB + rin)
-                          : 0.f;
+        if (tok < M) st_tagged(base + tok * RB + rin, 0ull);
       }
-#pragma unroll
-    for (int sb = 0; sb < SB; ++sb)
-#pragma unroll
-      for (int v = 0; v < NV; ++v) sum[v] += part[sb][v];
+    }
   }
+  if (!ok) return;
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
-    const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
-    const int row = rb * RB + rin;
+    const int row = rb * RB + 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
     const int tok = 8 * nt + 2 * cq + (i & 1);
-    if (tok < M && row < N) y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum[v]);
+    if (row < N && tok < M) y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum[v]);
   }
-  __syncwarp();
-  if (lane == 0) *cnt = 0u;
-}
-
-template <int NT>
-__device__ __noinline__ void flush_segment_ni(const float (&acc)[TPW][NT][4], int ga, int gb, int rb,
-                                              int G, int U, int C, int S, int M, int N, int cw,
-                                              int lane, __nv_bfloat16* __restrict__ y,
-                                              unsigned int* __restrict__ counters,
-                                              float* __restrict__ partials) {
-  flush_segment<NT>(acc, ga, gb, rb, G, U, C, S, M, N, cw, lane, y, counters, partials);
 }
 
 template <int NT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t* __restrict__ packed,
                 const float* __restrict__ xs, int M, int N, int K, __nv_bfloat16* __restrict__ y,
-                unsigned int* __restrict__ counters, float* __restrict__ partials, int U, int S) {
+                unsigned long long* __restrict__ partials, int U, int S) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -301,104 +320,105 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     int rb = u0 / G, g = u0 % G, seg_g0 = g;
 
-    // A segment of a row block ends here.  A row block finished by this CTA
-    // is written directly.  Otherwise each warp stores its 32 rows in this
-    // CTA's slot and bumps the arrival counter of (row block, warp slice); the
-    // warp whose add completes all G groups sums the slots in fixed order.
-    // No warp ever waits for another.
-    for (int i = 0; i < n_units; ++i) {
-      const int s = i % STAGES;
-      const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
-      if (!ptx::mbar_wait(&full[s], ph, abort_flag, WAIT_LIMIT)) {
-        if (!*abort_flag) fail(abort_flag, ERR_CONSUMER);
-        break;
-      }
-      const uint8_t* st = smem + s * STAGE_BYTES;
-      const uint8_t* unit = st + XTILE_BYTES;
-      uint4 cv[TPW];
-      uint32_t sp[TPW];
+    // The CTA's units form segments, one per row block they touch; the hot
+    // loop runs over the units of one segment and the segment's end (direct
+    // write, publication or reduction) happens outside it.
+    bool alive = true;
+    for (int i = 0; alive && i < n_units;) {
+      const int seg_len = (n_units - i < G - g) ? n_units - i : G - g;
+      const int i_end = i + seg_len;
+      for (; i < i_end; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
+        if (!ptx::mbar_wait(&full[s], ph, abort_flag, WAIT_LIMIT)) {
+          if (!*abort_flag) fail(abort_flag, ERR_CONSUMER);
+          alive = false;
+          break;
+        }
+        const uint8_t* st = smem + s * STAGE_BYTES;
+        const uint8_t* unit = st + XTILE_BYTES;
+        uint4 cv[TPW];
+        uint32_t sp[TPW];
 #pragma unroll
-      for (int tt = 0; tt < TPW; ++tt) {
-        cv[tt] = *reinterpret_cast<const uint4*>(unit + 512 * (TPW * cw + tt) + 16 * lane);
-        sp[tt] = *reinterpret_cast<const uint32_t*>(unit + UNIT_CODE_BYTES + 32 * (TPW * cw + tt) +
-                                                    4 * gq);
-      }
-      // B fragments: bf[nt][j][0..1] for the 8 k16 steps of the group
-      uint32_t bf[NT][8][2];
-      const uint32_t xb = smem_base + s * STAGE_BYTES;
+        for (int tt = 0; tt < TPW; ++tt) {
+          cv[tt] = *reinterpret_cast<const uint4*>(unit + 512 * (TPW * cw + tt) + 16 * lane);
+          sp[tt] = *reinterpret_cast<const uint32_t*>(unit + UNIT_CODE_BYTES + 32 * (TPW * cw + tt) +
+                                                      4 * gq);
+        }
+        // B fragments: bf[nt][j][0..1] for the 8 k16 steps of the group
+        uint32_t bf[NT][8][2];
+        const uint32_t xb = smem_base + s * STAGE_BYTES;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          ldmatrix_x4(xb + bf_off[nt][q], bf[nt][2 * q][0], bf[nt][2 * q][1], bf[nt][2 * q + 1][0],
-                      bf[nt][2 * q + 1][1]);
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&empty[s]);
+          for (int q = 0; q < 4; ++q)
+            ldmatrix_x4(xb + bf_off[nt][q], bf[nt][2 * q][0], bf[nt][2 * q][1], bf[nt][2 * q + 1][0],
+                        bf[nt][2 * q + 1][1]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&empty[s]);
 
 #pragma unroll
-      for (int tt = 0; tt < TPW; ++tt) {
-        float d[NT][4];
+        for (int tt = 0; tt < TPW; ++tt) {
+          float d[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) d[nt][q] = 0.f;
-        const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
+            for (int q = 0; q < 4; ++q) d[nt][q] = 0.f;
+          const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t w = w4[j >> 1];
-          const int e0 = (j & 1) * 4;
-          uint32_t a[4];
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t w = w4[j >> 1];
+            const int e0 = (j & 1) * 4;
+            uint32_t a[4];
 #pragma unroll
-          for (int p = 0; p < 4; ++p) a[p] = (w << (14 - 2 * (e0 + p))) & 0xC000C000u;
+            for (int p = 0; p < 4; ++p) a[p] = (w << (14 - 2 * (e0 + p))) & 0xC000C000u;
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
-        }
-        __half2 s2h = *reinterpret_cast<__half2*>(&sp[tt]);
-        const float2 s2 = __half22float2(s2h);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          bacc[tt][nt][0] = fmaf(d[nt][0], s2.x, bacc[tt][nt][0]);
-          bacc[tt][nt][1] = fmaf(d[nt][1], s2.x, bacc[tt][nt][1]);
-          bacc[tt][nt][2] = fmaf(d[nt][2], s2.y, bacc[tt][nt][2]);
-          bacc[tt][nt][3] = fmaf(d[nt][3], s2.y, bacc[tt][nt][3]);
-        }
-      }
-      const bool seg_end = (i + 1 == n_units) || (g + 1 == G);
-      if (((g & 7) == 7) || seg_end) {
-        const int blk = g >> 3;
-        float f[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int tok = 8 * nt + 2 * cq + h;
-            // 1/2 undoes the 2*code reading of the weights
-            f[nt][h] = tok < M ? 0.5f * __ldg(xs + static_cast<long>(tok) * B + blk) : 0.f;
+            for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
           }
+          __half2 s2h = *reinterpret_cast<__half2*>(&sp[tt]);
+          const float2 s2 = __half22float2(s2h);
 #pragma unroll
-        for (int tt = 0; tt < TPW; ++tt)
+          for (int nt = 0; nt < NT; ++nt) {
+            bacc[tt][nt][0] = fmaf(d[nt][0], s2.x, bacc[tt][nt][0]);
+            bacc[tt][nt][1] = fmaf(d[nt][1], s2.x, bacc[tt][nt][1]);
+            bacc[tt][nt][2] = fmaf(d[nt][2], s2.y, bacc[tt][nt][2]);
+            bacc[tt][nt][3] = fmaf(d[nt][3], s2.y, bacc[tt][nt][3]);
+          }
+        }
+        if ((g & 7) == 7 || i + 1 == i_end) {
+          const int blk = g >> 3;
+          float f[NT][2];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              acc[tt][nt][q] = fmaf(bacc[tt][nt][q], f[nt][q & 1], acc[tt][nt][q]);
-              bacc[tt][nt][q] = 0.f;
+            for (int h = 0; h < 2; ++h) {
+              const int tok = 8 * nt + 2 * cq + h;
+              // 1/2 undoes the 2*code reading of the weights
+              f[nt][h] = tok < M ? 0.5f * __ldg(xs + static_cast<long>(tok) * B + blk) : 0.f;
             }
-      }
-      if (seg_end) {
-        flush_segment_ni<NT>(acc, seg_g0, g + 1, rb, G, U, C, S, M, N, cw, lane, y, counters, partials);
 #pragma unroll
-        for (int tt = 0; tt < TPW; ++tt)
+          for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[tt][nt][q] = 0.f;
-        seg_g0 = 0;
+              for (int q = 0; q < 4; ++q) {
+                acc[tt][nt][q] = fmaf(bacc[tt][nt][q], f[nt][q & 1], acc[tt][nt][q]);
+                bacc[tt][nt][q] = 0.f;
+              }
+        }
+        ++g;
       }
-      if (++g == G) {
-        g = 0;
-        ++rb;
-      }
+      if (!alive) break;
+      end_segment<NT>(acc, seg_g0, g, rb, G, U, C, S, M, N, cw, lane, y, partials, abort_flag);
+#pragma unroll
+      for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[tt][nt][q] = 0.f;
+      seg_g0 = 0;
+      g = 0;
+      ++rb;
     }
     __syncwarp();
   }
@@ -451,7 +471,7 @@ EncodeTiledFn encode_fn() {
 
 template <int NT>
 cudaError_t launch_nt(const CUtensorMap& tm, const uint8_t* packed, const float* xs, int M, int N,
-                      int K, __nv_bfloat16* y, unsigned int* counters, float* partials,
+                      int K, __nv_bfloat16* y, unsigned long long* partials,
                       const GemvPlan& p, cudaStream_t st) {
   static bool attr_done = false;
   if (!attr_done) {
@@ -462,7 +482,7 @@ cudaError_t launch_nt(const CUtensorMap& tm, const uint8_t* packed, const float*
     attr_done = true;
   }
   return launch(gemv_kernel<NT>, dim3(p.C), dim3(NUM_THREADS), SMEM_BYTES, st, tm, packed, xs, M,
-                N, K, y, counters, partials, p.U, p.S);
+                N, K, y, partials, p.U, p.S);
 }
 
 }  // namespace
@@ -471,23 +491,17 @@ size_t gemv_packed_bytes(int64_t N, int64_t K) {
   return static_cast<size_t>((N + RB - 1) / RB) * static_cast<size_t>(K / kGroup) * UNIT_BYTES;
 }
 
-// Bytes of the counter region at the start of the workspace.
-size_t gemv_counter_bytes(int64_t N) {
-  return (static_cast<size_t>((N + RB - 1) / RB) * CONSUMERS * 4 + 255) / 256 * 256;
-}
-
-// Workspace: counters [RBn][16 warp slices] (padded to 256 B), then partials
-// [RBn][S][M][512] fp32.
+// Workspace: tagged partial sums [RBn][S][M][512] (64-bit words, zero when
+// idle: every call leaves the tags it set cleared).
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const GemvPlan p = make_plan(N, K, sm_count());
-  return gemv_counter_bytes(N) + static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(float);
+  return static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(unsigned long long);
 }
 
 cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* xs, int64_t M,
                         int64_t N, int64_t K, uint16_t* y, void* ws, cudaStream_t st) {
   const GemvPlan p = make_plan(N, K, sm_count());
-  unsigned int* counters = static_cast<unsigned int*>(ws);
-  float* partials = reinterpret_cast<float*>(static_cast<char*>(ws) + gemv_counter_bytes(N));
+  auto* partials = static_cast<unsigned long long*>(ws);
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   // the fp16 activations [M][K]; boxes of 64 k x 16 token rows
@@ -502,8 +516,8 @@ cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* 
     return cudaErrorInvalidValue;
   auto* yy = reinterpret_cast<__nv_bfloat16*>(y);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  if (M <= 8) return launch_nt<1>(tm, packed, xs, m, n, k, yy, counters, partials, p, st);
-  return launch_nt<2>(tm, packed, xs, m, n, k, yy, counters, partials, p, st);
+  if (M <= 8) return launch_nt<1>(tm, packed, xs, m, n, k, yy, partials, p, st);
+  return launch_nt<2>(tm, packed, xs, m, n, k, yy, partials, p, st);
 }
 
 cudaError_t gemv_read_clear_error(unsigned int* err) {

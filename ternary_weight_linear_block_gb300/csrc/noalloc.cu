@@ -6,16 +6,17 @@
 // output buffers) cannot let the library take a separate workspace, and a
 // decode loop that must never stall cannot call cudaMalloc, which may
 // synchronise the whole device.  This entry point allocates nothing: the
-// GEMV's per-row-block arrival counters and partial sums live in
+// GEMV's tagged partial sums (row blocks shared by several CTAs) live in
 // g_noalloc_scratch, a static device array of TERN_NOALLOC_SCRATCH_BYTES that
 // every GPU loading the library keeps until the process exits.
 //
 // The first call on a device (with that device current) looks up the array's
 // device address with cudaGetSymbolAddress and caches it per device; that
 // first call should come before any stream capture.  All calls share the one
-// array and it keeps the last call's contents, so each call clears the
-// counter region on its stream before the kernel; calls that overlap on the
-// GPU (for example on two streams) race on the array.
+// array and it keeps the last call's contents, so each call zero-fills the
+// part it uses on its stream before the kernel (a call that gave up waiting
+// may have left tags set); calls that overlap on the GPU (for example on two
+// streams) race on the array.
 #include "tern_internal.cuh"
 
 namespace tern {
@@ -70,7 +71,8 @@ extern "C" tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uin
   void* scratch = nullptr;
   if (scratch_address(dev, &scratch) != cudaSuccess) return TERN_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, gemv_counter_bytes(N), st) != cudaSuccess) return TERN_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, gemv_workspace_bytes(M, N, K), st) != cudaSuccess)
+    return TERN_ERR_CUDA;
   return launch_gemv(packed, xh, xs, M, N, K, y, scratch, st) == cudaSuccess ? TERN_OK
                                                                            : TERN_ERR_CUDA;
 }

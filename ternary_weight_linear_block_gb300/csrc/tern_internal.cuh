@@ -47,7 +47,6 @@ cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, 
                         cudaStream_t st);
 size_t gemv_packed_bytes(int64_t N, int64_t K);
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
-size_t gemv_counter_bytes(int64_t N);
 cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* xs, int64_t M,
                         int64_t N, int64_t K, uint16_t* y, void* ws, cudaStream_t st);
 cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
