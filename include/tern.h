@@ -173,6 +173,28 @@ tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const fl
                              size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * tern_linear_decode -- the layer's whole decode path in one launch:
+ *     y = tern_gemv_decode(tern_fwht_quant(x, sign, TERN_FWHT_DECODE))
+ * Page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2", section "前提"
+ * (input-side block rotation, then the ternary g128 product).  The rotation
+ * is folded into the GEMV's prologue: each CTA rotates only the 1024-blocks
+ * its share of the weights needs and keeps the fp16 operand on chip, so the
+ * separate rotation launch and its [M][K] round trip through memory go away.
+ * The result is bit-identical to the two calls.
+ *
+ *   x                       bf16 [M][K], 16-byte aligned
+ *   sign                    optional +-1 per k (NULL = identity), as for
+ *                           tern_fwht_quant; any alignment
+ *   packed, M, N, K, y, ws, ws_bytes, stream: as for tern_gemv_decode (the
+ *                           workspace size is tern_workspace_bytes(
+ *                           TERN_OP_GEMV, M, N, K))
+ * Requirements and errors as for tern_gemv_decode.
+ * ---------------------------------------------------------------------- */
+tern_status tern_linear_decode(const uint16_t* x, const int8_t* sign, const uint8_t* packed,
+                               int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * tern_gemv_decode_noalloc -- the same decode GEMV as tern_gemv_decode, for
  * callers that cannot allocate device memory.  The page has no counterpart.
  *

@@ -49,6 +49,7 @@ _SIGS = {
                                               _p]),
     "tern_check": (ctypes.c_int, [_p]),
     "tern_gemv_decode_noalloc": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
+    "tern_linear_decode": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
 }
 
 _lib = None
@@ -154,6 +155,11 @@ def tern_check(stream=None):
     return _call("tern_check", _stream(stream))
 
 
+def tern_linear_decode(x, sign, packed, m, n, k, y, ws, ws_bytes, stream=None):
+    return _call("tern_linear_decode", _ptr(x), _ptr(sign), _ptr(packed), m, n, k, _ptr(y),
+                 _ptr(ws), ws_bytes, _stream(stream))
+
+
 def tern_gemv_decode_noalloc(packed, xh, xs, m, n, k, y, stream=None):
     """Decode GEMV with the library's fixed scratch array (no workspace, no
     allocation), for callers that cannot allocate device memory."""
@@ -234,14 +240,20 @@ class Workspace:
 
 
 def decode(layer: PackedLayer, x: torch.Tensor, ws: Workspace, y: torch.Tensor | None = None,
-           sign=None, stream=None) -> torch.Tensor:
-    """Decode forward for M <= 16 bf16 tokens: rotation, then the GEMV."""
+           sign=None, stream=None, fused: bool = False) -> torch.Tensor:
+    """Decode forward for M <= 16 bf16 tokens: rotation, then the GEMV (the
+    two calls, or one launch of tern_linear_decode with ``fused=True``; the
+    results agree bit for bit)."""
     m = x.shape[0]
-    xh, xs = fwht(x, TERN_FWHT_DECODE, sign, stream)
+    _need(x, torch.bfloat16, "x")
     if y is None:
         y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=x.device)
     nb = tern_workspace_bytes(TERN_OP_GEMV, m, layer.n, layer.k)
     buf = ws.get(nb, stream)
+    if fused:
+        tern_linear_decode(x, sign, layer.packed, m, layer.n, layer.k, y, buf, buf.numel(), stream)
+        return y
+    xh, xs = fwht(x, TERN_FWHT_DECODE, sign, stream)
     tern_gemv_decode(layer.packed, xh, xs, m, layer.n, layer.k, y, buf, buf.numel(), stream)
     return y
 

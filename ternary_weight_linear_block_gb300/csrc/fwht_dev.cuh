@@ -1,0 +1,133 @@
+// Device routines of the block Hadamard rotation, shared by the rotation
+// kernels (fwht.cu) and the fused rotate + decode GEMV (gemv.cu), so that both
+// produce bit-identical operands.
+//
+// Page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2": section "前提"
+// (block-wise Hadamard rotation on the input side) and section 1 (Sylvester
+// structure, split identity H1024[a;b] = [H512 a + H512 b ; H512 a - H512 b]
+// as the last butterfly stage).
+//
+// One warp transforms one 1024-block of one token.  Lane l holds the 32
+// elements with index  ih*256 + l*8 + il  (ih = 0..3, il = 0..7): index bits
+// 0-2 are the register index il, bits 3-7 the lane, bits 8-9 the register
+// index ih.  Stage s (stride 2^s) therefore runs inside a thread for
+// s = 0,1,2,8,9 and across lanes (shuffle xor 2^(s-3)) for s = 3..7.  The
+// stages run in the order s = 0..9 so the fp32 rounding is that of the
+// canonical transform with the stride-512 split identity last.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace tern {
+namespace fwht {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ void load_block(const uint16_t* __restrict__ xb,
+                                           const int8_t* __restrict__ sb, int lane,
+                                           float (&v)[4][8]) {
+#pragma unroll
+  for (int ih = 0; ih < 4; ++ih) {
+    uint4 raw = __ldg(reinterpret_cast<const uint4*>(xb + ih * 256 + lane * 8));
+    uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[ih][2 * q] = __uint_as_float(w[q] << 16);           // bf16 -> fp32 is exact
+      v[ih][2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+    }
+    if (sb != nullptr) {
+#pragma unroll
+      for (int il = 0; il < 8; ++il) {
+        float s = static_cast<float>(__ldg(sb + ih * 256 + lane * 8 + il));
+        v[ih][il] = v[ih][il] * s;
+      }
+    }
+  }
+}
+
+// In-register butterfly between registers a (lower index) and b.
+__device__ __forceinline__ void bfly(float& a, float& b) {
+  float s = __fadd_rn(a, b);
+  float d = __fsub_rn(a, b);
+  a = s;
+  b = d;
+}
+
+__device__ __forceinline__ void fwht_1024(float (&v)[4][8], int lane) {
+  // stages 0, 1, 2: within the 8 registers of one ih
+#pragma unroll
+  for (int s = 0; s < 3; ++s) {
+    const int h = 1 << s;
+#pragma unroll
+    for (int ih = 0; ih < 4; ++ih)
+#pragma unroll
+      for (int il = 0; il < 8; ++il)
+        if ((il & h) == 0) bfly(v[ih][il], v[ih][il + h]);
+  }
+  // stages 3..7: across lanes
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int lm = 1 << s;
+    const bool upper = (lane & lm) != 0;
+#pragma unroll
+    for (int ih = 0; ih < 4; ++ih)
+#pragma unroll
+      for (int il = 0; il < 8; ++il) {
+        float p = __shfl_xor_sync(kFull, v[ih][il], lm);
+        // lower lane: u + v (own + partner); upper lane: u - v (partner - own)
+        v[ih][il] = upper ? __fsub_rn(p, v[ih][il]) : __fadd_rn(v[ih][il], p);
+      }
+  }
+  // stages 8, 9: across the 4 register groups
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int h = 1 << s;
+#pragma unroll
+    for (int ih = 0; ih < 4; ++ih)
+      if ((ih & h) == 0)
+#pragma unroll
+        for (int il = 0; il < 8; ++il) bfly(v[ih][il], v[ih + h][il]);
+  }
+#pragma unroll
+  for (int ih = 0; ih < 4; ++ih)
+#pragma unroll
+    for (int il = 0; il < 8; ++il) v[ih][il] = __fmul_rn(v[ih][il], 0.03125f);
+}
+
+__device__ __forceinline__ float warp_max(float a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFull, a, o));
+  return a;
+}
+
+
+// Decode operand of one rotated block: the power-of-two factor F with
+// max|xr * F| in [2^14, 2^15) (F = 2^min(14 - E, 126), E the exponent of the
+// block's absmax), returned with its exact inverse; xr * F rounds to fp16.
+__device__ __forceinline__ void decode_factor(const float (&v)[4][8], float& f, float& finv) {
+  float amax = 0.f;
+#pragma unroll
+  for (int ih = 0; ih < 4; ++ih)
+#pragma unroll
+    for (int il = 0; il < 8; ++il) amax = fmaxf(amax, fabsf(v[ih][il]));
+  amax = warp_max(amax);
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+  const int sh = min(14 - e, 126);                 // >= -114, so 2^sh is a normal float
+  f = __uint_as_float(static_cast<uint32_t>(sh + 127) << 23);
+  finv = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+}
+
+// fp16 (xr * F) of the 8 elements ih*256 + lane*8 + 0..7, packed as a uint4.
+__device__ __forceinline__ uint4 decode_pack8(const float (&v)[4][8], int ih, float f) {
+  uint32_t w[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    __half2 h2 = __floats2half2_rn(__fmul_rn(v[ih][2 * t], f), __fmul_rn(v[ih][2 * t + 1], f));
+    w[t] = *reinterpret_cast<uint32_t*>(&h2);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+}  // namespace fwht
+}  // namespace tern

@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "fwht_dev.cuh"
 #include "sm100_ptx.cuh"
 #include "tern_internal.cuh"
 
@@ -211,6 +212,59 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
   }
 }
 
+// The MMAs of one unit for this warp's tiles: codes cv, scale pairs sp and the
+// B fragments bf of the group's 8 k16 steps; the group sums, scaled by the
+// rows' group scales, are added to bacc.
+template <int NT>
+__device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t (&sp)[TPW],
+                                          const uint32_t (&bf)[NT][8][2],
+                                          float (&bacc)[TPW][NT][4]) {
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt) {
+    float d[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d[nt][q] = 0.f;
+    const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t w = w4[j >> 1];
+      const int e0 = (j & 1) * 4;
+      uint32_t a[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) a[p] = (w << (14 - 2 * (e0 + p))) & 0xC000C000u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
+    }
+    uint32_t spv = sp[tt];
+    const float2 s2 = __half22float2(*reinterpret_cast<__half2*>(&spv));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      bacc[tt][nt][0] = fmaf(d[nt][0], s2.x, bacc[tt][nt][0]);
+      bacc[tt][nt][1] = fmaf(d[nt][1], s2.x, bacc[tt][nt][1]);
+      bacc[tt][nt][2] = fmaf(d[nt][2], s2.y, bacc[tt][nt][2]);
+      bacc[tt][nt][3] = fmaf(d[nt][3], s2.y, bacc[tt][nt][3]);
+    }
+  }
+}
+
+// End of a 1024-block: acc += bacc * f (f the block's activation factor of
+// the thread's two tokens per n8 tile, times 1/2 for the 2 code reading).
+template <int NT>
+__device__ __forceinline__ void fold_block(float (&acc)[TPW][NT][4], float (&bacc)[TPW][NT][4],
+                                           const float (&f)[NT][2]) {
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[tt][nt][q] = fmaf(bacc[tt][nt][q], f[nt][q & 1], acc[tt][nt][q]);
+        bacc[tt][nt][q] = 0.f;
+      }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t* __restrict__ packed,
@@ -356,35 +410,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         bf[nt][2 * q + 1][1]);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[s]);
-
-#pragma unroll
-        for (int tt = 0; tt < TPW; ++tt) {
-          float d[NT][4];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) d[nt][q] = 0.f;
-          const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t w = w4[j >> 1];
-            const int e0 = (j & 1) * 4;
-            uint32_t a[4];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) a[p] = (w << (14 - 2 * (e0 + p))) & 0xC000C000u;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
-          }
-          __half2 s2h = *reinterpret_cast<__half2*>(&sp[tt]);
-          const float2 s2 = __half22float2(s2h);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            bacc[tt][nt][0] = fmaf(d[nt][0], s2.x, bacc[tt][nt][0]);
-            bacc[tt][nt][1] = fmaf(d[nt][1], s2.x, bacc[tt][nt][1]);
-            bacc[tt][nt][2] = fmaf(d[nt][2], s2.y, bacc[tt][nt][2]);
-            bacc[tt][nt][3] = fmaf(d[nt][3], s2.y, bacc[tt][nt][3]);
-          }
-        }
+        unit_math<NT>(cv, sp, bf, bacc);
         if ((g & 7) == 7 || i + 1 == i_end) {
           const int blk = g >> 3;
           float f[NT][2];
@@ -396,15 +422,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               // 1/2 undoes the 2*code reading of the weights
               f[nt][h] = tok < M ? 0.5f * __ldg(xs + static_cast<long>(tok) * B + blk) : 0.f;
             }
-#pragma unroll
-          for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                acc[tt][nt][q] = fmaf(bacc[tt][nt][q], f[nt][q & 1], acc[tt][nt][q]);
-                bacc[tt][nt][q] = 0.f;
-              }
+          fold_block<NT>(acc, bacc, f);
         }
         ++g;
       }
@@ -420,6 +438,241 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       g = 0;
       ++rb;
     }
+    __syncwarp();
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Fused decode linear: rotation + quantisation to the decode operand + GEMV in
+// one launch (the layer's decode path with tern_fwht_quant folded into the
+// GEMV prologue).  Each CTA rotates only the 1024-blocks its units touch, from
+// the bf16 input, with the same butterflies and scaling as the rotation
+// kernel (fwht_dev.cuh), and keeps the resulting fp16 operand of its groups
+// resident in shared memory (token rows padded by 16 bytes so ldmatrix reads
+// hit distinct banks); the pipeline ring then carries weight units only.  A
+// CTA whose groups do not fit the resident area processes them in chunks and
+// rotates again for each chunk.  Results are bit-identical to
+// tern_fwht_quant(TERN_FWHT_DECODE) followed by tern_gemv_decode.
+constexpr int LSTAGES = 8;
+constexpr int LX_BYTES = 80 * 1024;             // resident decode operand (a chunk of groups)
+constexpr int LXS_FLOATS = 16 * 64;             // block factors of 16 tokens x 64 blocks
+constexpr size_t LSMEM_BYTES = static_cast<size_t>(LSTAGES) * UNIT_BYTES + LX_BYTES +
+                               LXS_FLOATS * 4 + 1024 + 256;
+static_assert(LSMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+// Groups of one chunk: each 256 bytes per token row.
+__host__ __device__ inline int chunk_groups(int M, int G) {
+  const int cu = (LX_BYTES / M - 16) / 256;
+  return cu < G ? cu : G;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    linear_kernel(const uint16_t* __restrict__ x, const int8_t* __restrict__ sign,
+                  const uint8_t* __restrict__ packed, int M, int N, int K,
+                  __nv_bfloat16* __restrict__ y, unsigned long long* __restrict__ partials, int U,
+                  int S) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* xreg = smem + LSTAGES * UNIT_BYTES;
+  float* xs_s = reinterpret_cast<float*>(xreg + LX_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(xs_s + LXS_FLOATS);
+  uint64_t* empty = full + LSTAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + LSTAGES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = K / kGroup;
+  const int B = K / kHBlock;
+  const int C = gridDim.x;
+  const int u0 = static_cast<int>(unit_begin(blockIdx.x, U, C));
+  const int u1 = static_cast<int>(unit_begin(blockIdx.x + 1, U, C));
+  const int n_units = u1 - u0;
+  const int CU = chunk_groups(M, G);
+  const int pitch = CU * 256 + 16;               // bytes per token row of the resident operand
+
+  pdl_launch_dependents();   // the next kernel may start its own independent prologue
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < LSTAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], CONSUMERS);
+    }
+    *abort_flag = 0;
+    ptx::mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ producer: weights only,
+      // which do not depend on the previous kernel
+      const uint64_t pol = ptx::l2_policy_evict_first();
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < n_units; ++i) {
+        const int s = i % LSTAGES;
+        if (i >= LSTAGES) {
+          const uint32_t ph = static_cast<uint32_t>(i / LSTAGES) & 1u;
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, WAIT_LIMIT)) {
+            if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
+            ok = false;
+            break;
+          }
+        }
+        ptx::mbar_arrive_expect_tx(&full[s], UNIT_BYTES);
+        ptx::bulk_load_hint(smem + s * UNIT_BYTES, packed + static_cast<size_t>(u0 + i) * UNIT_BYTES,
+                            UNIT_BYTES, &full[s], pol);
+        ++issued;
+      }
+      if (!ok) {
+        // let every copy still in flight land before the CTA exits
+        for (int i = issued - 1; i >= 0 && i >= issued - LSTAGES; --i) {
+          const uint32_t ph = static_cast<uint32_t>(i / LSTAGES) & 1u;
+          if (!ptx::mbar_wait_bounded(&full[i % LSTAGES], ph, WAIT_LIMIT))
+            atomicOr(&g_gemv_error, ERR_DRAIN);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ consumers
+    const int cw = warp - 1;          // owns tiles TPW*cw .. TPW*cw + TPW-1 of each unit
+    const int gq = lane >> 2, cq = lane & 3;
+    pdl_wait();   // x is written by the previous kernel; y / ws may still be read by it
+
+    // ldmatrix: matrix mi = lane / 8 covers (k16 step 2q + mi / 2, 8-wide k
+    // half mi % 2) of token row 8 nt + lane % 8; rows >= M read row 0 (their
+    // products land in output columns that are never stored).
+    const int mi = lane >> 3;
+    uint32_t bf_off[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int tok = 8 * nt + (lane & 7);
+      bf_off[nt] = (tok < M ? tok : 0) * pitch + 32 * (mi >> 1) + 16 * (mi & 1);
+    }
+    const uint32_t smem_base = ptx::smem_u32(smem);
+    const uint32_t x_base = ptx::smem_u32(xreg);
+
+    // Rotate the 1024-blocks holding the groups gs .. gs + ng - 1 (mod G) and
+    // store those groups' decode operand at positions 0 .. ng - 1, and the
+    // blocks' factors (x 1/2 for the 2 code reading) in xs_s[token][block].
+    auto build = [&](int gs, int ng) {
+      for (int t = cw; t < M * B; t += CONSUMERS) {
+        const int m = t / B, b = t - m * B;
+        // the block is needed when one of its groups lies in the chunk
+        bool need = false;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) need = need || ((8 * b + j - gs + G) % G) < ng;
+        if (!need) continue;
+        float v[4][8];
+        fwht::load_block(x + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock,
+                         sign ? sign + static_cast<long>(b) * kHBlock : nullptr, lane, v);
+        fwht::fwht_1024(v, lane);
+        float f, finv;
+        fwht::decode_factor(v, f, finv);
+#pragma unroll
+        for (int ih = 0; ih < 4; ++ih) {
+          // lanes 0-15 hold group 2 ih of the block, lanes 16-31 group 2 ih + 1
+          const int gg = 8 * b + 2 * ih + (lane >> 4);
+          const int pos = (gg - gs + G) % G;
+          const uint4 w = fwht::decode_pack8(v, ih, f);
+          if (pos < ng)
+            *reinterpret_cast<uint4*>(xreg + m * pitch + pos * 256 + (lane & 15) * 16) = w;
+        }
+        if (lane == 0) xs_s[m * 64 + b] = 0.5f * finv;
+      }
+    };
+
+    float acc[TPW][NT][4], bacc[TPW][NT][4];
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[tt][nt][i] = bacc[tt][nt][i] = 0.f;
+
+    int rb = u0 / G, g = u0 % G, seg_g0 = g, gs = g;
+    bool alive = true;
+    int c_end = 0;
+    for (int i = 0; alive && i < n_units;) {
+      if (i == c_end) {
+        // next chunk: every consumer is done with the resident operand
+        if (i > 0) ptx::named_sync(1, 32 * CONSUMERS);
+        gs = g;
+        c_end = n_units - i < CU ? n_units : i + CU;
+        build(gs, c_end - i);
+        ptx::named_sync(1, 32 * CONSUMERS);
+      }
+      // units up to the end of the segment (row block) or of the chunk
+      const int seg_stop = i + (G - g);
+      const int stop = seg_stop < c_end ? seg_stop : c_end;
+      for (; i < stop; ++i) {
+        const int s = i % LSTAGES;
+        const uint32_t ph = static_cast<uint32_t>(i / LSTAGES) & 1u;
+        if (!ptx::mbar_wait(&full[s], ph, abort_flag, WAIT_LIMIT)) {
+          if (!*abort_flag) fail(abort_flag, ERR_CONSUMER);
+          alive = false;
+          break;
+        }
+        const uint8_t* unit = smem + s * UNIT_BYTES;
+        uint4 cv[TPW];
+        uint32_t sp[TPW];
+#pragma unroll
+        for (int tt = 0; tt < TPW; ++tt) {
+          cv[tt] = *reinterpret_cast<const uint4*>(unit + 512 * (TPW * cw + tt) + 16 * lane);
+          sp[tt] = *reinterpret_cast<const uint32_t*>(unit + UNIT_CODE_BYTES + 32 * (TPW * cw + tt) +
+                                                      4 * gq);
+        }
+        uint32_t bf[NT][8][2];
+        const int pos = g >= gs ? g - gs : g + G - gs;
+        const uint32_t xb = x_base + pos * 256;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            ldmatrix_x4(xb + bf_off[nt] + 64 * q, bf[nt][2 * q][0], bf[nt][2 * q][1],
+                        bf[nt][2 * q + 1][0], bf[nt][2 * q + 1][1]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&empty[s]);
+        unit_math<NT>(cv, sp, bf, bacc);
+        if ((g & 7) == 7 || i + 1 == n_units) {
+          const int blk = g >> 3;
+          float f[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int tok = 8 * nt + 2 * cq + h;
+              f[nt][h] = tok < M ? xs_s[tok * 64 + blk] : 0.f;
+            }
+          fold_block<NT>(acc, bacc, f);
+        }
+        ++g;
+      }
+      if (!alive) break;
+      if (g == G || i == n_units) {
+        end_segment<NT>(acc, seg_g0, g, rb, G, U, C, S, M, N, cw, lane, y, partials, abort_flag);
+#pragma unroll
+        for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[tt][nt][q] = 0.f;
+        seg_g0 = 0;
+        if (g == G) {
+          g = 0;
+          ++rb;
+        }
+      }
+    }
+    // a consumer that stopped early still meets the others at their barriers
+    if (!alive)
+      for (int i = c_end; i < n_units; i += CU) {
+        ptx::named_sync(1, 32 * CONSUMERS);
+        ptx::named_sync(1, 32 * CONSUMERS);
+      }
     __syncwarp();
   }
   __syncthreads();
@@ -518,6 +771,35 @@ cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* 
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   if (M <= 8) return launch_nt<1>(tm, packed, xs, m, n, k, yy, partials, p, st);
   return launch_nt<2>(tm, packed, xs, m, n, k, yy, partials, p, st);
+}
+
+namespace {
+template <int NT>
+cudaError_t launch_linear_nt(const uint16_t* x, const int8_t* sign, const uint8_t* packed, int M,
+                             int N, int K, __nv_bfloat16* y, unsigned long long* partials,
+                             const GemvPlan& p, cudaStream_t st) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(linear_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(LSMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  return launch(linear_kernel<NT>, dim3(p.C), dim3(NUM_THREADS), LSMEM_BYTES, st, x, sign, packed,
+                M, N, K, y, partials, p.U, p.S);
+}
+}  // namespace
+
+cudaError_t launch_linear_decode(const uint16_t* x, const int8_t* sign, const uint8_t* packed,
+                                 int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                                 cudaStream_t st) {
+  const GemvPlan p = make_plan(N, K, sm_count());
+  auto* partials = static_cast<unsigned long long*>(ws);
+  auto* yy = reinterpret_cast<__nv_bfloat16*>(y);
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (M <= 8) return launch_linear_nt<1>(x, sign, packed, m, n, k, yy, partials, p, st);
+  return launch_linear_nt<2>(x, sign, packed, m, n, k, yy, partials, p, st);
 }
 
 cudaError_t gemv_read_clear_error(unsigned int* err) {

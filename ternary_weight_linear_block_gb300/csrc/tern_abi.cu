@@ -120,6 +120,24 @@ tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const fl
   return from_cuda(launch_gemv(packed, xh, xs, M, N, K, y, ws, static_cast<cudaStream_t>(stream)));
 }
 
+tern_status tern_linear_decode(const uint16_t* x, const int8_t* sign, const uint8_t* packed,
+                               int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
+  if (M > 16) return TERN_ERR_SHAPE;
+  if (N > (int64_t(1) << 30) / (K / 16)) return TERN_ERR_SHAPE;
+  if (M == 0 || N == 0) return TERN_OK;
+  if (x == nullptr || packed == nullptr || y == nullptr) return TERN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(packed) || !aligned16(y)) return TERN_ERR_ALIGN;
+  const size_t need = gemv_workspace_bytes(M, N, K);
+  if (ws == nullptr || ws_bytes < need) return TERN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(
+      launch_linear_decode(x, sign, packed, M, N, K, y, ws, static_cast<cudaStream_t>(stream)));
+}
+
 tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
                                    const float* rscale, int64_t M, int64_t N, int64_t K,
                                    uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,

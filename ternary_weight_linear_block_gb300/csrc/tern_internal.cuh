@@ -49,6 +49,9 @@ size_t gemv_packed_bytes(int64_t N, int64_t K);
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* xs, int64_t M,
                         int64_t N, int64_t K, uint16_t* y, void* ws, cudaStream_t st);
+cudaError_t launch_linear_decode(const uint16_t* x, const int8_t* sign, const uint8_t* packed,
+                                 int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                                 cudaStream_t st);
 cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
                         const float* rscale, int64_t M, int64_t N, int64_t K, uint16_t* y,
                         int32_t* acc, cudaStream_t st);

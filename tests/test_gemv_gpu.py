@@ -27,7 +27,7 @@ def _layer(codes, scales):
 def _decode(layer, bits, m, ws=None):
     ws = ws or B.Workspace()
     y = poison(torch.empty((m, layer.n), dtype=torch.bfloat16, device="cuda"))
-    B.decode(layer, to_dev_bf16(bits), ws, y=y)
+    B.decode(layer, to_dev_bf16(bits), ws, y=y)   # rotation, then tern_gemv_decode
     B.tern_check()          # raises if a bounded device-side wait gave up
     return bf16_to_f32(y)
 
