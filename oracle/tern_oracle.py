@@ -49,8 +49,8 @@ from __future__ import annotations
 
 import numpy as np
 
-HBLOCK = 1024          # Hadamard block width (page 1, section 1)
-GROUP = 128            # elements per scale group (page 1, premises)
+HBLOCK = 1024          # Hadamard block width (the page's section 1)
+GROUP = 128            # elements per scale group (the page's premises)
 INV_SQRT_BLOCK = 1.0 / 32.0
 
 
@@ -61,7 +61,7 @@ INV_SQRT_BLOCK = 1.0 / 32.0
 def hadamard_dense(n: int) -> np.ndarray:
     """Natural-order Sylvester Hadamard matrix of size n (fp64, entries +-1).
 
-    H_1 = [1];  H_2m = [[H_m, H_m], [H_m, -H_m]]  (page 1, section 1: the
+    H_1 = [1];  H_2m = [[H_m, H_m], [H_m, -H_m]]  (the page's section 1: the
     recursive Sylvester structure behind the split identity).
     """
     if n < 1 or (n & (n - 1)) != 0:
@@ -85,7 +85,7 @@ def _h1024() -> np.ndarray:
 def rotate_f64(x, sign=None) -> np.ndarray:
     """O1 rotation: xr = (I_B kron H1024/32) (sign * x), exactly, in fp64.
 
-    Computed as a dense matrix product per 1024-block (page 1, premises and
+    Computed as a dense matrix product per 1024-block (the page's premises and
     section 1), deliberately not as butterflies.
     x: [M, K] (any float dtype), K a multiple of 1024.  sign: None or [K] of +-1.
     """
@@ -108,7 +108,7 @@ def fwht_f32(x, sign=None) -> np.ndarray:
 
     Per 1024-block, butterfly stages with stride h = 1, 2, 4, ..., 512 in that
     order; each butterfly maps (u, v) -> (u + v, u - v) with u the lower index.
-    The last stage (h = 512) is the split identity printed on page 1,
+    The last stage (h = 512) is the split identity printed on the page,
     section 1.  Then every element is multiplied by 1/32 (exact).  Every
     operation is one correctly rounded fp32 add, subtract or multiply.
     x: [M, K]; bf16 inputs must be passed already widened to fp32 (exact).
@@ -138,14 +138,14 @@ def fwht_f32(x, sign=None) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def dequant_f64(codes, scales) -> np.ndarray:
-    """O1 weight: W[n,k] = code[n,k] * s[n, k // 128] in fp64 (page 1, premises)."""
+    """O1 weight: W[n,k] = code[n,k] * s[n, k // 128] in fp64 (the page's premises)."""
     codes = np.asarray(codes)
     s = np.asarray(scales).astype(np.float64)
     return codes.astype(np.float64) * np.repeat(s, GROUP, axis=1)
 
 
 def decompose_scales(scales):
-    """Scale decomposition of page 1, section 4 (int8 prefill).
+    """Scale decomposition of the page's section 4 (int8 prefill).
 
     smax[n] = max_g |s[n,g]| (fp32, exact from fp16),
     q[n,g]  = rint((127 * s[n,g]) / smax[n]) with both operations in fp32,
@@ -168,7 +168,7 @@ def decompose_scales(scales):
 
 
 def w_int8(codes, q) -> np.ndarray:
-    """W_int8[n,k] = code[n,k] * q[n, k // 128]  (page 1, section 4).  int16 result."""
+    """W_int8[n,k] = code[n,k] * q[n, k // 128]  (the page's section 4).  int16 result."""
     codes = np.asarray(codes).astype(np.int16)
     qq = np.repeat(np.asarray(q).astype(np.int16), GROUP, axis=1)
     return codes * qq
@@ -181,7 +181,7 @@ def w_int8(codes, q) -> np.ndarray:
 def quant_tokens(xr):
     """Per-token symmetric int8 quantisation of the rotated activations.
 
-    Page 1, section 4: activations are quantised to int8 per token after the
+    The page's section 4: activations are quantised to int8 per token after the
     Hadamard rotation.  a[m] = max_k |xr[m,k]| (fp32), tscale[m] = a[m]/127
     (fp32), xq = clamp(rint(xr / tscale), -127, 127) with the division and the
     rounding in fp32 (half to even).  A zero token gives xq = 0, tscale = 0.
@@ -265,12 +265,12 @@ def y_int8(acc, tscale, rscale) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def linear_f64(x, codes, scales, sign=None) -> np.ndarray:
-    """O1: y = (H_blk (sign*x)) W^T in fp64, W = code * s (page 1, premises)."""
+    """O1: y = (H_blk (sign*x)) W^T in fp64, W = code * s (the page's premises)."""
     return rotate_f64(x, sign) @ dequant_f64(codes, scales).T
 
 
 def linear_int8(x, codes, scales, sign=None):
-    """O2: the whole int8 prefill path of page 1, section 4.
+    """O2: the whole int8 prefill path of the page's section 4.
 
     Returns a dict with xr (fp32), xq, tscale, q, rscale, w (int16 holding the
     int8 weights), acc (int64) and y (fp32 on the bf16 grid).

@@ -60,7 +60,7 @@ def test_normalised_rotation_is_an_involution_and_orthonormal():
 
 
 def test_split_identity_of_the_page():
-    # H1024 [a; b] = [H512 a + H512 b ; H512 a - H512 b]   (page 1, section 1)
+    # H1024 [a; b] = [H512 a + H512 b ; H512 a - H512 b]   (the page's section 1)
     rng = np.random.default_rng(2)
     a = rng.integers(-50, 50, 512).astype(np.float64)
     b = rng.integers(-50, 50, 512).astype(np.float64)
