@@ -273,18 +273,19 @@ def run_decode(args, rank, ws, local):
         tk = _time_region(lambda: run.gemv_only(kb), kernel_launches, stream, 1)
         gemv_us = tk / kernel_launches * 1e6
 
-        # end to end through the public API: pinned host x in, host y out
-        x_pin = [x.pin_memory() for x in xs_host]
-        y_pin = [torch.empty((m, layer.n), dtype=torch.bfloat16).pin_memory() for m in DECODE_MS]
-        wsp = [B.Workspace() for _ in DECODE_MS]
+        # end to end through the public API (B.DecodeGraph): every step copies
+        # its pinned host activations in, rotates, multiplies and copies y back
+        # to pinned host memory, then waits
+        plans = [[B.DecodeGraph(lay, m) for lay in layers] for m in DECODE_MS]
+        for b, m in enumerate(DECODE_MS):
+            for pl in plans[b]:
+                pl.x_host.copy_(xs_host[b])
+        e2e_i = [0]
 
         def e2e_step():
-            for b, m in enumerate(DECODE_MS):
-                lay = layers[run.i % len(layers)]
-                run.i += 1
-                xd = x_pin[b].to("cuda", non_blocking=True)
-                y = B.decode(lay, xd, wsp[b], stream=stream.cuda_stream)
-                y_pin[b].copy_(y, non_blocking=True)
+            for b in range(len(DECODE_MS)):
+                plans[b][e2e_i[0] % len(layers)].launch()
+            e2e_i[0] += 1
             stream.synchronize()
 
         for _ in range(args.warmup):

@@ -258,6 +258,60 @@ def decode(layer: PackedLayer, x: torch.Tensor, ws: Workspace, y: torch.Tensor |
     return y
 
 
+class DecodeGraph:
+    """One layer's decode forward for a fixed M, captured once as a CUDA graph
+    with its host transfers: the pinned host input ``x_host`` is copied to the
+    device, rotated, multiplied (tern_fwht_quant + tern_gemv_decode, or
+    tern_linear_decode with ``fused=True``) and the bf16 result is copied back
+    to the pinned host buffer ``y_host``.  ``run()`` replays the graph on the
+    current stream and waits for it, so a decode loop pays one graph launch
+    and one wait per call instead of per-call host work.  The buffers belong
+    to the graph: write the next input into ``x_host`` (or pass it to
+    ``run``) and read ``y_host`` after ``run`` returns."""
+
+    def __init__(self, layer: PackedLayer, m: int, sign: torch.Tensor | None = None,
+                 fused: bool = False, device="cuda"):
+        self.layer, self.m, self.sign, self.fused = layer, m, sign, fused
+        self.x_host = torch.zeros((m, layer.k), dtype=torch.bfloat16).pin_memory()
+        self.y_host = torch.empty((m, layer.n), dtype=torch.bfloat16).pin_memory()
+        self.x = torch.empty((m, layer.k), dtype=torch.bfloat16, device=device)
+        self.y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=device)
+        self.xh = torch.empty((m, layer.k), dtype=torch.float16, device=device)
+        self.xs = torch.empty((m, layer.k // 1024), dtype=torch.float32, device=device)
+        nb = tern_workspace_bytes(TERN_OP_GEMV, m, layer.n, layer.k)
+        self.ws = Workspace(device).get(nb)
+        self._body()                      # first launch outside capture (sets kernel attributes)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._body()
+
+    def _body(self):
+        lay, m = self.layer, self.m
+        st = torch.cuda.current_stream().cuda_stream
+        self.x.copy_(self.x_host, non_blocking=True)
+        if self.fused:
+            tern_linear_decode(self.x, self.sign, lay.packed, m, lay.n, lay.k, self.y, self.ws,
+                               self.ws.numel(), st)
+        else:
+            tern_fwht_quant(self.x, m, lay.k, self.sign, TERN_FWHT_DECODE, self.xh, self.xs, st)
+            tern_gemv_decode(lay.packed, self.xh, self.xs, m, lay.n, lay.k, self.y, self.ws,
+                             self.ws.numel(), st)
+        self.y_host.copy_(self.y, non_blocking=True)
+
+    def launch(self, x: torch.Tensor | None = None):
+        """Replay on the current stream without waiting."""
+        if x is not None:
+            self.x_host.copy_(x)
+        self.graph.replay()
+
+    def run(self, x: torch.Tensor | None = None) -> torch.Tensor:
+        """Replay and wait; returns the pinned host output."""
+        self.launch(x)
+        torch.cuda.current_stream().synchronize()
+        return self.y_host
+
+
 def prefill(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,
             acc: torch.Tensor | None = None, sign=None, stream=None) -> torch.Tensor:
     """Prefill forward: rotation + per-token int8 quantisation, then the GEMM."""

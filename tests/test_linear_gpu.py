@@ -97,3 +97,19 @@ def test_empty_and_repeat():
     y2 = B.decode(lay, x, ws, fused=True)
     B.tern_check()
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_graph_matches_decode(fused):
+    """B.DecodeGraph (host in, graph replay, host out) returns exactly what
+    B.decode returns, for two different inputs replayed through one graph."""
+    d = I.make_layer(I.QKV, 4, seed=4)
+    lay = _layer(d.codes, d.scales)
+    plan = B.DecodeGraph(lay, 4, fused=fused)
+    for seed in (5, 6):
+        bits, _ = I.make_activations(seed, 4, lay.k, 0.001, 50.0)
+        x = to_dev_bf16(bits)
+        want = B.decode(lay, x, B.Workspace())
+        got = plan.run(x.cpu())
+        B.tern_check()
+        assert torch.equal(got, want.cpu())
