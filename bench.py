@@ -379,6 +379,103 @@ def run_prefill(args, local, m=2048):
                                         "sm_103a has no tcgen05 int8 kind"}}
 
 
+def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 16), prefill_ms=(512, 2048)):
+    """The 64-layer linear stack of a 27B hybrid model: per layer qkv
+    5120->10240, o 5120->5120, gate/up 5120->34816, down 17408->5120, each with
+    its own seeded weights (seed = 4 * layer + linear).  The linears are not
+    chained (there is no model): each shape has its own synthetic input.  A
+    decode step runs rotation + GEMV through all 256 linears (captured as one
+    CUDA graph, replayed); a prefill step runs rotation + int8 quantisation +
+    the int8 GEMM through all 256."""
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    shapes = I.STACK_LAYERS
+    hbm_peak, tc_peak, _ = _peaks()
+    with torch.cuda.stream(stream):
+        g = torch.Generator(device="cuda")
+        layers = []
+        for li in range(n_layers):
+            row = []
+            for si, shp in enumerate(shapes):
+                g.manual_seed(4 * li + si)
+                codes = (torch.randint(0, 3, (shp.n, shp.k), dtype=torch.int8, device="cuda",
+                                       generator=g) - 1).to(torch.int8)
+                scales = (0.02 * torch.randn((shp.n, shp.k // 128), device="cuda", generator=g)
+                          .abs() + 1e-3).to(torch.float16)
+                row.append(B.pack_layer(codes, scales, decode=True, prefill=True))
+                del codes, scales
+            layers.append(row)
+        torch.cuda.synchronize()
+        packed_bytes = sum(l.weight_bytes for row in layers for l in row)
+        wq_bytes = sum(l.w_q.numel() * 2 for row in layers for l in row)
+        st = stream.cuda_stream
+        out = {"layers": n_layers, "linears": [s.name for s in shapes],
+               "packed_bytes": packed_bytes, "w_int8_held_as_fp16_bytes": wq_bytes,
+               "inputs": "each linear shape has its own seeded synthetic input (not chained)",
+               "decode": [], "prefill": []}
+        for m in decode_ms:
+            xs_in = [_activations(shp, m, seed=900 + si).cuda() for si, shp in enumerate(shapes)]
+            xh = [torch.empty((m, shp.k), dtype=torch.float16, device="cuda") for shp in shapes]
+            sc = [torch.empty((m, shp.k // 1024), dtype=torch.float32, device="cuda") for shp in shapes]
+            ys = [torch.empty((m, shp.n), dtype=torch.bfloat16, device="cuda") for shp in shapes]
+            wss = [B.Workspace().get(B.tern_workspace_bytes(B.TERN_OP_GEMV, m, shp.n, shp.k))
+                   for shp in shapes]
+
+            def decode_step(st_handle):
+                for row in layers:
+                    for si, (shp, lay) in enumerate(zip(shapes, row)):
+                        B.tern_fwht_quant(xs_in[si], m, shp.k, None, B.TERN_FWHT_DECODE, xh[si],
+                                          sc[si], st_handle)
+                        B.tern_gemv_decode(lay.packed, xh[si], sc[si], m, shp.n, shp.k, ys[si],
+                                           wss[si], wss[si].numel(), st_handle)
+
+            decode_step(st)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                decode_step(torch.cuda.current_stream().cuda_stream)
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize()
+            reps = 10
+            t = _time_region(graph.replay, reps, stream, 1)
+            B.tern_check(stream)
+            gbps = packed_bytes * reps / t / 1e9
+            out["decode"].append({"M": m, "ms_per_step": round(t / reps * 1e3, 4),
+                                  "weight_GBps": round(gbps, 1),
+                                  "pct_hbm_peak": round(100 * gbps / hbm_peak, 1),
+                                  "launches_per_step": 2 * len(shapes) * n_layers})
+            del graph
+        ops_step = sum(2.0 * shp.n * shp.k for shp in shapes) * n_layers
+        for m in prefill_ms:
+            xs_in = [_activations(shp, m, seed=950 + si).cuda() for si, shp in enumerate(shapes)]
+            xq = [torch.empty((m, shp.k), dtype=torch.float16, device="cuda") for shp in shapes]
+            ts = [torch.empty(m, dtype=torch.float32, device="cuda") for shp in shapes]
+            ys = [torch.empty((m, shp.n), dtype=torch.bfloat16, device="cuda") for shp in shapes]
+
+            def prefill_step():
+                for row in layers:
+                    for si, (shp, lay) in enumerate(zip(shapes, row)):
+                        B.tern_fwht_quant(xs_in[si], m, shp.k, None, B.TERN_FWHT_I8, xq[si],
+                                          ts[si], st)
+                        B.tern_gemm_prefill_int8(xq[si], ts[si], lay.w_q, lay.rscale, m, shp.n,
+                                                 shp.k, ys[si], stream=st)
+
+            prefill_step()
+            torch.cuda.synchronize()
+            reps = 3
+            t = _time_region(prefill_step, reps, stream, 1)
+            B.tern_check(stream)
+            tops = ops_step * m * reps / t / 1e12
+            out["prefill"].append({"M": m, "ms_per_step": round(t / reps * 1e3, 3),
+                                   "TOPS": round(tops, 1),
+                                   "frac_of_bf16_peak": round(tops / tc_peak, 4)})
+            del xq, ys
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_cpu_baseline(args, budget_s=15.0):
     """The oracle (fp64 dense reference) timed on a bounded sample of the workload."""
     from oracle import tern_oracle as O
@@ -447,6 +544,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-stack", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -468,6 +566,8 @@ def main():
     torch.cuda.empty_cache()
     if not args.no_prefill:
         line["prefill"] = run_prefill(args, local)
+    if not args.no_stack and rank == 0:
+        line["stack"] = run_stack(args, local)
     if rank == 0:
         if not args.no_cpu_baseline and ws == 1:
             line["cpu_baseline"] = run_cpu_baseline(args)

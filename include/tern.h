@@ -161,12 +161,16 @@ tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_
  *                           tern_workspace_bytes(TERN_OP_GEMV, M, N, K) bytes,
  *                           16-byte aligned, ZERO-FILLED before its first use
  *                           (tern_workspace_init); every call leaves it
- *                           zero-filled again on completion.  Calls that share
- *                           a workspace must not run concurrently.
+ *                           zero-filled again on completion (it holds the
+ *                           partial sums of 512-row blocks that several CTAs
+ *                           share).  Calls that share a workspace must not run
+ *                           concurrently.
  * Requirements: 1 <= M <= 16 (M == 0 is a no-op), K % 1024 == 0, K <= 65536.
- * Device-side waits are bounded; a wait that gives up makes the call's
- * outputs undefined and is reported by tern_check(); the workspace must then
- * be zero-filled again (tern_workspace_init) before its next use.
+ * A call is the GEMV kernel and, when some 512-row block is shared by more
+ * than four CTAs (M <= 8) or by several CTAs (M > 8), a fixup kernel that
+ * adds those blocks' partial sums in slot order.  Device-side waits are bounded; a wait that gives up makes the
+ * call's outputs undefined and is reported by tern_check(); the workspace
+ * must then be zero-filled again (tern_workspace_init) before its next use.
  * ---------------------------------------------------------------------- */
 tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const float* xs,
                              int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
@@ -202,8 +206,8 @@ tern_status tern_linear_decode(const uint16_t* x, const int8_t* sign, const uint
  * through its own pool, handing the layer only its inputs and outputs, cannot
  * give it a separate workspace, and a decode loop that must never stall
  * cannot call cudaMalloc, which may synchronise the device.  This call takes
- * no workspace and allocates nothing: its scratch (the tagged partial sums
- * of row blocks shared by several CTAs) lives in a static device array of
+ * no workspace and allocates nothing: its scratch (the partial sums of row
+ * blocks shared by several CTAs) lives in a static device array of
  * TERN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library holds until the process exits.
  *

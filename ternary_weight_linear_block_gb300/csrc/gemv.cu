@@ -29,13 +29,14 @@
 //   1024-block by the block's power-of-two activation factor.
 // * units are cut into equal contiguous ranges, one per persistent CTA
 //   (stream-K).  A 512-row block finished by one CTA is written directly.  A
-//   block shared by several CTAs is summed by its first owner, which in this
-//   order reaches the block last: the other owners publish their partial sums
-//   as tagged 64-bit words (no fence, no atomic), the first owner reads them
-//   in slot order, writes bf16 y and clears the tags.  Each warp's rows are
-//   independent, so the flags are per value and no warp waits for a CTA-wide
-//   event.  The segment's end runs outside the per-unit loop, which keeps the
-//   hot loop's registers for the hot loop.
+//   block shared by at most 4 CTAs at M <= 8 is summed by its first owner,
+//   which in this order reaches it last, from tagged 64-bit words the other
+//   owners publish without fences or atomics; otherwise (more owners: small
+//   N, large K; or M > 8) the block gets untagged partial sums that a small
+//   fixup kernel, launched right after (programmatic launch), adds in slot
+//   order across the whole GPU, so no block's first owner reads many slots.  The segment's end
+//   runs outside the per-unit loop, which keeps the hot loop's registers for
+//   the hot loop.
 // * the weight copies do not depend on the previous kernel, so the producer
 //   issues the first ring of them before the programmatic launch wait, and
 //   every CTA lets the next kernel launch as soon as it starts.
@@ -73,6 +74,12 @@ static_assert(STAGE_BYTES % 1024 == 0 && XTILE_BYTES % 16 == 0, "stage alignment
 
 enum : unsigned int { ERR_PRODUCER = 1u, ERR_CONSUMER = 2u, ERR_DRAIN = 4u, ERR_REDUCE = 8u };
 
+// Owners of a 512-row block summed inside the GEMV (M <= 8 only: with two n8
+// tiles the first owner's share of the sums costs more than the fixup
+// launch); blocks with more owners go through the fixup kernel.
+template <int NT>
+__host__ __device__ constexpr int tag_slots() { return NT == 1 ? 4 : 1; }
+
 __host__ __device__ inline long unit_begin(long c, long U, long C) { return c * U / C; }
 __host__ __device__ inline long owner_of(long u, long U, long C) { return ((u + 1) * C - 1) / U; }
 
@@ -108,13 +115,16 @@ __device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long
 }
 
 // A segment [ga, gb) of row block rb ends.  A row block finished by one CTA
-// is written directly.  Otherwise the first CTA owning part of the block sums
-// it: every other owner publishes its 32 rows per warp as tagged 64-bit words
+// is written directly.  A block shared by at most tag_slots CTAs is summed by
+// its first owner, which in stream-K order finishes the block last: every
+// other owner publishes its 32 rows per warp as tagged 64-bit words
 // (value | 1 << 32) in its slot, with no fence and no atomic (each word is
 // single-copy atomic, so a set tag vouches for the value beside it), and the
-// first owner, which in stream-K order finishes the block last, reads them,
-// adds them in slot order, writes y and clears the tags for the next call.
-// Out of line: the hot loop must not pay registers for this path.
+// first owner reads them, adds them in slot order, writes y and clears the
+// tags.  A block with more owners would load its first owner with too many
+// slots: there every owner stores its words untagged (tag 0) and the fixup
+// kernel adds them across the whole GPU after the GEMV.  Between calls every
+// word of the workspace has tag 0.
 template <int NT>
 __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int ga, int gb, int rb,
                                          int G, int U, int C, int S, int M, int N, int cw,
@@ -136,6 +146,18 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
   }
   const long first = owner_of(static_cast<long>(rb) * G, U, C);
   const int slot = static_cast<int>(blockIdx.x - first);
+  const int nslots = static_cast<int>(owner_of(static_cast<long>(rb) * G + G - 1, U, C) - first + 1);
+  if (NT == 2 || nslots > tag_slots<NT>()) {
+    unsigned long long* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
+      const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
+      const int tok = 8 * nt + 2 * cq + (i & 1);
+      if (tok < M) __stcg(base + tok * RB + rin, static_cast<unsigned long long>(__float_as_uint(acc[tt][nt][i])));
+    }
+    return;
+  }
   if (slot != 0) {
     unsigned long long* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
 #pragma unroll
@@ -149,7 +171,6 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
     }
     return;
   }
-  const int nslots = static_cast<int>(owner_of(static_cast<long>(rb) * G + G - 1, U, C) - first + 1);
   float sum[NV];
 #pragma unroll
   for (int v = 0; v < NV; ++v) sum[v] = acc[v / (NT * 4)][(v / 4) % NT][v % 4];
@@ -210,6 +231,42 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
     const int tok = 8 * nt + 2 * cq + (i & 1);
     if (row < N && tok < M) y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum[v]);
   }
+}
+
+// Fixup after the GEMV: y[tok][row] = bf16(sum of the slots of the row's
+// block, in slot order) for every row of a block shared by more than
+// tag_slots CTAs.
+// One thread per (block, token, row), consecutive threads on consecutive rows
+// (coalesced); the slot loads of a thread are independent.  The reduction is
+// spread over the whole GPU instead of the blocks' owners.
+constexpr int FIX_THREADS = 256;
+__global__ void __launch_bounds__(FIX_THREADS)
+    fixup_kernel(const unsigned long long* __restrict__ partials, __nv_bfloat16* __restrict__ y,
+                 int M, int N, int G, int U, int C, int S, int tag) {
+  pdl_launch_dependents();
+  const long t = static_cast<long>(blockIdx.x) * FIX_THREADS + threadIdx.x;
+  const int rin = static_cast<int>(t % RB);
+  const int tok = static_cast<int>((t / RB) % M);
+  const long rb = t / (static_cast<long>(RB) * M);
+  const long first = owner_of(rb * G, U, C);
+  const int nslots = static_cast<int>(owner_of(rb * G + G - 1, U, C) - first + 1);
+  const long row = rb * RB + rin;
+  pdl_wait();   // the GEMV's partial sums
+  if (nslots <= tag || row >= N) return;
+  const unsigned long long* p = partials + (rb * S * M + tok) * RB + rin;
+  const long stride = static_cast<long>(M) * RB;   // one slot
+  float sum = 0.f;
+  int sl = 0;
+  for (; sl + 4 <= nslots; sl += 4) {
+    const unsigned long long a0 = __ldcg(p + (sl + 0) * stride), a1 = __ldcg(p + (sl + 1) * stride);
+    const unsigned long long a2 = __ldcg(p + (sl + 2) * stride), a3 = __ldcg(p + (sl + 3) * stride);
+    sum += __uint_as_float(static_cast<unsigned int>(a0));
+    sum += __uint_as_float(static_cast<unsigned int>(a1));
+    sum += __uint_as_float(static_cast<unsigned int>(a2));
+    sum += __uint_as_float(static_cast<unsigned int>(a3));
+  }
+  for (; sl < nslots; ++sl) sum += __uint_as_float(static_cast<unsigned int>(__ldcg(p + sl * stride)));
+  y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum);
 }
 
 // The MMAs of one unit for this warp's tiles: codes cv, scale pairs sp and the
@@ -744,11 +801,23 @@ size_t gemv_packed_bytes(int64_t N, int64_t K) {
   return static_cast<size_t>((N + RB - 1) / RB) * static_cast<size_t>(K / kGroup) * UNIT_BYTES;
 }
 
-// Workspace: tagged partial sums [RBn][S][M][512] (64-bit words, zero when
-// idle: every call leaves the tags it set cleared).
+// Workspace: 64-bit partial-sum words [RBn][S][M][512] of row blocks shared
+// by several CTAs (value in the low half, ready tag in the high half); every
+// call leaves all tags at 0.
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const GemvPlan p = make_plan(N, K, sm_count());
   return static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(unsigned long long);
+}
+
+// The fixup kernel over every (block, token, row), when some block is shared.
+cudaError_t launch_fixup(const GemvPlan& p, unsigned long long* partials, __nv_bfloat16* y, int M,
+                         int N, int G, cudaStream_t st) {
+  const int tag = M <= 8 ? tag_slots<1>() : tag_slots<2>();
+  if (p.S <= tag) return cudaSuccess;
+  const long threads = static_cast<long>(p.RBn) * M * RB;
+  const dim3 grid(static_cast<unsigned>((threads + FIX_THREADS - 1) / FIX_THREADS));
+  return launch(fixup_kernel, grid, dim3(FIX_THREADS), 0, st,
+                static_cast<const unsigned long long*>(partials), y, M, N, G, p.U, p.C, p.S, tag);
 }
 
 cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* xs, int64_t M,
@@ -769,8 +838,10 @@ cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* 
     return cudaErrorInvalidValue;
   auto* yy = reinterpret_cast<__nv_bfloat16*>(y);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  if (M <= 8) return launch_nt<1>(tm, packed, xs, m, n, k, yy, partials, p, st);
-  return launch_nt<2>(tm, packed, xs, m, n, k, yy, partials, p, st);
+  const cudaError_t e = M <= 8 ? launch_nt<1>(tm, packed, xs, m, n, k, yy, partials, p, st)
+                               : launch_nt<2>(tm, packed, xs, m, n, k, yy, partials, p, st);
+  if (e != cudaSuccess) return e;
+  return launch_fixup(p, partials, yy, m, n, static_cast<int>(K / kGroup), st);
 }
 
 namespace {
@@ -798,8 +869,10 @@ cudaError_t launch_linear_decode(const uint16_t* x, const int8_t* sign, const ui
   auto* partials = static_cast<unsigned long long*>(ws);
   auto* yy = reinterpret_cast<__nv_bfloat16*>(y);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  if (M <= 8) return launch_linear_nt<1>(x, sign, packed, m, n, k, yy, partials, p, st);
-  return launch_linear_nt<2>(x, sign, packed, m, n, k, yy, partials, p, st);
+  const cudaError_t e = M <= 8 ? launch_linear_nt<1>(x, sign, packed, m, n, k, yy, partials, p, st)
+                               : launch_linear_nt<2>(x, sign, packed, m, n, k, yy, partials, p, st);
+  if (e != cudaSuccess) return e;
+  return launch_fixup(p, partials, yy, m, n, static_cast<int>(K / kGroup), st);
 }
 
 cudaError_t gemv_read_clear_error(unsigned int* err) {

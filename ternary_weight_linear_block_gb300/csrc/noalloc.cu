@@ -6,7 +6,7 @@
 // output buffers) cannot let the library take a separate workspace, and a
 // decode loop that must never stall cannot call cudaMalloc, which may
 // synchronise the whole device.  This entry point allocates nothing: the
-// GEMV's tagged partial sums (row blocks shared by several CTAs) live in
+// GEMV's partial sums (row blocks shared by several CTAs) live in
 // g_noalloc_scratch, a static device array of TERN_NOALLOC_SCRATCH_BYTES that
 // every GPU loading the library keeps until the process exits.
 //
@@ -15,8 +15,8 @@
 // first call should come before any stream capture.  All calls share the one
 // array and it keeps the last call's contents, so each call zero-fills the
 // part it uses on its stream before the kernel (a call that gave up waiting
-// may have left tags set); calls that overlap on the GPU (for example on two
-// streams) race on the array.
+// may have left ready tags set); calls that overlap on the GPU (for example
+// on two streams) race on the array.
 #include "tern_internal.cuh"
 
 namespace tern {
