@@ -221,7 +221,10 @@ class DecodeRunner:
                            self.ws[b], self.ws[b].numel(), st)
 
     def launches_per_step(self):
-        return 2 * len(self.ms)
+        # per batch: the rotation kernel, then the GEMV (and its fixup kernel
+        # at shapes where a row block is shared by many CTAs)
+        return sum(1 + B.tern_kernel_launches(B.TERN_OP_GEMV, m, self.n, self.k)
+                   for m in self.ms)
 
     def bytes_per_step(self):
         return sum(self.layers[0].weight_bytes for _ in self.ms)
@@ -444,7 +447,9 @@ def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 16), prefill_ms=(512, 2
             out["decode"].append({"M": m, "ms_per_step": round(t / reps * 1e3, 4),
                                   "weight_GBps": round(gbps, 1),
                                   "pct_hbm_peak": round(100 * gbps / hbm_peak, 1),
-                                  "launches_per_step": 2 * len(shapes) * n_layers})
+                                  "launches_per_step": n_layers * sum(
+                                      1 + B.tern_kernel_launches(B.TERN_OP_GEMV, m, shp.n, shp.k)
+                                      for shp in shapes)})
             del graph
         ops_step = sum(2.0 * shp.n * shp.k for shp in shapes) * n_layers
         for m in prefill_ms:

@@ -252,6 +252,14 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
 #define TERN_OP_GEMV 1
 #define TERN_OP_GEMM 2
 size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+/* Number of kernels one call launches at this shape on the current device
+ * (0 for an empty call or an unknown op): for TERN_OP_GEMV the GEMV kernel,
+ * plus the fixup kernel when a 512-row block is shared by more CTAs than the
+ * GEMV sums in place (tern_gemv_decode, tern_linear_decode and
+ * tern_gemv_decode_noalloc launch the same count); for TERN_OP_GEMM the one
+ * int8 GEMM kernel.  Host-only; launch counting for CUDA-graph sizing and
+ * profiling. */
+int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K);
 /* Zero-fill `bytes` of device memory at ws on `stream` (asynchronous). */
 tern_status tern_workspace_init(void* ws, size_t bytes, void* stream);
 

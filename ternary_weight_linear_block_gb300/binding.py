@@ -41,6 +41,7 @@ _SIGS = {
     "tern_version": (ctypes.c_int, []),
     "tern_packed_bytes": (_sz, [_i64, _i64]),
     "tern_workspace_bytes": (_sz, [ctypes.c_int, _i64, _i64, _i64]),
+    "tern_kernel_launches": (ctypes.c_int, [ctypes.c_int, _i64, _i64, _i64]),
     "tern_workspace_init": (ctypes.c_int, [_p, _sz, _p]),
     "tern_pack": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p]),
     "tern_fwht_quant": (ctypes.c_int, [_p, _i64, _i64, _p, ctypes.c_int, _p, _p, _p]),
@@ -123,6 +124,10 @@ def tern_packed_bytes(n: int, k: int) -> int:
 
 def tern_workspace_bytes(op: int, m: int, n: int, k: int) -> int:
     return lib().tern_workspace_bytes(op, m, n, k)
+
+
+def tern_kernel_launches(op: int, m: int, n: int, k: int) -> int:
+    return lib().tern_kernel_launches(op, m, n, k)
 
 
 def tern_workspace_init(ws, nbytes: int | None = None, stream=None):

@@ -82,6 +82,12 @@ __host__ __device__ constexpr int tag_slots() { return NT == 1 ? 4 : 1; }
 
 __host__ __device__ inline long unit_begin(long c, long U, long C) { return c * U / C; }
 __host__ __device__ inline long owner_of(long u, long U, long C) { return ((u + 1) * C - 1) / U; }
+// The same owner in 32-bit arithmetic for the kernels: the entry points keep
+// N * K <= 2^34, so U <= 2^18 + 512 and (u + 1) * C stays far below 2^32.
+__device__ __forceinline__ int owner32(int u, int U, int C) {
+  return static_cast<int>((static_cast<unsigned>(u + 1) * static_cast<unsigned>(C) - 1u) /
+                          static_cast<unsigned>(U));
+}
 
 __device__ __forceinline__ void fail(volatile int* abort_flag, unsigned int code) {
   *abort_flag = 1;
@@ -144,9 +150,9 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
     }
     return;
   }
-  const long first = owner_of(static_cast<long>(rb) * G, U, C);
-  const int slot = static_cast<int>(blockIdx.x - first);
-  const int nslots = static_cast<int>(owner_of(static_cast<long>(rb) * G + G - 1, U, C) - first + 1);
+  const int first = owner32(rb * G, U, C);
+  const int slot = static_cast<int>(blockIdx.x) - first;
+  const int nslots = owner32(rb * G + G - 1, U, C) - first + 1;
   if (NT == 2 || nslots > tag_slots<NT>()) {
     unsigned long long* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
 #pragma unroll
@@ -244,16 +250,16 @@ __global__ void __launch_bounds__(FIX_THREADS)
     fixup_kernel(const unsigned long long* __restrict__ partials, __nv_bfloat16* __restrict__ y,
                  int M, int N, int G, int U, int C, int S, int tag) {
   pdl_launch_dependents();
-  const long t = static_cast<long>(blockIdx.x) * FIX_THREADS + threadIdx.x;
-  const int rin = static_cast<int>(t % RB);
-  const int tok = static_cast<int>((t / RB) % M);
-  const long rb = t / (static_cast<long>(RB) * M);
-  const long first = owner_of(rb * G, U, C);
-  const int nslots = static_cast<int>(owner_of(rb * G + G - 1, U, C) - first + 1);
-  const long row = rb * RB + rin;
+  const int t = static_cast<int>(blockIdx.x) * FIX_THREADS + threadIdx.x;
+  const int rin = t % RB;
+  const int tok = (t / RB) % M;
+  const int rb = t / (RB * M);
+  const int first = owner32(rb * G, U, C);
+  const int nslots = owner32(rb * G + G - 1, U, C) - first + 1;
+  const long row = static_cast<long>(rb) * RB + rin;
   pdl_wait();   // the GEMV's partial sums
   if (nslots <= tag || row >= N) return;
-  const unsigned long long* p = partials + (rb * S * M + tok) * RB + rin;
+  const unsigned long long* p = partials + (static_cast<long>(rb) * S * M + tok) * RB + rin;
   const long stride = static_cast<long>(M) * RB;   // one slot
   float sum = 0.f;
   int sl = 0;
@@ -807,6 +813,13 @@ size_t gemv_packed_bytes(int64_t N, int64_t K) {
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const GemvPlan p = make_plan(N, K, sm_count());
   return static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(unsigned long long);
+}
+
+// Whether a call at this shape ends with the fixup kernel: some row block is
+// shared by more CTAs than the main kernel sums in place.
+bool gemv_needs_fixup(int64_t M, int64_t N, int64_t K) {
+  const GemvPlan p = make_plan(N, K, sm_count());
+  return p.S > (M <= 8 ? tag_slots<1>() : tag_slots<2>());
 }
 
 // The fixup kernel over every (block, token, row), when some block is shared.

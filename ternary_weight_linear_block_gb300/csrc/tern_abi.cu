@@ -60,6 +60,13 @@ size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
   return 0;
 }
 
+int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (op == TERN_OP_GEMV) return gemv_needs_fixup(M, N, K) ? 2 : 1;
+  if (op == TERN_OP_GEMM) return 1;
+  return 0;
+}
+
 tern_status tern_workspace_init(void* ws, size_t bytes, void* stream) {
   if (bytes == 0) return TERN_OK;
   if (ws == nullptr) return TERN_ERR_INVALID_ARG;

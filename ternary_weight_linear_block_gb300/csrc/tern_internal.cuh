@@ -47,6 +47,7 @@ cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, 
                         cudaStream_t st);
 size_t gemv_packed_bytes(int64_t N, int64_t K);
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
+bool gemv_needs_fixup(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* xs, int64_t M,
                         int64_t N, int64_t K, uint16_t* y, void* ws, cudaStream_t st);
 cudaError_t launch_linear_decode(const uint16_t* x, const int8_t* sign, const uint8_t* packed,

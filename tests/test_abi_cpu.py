@@ -45,6 +45,25 @@ def test_sizes(lib):
     assert B.tern_workspace_bytes(B.TERN_OP_GEMV, 4, 34816, 5120) > 0
 
 
+def test_kernel_launch_counts(lib):
+    # 152 SMs (the host default with no device, and GB300's count)
+    G = B.TERN_OP_GEMV
+    assert B.tern_kernel_launches(G, 0, 34816, 5120) == 0
+    assert B.tern_kernel_launches(99, 4, 34816, 5120) == 0
+    assert B.tern_kernel_launches(B.TERN_OP_GEMM, 2048, 34816, 5120) == 1
+    # gate/up: 68 blocks x 40 groups over 152 CTAs (17.9 units each): a block
+    # has at most 4 owners, summed in place at M <= 8; any sharing at M > 8
+    assert B.tern_kernel_launches(G, 1, 34816, 5120) == 1
+    assert B.tern_kernel_launches(G, 8, 34816, 5120) == 1
+    assert B.tern_kernel_launches(G, 9, 34816, 5120) == 2
+    # down: 10 blocks x 136 groups -> about 16 owners per block
+    assert B.tern_kernel_launches(G, 1, 5120, 17408) == 2
+    # 152 blocks of 8 groups: one block per CTA, nothing shared
+    assert B.tern_kernel_launches(G, 16, 152 * 512, 1024) == 1
+    # one block of 8 groups split over 8 CTAs
+    assert B.tern_kernel_launches(G, 16, 512, 1024) == 2
+
+
 FAKE = 1 << 20          # an aligned, never dereferenced address
 
 
