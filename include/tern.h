@@ -248,17 +248,52 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
                                    uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
                                    void* stream);
 
+/* ------------------------------------------------------------------------
+ * tern_gemm_prefill_packed -- the same int8 prefill GEMM (page section 4)
+ * read straight from the decode's 2-bit packed weights and q, with no
+ * W_int8 in memory (page section 6 measured the run-time 2-bit -> int8
+ * expansion; here it happens in shared memory beside the tensor cores):
+ *     W_int8[n,k] = code[n,k] * q[n,k/128]     (formed on chip, never stored)
+ *     acc[m,n]    = sum_k xq[m,k] * W_int8[n,k]  (exact int32)
+ *     y[m,n]      = bf16_rn(((float)acc[m,n] * tscale[m]) * rscale[n])
+ * Results are bit-identical to tern_gemm_prefill_int8 on the same layer.
+ * The weights are read at 2 bits each (plus q) once per 128 tokens, so
+ * mid-size M costs the packed bytes instead of the 2-byte expanded weight.
+ *
+ *   xq      fp16 [M][K] (TERN_FWHT_I8 output), tscale fp32 [M]
+ *   packed  tern_pack's `packed` output (tern_packed_bytes(N, K) bytes)
+ *   q       int8 [N][G] and rscale fp32 [N] (tern_pack outputs)
+ *   y       bf16 [M][N]
+ *   acc     int32 [M][N] or NULL
+ *   ws      device workspace of tern_workspace_bytes(TERN_OP_GEMM_PACKED,
+ *           M, N, K) bytes (any contents; NULL when that is 0).  When the
+ *           128-token x 256-row tiles are too few to fill the GPU, each
+ *           tile's K range is split in S slices of whole 1024-chunks whose
+ *           exact int32 partial sums go to S planes [M][N] of ws; a second
+ *           kernel adds the planes (integer sums: the same result in any
+ *           order) and applies the rescale (tern_kernel_launches).
+ * Requirements: K % 1024 == 0, K <= 65536, N % 16 == 0, 0 <= M, N <= 2^24.
+ * Device-side waits are bounded; a wait that gives up makes the call's
+ * outputs undefined and is reported by tern_check().
+ * ---------------------------------------------------------------------- */
+tern_status tern_gemm_prefill_packed(const uint16_t* xq, const float* tscale,
+                                     const uint8_t* packed, const int8_t* q, const float* rscale,
+                                     int64_t M, int64_t N, int64_t K, uint16_t* y, int32_t* acc,
+                                     void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace sizing and initialisation. */
 #define TERN_OP_GEMV 1
 #define TERN_OP_GEMM 2
+#define TERN_OP_GEMM_PACKED 3
 size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
 /* Number of kernels one call launches at this shape on the current device
  * (0 for an empty call or an unknown op): for TERN_OP_GEMV the GEMV kernel,
  * plus the fixup kernel when a 512-row block is shared by more CTAs than the
  * GEMV sums in place (tern_gemv_decode, tern_linear_decode and
  * tern_gemv_decode_noalloc launch the same count); for TERN_OP_GEMM the one
- * int8 GEMM kernel.  Host-only; launch counting for CUDA-graph sizing and
- * profiling. */
+ * int8 GEMM kernel; for TERN_OP_GEMM_PACKED the GEMM, plus the rescale
+ * kernel when its tiles are split along K.  Host-only; launch counting for
+ * CUDA-graph sizing and profiling. */
 int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K);
 /* Zero-fill `bytes` of device memory at ws on `stream` (asynchronous). */
 tern_status tern_workspace_init(void* ws, size_t bytes, void* stream);

@@ -29,6 +29,7 @@ TERN_FWHT_DECODE = 1
 TERN_FWHT_I8 = 2
 TERN_OP_GEMV = 1
 TERN_OP_GEMM = 2
+TERN_OP_GEMM_PACKED = 3
 STATUS_NAMES = {0: "TERN_OK", 1: "TERN_ERR_INVALID_ARG", 2: "TERN_ERR_SHAPE", 3: "TERN_ERR_ALIGN",
                 4: "TERN_ERR_UNSUPPORTED", 5: "TERN_ERR_CUDA", 6: "TERN_ERR_WORKSPACE",
                 7: "TERN_ERR_TIMEOUT"}
@@ -48,6 +49,8 @@ _SIGS = {
     "tern_gemv_decode": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
     "tern_gemm_prefill_int8": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _p, _sz,
                                               _p]),
+    "tern_gemm_prefill_packed": (ctypes.c_int, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _p,
+                                                _p, _sz, _p]),
     "tern_check": (ctypes.c_int, [_p]),
     "tern_gemv_decode_noalloc": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
     "tern_linear_decode": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
@@ -156,6 +159,12 @@ def tern_gemm_prefill_int8(xq, tscale, w_q, rscale, m, n, k, y, acc=None, ws=Non
                  k, _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream))
 
 
+def tern_gemm_prefill_packed(xq, tscale, packed, q, rscale, m, n, k, y, acc=None, ws=None,
+                             ws_bytes=0, stream=None):
+    return _call("tern_gemm_prefill_packed", _ptr(xq), _ptr(tscale), _ptr(packed), _ptr(q),
+                 _ptr(rscale), m, n, k, _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream))
+
+
 def tern_check(stream=None):
     return _call("tern_check", _stream(stream))
 
@@ -195,8 +204,11 @@ class PackedLayer:
 
 
 def pack_layer(codes: torch.Tensor, scales: torch.Tensor, decode: bool = True,
-               prefill: bool = True, stream=None) -> PackedLayer:
-    """Run tern_pack on device codes (int8 [N,K]) and scales (fp16 [N,G])."""
+               prefill: bool = True, expand: bool = True, stream=None) -> PackedLayer:
+    """Run tern_pack on device codes (int8 [N,K]) and scales (fp16 [N,G]).
+    ``decode`` keeps the packed 2-bit units, ``prefill`` the scale split
+    (q, rscale) and, with ``expand``, the expanded int8 weight w_q; without
+    w_q, prefill reads the packed units (tern_gemm_prefill_packed)."""
     _need(codes, torch.int8, "codes")
     _need(scales, torch.float16, "scales")
     n, k = codes.shape
@@ -207,7 +219,8 @@ def pack_layer(codes: torch.Tensor, scales: torch.Tensor, decode: bool = True,
     if prefill:
         q = torch.empty((n, k // 128), dtype=torch.int8, device=dev)
         rs = torch.empty(n, dtype=torch.float32, device=dev)
-        wq = torch.empty((n, k), dtype=torch.float16, device=dev)
+        if expand:
+            wq = torch.empty((n, k), dtype=torch.float16, device=dev)
     tern_pack(codes, scales, n, k, packed, q, rs, wq, stream)
     return PackedLayer(n, k, packed, q, rs, wq)
 
@@ -318,12 +331,25 @@ class DecodeGraph:
 
 
 def prefill(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,
-            acc: torch.Tensor | None = None, sign=None, stream=None) -> torch.Tensor:
-    """Prefill forward: rotation + per-token int8 quantisation, then the GEMM."""
+            acc: torch.Tensor | None = None, sign=None, stream=None,
+            from_packed: bool | None = None, ws: Workspace | None = None) -> torch.Tensor:
+    """Prefill forward: rotation + per-token int8 quantisation, then the int8
+    GEMM, on the expanded weight w_q or (``from_packed``; the default when
+    the layer holds no w_q) straight from the packed units.  Both GEMMs give
+    bit-identical results."""
     m = x.shape[0]
+    if from_packed is None:
+        from_packed = layer.w_q is None
     xq, ts = fwht(x, TERN_FWHT_I8, sign, stream)
     if y is None:
         y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=x.device)
-    tern_gemm_prefill_int8(xq, ts, layer.w_q, layer.rscale, m, layer.n, layer.k, y, acc,
-                           stream=stream)
+    if from_packed:
+        nb = tern_workspace_bytes(TERN_OP_GEMM_PACKED, m, layer.n, layer.k)
+        buf = (ws or Workspace(x.device)).get(nb, stream) if nb > 0 else None
+        tern_gemm_prefill_packed(xq, ts, layer.packed, layer.q, layer.rscale, m, layer.n,
+                                 layer.k, y, acc, buf, 0 if buf is None else buf.numel(),
+                                 stream=stream)
+    else:
+        tern_gemm_prefill_int8(xq, ts, layer.w_q, layer.rscale, m, layer.n, layer.k, y, acc,
+                               stream=stream)
     return y

@@ -47,7 +47,9 @@ constexpr uint32_t WAIT_LIMIT = 1u << 26;
 constexpr uint32_t IDESC = ptx::idesc_f16_f32(BM, BN);
 constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
 
-enum : unsigned int { ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_EPILOGUE = 4u, ERR_DRAIN = 8u };
+enum : unsigned int {
+  ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_EPILOGUE = 4u, ERR_DRAIN = 8u, ERR_EXPAND = 16u
+};
 
 __device__ __forceinline__ void fail(volatile int* abort_flag, unsigned int code) {
   *abort_flag = 1;
@@ -270,6 +272,479 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// The same int8 GEMM straight from the decode's 2-bit packed weights: no
+// W_int8 is held in memory (section 6 of the page measured the run-time
+// 2-bit -> int8 expansion as 31 of 83 ms per step; here it runs in shared
+// memory, beside the tensor cores).
+//
+// Tile: 128 tokens (MMA M) x 256 weight rows (MMA N: half of a 512-row unit
+// of the packed format), 64-wide K stages -- the instruction shape of the
+// kernel above, since a tcgen05.mma costs about the same time at any N up to
+// 256.  Per 128-wide group the producer bulk-copies the 8 KB of codes of the
+// tile's 256 rows into a code ring and TMA-loads the tokens; four expansion
+// warps turn the codes into the exact int8 weight values code * q[n, g],
+// held in fp16 and written in the 128-byte-swizzled K-major layout the MMA
+// reads (the sign trick gives 2 code as fp16, times q/2: both exact).  MMA,
+// per-1024 chunk int32 conversion and epilogue are those of the kernel above.
+// Warp roles: 0 producer, 1 MMA issuer, 2 TMEM allocator, 3 idle, 4-11
+// epilogue, 12-15 expansion.  The 512 threads launch with 128 registers each;
+// the epilogue's 128 int32 sums per thread need more, so the warpgroups
+// re-split the block's registers with setmaxnreg (control 48, epilogue 168,
+// expansion 120 per thread); the launcher refuses to launch unless the kernel
+// was built with exactly 128 registers per thread, so the split always fits.
+constexpr int PBN = 256;                 // weight rows per tile
+constexpr int PUNIT_BYTES = 17408;       // one 512-row x 128-k unit of the packed format
+constexpr int PCODE_BYTES = 8192;        // codes of 256 rows (16 tiles of 16) of one unit
+constexpr int PSTAGES = 4;
+constexpr int PCSTAGES = 4;
+constexpr int PA_BYTES = BM * BK * 2;    // tokens
+constexpr int PB_BYTES = PBN * BK * 2;   // expanded weights
+constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr int P_THREADS = 512;
+constexpr int P_LAUNCH_REGS = 128;
+constexpr int P_REGS_CONTROL = 48, P_REGS_EPILOGUE = 168, P_REGS_EXPAND = 120;
+constexpr size_t PSMEM_BYTES =
+    static_cast<size_t>(PSTAGES) * PSTAGE_BYTES + PCSTAGES * PCODE_BYTES + 1024 + 512;
+static_assert(PSMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(PSTAGE_BYTES % 1024 == 0 && PA_BYTES % 1024 == 0, "stage alignment");
+static_assert(128 * P_REGS_CONTROL + 256 * P_REGS_EPILOGUE + 128 * P_REGS_EXPAND <=
+                  P_THREADS * P_LAUNCH_REGS,
+              "register split exceeds the block's launch allocation");
+
+template <int R>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+__global__ void __launch_bounds__(P_THREADS, 1)
+    gemm_packed_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t* __restrict__ packed,
+                       const int8_t* __restrict__ q, const float* __restrict__ tscale,
+                       const float* __restrict__ rscale, int M, int N, int K,
+                       __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out, int S,
+                       int32_t* __restrict__ part) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* scode = smem + PSTAGES * PSTAGE_BYTES;
+  uint64_t* afull = reinterpret_cast<uint64_t*>(scode + PCSTAGES * PCODE_BYTES);
+  uint64_t* wfull = afull + PSTAGES;
+  uint64_t* empty = wfull + PSTAGES;
+  uint64_t* cfull = empty + PSTAGES;
+  uint64_t* cempty = cfull + PCSTAGES;
+  uint64_t* dfull = cempty + PCSTAGES;
+  uint64_t* dempty = dfull + 2;
+  uint64_t* done = dempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = K / kGroup;
+  const int m_blocks = (M + BM - 1) / BM;
+  const int tiles = m_blocks * ((N + PBN - 1) / PBN);
+  const int units = tiles * S;   // unit = (tile, K slice of whole 128-groups)
+  // the tile and the group range [g0, g1) of a unit; the MMA accumulates it
+  // in pieces that end at every 1024-chunk boundary (and at g1), so each
+  // fp32 partial stays exact
+  auto unit_of = [&](int u, int& tile, int& g0, int& g1) {
+    tile = u / S;
+    const int sl = u % S;
+    g0 = sl * G / S;
+    g1 = (sl + 1) * G / S;
+  };
+  auto piece_end = [&](int gp, int g1) {
+    const int e = (gp / 8 + 1) * 8;
+    return e < g1 ? e : g1;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      ptx::mbar_init(&afull[s], 1);
+      ptx::mbar_init(&wfull[s], 4);   // one arrival per expansion warp
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int c = 0; c < PCSTAGES; ++c) {
+      ptx::mbar_init(&cfull[c], 1);
+      ptx::mbar_init(&cempty[c], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&dfull[b], 1);
+      ptx::mbar_init(&dempty[b], 8);   // one arrival per epilogue warp
+    }
+    ptx::mbar_init(done, 1);
+    *abort_flag = 0;
+    ptx::mbar_fence_init();
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) ptx::prefetch_tmap(&tmA);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_wait();   // xq / tscale come from the previous kernel
+  pdl_launch_dependents();
+
+  if (warp < 4) {
+    regs_dec<P_REGS_CONTROL>();
+    if (warp == 0 && lane == 0) {
+      // ---------------- producer: code groups (bulk) and token stages (TMA)
+      int s = 0, c = 0;
+      uint32_t ph = 0, cph = 0;
+      long a_issued = 0, c_issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        int tile, g0, g1;
+        unit_of(u, tile, g0, g1);
+        const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
+        const uint8_t* wsrc =
+            packed + static_cast<size_t>(n_blk >> 1) * G * PUNIT_BYTES + (n_blk & 1) * PCODE_BYTES;
+        for (int g = g0; g < g1 && ok; ++g) {
+          if (!ptx::mbar_wait(&cempty[c], cph ^ 1u, abort_flag, WAIT_LIMIT)) {
+            if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&cfull[c], PCODE_BYTES);
+          ptx::bulk_load(scode + c * PCODE_BYTES, wsrc + static_cast<size_t>(g) * PUNIT_BYTES,
+                         PCODE_BYTES, &cfull[c]);
+          ++c_issued;
+          if (++c == PCSTAGES) {
+            c = 0;
+            cph ^= 1u;
+          }
+          for (int h = 0; h < 2; ++h) {
+            if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, WAIT_LIMIT)) {
+              if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&afull[s], PA_BYTES);
+            ptx::tma_load_2d(smem + s * PSTAGE_BYTES, &tmA, &afull[s], g * kGroup + h * BK,
+                             m_blk * BM);
+            ++a_issued;
+            if (++s == PSTAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // let the copies still in flight land before the CTA exits
+        long back = a_issued < PSTAGES ? a_issued : PSTAGES;
+        for (long i = 0; i < back; ++i) {
+          if (--s < 0) {
+            s = PSTAGES - 1;
+            ph ^= 1u;
+          }
+          if (!ptx::mbar_wait_bounded(&afull[s], ph, WAIT_LIMIT)) atomicOr(&g_gemm_error, ERR_DRAIN);
+        }
+        back = c_issued < PCSTAGES ? c_issued : PCSTAGES;
+        for (long i = 0; i < back; ++i) {
+          if (--c < 0) {
+            c = PCSTAGES - 1;
+            cph ^= 1u;
+          }
+          if (!ptx::mbar_wait_bounded(&cfull[c], cph, WAIT_LIMIT)) atomicOr(&g_gemm_error, ERR_DRAIN);
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- MMA issuer (one thread)
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t cc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        int tile, g0, g1;
+        unit_of(u, tile, g0, g1);
+        for (int gp = g0; gp < g1 && ok; gp = piece_end(gp, g1), ++cc) {
+          const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
+          if (!ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag, WAIT_LIMIT)) {
+            if (!*abort_flag) fail(abort_flag, ERR_MMA);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem + buf * BN;
+          const int n_stages = 2 * (piece_end(gp, g1) - gp);
+          for (int j = 0; j < n_stages; ++j) {
+            if (!ptx::mbar_wait(&afull[s], ph, abort_flag, WAIT_LIMIT) ||
+                !ptx::mbar_wait(&wfull[s], ph, abort_flag, WAIT_LIMIT)) {
+              if (!*abort_flag) fail(abort_flag, ERR_MMA);
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t a0 = ptx::sw128_kmajor_desc(ptx::smem_u32(smem + s * PSTAGE_BYTES));
+            const uint64_t b0 =
+                ptx::sw128_kmajor_desc(ptx::smem_u32(smem + s * PSTAGE_BYTES + PA_BYTES));
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              ptx::mma_f16_ss(d_tmem, a0 + 2u * kk, b0 + 2u * kk, IDESC,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(&empty[s]);
+            if (++s == PSTAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          if (ok) ptx::mma_commit(&dfull[buf]);
+        }
+      }
+      ptx::mma_commit(done);
+      if (!ptx::mbar_wait_bounded(done, 0, WAIT_LIMIT)) atomicOr(&g_gemm_error, ERR_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp < 12) {
+    regs_inc<P_REGS_EPILOGUE>();
+    // ---------------- epilogue: warpgroup wg owns columns [128 wg, 128 wg + 128)
+    const int wg = (warp - 4) >> 2;
+    const int qd = warp & 3;   // TMEM lane quarter accessible to this warp
+    uint32_t cc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      int tile, g0, g1;
+      unit_of(u, tile, g0, g1);
+      const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
+      int32_t sums[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sums[i] = 0;
+      for (int gp = g0; gp < g1; gp = piece_end(gp, g1), ++cc) {
+        const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
+        if (!ptx::mbar_wait(&dfull[buf], dph, abort_flag, WAIT_LIMIT)) {
+          if (!*abort_flag) fail(abort_flag, ERR_EPILOGUE);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int piece = 0; piece < 4; ++piece) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * qd) << 16) + buf * BN +
+                                      wg * 128 + piece * 32,
+                                  v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            sums[piece * 32 + i] += __float2int_rn(__uint_as_float(v[i]));   // exact integers
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&dempty[buf]);
+      }
+      if (!ok) break;
+      const int row = m_blk * BM + 32 * qd + lane;
+      if (S > 1) {
+        // one K slice of the tile: store its exact partial sums in the
+        // slice's plane of the workspace; the rescale kernel adds the planes
+        if (row < M) {
+          const int n0 = n_blk * PBN + wg * 128;
+          int32_t* prow = part + (static_cast<long>(u % S) * M + row) * N + n0;
+#pragma unroll
+          for (int j = 0; j < 128; j += 8)
+            if (n0 + j < N) {
+              int4* pp = reinterpret_cast<int4*>(prow + j);
+              pp[0] = make_int4(sums[j], sums[j + 1], sums[j + 2], sums[j + 3]);
+              pp[1] = make_int4(sums[j + 4], sums[j + 5], sums[j + 6], sums[j + 7]);
+            }
+        }
+        continue;
+      }
+      if (row < M) {
+        const float ts = tscale[row];
+        const int n0 = n_blk * PBN + wg * 128;
+        __nv_bfloat16* yrow = y + static_cast<long>(row) * N;
+#pragma unroll
+        for (int j = 0; j < 128; j += 8) {
+          const int n = n0 + j;
+          if (n < N) {
+            const float4 r0 = __ldg(reinterpret_cast<const float4*>(rscale + n));
+            const float4 r1 = __ldg(reinterpret_cast<const float4*>(rscale + n + 4));
+            const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+            uint32_t packed_y[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float f0 = __fmul_rn(__fmul_rn(__int2float_rn(sums[j + 2 * t]), ts), rr[2 * t]);
+              const float f1 =
+                  __fmul_rn(__fmul_rn(__int2float_rn(sums[j + 2 * t + 1]), ts), rr[2 * t + 1]);
+              __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+              packed_y[t] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(yrow + n) =
+                make_uint4(packed_y[0], packed_y[1], packed_y[2], packed_y[3]);
+            if (acc_out != nullptr) {
+              int4* ap = reinterpret_cast<int4*>(acc_out + static_cast<long>(row) * N + n);
+              ap[0] = make_int4(sums[j], sums[j + 1], sums[j + 2], sums[j + 3]);
+              ap[1] = make_int4(sums[j + 4], sums[j + 5], sums[j + 6], sums[j + 7]);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    regs_dec<P_REGS_EXPAND>();
+    // ---------------- expansion: warp xw owns tiles xw + 4 u (u = 0..3) of the
+    // 16 16-row tiles of the half unit; lane = slot L = 4 r + c of the packed
+    // format
+    const int xw = warp - 12;
+    const int r = lane >> 2, cq = lane & 3;
+    // byte offset of (u = 0, row parity 0, chunk 0) inside a weight stage:
+    // row 16 xw + r, 4 c bytes into the 16-byte chunk; u adds 64 rows, the
+    // row parity 8 rows
+    const uint32_t row_off = static_cast<uint32_t>(PA_BYTES + (16 * xw + r) * 128 + 4 * cq);
+    uint32_t xo[8];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) xo[ch] = static_cast<uint32_t>((ch ^ r) << 4);
+    const uint32_t smem_base = ptx::smem_u32(smem);
+    int s = 0, c = 0;
+    uint32_t ph = 0, cph = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
+      int tile, g0, g1;
+      unit_of(unit, tile, g0, g1);
+      const int n_blk = tile / m_blocks;
+      // q of the thread's eight rows (slots u, row parities par); rows past N read row 0
+      const int8_t* qp[4][2];
+      bool qv_ok[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int par = 0; par < 2; ++par) {
+          const int n = n_blk * PBN + 16 * (xw + 4 * u) + r + 8 * par;
+          qv_ok[u][par] = n < N;
+          qp[u][par] = q + static_cast<long>(n < N ? n : 0) * G;
+        }
+      for (int g = g0; g < g1 && ok; ++g) {
+        int qv[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int par = 0; par < 2; ++par)
+            qv[u][par] = qv_ok[u][par] ? static_cast<int>(__ldg(qp[u][par] + g)) : 0;
+        if (!ptx::mbar_wait(&cfull[c], cph, abort_flag, WAIT_LIMIT)) {
+          if (!*abort_flag) fail(abort_flag, ERR_EXPAND);
+          ok = false;
+          break;
+        }
+        uint4 wv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          wv[u] = *reinterpret_cast<const uint4*>(scode + c * PCODE_BYTES + 512 * (xw + 4 * u) +
+                                                  16 * lane);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&cempty[c]);
+        if (++c == PCSTAGES) {
+          c = 0;
+          cph ^= 1u;
+        }
+        __half2 qh[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int par = 0; par < 2; ++par)
+            qh[u][par] = __half2half2(__float2half_rn(0.5f * static_cast<float>(qv[u][par])));
+        for (int h = 0; h < 2; ++h) {
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, WAIT_LIMIT)) {
+            if (!*abort_flag) fail(abort_flag, ERR_EXPAND);
+            ok = false;
+            break;
+          }
+          const uint32_t base = smem_base + s * PSTAGE_BYTES + row_off;
+#pragma unroll
+          for (int ii = 0; ii < 2; ++ii) {
+            // words 2h + ii hold k16 steps 4h + 2ii and 4h + 2ii + 1 of the group
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int chunk = 4 * ii + 2 * (e >> 2) + ((e >> 1) & 1);
+              const int par = e & 1;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t w =
+                    h == 0 ? (ii == 0 ? wv[u].x : wv[u].y) : (ii == 0 ? wv[u].z : wv[u].w);
+                const uint32_t two_code = (w << (14 - 2 * e)) & 0xC000C000u;
+                __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&two_code), qh[u][par]);
+                ptx::st_shared_b32(base + xo[chunk] + 8192u * u + 1024u * par,
+                                   *reinterpret_cast<uint32_t*>(&v));
+              }
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&wfull[s]);
+          if (++s == PSTAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// After a split-K packed GEMM: acc = the sum of the S slices' exact partial
+// sums (int32, any order gives the same integer), then y = bf16_rn((acc *
+// tscale[m]) * rscale[n]) with the epilogue's arithmetic; one thread per 8
+// outputs of a row (N % 16 == 0).
+constexpr int FIN_THREADS = 256;
+__global__ void __launch_bounds__(FIN_THREADS)
+    packed_finalize_kernel(const int32_t* __restrict__ part, int S,
+                           const float* __restrict__ tscale, const float* __restrict__ rscale,
+                           int M, int N, __nv_bfloat16* __restrict__ y,
+                           int32_t* __restrict__ acc_out) {
+  pdl_launch_dependents();
+  const long i = static_cast<long>(blockIdx.x) * FIN_THREADS + threadIdx.x;
+  const long per_row = N / 8;
+  const long row = i / per_row;
+  const int n = static_cast<int>(i % per_row) * 8;
+  pdl_wait();   // the GEMM's partial sums
+  if (row >= M) return;
+  int aa[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int sl = 0; sl < S; ++sl) {
+    const int32_t* p = part + (static_cast<long>(sl) * M + row) * N + n;
+    const int4 a0 = __ldcs(reinterpret_cast<const int4*>(p));
+    const int4 a1 = __ldcs(reinterpret_cast<const int4*>(p + 4));
+    aa[0] += a0.x; aa[1] += a0.y; aa[2] += a0.z; aa[3] += a0.w;
+    aa[4] += a1.x; aa[5] += a1.y; aa[6] += a1.z; aa[7] += a1.w;
+  }
+  const float4 r0 = __ldg(reinterpret_cast<const float4*>(rscale + n));
+  const float4 r1 = __ldg(reinterpret_cast<const float4*>(rscale + n + 4));
+  const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+  const float ts = tscale[row];
+  uint32_t out[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float f0 = __fmul_rn(__fmul_rn(__int2float_rn(aa[2 * t]), ts), rr[2 * t]);
+    const float f1 = __fmul_rn(__fmul_rn(__int2float_rn(aa[2 * t + 1]), ts), rr[2 * t + 1]);
+    __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+    out[t] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(y + row * N + n) = make_uint4(out[0], out[1], out[2], out[3]);
+  if (acc_out != nullptr) {
+    int4* ap = reinterpret_cast<int4*>(acc_out + row * N + n);
+    ap[0] = make_int4(aa[0], aa[1], aa[2], aa[3]);
+    ap[1] = make_int4(aa[4], aa[5], aa[6], aa[7]);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -327,6 +802,60 @@ cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t*
   return launch(gemm_i8_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, tscale,
                 rscale, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                 reinterpret_cast<__nv_bfloat16*>(y), acc);
+}
+
+// K slices per tile of the packed GEMM: 1 when the tiles alone fill most of
+// the GPU, else as many slices (of whole 128-groups) as keep one unit per SM.
+int packed_splits(int64_t M, int64_t N, int64_t K) {
+  const long tiles = ((M + BM - 1) / BM) * ((N + PBN - 1) / PBN);
+  const long sms = sm_count();
+  if (4 * tiles >= 3 * sms) return 1;
+  const long want = sms / tiles;
+  const long groups = K / kGroup;
+  return static_cast<int>(want < groups ? want : groups);
+}
+
+size_t gemm_packed_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int S = packed_splits(M, N, K);
+  return S > 1 ? static_cast<size_t>(S) * M * N * sizeof(int32_t) : 0;
+}
+
+cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const uint8_t* packed,
+                               const int8_t* q, const float* rscale, int64_t M, int64_t N,
+                               int64_t K, uint16_t* y, int32_t* acc, void* ws, cudaStream_t st) {
+  static int regs_ok = 0;   // 0 unknown, 1 built with the launch allocation the split needs
+  if (regs_ok == 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, gemm_packed_kernel);
+    if (e != cudaSuccess) return e;
+    regs_ok = fa.numRegs == P_LAUNCH_REGS ? 1 : -1;
+    if (regs_ok > 0) {
+      e = cudaFuncSetAttribute(gemm_packed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(PSMEM_BYTES));
+      if (e != cudaSuccess) {
+        regs_ok = 0;
+        return e;
+      }
+    }
+  }
+  // never launch a register split that may not fit the block's allocation
+  if (regs_ok < 0) return cudaErrorNotSupported;
+  CUtensorMap ta;
+  if (!make_map(&ta, xq, M, K, BM)) return cudaErrorInvalidValue;
+  const int S = packed_splits(M, N, K);
+  int32_t* part = S > 1 ? static_cast<int32_t*>(ws) : nullptr;
+  const long units = ((M + BM - 1) / BM) * ((N + PBN - 1) / PBN) * S;
+  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
+  cudaError_t e = launch(gemm_packed_kernel, dim3(grid), dim3(P_THREADS), PSMEM_BYTES, st, ta,
+                         packed, q, tscale, rscale, static_cast<int>(M), static_cast<int>(N),
+                         static_cast<int>(K), reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
+  if (e != cudaSuccess || S == 1) return e;
+  const long threads = M * N / 8;
+  return launch(packed_finalize_kernel, dim3(static_cast<unsigned>((threads + FIN_THREADS - 1) /
+                                                                   FIN_THREADS)),
+                dim3(FIN_THREADS), 0, st, static_cast<const int32_t*>(part), S, tscale, rscale,
+                static_cast<int>(M), static_cast<int>(N), reinterpret_cast<__nv_bfloat16*>(y),
+                acc);
 }
 
 cudaError_t gemm_read_clear_error(unsigned int* err) {

@@ -57,6 +57,7 @@ size_t tern_packed_bytes(int64_t N, int64_t K) {
 size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == TERN_OP_GEMV) return gemv_workspace_bytes(M, N, K);
+  if (op == TERN_OP_GEMM_PACKED) return gemm_packed_workspace_bytes(M, N, K);
   return 0;
 }
 
@@ -64,6 +65,7 @@ int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == TERN_OP_GEMV) return gemv_needs_fixup(M, N, K) ? 2 : 1;
   if (op == TERN_OP_GEMM) return 1;
+  if (op == TERN_OP_GEMM_PACKED) return packed_splits(M, N, K) > 1 ? 2 : 1;
   return 0;
 }
 
@@ -155,6 +157,7 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
   if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
   if (N % 16 != 0) return TERN_ERR_SHAPE;
   if (M > (int64_t(1) << 24) || N > (int64_t(1) << 24)) return TERN_ERR_SHAPE;
+  if ((M + 127) / 128 * ((N + 255) / 256) >= (int64_t(1) << 31)) return TERN_ERR_SHAPE;  // tile count
   if (M == 0 || N == 0) return TERN_OK;
   if (xq == nullptr || tscale == nullptr || w_q == nullptr || rscale == nullptr || y == nullptr)
     return TERN_ERR_INVALID_ARG;
@@ -164,6 +167,31 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
   if (!device_supported()) return TERN_ERR_UNSUPPORTED;
   return from_cuda(launch_gemm(xq, tscale, w_q, rscale, M, N, K, y, acc,
                                static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_gemm_prefill_packed(const uint16_t* xq, const float* tscale,
+                                     const uint8_t* packed, const int8_t* q, const float* rscale,
+                                     int64_t M, int64_t N, int64_t K, uint16_t* y, int32_t* acc,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
+  if (M > (int64_t(1) << 24) || N > (int64_t(1) << 24)) return TERN_ERR_SHAPE;
+  if (N % 16 != 0) return TERN_ERR_SHAPE;
+  if ((M + 127) / 128 * ((N + 255) / 256) >= (int64_t(1) << 31)) return TERN_ERR_SHAPE;  // tile count
+  if (M == 0 || N == 0) return TERN_OK;
+  if (xq == nullptr || tscale == nullptr || packed == nullptr || q == nullptr ||
+      rscale == nullptr || y == nullptr)
+    return TERN_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(tscale) || !aligned16(packed) || !aligned16(q) ||
+      !aligned16(rscale) || !aligned16(y) || (acc && !aligned16(acc)))
+    return TERN_ERR_ALIGN;
+  if (gemm_packed_workspace_bytes(M, N, K) > 0 &&
+      (ws == nullptr || ws_bytes < gemm_packed_workspace_bytes(M, N, K)))
+    return TERN_ERR_WORKSPACE;
+  if (ws != nullptr && !aligned16(ws)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_gemm_packed(xq, tscale, packed, q, rscale, M, N, K, y, acc, ws,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 tern_status tern_check(void* stream) {

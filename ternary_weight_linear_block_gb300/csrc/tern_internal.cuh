@@ -56,6 +56,11 @@ cudaError_t launch_linear_decode(const uint16_t* x, const int8_t* sign, const ui
 cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
                         const float* rscale, int64_t M, int64_t N, int64_t K, uint16_t* y,
                         int32_t* acc, cudaStream_t st);
+size_t gemm_packed_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int packed_splits(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const uint8_t* packed,
+                               const int8_t* q, const float* rscale, int64_t M, int64_t N,
+                               int64_t K, uint16_t* y, int32_t* acc, void* ws, cudaStream_t st);
 // Read and clear the device error word of the GEMV / GEMM translation unit.
 cudaError_t gemv_read_clear_error(unsigned int* err);
 cudaError_t gemm_read_clear_error(unsigned int* err);

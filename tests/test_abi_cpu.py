@@ -62,6 +62,14 @@ def test_kernel_launch_counts(lib):
     assert B.tern_kernel_launches(G, 16, 152 * 512, 1024) == 1
     # one block of 8 groups split over 8 CTAs
     assert B.tern_kernel_launches(G, 16, 512, 1024) == 2
+    # the packed GEMM: 16 x 136 tiles fill the GPU; down at 128 tokens has
+    # 20 tiles, split along K (a second, rescale kernel and an int32 workspace)
+    P = B.TERN_OP_GEMM_PACKED
+    assert B.tern_kernel_launches(P, 2048, 34816, 5120) == 1
+    assert B.tern_workspace_bytes(P, 2048, 34816, 5120) == 0
+    assert B.tern_kernel_launches(P, 128, 5120, 17408) == 2
+    # 20 tiles -> 7 slices of whole 128-groups (140 units), one int32 plane each
+    assert B.tern_workspace_bytes(P, 128, 5120, 17408) == 7 * 128 * 5120 * 4
 
 
 FAKE = 1 << 20          # an aligned, never dereferenced address
