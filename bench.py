@@ -360,12 +360,21 @@ def run_prefill(args, local, m=2048):
             B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y,
                                      stream=st)
 
+        nbp = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, layer.n, layer.k)
+        wsp = B.Workspace().get(nbp) if nbp else None
+
+        def packed_only():
+            B.tern_gemm_prefill_packed(xq, ts, lay.packed, lay.q, lay.rscale, m, layer.n,
+                                       layer.k, y, None, wsp, nbp, stream=st)
+
         for _ in range(max(3, args.warmup // 4)):
             step()
+            packed_only()
         torch.cuda.synchronize()
         n = 20
         t = _time_region(step, n, stream, 1)
         tg = _time_region(gemm_only, n, stream, 1)
+        tp = _time_region(packed_only, n, stream, 1)
         B.tern_check(stream)
     ops = 2.0 * m * layer.n * layer.k
     del lay
@@ -379,10 +388,66 @@ def run_prefill(args, local, m=2048):
                          "avg_launch_us": round(tg / n * 1e6, 2), "traffic": None,
                          "peak_source": f"{peak_kind} bf16_tflops (MEASURED_PEAKS.json): the "
                                         "int8 values run on the fp16/bf16 tensor pipe; "
-                                        "sm_103a has no tcgen05 int8 kind"}}
+                                        "sm_103a has no tcgen05 int8 kind"},
+            "packed": {"kernel": "tern_gemm_prefill_packed (no expanded weight in memory)",
+                       "achieved": round(ops * n / tp / 1e12, 1), "unit": "TFLOP/s",
+                       "frac": round(ops * n / tp / 1e12 / tc_peak, 4),
+                       "avg_launch_us": round(tp / n * 1e6, 2),
+                       "weight_bytes": layer.n * layer.k // 4 + layer.n * (layer.k // 128) * 3,
+                       "expanded_weight_bytes": layer.n * layer.k * 2}}
 
 
-def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 16), prefill_ms=(512, 2048)):
+def run_mid_m(args, local, ms=(32, 64, 128, 256)):
+    """Mid-size M (17..256 tokens) through each linear shape: the packed GEMM
+    (2-bit weights, split along K when its tiles do not fill the GPU) against
+    the GEMM on the expanded weight; GEMM alone, weights rotating over copies
+    larger than L2, bit-identical outputs."""
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    out = []
+    with torch.cuda.stream(stream):
+        st = stream.cuda_stream
+        for shp in I.STACK_LAYERS:
+            # both weight forms rotate over more than twice the L2
+            copies = max(2, int(np.ceil(2 * L2_BYTES / B.tern_packed_bytes(shp.n, shp.k))))
+            lays = _make_layers(shp, copies, seed=11, prefill=True)
+            for m in ms:
+                xq = torch.randint(-127, 128, (m, shp.k), device="cuda").half()
+                ts = torch.full((m,), 1e-3, device="cuda")
+                y = torch.empty((m, shp.n), dtype=torch.bfloat16, device="cuda")
+                nb = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, shp.n, shp.k)
+                wsb = B.Workspace().get(nb) if nb else None
+                i = [0]
+
+                def packed():
+                    l = lays[i[0] % copies]
+                    i[0] += 1
+                    B.tern_gemm_prefill_packed(xq, ts, l.packed, l.q, l.rscale, m, shp.n, shp.k,
+                                               y, None, wsb, nb, stream=st)
+
+                def expanded():
+                    l = lays[i[0] % copies]
+                    i[0] += 1
+                    B.tern_gemm_prefill_int8(xq, ts, l.w_q, l.rscale, m, shp.n, shp.k, y,
+                                             stream=st)
+
+                for f in (packed, expanded):
+                    for _ in range(3):
+                        f()
+                reps = 30
+                tp = _time_region(packed, reps, stream, 1) / reps
+                te = _time_region(expanded, reps, stream, 1) / reps
+                out.append({"linear": shp.name, "M": m, "packed_us": round(tp * 1e6, 2),
+                            "expanded_us": round(te * 1e6, 2),
+                            "packed_launches": B.tern_kernel_launches(B.TERN_OP_GEMM_PACKED, m,
+                                                                      shp.n, shp.k)})
+            del lays
+            torch.cuda.empty_cache()
+        B.tern_check(stream)
+    return out
+
+
+def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 16), prefill_ms=(128, 512, 2048)):
     """The 64-layer linear stack of a 27B hybrid model: per layer qkv
     5120->10240, o 5120->5120, gate/up 5120->34816, down 17408->5120, each with
     its own seeded weights (seed = 4 * layer + linear).  The linears are not
@@ -458,23 +523,36 @@ def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 16), prefill_ms=(512, 2
             ts = [torch.empty(m, dtype=torch.float32, device="cuda") for shp in shapes]
             ys = [torch.empty((m, shp.n), dtype=torch.bfloat16, device="cuda") for shp in shapes]
 
-            def prefill_step():
+            nbs = [B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, shp.n, shp.k)
+                   for shp in shapes]
+            wsp = B.Workspace().get(max(nbs)) if max(nbs) else None
+
+            def prefill_step(packed=False):
                 for row in layers:
                     for si, (shp, lay) in enumerate(zip(shapes, row)):
                         B.tern_fwht_quant(xs_in[si], m, shp.k, None, B.TERN_FWHT_I8, xq[si],
                                           ts[si], st)
-                        B.tern_gemm_prefill_int8(xq[si], ts[si], lay.w_q, lay.rscale, m, shp.n,
-                                                 shp.k, ys[si], stream=st)
+                        if packed:
+                            B.tern_gemm_prefill_packed(xq[si], ts[si], lay.packed, lay.q,
+                                                       lay.rscale, m, shp.n, shp.k, ys[si], None,
+                                                       wsp, nbs[si], stream=st)
+                        else:
+                            B.tern_gemm_prefill_int8(xq[si], ts[si], lay.w_q, lay.rscale, m,
+                                                     shp.n, shp.k, ys[si], stream=st)
 
             prefill_step()
+            prefill_step(packed=True)
             torch.cuda.synchronize()
             reps = 3
             t = _time_region(prefill_step, reps, stream, 1)
+            tp = _time_region(lambda: prefill_step(packed=True), reps, stream, 1)
             B.tern_check(stream)
             tops = ops_step * m * reps / t / 1e12
             out["prefill"].append({"M": m, "ms_per_step": round(t / reps * 1e3, 3),
                                    "TOPS": round(tops, 1),
-                                   "frac_of_bf16_peak": round(tops / tc_peak, 4)})
+                                   "frac_of_bf16_peak": round(tops / tc_peak, 4),
+                                   "packed_ms_per_step": round(tp / reps * 1e3, 3),
+                                   "packed_TOPS": round(ops_step * m * reps / tp / 1e12, 1)})
             del xq, ys
     del layers
     torch.cuda.empty_cache()
@@ -571,6 +649,8 @@ def main():
     torch.cuda.empty_cache()
     if not args.no_prefill:
         line["prefill"] = run_prefill(args, local)
+    if not args.no_prefill and rank == 0:
+        line["mid_m"] = run_mid_m(args, local)
     if not args.no_stack and rank == 0:
         line["stack"] = run_stack(args, local)
     if rank == 0:
