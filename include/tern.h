@@ -148,6 +148,54 @@ tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_
                             int mode, void* out, float* out_scale, void* stream);
 
 /* ------------------------------------------------------------------------
+ * K-split tensor parallelism (page section 1, "TP=2 への移植"): when a
+ * row-parallel layer's input width is split over ranks, a shard boundary
+ * may fall in the middle of a 1024-block (down 17408 over 2 ranks: 8704 =
+ * 8.5 blocks).  Each rank transforms its own 512-element half with H512,
+ * the ranks exchange those halves (an all-gather), and the rank holding the
+ * first half takes their sum, the rank holding the second half their
+ * difference (the split identity H1024[a;b] = [H512 a + H512 b ; H512 a -
+ * H512 b], which is the last butterfly stage), times 1/32.  The rotated
+ * values are then bit for bit those of the whole-width rotation.
+ *
+ * A rank's shard x: bf16 [M][Kr] (dense rows, Kr = 1024 nb + 512 (lead +
+ * trail)): an optional leading half (the second half of a block shared with
+ * the previous rank), nb whole blocks, an optional trailing half (the first
+ * half of a block shared with the next rank).  Its padded layout, of width
+ * Kp = 1024 (nb + lead + trail), is [lead block] [nb whole blocks] [trail
+ * block]; in a padded half block the rank's 512 values come first and the
+ * other 512 are zero (the rank's weights get 512 zero columns there, so the
+ * GEMV and GEMM run unchanged on Kp).
+ *
+ * tern_fwht_shard -- the rank-local part: whole blocks rotated into
+ *   xr (fp32 [M][Kp], at their padded positions; the half blocks' places are
+ *   left for tern_fwht_combine), and the unnormalised H512 (canonical stages
+ *   of stride 1 .. 256, fp32) of the leading / trailing half into
+ *   h_lead / h_trail (fp32 [M][512]; NULL when that half is absent).
+ *   sign: int8 [Kr] of +-1 for the shard's columns, or NULL.
+ *   Requirements: lead, trail in {0,1}; Kr - 512 (lead + trail) a
+ *   non-negative multiple of 1024; Kp <= 65536; M Kp < 2^31.
+ * tern_fwht_combine -- one split block after the exchange: h_first is the
+ *   H512 of the block's first half (from the rank that holds it), h_second
+ *   of its second half; part 0 (this rank holds the first half) writes
+ *   (h_first + h_second) / 32, part 1 writes (h_first - h_second) / 32, into
+ *   xr[:, 1024 blk .. 1024 blk + 511] of the padded layout (width Kp), and
+ *   zeros into xr[:, 1024 blk + 512 .. 1024 blk + 1023].
+ * tern_quant_rotated -- quantise rotated fp32 activations xr [M][K]
+ *   (K % 1024 == 0) exactly as tern_fwht_quant does after its rotation:
+ *   mode TERN_FWHT_DECODE (fp16 + per-block factors) or TERN_FWHT_I8 (xq +
+ *   per-token tscale).  After a K split each rank quantises its own padded
+ *   shard (per-token int8 scales are the rank's own).
+ * ---------------------------------------------------------------------- */
+tern_status tern_fwht_shard(const uint16_t* x, int64_t M, int64_t Kr, int lead, int trail,
+                            const int8_t* sign, float* xr, float* h_lead, float* h_trail,
+                            void* stream);
+tern_status tern_fwht_combine(const float* h_first, const float* h_second, int64_t M, int part,
+                              float* xr, int64_t Kp, int64_t blk, void* stream);
+tern_status tern_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, void* out,
+                               float* out_scale, void* stream);
+
+/* ------------------------------------------------------------------------
  * tern_gemv_decode -- decode GEMV for 1 <= M <= 16 tokens:
  *     y[m,n] = bf16_rn( sum_g s[n,g] * sum_{k in g} code[n,k] * xr[m,k] )
  * computed from the packed weights and the TERN_FWHT_DECODE operand with fp16

@@ -25,6 +25,7 @@ O1 (exact, fp64)        rotate_f64 / dequant_f64 / linear_f64
 O2 (int8 path, spec-exact fp32 operation sequence)
                         fwht_f32 / quant_tokens / decompose_scales /
                         w_int8 / acc_int8 / y_int8 / linear_int8
+K split (section 1)     fwht_half_f32 / ksplit_combine / ksplit_rotate_f32
 
 plus the 2-bit storage format (pack_weights / unpack_weights) and the fp16
 decode operand (decode_operand), which the pages leave open and this library
@@ -131,6 +132,80 @@ def fwht_f32(x, sign=None) -> np.ndarray:
         h *= 2
     v = v * np.float32(INV_SQRT_BLOCK)
     return v.reshape(m, k).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# K split over ranks with the half-block exchange (the page's section 1)
+# --------------------------------------------------------------------------
+
+HALF = HBLOCK // 2
+
+
+def fwht_half_f32(x) -> np.ndarray:
+    """Unnormalised H512 of each 512-element row in fp32: the butterfly
+    stages of stride 1, 2, ..., 256 of the canonical order, i.e. what one rank
+    computes on its half of a block that the K split cuts in the middle
+    (the page's section 1).  x: [M, 512]."""
+    v = np.asarray(x, dtype=np.float32).copy()
+    m = v.shape[0]
+    if v.shape[1] != HALF:
+        raise ValueError("rows of 512 elements expected")
+    h = 1
+    while h < HALF:
+        w = v.reshape(m, HALF // (2 * h), 2, h)
+        lo = w[:, :, 0, :]
+        hi = w[:, :, 1, :]
+        v = np.stack([lo + hi, lo - hi], axis=2).reshape(m, HALF)
+        h *= 2
+    return v
+
+
+def ksplit_combine(h_first, h_second, part) -> np.ndarray:
+    """The exchange of the page's section 1: with a = H512 of a block's first
+    half and b = H512 of its second half, H1024 [a; b] = [a + b ; a - b]; the
+    rank that holds the first half keeps (a + b) / 32 (part 0), the rank that
+    holds the second half keeps (a - b) / 32 (part 1).  fp32."""
+    a = np.asarray(h_first, dtype=np.float32)
+    b = np.asarray(h_second, dtype=np.float32)
+    v = (a + b) if part == 0 else (a - b)
+    return (v * np.float32(INV_SQRT_BLOCK)).astype(np.float32)
+
+
+def ksplit_rotate_f32(x, world: int, sign=None):
+    """Rotation of x [M, K] whose columns are split in `world` equal
+    contiguous shards (K / world a multiple of 512), as the page's section 1
+    runs it: each rank rotates its whole blocks itself (fwht_f32), a block cut
+    in the middle is transformed half by half on its two ranks
+    (fwht_half_f32), the halves are exchanged, and each rank combines them
+    (ksplit_combine).  Returns the ranks' rotated columns, in order."""
+    x = np.asarray(x, dtype=np.float32)
+    if sign is not None:
+        x = x * np.asarray(sign, dtype=np.float32)[None, :]
+    m, k = x.shape
+    if k % world or (k // world) % HALF:
+        raise ValueError("each shard must be a whole number of half blocks")
+    kr = k // world
+    bounds = [(r * kr, (r + 1) * kr) for r in range(world)]
+    # every rank's transform of each half block it holds (rank-local step)
+    halves = {}
+    for r, (k0, k1) in enumerate(bounds):
+        if k0 % HBLOCK:
+            halves[(r, "lead")] = fwht_half_f32(x[:, k0:k0 + HALF])
+        if k1 % HBLOCK:
+            halves[(r, "trail")] = fwht_half_f32(x[:, k1 - HALF:k1])
+    out = []
+    for r, (k0, k1) in enumerate(bounds):
+        parts = []
+        if k0 % HBLOCK:   # second half of a block shared with rank r - 1
+            parts.append(ksplit_combine(halves[(r - 1, "trail")], halves[(r, "lead")], 1))
+        a = k0 + (HALF if k0 % HBLOCK else 0)
+        b = k1 - (HALF if k1 % HBLOCK else 0)
+        if b > a:
+            parts.append(fwht_f32(x[:, a:b]))
+        if k1 % HBLOCK:   # first half of a block shared with rank r + 1
+            parts.append(ksplit_combine(halves[(r, "trail")], halves[(r + 1, "lead")], 0))
+        out.append(np.concatenate(parts, axis=1))
+    return out
 
 
 # --------------------------------------------------------------------------

@@ -47,6 +47,10 @@ _SIGS = {
     "tern_pack": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p]),
     "tern_fwht_quant": (ctypes.c_int, [_p, _i64, _i64, _p, ctypes.c_int, _p, _p, _p]),
     "tern_gemv_decode": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
+    "tern_fwht_shard": (ctypes.c_int, [_p, _i64, _i64, ctypes.c_int, ctypes.c_int, _p, _p, _p, _p,
+                                       _p]),
+    "tern_fwht_combine": (ctypes.c_int, [_p, _p, _i64, ctypes.c_int, _p, _i64, _i64, _p]),
+    "tern_quant_rotated": (ctypes.c_int, [_p, _i64, _i64, ctypes.c_int, _p, _p, _p]),
     "tern_gemm_prefill_int8": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _p, _sz,
                                               _p]),
     "tern_gemm_prefill_packed": (ctypes.c_int, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _p,
@@ -163,6 +167,21 @@ def tern_gemm_prefill_packed(xq, tscale, packed, q, rscale, m, n, k, y, acc=None
                              ws_bytes=0, stream=None):
     return _call("tern_gemm_prefill_packed", _ptr(xq), _ptr(tscale), _ptr(packed), _ptr(q),
                  _ptr(rscale), m, n, k, _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def tern_fwht_shard(x, m, kr, lead, trail, sign, xr, h_lead, h_trail, stream=None):
+    return _call("tern_fwht_shard", _ptr(x), m, kr, int(lead), int(trail), _ptr(sign), _ptr(xr),
+                 _ptr(h_lead), _ptr(h_trail), _stream(stream))
+
+
+def tern_fwht_combine(h_first, h_second, m, part, xr, kp, blk, stream=None):
+    return _call("tern_fwht_combine", _ptr(h_first), _ptr(h_second), m, part, _ptr(xr), kp, blk,
+                 _stream(stream))
+
+
+def tern_quant_rotated(xr, m, k, mode, out, out_scale, stream=None):
+    return _call("tern_quant_rotated", _ptr(xr), m, k, mode, _ptr(out), _ptr(out_scale),
+                 _stream(stream))
 
 
 def tern_check(stream=None):

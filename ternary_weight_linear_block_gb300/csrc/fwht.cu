@@ -114,7 +114,196 @@ __global__ void __launch_bounds__(256) fwht_i8_kernel(const uint16_t* __restrict
   }
 }
 
+// ---------------------------------------------------------------------------
+// K-split tensor parallelism (page section 1): a rank's shard of the input
+// columns may start and/or end in the middle of a 1024-block.  The shard's
+// whole blocks are rotated as usual (fp32, written to their place in the
+// rank's padded layout: [lead block] [whole blocks] [trail block]); each half
+// block gets the unnormalised H512 of its 512 values, which the ranks then
+// exchange.
+
+// One warp per (token, task): task 0 is the leading half (if any), the last
+// task the trailing half (if any), the others the whole blocks.
+__global__ void __launch_bounds__(128) fwht_shard_kernel(
+    const uint16_t* __restrict__ x, int M, int Kr, int lead, int trail,
+    const int8_t* __restrict__ sign, float* __restrict__ xr, int Kp, float* __restrict__ h_lead,
+    float* __restrict__ h_trail) {
+  const int lane = threadIdx.x & 31;
+  const int nb = (Kr - 512 * (lead + trail)) / kHBlock;
+  const int T = nb + lead + trail;
+  const long wid = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  pdl_launch_dependents();
+  pdl_wait();
+  if (wid >= static_cast<long>(M) * T) return;
+  const int m = static_cast<int>(wid / T);
+  const int t = static_cast<int>(wid % T);
+  const uint16_t* xm = x + static_cast<long>(m) * Kr;
+  const bool is_lead = lead && t == 0;
+  const bool is_trail = trail && t == T - 1;
+  if (is_lead || is_trail) {
+    const int off = is_lead ? 0 : Kr - 512;
+    float v[2][8];
+    load_half(xm + off, sign ? sign + off : nullptr, lane, v);
+    fwht_512_unscaled(v, lane);
+    float* o = (is_lead ? h_lead : h_trail) + static_cast<long>(m) * 512;
+#pragma unroll
+    for (int ih = 0; ih < 2; ++ih) {
+      float4* p = reinterpret_cast<float4*>(o + ih * 256 + lane * 8);
+      p[0] = make_float4(v[ih][0], v[ih][1], v[ih][2], v[ih][3]);
+      p[1] = make_float4(v[ih][4], v[ih][5], v[ih][6], v[ih][7]);
+    }
+    return;
+  }
+  const int j = t - lead;
+  const int off = 512 * lead + j * kHBlock;
+  float v[4][8];
+  load_block(xm + off, sign ? sign + off : nullptr, lane, v);
+  fwht_1024(v, lane);
+  float* o = xr + static_cast<long>(m) * Kp + static_cast<long>(lead + j) * kHBlock;
+#pragma unroll
+  for (int ih = 0; ih < 4; ++ih) {
+    float4* p = reinterpret_cast<float4*>(o + ih * 256 + lane * 8);
+    p[0] = make_float4(v[ih][0], v[ih][1], v[ih][2], v[ih][3]);
+    p[1] = make_float4(v[ih][4], v[ih][5], v[ih][6], v[ih][7]);
+  }
+}
+
+// The exchanged halves of one split block -> this rank's half of the rotated
+// block: the stride-512 butterfly (first half: a + b, second half: a - b),
+// then * 1/32, written to padded block `blk`; the block's other 512 entries
+// (the peer's half) are set to 0.  One thread per 4 values of a token.
+__global__ void __launch_bounds__(256) fwht_combine_kernel(
+    const float* __restrict__ h_first, const float* __restrict__ h_second, int M, int part,
+    float* __restrict__ xr, int Kp, int blk) {
+  const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;   // (m, quad)
+  pdl_launch_dependents();
+  pdl_wait();
+  if (i >= static_cast<long>(M) * 128) return;
+  const long m = i / 128;
+  const int qd = static_cast<int>(i % 128);
+  const float4 a = reinterpret_cast<const float4*>(h_first + m * 512)[qd];
+  const float4 b = reinterpret_cast<const float4*>(h_second + m * 512)[qd];
+  float4 r;
+  if (part == 0) {
+    r = make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z),
+                    __fadd_rn(a.w, b.w));
+  } else {
+    r = make_float4(__fsub_rn(a.x, b.x), __fsub_rn(a.y, b.y), __fsub_rn(a.z, b.z),
+                    __fsub_rn(a.w, b.w));
+  }
+  r = make_float4(__fmul_rn(r.x, 0.03125f), __fmul_rn(r.y, 0.03125f), __fmul_rn(r.z, 0.03125f),
+                  __fmul_rn(r.w, 0.03125f));
+  float* o = xr + m * Kp + static_cast<long>(blk) * kHBlock;
+  reinterpret_cast<float4*>(o)[qd] = r;
+  reinterpret_cast<float4*>(o + 512)[qd] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Quantisation of already rotated fp32 activations to the GEMV's decode
+// operand (one warp per (token, block), the scaling of the rotation kernel).
+__global__ void __launch_bounds__(128) quant_decode_kernel(const float* __restrict__ xr, int M,
+                                                           int K, __half* __restrict__ out,
+                                                           float* __restrict__ out_scale) {
+  const int lane = threadIdx.x & 31;
+  const int B = K / kHBlock;
+  const long wid = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  pdl_launch_dependents();
+  pdl_wait();
+  if (wid >= static_cast<long>(M) * B) return;
+  const int m = static_cast<int>(wid / B);
+  const int b = static_cast<int>(wid % B);
+  const float* src = xr + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock;
+  float v[4][8];
+#pragma unroll
+  for (int ih = 0; ih < 4; ++ih) {
+    const float4 p0 = reinterpret_cast<const float4*>(src + ih * 256 + lane * 8)[0];
+    const float4 p1 = reinterpret_cast<const float4*>(src + ih * 256 + lane * 8)[1];
+    v[ih][0] = p0.x; v[ih][1] = p0.y; v[ih][2] = p0.z; v[ih][3] = p0.w;
+    v[ih][4] = p1.x; v[ih][5] = p1.y; v[ih][6] = p1.z; v[ih][7] = p1.w;
+  }
+  float f, finv;
+  decode_factor(v, f, finv);
+  __half* o = out + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock;
+#pragma unroll
+  for (int ih = 0; ih < 4; ++ih)
+    *reinterpret_cast<uint4*>(o + ih * 256 + lane * 8) = decode_pack8(v, ih, f);
+  if (lane == 0) out_scale[static_cast<long>(m) * B + b] = finv;
+}
+
+// Per-token int8 quantisation of already rotated fp32 activations (the
+// arithmetic of fwht_i8_kernel); one CTA per token, two passes over the row.
+__global__ void __launch_bounds__(256) quant_i8_kernel(const float* __restrict__ xr, int M, int K,
+                                                       __half* __restrict__ xq,
+                                                       float* __restrict__ tscale) {
+  __shared__ float red[8];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int m = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  const float* xm = xr + static_cast<long>(m) * K;
+  float amax = 0.f;
+  for (int i = threadIdx.x * 4; i < K; i += 256 * 4) {
+    const float4 p = reinterpret_cast<const float4*>(xm + i)[0];
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(p.x), fabsf(p.y)), fmaxf(fabsf(p.z), fabsf(p.w))));
+  }
+  amax = warp_max(amax);
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  float a = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w]);
+  const float ts = __fdiv_rn(a, 127.0f);
+  const bool nz = ts > 0.f;
+  if (threadIdx.x == 0) tscale[m] = nz ? ts : 0.f;
+  __half* om = xq + static_cast<long>(m) * K;
+  for (int i = threadIdx.x * 4; i < K; i += 256 * 4) {
+    const float4 p = reinterpret_cast<const float4*>(xm + i)[0];
+    const float vv[4] = {p.x, p.y, p.z, p.w};
+    uint32_t w[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      float q0 = 0.f, q1 = 0.f;
+      if (nz) {
+        q0 = fminf(fmaxf(rintf(__fdiv_rn(vv[2 * t], ts)), -127.f), 127.f);
+        q1 = fminf(fmaxf(rintf(__fdiv_rn(vv[2 * t + 1], ts)), -127.f), 127.f);
+      }
+      __half2 h2 = __floats2half2_rn(q0, q1);
+      w[t] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint2*>(om + i) = make_uint2(w[0], w[1]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fwht_shard(const uint16_t* x, int64_t M, int64_t Kr, int lead, int trail,
+                              const int8_t* sign, float* xr, float* h_lead, float* h_trail,
+                              cudaStream_t st) {
+  const int64_t Kp = Kr + 512 * (lead + trail);
+  const long warps = M * ((Kr - 512 * (lead + trail)) / kHBlock + lead + trail);
+  return launch(fwht_shard_kernel, dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128), 0, st,
+                x, static_cast<int>(M), static_cast<int>(Kr), lead, trail, sign, xr,
+                static_cast<int>(Kp), h_lead, h_trail);
+}
+
+cudaError_t launch_fwht_combine(const float* h_first, const float* h_second, int64_t M, int part,
+                                float* xr, int64_t Kp, int64_t blk, cudaStream_t st) {
+  const long threads = M * 128;
+  return launch(fwht_combine_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
+                0, st, h_first, h_second, static_cast<int>(M), part, xr, static_cast<int>(Kp),
+                static_cast<int>(blk));
+}
+
+cudaError_t launch_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, void* out,
+                                 float* out_scale, cudaStream_t st) {
+  if (mode == TERN_FWHT_I8)
+    return launch(quant_i8_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, st, xr,
+                  static_cast<int>(M), static_cast<int>(K), static_cast<__half*>(out), out_scale);
+  const long warps = M * (K / kHBlock);
+  return launch(quant_decode_kernel, dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128), 0,
+                st, xr, static_cast<int>(M), static_cast<int>(K), static_cast<__half*>(out),
+                out_scale);
+}
 
 cudaError_t launch_fwht(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign, int mode,
                         void* out, float* out_scale, cudaStream_t st) {

@@ -95,6 +95,63 @@ __device__ __forceinline__ void fwht_1024(float (&v)[4][8], int lane) {
     for (int il = 0; il < 8; ++il) v[ih][il] = __fmul_rn(v[ih][il], 0.03125f);
 }
 
+// The 512-element half of a block (page section 1: each rank of a K split
+// that cuts a block in the middle transforms its own half): lane l holds the
+// 16 elements ih*256 + l*8 + il (ih = 0..1, il = 0..7), loaded like
+// load_block.
+__device__ __forceinline__ void load_half(const uint16_t* __restrict__ xb,
+                                          const int8_t* __restrict__ sb, int lane,
+                                          float (&v)[2][8]) {
+#pragma unroll
+  for (int ih = 0; ih < 2; ++ih) {
+    uint4 raw = __ldg(reinterpret_cast<const uint4*>(xb + ih * 256 + lane * 8));
+    uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[ih][2 * q] = __uint_as_float(w[q] << 16);
+      v[ih][2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+    }
+    if (sb != nullptr) {
+#pragma unroll
+      for (int il = 0; il < 8; ++il) {
+        float s = static_cast<float>(__ldg(sb + ih * 256 + lane * 8 + il));
+        v[ih][il] = v[ih][il] * s;
+      }
+    }
+  }
+}
+
+// Unnormalised H512 of a half block: the stages with stride 1 .. 256 of the
+// canonical transform, in the same order and fp32 operations as the first
+// nine stages of fwht_1024, so that the stride-512 stage applied to two
+// halves afterwards (sum for the first half, difference for the second,
+// then * 1/32) reproduces fwht_1024 bit for bit.
+__device__ __forceinline__ void fwht_512_unscaled(float (&v)[2][8], int lane) {
+#pragma unroll
+  for (int s = 0; s < 3; ++s) {
+    const int h = 1 << s;
+#pragma unroll
+    for (int ih = 0; ih < 2; ++ih)
+#pragma unroll
+      for (int il = 0; il < 8; ++il)
+        if ((il & h) == 0) bfly(v[ih][il], v[ih][il + h]);
+  }
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int lm = 1 << s;
+    const bool upper = (lane & lm) != 0;
+#pragma unroll
+    for (int ih = 0; ih < 2; ++ih)
+#pragma unroll
+      for (int il = 0; il < 8; ++il) {
+        float p = __shfl_xor_sync(kFull, v[ih][il], lm);
+        v[ih][il] = upper ? __fsub_rn(p, v[ih][il]) : __fadd_rn(v[ih][il], p);
+      }
+  }
+#pragma unroll
+  for (int il = 0; il < 8; ++il) bfly(v[0][il], v[1][il]);
+}
+
 __device__ __forceinline__ float warp_max(float a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFull, a, o));

@@ -110,6 +110,54 @@ tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_
       launch_fwht(x, M, K, sign, mode, out, out_scale, static_cast<cudaStream_t>(stream)));
 }
 
+tern_status tern_fwht_shard(const uint16_t* x, int64_t M, int64_t Kr, int lead, int trail,
+                            const int8_t* sign, float* xr, float* h_lead, float* h_trail,
+                            void* stream) {
+  if (M < 0 || Kr < 0 || (lead != 0 && lead != 1) || (trail != 0 && trail != 1))
+    return TERN_ERR_INVALID_ARG;
+  const int64_t whole = Kr - 512 * (lead + trail);
+  const int64_t Kp = Kr + 512 * (lead + trail);
+  if (whole < 0 || whole % kHBlock != 0 || Kp == 0 || Kp > kMaxK) return TERN_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) / Kp) return TERN_ERR_SHAPE;
+  if (M == 0) return TERN_OK;
+  if (x == nullptr || (whole > 0 && xr == nullptr) || (lead && h_lead == nullptr) ||
+      (trail && h_trail == nullptr))
+    return TERN_ERR_INVALID_ARG;
+  if (!aligned16(x) || (xr && !aligned16(xr)) || (h_lead && !aligned16(h_lead)) ||
+      (h_trail && !aligned16(h_trail)))
+    return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_fwht_shard(x, M, Kr, lead, trail, sign, xr, h_lead, h_trail,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_fwht_combine(const float* h_first, const float* h_second, int64_t M, int part,
+                              float* xr, int64_t Kp, int64_t blk, void* stream) {
+  if (M < 0 || Kp < 0 || blk < 0 || (part != 0 && part != 1)) return TERN_ERR_INVALID_ARG;
+  if (Kp == 0 || Kp % kHBlock != 0 || Kp > kMaxK || blk >= Kp / kHBlock) return TERN_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) / Kp) return TERN_ERR_SHAPE;
+  if (M == 0) return TERN_OK;
+  if (h_first == nullptr || h_second == nullptr || xr == nullptr) return TERN_ERR_INVALID_ARG;
+  if (!aligned16(h_first) || !aligned16(h_second) || !aligned16(xr)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_fwht_combine(h_first, h_second, M, part, xr, Kp, blk,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, void* out,
+                               float* out_scale, void* stream) {
+  if (M < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (mode != TERN_FWHT_DECODE && mode != TERN_FWHT_I8) return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) / K) return TERN_ERR_SHAPE;
+  if (M == 0) return TERN_OK;
+  if (xr == nullptr || out == nullptr || out_scale == nullptr) return TERN_ERR_INVALID_ARG;
+  if (!aligned16(xr) || !aligned16(out) || !aligned16(out_scale)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_quant_rotated(xr, M, K, mode, out, out_scale,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const float* xs,
                              int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
                              size_t ws_bytes, void* stream) {

@@ -42,6 +42,13 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // Launchers (one per translation unit); they assume validated arguments.
 cudaError_t launch_fwht(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign, int mode,
                         void* out, float* out_scale, cudaStream_t st);
+cudaError_t launch_fwht_shard(const uint16_t* x, int64_t M, int64_t Kr, int lead, int trail,
+                              const int8_t* sign, float* xr, float* h_lead, float* h_trail,
+                              cudaStream_t st);
+cudaError_t launch_fwht_combine(const float* h_first, const float* h_second, int64_t M, int part,
+                                float* xr, int64_t Kp, int64_t blk, cudaStream_t st);
+cudaError_t launch_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, void* out,
+                                 float* out_scale, cudaStream_t st);
 cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
                         uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q,
                         cudaStream_t st);

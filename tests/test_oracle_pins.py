@@ -382,3 +382,46 @@ def test_decode_operand_range_and_precision():
                 assert 2 ** 14 <= bm[m, b] < 2 ** 15
     back = vals.astype(np.float64) * np.repeat(inv, 1024, axis=1)
     assert np.all(np.abs(back - xr) <= np.abs(xr) * 2.0 ** -11 + 1e-30)
+
+
+# ---------------------------------------------------------------- K split (section 1)
+
+def test_half_transform_is_dense_h512():
+    """fwht_half_f32 is the unnormalised H512 (closed form, exact on integers)."""
+    rng = np.random.default_rng(40)
+    x = rng.integers(-50, 51, (3, 512)).astype(np.float32)
+    ref = x.astype(np.float64) @ _walsh_popcount(512).T
+    assert np.array_equal(O.fwht_half_f32(x).astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("k,world", [(17408, 2), (3072, 2), (4096, 4), (2048, 4), (5120, 2)])
+def test_ksplit_rotation_equals_whole_width_rotation(k, world):
+    """The half-block exchange reproduces the canonical whole-width rotation
+    bit for bit (the stride-512 stage is the last one), with or without a
+    sign vector, whether the shard boundaries cut blocks or not."""
+    rng = np.random.default_rng(k + world)
+    x = O.bf16_round(rng.standard_normal((3, k)).astype(np.float32))
+    sign = np.where(rng.random(k) < 0.5, -1, 1).astype(np.int8)
+    for sg in (None, sign):
+        got = np.concatenate(O.ksplit_rotate_f32(x, world, sg), axis=1)
+        ref = O.fwht_f32(x, sg)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    # and it matches the exact fp64 rotation to fp32 accuracy
+    assert O.rel_frobenius(got, O.rotate_f64(x, sign)) < 1e-6
+
+
+def test_ksplit_swapped_parts_is_caught():
+    """Negative control (the page's section 1 checks that swapping the ranks'
+    roles is detected): if the first-half rank takes the difference and the
+    second-half rank the sum, the result is far from the rotation."""
+    rng = np.random.default_rng(41)
+    k = 17408
+    x = rng.standard_normal((2, k)).astype(np.float32)
+    half = k // 2
+    a = O.fwht_half_f32(x[:, half - 512:half])
+    b = O.fwht_half_f32(x[:, half:half + 512])
+    ref = O.fwht_f32(x)[:, half - 512:half + 512]   # the split block, columns 8192 .. 9215
+    good = np.concatenate([O.ksplit_combine(a, b, 0), O.ksplit_combine(a, b, 1)], axis=1)
+    bad = np.concatenate([O.ksplit_combine(a, b, 1), O.ksplit_combine(a, b, 0)], axis=1)
+    assert np.array_equal(good, ref)
+    assert O.rel_frobenius(bad, ref) > 1.0
