@@ -628,6 +628,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--stack-layers", type=int, default=64,
+                    help="layers of the linear stack section (64 = the 27B model's stack)")
+    ap.add_argument("--stack-only", action="store_true",
+                    help="run only the stack section (for profiling); prints its JSON object")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -644,6 +648,11 @@ def main():
         if rank == 0:
             BUILD.build()
         _barrier(ws)
+    if args.stack_only:
+        if rank == 0:
+            print(json.dumps({"stack": run_stack(args, local, n_layers=args.stack_layers)}),
+                  flush=True)
+        return
     line, layers = run_decode(args, rank, ws, local)
     del layers
     torch.cuda.empty_cache()
@@ -652,7 +661,7 @@ def main():
     if not args.no_prefill and rank == 0:
         line["mid_m"] = run_mid_m(args, local)
     if not args.no_stack and rank == 0:
-        line["stack"] = run_stack(args, local)
+        line["stack"] = run_stack(args, local, n_layers=args.stack_layers)
     if rank == 0:
         if not args.no_cpu_baseline and ws == 1:
             line["cpu_baseline"] = run_cpu_baseline(args)
