@@ -1,4 +1,6 @@
-// The int8 prefill GEMM with per-row and per-token rescale.
+// The int8 prefill GEMMs with per-row and per-token rescale: gemm_i8_kernel
+// on the expanded weight (below) and gemm_packed_kernel straight from the
+// decode's 2-bit packed weights (further down), with bit-identical results.
 //
 // Page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2", section 4
 // ("prefill の線形層を int8 GEMM に"): with q[n,g] = round(127 s[n,g]/smax[n])

@@ -132,3 +132,45 @@ def test_binding_raises_named_error(lib):
     with pytest.raises(B.TernError) as ei:
         B.tern_fwht_quant(FAKE, 4, 1000, None, 0, FAKE, None, stream=0)
     assert ei.value.status == 2 and "TERN_ERR_SHAPE" in str(ei.value)
+
+
+def test_gemm_packed_argument_errors(lib):
+    need = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, 64, 256, 5120)
+    a = lambda m=64, n=256, k=5120, y=FAKE, ws=FAKE, wsb=need: (
+        FAKE, FAKE, FAKE, FAKE, FAKE, m, n, k, y, None, ws, wsb, None)
+    assert need > 0                                            # 1 x 1 tile: split along K
+    assert _st("tern_gemm_prefill_packed", *a(n=250)) == 2       # N % 16
+    assert _st("tern_gemm_prefill_packed", *a(k=1536)) == 2
+    assert _st("tern_gemm_prefill_packed", *a(m=-1)) == 1
+    assert _st("tern_gemm_prefill_packed", *a(y=None)) == 1
+    assert _st("tern_gemm_prefill_packed", *a(y=FAKE + 2)) == 3
+    assert _st("tern_gemm_prefill_packed", *a(wsb=need - 1)) == 6
+    assert _st("tern_gemm_prefill_packed", *a(ws=None)) == 6
+    assert _st("tern_gemm_prefill_packed", *a(ws=FAKE + 8)) == 3
+    assert _st("tern_gemm_prefill_packed", *a(m=0)) == 0
+    assert _st("tern_gemm_prefill_packed", *a(n=0)) == 0
+
+
+def test_ksplit_argument_errors(lib):
+    sh = lambda m=2, kr=8704, lead=0, trail=1, x=FAKE, xr=FAKE, hl=None, ht=FAKE: (
+        x, m, kr, lead, trail, None, xr, hl, ht, None)
+    assert _st("tern_fwht_shard", *sh(trail=0)) == 2                 # 8.5 blocks, no half marked
+    assert _st("tern_fwht_shard", *sh(lead=2)) == 1
+    assert _st("tern_fwht_shard", *sh(ht=None)) == 1                 # trailing half, no output
+    assert _st("tern_fwht_shard", *sh(lead=1, trail=1, kr=9216, hl=None)) == 1
+    assert _st("tern_fwht_shard", *sh(x=None)) == 1
+    assert _st("tern_fwht_shard", *sh(x=FAKE + 2)) == 3
+    assert _st("tern_fwht_shard", *sh(kr=512 + 65536)) == 2          # padded width > 65536
+    assert _st("tern_fwht_shard", *sh(m=0)) == 0
+    cb = lambda m=2, part=0, kp=9216, blk=8, hf=FAKE: (hf, FAKE, m, part, FAKE, kp, blk, None)
+    assert _st("tern_fwht_combine", *cb(part=2)) == 1
+    assert _st("tern_fwht_combine", *cb(blk=9)) == 2
+    assert _st("tern_fwht_combine", *cb(kp=9000)) == 2
+    assert _st("tern_fwht_combine", *cb(hf=None)) == 1
+    assert _st("tern_fwht_combine", *cb(hf=FAKE + 4)) == 3
+    assert _st("tern_fwht_combine", *cb(m=0)) == 0
+    qr = lambda m=2, k=9216, mode=1, sc=FAKE: (FAKE, m, k, mode, FAKE, sc, None)
+    assert _st("tern_quant_rotated", *qr(mode=0)) == 1               # only DECODE and I8
+    assert _st("tern_quant_rotated", *qr(k=8704)) == 2
+    assert _st("tern_quant_rotated", *qr(sc=None)) == 1
+    assert _st("tern_quant_rotated", *qr(m=0)) == 0
