@@ -344,7 +344,15 @@ def run_prefill(args, local, m=2048):
     layer = I.GATE_UP
     _, tc_peak, peak_kind = _peaks()
     with torch.cuda.stream(stream):
-        lay = _make_layers(layer, 1, seed=7, prefill=True)[0]
+        g = torch.Generator(device="cuda")
+        g.manual_seed(7000)
+        codes = (torch.randint(0, 3, (layer.n, layer.k), dtype=torch.int8, device="cuda",
+                               generator=g) - 1).to(torch.int8)
+        scales = (0.02 * torch.randn((layer.n, layer.k // 128), device="cuda", generator=g).abs()
+                  + 1e-3).to(torch.float16)
+        lay = B.pack_layer(codes, scales, decode=True, prefill=True)
+        w_h = B.expand_fp16(codes, scales)
+        del codes, scales
         x = _activations(layer, m, seed=77).cuda()
         xq = torch.empty((m, layer.k), dtype=torch.float16, device="cuda")
         ts = torch.empty(m, dtype=torch.float32, device="cuda")
@@ -367,17 +375,26 @@ def run_prefill(args, local, m=2048):
             B.tern_gemm_prefill_packed(xq, ts, lay.packed, lay.q, lay.rscale, m, layer.n,
                                        layer.k, y, None, wsp, nbp, stream=st)
 
+        xh = torch.empty((m, layer.k), dtype=torch.float16, device="cuda")
+        xs = torch.empty((m, layer.k // 1024), dtype=torch.float32, device="cuda")
+        B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_DECODE, xh, xs, st)
+
+        def fp16_only():
+            B.tern_gemm_prefill_fp16(xh, xs, w_h, m, layer.n, layer.k, y, st)
+
         for _ in range(max(3, args.warmup // 4)):
             step()
             packed_only()
+            fp16_only()
         torch.cuda.synchronize()
         n = 20
         t = _time_region(step, n, stream, 1)
         tg = _time_region(gemm_only, n, stream, 1)
         tp = _time_region(packed_only, n, stream, 1)
+        th = _time_region(fp16_only, n, stream, 1)
         B.tern_check(stream)
     ops = 2.0 * m * layer.n * layer.k
-    del lay
+    del lay, w_h
     torch.cuda.empty_cache()
     return {"metric": "prefill int8 TOPS (2*M*N*K / step time)", "value": round(ops * n / t / 1e12, 1),
             "unit": "TOPS", "workload": f"prefill gate/up 5120->34816, M={m}",
@@ -394,7 +411,12 @@ def run_prefill(args, local, m=2048):
                        "frac": round(ops * n / tp / 1e12 / tc_peak, 4),
                        "avg_launch_us": round(tp / n * 1e6, 2),
                        "weight_bytes": layer.n * layer.k // 4 + layer.n * (layer.k // 128) * 3,
-                       "expanded_weight_bytes": layer.n * layer.k * 2}}
+                       "expanded_weight_bytes": layer.n * layer.k * 2},
+            "fp16_variant": {"kernel": "tern_gemm_prefill_fp16 (decode operand x fp16 code*s, "
+                                       "no int8 quantisation)",
+                             "achieved": round(ops * n / th / 1e12, 1), "unit": "TFLOP/s",
+                             "frac": round(ops * n / th / 1e12 / tc_peak, 4),
+                             "avg_launch_us": round(th / n * 1e6, 2)}}
 
 
 def run_mid_m(args, local, ms=(32, 64, 128, 256)):

@@ -329,6 +329,29 @@ tern_status tern_gemm_prefill_packed(const uint16_t* xq, const float* tscale,
                                      int64_t M, int64_t N, int64_t K, uint16_t* y, int32_t* acc,
                                      void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * The fp16 prefill variant (compared with the int8 path of page section 4).
+ * On sm_103a the int8 values of section 4 already run on the f16 tensor
+ * kind (there is no tcgen05 int8 kind), so an fp16 GEMM costs the same MMA
+ * time; it keeps the scales exact instead of rounding them to q, and the
+ * activations at the decode operand's precision instead of per-token int8.
+ *
+ * tern_expand_fp16 -- w_h fp16 [N][K] = code[n,k] * s[n, k/128] (exact).
+ *   codes int8 [N][K], scales fp16 [N][G].  Requirements: K % 1024 == 0,
+ *   K <= 65536, N * K < 2^34.
+ * tern_gemm_prefill_fp16 --
+ *     y[m,n] = bf16_rn( sum_b xs[m,b] * sum_{k in block b} xh[m,k] w_h[n,k] )
+ *   with xh fp16 [M][K] and xs fp32 [M][K/1024] the decode operand of
+ *   tern_fwht_quant(TERN_FWHT_DECODE) (any M), each block's sum accumulated
+ *   in fp32 by the tensor cores and the blocks added in fp32 in order.
+ *   y bf16 [M][N].  Requirements: K % 1024 == 0, K <= 65536, N % 16 == 0,
+ *   0 <= M, N <= 2^24.
+ * ---------------------------------------------------------------------- */
+tern_status tern_expand_fp16(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                             uint16_t* w_h, void* stream);
+tern_status tern_gemm_prefill_fp16(const uint16_t* xh, const float* xs, const uint16_t* w_h,
+                                   int64_t M, int64_t N, int64_t K, uint16_t* y, void* stream);
+
 /* Workspace sizing and initialisation. */
 #define TERN_OP_GEMV 1
 #define TERN_OP_GEMM 2

@@ -47,6 +47,8 @@ _SIGS = {
     "tern_pack": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p]),
     "tern_fwht_quant": (ctypes.c_int, [_p, _i64, _i64, _p, ctypes.c_int, _p, _p, _p]),
     "tern_gemv_decode": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
+    "tern_expand_fp16": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p]),
+    "tern_gemm_prefill_fp16": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
     "tern_fwht_shard": (ctypes.c_int, [_p, _i64, _i64, ctypes.c_int, ctypes.c_int, _p, _p, _p, _p,
                                        _p]),
     "tern_fwht_combine": (ctypes.c_int, [_p, _p, _i64, ctypes.c_int, _p, _i64, _i64, _p]),
@@ -167,6 +169,15 @@ def tern_gemm_prefill_packed(xq, tscale, packed, q, rscale, m, n, k, y, acc=None
                              ws_bytes=0, stream=None):
     return _call("tern_gemm_prefill_packed", _ptr(xq), _ptr(tscale), _ptr(packed), _ptr(q),
                  _ptr(rscale), m, n, k, _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def tern_expand_fp16(codes, scales, n, k, w_h, stream=None):
+    return _call("tern_expand_fp16", _ptr(codes), _ptr(scales), n, k, _ptr(w_h), _stream(stream))
+
+
+def tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y, stream=None):
+    return _call("tern_gemm_prefill_fp16", _ptr(xh), _ptr(xs), _ptr(w_h), m, n, k, _ptr(y),
+                 _stream(stream))
 
 
 def tern_fwht_shard(x, m, kr, lead, trail, sign, xr, h_lead, h_trail, stream=None):
@@ -347,6 +358,30 @@ class DecodeGraph:
         self.launch(x)
         torch.cuda.current_stream().synchronize()
         return self.y_host
+
+
+def expand_fp16(codes: torch.Tensor, scales: torch.Tensor, stream=None) -> torch.Tensor:
+    """The fp16 weight code * s [N, K] of the fp16 prefill variant."""
+    _need(codes, torch.int8, "codes")
+    _need(scales, torch.float16, "scales")
+    n, k = codes.shape
+    w_h = torch.empty((n, k), dtype=torch.float16, device=codes.device)
+    tern_expand_fp16(codes, scales, n, k, w_h, stream)
+    return w_h
+
+
+def prefill_fp16(w_h: torch.Tensor, x: torch.Tensor, y: torch.Tensor | None = None, sign=None,
+                 stream=None) -> torch.Tensor:
+    """fp16 prefill variant: rotation to the decode operand (fp16 + per-block
+    factors), then one tensor-core GEMM against w_h with the factors applied
+    per 1024-block in the epilogue."""
+    m = x.shape[0]
+    n, k = w_h.shape
+    xh, xs = fwht(x, TERN_FWHT_DECODE, sign, stream)
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y, stream)
+    return y
 
 
 def prefill(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,

@@ -26,6 +26,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "sm100_ptx.cuh"
 #include "tern_internal.cuh"
 
@@ -58,10 +60,19 @@ __device__ __forceinline__ void fail(volatile int* abort_flag, unsigned int code
   atomicOr(&g_gemm_error, code);
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const float* __restrict__ tscale, const float* __restrict__ rscale, int M,
-                   int N, int K, __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out) {
+// The kernel body of both tensor-core GEMMs on an fp16 [N][K] weight.  FP =
+// false: the int8 path (integer values, exact chunk sums, per-row and
+// per-token rescale).  FP = true: the fp16 path, whose activations are the
+// decode operand (fp16 with one power-of-two factor per token and 1024-block):
+// each 1024-chunk of K is one rotation block, so the epilogue multiplies the
+// chunk's fp32 sum by the token's block factor (`tscale` holds xs [M][K/1024])
+// and adds the chunks in fp32; `rscale` and `acc_out` are unused.
+template <bool FP>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                          const float* __restrict__ tscale,
+                                          const float* __restrict__ rscale, int M, int N, int K,
+                                          __nv_bfloat16* __restrict__ y,
+                                          int32_t* __restrict__ acc_out) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -205,7 +216,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
-      int32_t sums[128];
+      const int row = m_blk * BM + 32 * q + lane;
+      typename std::conditional<FP, float, int32_t>::type sums[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sums[i] = 0;
       for (int c = 0; c < chunks; ++c, ++cc) {
@@ -216,6 +228,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         ptx::tc_fence_after();
+        float f = 0.f;   // the token's factor of rotation block c (fp16 path)
+        if (FP && row < M) f = __ldg(tscale + static_cast<long>(row) * chunks + c);
 #pragma unroll
         for (int piece = 0; piece < 4; ++piece) {
           uint32_t v[32];
@@ -224,16 +238,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tmem_ld_32x32b_x32(taddr, v);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            sums[piece * 32 + i] += __float2int_rn(__uint_as_float(v[i]));   // exact integers
+          for (int i = 0; i < 32; ++i) {
+            if constexpr (FP)
+              sums[piece * 32 + i] = __fadd_rn(sums[piece * 32 + i],
+                                               __fmul_rn(__uint_as_float(v[i]), f));
+            else
+              sums[piece * 32 + i] += __float2int_rn(__uint_as_float(v[i]));   // exact integers
+          }
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&dempty[buf]);
       }
       if (!ok) break;
-      const int row = m_blk * BM + 32 * q + lane;
-      if (row < M) {
+      if (FP && row < M) {
+        const int n0 = n_blk * BN + wg * 128;
+        __nv_bfloat16* yrow = y + static_cast<long>(row) * N;
+#pragma unroll
+        for (int j = 0; j < 128; j += 8) {
+          const int n = n0 + j;
+          if (n < N) {
+            uint32_t packed[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(sums[j + 2 * t]),
+                                                       static_cast<float>(sums[j + 2 * t + 1]));
+              packed[t] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(yrow + n) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          }
+        }
+      }
+      if (!FP && row < M) {
         const float ts = tscale[row];
         const int n0 = n_blk * BN + wg * 128;
         __nv_bfloat16* yrow = y + static_cast<long>(row) * N;
@@ -247,17 +283,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t packed[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-              const float f0 = __fmul_rn(__fmul_rn(__int2float_rn(sums[j + 2 * t]), ts), rr[2 * t]);
-              const float f1 =
-                  __fmul_rn(__fmul_rn(__int2float_rn(sums[j + 2 * t + 1]), ts), rr[2 * t + 1]);
+              const float f0 = __fmul_rn(
+                  __fmul_rn(__int2float_rn(static_cast<int>(sums[j + 2 * t])), ts), rr[2 * t]);
+              const float f1 = __fmul_rn(
+                  __fmul_rn(__int2float_rn(static_cast<int>(sums[j + 2 * t + 1])), ts),
+                  rr[2 * t + 1]);
               __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
               packed[t] = *reinterpret_cast<uint32_t*>(&h);
             }
             *reinterpret_cast<uint4*>(yrow + n) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             if (acc_out != nullptr) {
               int4* ap = reinterpret_cast<int4*>(acc_out + static_cast<long>(row) * N + n);
-              ap[0] = make_int4(sums[j], sums[j + 1], sums[j + 2], sums[j + 3]);
-              ap[1] = make_int4(sums[j + 4], sums[j + 5], sums[j + 6], sums[j + 7]);
+              ap[0] = make_int4(static_cast<int>(sums[j]), static_cast<int>(sums[j + 1]),
+                                static_cast<int>(sums[j + 2]), static_cast<int>(sums[j + 3]));
+              ap[1] = make_int4(static_cast<int>(sums[j + 4]), static_cast<int>(sums[j + 5]),
+                                static_cast<int>(sums[j + 6]), static_cast<int>(sums[j + 7]));
             }
           }
         }
@@ -272,6 +312,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const float* __restrict__ tscale, const float* __restrict__ rscale, int M,
+                   int N, int K, __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out) {
+  gemm_body<false>(tmA, tmB, tscale, rscale, M, N, K, y, acc_out);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const float* __restrict__ xs, int M, int N, int K,
+                    __nv_bfloat16* __restrict__ y) {
+  gemm_body<true>(tmA, tmB, xs, nullptr, M, N, K, y, nullptr);
 }
 
 
@@ -858,6 +912,25 @@ cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const ui
                 dim3(FIN_THREADS), 0, st, static_cast<const int32_t*>(part), S, tscale, rscale,
                 static_cast<int>(M), static_cast<int>(N), reinterpret_cast<__nv_bfloat16*>(y),
                 acc);
+}
+
+cudaError_t launch_gemm_f16(const uint16_t* xh, const float* xs, const uint16_t* w_h, int64_t M,
+                            int64_t N, int64_t K, uint16_t* y, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, xh, M, K, BM) || !make_map(&tb, w_h, N, K, BN)) return cudaErrorInvalidValue;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_f16_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  return launch(gemm_f16_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, xs,
+                static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                reinterpret_cast<__nv_bfloat16*>(y));
 }
 
 cudaError_t gemm_read_clear_error(unsigned int* err) {

@@ -109,6 +109,29 @@ __global__ void wq_kernel(const int8_t* __restrict__ codes, const int8_t* __rest
   }
 }
 
+// One thread per 8 consecutive elements of a row: w_h = code * s, the fp16
+// weight of the fp16 prefill path (exact: a code is -1, 0 or +1).
+__global__ void wh_kernel(const int8_t* __restrict__ codes, const __half* __restrict__ scales,
+                          int N, int K, __half* __restrict__ wh, long n_vec) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int G = K / kGroup;
+  for (long vi = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; vi < n_vec;
+       vi += static_cast<long>(gridDim.x) * blockDim.x) {
+    const long e0 = vi * 8;
+    const long row = e0 / K;
+    const int k = static_cast<int>(e0 % K);
+    const __half sc = scales[row * G + k / kGroup];
+    const __half nsc = __hneg(sc);
+    const uint2 cw = *reinterpret_cast<const uint2*>(codes + e0);
+    const int8_t* cb = reinterpret_cast<const int8_t*>(&cw);
+    __half v[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) v[t] = cb[t] > 0 ? sc : (cb[t] < 0 ? nsc : __float2half_rn(0.f));
+    *reinterpret_cast<uint4*>(wh + e0) = *reinterpret_cast<const uint4*>(v);
+  }
+}
+
 unsigned grid_for(long items, int threads) {
   long b = (items + threads - 1) / threads;
   if (b > 152L * 32) b = 152L * 32;
@@ -116,6 +139,14 @@ unsigned grid_for(long items, int threads) {
 }
 
 }  // namespace
+
+cudaError_t launch_expand_fp16(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                               uint16_t* w_h, cudaStream_t st) {
+  const long n_vec = N * K / 8;
+  return launch(wh_kernel, dim3(grid_for(n_vec, 256)), dim3(256), 0, st, codes,
+                reinterpret_cast<const __half*>(scales), static_cast<int>(N), static_cast<int>(K),
+                reinterpret_cast<__half*>(w_h), n_vec);
+}
 
 cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
                         uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q,

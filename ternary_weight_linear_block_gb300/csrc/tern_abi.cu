@@ -242,6 +242,32 @@ tern_status tern_gemm_prefill_packed(const uint16_t* xq, const float* tscale,
                                       static_cast<cudaStream_t>(stream)));
 }
 
+tern_status tern_expand_fp16(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                             uint16_t* w_h, void* stream) {
+  if (N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
+  if (N > (int64_t(1) << 34) / K) return TERN_ERR_SHAPE;
+  if (N == 0) return TERN_OK;
+  if (codes == nullptr || scales == nullptr || w_h == nullptr) return TERN_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(w_h)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_expand_fp16(codes, scales, N, K, w_h, static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_gemm_prefill_fp16(const uint16_t* xh, const float* xs, const uint16_t* w_h,
+                                   int64_t M, int64_t N, int64_t K, uint16_t* y, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
+  if (N % 16 != 0) return TERN_ERR_SHAPE;
+  if (M > (int64_t(1) << 24) || N > (int64_t(1) << 24)) return TERN_ERR_SHAPE;
+  if ((M + 127) / 128 * ((N + 255) / 256) >= (int64_t(1) << 31)) return TERN_ERR_SHAPE;
+  if (M == 0 || N == 0) return TERN_OK;
+  if (xh == nullptr || xs == nullptr || w_h == nullptr || y == nullptr) return TERN_ERR_INVALID_ARG;
+  if (!aligned16(xh) || !aligned16(xs) || !aligned16(w_h) || !aligned16(y)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_gemm_f16(xh, xs, w_h, M, N, K, y, static_cast<cudaStream_t>(stream)));
+}
+
 tern_status tern_check(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return TERN_ERR_CUDA;

@@ -174,3 +174,17 @@ def test_ksplit_argument_errors(lib):
     assert _st("tern_quant_rotated", *qr(k=8704)) == 2
     assert _st("tern_quant_rotated", *qr(sc=None)) == 1
     assert _st("tern_quant_rotated", *qr(m=0)) == 0
+
+
+def test_fp16_variant_argument_errors(lib):
+    assert _st("tern_expand_fp16", FAKE, FAKE, 16, 1000, FAKE, None) == 2
+    assert _st("tern_expand_fp16", FAKE, FAKE, -1, 1024, FAKE, None) == 1
+    assert _st("tern_expand_fp16", FAKE, FAKE, 16, 1024, None, None) == 1
+    assert _st("tern_expand_fp16", FAKE + 1, FAKE, 16, 1024, FAKE, None) == 3
+    assert _st("tern_expand_fp16", FAKE, FAKE, 0, 1024, FAKE, None) == 0
+    g = lambda m=64, n=256, k=1024, y=FAKE: (FAKE, FAKE, FAKE, m, n, k, y, None)
+    assert _st("tern_gemm_prefill_fp16", *g(n=250)) == 2
+    assert _st("tern_gemm_prefill_fp16", *g(k=1536)) == 2
+    assert _st("tern_gemm_prefill_fp16", *g(y=None)) == 1
+    assert _st("tern_gemm_prefill_fp16", *g(y=FAKE + 2)) == 3
+    assert _st("tern_gemm_prefill_fp16", *g(m=0)) == 0
