@@ -244,6 +244,13 @@ def _time_region(fn, steps, stream, ws):
     return e0.elapsed_time(e1) / 1e3   # seconds
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the timed kernels at the bench's shapes, from one ncu capture on GB300 of
+# the current kernels; they change only when a kernel changes.
+TRAFFIC_GEMV_GATEUP_M4 = 47_495_680 + 6_144          # gemv_kernel<1>, 5120 -> 34816, M = 4
+TRAFFIC_GEMM_I8_GATEUP_M2048 = 380_519_168 + 120_336_128   # gemm_i8_kernel, M = 2048
+
+
 def _gemv_algorithmic_bytes(m, n, k):
     """Bytes one GEMV launch must move: codes + scales + the fp16 activation
     operand + per-block factors + bf16 output."""
@@ -323,7 +330,8 @@ def run_decode(args, rank, ws, local):
         "pct_hbm_peak": round(100 * value / ws / hbm_peak, 1),
         "roofline": {"bound": "hbm", "kernel": "tern_gemv_decode (M=%d)" % m,
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "frac": round(achieved / hbm_peak, 4),
+                     "traffic": TRAFFIC_GEMV_GATEUP_M4 if m == 4 else None,
                      "algorithmic_bytes": alg, "avg_launch_us": round(gemv_us, 3),
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"},
         "e2e": {"value": round(bytes_step * e2e_steps * ws / te2e / 1e9, 1), "unit": "GB/s",
@@ -402,7 +410,10 @@ def run_prefill(args, local, m=2048):
             "roofline": {"bound": "tensor", "kernel": "tern_gemm_prefill_int8",
                          "achieved": round(ops * n / tg / 1e12, 1), "peak": tc_peak,
                          "unit": "TFLOP/s", "frac": round(ops * n / tg / 1e12 / tc_peak, 4),
-                         "avg_launch_us": round(tg / n * 1e6, 2), "traffic": None,
+                         "avg_launch_us": round(tg / n * 1e6, 2),
+                         "traffic": TRAFFIC_GEMM_I8_GATEUP_M2048 if m == 2048 else None,
+                         "algorithmic_bytes": layer.n * layer.k * 2 + m * layer.k * 2
+                                              + m * layer.n * 2 + 4 * (m + layer.n),
                          "peak_source": f"{peak_kind} bf16_tflops (MEASURED_PEAKS.json): the "
                                         "int8 values run on the fp16/bf16 tensor pipe; "
                                         "sm_103a has no tcgen05 int8 kind"},
