@@ -20,7 +20,8 @@
  * multiple of 16.
  *
  * Conventions for every entry point:
- *   - all data pointers are DEVICE pointers unless stated; the caller
+ *   - all data pointers are DEVICE pointers unless stated (host memory the
+ *     GPU can address directly counts, see tern_host_accessible); the caller
  *     allocates and owns every buffer; the library allocates nothing and
  *     keeps no state besides a per-translation-unit device error word;
  *   - fp16 and bf16 data are passed as uint16_t bit patterns;
@@ -357,6 +358,15 @@ tern_status tern_gemm_prefill_fp16(const uint16_t* xh, const float* xs, const ui
 #define TERN_OP_GEMM 2
 #define TERN_OP_GEMM_PACKED 3
 size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+/* 1 if the GPU current on this thread can load and store `host` directly
+ * at that same address -- a pinned host buffer mapped into the device's
+ * address space, or any host memory on a system whose GPU walks the host
+ * page tables (Grace-Blackwell, over NVLink-C2C) -- else 0.  Such a pointer
+ * may be passed wherever these calls take a device pointer: the kernels
+ * then read their input from, or write their output to, host memory without
+ * a separate copy. */
+int tern_host_accessible(const void* host);
+
 /* Number of kernels one call launches at this shape on the current device
  * (0 for an empty call or an unknown op): for TERN_OP_GEMV the GEMV kernel,
  * plus the fixup kernel when a 512-row block is shared by more CTAs than the

@@ -43,6 +43,7 @@ _SIGS = {
     "tern_packed_bytes": (_sz, [_i64, _i64]),
     "tern_workspace_bytes": (_sz, [ctypes.c_int, _i64, _i64, _i64]),
     "tern_kernel_launches": (ctypes.c_int, [ctypes.c_int, _i64, _i64, _i64]),
+    "tern_host_accessible": (ctypes.c_int, [_p]),
     "tern_workspace_init": (ctypes.c_int, [_p, _sz, _p]),
     "tern_pack": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p]),
     "tern_fwht_quant": (ctypes.c_int, [_p, _i64, _i64, _p, ctypes.c_int, _p, _p, _p]),
@@ -137,6 +138,11 @@ def tern_workspace_bytes(op: int, m: int, n: int, k: int) -> int:
 
 def tern_kernel_launches(op: int, m: int, n: int, k: int) -> int:
     return lib().tern_kernel_launches(op, m, n, k)
+
+
+def tern_host_accessible(t) -> bool:
+    """Whether the GPU can read and write this host buffer in place."""
+    return bool(lib().tern_host_accessible(_ptr(t)))
 
 
 def tern_workspace_init(ws, nbytes: int | None = None, stream=None):
@@ -306,28 +312,68 @@ def decode(layer: PackedLayer, x: torch.Tensor, ws: Workspace, y: torch.Tensor |
     return y
 
 
-class DecodeGraph:
-    """One layer's decode forward for a fixed M, captured once as a CUDA graph
-    with its host transfers: the pinned host input ``x_host`` is copied to the
-    device, rotated, multiplied (tern_fwht_quant + tern_gemv_decode, or
-    tern_linear_decode with ``fused=True``) and the bf16 result is copied back
-    to the pinned host buffer ``y_host``.  ``run()`` replays the graph on the
-    current stream and waits for it, so a decode loop pays one graph launch
-    and one wait per call instead of per-call host work.  The buffers belong
-    to the graph: write the next input into ``x_host`` (or pass it to
-    ``run``) and read ``y_host`` after ``run`` returns."""
+class _DecodeCall:
+    """Device and pinned host buffers of one decode forward (layer, M).  With
+    zero_copy the kernels read x from, and write y to, the pinned host
+    buffers in place; otherwise the graph copies them (memcpy nodes)."""
 
-    def __init__(self, layer: PackedLayer, m: int, sign: torch.Tensor | None = None,
-                 fused: bool = False, device="cuda"):
+    def __init__(self, layer: PackedLayer, m: int, sign, fused: bool, device, zero_copy):
         self.layer, self.m, self.sign, self.fused = layer, m, sign, fused
         self.x_host = torch.zeros((m, layer.k), dtype=torch.bfloat16).pin_memory()
         self.y_host = torch.empty((m, layer.n), dtype=torch.bfloat16).pin_memory()
-        self.x = torch.empty((m, layer.k), dtype=torch.bfloat16, device=device)
-        self.y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=device)
+        if zero_copy is None:
+            zero_copy = tern_host_accessible(self.x_host) and tern_host_accessible(self.y_host)
+        self.zero_copy = bool(zero_copy)
+        if self.zero_copy:
+            self.x, self.y = self.x_host, self.y_host
+        else:
+            self.x = torch.empty((m, layer.k), dtype=torch.bfloat16, device=device)
+            self.y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=device)
         self.xh = torch.empty((m, layer.k), dtype=torch.float16, device=device)
         self.xs = torch.empty((m, layer.k // 1024), dtype=torch.float32, device=device)
         nb = tern_workspace_bytes(TERN_OP_GEMV, m, layer.n, layer.k)
         self.ws = Workspace(device).get(nb)
+
+    def body(self):
+        lay, m = self.layer, self.m
+        st = torch.cuda.current_stream().cuda_stream
+        if not self.zero_copy:
+            self.x.copy_(self.x_host, non_blocking=True)
+        x, y = self.x.data_ptr(), self.y.data_ptr()
+        if self.fused:
+            tern_linear_decode(x, self.sign, lay.packed, m, lay.n, lay.k, y, self.ws,
+                               self.ws.numel(), st)
+        else:
+            tern_fwht_quant(x, m, lay.k, self.sign, TERN_FWHT_DECODE, self.xh, self.xs, st)
+            tern_gemv_decode(lay.packed, self.xh, self.xs, m, lay.n, lay.k, y, self.ws,
+                             self.ws.numel(), st)
+        if not self.zero_copy:
+            self.y_host.copy_(self.y, non_blocking=True)
+
+
+class DecodeStepGraph:
+    """Several decode forwards -- (layer, M) pairs, e.g. the batches or the
+    layers of one decode step -- captured once as a single CUDA graph with
+    their host transfers: each call copies its pinned host input
+    ``x_host[i]`` to the device, rotates, multiplies (tern_fwht_quant +
+    tern_gemv_decode, or tern_linear_decode with ``fused=True``) and copies
+    its bf16 result back to the pinned ``y_host[i]``.  ``run()`` replays the
+    graph on the current stream and waits for it, so the whole step pays one
+    graph launch and one wait.  The buffers belong to the graph: write the
+    inputs into ``x_host`` and read ``y_host`` after ``run`` returns.
+
+    Where the GPU can address the pinned buffers directly
+    (tern_host_accessible, e.g. over NVLink-C2C on Grace-Blackwell) the
+    rotation reads x from host memory and the GEMV writes y into it, with no
+    copy (``zero_copy=None`` chooses; True forces it, False uses copies)."""
+
+    def __init__(self, entries, sign: torch.Tensor | None = None, fused: bool = False,
+                 device="cuda", zero_copy: bool | None = None):
+        self.calls = [_DecodeCall(layer, m, sign, fused, device, zero_copy)
+                      for layer, m in entries]
+        self.zero_copy = all(c.zero_copy for c in self.calls)
+        self.x_host = [c.x_host for c in self.calls]
+        self.y_host = [c.y_host for c in self.calls]
         self._body()                      # first launch outside capture (sets kernel attributes)
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
@@ -335,17 +381,30 @@ class DecodeGraph:
             self._body()
 
     def _body(self):
-        lay, m = self.layer, self.m
-        st = torch.cuda.current_stream().cuda_stream
-        self.x.copy_(self.x_host, non_blocking=True)
-        if self.fused:
-            tern_linear_decode(self.x, self.sign, lay.packed, m, lay.n, lay.k, self.y, self.ws,
-                               self.ws.numel(), st)
-        else:
-            tern_fwht_quant(self.x, m, lay.k, self.sign, TERN_FWHT_DECODE, self.xh, self.xs, st)
-            tern_gemv_decode(lay.packed, self.xh, self.xs, m, lay.n, lay.k, self.y, self.ws,
-                             self.ws.numel(), st)
-        self.y_host.copy_(self.y, non_blocking=True)
+        for c in self.calls:
+            c.body()
+
+    def launch(self):
+        """Replay on the current stream without waiting."""
+        self.graph.replay()
+
+    def run(self):
+        """Replay and wait; returns the pinned host outputs."""
+        self.launch()
+        torch.cuda.current_stream().synchronize()
+        return self.y_host
+
+
+class DecodeGraph(DecodeStepGraph):
+    """One layer's decode forward for a fixed M (a DecodeStepGraph of one
+    call), with ``x_host`` / ``y_host`` the call's pinned buffers."""
+
+    def __init__(self, layer: PackedLayer, m: int, sign: torch.Tensor | None = None,
+                 fused: bool = False, device="cuda", zero_copy: bool | None = None):
+        super().__init__([(layer, m)], sign, fused, device, zero_copy)
+        self.layer, self.m, self.sign, self.fused = layer, m, sign, fused
+        self.x_host = self.calls[0].x_host
+        self.y_host = self.calls[0].y_host
 
     def launch(self, x: torch.Tensor | None = None):
         """Replay on the current stream without waiting."""

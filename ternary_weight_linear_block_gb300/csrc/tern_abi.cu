@@ -61,6 +61,32 @@ size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
   return 0;
 }
 
+int tern_host_accessible(const void* host) {
+  if (host == nullptr) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer == host ? 1 : 0;
+  if (a.type == cudaMemoryTypeUnregistered) {
+    // pageable memory: only where the GPU uses the host's page tables
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrPageableMemoryAccessUsesHostPageTables, dev) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return v ? 1 : 0;
+  }
+  return 0;
+}
+
 int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == TERN_OP_GEMV) return gemv_needs_fixup(M, N, K) ? 2 : 1;

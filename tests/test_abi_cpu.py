@@ -188,3 +188,9 @@ def test_fp16_variant_argument_errors(lib):
     assert _st("tern_gemm_prefill_fp16", *g(y=None)) == 1
     assert _st("tern_gemm_prefill_fp16", *g(y=FAKE + 2)) == 3
     assert _st("tern_gemm_prefill_fp16", *g(m=0)) == 0
+
+
+def test_host_accessible_query(lib):
+    assert B.lib().tern_host_accessible(None) == 0
+    if not torch.cuda.is_available():
+        assert B.lib().tern_host_accessible(FAKE) == 0        # no device: never

@@ -113,3 +113,45 @@ def test_decode_graph_matches_decode(fused):
         got = plan.run(x.cpu())
         B.tern_check()
         assert torch.equal(got, want.cpu())
+
+
+def test_decode_step_graph_matches_decode():
+    """B.DecodeStepGraph: several (layer, M) decode forwards in one graph, each
+    returning exactly what B.decode returns."""
+    d1 = I.make_layer(I.QKV, 4, seed=7)
+    d2 = I.make_layer(I.O_PROJ, 1, seed=8)
+    l1 = _layer(d1.codes, d1.scales)
+    l2 = _layer(d2.codes, d2.scales)
+    plan = B.DecodeStepGraph([(l1, 1), (l1, 4), (l2, 1)])
+    for seed in (9, 10):
+        xs = []
+        for i, (lay, m) in enumerate([(l1, 1), (l1, 4), (l2, 1)]):
+            bits, _ = I.make_activations(seed + 10 * i, m, lay.k, 0.001, 50.0)
+            xs.append(to_dev_bf16(bits))
+            plan.x_host[i].copy_(xs[-1].cpu())
+        got = plan.run()
+        B.tern_check()
+        for (lay, m), x, y in zip([(l1, 1), (l1, 4), (l2, 1)], xs, got):
+            assert torch.equal(y, B.decode(lay, x, B.Workspace()).cpu())
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_zero_copy_graph_matches_copies(fused):
+    """Zero-copy (kernels read x from and write y to pinned host memory) and
+    copying graphs return the same bits, at a fixup shape (M = 16) too."""
+    d = I.make_layer(I.QKV, 16, seed=11)
+    lay = _layer(d.codes, d.scales)
+    entries = [(lay, 1), (lay, 16)]
+    zc = B.DecodeStepGraph(entries, fused=fused, zero_copy=None)
+    cp = B.DecodeStepGraph(entries, fused=fused, zero_copy=False)
+    assert not cp.zero_copy
+    for i, (_, m) in enumerate(entries):
+        bits, _ = I.make_activations(12 + i, m, lay.k, 0.001, 50.0)
+        x = to_dev_bf16(bits).cpu()
+        zc.x_host[i].copy_(x)
+        cp.x_host[i].copy_(x)
+    a = zc.run()
+    b = cp.run()
+    B.tern_check()
+    for ya, yb in zip(a, b):
+        assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
