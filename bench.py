@@ -369,14 +369,17 @@ def run_prefill(args, local, m=2048):
         y = torch.empty((m, layer.n), dtype=torch.bfloat16, device="cuda")
         st = stream.cuda_stream
 
+        nbd = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, layer.n, layer.k)
+        wsd = B.Workspace().get(nbd) if nbd else None
+
         def step():
             B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_I8, xq, ts, st)
-            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y,
-                                     stream=st)
+            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y, None,
+                                     wsd, nbd, stream=st)
 
         def gemm_only():
-            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y,
-                                     stream=st)
+            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y, None,
+                                     wsd, nbd, stream=st)
 
         nbp = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, layer.n, layer.k)
         wsp = B.Workspace().get(nbp) if nbp else None
@@ -390,7 +393,7 @@ def run_prefill(args, local, m=2048):
         B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_DECODE, xh, xs, st)
 
         def fp16_only():
-            B.tern_gemm_prefill_fp16(xh, xs, w_h, m, layer.n, layer.k, y, st)
+            B.tern_gemm_prefill_fp16(xh, xs, w_h, m, layer.n, layer.k, y, wsd, nbd, st)
 
         for _ in range(max(3, args.warmup // 4)):
             step()
@@ -452,6 +455,8 @@ def run_mid_m(args, local, ms=(32, 64, 128, 256)):
                 y = torch.empty((m, shp.n), dtype=torch.bfloat16, device="cuda")
                 nb = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, shp.n, shp.k)
                 wsb = B.Workspace().get(nb) if nb else None
+                nbe = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, shp.n, shp.k)
+                wse = B.Workspace().get(nbe) if nbe else None
                 i = [0]
 
                 def packed():
@@ -463,8 +468,8 @@ def run_mid_m(args, local, ms=(32, 64, 128, 256)):
                 def expanded():
                     l = lays[i[0] % copies]
                     i[0] += 1
-                    B.tern_gemm_prefill_int8(xq, ts, l.w_q, l.rscale, m, shp.n, shp.k, y,
-                                             stream=st)
+                    B.tern_gemm_prefill_int8(xq, ts, l.w_q, l.rscale, m, shp.n, shp.k, y, None,
+                                             wse, nbe, stream=st)
 
                 for f in (packed, expanded):
                     for _ in range(3):
@@ -561,6 +566,8 @@ def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 16), prefill_ms=(128, 5
             nbs = [B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, shp.n, shp.k)
                    for shp in shapes]
             wsp = B.Workspace().get(max(nbs)) if max(nbs) else None
+            nbe = [B.tern_workspace_bytes(B.TERN_OP_GEMM, m, shp.n, shp.k) for shp in shapes]
+            wse = B.Workspace().get(max(nbe)) if max(nbe) else None
 
             def prefill_step(packed=False):
                 for row in layers:
@@ -573,7 +580,8 @@ def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 16), prefill_ms=(128, 5
                                                        wsp, nbs[si], stream=st)
                         else:
                             B.tern_gemm_prefill_int8(xq[si], ts[si], lay.w_q, lay.rscale, m,
-                                                     shp.n, shp.k, ys[si], stream=st)
+                                                     shp.n, shp.k, ys[si], None, wse, nbe[si],
+                                                     stream=st)
 
             prefill_step()
             prefill_step(packed=True)

@@ -287,7 +287,13 @@ tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uint16_t* xh, 
  *   w_q     fp16 [N][K] (tern_pack output),    rscale fp32 [N]
  *   y       bf16 [M][N]
  *   acc     int32 [M][N] or NULL
- *   ws      unused by this version (pass NULL, 0)
+ *   ws      optional device workspace (any contents) of
+ *           tern_workspace_bytes(TERN_OP_GEMM, M, N, K) bytes.  With it, a
+ *           call whose 128 x 256 tiles fill the GPU unevenly splits each
+ *           tile's K range in slices of whole 1024-chunks: the slices' exact
+ *           int32 partial sums go to planes of ws and a second kernel adds
+ *           them and rescales (same results bit for bit).  With NULL (or
+ *           less) the call runs unsplit.
  * Requirements: K % 1024 == 0, K <= 65536, M >= 0, N % 16 == 0, N >= 0.
  * Device-side waits are bounded; a wait that gives up makes the call's
  * outputs undefined and is reported by tern_check().
@@ -345,13 +351,16 @@ tern_status tern_gemm_prefill_packed(const uint16_t* xq, const float* tscale,
  *   with xh fp16 [M][K] and xs fp32 [M][K/1024] the decode operand of
  *   tern_fwht_quant(TERN_FWHT_DECODE) (any M), each block's sum accumulated
  *   in fp32 by the tensor cores and the blocks added in fp32 in order.
- *   y bf16 [M][N].  Requirements: K % 1024 == 0, K <= 65536, N % 16 == 0,
- *   0 <= M, N <= 2^24.
+ *   y bf16 [M][N].  ws: optional workspace as for tern_gemm_prefill_int8
+ *   (TERN_OP_GEMM); a split call adds fp32 slice sums in slice order, so
+ *   its rounding differs from the unsplit order.  Requirements:
+ *   K % 1024 == 0, K <= 65536, N % 16 == 0, 0 <= M, N <= 2^24.
  * ---------------------------------------------------------------------- */
 tern_status tern_expand_fp16(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
                              uint16_t* w_h, void* stream);
 tern_status tern_gemm_prefill_fp16(const uint16_t* xh, const float* xs, const uint16_t* w_h,
-                                   int64_t M, int64_t N, int64_t K, uint16_t* y, void* stream);
+                                   int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                                   size_t ws_bytes, void* stream);
 
 /* Workspace sizing and initialisation. */
 #define TERN_OP_GEMV 1
@@ -371,9 +380,10 @@ int tern_host_accessible(const void* host);
  * (0 for an empty call or an unknown op): for TERN_OP_GEMV the GEMV kernel,
  * plus the fixup kernel when a 512-row block is shared by more CTAs than the
  * GEMV sums in place (tern_gemv_decode, tern_linear_decode and
- * tern_gemv_decode_noalloc launch the same count); for TERN_OP_GEMM the one
- * int8 GEMM kernel; for TERN_OP_GEMM_PACKED the GEMM, plus the rescale
- * kernel when its tiles are split along K.  Host-only; launch counting for
+ * tern_gemv_decode_noalloc launch the same count); for TERN_OP_GEMM the
+ * int8 (or fp16) GEMM, plus its finishing kernel when it is given the
+ * workspace and splits K; for TERN_OP_GEMM_PACKED the GEMM, plus the
+ * rescale kernel when its tiles are split along K.  Host-only; launch counting for
  * CUDA-graph sizing and profiling. */
 int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K);
 /* Zero-fill `bytes` of device memory at ws on `stream` (asynchronous). */

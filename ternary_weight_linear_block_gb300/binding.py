@@ -49,7 +49,7 @@ _SIGS = {
     "tern_fwht_quant": (ctypes.c_int, [_p, _i64, _i64, _p, ctypes.c_int, _p, _p, _p]),
     "tern_gemv_decode": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
     "tern_expand_fp16": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p]),
-    "tern_gemm_prefill_fp16": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
+    "tern_gemm_prefill_fp16": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
     "tern_fwht_shard": (ctypes.c_int, [_p, _i64, _i64, ctypes.c_int, ctypes.c_int, _p, _p, _p, _p,
                                        _p]),
     "tern_fwht_combine": (ctypes.c_int, [_p, _p, _i64, ctypes.c_int, _p, _i64, _i64, _p]),
@@ -181,9 +181,9 @@ def tern_expand_fp16(codes, scales, n, k, w_h, stream=None):
     return _call("tern_expand_fp16", _ptr(codes), _ptr(scales), n, k, _ptr(w_h), _stream(stream))
 
 
-def tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y, stream=None):
+def tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y, ws=None, ws_bytes=0, stream=None):
     return _call("tern_gemm_prefill_fp16", _ptr(xh), _ptr(xs), _ptr(w_h), m, n, k, _ptr(y),
-                 _stream(stream))
+                 _ptr(ws), ws_bytes, _stream(stream))
 
 
 def tern_fwht_shard(x, m, kr, lead, trail, sign, xr, h_lead, h_trail, stream=None):
@@ -430,7 +430,7 @@ def expand_fp16(codes: torch.Tensor, scales: torch.Tensor, stream=None) -> torch
 
 
 def prefill_fp16(w_h: torch.Tensor, x: torch.Tensor, y: torch.Tensor | None = None, sign=None,
-                 stream=None) -> torch.Tensor:
+                 stream=None, ws: Workspace | None = None) -> torch.Tensor:
     """fp16 prefill variant: rotation to the decode operand (fp16 + per-block
     factors), then one tensor-core GEMM against w_h with the factors applied
     per 1024-block in the epilogue."""
@@ -439,7 +439,9 @@ def prefill_fp16(w_h: torch.Tensor, x: torch.Tensor, y: torch.Tensor | None = No
     xh, xs = fwht(x, TERN_FWHT_DECODE, sign, stream)
     if y is None:
         y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
-    tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y, stream)
+    nb = tern_workspace_bytes(TERN_OP_GEMM, m, n, k)
+    buf = (ws or Workspace(x.device)).get(nb, stream) if nb > 0 else None
+    tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y, buf, nb, stream)
     return y
 
 
@@ -463,6 +465,8 @@ def prefill(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,
                                  layer.k, y, acc, buf, 0 if buf is None else buf.numel(),
                                  stream=stream)
     else:
+        nb = tern_workspace_bytes(TERN_OP_GEMM, m, layer.n, layer.k)
+        buf = (ws or Workspace(x.device)).get(nb, stream) if nb > 0 else None
         tern_gemm_prefill_int8(xq, ts, layer.w_q, layer.rscale, m, layer.n, layer.k, y, acc,
-                               stream=stream)
+                               buf, nb, stream=stream)
     return y

@@ -67,12 +67,18 @@ __device__ __forceinline__ void fail(volatile int* abort_flag, unsigned int code
 // each 1024-chunk of K is one rotation block, so the epilogue multiplies the
 // chunk's fp32 sum by the token's block factor (`tscale` holds xs [M][K/1024])
 // and adds the chunks in fp32; `rscale` and `acc_out` are unused.
-template <bool FP>
+// With S > 1 every tile's K range is cut in S slices of whole 1024-chunks
+// (units of work = (tile, slice)); a slice stores its partial sums (int32 or
+// fp32) in its plane of `part` [S][M][N] and a second kernel adds the planes
+// in slice order and finishes the output.
+template <bool FP, bool SPLIT>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const float* __restrict__ tscale,
                                           const float* __restrict__ rscale, int M, int N, int K,
                                           __nv_bfloat16* __restrict__ y,
-                                          int32_t* __restrict__ acc_out) {
+                                          int32_t* __restrict__ acc_out, int S_arg,
+                                          void* __restrict__ part) {
+  const int S = SPLIT ? S_arg : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -91,8 +97,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   const int m_blocks = (M + BM - 1) / BM;
   const int n_blocks = (N + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
-  const int kstages = K / BK;
   const int chunks = K / KCHUNK;
+  const int units = tiles * S;
   constexpr int kStagesPerChunk = KCHUNK / BK;
 
   if (threadIdx.x == 0) {
@@ -131,9 +137,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       uint32_t phase = 0;
       long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int tile = u / S, sl = u % S;
         const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
-        for (int ks = 0; ks < kstages; ++ks) {
+        const int ks1 = (sl + 1) * chunks / S * kStagesPerChunk;
+        for (int ks = sl * chunks / S * kStagesPerChunk; ks < ks1; ++ks) {
           if (!ptx::mbar_wait(&empty[s], phase ^ 1u, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
             ok = false;
@@ -171,8 +179,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       uint32_t phase = 0;
       uint32_t cc = 0;   // chunk counter across tiles
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-        for (int c = 0; c < chunks && ok; ++c, ++cc) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int sl = u % S;
+        for (int c = sl * chunks / S; c < (sl + 1) * chunks / S && ok; ++c, ++cc) {
           const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
           if (!ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_MMA);
@@ -214,13 +223,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     const int q = warp & 3;   // TMEM lane quarter accessible to this warp
     uint32_t cc = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int tile = u / S, sl = u % S;
       const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
       const int row = m_blk * BM + 32 * q + lane;
       typename std::conditional<FP, float, int32_t>::type sums[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sums[i] = 0;
-      for (int c = 0; c < chunks; ++c, ++cc) {
+      for (int c = sl * chunks / S; c < (sl + 1) * chunks / S; ++c, ++cc) {
         const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
         if (!ptx::mbar_wait(&dfull[buf], dph, abort_flag, WAIT_LIMIT)) {
           if (!*abort_flag) fail(abort_flag, ERR_EPILOGUE);
@@ -251,6 +261,28 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         if (lane == 0) ptx::mbar_arrive(&dempty[buf]);
       }
       if (!ok) break;
+      if constexpr (SPLIT) {
+        // this slice's partial sums into its plane; the finishing kernel adds them
+        if (row < M) {
+          const int n0 = n_blk * BN + wg * 128;
+          auto* prow = static_cast<typename std::conditional<FP, float, int32_t>::type*>(part) +
+                       (static_cast<long>(sl) * M + row) * N + n0;
+#pragma unroll
+          for (int j = 0; j < 128; j += 8)
+            if (n0 + j < N) {
+              if constexpr (FP) {
+                float4* pp = reinterpret_cast<float4*>(prow + j);
+                pp[0] = make_float4(sums[j], sums[j + 1], sums[j + 2], sums[j + 3]);
+                pp[1] = make_float4(sums[j + 4], sums[j + 5], sums[j + 6], sums[j + 7]);
+              } else {
+                int4* pp = reinterpret_cast<int4*>(prow + j);
+                pp[0] = make_int4(sums[j], sums[j + 1], sums[j + 2], sums[j + 3]);
+                pp[1] = make_int4(sums[j + 4], sums[j + 5], sums[j + 6], sums[j + 7]);
+              }
+            }
+        }
+        continue;
+      }
       if (FP && row < M) {
         const int n0 = n_blk * BN + wg * 128;
         __nv_bfloat16* yrow = y + static_cast<long>(row) * N;
@@ -314,18 +346,54 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   }
 }
 
+// SPLIT = false: one unit per tile (no slice arithmetic in the loops);
+// SPLIT = true: S K slices per tile, partial sums to `part`.
+template <bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float* __restrict__ tscale, const float* __restrict__ rscale, int M,
-                   int N, int K, __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out) {
-  gemm_body<false>(tmA, tmB, tscale, rscale, M, N, K, y, acc_out);
+                   int N, int K, __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out,
+                   int S, int32_t* __restrict__ part) {
+  gemm_body<false, SPLIT>(tmA, tmB, tscale, rscale, M, N, K, y, acc_out, S, part);
 }
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const float* __restrict__ xs, int M, int N, int K,
-                    __nv_bfloat16* __restrict__ y) {
-  gemm_body<true>(tmA, tmB, xs, nullptr, M, N, K, y, nullptr);
+                    __nv_bfloat16* __restrict__ y, int S, float* __restrict__ part) {
+  gemm_body<true, SPLIT>(tmA, tmB, xs, nullptr, M, N, K, y, nullptr, S, part);
+}
+
+// After a split fp16 GEMM: y = bf16_rn(sum of the S planes, added in slice
+// order); one thread per 8 outputs of a row (N % 16 == 0).
+__global__ void __launch_bounds__(256)
+    f16_finalize_kernel(const float* __restrict__ part, int S, int M, int N,
+                        __nv_bfloat16* __restrict__ y) {
+  pdl_launch_dependents();
+  const long i = static_cast<long>(blockIdx.x) * 256 + threadIdx.x;
+  const long per_row = N / 8;
+  const long row = i / per_row;
+  const int n = static_cast<int>(i % per_row) * 8;
+  pdl_wait();
+  if (row >= M) return;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int sl = 0; sl < S; ++sl) {
+    const float* p = part + (static_cast<long>(sl) * M + row) * N + n;
+    const float4 a0 = __ldcs(reinterpret_cast<const float4*>(p));
+    const float4 a1 = __ldcs(reinterpret_cast<const float4*>(p + 4));
+    a[0] = __fadd_rn(a[0], a0.x); a[1] = __fadd_rn(a[1], a0.y);
+    a[2] = __fadd_rn(a[2], a0.z); a[3] = __fadd_rn(a[3], a0.w);
+    a[4] = __fadd_rn(a[4], a1.x); a[5] = __fadd_rn(a[5], a1.y);
+    a[6] = __fadd_rn(a[6], a1.z); a[7] = __fadd_rn(a[7], a1.w);
+  }
+  uint32_t out[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a[2 * t], a[2 * t + 1]);
+    out[t] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(y + row * N + n) = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 
@@ -841,23 +909,74 @@ int sm_count() {
 
 }  // namespace
 
+// K slices per tile of the expanded-weight GEMMs (whole 1024-chunks): the
+// count with the least estimated time, (units per CTA) x (chunks per slice) x
+// (one tile-chunk, ~5.9 us measured on GB300) plus writing and reading the
+// S partial planes; 1 when the tiles already fill the GPU evenly.
+int dense_splits(int64_t M, int64_t N, int64_t K) {
+  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const long sms = sm_count();
+  const long chunks = K / KCHUNK;
+  const double t_chunk = 5.9e-6, bw = 6.0e12, t_launch = 3e-6;
+  double best = 0.0;
+  int best_s = 1;
+  for (long S = 1; S <= chunks && S <= 32; ++S) {
+    const long per_cta = (tiles * S + sms - 1) / sms;
+    const long slice = (chunks + S - 1) / S;
+    double t = static_cast<double>(per_cta * slice) * t_chunk;
+    if (S > 1) t += (2.0 * S * M * N * 4 + 2.0 * M * N) / bw + t_launch;
+    if (S == 1 || t < 0.97 * best) {   // a split has to win clearly
+      best = t;
+      best_s = static_cast<int>(S);
+    }
+  }
+  return best_s;
+}
+
+size_t gemm_dense_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int S = dense_splits(M, N, K);
+  return S > 1 ? static_cast<size_t>(S) * M * N * 4 : 0;
+}
+
+namespace {
+// The split to use: dense_splits' choice when the caller gave a large enough
+// workspace, else 1.
+int usable_splits(int64_t M, int64_t N, int64_t K, const void* ws, size_t ws_bytes) {
+  const int S = dense_splits(M, N, K);
+  if (S > 1 && (ws == nullptr || ws_bytes < static_cast<size_t>(S) * M * N * 4)) return 1;
+  return S;
+}
+}  // namespace
+
 cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
                         const float* rscale, int64_t M, int64_t N, int64_t K, uint16_t* y,
-                        int32_t* acc, cudaStream_t st) {
+                        int32_t* acc, void* ws, size_t ws_bytes, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!make_map(&ta, xq, M, K, BM) || !make_map(&tb, w_q, N, K, BN)) return cudaErrorInvalidValue;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
+    for (auto* kern : {gemm_i8_kernel<false>, gemm_i8_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(SMEM_BYTES));
+      if (e != cudaSuccess) return e;
+    }
     attr_done = true;
   }
-  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  return launch(gemm_i8_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, tscale,
-                rscale, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                reinterpret_cast<__nv_bfloat16*>(y), acc);
+  const int S = usable_splits(M, N, K, ws, ws_bytes);
+  int32_t* part = S > 1 ? static_cast<int32_t*>(ws) : nullptr;
+  const long units = ((M + BM - 1) / BM) * ((N + BN - 1) / BN) * S;
+  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
+  cudaError_t e = launch(S > 1 ? gemm_i8_kernel<true> : gemm_i8_kernel<false>, dim3(grid),
+                         dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, tscale, rscale,
+                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                         reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
+  if (e != cudaSuccess || S == 1) return e;
+  const long threads = M * N / 8;
+  return launch(packed_finalize_kernel, dim3(static_cast<unsigned>((threads + FIN_THREADS - 1) /
+                                                                   FIN_THREADS)),
+                dim3(FIN_THREADS), 0, st, static_cast<const int32_t*>(part), S, tscale, rscale,
+                static_cast<int>(M), static_cast<int>(N), reinterpret_cast<__nv_bfloat16*>(y),
+                acc);
 }
 
 // K slices per tile of the packed GEMM: 1 when the tiles alone fill most of
@@ -915,22 +1034,32 @@ cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const ui
 }
 
 cudaError_t launch_gemm_f16(const uint16_t* xh, const float* xs, const uint16_t* w_h, int64_t M,
-                            int64_t N, int64_t K, uint16_t* y, cudaStream_t st) {
+                            int64_t N, int64_t K, uint16_t* y, void* ws, size_t ws_bytes,
+                            cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!make_map(&ta, xh, M, K, BM) || !make_map(&tb, w_h, N, K, BN)) return cudaErrorInvalidValue;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_f16_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
+    for (auto* kern : {gemm_f16_kernel<false>, gemm_f16_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(SMEM_BYTES));
+      if (e != cudaSuccess) return e;
+    }
     attr_done = true;
   }
-  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  return launch(gemm_f16_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, xs,
-                static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                reinterpret_cast<__nv_bfloat16*>(y));
+  const int S = usable_splits(M, N, K, ws, ws_bytes);
+  float* part = S > 1 ? static_cast<float*>(ws) : nullptr;
+  const long units = ((M + BM - 1) / BM) * ((N + BN - 1) / BN) * S;
+  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
+  cudaError_t e = launch(S > 1 ? gemm_f16_kernel<true> : gemm_f16_kernel<false>, dim3(grid),
+                         dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, xs, static_cast<int>(M),
+                         static_cast<int>(N), static_cast<int>(K),
+                         reinterpret_cast<__nv_bfloat16*>(y), S, part);
+  if (e != cudaSuccess || S == 1) return e;
+  const long threads = M * N / 8;
+  return launch(f16_finalize_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
+                0, st, static_cast<const float*>(part), S, static_cast<int>(M),
+                static_cast<int>(N), reinterpret_cast<__nv_bfloat16*>(y));
 }
 
 cudaError_t gemm_read_clear_error(unsigned int* err) {

@@ -58,6 +58,7 @@ size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == TERN_OP_GEMV) return gemv_workspace_bytes(M, N, K);
   if (op == TERN_OP_GEMM_PACKED) return gemm_packed_workspace_bytes(M, N, K);
+  if (op == TERN_OP_GEMM) return gemm_dense_workspace_bytes(M, N, K);
   return 0;
 }
 
@@ -90,7 +91,7 @@ int tern_host_accessible(const void* host) {
 int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == TERN_OP_GEMV) return gemv_needs_fixup(M, N, K) ? 2 : 1;
-  if (op == TERN_OP_GEMM) return 1;
+  if (op == TERN_OP_GEMM) return dense_splits(M, N, K) > 1 ? 2 : 1;
   if (op == TERN_OP_GEMM_PACKED) return packed_splits(M, N, K) > 1 ? 2 : 1;
   return 0;
 }
@@ -225,8 +226,6 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
                                    const float* rscale, int64_t M, int64_t N, int64_t K,
                                    uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
                                    void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
   if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
   if (N % 16 != 0) return TERN_ERR_SHAPE;
@@ -236,10 +235,10 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
   if (xq == nullptr || tscale == nullptr || w_q == nullptr || rscale == nullptr || y == nullptr)
     return TERN_ERR_INVALID_ARG;
   if (!aligned16(xq) || !aligned16(tscale) || !aligned16(w_q) || !aligned16(rscale) ||
-      !aligned16(y) || (acc && !aligned16(acc)))
+      !aligned16(y) || (acc && !aligned16(acc)) || (ws && !aligned16(ws)))
     return TERN_ERR_ALIGN;
   if (!device_supported()) return TERN_ERR_UNSUPPORTED;
-  return from_cuda(launch_gemm(xq, tscale, w_q, rscale, M, N, K, y, acc,
+  return from_cuda(launch_gemm(xq, tscale, w_q, rscale, M, N, K, y, acc, ws, ws_bytes,
                                static_cast<cudaStream_t>(stream)));
 }
 
@@ -281,7 +280,8 @@ tern_status tern_expand_fp16(const int8_t* codes, const uint16_t* scales, int64_
 }
 
 tern_status tern_gemm_prefill_fp16(const uint16_t* xh, const float* xs, const uint16_t* w_h,
-                                   int64_t M, int64_t N, int64_t K, uint16_t* y, void* stream) {
+                                   int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
+                                   size_t ws_bytes, void* stream) {
   if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
   if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
   if (N % 16 != 0) return TERN_ERR_SHAPE;
@@ -289,9 +289,12 @@ tern_status tern_gemm_prefill_fp16(const uint16_t* xh, const float* xs, const ui
   if ((M + 127) / 128 * ((N + 255) / 256) >= (int64_t(1) << 31)) return TERN_ERR_SHAPE;
   if (M == 0 || N == 0) return TERN_OK;
   if (xh == nullptr || xs == nullptr || w_h == nullptr || y == nullptr) return TERN_ERR_INVALID_ARG;
-  if (!aligned16(xh) || !aligned16(xs) || !aligned16(w_h) || !aligned16(y)) return TERN_ERR_ALIGN;
+  if (!aligned16(xh) || !aligned16(xs) || !aligned16(w_h) || !aligned16(y) ||
+      (ws && !aligned16(ws)))
+    return TERN_ERR_ALIGN;
   if (!device_supported()) return TERN_ERR_UNSUPPORTED;
-  return from_cuda(launch_gemm_f16(xh, xs, w_h, M, N, K, y, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_gemm_f16(xh, xs, w_h, M, N, K, y, ws, ws_bytes,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 tern_status tern_check(void* stream) {

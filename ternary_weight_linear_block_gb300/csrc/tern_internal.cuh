@@ -60,11 +60,14 @@ cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* 
 cudaError_t launch_linear_decode(const uint16_t* x, const int8_t* sign, const uint8_t* packed,
                                  int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
                                  cudaStream_t st);
+int dense_splits(int64_t M, int64_t N, int64_t K);
+size_t gemm_dense_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
                         const float* rscale, int64_t M, int64_t N, int64_t K, uint16_t* y,
-                        int32_t* acc, cudaStream_t st);
+                        int32_t* acc, void* ws, size_t ws_bytes, cudaStream_t st);
 cudaError_t launch_gemm_f16(const uint16_t* xh, const float* xs, const uint16_t* w_h, int64_t M,
-                            int64_t N, int64_t K, uint16_t* y, cudaStream_t st);
+                            int64_t N, int64_t K, uint16_t* y, void* ws, size_t ws_bytes,
+                            cudaStream_t st);
 cudaError_t launch_expand_fp16(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
                                uint16_t* w_h, cudaStream_t st);
 size_t gemm_packed_workspace_bytes(int64_t M, int64_t N, int64_t K);

@@ -166,7 +166,9 @@ class GpuOps:
         y = torch.empty((m, lin.n), dtype=torch.bfloat16, device=xr.device)
         lay = lin.layer
         if lay.w_q is not None:
-            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, lin.n, kp, y)
+            nb = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, lin.n, kp)
+            buf = ws.get(nb) if nb else None
+            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, lin.n, kp, y, None, buf, nb)
         else:
             nb = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, lin.n, kp)
             buf = ws.get(nb) if nb else None

@@ -182,12 +182,18 @@ def test_fp16_variant_argument_errors(lib):
     assert _st("tern_expand_fp16", FAKE, FAKE, 16, 1024, None, None) == 1
     assert _st("tern_expand_fp16", FAKE + 1, FAKE, 16, 1024, FAKE, None) == 3
     assert _st("tern_expand_fp16", FAKE, FAKE, 0, 1024, FAKE, None) == 0
-    g = lambda m=64, n=256, k=1024, y=FAKE: (FAKE, FAKE, FAKE, m, n, k, y, None)
+    g = lambda m=64, n=256, k=1024, y=FAKE, ws=None: (FAKE, FAKE, FAKE, m, n, k, y, ws, 0, None)
     assert _st("tern_gemm_prefill_fp16", *g(n=250)) == 2
     assert _st("tern_gemm_prefill_fp16", *g(k=1536)) == 2
     assert _st("tern_gemm_prefill_fp16", *g(y=None)) == 1
     assert _st("tern_gemm_prefill_fp16", *g(y=FAKE + 2)) == 3
+    assert _st("tern_gemm_prefill_fp16", *g(ws=FAKE + 4)) == 3
     assert _st("tern_gemm_prefill_fp16", *g(m=0)) == 0
+    # the expanded GEMMs' optional split: 20 tiles of down at 128 tokens
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMM, 128, 5120, 17408) > 0
+    assert B.tern_kernel_launches(B.TERN_OP_GEMM, 128, 5120, 17408) == 2
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMM, 2048, 34816, 5120) == 0
+    assert B.tern_kernel_launches(B.TERN_OP_GEMM, 2048, 34816, 5120) == 1
 
 
 def test_host_accessible_query(lib):

@@ -98,3 +98,27 @@ def test_zero_and_empty():
     B.tern_check()
     assert not bf16_to_f32(y).any()
     B.tern_gemm_prefill_fp16(xh, xs, w_h, 0, n, k, y)
+
+
+def test_split_k_within_rounding():
+    """Split along K (workspace given), the fp32 slice sums are added in slice
+    order: the same output up to fp32 rounding."""
+    m, n, k = 128, 5120, 17408
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMM, m, n, k) > 0
+    codes = I.make_codes(24, n, k)
+    scales = I.make_scales(24, n, k)
+    bits, x = I.make_activations(24, m, k, 0.001, 50.0)
+    w_h = B.expand_fp16(to_dev(codes), to_dev(scales))
+    xh, xs = B.fwht(to_dev_bf16(bits), B.TERN_FWHT_DECODE)
+    y0 = poison(torch.empty((m, n), dtype=torch.bfloat16, device="cuda"))
+    y1 = poison(torch.empty((m, n), dtype=torch.bfloat16, device="cuda"))
+    B.tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y0)
+    nb = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, n, k)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    B.tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y1, ws, nb)
+    B.tern_check()
+    a, b = bf16_to_f32(y0), bf16_to_f32(y1)
+    assert O.rel_frobenius(b, a) <= 2e-3
+    rows = np.sort(np.random.default_rng(7).choice(n, 128, replace=False))
+    exact = O.linear_f64(x, codes[rows], scales[rows])
+    assert O.rel_frobenius(b[:, rows], exact) <= 4e-3

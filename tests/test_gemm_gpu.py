@@ -116,3 +116,32 @@ def test_zero_operands():
     acc, y = _gemm_raw(np.zeros((m, k), np.int16), np.zeros(m, np.float32),
                        np.zeros((n, k), np.int16), np.zeros(n, np.float32))
     assert not acc.any() and not y.any()
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 5120, 17408), (40, 1024, 5120), (512, 5120, 17408)])
+def test_split_k_is_bit_identical(m, n, k):
+    """With a workspace, calls whose tiles fill the GPU unevenly split K in
+    slices of whole chunks; the int32 partials are exact, so acc and y equal
+    the unsplit call's bit for bit (and the integer oracle on a sample)."""
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMM, m, n, k) > 0
+    codes = I.make_codes(23, n, k)
+    scales = I.make_scales(23, n, k)
+    bits, x = I.make_activations(23, m, k, 0.001, 50.0)
+    layer = B.pack_layer(to_dev(codes), to_dev(scales), decode=False, prefill=True)
+    xq, ts = B.fwht(to_dev_bf16(bits), B.TERN_FWHT_I8)
+    outs = []
+    for split in (False, True):
+        y = poison(torch.empty((m, n), dtype=torch.bfloat16, device="cuda"))
+        acc = poison(torch.empty((m, n), dtype=torch.int32, device="cuda"))
+        nb = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, n, k) if split else 0
+        ws = torch.full((max(nb, 16),), 0x5A, dtype=torch.uint8, device="cuda")
+        B.tern_gemm_prefill_int8(xq, ts, layer.w_q, layer.rscale, m, n, k, y, acc,
+                                 ws if split else None, nb)
+        outs.append((acc, y))
+    B.tern_check()
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
+    rows = np.sort(np.random.default_rng(6).choice(n, 64, replace=False))
+    r = O.linear_int8(x, codes[rows], scales[rows])
+    assert np.array_equal(outs[1][0][:, torch.from_numpy(rows).cuda()].cpu().numpy()
+                          .astype(np.int64), r["acc"])
