@@ -189,3 +189,25 @@ def test_zero_and_empty():
                                0, n, k, y, acc)
     B.tern_gemm_prefill_packed(xq, to_dev(np.ones(m, np.float32)), lay.packed, lay.q, lay.rscale,
                                m, 0, k, y, acc)
+
+
+@pytest.mark.parametrize("m", [4, 16, 17, 128, 129, 300])
+def test_forward_picks_the_path(m):
+    """binding.forward: the decode GEMV up to 16 tokens, the packed GEMM up to
+    128, the expanded GEMM above -- each call equal to its path's own call."""
+    n, k = 512, 2048
+    codes = I.make_codes(33, n, k)
+    scales = I.make_scales(33, n, k)
+    bits, x = I.make_activations(33, m, k, 0.001, 50.0)
+    lay = _layer(codes, scales, expand=True)
+    xd = to_dev_bf16(bits)
+    ws = B.Workspace()
+    got = B.forward(lay, xd, ws=ws)
+    if m <= 16:
+        want = B.decode(lay, xd, ws)
+    else:
+        want = B.prefill(lay, xd, from_packed=m <= 128, ws=ws)
+    B.tern_check()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    tol = 4e-3 if m <= 16 else 2e-2
+    assert O.rel_frobenius(bf16_to_f32(got), O.linear_f64(x, codes, scales)) <= tol
