@@ -77,7 +77,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                                           const float* __restrict__ rscale, int M, int N, int K,
                                           __nv_bfloat16* __restrict__ y,
                                           int32_t* __restrict__ acc_out, int S_arg,
-                                          void* __restrict__ part) {
+                                          int full_arg, void* __restrict__ part) {
   const int S = SPLIT ? S_arg : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -98,8 +98,27 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   const int n_blocks = (N + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
   const int chunks = K / KCHUNK;
-  const int units = tiles * S;
+  // units: the first n_whole tiles whole, then every later tile in S slices
+  const int n_whole = SPLIT ? full_arg : tiles;
+  const int units = n_whole + (tiles - n_whole) * S;
   constexpr int kStagesPerChunk = KCHUNK / BK;
+  // tile and chunk range [c0, c1) of unit u; piece = its slice index among
+  // all slices (-1 for a whole tile)
+  auto unit_of = [&](int u, int& tile, int& c0, int& c1, int& piece) {
+    if (!SPLIT || u < n_whole) {
+      tile = u;
+      c0 = 0;
+      c1 = chunks;
+      piece = -1;
+    } else {
+      const int v = u - n_whole;
+      const int sl = v % S;
+      tile = n_whole + v / S;
+      c0 = sl * chunks / S;
+      c1 = (sl + 1) * chunks / S;
+      piece = v;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -138,10 +157,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       long issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const int tile = u / S, sl = u % S;
+        int tile, c0, c1, piece;
+        unit_of(u, tile, c0, c1, piece);
         const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
-        const int ks1 = (sl + 1) * chunks / S * kStagesPerChunk;
-        for (int ks = sl * chunks / S * kStagesPerChunk; ks < ks1; ++ks) {
+        const int ks1 = c1 * kStagesPerChunk;
+        for (int ks = c0 * kStagesPerChunk; ks < ks1; ++ks) {
           if (!ptx::mbar_wait(&empty[s], phase ^ 1u, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
             ok = false;
@@ -180,8 +200,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       uint32_t cc = 0;   // chunk counter across tiles
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const int sl = u % S;
-        for (int c = sl * chunks / S; c < (sl + 1) * chunks / S && ok; ++c, ++cc) {
+        int tile, c0, c1, piece;
+        unit_of(u, tile, c0, c1, piece);
+        for (int c = c0; c < c1 && ok; ++c, ++cc) {
           const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
           if (!ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_MMA);
@@ -224,13 +245,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     uint32_t cc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const int tile = u / S, sl = u % S;
+      int tile, c0, c1, piece;
+      unit_of(u, tile, c0, c1, piece);
       const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
       const int row = m_blk * BM + 32 * q + lane;
       typename std::conditional<FP, float, int32_t>::type sums[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sums[i] = 0;
-      for (int c = sl * chunks / S; c < (sl + 1) * chunks / S; ++c, ++cc) {
+      for (int c = c0; c < c1; ++c, ++cc) {
         const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
         if (!ptx::mbar_wait(&dfull[buf], dph, abort_flag, WAIT_LIMIT)) {
           if (!*abort_flag) fail(abort_flag, ERR_EPILOGUE);
@@ -261,12 +283,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         if (lane == 0) ptx::mbar_arrive(&dempty[buf]);
       }
       if (!ok) break;
-      if constexpr (SPLIT) {
-        // this slice's partial sums into its plane; the finishing kernel adds them
+      if (SPLIT && piece >= 0) {
+        // one slice of a split tile: its partial sums into the slice's
+        // [128][256] piece of `part`; the finishing kernel adds the pieces
         if (row < M) {
           const int n0 = n_blk * BN + wg * 128;
           auto* prow = static_cast<typename std::conditional<FP, float, int32_t>::type*>(part) +
-                       (static_cast<long>(sl) * M + row) * N + n0;
+                       (static_cast<long>(piece) * BM + 32 * q + lane) * BN + wg * 128;
 #pragma unroll
           for (int j = 0; j < 128; j += 8)
             if (n0 + j < N) {
@@ -353,45 +376,84 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float* __restrict__ tscale, const float* __restrict__ rscale, int M,
                    int N, int K, __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out,
-                   int S, int32_t* __restrict__ part) {
-  gemm_body<false, SPLIT>(tmA, tmB, tscale, rscale, M, N, K, y, acc_out, S, part);
+                   int S, int full, int32_t* __restrict__ part) {
+  gemm_body<false, SPLIT>(tmA, tmB, tscale, rscale, M, N, K, y, acc_out, S, full, part);
 }
 
 template <bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const float* __restrict__ xs, int M, int N, int K,
-                    __nv_bfloat16* __restrict__ y, int S, float* __restrict__ part) {
-  gemm_body<true, SPLIT>(tmA, tmB, xs, nullptr, M, N, K, y, nullptr, S, part);
+                    __nv_bfloat16* __restrict__ y, int S, int full, float* __restrict__ part) {
+  gemm_body<true, SPLIT>(tmA, tmB, xs, nullptr, M, N, K, y, nullptr, S, full, part);
 }
 
-// After a split fp16 GEMM: y = bf16_rn(sum of the S planes, added in slice
-// order); one thread per 8 outputs of a row (N % 16 == 0).
+// After a split GEMM: for every split tile (tiles full .. tiles-1), add its
+// S pieces in slice order and finish the output -- int8 path: the exact sum,
+// rescaled (and stored to acc when given); fp16 path: bf16 of the fp32 sum.
+// One thread per 8 outputs of a tile row.
+template <bool FP>
 __global__ void __launch_bounds__(256)
-    f16_finalize_kernel(const float* __restrict__ part, int S, int M, int N,
-                        __nv_bfloat16* __restrict__ y) {
+    split_finalize_kernel(const void* __restrict__ part, int S, int full, int n_split,
+                          int m_blocks, int M, int N, const float* __restrict__ tscale,
+                          const float* __restrict__ rscale, __nv_bfloat16* __restrict__ y,
+                          int32_t* __restrict__ acc_out) {
   pdl_launch_dependents();
   const long i = static_cast<long>(blockIdx.x) * 256 + threadIdx.x;
-  const long per_row = N / 8;
-  const long row = i / per_row;
-  const int n = static_cast<int>(i % per_row) * 8;
-  pdl_wait();
-  if (row >= M) return;
-  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  constexpr int PER_ROW = BN / 8;
+  const long st = i / (BM * PER_ROW);
+  const int r = static_cast<int>((i / PER_ROW) % BM);
+  const int c8 = static_cast<int>(i % PER_ROW);
+  pdl_wait();   // the GEMM's pieces
+  if (st >= n_split) return;
+  const int tile = full + static_cast<int>(st);
+  const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
+  const long row = static_cast<long>(m_blk) * BM + r;
+  const int n = n_blk * BN + c8 * 8;
+  if (row >= M || n >= N) return;
+  typename std::conditional<FP, float, int>::type a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int sl = 0; sl < S; ++sl) {
-    const float* p = part + (static_cast<long>(sl) * M + row) * N + n;
-    const float4 a0 = __ldcs(reinterpret_cast<const float4*>(p));
-    const float4 a1 = __ldcs(reinterpret_cast<const float4*>(p + 4));
-    a[0] = __fadd_rn(a[0], a0.x); a[1] = __fadd_rn(a[1], a0.y);
-    a[2] = __fadd_rn(a[2], a0.z); a[3] = __fadd_rn(a[3], a0.w);
-    a[4] = __fadd_rn(a[4], a1.x); a[5] = __fadd_rn(a[5], a1.y);
-    a[6] = __fadd_rn(a[6], a1.z); a[7] = __fadd_rn(a[7], a1.w);
+    const long off = ((st * S + sl) * BM + r) * BN + c8 * 8;
+    if constexpr (FP) {
+      const float* p = static_cast<const float*>(part) + off;
+      const float4 a0 = __ldcs(reinterpret_cast<const float4*>(p));
+      const float4 a1 = __ldcs(reinterpret_cast<const float4*>(p + 4));
+      a[0] = __fadd_rn(a[0], a0.x); a[1] = __fadd_rn(a[1], a0.y);
+      a[2] = __fadd_rn(a[2], a0.z); a[3] = __fadd_rn(a[3], a0.w);
+      a[4] = __fadd_rn(a[4], a1.x); a[5] = __fadd_rn(a[5], a1.y);
+      a[6] = __fadd_rn(a[6], a1.z); a[7] = __fadd_rn(a[7], a1.w);
+    } else {
+      const int32_t* p = static_cast<const int32_t*>(part) + off;
+      const int4 a0 = __ldcs(reinterpret_cast<const int4*>(p));
+      const int4 a1 = __ldcs(reinterpret_cast<const int4*>(p + 4));
+      a[0] += a0.x; a[1] += a0.y; a[2] += a0.z; a[3] += a0.w;
+      a[4] += a1.x; a[5] += a1.y; a[6] += a1.z; a[7] += a1.w;
+    }
   }
   uint32_t out[4];
+  if constexpr (FP) {
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a[2 * t], a[2 * t + 1]);
-    out[t] = *reinterpret_cast<uint32_t*>(&h);
+    for (int t = 0; t < 4; ++t) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(a[2 * t], a[2 * t + 1]);
+      out[t] = *reinterpret_cast<uint32_t*>(&h);
+    }
+  } else {
+    const float4 r0 = __ldg(reinterpret_cast<const float4*>(rscale + n));
+    const float4 r1 = __ldg(reinterpret_cast<const float4*>(rscale + n + 4));
+    const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    const float ts = tscale[row];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float f0 = __fmul_rn(__fmul_rn(__int2float_rn(a[2 * t]), ts), rr[2 * t]);
+      const float f1 = __fmul_rn(__fmul_rn(__int2float_rn(a[2 * t + 1]), ts), rr[2 * t + 1]);
+      __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+      out[t] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    if (acc_out != nullptr) {
+      int4* ap = reinterpret_cast<int4*>(acc_out + row * N + n);
+      ap[0] = make_int4(a[0], a[1], a[2], a[3]);
+      ap[1] = make_int4(a[4], a[5], a[6], a[7]);
+    }
   }
   *reinterpret_cast<uint4*>(y + row * N + n) = make_uint4(out[0], out[1], out[2], out[3]);
 }
@@ -909,42 +971,79 @@ int sm_count() {
 
 }  // namespace
 
-// K slices per tile of the expanded-weight GEMMs (whole 1024-chunks): the
-// count with the least estimated time, (units per CTA) x (chunks per slice) x
-// (one tile-chunk, ~5.9 us measured on GB300) plus writing and reading the
-// S partial planes; 1 when the tiles already fill the GPU evenly.
-int dense_splits(int64_t M, int64_t N, int64_t K) {
+// How the expanded-weight GEMMs cut their work: the first `full` tiles whole,
+// the others (the last, partial wave, or all tiles) in S slices of whole
+// 1024-chunks.  The plan with the least estimated time wins: waves of units
+// x chunks per unit x one tile-chunk (~5.9 us measured on GB300), plus
+// writing and reading the partial pieces and a launch for the finishing
+// kernel; a split has to win clearly.
+DensePlan dense_plan(int64_t M, int64_t N, int64_t K) {
   const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const long sms = sm_count();
   const long chunks = K / KCHUNK;
   const double t_chunk = 5.9e-6, bw = 6.0e12, t_launch = 3e-6;
-  double best = 0.0;
-  int best_s = 1;
-  for (long S = 1; S <= chunks && S <= 32; ++S) {
-    const long per_cta = (tiles * S + sms - 1) / sms;
-    const long slice = (chunks + S - 1) / S;
-    double t = static_cast<double>(per_cta * slice) * t_chunk;
-    if (S > 1) t += (2.0 * S * M * N * 4 + 2.0 * M * N) / bw + t_launch;
-    if (S == 1 || t < 0.97 * best) {   // a split has to win clearly
-      best = t;
-      best_s = static_cast<int>(S);
+  const double piece_bytes = static_cast<double>(BM) * BN * 4;
+  auto cost = [&](long full, long S) {
+    const long split = tiles - full;
+    const long per_cta_whole = (full + sms - 1) / sms;
+    const long per_cta_split = (split * S + sms - 1) / sms;
+    double t = (static_cast<double>(per_cta_whole) * chunks +
+                static_cast<double>(per_cta_split) * ((chunks + S - 1) / S)) * t_chunk;
+    if (S > 1) t += (2.0 * split * S * piece_bytes + 2.0 * split * BM * BN) / bw + t_launch;
+    return t;
+  };
+  DensePlan best{1, static_cast<int>(tiles)};
+  double best_t = cost(tiles, 1);
+  auto consider = [&](long full, long S) {
+    if (S < 2 || S > chunks || full >= tiles) return;
+    const double t = cost(full, S);
+    if (t < 0.97 * best_t) {
+      best_t = t;
+      best = DensePlan{static_cast<int>(S), static_cast<int>(full)};
     }
+  };
+  for (long S = 2; S <= chunks && S <= 32; ++S) consider(0, S);      // every tile split
+  const long full = tiles / sms * sms;                                 // whole waves kept whole
+  if (full > 0 && full < tiles) {
+    const long tail = tiles - full;
+    for (long S = 2; S <= chunks && S <= 32; ++S) consider(full, S);   // the last wave split
+    (void)tail;
   }
-  return best_s;
+  return best;
 }
 
 size_t gemm_dense_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  const int S = dense_splits(M, N, K);
-  return S > 1 ? static_cast<size_t>(S) * M * N * 4 : 0;
+  const DensePlan p = dense_plan(M, N, K);
+  if (p.S == 1) return 0;
+  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  return static_cast<size_t>(tiles - p.full) * p.S * BM * BN * 4;
 }
 
+int dense_splits(int64_t M, int64_t N, int64_t K) { return dense_plan(M, N, K).S; }
+
 namespace {
-// The split to use: dense_splits' choice when the caller gave a large enough
-// workspace, else 1.
-int usable_splits(int64_t M, int64_t N, int64_t K, const void* ws, size_t ws_bytes) {
-  const int S = dense_splits(M, N, K);
-  if (S > 1 && (ws == nullptr || ws_bytes < static_cast<size_t>(S) * M * N * 4)) return 1;
-  return S;
+// The plan to use: dense_plan's when the caller gave a large enough
+// workspace, else everything whole.
+DensePlan usable_plan(int64_t M, int64_t N, int64_t K, const void* ws, size_t ws_bytes) {
+  const DensePlan p = dense_plan(M, N, K);
+  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  if (p.S > 1 && (ws == nullptr || ws_bytes < gemm_dense_workspace_bytes(M, N, K)))
+    return DensePlan{1, static_cast<int>(tiles)};
+  return p;
+}
+
+template <bool FP>
+cudaError_t launch_split_finalize(const void* part, const DensePlan& p, int64_t M, int64_t N,
+                                  const float* tscale, const float* rscale, uint16_t* y,
+                                  int32_t* acc, cudaStream_t st) {
+  const long m_blocks = (M + BM - 1) / BM;
+  const long tiles = m_blocks * ((N + BN - 1) / BN);
+  const long n_split = tiles - p.full;
+  const long threads = n_split * BM * (BN / 8);
+  return launch(split_finalize_kernel<FP>, dim3(static_cast<unsigned>((threads + 255) / 256)),
+                dim3(256), 0, st, part, p.S, p.full, static_cast<int>(n_split),
+                static_cast<int>(m_blocks), static_cast<int>(M), static_cast<int>(N), tscale,
+                rscale, reinterpret_cast<__nv_bfloat16*>(y), acc);
 }
 }  // namespace
 
@@ -962,21 +1061,17 @@ cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t*
     }
     attr_done = true;
   }
-  const int S = usable_splits(M, N, K, ws, ws_bytes);
-  int32_t* part = S > 1 ? static_cast<int32_t*>(ws) : nullptr;
-  const long units = ((M + BM - 1) / BM) * ((N + BN - 1) / BN) * S;
+  const DensePlan p = usable_plan(M, N, K, ws, ws_bytes);
+  int32_t* part = p.S > 1 ? static_cast<int32_t*>(ws) : nullptr;
+  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const long units = p.full + (tiles - p.full) * p.S;
   const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
-  cudaError_t e = launch(S > 1 ? gemm_i8_kernel<true> : gemm_i8_kernel<false>, dim3(grid),
+  cudaError_t e = launch(p.S > 1 ? gemm_i8_kernel<true> : gemm_i8_kernel<false>, dim3(grid),
                          dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, tscale, rscale,
                          static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                         reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
-  if (e != cudaSuccess || S == 1) return e;
-  const long threads = M * N / 8;
-  return launch(packed_finalize_kernel, dim3(static_cast<unsigned>((threads + FIN_THREADS - 1) /
-                                                                   FIN_THREADS)),
-                dim3(FIN_THREADS), 0, st, static_cast<const int32_t*>(part), S, tscale, rscale,
-                static_cast<int>(M), static_cast<int>(N), reinterpret_cast<__nv_bfloat16*>(y),
-                acc);
+                         reinterpret_cast<__nv_bfloat16*>(y), acc, p.S, p.full, part);
+  if (e != cudaSuccess || p.S == 1) return e;
+  return launch_split_finalize<false>(part, p, M, N, tscale, rscale, y, acc, st);
 }
 
 // K slices per tile of the packed GEMM: 1 when the tiles alone fill most of
@@ -1047,19 +1142,17 @@ cudaError_t launch_gemm_f16(const uint16_t* xh, const float* xs, const uint16_t*
     }
     attr_done = true;
   }
-  const int S = usable_splits(M, N, K, ws, ws_bytes);
-  float* part = S > 1 ? static_cast<float*>(ws) : nullptr;
-  const long units = ((M + BM - 1) / BM) * ((N + BN - 1) / BN) * S;
+  const DensePlan p = usable_plan(M, N, K, ws, ws_bytes);
+  float* part = p.S > 1 ? static_cast<float*>(ws) : nullptr;
+  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const long units = p.full + (tiles - p.full) * p.S;
   const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
-  cudaError_t e = launch(S > 1 ? gemm_f16_kernel<true> : gemm_f16_kernel<false>, dim3(grid),
+  cudaError_t e = launch(p.S > 1 ? gemm_f16_kernel<true> : gemm_f16_kernel<false>, dim3(grid),
                          dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, xs, static_cast<int>(M),
                          static_cast<int>(N), static_cast<int>(K),
-                         reinterpret_cast<__nv_bfloat16*>(y), S, part);
-  if (e != cudaSuccess || S == 1) return e;
-  const long threads = M * N / 8;
-  return launch(f16_finalize_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
-                0, st, static_cast<const float*>(part), S, static_cast<int>(M),
-                static_cast<int>(N), reinterpret_cast<__nv_bfloat16*>(y));
+                         reinterpret_cast<__nv_bfloat16*>(y), p.S, p.full, part);
+  if (e != cudaSuccess || p.S == 1) return e;
+  return launch_split_finalize<true>(part, p, M, N, nullptr, nullptr, y, nullptr, st);
 }
 
 cudaError_t gemm_read_clear_error(unsigned int* err) {

@@ -60,6 +60,11 @@ cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* 
 cudaError_t launch_linear_decode(const uint16_t* x, const int8_t* sign, const uint8_t* packed,
                                  int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
                                  cudaStream_t st);
+struct DensePlan {
+  int S;      // slices per split tile (1: nothing split)
+  int full;   // tiles computed whole, before the split ones
+};
+DensePlan dense_plan(int64_t M, int64_t N, int64_t K);
 int dense_splits(int64_t M, int64_t N, int64_t K);
 size_t gemm_dense_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t* w_q,

@@ -100,10 +100,10 @@ def test_zero_and_empty():
     B.tern_gemm_prefill_fp16(xh, xs, w_h, 0, n, k, y)
 
 
-def test_split_k_within_rounding():
-    """Split along K (workspace given), the fp32 slice sums are added in slice
-    order: the same output up to fp32 rounding."""
-    m, n, k = 128, 5120, 17408
+@pytest.mark.parametrize("m,n,k", [(128, 5120, 17408), (2048, 5120, 17408)])
+def test_split_k_within_rounding(m, n, k):
+    """Split along K (workspace given; all tiles, or the last wave's), the fp32
+    slice sums are added in slice order: the same output up to fp32 rounding."""
     assert B.tern_workspace_bytes(B.TERN_OP_GEMM, m, n, k) > 0
     codes = I.make_codes(24, n, k)
     scales = I.make_scales(24, n, k)

@@ -118,11 +118,14 @@ def test_zero_operands():
     assert not acc.any() and not y.any()
 
 
-@pytest.mark.parametrize("m,n,k", [(128, 5120, 17408), (40, 1024, 5120), (512, 5120, 17408)])
+@pytest.mark.parametrize("m,n,k", [(128, 5120, 17408), (40, 1024, 5120), (512, 5120, 17408),
+                                   (2048, 5120, 17408), (512, 10240, 5120)])
 def test_split_k_is_bit_identical(m, n, k):
     """With a workspace, calls whose tiles fill the GPU unevenly split K in
-    slices of whole chunks; the int32 partials are exact, so acc and y equal
-    the unsplit call's bit for bit (and the integer oracle on a sample)."""
+    slices of whole chunks -- every tile, or only the tiles of the last,
+    partial wave (the last two shapes); the int32 partials are exact, so acc
+    and y equal the unsplit call's bit for bit (and the integer oracle on a
+    sample)."""
     assert B.tern_workspace_bytes(B.TERN_OP_GEMM, m, n, k) > 0
     codes = I.make_codes(23, n, k)
     scales = I.make_scales(23, n, k)
