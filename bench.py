@@ -487,7 +487,64 @@ def run_mid_m(args, local, ms=(32, 64, 128, 256)):
     return out
 
 
-def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 16), prefill_ms=(128, 512, 2048)):
+def run_prefill_configs(args, local, configs=((I.GATE_UP, 512), (I.DOWN, 512), (I.DOWN, 2048))):
+    """The other prefill configurations (gate/up and down at M = 512 and
+    2048): rotation + int8 quantisation + the int8 GEMM on the expanded
+    weight (with its K-split workspace), and the GEMM alone, expanded and
+    packed."""
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    _, tc_peak, _ = _peaks()
+    out = []
+    with torch.cuda.stream(stream):
+        st = stream.cuda_stream
+        for layer, m in configs:
+            lay = _make_layers(layer, 1, seed=8, prefill=True)[0]
+            x = _activations(layer, m, seed=88).cuda()
+            xq = torch.empty((m, layer.k), dtype=torch.float16, device="cuda")
+            ts = torch.empty(m, dtype=torch.float32, device="cuda")
+            y = torch.empty((m, layer.n), dtype=torch.bfloat16, device="cuda")
+            nbd = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, layer.n, layer.k)
+            wsd = B.Workspace().get(nbd) if nbd else None
+            nbp = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, layer.n, layer.k)
+            wsp = B.Workspace().get(nbp) if nbp else None
+
+            def gemm():
+                B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y,
+                                         None, wsd, nbd, stream=st)
+
+            def step():
+                B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_I8, xq, ts, st)
+                gemm()
+
+            def packed():
+                B.tern_gemm_prefill_packed(xq, ts, lay.packed, lay.q, lay.rscale, m, layer.n,
+                                           layer.k, y, None, wsp, nbp, stream=st)
+
+            for f in (step, packed):
+                for _ in range(3):
+                    f()
+            torch.cuda.synchronize()
+            n = 20
+            t = _time_region(step, n, stream, 1)
+            tg = _time_region(gemm, n, stream, 1)
+            tp = _time_region(packed, n, stream, 1)
+            B.tern_check(stream)
+            ops = 2.0 * m * layer.n * layer.k
+            out.append({"workload": f"prefill {layer.name}, M={m}",
+                        "TOPS": round(ops * n / t / 1e12, 1),
+                        "ms_per_step": round(t / n * 1e3, 4),
+                        "gemm_us": round(tg / n * 1e6, 2),
+                        "gemm_frac_of_bf16_peak": round(ops * n / tg / 1e12 / tc_peak, 4),
+                        "gemm_launches": B.tern_kernel_launches(B.TERN_OP_GEMM, m, layer.n,
+                                                                layer.k),
+                        "packed_gemm_us": round(tp / n * 1e6, 2)})
+            del lay
+            torch.cuda.empty_cache()
+    return out
+
+
+def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 8, 16), prefill_ms=(128, 512, 2048)):
     """The 64-layer linear stack of a 27B hybrid model: per layer qkv
     5120->10240, o 5120->5120, gate/up 5120->34816, down 17408->5120, each with
     its own seeded weights (seed = 4 * layer + linear).  The linears are not
@@ -701,6 +758,8 @@ def main():
     torch.cuda.empty_cache()
     if not args.no_prefill:
         line["prefill"] = run_prefill(args, local)
+        if rank == 0:
+            line["prefill"]["other_configs"] = run_prefill_configs(args, local)
     if not args.no_prefill and rank == 0:
         line["mid_m"] = run_mid_m(args, local)
     if not args.no_stack and rank == 0:
