@@ -937,16 +937,19 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<EncodeTiledFn>(p);
+      fn.store(f, std::memory_order_release);
+    }
   }
-  return fn;
+  return f;
 }
 
 // 2-D map over a row-major fp16 [rows][K] matrix, boxes of 64 K x box_rows rows.
@@ -1052,15 +1055,16 @@ cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t*
                         int32_t* acc, void* ws, size_t ws_bytes, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!make_map(&ta, xq, M, K, BM) || !make_map(&tb, w_q, N, K, BN)) return cudaErrorInvalidValue;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t ea = once_per_device(attr_done, [] {
     for (auto* kern : {gemm_i8_kernel<false>, gemm_i8_kernel<true>}) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_BYTES));
       if (e != cudaSuccess) return e;
     }
-    attr_done = true;
-  }
+    return cudaSuccess;
+  });
+  if (ea != cudaSuccess) return ea;
   const DensePlan p = usable_plan(M, N, K, ws, ws_bytes);
   int32_t* part = p.S > 1 ? static_cast<int32_t*>(ws) : nullptr;
   const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
@@ -1093,23 +1097,22 @@ size_t gemm_packed_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const uint8_t* packed,
                                const int8_t* q, const float* rscale, int64_t M, int64_t N,
                                int64_t K, uint16_t* y, int32_t* acc, void* ws, cudaStream_t st) {
-  static int regs_ok = 0;   // 0 unknown, 1 built with the launch allocation the split needs
-  if (regs_ok == 0) {
+  // 0 unknown, 1 built with the launch allocation the register split needs, -1 not
+  static std::atomic<int> regs_ok{0};
+  if (regs_ok.load(std::memory_order_acquire) == 0) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, gemm_packed_kernel);
     if (e != cudaSuccess) return e;
-    regs_ok = fa.numRegs == P_LAUNCH_REGS ? 1 : -1;
-    if (regs_ok > 0) {
-      e = cudaFuncSetAttribute(gemm_packed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(PSMEM_BYTES));
-      if (e != cudaSuccess) {
-        regs_ok = 0;
-        return e;
-      }
-    }
+    regs_ok.store(fa.numRegs == P_LAUNCH_REGS ? 1 : -1, std::memory_order_release);
   }
   // never launch a register split that may not fit the block's allocation
-  if (regs_ok < 0) return cudaErrorNotSupported;
+  if (regs_ok.load(std::memory_order_acquire) < 0) return cudaErrorNotSupported;
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t ea = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(gemm_packed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(PSMEM_BYTES));
+  });
+  if (ea != cudaSuccess) return ea;
   CUtensorMap ta;
   if (!make_map(&ta, xq, M, K, BM)) return cudaErrorInvalidValue;
   const int S = packed_splits(M, N, K);
@@ -1133,15 +1136,16 @@ cudaError_t launch_gemm_f16(const uint16_t* xh, const float* xs, const uint16_t*
                             cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!make_map(&ta, xh, M, K, BM) || !make_map(&tb, w_h, N, K, BN)) return cudaErrorInvalidValue;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t ea = once_per_device(attr_done, [] {
     for (auto* kern : {gemm_f16_kernel<false>, gemm_f16_kernel<true>}) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_BYTES));
       if (e != cudaSuccess) return e;
     }
-    attr_done = true;
-  }
+    return cudaSuccess;
+  });
+  if (ea != cudaSuccess) return ea;
   const DensePlan p = usable_plan(M, N, K, ws, ws_bytes);
   float* part = p.S > 1 ? static_cast<float*>(ws) : nullptr;
   const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);

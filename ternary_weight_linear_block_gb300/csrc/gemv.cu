@@ -773,30 +773,31 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<EncodeTiledFn>(p);
+      fn.store(f, std::memory_order_release);
+    }
   }
-  return fn;
+  return f;
 }
 
 template <int NT>
 cudaError_t launch_nt(const CUtensorMap& tm, const uint8_t* packed, const float* xs, int M, int N,
                       int K, __nv_bfloat16* y, unsigned long long* partials,
                       const GemvPlan& p, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t e = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(gemv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(SMEM_BYTES));
+  });
+  if (e != cudaSuccess) return e;
   return launch(gemv_kernel<NT>, dim3(p.C), dim3(NUM_THREADS), SMEM_BYTES, st, tm, packed, xs, M,
                 N, K, y, partials, p.U, p.S);
 }
@@ -862,14 +863,12 @@ template <int NT>
 cudaError_t launch_linear_nt(const uint16_t* x, const int8_t* sign, const uint8_t* packed, int M,
                              int N, int K, __nv_bfloat16* y, unsigned long long* partials,
                              const GemvPlan& p, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(linear_kernel<NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(LSMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t e = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(linear_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(LSMEM_BYTES));
+  });
+  if (e != cudaSuccess) return e;
   return launch(linear_kernel<NT>, dim3(p.C), dim3(NUM_THREADS), LSMEM_BYTES, st, x, sign, packed,
                 M, N, K, y, partials, p.U, p.S);
 }

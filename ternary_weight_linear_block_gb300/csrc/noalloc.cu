@@ -25,28 +25,19 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TERN_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];   // device address of g_noalloc_scratch, per device
-int g_dev_ok[kMaxDevices];           // 0 unknown, 1 sm_103, -1 other
+// Per device: the device address of g_noalloc_scratch.  Concurrent first
+// calls store the same value.
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 cudaError_t scratch_address(int dev, void** out) {
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
-}
-
-bool device_ok(int dev) {
-  if (g_dev_ok[dev] != 0) return g_dev_ok[dev] > 0;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return false;
-  g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
-  return g_dev_ok[dev] > 0;
 }
 
 }  // namespace
@@ -66,7 +57,7 @@ extern "C" tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uin
     return TERN_ERR_ALIGN;
   if (gemv_workspace_bytes(M, N, K) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ERR_WORKSPACE;
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || !device_ok(dev))
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || !device_supported())
     return TERN_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   if (scratch_address(dev, &scratch) != cudaSuccess) return TERN_ERR_CUDA;

@@ -5,25 +5,34 @@
 
 #include "tern_internal.cuh"
 
-using namespace tern;
-
+namespace tern {
 namespace {
-
 constexpr int kMaxDevices = 64;
-int g_dev_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+// Per device: 0 unknown, 1 sm_103, -1 other.  Concurrent first calls store
+// the same value.
+std::atomic<int> g_dev_ok[kMaxDevices];
+}  // namespace
 
 bool device_supported() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
-  if (dev < kMaxDevices && g_dev_ok[dev] != 0) return g_dev_ok[dev] > 0;
+  if (dev < kMaxDevices) {
+    const int known = g_dev_ok[dev].load(std::memory_order_acquire);
+    if (known != 0) return known > 0;
+  }
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return false;
   const bool ok = (major == 10 && minor == 3);
-  if (dev < kMaxDevices) g_dev_ok[dev] = ok ? 1 : -1;
+  if (dev < kMaxDevices) g_dev_ok[dev].store(ok ? 1 : -1, std::memory_order_release);
   return ok;
 }
+}  // namespace tern
+
+using namespace tern;
+
+namespace {
 
 tern_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA; }
 

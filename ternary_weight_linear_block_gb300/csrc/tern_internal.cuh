@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/tern.h"
 
 namespace tern {
@@ -14,6 +16,27 @@ constexpr int kMaxK = 65536;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t pad16(int64_t n) { return (n + 15) / 16 * 16; }
+
+// Whether the calling thread's current device is an sm_103 GPU (cached per
+// device).
+bool device_supported();
+
+// Per-device set-up (a kernel's shared-memory limit is an attribute of the
+// kernel on the current device): runs set_up() until it first succeeds on
+// the calling thread's current device, one bit of `done` per device (0-63).
+// Concurrent first calls may both run it, so set_up must be idempotent.
+template <class F>
+cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& set_up) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const unsigned long long bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = set_up();
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Programmatic dependent launch: every kernel waits for its predecessor
 // grid before touching data a previous kernel may have written, and lets its
