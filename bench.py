@@ -370,7 +370,7 @@ def run_prefill(args, local, m=2048):
         st = stream.cuda_stream
 
         nbd = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, layer.n, layer.k)
-        wsd = B.Workspace().get(nbd) if nbd else None
+        wsd = B.Workspace().scratch(nbd) if nbd else None
 
         def step():
             B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_I8, xq, ts, st)
@@ -382,7 +382,7 @@ def run_prefill(args, local, m=2048):
                                      wsd, nbd, stream=st)
 
         nbp = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, layer.n, layer.k)
-        wsp = B.Workspace().get(nbp) if nbp else None
+        wsp = B.Workspace().scratch(nbp) if nbp else None
 
         def packed_only():
             B.tern_gemm_prefill_packed(xq, ts, lay.packed, lay.q, lay.rscale, m, layer.n,
@@ -454,9 +454,9 @@ def run_mid_m(args, local, ms=(32, 64, 128, 256)):
                 ts = torch.full((m,), 1e-3, device="cuda")
                 y = torch.empty((m, shp.n), dtype=torch.bfloat16, device="cuda")
                 nb = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, shp.n, shp.k)
-                wsb = B.Workspace().get(nb) if nb else None
+                wsb = B.Workspace().scratch(nb) if nb else None
                 nbe = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, shp.n, shp.k)
-                wse = B.Workspace().get(nbe) if nbe else None
+                wse = B.Workspace().scratch(nbe) if nbe else None
                 i = [0]
 
                 def packed():
@@ -505,9 +505,9 @@ def run_prefill_configs(args, local, configs=((I.GATE_UP, 512), (I.DOWN, 512), (
             ts = torch.empty(m, dtype=torch.float32, device="cuda")
             y = torch.empty((m, layer.n), dtype=torch.bfloat16, device="cuda")
             nbd = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, layer.n, layer.k)
-            wsd = B.Workspace().get(nbd) if nbd else None
+            wsd = B.Workspace().scratch(nbd) if nbd else None
             nbp = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, layer.n, layer.k)
-            wsp = B.Workspace().get(nbp) if nbp else None
+            wsp = B.Workspace().scratch(nbp) if nbp else None
 
             def gemm():
                 B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y,
@@ -622,9 +622,9 @@ def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 8, 16), prefill_ms=(128
 
             nbs = [B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, shp.n, shp.k)
                    for shp in shapes]
-            wsp = B.Workspace().get(max(nbs)) if max(nbs) else None
+            wsp = B.Workspace().scratch(max(nbs)) if max(nbs) else None
             nbe = [B.tern_workspace_bytes(B.TERN_OP_GEMM, m, shp.n, shp.k) for shp in shapes]
-            wse = B.Workspace().get(max(nbe)) if max(nbe) else None
+            wse = B.Workspace().scratch(max(nbe)) if max(nbe) else None
 
             def prefill_step(packed=False):
                 for row in layers:

@@ -217,9 +217,10 @@ tern_status tern_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, 
  * Requirements: 1 <= M <= 16 (M == 0 is a no-op), K % 1024 == 0, K <= 65536.
  * A call is the GEMV kernel and, when some 512-row block is shared by more
  * than four CTAs (M <= 8) or by several CTAs (M > 8), a fixup kernel that
- * adds those blocks' partial sums in slot order.  Device-side waits are bounded; a wait that gives up makes the
- * call's outputs undefined and is reported by tern_check(); the workspace
- * must then be zero-filled again (tern_workspace_init) before its next use.
+ * adds those blocks' partial sums in slot order.  Device-side waits are
+ * bounded; a wait that gives up makes the call's outputs undefined and is
+ * reported by tern_check(); the workspace must then be zero-filled again
+ * (tern_workspace_init) before its next use.
  * ---------------------------------------------------------------------- */
 tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const float* xs,
                              int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
@@ -293,7 +294,9 @@ tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uint16_t* xh, 
  *           tile's K range in slices of whole 1024-chunks: the slices' exact
  *           int32 partial sums go to planes of ws and a second kernel adds
  *           them and rescales (same results bit for bit).  With NULL (or
- *           less) the call runs unsplit.
+ *           less) the call runs unsplit.  A split call leaves partial sums
+ *           in ws: a buffer also used as a tern_gemv_decode workspace must
+ *           be zero-filled again (tern_workspace_init) before that call.
  * Requirements: K % 1024 == 0, K <= 65536, M >= 0, N % 16 == 0, N >= 0.
  * Device-side waits are bounded; a wait that gives up makes the call's
  * outputs undefined and is reported by tern_check().
@@ -326,7 +329,8 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
  *           tile's K range is split in S slices of whole 1024-chunks whose
  *           exact int32 partial sums go to S planes [M][N] of ws; a second
  *           kernel adds the planes (integer sums: the same result in any
- *           order) and applies the rescale (tern_kernel_launches).
+ *           order) and applies the rescale (tern_kernel_launches).  As for
+ *           tern_gemm_prefill_int8, a split call leaves partial sums in ws.
  * Requirements: K % 1024 == 0, K <= 65536, N % 16 == 0, 0 <= M, N <= 2^24.
  * Device-side waits are bounded; a wait that gives up makes the call's
  * outputs undefined and is reported by tern_check().
@@ -383,8 +387,8 @@ int tern_host_accessible(const void* host);
  * tern_gemv_decode_noalloc launch the same count); for TERN_OP_GEMM the
  * int8 (or fp16) GEMM, plus its finishing kernel when it is given the
  * workspace and splits K; for TERN_OP_GEMM_PACKED the GEMM, plus the
- * rescale kernel when its tiles are split along K.  Host-only; launch counting for
- * CUDA-graph sizing and profiling. */
+ * rescale kernel when its tiles are split along K.  Host-only; launch
+ * counting for CUDA-graph sizing and profiling. */
 int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K);
 /* Zero-fill `bytes` of device memory at ws on `stream` (asynchronous). */
 tern_status tern_workspace_init(void* ws, size_t bytes, void* stream);

@@ -279,17 +279,38 @@ def fwht(x: torch.Tensor, mode: int, sign: torch.Tensor | None = None, stream=No
 
 
 class Workspace:
-    """A zero-initialised device workspace, grown on demand."""
+    """A device workspace for the library's calls, grown on demand; use it
+    from one stream.  The decode GEMV needs the bytes it uses zero-filled and
+    leaves them so, while the split GEMMs leave partial sums behind: ``get``
+    returns the buffer ready for the GEMV (zero-filling it on the stream
+    first if a GEMM used it since), ``scratch`` returns it for a GEMM."""
 
     def __init__(self, device="cuda"):
         self.device = device
         self.buf = None
+        self.clean = 0        # leading bytes known to be zero
 
-    def get(self, nbytes: int, stream=None) -> torch.Tensor:
+    def _ensure(self, nbytes: int) -> int:
         nbytes = max(int(nbytes), 256)
         if self.buf is None or self.buf.numel() < nbytes:
             self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
-            tern_workspace_init(self.buf, nbytes, stream)
+            self.clean = 0
+        return nbytes
+
+    def get(self, nbytes: int, stream=None) -> torch.Tensor:
+        """The buffer with at least ``nbytes`` zero bytes, for tern_gemv_decode
+        or tern_linear_decode."""
+        nbytes = self._ensure(nbytes)
+        if self.clean < nbytes:
+            tern_workspace_init(self.buf, self.buf.numel(), stream)
+            self.clean = self.buf.numel()
+        return self.buf
+
+    def scratch(self, nbytes: int, stream=None) -> torch.Tensor:
+        """The buffer of at least ``nbytes`` bytes, any contents, for a GEMM
+        (which leaves partial sums in it)."""
+        self._ensure(nbytes)
+        self.clean = 0
         return self.buf
 
 
@@ -440,7 +461,7 @@ def prefill_fp16(w_h: torch.Tensor, x: torch.Tensor, y: torch.Tensor | None = No
     if y is None:
         y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
     nb = tern_workspace_bytes(TERN_OP_GEMM, m, n, k)
-    buf = (ws or Workspace(x.device)).get(nb, stream) if nb > 0 else None
+    buf = (ws or Workspace(x.device)).scratch(nb, stream) if nb > 0 else None
     tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y, buf, nb, stream)
     return y
 
@@ -460,13 +481,13 @@ def prefill(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,
         y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=x.device)
     if from_packed:
         nb = tern_workspace_bytes(TERN_OP_GEMM_PACKED, m, layer.n, layer.k)
-        buf = (ws or Workspace(x.device)).get(nb, stream) if nb > 0 else None
+        buf = (ws or Workspace(x.device)).scratch(nb, stream) if nb > 0 else None
         tern_gemm_prefill_packed(xq, ts, layer.packed, layer.q, layer.rscale, m, layer.n,
                                  layer.k, y, acc, buf, 0 if buf is None else buf.numel(),
                                  stream=stream)
     else:
         nb = tern_workspace_bytes(TERN_OP_GEMM, m, layer.n, layer.k)
-        buf = (ws or Workspace(x.device)).get(nb, stream) if nb > 0 else None
+        buf = (ws or Workspace(x.device)).scratch(nb, stream) if nb > 0 else None
         tern_gemm_prefill_int8(xq, ts, layer.w_q, layer.rscale, m, layer.n, layer.k, y, acc,
                                buf, nb, stream=stream)
     return y

@@ -167,11 +167,11 @@ class GpuOps:
         lay = lin.layer
         if lay.w_q is not None:
             nb = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, lin.n, kp)
-            buf = ws.get(nb) if nb else None
+            buf = ws.scratch(nb) if nb else None
             B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, lin.n, kp, y, None, buf, nb)
         else:
             nb = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, lin.n, kp)
-            buf = ws.get(nb) if nb else None
+            buf = ws.scratch(nb) if nb else None
             B.tern_gemm_prefill_packed(xq, ts, lay.packed, lay.q, lay.rscale, m, lin.n, kp, y,
                                        None, buf, nb)
         return y

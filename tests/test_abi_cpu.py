@@ -200,3 +200,30 @@ def test_host_accessible_query(lib):
     assert B.lib().tern_host_accessible(None) == 0
     if not torch.cuda.is_available():
         assert B.lib().tern_host_accessible(FAKE) == 0        # no device: never
+
+
+def test_workspace_zero_fills_for_the_gemv_after_a_gemm(monkeypatch):
+    """Workspace bookkeeping (host logic; the zero-fill call is faked on a
+    CPU tensor): ``get`` zero-fills a new or GEMM-used buffer once, and not
+    again while only GEMV calls use it."""
+    fills = []
+
+    def fake_init(ws, nbytes=None, stream=None):
+        ws[:nbytes].zero_()
+        fills.append(nbytes)
+        return B.TERN_OK
+
+    monkeypatch.setattr(B, "tern_workspace_init", fake_init)
+    ws = B.Workspace(device="cpu")
+    a = ws.get(1000)
+    assert a.numel() == 1000 and not a.any() and fills == [1000]
+    ws.get(600)
+    assert fills == [1000]                      # still clean
+    s = ws.scratch(800)
+    assert s.data_ptr() == a.data_ptr()
+    s.fill_(0x5A)                               # what a split GEMM may leave
+    b = ws.get(600)
+    assert not b.any() and fills == [1000, 1000]
+    ws.scratch(4000).fill_(7)                   # grows: a new buffer, contents undefined
+    c = ws.get(100)
+    assert c.numel() == 4000 and not c.any() and fills[-1] == 4000

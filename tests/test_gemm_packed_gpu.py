@@ -146,7 +146,7 @@ def test_split_k_with_and_without_acc(m, n, k):
     acc, y = _run(lay, bits, m)
     y2 = poison(torch.empty((m, n), dtype=torch.bfloat16, device="cuda"))
     ws = B.Workspace()
-    ws.get(B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, n, k)).fill_(0x5A)   # any contents
+    ws.scratch(B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, n, k)).fill_(0x5A)   # any contents
     B.prefill(lay, to_dev_bf16(bits), y=y2, from_packed=True, ws=ws)
     B.tern_check()
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))

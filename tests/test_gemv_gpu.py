@@ -91,3 +91,26 @@ def test_special_weights():
     want = -float(scales[5, 1300 // 128]) * xr[:, 1300]
     assert np.allclose(y[:, 5], want, rtol=2 ** -8, atol=0)
     assert not np.delete(y, 5, axis=1).any()
+
+
+def test_workspace_after_a_gemm_is_cleaned():
+    """A Workspace a split GEMM used holds partial sums; words whose high half
+    is 1 would pass for the GEMV's ready tags.  Poison it that way through
+    ``scratch`` (as a GEMM may leave it): the next decode through ``get``
+    zero-fills it first, so the in-kernel reduction (one launch, row blocks
+    shared by up to four CTAs at M = 1) matches a fresh workspace bit for
+    bit."""
+    n, k, m = 34816, 1024, 1
+    assert B.tern_kernel_launches(B.TERN_OP_GEMV, m, n, k) == 1
+    codes = I.make_codes(41, n, k)
+    scales = I.make_scales(41, n, k)
+    bits, x = I.make_activations(41, m, k, 0.001, 50.0)
+    layer = _layer(codes, scales)
+    want = _decode(layer, bits, m)
+    ws = B.Workspace()
+    buf = ws.scratch(B.tern_workspace_bytes(B.TERN_OP_GEMM, 512, 5120, 17408))
+    buf.view(torch.int64).fill_((1 << 32) | 0x3F800000)   # tag 1, value 1.0f
+    got = _decode(layer, bits, m, ws)
+    assert np.array_equal(got, want)
+    rows = np.sort(np.random.default_rng(2).choice(n, 256, replace=False))
+    assert O.rel_frobenius(got[:, rows], O.linear_f64(x, codes[rows], scales[rows])) <= TOL
