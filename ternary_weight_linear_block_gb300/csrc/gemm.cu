@@ -475,14 +475,27 @@ __global__ void __launch_bounds__(256)
 // reads (the sign trick gives 2 code as fp16, times q/2: both exact).  MMA,
 // per-1024 chunk int32 conversion and epilogue are those of the kernel above.
 // Warp roles: 0 producer, 1 MMA issuer, 2 TMEM allocator, 3 idle, 4-11
-// epilogue, 12-15 expansion.  The 512 threads launch with 128 registers each;
+// epilogue, 12-15 expansion.
+//
+// Two tile orientations (template WM).  WM = false: tokens on the MMA's M
+// side (128 per tile) and weight rows on its N side (256), for M <= 128
+// (one token block).  WM = true, for larger M: 128 weight rows on the M side
+// and 256 tokens on the N side, so each expanded weight value feeds 256
+// tokens instead of 128 -- half the expansion work and half the shared-
+// memory writes per MMA -- while the MMA shape, the stage size (A 16 KB, B
+// 32 KB) and the TMEM buffers stay the same; the accumulator's lanes are
+// then weight rows and its columns tokens.  The 512 threads launch with 128 registers each;
 // the epilogue's 128 int32 sums per thread need more, so the warpgroups
 // re-split the block's registers with setmaxnreg (control 48, epilogue 168,
 // expansion 120 per thread); the launcher refuses to launch unless the kernel
 // was built with exactly 128 registers per thread, so the split always fits.
-constexpr int PBN = 256;                 // weight rows per tile
+constexpr int PBN = 256;                 // weight rows per tile (WM = false)
 constexpr int PUNIT_BYTES = 17408;       // one 512-row x 128-k unit of the packed format
-constexpr int PCODE_BYTES = 8192;        // codes of 256 rows (16 tiles of 16) of one unit
+constexpr int PCODE_BYTES = 8192;        // code ring slot: the codes of up to 256 rows of a unit
+// tokens and weight rows per tile, and the bytes of a tile's codes per group
+template <bool WM> constexpr int p_tok() { return WM ? 256 : BM; }
+template <bool WM> constexpr int p_wrows() { return WM ? 128 : PBN; }
+template <bool WM> constexpr int p_code_bytes() { return p_wrows<WM>() * 32; }
 constexpr int PSTAGES = 4;
 constexpr int PCSTAGES = 4;
 constexpr int PA_BYTES = BM * BK * 2;    // tokens
@@ -508,6 +521,7 @@ __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
 }
 
+template <bool WM>
 __global__ void __launch_bounds__(P_THREADS, 1)
     gemm_packed_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t* __restrict__ packed,
                        const int8_t* __restrict__ q, const float* __restrict__ tscale,
@@ -531,9 +545,14 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  constexpr int TOK = p_tok<WM>(), WROWS = p_wrows<WM>(), CODE_BYTES = p_code_bytes<WM>();
+  // stage layout: MMA operand A (16 KB) at offset 0, B (32 KB) after it; the
+  // tokens are A for WM = false and B for WM = true
+  constexpr uint32_t TOK_OFF = WM ? PA_BYTES : 0, W_OFF = WM ? 0 : PA_BYTES;
+  constexpr uint32_t TOK_BYTES = TOK * BK * 2;
   const int G = K / kGroup;
-  const int m_blocks = (M + BM - 1) / BM;
-  const int tiles = m_blocks * ((N + PBN - 1) / PBN);
+  const int m_blocks = (M + TOK - 1) / TOK;   // token blocks (fastest in the tile order)
+  const int tiles = m_blocks * ((N + WROWS - 1) / WROWS);
   const int units = tiles * S;   // unit = (tile, K slice of whole 128-groups)
   // the tile and the group range [g0, g1) of a unit; the MMA accumulates it
   // in pieces that end at every 1024-chunk boundary (and at g1), so each
@@ -592,17 +611,18 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         int tile, g0, g1;
         unit_of(u, tile, g0, g1);
         const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
-        const uint8_t* wsrc =
-            packed + static_cast<size_t>(n_blk >> 1) * G * PUNIT_BYTES + (n_blk & 1) * PCODE_BYTES;
+        constexpr int PER_UNIT = 512 / WROWS;   // weight blocks per 512-row unit
+        const uint8_t* wsrc = packed + static_cast<size_t>(n_blk / PER_UNIT) * G * PUNIT_BYTES +
+                              (n_blk % PER_UNIT) * CODE_BYTES;
         for (int g = g0; g < g1 && ok; ++g) {
           if (!ptx::mbar_wait(&cempty[c], cph ^ 1u, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&cfull[c], PCODE_BYTES);
+          ptx::mbar_arrive_expect_tx(&cfull[c], CODE_BYTES);
           ptx::bulk_load(scode + c * PCODE_BYTES, wsrc + static_cast<size_t>(g) * PUNIT_BYTES,
-                         PCODE_BYTES, &cfull[c]);
+                         CODE_BYTES, &cfull[c]);
           ++c_issued;
           if (++c == PCSTAGES) {
             c = 0;
@@ -614,9 +634,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
               ok = false;
               break;
             }
-            ptx::mbar_arrive_expect_tx(&afull[s], PA_BYTES);
-            ptx::tma_load_2d(smem + s * PSTAGE_BYTES, &tmA, &afull[s], g * kGroup + h * BK,
-                             m_blk * BM);
+            ptx::mbar_arrive_expect_tx(&afull[s], TOK_BYTES);
+            ptx::tma_load_2d(smem + s * PSTAGE_BYTES + TOK_OFF, &tmA, &afull[s],
+                             g * kGroup + h * BK, m_blk * TOK);
             ++a_issued;
             if (++s == PSTAGES) {
               s = 0;
@@ -729,6 +749,33 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         if (lane == 0) ptx::mbar_arrive(&dempty[buf]);
       }
       if (!ok) break;
+      if constexpr (WM) {
+        // lanes are weight rows, columns tokens: per token, the warp's 32
+        // lanes write 32 consecutive outputs of y (or of the slice's plane)
+        const int n = n_blk * WROWS + 32 * qd + lane;
+        const int t0 = m_blk * TOK + wg * 128;
+        if (n < N) {
+          if (S > 1) {
+            int32_t* pcol = part + static_cast<long>(u % S) * M * N + n;
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+              if (t0 + j < M) pcol[static_cast<long>(t0 + j) * N] = sums[j];
+          } else {
+            const float rs = rscale[n];
+#pragma unroll
+            for (int j = 0; j < 128; ++j) {
+              const int t = t0 + j;
+              if (t < M) {
+                const float f =
+                    __fmul_rn(__fmul_rn(__int2float_rn(sums[j]), __ldg(tscale + t)), rs);
+                y[static_cast<long>(t) * N + n] = __float2bfloat16_rn(f);
+                if (acc_out != nullptr) acc_out[static_cast<long>(t) * N + n] = sums[j];
+              }
+            }
+          }
+        }
+        continue;
+      }
       const int row = m_blk * BM + 32 * qd + lane;
       if (S > 1) {
         // one K slice of the tile: store its exact partial sums in the
@@ -785,10 +832,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     // format
     const int xw = warp - 12;
     const int r = lane >> 2, cq = lane & 3;
+    constexpr int UPW = WROWS / 64;   // tiles of 16 rows per expansion warp
     // byte offset of (u = 0, row parity 0, chunk 0) inside a weight stage:
     // row 16 xw + r, 4 c bytes into the 16-byte chunk; u adds 64 rows, the
     // row parity 8 rows
-    const uint32_t row_off = static_cast<uint32_t>(PA_BYTES + (16 * xw + r) * 128 + 4 * cq);
+    const uint32_t row_off = static_cast<uint32_t>(W_OFF + (16 * xw + r) * 128 + 4 * cq);
     uint32_t xo[8];
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) xo[ch] = static_cast<uint32_t>((ch ^ r) << 4);
@@ -800,21 +848,21 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int tile, g0, g1;
       unit_of(unit, tile, g0, g1);
       const int n_blk = tile / m_blocks;
-      // q of the thread's eight rows (slots u, row parities par); rows past N read row 0
-      const int8_t* qp[4][2];
-      bool qv_ok[4][2];
+      // q of the thread's 2 UPW rows (slots u, row parities par); rows past N read row 0
+      const int8_t* qp[UPW][2];
+      bool qv_ok[UPW][2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < UPW; ++u)
 #pragma unroll
         for (int par = 0; par < 2; ++par) {
-          const int n = n_blk * PBN + 16 * (xw + 4 * u) + r + 8 * par;
+          const int n = n_blk * WROWS + 16 * (xw + 4 * u) + r + 8 * par;
           qv_ok[u][par] = n < N;
           qp[u][par] = q + static_cast<long>(n < N ? n : 0) * G;
         }
       for (int g = g0; g < g1 && ok; ++g) {
-        int qv[4][2];
+        int qv[UPW][2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < UPW; ++u)
 #pragma unroll
           for (int par = 0; par < 2; ++par)
             qv[u][par] = qv_ok[u][par] ? static_cast<int>(__ldg(qp[u][par] + g)) : 0;
@@ -823,9 +871,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           ok = false;
           break;
         }
-        uint4 wv[4];
+        uint4 wv[UPW];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < UPW; ++u)
           wv[u] = *reinterpret_cast<const uint4*>(scode + c * PCODE_BYTES + 512 * (xw + 4 * u) +
                                                   16 * lane);
         __syncwarp();
@@ -834,9 +882,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           c = 0;
           cph ^= 1u;
         }
-        __half2 qh[4][2];
+        __half2 qh[UPW][2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < UPW; ++u)
 #pragma unroll
           for (int par = 0; par < 2; ++par)
             qh[u][par] = __half2half2(__float2half_rn(0.5f * static_cast<float>(qv[u][par])));
@@ -855,7 +903,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
               const int chunk = 4 * ii + 2 * (e >> 2) + ((e >> 1) & 1);
               const int par = e & 1;
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
+              for (int u = 0; u < UPW; ++u) {
                 const uint32_t w =
                     h == 0 ? (ii == 0 ? wv[u].x : wv[u].y) : (ii == 0 ? wv[u].z : wv[u].w);
                 const uint32_t two_code = (w << (14 - 2 * e)) & 0xC000C000u;
@@ -1078,10 +1126,21 @@ cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t*
   return launch_split_finalize<false>(part, p, M, N, tscale, rscale, y, acc, st);
 }
 
+namespace {
+// Tile orientation of the packed GEMM: weight rows on the MMA's M side
+// (256-token tiles) above one 128-token block.
+bool packed_wm(int64_t M) { return M > BM; }
+
+long packed_tiles(int64_t M, int64_t N) {
+  return packed_wm(M) ? ((M + 255) / 256) * ((N + 127) / 128)
+                      : ((M + BM - 1) / BM) * ((N + PBN - 1) / PBN);
+}
+}  // namespace
+
 // K slices per tile of the packed GEMM: 1 when the tiles alone fill most of
 // the GPU, else as many slices (of whole 128-groups) as keep one unit per SM.
 int packed_splits(int64_t M, int64_t N, int64_t K) {
-  const long tiles = ((M + BM - 1) / BM) * ((N + PBN - 1) / PBN);
+  const long tiles = packed_tiles(M, N);
   const long sms = sm_count();
   if (4 * tiles >= 3 * sms) return 1;
   const long want = sms / tiles;
@@ -1097,31 +1156,42 @@ size_t gemm_packed_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const uint8_t* packed,
                                const int8_t* q, const float* rscale, int64_t M, int64_t N,
                                int64_t K, uint16_t* y, int32_t* acc, void* ws, cudaStream_t st) {
-  // 0 unknown, 1 built with the launch allocation the register split needs, -1 not
+  // 0 unknown, 1 both orientations built with the launch allocation the
+  // register split needs, -1 not
   static std::atomic<int> regs_ok{0};
   if (regs_ok.load(std::memory_order_acquire) == 0) {
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, gemm_packed_kernel);
-    if (e != cudaSuccess) return e;
-    regs_ok.store(fa.numRegs == P_LAUNCH_REGS ? 1 : -1, std::memory_order_release);
+    int ok = 1;
+    for (auto* kern : {gemm_packed_kernel<false>, gemm_packed_kernel<true>}) {
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != P_LAUNCH_REGS) ok = -1;
+    }
+    regs_ok.store(ok, std::memory_order_release);
   }
   // never launch a register split that may not fit the block's allocation
   if (regs_ok.load(std::memory_order_acquire) < 0) return cudaErrorNotSupported;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t ea = once_per_device(attr_done, [] {
-    return cudaFuncSetAttribute(gemm_packed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(PSMEM_BYTES));
+    for (auto* kern : {gemm_packed_kernel<false>, gemm_packed_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(PSMEM_BYTES));
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
   });
   if (ea != cudaSuccess) return ea;
+  const bool wm = packed_wm(M);
   CUtensorMap ta;
-  if (!make_map(&ta, xq, M, K, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, xq, M, K, wm ? 256 : BM)) return cudaErrorInvalidValue;
   const int S = packed_splits(M, N, K);
   int32_t* part = S > 1 ? static_cast<int32_t*>(ws) : nullptr;
-  const long units = ((M + BM - 1) / BM) * ((N + PBN - 1) / PBN) * S;
+  const long units = packed_tiles(M, N) * S;
   const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
-  cudaError_t e = launch(gemm_packed_kernel, dim3(grid), dim3(P_THREADS), PSMEM_BYTES, st, ta,
-                         packed, q, tscale, rscale, static_cast<int>(M), static_cast<int>(N),
-                         static_cast<int>(K), reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
+  cudaError_t e = launch(wm ? gemm_packed_kernel<true> : gemm_packed_kernel<false>, dim3(grid),
+                         dim3(P_THREADS), PSMEM_BYTES, st, ta, packed, q, tscale, rscale,
+                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                         reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
   if (e != cudaSuccess || S == 1) return e;
   const long threads = M * N / 8;
   return launch(packed_finalize_kernel, dim3(static_cast<unsigned>((threads + FIN_THREADS - 1) /
