@@ -435,11 +435,12 @@ def run_prefill(args, local, m=2048):
                              "avg_launch_us": round(th / n * 1e6, 2)}}
 
 
-def run_mid_m(args, local, ms=(32, 64, 128, 256)):
-    """Mid-size M (17..256 tokens) through each linear shape: the packed GEMM
-    (2-bit weights, split along K when its tiles do not fill the GPU) against
-    the GEMM on the expanded weight; GEMM alone, weights rotating over copies
-    larger than L2, bit-identical outputs."""
+def run_mid_m(args, local, ms=(32, 64, 128, 256, 512)):
+    """Mid-size M (17..512 tokens) through each linear shape: the packed GEMM
+    (2-bit weights; 128-token tiles up to M = 128, weight rows on the MMA's M
+    side with 256-token tiles above; split along K when its tiles do not fill
+    the GPU) against the GEMM on the expanded weight; GEMM alone, weights
+    rotating over copies larger than L2, bit-identical outputs."""
     torch.cuda.set_device(local)
     stream = torch.cuda.Stream()
     out = []

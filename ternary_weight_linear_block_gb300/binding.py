@@ -497,7 +497,7 @@ def forward(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,
             ws: Workspace | None = None, sign=None, stream=None) -> torch.Tensor:
     """The layer for any number of tokens, on the path measured fastest on
     GB300 for that M: the decode GEMV for M <= 16; the int8 GEMM straight from
-    the packed weights for 16 < M <= 128 (or whenever the layer holds no
+    the packed weights for 16 < M <= 256 (or whenever the layer holds no
     expanded weight); the int8 GEMM on the expanded weight w_q above that.
     The decode path keeps fp16 activations; the int8 paths quantise them per
     token (the page's section 4), so results differ by the int8 tolerance
@@ -508,6 +508,6 @@ def forward(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,
         return decode(layer, x, ws, y=y, sign=sign, stream=stream)
     if layer.q is None:
         raise ValueError("prefill needs the layer packed with prefill=True (q, rscale)")
-    from_packed = layer.packed is not None and (layer.w_q is None or m <= 128)
+    from_packed = layer.packed is not None and (layer.w_q is None or m <= 256)
     return prefill(layer, x, y=y, sign=sign, stream=stream, from_packed=from_packed, ws=ws)
 

@@ -193,10 +193,10 @@ def test_zero_and_empty():
                                m, 0, k, y, acc)
 
 
-@pytest.mark.parametrize("m", [4, 16, 17, 128, 129, 300])
+@pytest.mark.parametrize("m", [4, 16, 17, 128, 129, 256, 257, 300])
 def test_forward_picks_the_path(m):
     """binding.forward: the decode GEMV up to 16 tokens, the packed GEMM up to
-    128, the expanded GEMM above -- each call equal to its path's own call."""
+    256, the expanded GEMM above -- each call equal to its path's own call."""
     n, k = 512, 2048
     codes = I.make_codes(33, n, k)
     scales = I.make_scales(33, n, k)
@@ -208,7 +208,7 @@ def test_forward_picks_the_path(m):
     if m <= 16:
         want = B.decode(lay, xd, ws)
     else:
-        want = B.prefill(lay, xd, from_packed=m <= 128, ws=ws)
+        want = B.prefill(lay, xd, from_packed=m <= 256, ws=ws)
     B.tern_check()
     assert torch.equal(got.view(torch.int16), want.view(torch.int16))
     tol = 4e-3 if m <= 16 else 2e-2
