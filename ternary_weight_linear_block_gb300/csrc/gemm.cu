@@ -254,7 +254,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       for (int i = 0; i < 128; ++i) sums[i] = 0;
       for (int c = c0; c < c1; ++c, ++cc) {
         const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
-        if (!ptx::mbar_wait(&dfull[buf], dph, abort_flag, WAIT_LIMIT)) {
+        if (!ptx::mbar_wait_warp(&dfull[buf], dph, abort_flag, WAIT_LIMIT)) {
           if (!*abort_flag) fail(abort_flag, ERR_EPILOGUE);
           ok = false;
           break;
@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       for (int i = 0; i < 128; ++i) sums[i] = 0;
       for (int gp = g0; gp < g1; gp = piece_end(gp, g1), ++cc) {
         const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
-        if (!ptx::mbar_wait(&dfull[buf], dph, abort_flag, WAIT_LIMIT)) {
+        if (!ptx::mbar_wait_warp(&dfull[buf], dph, abort_flag, WAIT_LIMIT)) {
           if (!*abort_flag) fail(abort_flag, ERR_EPILOGUE);
           ok = false;
           break;

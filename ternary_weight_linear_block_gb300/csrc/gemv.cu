@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (; i < i_end; ++i) {
         const int s = i % STAGES;
         const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
-        if (!ptx::mbar_wait(&full[s], ph, abort_flag, WAIT_LIMIT)) {
+        if (!ptx::mbar_wait_warp(&full[s], ph, abort_flag, WAIT_LIMIT)) {
           if (!*abort_flag) fail(abort_flag, ERR_CONSUMER);
           alive = false;
           break;
@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (; i < stop; ++i) {
         const int s = i % LSTAGES;
         const uint32_t ph = static_cast<uint32_t>(i / LSTAGES) & 1u;
-        if (!ptx::mbar_wait(&full[s], ph, abort_flag, WAIT_LIMIT)) {
+        if (!ptx::mbar_wait_warp(&full[s], ph, abort_flag, WAIT_LIMIT)) {
           if (!*abort_flag) fail(abort_flag, ERR_CONSUMER);
           alive = false;
           break;

@@ -67,6 +67,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return false;
 }
 
+// mbar_wait by every lane of a warp, with one answer for the whole warp (a
+// lane that gave up makes every lane give up), so warp-collective
+// instructions after the wait (tcgen05.ld, ldmatrix, mma.sync, shuffles) run
+// on all 32 lanes or on none.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint32_t limit) {
+  const bool ok = mbar_wait(bar, parity, abort, limit);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Poll until the phase with `parity` completes or `limit` polls have failed
 // (used while unwinding, when the abort flag is already set).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
