@@ -398,6 +398,17 @@ tern_status tern_workspace_init(void* ws, size_t bytes, void* stream);
  * last check, TERN_ERR_CUDA on a sticky CUDA error, else TERN_OK. */
 tern_status tern_check(void* stream);
 
+/* Self-test of the failure path of the bounded device-side waits: launches
+ * one warp on `stream` that waits, with the kernels' own wait helper, on a
+ * barrier nothing ever completes, gives up after `polls` polls
+ * (1 <= polls <= TERN_SELFTEST_MAX_POLLS) and records it in the error word,
+ * so that the next tern_check() returns TERN_ERR_TIMEOUT (and clears it).
+ * Nothing else is touched, no memory is faulted and the context stays
+ * usable.  TERN_ERR_INVALID_ARG for polls out of range, TERN_ERR_UNSUPPORTED
+ * without an sm_103 device. */
+#define TERN_SELFTEST_MAX_POLLS (1u << 20)
+tern_status tern_selftest_wait(uint32_t polls, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,6 +24,9 @@ LIB_PATH = os.path.join(_PKG, "libtern.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "tern.h")
 
 TERN_OK = 0
+TERN_ERR_INVALID_ARG = 1
+TERN_ERR_UNSUPPORTED = 4
+TERN_ERR_TIMEOUT = 7
 TERN_FWHT_F32 = 0
 TERN_FWHT_DECODE = 1
 TERN_FWHT_I8 = 2
@@ -59,6 +62,7 @@ _SIGS = {
     "tern_gemm_prefill_packed": (ctypes.c_int, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _p,
                                                 _p, _sz, _p]),
     "tern_check": (ctypes.c_int, [_p]),
+    "tern_selftest_wait": (ctypes.c_int, [ctypes.c_uint32, _p]),
     "tern_gemv_decode_noalloc": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
     "tern_linear_decode": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
 }
@@ -203,6 +207,12 @@ def tern_quant_rotated(xr, m, k, mode, out, out_scale, stream=None):
 
 def tern_check(stream=None):
     return _call("tern_check", _stream(stream))
+
+
+def tern_selftest_wait(polls: int, stream=None):
+    """Launch the bounded-wait self-test (a wait that gives up after ``polls``
+    polls); the next tern_check raises TERN_ERR_TIMEOUT."""
+    return _call("tern_selftest_wait", polls, _stream(stream))
 
 
 def tern_linear_decode(x, sign, packed, m, n, k, y, ws, ws_bytes, stream=None):

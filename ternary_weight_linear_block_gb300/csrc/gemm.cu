@@ -47,12 +47,17 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 384;
 constexpr int TMEM_COLS = 512;
-constexpr uint32_t WAIT_LIMIT = 1u << 26;
+// Polls of a bounded barrier wait before it gives up: a poll that finds the
+// phase incomplete suspends for about 3.8 us on GB300 (measured with
+// tern_selftest_wait), so 2^18 polls give up after about one second; a
+// wait of the working kernel lasts microseconds.
+constexpr uint32_t WAIT_LIMIT = 1u << 18;
 constexpr uint32_t IDESC = ptx::idesc_f16_f32(BM, BN);
 constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
 
 enum : unsigned int {
-  ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_EPILOGUE = 4u, ERR_DRAIN = 8u, ERR_EXPAND = 16u
+  ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_EPILOGUE = 4u, ERR_DRAIN = 8u, ERR_EXPAND = 16u,
+  ERR_SELFTEST = 32u
 };
 
 __device__ __forceinline__ void fail(volatile int* abort_flag, unsigned int code) {
@@ -1227,6 +1232,31 @@ cudaError_t launch_gemm_f16(const uint16_t* xh, const float* xs, const uint16_t*
                          reinterpret_cast<__nv_bfloat16*>(y), p.S, p.full, part);
   if (e != cudaSuccess || p.S == 1) return e;
   return launch_split_finalize<true>(part, p, M, N, nullptr, nullptr, y, nullptr, st);
+}
+
+namespace {
+// Self-test of the bounded waits: one warp waits, with the kernels' own wait
+// helper, on an mbarrier that nothing arrives on (parity 0 of a freshly
+// initialised barrier), gives up after `polls` polls and records it in the
+// error word tern_check() reads -- what a kernel whose copy never lands
+// does.  It holds no tensor memory and has no copies in flight.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t polls) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::mbar_fence_init();
+  }
+  __syncwarp();
+  if (!ptx::mbar_wait_warp(&bar, 0, &abort_flag, polls) && threadIdx.x == 0)
+    atomicOr(&g_gemm_error, ERR_SELFTEST);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t polls, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(polls);
+  return cudaGetLastError();
 }
 
 cudaError_t gemm_read_clear_error(unsigned int* err) {

@@ -66,7 +66,14 @@ constexpr int STAGES = 8;
 constexpr int CONSUMERS = 16;                   // consumer warps
 constexpr int TPW = TILES / CONSUMERS;          // tiles per consumer warp (2)
 constexpr int NUM_THREADS = 32 * (1 + CONSUMERS);
-constexpr uint32_t WAIT_LIMIT = 1u << 26;
+// Polls of a bounded barrier wait before it gives up: a poll that finds the
+// phase incomplete suspends for about 3.8 us on GB300 (measured with
+// tern_selftest_wait), so 2^18 polls give up after about one second; a
+// wait of the working kernel lasts microseconds.
+constexpr uint32_t WAIT_LIMIT = 1u << 18;
+// Tries of the tagged-word wait (a load round trip and a 200 ns sleep each:
+// about 0.1 s in all).
+constexpr uint32_t TAG_TRIES = 1u << 16;
 constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
 
 static_assert(XTILE_BYTES + UNIT_BYTES <= STAGE_BYTES, "stage too small");
@@ -206,7 +213,7 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
 #pragma unroll
         for (int v = 0; v < NV; ++v) ready = ready && (w[sb][v] >> 32) == 1ull;
       if (__all_sync(0xffffffffu, ready)) break;
-      if (tries >= (WAIT_LIMIT >> 10) || *abort_flag) {
+      if (tries >= TAG_TRIES || *abort_flag) {
         if (lane == 0) fail(abort_flag, ERR_REDUCE);
         ok = false;
         break;

@@ -306,6 +306,12 @@ tern_status tern_gemm_prefill_fp16(const uint16_t* xh, const float* xs, const ui
                                    static_cast<cudaStream_t>(stream)));
 }
 
+tern_status tern_selftest_wait(uint32_t polls, void* stream) {
+  if (polls == 0 || polls > TERN_SELFTEST_MAX_POLLS) return TERN_ERR_INVALID_ARG;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_wait_selftest(polls, static_cast<cudaStream_t>(stream)));
+}
+
 tern_status tern_check(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return TERN_ERR_CUDA;

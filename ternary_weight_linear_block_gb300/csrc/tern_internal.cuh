@@ -106,5 +106,6 @@ cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const ui
 // Read and clear the device error word of the GEMV / GEMM translation unit.
 cudaError_t gemv_read_clear_error(unsigned int* err);
 cudaError_t gemm_read_clear_error(unsigned int* err);
+cudaError_t launch_wait_selftest(uint32_t polls, cudaStream_t st);
 
 }  // namespace tern

@@ -126,6 +126,13 @@ def test_gemm_argument_errors(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_is_unsupported(lib):
     assert _st("tern_fwht_quant", FAKE, 4, 1024, None, 0, FAKE, None, None) == 4
+    assert _st("tern_selftest_wait", 64, None) == B.TERN_ERR_UNSUPPORTED
+
+
+def test_selftest_wait_argument_errors(lib):
+    """The poll count is checked before anything else (no GPU needed)."""
+    assert _st("tern_selftest_wait", 0, None) == B.TERN_ERR_INVALID_ARG
+    assert _st("tern_selftest_wait", (1 << 20) + 1, None) == B.TERN_ERR_INVALID_ARG
 
 
 def test_binding_raises_named_error(lib):
