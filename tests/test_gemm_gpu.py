@@ -91,9 +91,13 @@ def test_extreme_magnitudes_exact(k):
 
 
 @pytest.mark.parametrize("layer,m", [(I.GATE_UP, 512), (I.DOWN, 512), (I.GATE_UP, 2048),
-                                     (I.DOWN, 2048)])
+                                     (I.DOWN, 2048), (I.QKV, 512), (I.QKV, 2048), (I.O_PROJ, 512),
+                                     (I.O_PROJ, 2048)])
 def test_full_size_sampled(layer, m):
-    """Full prefill shapes; the oracle computes a seeded sample of rows."""
+    """Full prefill shapes of the 64-layer stack, with the workspace the bench
+    gives, so the K-split plans run where the cost model picks them (on 152
+    SMs: qkv and down at M = 512, down, qkv and o at M = 2048); the oracle
+    computes a seeded sample of rows."""
     d = I.make_layer(layer, m, seed=0)
     acc, y = _prefill(d.codes, d.scales, d.x_bits, m)
     rows = np.sort(np.random.default_rng(2).choice(layer.n, 256, replace=False))

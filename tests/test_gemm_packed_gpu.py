@@ -116,7 +116,8 @@ def test_equals_expanded_gemm(m):
     assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
 
 
-@pytest.mark.parametrize("layer,m", [(I.GATE_UP, 2048), (I.DOWN, 512), (I.QKV, 64)])
+@pytest.mark.parametrize("layer,m", [(I.GATE_UP, 2048), (I.DOWN, 512), (I.QKV, 64), (I.GATE_UP, 512),
+                                     (I.DOWN, 2048), (I.QKV, 2048), (I.O_PROJ, 512), (I.O_PROJ, 128)])
 def test_full_size_sampled(layer, m):
     """Full shapes, launched as the bench times them; the oracle computes a
     seeded sample of rows and tokens."""
