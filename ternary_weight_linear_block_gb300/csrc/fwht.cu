@@ -54,63 +54,55 @@ __global__ void __launch_bounds__(128) fwht_block_kernel(const uint16_t* __restr
   }
 }
 
-// Mode I8: one CTA (8 warps) per token; the rotated token is kept in shared
-// memory until its absmax is known.
-__global__ void __launch_bounds__(256) fwht_i8_kernel(const uint16_t* __restrict__ x, int M, int K,
-                                                      const int8_t* __restrict__ sign,
-                                                      __half* __restrict__ xq,
-                                                      float* __restrict__ tscale) {
-  extern __shared__ float4 smem_f4[];
-  float* xs = reinterpret_cast<float*>(smem_f4);
-  __shared__ float red[8];
+// Mode I8 (K <= 32768): one CTA per token with one warp per 1024-block.
+// Each warp keeps its rotated block in registers while the CTA reduces the
+// token's absmax, then quantises and writes its own block: no shared-memory
+// copy of the token, and every warp loads at once.  Launch bounds: up to 18
+// blocks (K <= 18432) two CTAs per SM (registers capped at 56), else one.
+template <int MAX_THREADS, int MIN_CTAS>
+__global__ void __launch_bounds__(MAX_THREADS, MIN_CTAS)
+    fwht_i8_reg_kernel(const uint16_t* __restrict__ x, int M, int K,
+                       const int8_t* __restrict__ sign, __half* __restrict__ xq,
+                       float* __restrict__ tscale) {
+  __shared__ float red[32];
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
+  const int b = threadIdx.x >> 5;   // the warp's block
+  const int nb = blockDim.x >> 5;   // = K / 1024
   const int m = blockIdx.x;
-  const int B = K / kHBlock;
   pdl_launch_dependents();
   pdl_wait();
-  const uint16_t* xm = x + static_cast<long>(m) * K;
+  float v[4][8];
+  load_block(x + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock,
+             sign ? sign + static_cast<long>(b) * kHBlock : nullptr, lane, v);
+  fwht_1024(v, lane);
   float amax = 0.f;
-  for (int b = warp; b < B; b += 8) {
-    float v[4][8];
-    load_block(xm + static_cast<long>(b) * kHBlock, sign ? sign + static_cast<long>(b) * kHBlock : nullptr,
-               lane, v);
-    fwht_1024(v, lane);
 #pragma unroll
-    for (int ih = 0; ih < 4; ++ih) {
-      float4* p = reinterpret_cast<float4*>(xs + b * kHBlock + ih * 256 + lane * 8);
-      p[0] = make_float4(v[ih][0], v[ih][1], v[ih][2], v[ih][3]);
-      p[1] = make_float4(v[ih][4], v[ih][5], v[ih][6], v[ih][7]);
+  for (int ih = 0; ih < 4; ++ih)
 #pragma unroll
-      for (int il = 0; il < 8; ++il) amax = fmaxf(amax, fabsf(v[ih][il]));
-    }
-  }
+    for (int il = 0; il < 8; ++il) amax = fmaxf(amax, fabsf(v[ih][il]));
   amax = warp_max(amax);
-  if (lane == 0) red[warp] = amax;
+  if (lane == 0) red[b] = amax;
   __syncthreads();
   float a = red[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w]);
+  for (int w = 1; w < nb; ++w) a = fmaxf(a, red[w]);
   const float ts = __fdiv_rn(a, 127.0f);
   const bool nz = ts > 0.f;
   if (threadIdx.x == 0) tscale[m] = nz ? ts : 0.f;
-  __half* om = xq + static_cast<long>(m) * K;
-  for (int i = threadIdx.x * 8; i < K; i += 256 * 8) {
-    const float4 p0 = reinterpret_cast<const float4*>(xs + i)[0];
-    const float4 p1 = reinterpret_cast<const float4*>(xs + i)[1];
-    float vv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  __half* ob = xq + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock;
+#pragma unroll
+  for (int ih = 0; ih < 4; ++ih) {
     uint32_t w[4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       float q0 = 0.f, q1 = 0.f;
       if (nz) {
-        q0 = fminf(fmaxf(rintf(__fdiv_rn(vv[2 * t], ts)), -127.f), 127.f);
-        q1 = fminf(fmaxf(rintf(__fdiv_rn(vv[2 * t + 1], ts)), -127.f), 127.f);
+        q0 = fminf(fmaxf(rintf(__fdiv_rn(v[ih][2 * t], ts)), -127.f), 127.f);
+        q1 = fminf(fmaxf(rintf(__fdiv_rn(v[ih][2 * t + 1], ts)), -127.f), 127.f);
       }
       __half2 h2 = __floats2half2_rn(q0, q1);   // integers in [-127,127]: exact
       w[t] = *reinterpret_cast<uint32_t*>(&h2);
     }
-    *reinterpret_cast<uint4*>(om + i) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(ob + ih * 256 + lane * 8) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -230,7 +222,7 @@ __global__ void __launch_bounds__(128) quant_decode_kernel(const float* __restri
 }
 
 // Per-token int8 quantisation of already rotated fp32 activations (the
-// arithmetic of fwht_i8_kernel); one CTA per token, two passes over the row.
+// arithmetic of fwht_i8_reg_kernel); one CTA per token, two passes over the row.
 __global__ void __launch_bounds__(256) quant_i8_kernel(const float* __restrict__ xr, int M, int K,
                                                        __half* __restrict__ xq,
                                                        float* __restrict__ tscale) {
@@ -309,11 +301,12 @@ cudaError_t launch_fwht(const uint16_t* x, int64_t M, int64_t K, const int8_t* s
                         void* out, float* out_scale, cudaStream_t st) {
   const int m = static_cast<int>(M), k = static_cast<int>(K);
   if (mode == TERN_FWHT_I8) {
-    const size_t smem = static_cast<size_t>(K) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(fwht_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    return launch(fwht_i8_kernel, dim3(m), dim3(256), smem, st, x, m, k, sign,
+    // the entry point admits K <= 32768 in this mode: at most 32 warps
+    const unsigned threads = static_cast<unsigned>(32 * (K / kHBlock));
+    if (K <= 18 * kHBlock)
+      return launch(fwht_i8_reg_kernel<576, 2>, dim3(m), dim3(threads), 0, st, x, m, k, sign,
+                    static_cast<__half*>(out), out_scale);
+    return launch(fwht_i8_reg_kernel<1024, 1>, dim3(m), dim3(threads), 0, st, x, m, k, sign,
                   static_cast<__half*>(out), out_scale);
   }
   const long warps = M * (K / kHBlock);

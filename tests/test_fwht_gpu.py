@@ -55,8 +55,12 @@ def test_fwht_decode_operand_bitwise(m, k, frac, mult):
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), inv.view(np.uint32))
 
 
-@pytest.mark.parametrize("m,k,frac,mult", CASES + [(64, 17408, 0.001, 50.0), (37, 5120, 0.001, 50.0)])
+@pytest.mark.parametrize("m,k,frac,mult", CASES + [(64, 17408, 0.001, 50.0), (37, 5120, 0.001, 50.0),
+                                           (5, 19456, 0.001, 50.0), (3, 32768, 0.001, 50.0)])
 def test_fwht_i8_bitwise(m, k, frac, mult):
+    """One CTA per token, one warp per block: up to 18 blocks two CTAs per
+    SM, up to the mode's limit of 32 blocks one; both give the oracle's xq
+    and tscale."""
     bits, x = I.make_activations(3, m, k, frac, mult)
     out, sc = _run(to_dev_bf16(bits), m, k, B.TERN_FWHT_I8)
     xq, ts = O.quant_tokens(O.fwht_f32(x))
