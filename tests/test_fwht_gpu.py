@@ -91,27 +91,31 @@ def test_sign_vector_all_modes():
 
 def test_degenerate_inputs():
     k = 2048
-    x = np.zeros((4, k), np.float32)
+    x = np.zeros((6, k), np.float32)
     x[1] = 3.0e30                      # huge, same sign everywhere
     x[2, 7] = -1.0e-30                 # one tiny value
     x[3, ::2] = 1.0
     x[3, 1::2] = -1.0
+    x[4, 3] = 1.0e-37                  # rotated values +-3e-39: a subnormal tscale
+    x[5, 0], x[5, 1] = 3.0, 1.0        # rotated 4/32 and 2/32: v / tscale next to 63.5
     from ternary_weight_linear_block_gb300.inputs import to_bf16_bits, bf16_bits_to_f32
     bits = to_bf16_bits(x)
     xf = bf16_bits_to_f32(bits)
     xd = to_dev_bf16(bits)
-    out, _ = _run(xd, 4, k, B.TERN_FWHT_F32)
+    out, _ = _run(xd, 6, k, B.TERN_FWHT_F32)
     ref = O.fwht_f32(xf)
     assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
-    out, sc = _run(xd, 4, k, B.TERN_FWHT_DECODE)
+    out, sc = _run(xd, 6, k, B.TERN_FWHT_DECODE)
     vals, inv = O.decode_operand(ref)
     assert np.array_equal(f16_bits(out), vals.view(np.uint16))
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), inv.view(np.uint32))
-    out, sc = _run(xd, 4, k, B.TERN_FWHT_I8)
+    out, sc = _run(xd, 6, k, B.TERN_FWHT_I8)
     xq, ts = O.quant_tokens(ref)
     assert np.array_equal(out.cpu().float().numpy(), xq.astype(np.float32))
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), ts.view(np.uint32))
     assert ts[0] == 0 and not xq[0].any()
+    assert 0 < ts[4] < np.finfo(np.float32).tiny      # the subnormal case is exercised
+    assert set(np.unique(np.abs(xq[5]))) <= {0, 63, 64, 127}
 
 
 def test_m_zero_is_a_noop():
