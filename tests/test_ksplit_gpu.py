@@ -68,9 +68,11 @@ def test_half_transforms_match_oracle():
     assert not locs[0][1][0].any() and not locs[1][1][1].any()   # absent halves stay zero
 
 
-@pytest.mark.parametrize("expand", [True, False])
-def test_prefill_int8(expand):
-    k, world, n, m = 17408, 2, 512, 40
+@pytest.mark.parametrize("expand,m", [(True, 40), (False, 40), (True, 200), (False, 200)])
+def test_prefill_int8(expand, m):
+    """Each rank's prefill on its padded shard; without the expanded weight at
+    M = 200 the packed GEMM runs 256-token tiles, split along K."""
+    k, world, n = 17408, 2, 512
     codes, scales, x, rot, y, _, _ = _emulate(k, n, m, world, "prefill", expand=expand)
     assert O.rel_frobenius(y, O.linear_f64(x, codes, scales)) <= 2e-2
 
