@@ -1,4 +1,5 @@
-"""K-split (row-parallel) tensor parallelism of the ternary linear layer.
+"""Tensor parallelism of the ternary linear layer: K split (row-parallel,
+below) and N split (column-parallel, at the end of the file).
 
 Page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2", section 1
 ("TP=2 への移植: アダマールブロックの真ん中で割れる"): a row-parallel layer's input
@@ -223,3 +224,87 @@ def forward(lin: KSplitLinear, x: torch.Tensor, group=None, mode: str = "decode"
     y = finish_phase(lin, xr, h_all, mode, ops, ws)
     dist.all_reduce(y, group=group)
     return y
+
+
+# ---------------------------------------------------------------------------
+# Column-parallel (N-split): each rank holds a contiguous block of output
+# rows.  Every rank rotates the whole input and computes its own rows with
+# the layer's usual calls, so the data path has no collective; one optional
+# all-gather joins the rows.
+
+@dataclass(frozen=True)
+class NSplitPlan:
+    """Rank `rank` of `world` holds output rows [n0, n1) of an N-row layer;
+    every rank's block starts at a multiple of `per` rows."""
+
+    N: int
+    world: int
+    rank: int
+    per: int
+    n0: int
+    n1: int
+
+    @property
+    def nr(self) -> int:
+        return self.n1 - self.n0
+
+
+def nsplit_plan(N: int, world: int, rank: int, align: int = 16) -> NSplitPlan:
+    """Blocks of ceil(N / world) rows rounded up to `align` (the GEMMs take
+    N % 16 == 0); the last ranks take what is left, possibly nothing."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad world size or rank")
+    if N % align:
+        raise ValueError(f"N={N} is not a multiple of {align}")
+    per = -(-N // world)
+    per = -(-per // align) * align
+    n0 = min(rank * per, N)
+    return NSplitPlan(N, world, rank, per, n0, min(n0 + per, N))
+
+
+class NSplitLinear:
+    """One rank's rows of a column-parallel ternary linear layer: codes int8
+    [nr, K] and scales fp16 [nr, K/128] of rows [n0, n1), packed like any
+    layer (binding.pack_layer); with pack=False they are kept as given (for
+    a reference implementation of the compute)."""
+
+    def __init__(self, plan: NSplitPlan, codes: torch.Tensor, scales: torch.Tensor,
+                 decode: bool = True, prefill: bool = True, expand: bool = True,
+                 pack: bool = True):
+        if codes.shape[0] != plan.nr or scales.shape[0] != plan.nr:
+            raise ValueError("shard rows do not match the plan")
+        self.plan = plan
+        self.layer = None
+        self.codes = self.scales = None
+        if pack and plan.nr:
+            self.layer = B.pack_layer(codes.contiguous(), scales.contiguous(), decode=decode,
+                                      prefill=prefill, expand=expand)
+        elif not pack:
+            self.codes, self.scales = codes, scales
+
+
+def nsplit_local(lin: NSplitLinear, x: torch.Tensor, sign=None, ws=None) -> torch.Tensor:
+    """This rank's columns of y, [M, nr]: the layer's own forward (rotation of
+    the whole input included) on the rank's rows."""
+    if lin.plan.nr == 0:
+        return torch.empty((x.shape[0], 0), dtype=torch.bfloat16, device=x.device)
+    return B.forward(lin.layer, x, ws=ws, sign=sign)
+
+
+def nsplit_forward(lin: NSplitLinear, x: torch.Tensor, group=None, gather: bool = True,
+                   sign=None, ws=None, local=None) -> torch.Tensor:
+    """The column-parallel forward on one rank of a torch.distributed process
+    group: the rank's columns of y, and with `gather` all of y [M, N] in rank
+    order (one all-gather of the blocks, padded to `per` columns so that
+    every rank sends the same size).  `local` replaces nsplit_local (for a
+    reference implementation of the compute)."""
+    import torch.distributed as dist
+    y = (local or nsplit_local)(lin, x, sign=sign, ws=ws)
+    if not gather:
+        return y
+    plan = lin.plan
+    ypad = torch.zeros((x.shape[0], plan.per), dtype=y.dtype, device=y.device)
+    ypad[:, :plan.nr] = y
+    parts = [torch.empty_like(ypad) for _ in range(plan.world)]
+    dist.all_gather(parts, ypad, group=group)
+    return torch.cat(parts, dim=1)[:, :plan.N]
