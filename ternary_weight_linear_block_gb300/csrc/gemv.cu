@@ -65,7 +65,17 @@ constexpr int STAGE_BYTES = 24576;
 constexpr int STAGES = 8;
 constexpr int CONSUMERS = 16;                   // consumer warps
 constexpr int TPW = TILES / CONSUMERS;          // tiles per consumer warp (2)
-constexpr int NUM_THREADS = 32 * (1 + CONSUMERS);
+constexpr int NUM_THREADS = 32 * (1 + CONSUMERS);   // a producer warp + the consumers
+// The GEMV's block: at M <= 8 (one n8 token tile) a producer warp and the 16
+// consumer warps; at M > 8 the producer thread is lane 0 of consumer warp 0,
+// so that 512 threads leave the larger accumulators their registers (ptxas
+// holds a 544-thread block to 96 registers per thread, a 512-thread one to
+// 128).  Measured on gate/up: a merged producer costs M = 4 2.5 us per launch,
+// a 96-register M = 16 kernel spills.
+template <int NT> constexpr bool gemv_merged() { return NT == 2; }
+template <int NT> constexpr int gemv_threads() {
+  return gemv_merged<NT>() ? 32 * CONSUMERS : NUM_THREADS;
+}
 // Polls of a bounded barrier wait before it gives up: a poll that finds the
 // phase incomplete suspends for about 3.8 us on GB300 (measured with
 // tern_selftest_wait), so 2^18 polls give up after about one second; a
@@ -336,7 +346,7 @@ __device__ __forceinline__ void fold_block(float (&acc)[TPW][NT][4], float (&bac
 }
 
 template <int NT>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(gemv_threads<NT>(), 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t* __restrict__ packed,
                 const float* __restrict__ xs, int M, int N, int K, __nv_bfloat16* __restrict__ y,
                 unsigned long long* __restrict__ partials, int U, int S) {
@@ -367,12 +377,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   __syncthreads();
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ producer
-      const uint64_t pol = ptx::l2_policy_evict_first();
+  // Lane 0 of warp 0 produces: it issues the first STAGES units (the weights
+  // before the programmatic launch wait, which they do not depend on, the
+  // activation tiles after it), then refills each stage once every consumer
+  // warp has released it -- in its own loop when warp 0 is a producer warp,
+  // or (MERGED) at the top of consumer iteration i, with unit i + STAGES - 1
+  // into the stage unit i - 1 used.
+  constexpr bool MERGED = gemv_merged<NT>();
+  const bool producer = warp == 0 && lane == 0;
+  const uint64_t pol = ptx::l2_policy_evict_first();
+  const int pre = n_units < STAGES ? n_units : STAGES;
+  int issued = 0;          // units whose copies lane 0 of warp 0 issued
+  bool prod_ok = true;
+  if constexpr (MERGED) {
+    if (producer) {
       ptx::prefetch_tmap(&tmX);
-      const int pre = n_units < STAGES ? n_units : STAGES;
+      for (int i = 0; i < pre; ++i) {
+        ptx::mbar_arrive_expect_tx(&full[i], UNIT_BYTES + XTILE_BYTES);
+        ptx::bulk_load_hint(smem + i * STAGE_BYTES + XTILE_BYTES,
+                            packed + static_cast<size_t>(u0 + i) * UNIT_BYTES, UNIT_BYTES,
+                            &full[i], pol);
+      }
+    }
+    pdl_wait();   // activations and xs come from the previous kernel
+    if (producer) {
+      for (int i = 0; i < pre; ++i) {
+        const int gi = (u0 + i) % G;
+        uint8_t* st = smem + i * STAGE_BYTES;
+        ptx::tma_load_2d(st, &tmX, &full[i], gi * kGroup, 0);
+        ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[i], gi * kGroup + 64, 0);
+      }
+      issued = pre;
+    }
+  }
+  // unit j into its stage, after the stage's previous unit was released
+  auto produce = [&](int j) {
+    const int s = j % STAGES;
+    const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1u;
+    if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, WAIT_LIMIT)) {
+      if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
+      prod_ok = false;
+      return;
+    }
+    uint8_t* st = smem + s * STAGE_BYTES;
+    const int gj = (u0 + j) % G;
+    ptx::mbar_arrive_expect_tx(&full[s], UNIT_BYTES + XTILE_BYTES);
+    ptx::bulk_load_hint(st + XTILE_BYTES, packed + static_cast<size_t>(u0 + j) * UNIT_BYTES,
+                        UNIT_BYTES, &full[s], pol);
+    ptx::tma_load_2d(st, &tmX, &full[s], gj * kGroup, 0);
+    ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[s], gj * kGroup + 64, 0);
+    ++issued;
+  };
+
+  if (!MERGED && warp == 0) {
+    // ------------------------------------------------ producer warp
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmX);
       for (int i = 0; i < pre; ++i) {
         ptx::mbar_arrive_expect_tx(&full[i], UNIT_BYTES + XTILE_BYTES);
         ptx::bulk_load_hint(smem + i * STAGE_BYTES + XTILE_BYTES,
@@ -381,7 +441,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       pdl_wait();   // the activations are written by the previous kernel
       int g = u0 % G;
-      int issued = pre;
+      issued = pre;
       bool ok = true;
       for (int i = 0; i < n_units; ++i) {
         const int s = i % STAGES;
@@ -414,9 +474,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------ consumers
-    const int cw = warp - 1;          // owns tiles TPW*cw .. TPW*cw + TPW-1 of each unit
+    const int cw = MERGED ? warp : warp - 1;   // owns tiles TPW*cw .. TPW*cw + TPW-1 of each unit
     const int gq = lane >> 2, cq = lane & 3;
-    pdl_wait();   // xs is written by the previous kernel; y / ws may still be read by it
+    if constexpr (!MERGED) pdl_wait();   // xs is written by the previous kernel; y / ws may still be read by it
 
     // Per-lane shared-memory offsets, fixed for the whole kernel.  ldmatrix
     // matrix mi = lane / 8 covers (k16 step j0 + mi / 2, 8-wide k half mi % 2),
@@ -452,6 +512,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int seg_len = (n_units - i < G - g) ? n_units - i : G - g;
       const int i_end = i + seg_len;
       for (; i < i_end; ++i) {
+        if (MERGED && warp == 0) {
+          if (lane == 0 && prod_ok && i >= 1 && i + STAGES - 1 < n_units) produce(i + STAGES - 1);
+          __syncwarp();
+        }
         const int s = i % STAGES;
         const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
         if (!ptx::mbar_wait_warp(&full[s], ph, abort_flag, WAIT_LIMIT)) {
@@ -509,6 +573,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ++rb;
     }
     __syncwarp();
+  }
+  if (MERGED && producer && (!prod_ok || *abort_flag)) {
+    // let every copy still in flight land before the CTA exits
+    for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i) {
+      const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
+      if (!ptx::mbar_wait_bounded(&full[i % STAGES], ph, WAIT_LIMIT))
+        atomicOr(&g_gemv_error, ERR_DRAIN);
+    }
   }
   __syncthreads();
 }
@@ -805,7 +877,7 @@ cudaError_t launch_nt(const CUtensorMap& tm, const uint8_t* packed, const float*
                                 static_cast<int>(SMEM_BYTES));
   });
   if (e != cudaSuccess) return e;
-  return launch(gemv_kernel<NT>, dim3(p.C), dim3(NUM_THREADS), SMEM_BYTES, st, tm, packed, xs, M,
+  return launch(gemv_kernel<NT>, dim3(p.C), dim3(gemv_threads<NT>()), SMEM_BYTES, st, tm, packed, xs, M,
                 N, K, y, partials, p.U, p.S);
 }
 
