@@ -40,6 +40,9 @@
 // * the weight copies do not depend on the previous kernel, so the producer
 //   issues the first ring of them before the programmatic launch wait, and
 //   every CTA lets the next kernel launch as soon as it starts.
+// * the producer is a warp of its own at M <= 8; at M > 8 it is lane 0 of
+//   consumer warp 0, so that the 512-thread block leaves the two token
+//   tiles' accumulators enough registers (see gemv_merged).
 // All barrier and tag waits are bounded; a wait that gives up sets an error
 // word that tern_check() reports (the workspace must then be re-initialised).
 #include <cuda.h>
