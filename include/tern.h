@@ -315,8 +315,11 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
  *     acc[m,n]    = sum_k xq[m,k] * W_int8[n,k]  (exact int32)
  *     y[m,n]      = bf16_rn(((float)acc[m,n] * tscale[m]) * rscale[n])
  * Results are bit-identical to tern_gemm_prefill_int8 on the same layer.
- * The weights are read at 2 bits each (plus q) once per 128 tokens, so
- * mid-size M costs the packed bytes instead of the 2-byte expanded weight.
+ * Tiles: 128 tokens x 256 weight rows up to M = 128; above, 256 tokens x
+ * 128 weight rows (the weights on the MMA's M side, so each expanded weight
+ * serves 256 tokens).  The weights are read at 2 bits each (plus q) once
+ * per token block, so mid-size M costs the packed bytes instead of the
+ * 2-byte expanded weight.
  *
  *   xq      fp16 [M][K] (TERN_FWHT_I8 output), tscale fp32 [M]
  *   packed  tern_pack's `packed` output (tern_packed_bytes(N, K) bytes)
@@ -325,12 +328,12 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
  *   acc     int32 [M][N] or NULL
  *   ws      device workspace of tern_workspace_bytes(TERN_OP_GEMM_PACKED,
  *           M, N, K) bytes (any contents; NULL when that is 0).  When the
- *           128-token x 256-row tiles are too few to fill the GPU, each
- *           tile's K range is split in S slices of whole 1024-chunks whose
- *           exact int32 partial sums go to S planes [M][N] of ws; a second
- *           kernel adds the planes (integer sums: the same result in any
- *           order) and applies the rescale (tern_kernel_launches).  As for
- *           tern_gemm_prefill_int8, a split call leaves partial sums in ws.
+ *           tiles are too few to fill the GPU, each tile's K range is split
+ *           in S slices of whole 128-groups whose exact int32 partial sums
+ *           go to S planes [M][N] of ws; a second kernel adds the planes
+ *           (integer sums: the same result in any order) and applies the
+ *           rescale (tern_kernel_launches).  As for tern_gemm_prefill_int8,
+ *           a split call leaves partial sums in ws.
  * Requirements: K % 1024 == 0, K <= 65536, N % 16 == 0, 0 <= M, N <= 2^24.
  * Device-side waits are bounded; a wait that gives up makes the call's
  * outputs undefined and is reported by tern_check().
