@@ -290,11 +290,12 @@ tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uint16_t* xh, 
  *   acc     int32 [M][N] or NULL
  *   ws      optional device workspace (any contents) of
  *           tern_workspace_bytes(TERN_OP_GEMM, M, N, K) bytes.  With it, a
- *           call whose 128 x 256 tiles fill the GPU unevenly splits each
- *           tile's K range in slices of whole 1024-chunks: the slices' exact
- *           int32 partial sums go to planes of ws and a second kernel adds
- *           them and rescales (same results bit for bit).  With NULL (or
- *           less) the call runs unsplit.  A split call leaves partial sums
+ *           call whose 128 x 256 tiles fill the GPU unevenly splits K in
+ *           slices of whole 1024-chunks -- in every tile, or only in the
+ *           tiles of the last, partial wave, as a cost model picks: the
+ *           slices' exact int32 partial sums go to [128][256] pieces in ws
+ *           and a second kernel adds them and rescales (same results bit
+ *           for bit).  With NULL (or less) the call runs unsplit.  A split call leaves partial sums
  *           in ws: a buffer also used as a tern_gemv_decode workspace must
  *           be zero-filled again (tern_workspace_init) before that call.
  * Requirements: K % 1024 == 0, K <= 65536, M >= 0, N % 16 == 0, N >= 0.

@@ -72,10 +72,11 @@ __device__ __forceinline__ void fail(volatile int* abort_flag, unsigned int code
 // each 1024-chunk of K is one rotation block, so the epilogue multiplies the
 // chunk's fp32 sum by the token's block factor (`tscale` holds xs [M][K/1024])
 // and adds the chunks in fp32; `rscale` and `acc_out` are unused.
-// With S > 1 every tile's K range is cut in S slices of whole 1024-chunks
-// (units of work = (tile, slice)); a slice stores its partial sums (int32 or
-// fp32) in its plane of `part` [S][M][N] and a second kernel adds the planes
-// in slice order and finishes the output.
+// SPLIT: the tiles after the first `full_arg` (all tiles, or those of the
+// last, partial wave) have their K range cut in S slices of whole
+// 1024-chunks (units of work = (tile, slice)); a slice stores its partial
+// sums (int32 or fp32) in its own [128][256] piece of `part`, and a second
+// kernel adds each tile's pieces in slice order and finishes the output.
 template <bool FP, bool SPLIT>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const float* __restrict__ tscale,
