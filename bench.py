@@ -660,8 +660,9 @@ def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 8, 16), prefill_ms=(128
     return out
 
 
-def run_cpu_baseline(args, budget_s=15.0):
-    """The oracle (fp64 dense reference) timed on a bounded sample of the workload."""
+def _oracle_rate(budget_s):
+    """The oracle (fp64 dense reference) timed on a bounded sample of the
+    decode workload: weight bytes per second, repetitions, seconds."""
     from oracle import tern_oracle as O
     layer = I.GATE_UP
     rows = 2048
@@ -679,6 +680,31 @@ def run_cpu_baseline(args, budget_s=15.0):
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
+    return done_bytes / dt, reps, dt, rows, layer
+
+
+def _oracle_rate_one_core(budget_s):
+    """The same on one core: a child process whose BLAS libraries start with
+    one thread (their thread count is fixed when numpy loads)."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "r = bench._oracle_rate(%r); print(json.dumps([r[0], r[1], r[2]]))" % (ROOT, budget_s))
+    try:
+        p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=budget_s + 120)
+        rate, reps, dt = json.loads(p.stdout.strip().splitlines()[-1])
+        return rate, reps, dt
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
+def run_cpu_baseline(args, budget_s=15.0, one_core_s=5.0):
+    """The oracle (fp64 dense reference) timed on a bounded sample of the
+    workload, on the host's cores, and (one_core_s > 0) on one core."""
+    rate, reps, dt, rows, layer = _oracle_rate(budget_s)
     try:
         cores = len(os.sched_getaffinity(0))
     except AttributeError:
@@ -689,10 +715,16 @@ def run_cpu_baseline(args, budget_s=15.0):
         cores = min(cores, blas)
     except ImportError:
         pass
-    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
-            "kind": "oracle",
-            "sample": f"fp64 dense oracle on {rows} of {layer.n} rows of gate/up 5120->34816, "
-                      f"M=1 and M=4, {reps} repetitions in {dt:.1f} s"}
+    out = {"value": round(rate / 1e9, 4), "unit": "GB/s", "cores": cores,
+           "kind": "oracle",
+           "sample": f"fp64 dense oracle on {rows} of {layer.n} rows of gate/up 5120->34816, "
+                     f"M=1 and M=4, {reps} repetitions in {dt:.1f} s"}
+    if one_core_s > 0:
+        r1 = _oracle_rate_one_core(one_core_s)
+        if r1 is not None:
+            out["one_core"] = {"value": round(r1[0] / 1e9, 4), "unit": "GB/s", "cores": 1,
+                               "sample": f"the same sample, {r1[1]} repetitions in {r1[2]:.1f} s"}
+    return out
 
 
 def run_reference(args, rank, ws):
@@ -701,12 +733,12 @@ def run_reference(args, rank, ws):
     steps = args.steps
     per = max(1.0, min(20.0, 60.0 / max(1, steps + args.warmup)))
     for _ in range(args.warmup):
-        run_cpu_baseline(args, budget_s=per / 4)
+        run_cpu_baseline(args, budget_s=per / 4, one_core_s=0)
     vals = []
     t0 = time.perf_counter()
     base = None
     for _ in range(min(steps, 10)):
-        base = run_cpu_baseline(args, budget_s=per)
+        base = run_cpu_baseline(args, budget_s=per, one_core_s=0)
         vals.append(base["value"])
     dt = time.perf_counter() - t0
     v = statistics.median(vals)
