@@ -545,6 +545,57 @@ def run_prefill_configs(args, local, configs=((I.GATE_UP, 512), (I.DOWN, 512), (
     return out
 
 
+def run_decode_configs(args, local, shapes=(I.DOWN, I.QKV), ms=(1, 4, 8, 16)):
+    """The decode configurations of down 17408->5120 and qkv 5120->10240 at
+    M = 1, 4, 8 and 16: a step of rotation + GEMV (+ fixup), and the GEMV
+    alone, each call streaming the next of several weight copies that
+    together exceed L2 by more than 3x."""
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    hbm_peak, _, _ = _peaks()
+    out = []
+    with torch.cuda.stream(stream):
+        st = stream.cuda_stream
+        for shp in shapes:
+            copies = max(3, int(np.ceil(3 * L2_BYTES / B.tern_packed_bytes(shp.n, shp.k))))
+            lays = _make_layers(shp, copies, seed=12, prefill=False)
+            wbytes = lays[0].weight_bytes
+            for m in ms:
+                x = _activations(shp, m, seed=120 + m).cuda()
+                xh = torch.empty((m, shp.k), dtype=torch.float16, device="cuda")
+                xs = torch.empty((m, shp.k // 1024), dtype=torch.float32, device="cuda")
+                y = torch.empty((m, shp.n), dtype=torch.bfloat16, device="cuda")
+                nb = B.tern_workspace_bytes(B.TERN_OP_GEMV, m, shp.n, shp.k)
+                ws = B.Workspace().get(nb)
+                i = [0]
+
+                def gemv():
+                    lay = lays[i[0] % copies]
+                    i[0] += 1
+                    B.tern_gemv_decode(lay.packed, xh, xs, m, shp.n, shp.k, y, ws, ws.numel(), st)
+
+                def step():
+                    B.tern_fwht_quant(x, m, shp.k, None, B.TERN_FWHT_DECODE, xh, xs, st)
+                    gemv()
+
+                for _ in range(5):
+                    step()
+                torch.cuda.synchronize()
+                reps = 200
+                ts = _time_region(step, reps, stream, 1) / reps
+                tg = _time_region(gemv, reps, stream, 1) / reps
+                B.tern_check(stream)
+                out.append({"workload": f"decode {shp.name}, M={m}",
+                            "weight_GBps": round(wbytes / ts / 1e9, 1),
+                            "pct_hbm_peak": round(100 * wbytes / ts / 1e9 / hbm_peak, 1),
+                            "step_us": round(ts * 1e6, 2), "gemv_us": round(tg * 1e6, 2),
+                            "launches_per_step": 1 + B.tern_kernel_launches(B.TERN_OP_GEMV, m,
+                                                                            shp.n, shp.k)})
+            del lays
+            torch.cuda.empty_cache()
+    return out
+
+
 def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 8, 16), prefill_ms=(128, 512, 2048)):
     """The 64-layer linear stack of a 27B hybrid model: per layer qkv
     5120->10240, o 5120->5120, gate/up 5120->34816, down 17408->5120, each with
@@ -789,6 +840,8 @@ def main():
     line, layers = run_decode(args, rank, ws, local)
     del layers
     torch.cuda.empty_cache()
+    if rank == 0:
+        line["decode_configs"] = run_decode_configs(args, local)
     if not args.no_prefill:
         line["prefill"] = run_prefill(args, local)
         if rank == 0:
