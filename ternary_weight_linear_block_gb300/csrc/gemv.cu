@@ -11,7 +11,7 @@
 // arranged so that stream runs at HBM speed with few instructions per byte:
 // * unit = 512 weight rows x one 128-wide group: 16384 bytes of codes and
 //   1024 bytes of scales, contiguous in the packed format, fetched by one
-//   bulk copy (L2 evict-first) into an 8-stage shared-memory ring; the
+//   bulk copy (L2 evict-first) into a 4-stage shared-memory ring; the
 //   activation tile of the group (16 token rows x 128 k, fp16) arrives by
 //   TMA (128-byte swizzle) into the same stage; token rows >= M are
 //   zero-filled by TMA and cost no memory traffic.
@@ -65,7 +65,10 @@ constexpr int UNIT_CODE_BYTES = RB * 32;        // 512 rows x 128 codes x 2 bits
 constexpr int UNIT_BYTES = UNIT_CODE_BYTES + TILES * 32;
 constexpr int XTILE_BYTES = 16 * kGroup * 2;    // 16 token rows x 128 k, fp16 (two 64-k boxes)
 constexpr int STAGE_BYTES = 24576;
-constexpr int STAGES = 8;
+// Ring depth: measured on gate/up, down, qkv and o at M = 1-16, four stages
+// beat three, five to nine (eight: 16.60 -> 16.41 us per gate/up launch at
+// M = 4, down 12.61 -> 11.65 us at M = 1).
+constexpr int STAGES = 4;
 constexpr int CONSUMERS = 16;                   // consumer warps
 constexpr int TPW = TILES / CONSUMERS;          // tiles per consumer warp (2)
 constexpr int NUM_THREADS = 32 * (1 + CONSUMERS);   // a producer warp + the consumers
