@@ -27,6 +27,16 @@
  *   - fp16 and bf16 data are passed as uint16_t bit patterns;
  *   - every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and returns after enqueueing its kernels;
+ *   - kernels use programmatic dependent launch: each waits for the kernel
+ *     before it in the stream before it reads anything that kernel may have
+ *     written, and lets the next kernel start early.  One exception: the
+ *     decode kernels (tern_gemv_decode, tern_gemv_decode_noalloc,
+ *     tern_linear_decode) stream the packed weights before that wait, so the
+ *     packed weights must be complete when the kernel before them starts.
+ *     tern_pack ensures this for its own output (its packing kernel lets no
+ *     later kernel start before it has finished); a caller that writes
+ *     packed weights with its own kernel must let that kernel finish first
+ *     (no programmatic early launch of what follows it);
  *   - argument errors are detected on the host before anything is enqueued
  *     and nothing is written; launch errors are reported as TERN_ERR_CUDA;
  *   - M == 0 (or N == 0) is a valid no-op returning TERN_OK;

@@ -24,11 +24,16 @@ constexpr int kUnitRows = 512;
 constexpr int kUnitWords = 4352;       // 17408-byte unit: 4096 code words + 256 scale words
 
 // One thread per 32-bit word of the packed units (codes and scales).
+// The decode kernels (tern_gemv_decode, tern_linear_decode) start streaming
+// the packed units before their programmatic launch wait, so a kernel that
+// runs at the same time as them must not write the units.  This kernel
+// therefore lets no later kernel start early (the stream's next kernel
+// launches when this one has finished) and makes its stores visible to the
+// whole GPU before its threads exit.
 __global__ void pack_units_kernel(const int8_t* __restrict__ codes,
                                   const uint16_t* __restrict__ scales, int N, int K,
                                   uint32_t* __restrict__ packed, long n_words) {
   pdl_wait();
-  pdl_launch_dependents();
   const int G = K / kGroup;
   for (long wi = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; wi < n_words;
        wi += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -61,6 +66,7 @@ __global__ void pack_units_kernel(const int8_t* __restrict__ codes,
     }
     packed[wi] = out;
   }
+  __threadfence();
 }
 
 // One warp per row: smax, q, rscale.

@@ -114,3 +114,44 @@ def test_workspace_after_a_gemm_is_cleaned():
     assert np.array_equal(got, want)
     rows = np.sort(np.random.default_rng(2).choice(n, 256, replace=False))
     assert O.rel_frobenius(got[:, rows], O.linear_f64(x, codes[rows], scales[rows])) <= TOL
+
+
+def test_repack_in_place_then_decode_on_the_same_stream():
+    """tern_pack rewrites a layer's packed units in place and the decode call
+    follows on the same stream with no synchronisation in between.  The GEMV
+    streams the weights before its programmatic launch wait, so it must still
+    see the new weights: the packing kernel lets no later kernel start before
+    it has finished."""
+    n, k, m = I.GATE_UP.n, I.GATE_UP.k, 4
+    g = torch.Generator(device="cuda")
+    sets = []
+    for s in range(2):
+        g.manual_seed(500 + s)
+        codes = (torch.randint(0, 3, (n, k), dtype=torch.int8, device="cuda", generator=g)
+                 - 1).to(torch.int8)
+        scales = (0.02 * torch.randn((n, k // 128), device="cuda", generator=g).abs()
+                  + 1e-3).to(torch.float16)
+        sets.append((codes, scales))
+    x = to_dev_bf16(I.make_activations(501, m, k, I.GATE_UP.outlier_frac,
+                                       I.GATE_UP.outlier_mult)[0])
+    ws = B.Workspace()
+    ref = []
+    for codes, scales in sets:
+        lay = B.pack_layer(codes, scales, decode=True, prefill=False)
+        torch.cuda.synchronize()
+        y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        B.decode(lay, x, ws, y=y)
+        torch.cuda.synchronize()
+        ref.append(y.clone())
+    assert not torch.equal(ref[0], ref[1])
+    shared = B.pack_layer(*sets[0], decode=True, prefill=False)
+    ys = []
+    for it in range(8):
+        codes, scales = sets[it % 2]
+        B.tern_pack(codes, scales, n, k, shared.packed, None, None, None)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        B.decode(shared, x, ws, y=y)
+        ys.append(y)
+    B.tern_check()
+    for it, y in enumerate(ys):
+        assert torch.equal(y, ref[it % 2]), f"call {it} saw other weights"
