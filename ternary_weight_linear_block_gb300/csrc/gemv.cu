@@ -305,32 +305,39 @@ template <int NT>
 __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t (&sp)[TPW],
                                           const uint32_t (&bf)[NT][8][2],
                                           float (&bacc)[TPW][NT][4]) {
+  float d[TPW][NT][4];
 #pragma unroll
-  for (int tt = 0; tt < TPW; ++tt) {
-    float d[NT][4];
+  for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) d[nt][q] = 0.f;
-    const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
+      for (int q = 0; q < 4; ++q) d[tt][nt][q] = 0.f;
+  // k16 steps outer, tiles inner: the tiles' MMA chains alternate
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < 8; ++j) {
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt) {
+      const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
       const uint32_t w = w4[j >> 1];
       const int e0 = (j & 1) * 4;
       uint32_t a[4];
 #pragma unroll
       for (int p = 0; p < 4; ++p) a[p] = (w << (14 - 2 * (e0 + p))) & 0xC000C000u;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
+      for (int nt = 0; nt < NT; ++nt)
+        mma_f16(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
     }
+  }
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt) {
     uint32_t spv = sp[tt];
     const float2 s2 = __half22float2(*reinterpret_cast<__half2*>(&spv));
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      bacc[tt][nt][0] = fmaf(d[nt][0], s2.x, bacc[tt][nt][0]);
-      bacc[tt][nt][1] = fmaf(d[nt][1], s2.x, bacc[tt][nt][1]);
-      bacc[tt][nt][2] = fmaf(d[nt][2], s2.y, bacc[tt][nt][2]);
-      bacc[tt][nt][3] = fmaf(d[nt][3], s2.y, bacc[tt][nt][3]);
+      bacc[tt][nt][0] = fmaf(d[tt][nt][0], s2.x, bacc[tt][nt][0]);
+      bacc[tt][nt][1] = fmaf(d[tt][nt][1], s2.x, bacc[tt][nt][1]);
+      bacc[tt][nt][2] = fmaf(d[tt][nt][2], s2.y, bacc[tt][nt][2]);
+      bacc[tt][nt][3] = fmaf(d[tt][nt][3], s2.y, bacc[tt][nt][3]);
     }
   }
 }
