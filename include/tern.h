@@ -276,11 +276,17 @@ tern_status tern_linear_decode(const uint16_t* x, const int8_t* sign, const uint
  * exceeds TERN_NOALLOC_SCRATCH_BYTES (nothing is launched).  The first call
  * on a device, with that device current, looks up the array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture.  Every call shares the one array: each call zero-fills the
- * part it uses on its stream first (so a call that gave up waiting leaves
- * nothing behind), and calls that overlap on the GPU race on the array.
+ * stream capture.  Later calls outside a stream capture look the address up
+ * again (a device reset moves the array; a call inside a capture uses the
+ * cached address, so capture no call after a reset before an uncaptured one
+ * has run).  Every call shares the one array: each call zero-fills the part
+ * it uses on its stream first (so a call that gave up waiting leaves nothing
+ * behind), and calls that overlap on the GPU race on the array.
+ * The limit, 24 MiB, covers every workload shape of the 27B model's linear
+ * stack up to M = 16 (gate/up 5120 -> 34816 at M = 16 needs about 17 MiB on
+ * a 152-SM GB300).
  * ---------------------------------------------------------------------- */
-#define TERN_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define TERN_NOALLOC_SCRATCH_BYTES (24u << 20)
 tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uint16_t* xh, const float* xs,
                                      int64_t M, int64_t N, int64_t K, uint16_t* y,
                                      void* stream);

@@ -15,6 +15,7 @@ from __future__ import annotations
 import ctypes
 import os
 import re
+import weakref
 from dataclasses import dataclass
 
 import torch
@@ -26,7 +27,9 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "tern.h")
 TERN_OK = 0
 TERN_ERR_INVALID_ARG = 1
 TERN_ERR_UNSUPPORTED = 4
+TERN_ERR_WORKSPACE = 6
 TERN_ERR_TIMEOUT = 7
+TERN_NOALLOC_SCRATCH_BYTES = 24 << 20     # include/tern.h, tern_gemv_decode_noalloc
 TERN_FWHT_F32 = 0
 TERN_FWHT_DECODE = 1
 TERN_FWHT_I8 = 2
@@ -206,7 +209,16 @@ def tern_quant_rotated(xr, m, k, mode, out, out_scale, stream=None):
 
 
 def tern_check(stream=None):
-    return _call("tern_check", _stream(stream))
+    """Synchronise and report bounded-wait timeouts.  After a timeout the
+    decode GEMV may have left ready tags in its workspace, so every live
+    ``Workspace`` is marked dirty (its next ``get`` zero-fills it again)."""
+    st = lib().tern_check(_stream(stream))
+    if st == TERN_ERR_TIMEOUT:
+        for w in list(_WORKSPACES):
+            w.clean = 0
+    if st != TERN_OK:
+        raise TernError("tern_check", st)
+    return st
 
 
 def tern_selftest_wait(polls: int, stream=None):
@@ -288,6 +300,11 @@ def fwht(x: torch.Tensor, mode: int, sign: torch.Tensor | None = None, stream=No
     return out, sc
 
 
+# Every live Workspace, so that a timeout reported by tern_check marks them
+# all dirty.
+_WORKSPACES: "weakref.WeakSet[Workspace]" = weakref.WeakSet()
+
+
 class Workspace:
     """A device workspace for the library's calls, grown on demand; use it
     from one stream.  The decode GEMV needs the bytes it uses zero-filled and
@@ -299,6 +316,7 @@ class Workspace:
         self.device = device
         self.buf = None
         self.clean = 0        # leading bytes known to be zero
+        _WORKSPACES.add(self)
 
     def _ensure(self, nbytes: int) -> int:
         nbytes = max(int(nbytes), 256)

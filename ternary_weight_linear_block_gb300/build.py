@@ -36,6 +36,30 @@ def _run(cmd):
     return p.returncode, p.stdout
 
 
+def _inputs():
+    """Every file the library is built from."""
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    inc = os.path.join(ROOT, "include")
+    files += [os.path.join(inc, f) for f in os.listdir(inc)]
+    files.append(os.path.abspath(__file__))
+    return [f for f in files if os.path.isfile(f)]
+
+
+def is_stale() -> bool:
+    """True when libtern.so is missing or older than any of its sources."""
+    if not os.path.exists(LIB):
+        return True
+    built = os.path.getmtime(LIB)
+    return any(os.path.getmtime(f) > built for f in _inputs())
+
+
+def ensure_built() -> str:
+    """Build libtern.so if it is missing or stale; returns its path."""
+    if is_stale():
+        build()
+    return LIB
+
+
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile every translation unit and link libtern.so; returns its path."""
     nvcc = _nvcc()

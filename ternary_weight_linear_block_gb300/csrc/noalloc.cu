@@ -12,7 +12,11 @@
 //
 // The first call on a device (with that device current) looks up the array's
 // device address with cudaGetSymbolAddress and caches it per device; that
-// first call should come before any stream capture.  All calls share the one
+// first call should come before any stream capture.  Every later call made
+// outside a stream capture looks the address up again and refreshes the
+// cache, so a device reset (which reloads the module at a new address) is
+// picked up by the next uncaptured call; a call inside a capture uses the
+// cached address.  All calls share the one
 // array and it keeps the last call's contents, so each call zero-fills the
 // part it uses on its stream before the kernel (a call that gave up waiting
 // may have left ready tags set); calls that overlap on the GPU (for example
@@ -29,9 +33,14 @@ constexpr int kMaxDevices = 64;
 // calls store the same value.
 std::atomic<void*> g_scratch_addr[kMaxDevices];
 
-cudaError_t scratch_address(int dev, void** out) {
+cudaError_t scratch_address(int dev, cudaStream_t st, void** out) {
   void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();          // e.g. the legacy stream during a global capture
+    cs = cudaStreamCaptureStatusActive;
+  }
+  if (p == nullptr || cs == cudaStreamCaptureStatusNone) {
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev].store(p, std::memory_order_release);
@@ -59,9 +68,9 @@ extern "C" tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uin
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || !device_supported())
     return TERN_ERR_UNSUPPORTED;
-  void* scratch = nullptr;
-  if (scratch_address(dev, &scratch) != cudaSuccess) return TERN_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  if (scratch_address(dev, st, &scratch) != cudaSuccess) return TERN_ERR_CUDA;
   if (cudaMemsetAsync(scratch, 0, gemv_workspace_bytes(M, N, K), st) != cudaSuccess)
     return TERN_ERR_CUDA;
   return launch_gemv(packed, xh, xs, M, N, K, y, scratch, st) == cudaSuccess ? TERN_OK

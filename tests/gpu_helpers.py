@@ -1,7 +1,5 @@
 """Shared helpers for the GPU parity tests (marshalling only)."""
 
-import os
-
 import numpy as np
 import torch
 
@@ -10,8 +8,7 @@ from ternary_weight_linear_block_gb300 import build as BUILD
 
 
 def ensure_lib():
-    if not os.path.exists(B.LIB_PATH):
-        BUILD.build()
+    BUILD.ensure_built()          # missing, or older than a source file
     return B.lib()
 
 

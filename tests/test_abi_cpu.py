@@ -16,8 +16,7 @@ from ternary_weight_linear_block_gb300 import build as BUILD
 
 @pytest.fixture(scope="session")
 def lib():
-    if not os.path.exists(B.LIB_PATH):
-        BUILD.build()
+    BUILD.ensure_built()          # missing, or older than a source file
     return B.lib()
 
 
@@ -234,3 +233,56 @@ def test_workspace_zero_fills_for_the_gemv_after_a_gemm(monkeypatch):
     ws.scratch(4000).fill_(7)                   # grows: a new buffer, contents undefined
     c = ws.get(100)
     assert c.numel() == 4000 and not c.any() and fills[-1] == 4000
+
+
+def test_a_timeout_marks_every_workspace_dirty(monkeypatch):
+    """After tern_check reports a bounded wait that gave up, the GEMV may have
+    left ready tags in its workspace: every live Workspace's next ``get``
+    zero-fills again (host logic; tern_check and the fill are faked)."""
+    fills = []
+
+    def fake_init(ws, nbytes=None, stream=None):
+        ws[:nbytes].zero_()
+        fills.append(nbytes)
+        return B.TERN_OK
+
+    class FakeLib:
+        status = B.TERN_OK
+
+        def tern_check(self, stream):
+            return self.status
+
+    fake = FakeLib()
+    monkeypatch.setattr(B, "tern_workspace_init", fake_init)
+    monkeypatch.setattr(B, "lib", lambda: fake)
+    a, b = B.Workspace(device="cpu"), B.Workspace(device="cpu")
+    a.get(512)
+    b.get(256)
+    assert fills == [512, 256]
+    B.tern_check(stream=0)                      # OK: nothing changes
+    a.get(512)
+    b.get(256)
+    assert fills == [512, 256]
+    fake.status = B.TERN_ERR_TIMEOUT
+    with pytest.raises(B.TernError) as ei:
+        B.tern_check(stream=0)
+    assert ei.value.status == B.TERN_ERR_TIMEOUT
+    a.get(512)
+    b.get(256)
+    assert fills == [512, 256, 512, 256]
+
+
+def test_binding_constants_match_the_header():
+    import re
+    with open(B.HEADER) as f:
+        text = f.read()
+    m = re.search(r"#define TERN_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == B.TERN_NOALLOC_SCRATCH_BYTES
+    for name in ("TERN_ERR_WORKSPACE", "TERN_ERR_TIMEOUT", "TERN_ERR_INVALID_ARG",
+                 "TERN_ERR_UNSUPPORTED"):
+        m = re.search(r"\b%s = (\d+)" % name, text)
+        assert m and int(m.group(1)) == getattr(B, name), name
+    for name in ("TERN_OP_GEMV", "TERN_OP_GEMM", "TERN_OP_GEMM_PACKED", "TERN_FWHT_F32",
+                 "TERN_FWHT_DECODE", "TERN_FWHT_I8"):
+        m = re.search(r"#define %s (\d+)" % name, text)
+        assert m and int(m.group(1)) == getattr(B, name), name

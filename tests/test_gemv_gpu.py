@@ -1,5 +1,6 @@
 """GPU parity of the decode path (rotation + tern_gemv_decode) against the
-fp64 oracle: relative Frobenius error <= 4e-3 on bf16 outputs."""
+fp64 oracle: relative Frobenius error <= 4e-3 on bf16 outputs, and every
+compared element within the element-wise bound of tests/decode_bounds.py."""
 
 import numpy as np
 import pytest
@@ -8,6 +9,7 @@ import torch
 from oracle import tern_oracle as O
 from ternary_weight_linear_block_gb300 import binding as B
 from ternary_weight_linear_block_gb300 import inputs as I
+from tests.decode_bounds import block_sample_rows, check_elementwise
 from tests.gpu_helpers import bf16_to_f32, ensure_lib, poison, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
@@ -41,6 +43,7 @@ def test_tiny_layer(m):
     e = O.rel_frobenius(y, ref)
     assert e <= TOL, e
     assert e > 0   # an exact match against fp64 would be suspicious for bf16 outputs
+    check_elementwise(y, ref, d.codes, d.scales, d.x, what=f"tiny M={m}")
 
 
 @pytest.mark.parametrize("n,k,m", [(100, 2048, 3), (272, 3072, 13), (16, 1024, 1), (4112, 4096, 5),
@@ -50,8 +53,10 @@ def test_ragged_shapes(n, k, m):
     scales = I.make_scales(7, n, k)
     bits, x = I.make_activations(7, m, k, 0.01, 20.0)
     y = _decode(_layer(codes, scales), bits, m)
-    e = O.rel_frobenius(y, O.linear_f64(x, codes, scales))
+    ref = O.linear_f64(x, codes, scales)
+    e = O.rel_frobenius(y, ref)
     assert e <= TOL, e
+    check_elementwise(y, ref, codes, scales, x, what=f"{n}x{k} M={m}")
 
 
 @pytest.mark.parametrize("layer,m", [(I.GATE_UP, 1), (I.GATE_UP, 4), (I.GATE_UP, 16), (I.DOWN, 1),
@@ -59,14 +64,18 @@ def test_ragged_shapes(n, k, m):
                                      (I.QKV, 8), (I.QKV, 16), (I.O_PROJ, 4)])
 def test_full_size_sampled_rows(layer, m):
     """Full workload shapes in the benchmarked launch; the oracle computes a
-    seeded sample of 512 output rows for all tokens."""
+    seeded sample of output rows for all tokens: 512 at random plus two of
+    every 512-row block (the GEMV's unit of rows, so every block, every
+    block's owners and every fixup slot are looked at)."""
     d = I.make_layer(layer, m, seed=0)
     y = _decode(_layer(d.codes, d.scales), d.x_bits, m)
-    rows = np.sort(np.random.default_rng(1).choice(layer.n, 512, replace=False))
+    rows = block_sample_rows(layer.n, seed=1)
     ref = O.linear_f64(d.x, d.codes[rows], d.scales[rows])
     e = O.rel_frobenius(y[:, rows], ref)
     assert e <= TOL, e
     assert np.isfinite(y).all()
+    check_elementwise(y[:, rows], ref, d.codes[rows], d.scales[rows], d.x,
+                      what=f"{layer.name} M={m}")
 
 
 def test_repeat_calls_reuse_workspace():
@@ -112,8 +121,10 @@ def test_workspace_after_a_gemm_is_cleaned():
     buf.view(torch.int64).fill_((1 << 32) | 0x3F800000)   # tag 1, value 1.0f
     got = _decode(layer, bits, m, ws)
     assert np.array_equal(got, want)
-    rows = np.sort(np.random.default_rng(2).choice(n, 256, replace=False))
-    assert O.rel_frobenius(got[:, rows], O.linear_f64(x, codes[rows], scales[rows])) <= TOL
+    rows = block_sample_rows(n, seed=2, extra=256)
+    ref = O.linear_f64(x, codes[rows], scales[rows])
+    assert O.rel_frobenius(got[:, rows], ref) <= TOL
+    check_elementwise(got[:, rows], ref, codes[rows], scales[rows], x, what="after a GEMM")
 
 
 def test_repack_in_place_then_decode_on_the_same_stream():

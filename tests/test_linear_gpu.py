@@ -10,6 +10,7 @@ import torch
 from oracle import tern_oracle as O
 from ternary_weight_linear_block_gb300 import binding as B
 from ternary_weight_linear_block_gb300 import inputs as I
+from tests.decode_bounds import block_sample_rows, check_elementwise
 from tests.gpu_helpers import bf16_to_f32, ensure_lib, poison, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
@@ -80,11 +81,13 @@ def test_against_oracle(layer, m):
     B.decode(lay, to_dev_bf16(d.x_bits), B.Workspace(), y=y, fused=True)
     B.tern_check()
     y = bf16_to_f32(y)
-    rows = np.arange(lay.n) if lay.n <= 512 else \
-        np.sort(np.random.default_rng(2).choice(lay.n, 512, replace=False))
-    e = O.rel_frobenius(y[:, rows], O.linear_f64(d.x, d.codes[rows], d.scales[rows]))
+    rows = np.arange(lay.n) if lay.n <= 512 else block_sample_rows(lay.n, seed=2)
+    ref = O.linear_f64(d.x, d.codes[rows], d.scales[rows])
+    e = O.rel_frobenius(y[:, rows], ref)
     assert e <= TOL, e
     assert np.isfinite(y).all()
+    check_elementwise(y[:, rows], ref, d.codes[rows], d.scales[rows], d.x,
+                      what=f"fused {layer.name} M={m}")
 
 
 def test_empty_and_repeat():

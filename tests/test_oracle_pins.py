@@ -425,3 +425,86 @@ def test_ksplit_swapped_parts_is_caught():
     bad = np.concatenate([O.ksplit_combine(a, b, 1), O.ksplit_combine(a, b, 0)], axis=1)
     assert np.array_equal(good, ref)
     assert O.rel_frobenius(bad, ref) > 1.0
+
+
+# ---------------------------------------------------------------- error metric
+
+def _matrix(txt):
+    return np.array([[float(v) for v in row.split()] for row in txt.split(";")])
+
+
+def _rel_frobenius_golden():
+    out = []
+    for r in _rows("rel_frobenius.txt"):
+        y_txt, ref_txt, sq_txt = [p.strip() for p in r.split("|")]
+        out.append((_matrix(y_txt), _matrix(ref_txt), Fraction(sq_txt)))
+    return out
+
+
+def test_rel_frobenius_hand_computed_golden():
+    """The metric every tolerance is stated in (relative Frobenius error over
+    the whole output), against hand-computed rationals: the square of the
+    returned value equals num^2 / den^2 to the last bits of fp64."""
+    cases = _rel_frobenius_golden()
+    assert len(cases) == 5
+    for y, ref, sq in cases:
+        got = O.rel_frobenius(y, ref)
+        assert abs(Fraction(got) ** 2 - sq) <= Fraction(1, 2 ** 48) * max(sq, 1), (y, ref, got)
+    # the first worked example: sqrt(10) / 5
+    assert O.rel_frobenius([[3.0, 4.0]], [[0.0, 5.0]]) == pytest.approx(np.sqrt(10) / 5, rel=1e-15)
+
+
+def test_rel_frobenius_invariants():
+    rng = np.random.default_rng(11)
+    ref = rng.standard_normal((4, 37))
+    y = ref + 1e-3 * rng.standard_normal((4, 37))
+    e = O.rel_frobenius(y, ref)
+    # scale invariance, exact for powers of two
+    assert O.rel_frobenius(8.0 * y, 8.0 * ref) == e
+    # invariant under any permutation of the entries applied to both
+    p = rng.permutation(y.size)
+    assert O.rel_frobenius(y.ravel()[p], ref.ravel()[p]) == pytest.approx(e, rel=1e-14)
+    # a whole-output metric: equals the root of the summed squared row errors
+    num = sum(float(np.sum((y[i] - ref[i]) ** 2)) for i in range(4))
+    den = sum(float(np.sum(ref[i] ** 2)) for i in range(4))
+    assert e == pytest.approx(np.sqrt(num / den), rel=1e-14)
+    # degenerate cases
+    assert O.rel_frobenius(ref, ref) == 0.0
+    assert O.rel_frobenius(np.zeros(3), np.zeros(3)) == 0.0
+    assert O.rel_frobenius(np.ones(3), np.zeros(3)) == float("inf")
+    assert O.rel_frobenius(np.zeros((2, 3)), ref[:2, :3]) == pytest.approx(1.0, rel=1e-15)
+
+
+def test_rel_frobenius_planted_mistakes_are_caught():
+    """Plausible slips in the metric (arguments swapped, the square root
+    dropped, a max norm or a per-row mean in place of the whole-output norm,
+    the denominator taken from the difference) each fail the golden."""
+    def swapped(y, ref):
+        y, ref = np.asarray(y, np.float64), np.asarray(ref, np.float64)
+        return float(np.linalg.norm(y - ref) / np.linalg.norm(y))
+
+    def no_sqrt(y, ref):
+        y, ref = np.asarray(y, np.float64), np.asarray(ref, np.float64)
+        return float(np.sum((y - ref) ** 2) / np.sum(ref ** 2))
+
+    def max_norm(y, ref):
+        y, ref = np.asarray(y, np.float64), np.asarray(ref, np.float64)
+        return float(np.max(np.abs(y - ref)) / np.max(np.abs(ref)))
+
+    def row_mean(y, ref):
+        y, ref = np.atleast_2d(np.asarray(y, np.float64)), np.atleast_2d(np.asarray(ref, np.float64))
+        return float(np.mean([np.linalg.norm(a - b) / np.linalg.norm(b) for a, b in zip(y, ref)]))
+
+    def diff_denominator(y, ref):
+        y, ref = np.asarray(y, np.float64), np.asarray(ref, np.float64)
+        return float(np.linalg.norm(y - ref) / np.linalg.norm(y - ref + ref))
+
+    cases = _rel_frobenius_golden()
+
+    def passes(fn):
+        return all(abs(Fraction(fn(y, ref)) ** 2 - sq) <= Fraction(1, 2 ** 40) * max(sq, 1)
+                   for y, ref, sq in cases)
+
+    assert passes(O.rel_frobenius)
+    for mutant in (swapped, no_sqrt, max_norm, row_mean, diff_denominator):
+        assert not passes(mutant), mutant.__name__
