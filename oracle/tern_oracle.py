@@ -27,9 +27,11 @@ O2 (int8 path, spec-exact fp32 operation sequence)
                         w_int8 / acc_int8 / y_int8 / linear_int8
 K split (section 1)     fwht_half_f32 / ksplit_combine / ksplit_rotate_f32
 
-plus the 2-bit storage format (pack_weights / unpack_weights) and the fp16
-decode operand (decode_operand), which the pages leave open and this library
-defines (see ``include/tern.h``).
+plus the 2-bit storage format (pack_weights / unpack_weights), the decode
+GEMV's activation operand (decode_operand: fp16 with a power of two per block
+and per k16 step, plus per-group offsets and per-block fold factors) and the
+fp16 prefill variant's operand (f16_operand), which the pages leave open and
+this library defines (see ``include/tern.h``).
 
 Readings of the pages taken here (each is also listed in the design notes):
 * natural (Sylvester) order H, not sequency order; normalised by 1/32 per block;
@@ -374,34 +376,34 @@ def rel_frobenius(y, yref) -> float:
 # 2-bit storage format (defined by this library; the pages leave it open)
 # --------------------------------------------------------------------------
 #
-# A 2-bit field holds one code: high bit = "negative", low bit = "nonzero".
-#   +1 -> 0b01, -1 -> 0b11, 0 -> 0b00 (0b10 also reads as 0 and is never written).
-#
-# Rows are padded with zero codes and zero scales to a multiple of 512.  The
-# packed buffer is a sequence of 17408-byte units, unit rb * G + g for row
-# block rb (512 rows) and group g (128 k), G = K / 128.  In a unit:
+# A 2-bit field holds u = code + 1: -1 -> 0, 0 -> 1, +1 -> 2 (3 is never
+# written).  Rows are padded with zero codes (u = 1) and zero scales to a
+# multiple of 512.  The packed buffer is a sequence of 17408-byte units, unit
+# rb * G + g for row block rb (512 rows) and group g (128 k), G = K / 128.
+# In a unit:
 #   bytes [0, 16384): 32 tiles of 16 rows, tile t at byte 512 t; slot L
 #     (bytes 512 t + 16 L ..) holds four little-endian 32-bit words w_0..w_3;
-#     with r = L // 4, c = L % 4, word i, field e (0..7), jj = e // 4,
-#     p = e % 4, j = 2 i + jj:
-#       bits 2e..2e+1 of w_i:     code(row, k)
-#       bits 16+2e..17+2e of w_i: code(row, k + 1)
+#     with r = L // 4, c = L % 4, word p and field j (0..7):
+#       bits 2j..2j+1 of w_p:     u(row, k)
+#       bits 16+2j..17+2j of w_p: u(row, k + 1)
 #     with row = 512 rb + 16 t + r + 8 (p % 2), k = 128 g + 16 j + 2 c + 8 (p // 2);
 #   bytes [16384, 17408): fp16 scale pairs, tile t at 16384 + 32 t:
 #     (s[512 rb + 16 t + r, g], s[512 rb + 16 t + r + 8, g]) for r = 0..7.
+#
+# Word p is register p of the A fragment of a 16 x 16 tensor-core tile for
+# all 8 k16 steps j of the group: field j masked in place (j < 6), or field
+# j of w_p >> 12 for j = 6, 7 (that is, field j - 6 of the shifted word),
+# read as an fp16 pair, is u * 4^e(j) * 2^-24 with e(j) = j for j < 6 and
+# j - 6 otherwise: a subnormal (e <= 4, the field inside the mantissa) or the
+# two lowest exponent bits (e = 5: 0x0400 = 2^-14, 0x0800 = 2^-13).
 
 UNIT_ROWS = 512
 UNIT_BYTES = 17408
 
 
-def _field(code):
-    code = np.asarray(code).astype(np.int64)
-    return np.where(code == 1, 1, np.where(code == -1, 3, 0)).astype(np.uint64)
-
-
-def _field_value(f):
-    f = np.asarray(f).astype(np.int64)
-    return np.where((f & 1) == 0, 0, np.where((f & 2) != 0, -1, 1)).astype(np.int8)
+def step_exponent(j: int) -> int:
+    """e(j): the power of four carried by the field of k16 step j."""
+    return j if j < 6 else j - 6
 
 
 def padded_rows(n: int) -> int:
@@ -416,22 +418,22 @@ def pack_weights(codes, scales) -> np.ndarray:
         raise ValueError("K must be a multiple of 128")
     g_count = k // GROUP
     npad = padded_rows(n)
-    full = np.zeros((npad, k), dtype=np.int8)
+    full = np.zeros((npad, k), dtype=np.int64)
     full[:n] = codes
     sfull = np.zeros((npad, g_count), dtype=np.float16)
     sfull[:n] = np.asarray(scales, dtype=np.float16)
     rbs = npad // UNIT_ROWS
-    # [rb, t, rh, r, g, i, jj, kh, c, lohi]: row = 512 rb + 16 t + 8 rh + r,
-    # k = 128 g + 32 i + 16 jj + 8 kh + 2 c + lohi
-    f = _field(full.reshape(rbs, 32, 2, 8, g_count, 4, 2, 2, 4, 2))
-    words = np.zeros((rbs, g_count, 32, 8, 4, 4), dtype=np.uint64)     # rb, g, t, r, c, i
-    for jj in range(2):
+    # [rb, t, rh, r, g, j, kh, c, lohi]: row = 512 rb + 16 t + 8 rh + r,
+    # k = 128 g + 16 j + 8 kh + 2 c + lohi
+    u = (full + 1).astype(np.uint64).reshape(rbs, 32, 2, 8, g_count, 8, 2, 4, 2)
+    words = np.zeros((rbs, g_count, 32, 8, 4, 4), dtype=np.uint64)     # rb, g, t, r, c, p
+    for j in range(8):
         for kh in range(2):
             for rh in range(2):
-                e = 4 * jj + 2 * kh + rh                                # p = 2 kh + rh
                 for lohi in range(2):
-                    part = f[:, :, rh, :, :, :, jj, kh, :, lohi]          # rb, t, r, g, i, c
-                    words |= part.transpose(0, 3, 1, 2, 5, 4) << np.uint64(16 * lohi + 2 * e)
+                    part = u[:, :, rh, :, :, j, kh, :, lohi]            # rb, t, r, g, c
+                    words[..., 2 * kh + rh] |= part.transpose(0, 3, 1, 2, 4) << \
+                        np.uint64(16 * lohi + 2 * j)
     code_bytes = words.astype("<u4").reshape(rbs, g_count, 4096).view(np.uint8)
     sc = sfull.reshape(rbs, 32, 2, 8, g_count).transpose(0, 4, 1, 3, 2)  # rb, g, t, r, rh
     scale_bytes = np.ascontiguousarray(sc).astype("<f2").view(np.uint8).reshape(rbs, g_count, 1024)
@@ -446,16 +448,15 @@ def unpack_weights(packed, n: int, k: int):
     rbs = npad // UNIT_ROWS
     units = np.ascontiguousarray(packed, dtype=np.uint8).reshape(rbs, g_count, UNIT_BYTES)
     words = units[:, :, :16384].copy().view("<u4").reshape(rbs, g_count, 32, 8, 4, 4)
-    words = words.astype(np.uint64)                                     # rb, g, t, r, c, i
-    out = np.zeros((rbs, 32, 2, 8, g_count, 4, 2, 2, 4, 2), dtype=np.int8)
-    for jj in range(2):
+    words = words.astype(np.uint64)                                     # rb, g, t, r, c, p
+    out = np.zeros((rbs, 32, 2, 8, g_count, 8, 2, 4, 2), dtype=np.int8)
+    for j in range(8):
         for kh in range(2):
             for rh in range(2):
-                e = 4 * jj + 2 * kh + rh
                 for lohi in range(2):
-                    fld = (words >> np.uint64(16 * lohi + 2 * e)) & np.uint64(3)
-                    out[:, :, rh, :, :, :, jj, kh, :, lohi] = \
-                        _field_value(fld).transpose(0, 2, 3, 1, 5, 4)
+                    fld = (words[..., 2 * kh + rh] >> np.uint64(16 * lohi + 2 * j)) & np.uint64(3)
+                    out[:, :, rh, :, :, j, kh, :, lohi] = \
+                        (fld.astype(np.int64) - 1).astype(np.int8).transpose(0, 2, 3, 1, 4)
     codes = out.reshape(npad, k)
     sc = units[:, :, 16384:].copy().view("<f2").reshape(rbs, g_count, 32, 8, 2)
     scales = sc.transpose(0, 2, 4, 3, 1).reshape(npad, g_count)
@@ -463,24 +464,84 @@ def unpack_weights(packed, n: int, k: int):
 
 
 # --------------------------------------------------------------------------
-# fp16 decode operand (the GEMV's activation format, defined in include/tern.h)
+# Decode operand (the GEMV's activation format, defined in include/tern.h)
 # --------------------------------------------------------------------------
 
-def decode_operand(xr):
-    """fp16 copy of the rotated activations, one power-of-two factor per block.
+def _block_shift(xr):
+    """sh[m, b] = min(14 - E, 126), E = (biased exponent field of the fp32
+    absmax of the block) - 127: 2^sh puts the block's largest magnitude in
+    [2^14, 2^15)."""
+    xr = np.asarray(xr, dtype=np.float32)
+    m, k = xr.shape
+    blocks = np.abs(xr).reshape(m, k // HBLOCK, HBLOCK).max(axis=2).astype(np.float32)
+    e = ((blocks.view(np.uint32) >> 23) & 0xFF).astype(np.int64) - 127
+    return np.minimum(14 - e, 126)
 
-    For token m and 1024-block b: E = (biased exponent field of the fp32
-    absmax of the block) - 127, F = 2^min(14 - E, 126); values
+
+def f16_operand(xr):
+    """fp16 copy of the rotated activations, one power-of-two factor per block
+    (the fp16 prefill variant's operand).
+
+    For token m and 1024-block b: F = 2^sh (_block_shift); values
     fp16_rn(xr * F) (the fp32 product is exact), natural [M, K] order.
     Returns (fp16 [M, K], inv [M, B] with inv = 1/F).
     """
     xr = np.asarray(xr, dtype=np.float32)
     m, k = xr.shape
     nb = k // HBLOCK
-    blocks = np.abs(xr).reshape(m, nb, HBLOCK).max(axis=2).astype(np.float32)
-    e = ((blocks.view(np.uint32) >> 23) & 0xFF).astype(np.int64) - 127
-    sh = np.minimum(14 - e, 126)
+    sh = _block_shift(xr)
     f = np.ldexp(np.float32(1.0), sh).astype(np.float32)
     inv = np.ldexp(np.float32(1.0), -sh).astype(np.float32)
     scaled = (xr.reshape(m, nb, HBLOCK) * f[:, :, None]).astype(np.float32).reshape(m, k)
     return scaled.astype(np.float16), inv
+
+
+def _k_exponents(k: int) -> np.ndarray:
+    """e(j(k)) for every column k: the k16 step j = (k mod 128) // 16."""
+    j = (np.arange(k) % GROUP) // 16
+    return np.where(j < 6, j, j - 6)
+
+
+def decode_operand(xr):
+    """The decode GEMV's activation operand for M <= 16 tokens.
+
+    For token m, 1024-block b (F = 2^sh, _block_shift) and column k of k16
+    step j (e = e(j), see the packed format):
+      xh[m, k] = fp16_rn(xr[m, k] * 2^(sh - 2e))      (the fp32 product is exact)
+    and per 128-group g, a 32-float record aux[g]:
+      aux[g][m]      = X[g, m] = the fp32 sum over k in g of xh[m, k] * 2^(2e - 24)
+                       (each term exact), added in this order: the eight
+                       consecutive columns 8q .. 8q + 7 of the group left to
+                       right (q = 0..15), then the sixteen partial sums by a
+                       butterfly tree, p[q] <- p[q] + p[q ^ s] for s = 1, 2, 4, 8;
+      aux[g][16 + m] = 2^(12 - sh) of the block holding g;
+      both 0 for m >= M.
+    A field read u * 4^e * 2^-24 times xh[m, k] is u * xh * 2^(2e - 24), so the
+    tensor core's group sum minus X is sum_k code * xr * 2^(sh - 24) (up to
+    rounding); times the block's 2^(12 - sh) that is 2^-12 sum_k code * xr.
+    Returns (fp16 [M, K], float32 [G, 32]).
+    """
+    xr = np.asarray(xr, dtype=np.float32)
+    m, k = xr.shape
+    if m > 16:
+        raise ValueError("the decode operand holds at most 16 tokens")
+    nb, g_count = k // HBLOCK, k // GROUP
+    sh = _block_shift(xr)                                             # [m, nb]
+    e = _k_exponents(k)                                               # [k]
+    shk = np.repeat(sh, HBLOCK, axis=1) - 2 * e[None, :]              # [m, k]
+    xh = (xr * np.ldexp(np.float32(1.0), shk).astype(np.float32)).astype(np.float32)
+    xh = xh.astype(np.float16)
+    terms = (xh.astype(np.float32) * np.ldexp(np.float32(1.0), 2 * e - 24)
+             .astype(np.float32)[None, :]).astype(np.float32)         # exact
+    t = terms.reshape(m, g_count, 16, 8)
+    p = t[..., 0].copy()
+    for i in range(1, 8):
+        p = (p + t[..., i]).astype(np.float32)
+    idx = np.arange(16)
+    for sft in (1, 2, 4, 8):
+        p = (p + p[..., idx ^ sft]).astype(np.float32)
+    aux = np.zeros((g_count, 32), dtype=np.float32)
+    aux[:, :m] = p[:, :, 0].T
+    fold = np.ldexp(np.float32(1.0), 12 - sh).astype(np.float32)      # [m, nb]
+    aux[:, 16:16 + m] = np.repeat(fold, HBLOCK // GROUP, axis=1).T
+    return xh, aux

@@ -63,3 +63,24 @@ def block_sample_rows(n: int, seed: int, extra: int = 512, per_block: int = 2) -
         rows.update(rng.choice(np.arange(b0, b1), min(per_block, b1 - b0),
                                replace=False).tolist())
     return np.array(sorted(rows))
+
+
+def emulate_decode(codes, scales, x, sign=None):
+    """The decode GEMV's arithmetic in fp64 from the oracle's pieces: the
+    packed fields read as A fragments (u * 4^e * 2^-24), the decode operand as
+    B, each group's sum minus its offset times the group scale, each block's
+    sum times its fold factor, times 2^12, then the bf16 output rounding."""
+    n, k = codes.shape
+    packed = O.pack_weights(codes, scales)
+    c2, s2 = O.unpack_weights(packed, n, k)
+    xh, aux = O.decode_operand(O.fwht_f32(np.asarray(x, np.float32), sign))
+    m = xh.shape[0]
+    j = (np.arange(k) % 128) // 16
+    e = np.where(j < 6, j, j - 6)
+    a = (c2.astype(np.float64) + 1.0) * 4.0 ** e[None, :] * 2.0 ** -24
+    y = np.zeros((m, n))
+    for g in range(k // 128):
+        cols = slice(128 * g, 128 * g + 128)
+        d = xh[:, cols].astype(np.float64) @ a[:, cols].T - aux[g, :m][:, None].astype(np.float64)
+        y += (d * s2[:, g].astype(np.float64)[None, :]) * aux[g, 16:16 + m][:, None]
+    return O.bf16_round((y * 2.0 ** 12).astype(np.float32)).astype(np.float64)

@@ -1,8 +1,9 @@
 """The element-wise decode bound (tests/decode_bounds.py) on the CPU.
 
-An emulation of the decode arithmetic from the oracle's pieces (the fp16
-decode operand, the exact fp16 scales, fp64 accumulation, bf16 output
-rounding) must pass the bound on every element; the same emulation with a
+An emulation of the decode arithmetic from the oracle's pieces (the packed
+fields as tensor-core fragments, the decode operand with its group offsets
+and fold factors, fp64 accumulation, bf16 output rounding) must pass the
+bound on every element; the same emulation with a
 planted localised mistake (one 128-group of one row dropped, one group's
 scale doubled, one row block's output left at zero) must fail it, although
 the first two stay far inside the whole-output 4e-3 Frobenius bar.
@@ -13,17 +14,11 @@ import pytest
 
 from oracle import tern_oracle as O
 from ternary_weight_linear_block_gb300 import inputs as I
-from tests.decode_bounds import block_sample_rows, check_elementwise
+from tests.decode_bounds import block_sample_rows, check_elementwise, emulate_decode
 
 
 def _emulated_decode(x, codes, scales):
-    """y = bf16(sum_b inv[m,b] sum_{k in b} W[n,k] fp16(xr F)) in fp64."""
-    xr = O.fwht_f32(x)
-    xh, inv = O.decode_operand(xr)
-    m, k = xh.shape
-    xd = (xh.astype(np.float64).reshape(m, k // 1024, 1024) * inv[:, :, None]).reshape(m, k)
-    y = xd @ O.dequant_f64(codes, scales).T
-    return O.bf16_round(y.astype(np.float32)).astype(np.float64)
+    return emulate_decode(codes, scales, x)
 
 
 @pytest.mark.parametrize("k,n,m", [(5120, 256, 4), (17408, 128, 2)])

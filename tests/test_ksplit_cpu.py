@@ -53,7 +53,7 @@ class OracleOps:
         xr[:, 1024 * blk + 512:1024 * (blk + 1)] = 0
 
     def decode(self, lin, xr, ws):
-        xh, inv = O.decode_operand(xr.numpy())
+        xh, inv = O.f16_operand(xr.numpy())
         kp = xr.shape[1]
         x_eff = (xh.astype(np.float64).reshape(-1, kp // 1024, 1024) *
                  inv.astype(np.float64)[:, :, None]).reshape(-1, kp)

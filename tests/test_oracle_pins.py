@@ -319,7 +319,8 @@ def test_pack_format_golden():
     code_words = {}
     for unit in range(2):
         w = p[unit * 17408:unit * 17408 + 16384].view("<u4")
-        code_words.update({unit * 17408 + 4 * i: int(v) for i, v in enumerate(w) if v})
+        code_words.update({unit * 17408 + 4 * i: int(v) for i, v in enumerate(w)
+                           if v != 0x55555555})
     assert code_words == expect
     # scale pairs: s[3, 1] -> unit 1, tile 0, pair 3, low half; s[20, 0] -> tile 1, pair 4
     assert p[17408 + 16384 + 12:17408 + 16384 + 14].view("<f2")[0] == np.float16(0.5)
@@ -338,11 +339,18 @@ def test_pack_roundtrip(n, k):
     assert np.array_equal(c2, codes) and np.array_equal(s2, s)
 
 
-def test_pack_halfword_reading_gives_two_times_code():
-    # (w_i << (14 - 2e)) & 0xC000C000 read as an fp16 pair is
-    # (2 code(row, k), 2 code(row, k + 1)) with row = 16 t + r + 8 (p % 2),
-    # k = 16 j + 2 c + 8 (p // 2): register p of the A fragment of the
-    # m16n8k16 MMA for k16 step j (0x4000 = 2.0, 0xC000 = -2.0).
+def _f16(bits):
+    return float(np.array([bits], np.uint16).view(np.float16)[0])
+
+
+def test_pack_field_reading_is_the_a_fragment():
+    """Field j of word p, masked in place (j < 6) or from the word shifted
+    right by 12 (j = 6, 7), read as an fp16 pair, is (u(row, k), u(row, k+1))
+    * 4^e(j) * 2^-24 with u = code + 1, row = 16 t + r + 8 (p % 2),
+    k = 16 j + 2 c + 8 (p // 2): register p of the A fragment of a 16 x 16
+    tensor-core tile for k16 step j.  The fp16 values are computed here from
+    the IEEE encoding (subnormal: m * 2^-24; exponent field 1 or 2 with a zero
+    mantissa: 2^-14, 2^-13), not from the oracle."""
     rng = np.random.default_rng(12)
     codes = rng.integers(-1, 2, (512, 128)).astype(np.int8)
     words = O.pack_weights(codes, np.zeros((512, 1), np.float16))[:16384].view("<u4")
@@ -350,33 +358,125 @@ def test_pack_halfword_reading_gives_two_times_code():
     for t in range(0, 32, 7):
         for lane in range(32):
             r, c = lane // 4, lane % 4
-            for i in range(4):
-                for e in range(8):
-                    v = (int(words[t, lane, i]) << (14 - 2 * e)) & 0xC000C000
-                    lo = np.array([v & 0xFFFF], np.uint16).view(np.float16)[0]
-                    hi = np.array([v >> 16], np.uint16).view(np.float16)[0]
-                    jj, p = e // 4, e % 4
+            for p in range(4):
+                w = int(words[t, lane, p])
+                for j in range(8):
+                    v = (w if j < 6 else w >> 12) & (0x00030003 << (2 * (j % 6)))
+                    e = j if j < 6 else j - 6
                     row = 16 * t + r + 8 * (p % 2)
-                    k = 16 * (2 * i + jj) + 2 * c + 8 * (p // 2)
-                    assert float(lo) == 2.0 * codes[row, k]
-                    assert float(hi) == 2.0 * codes[row, k + 1]
+                    k = 16 * j + 2 * c + 8 * (p // 2)
+                    for half, kk in ((v & 0xFFFF, k), (v >> 16, k + 1)):
+                        u = codes[row, kk] + 1
+                        assert _f16(half) == u * 4.0 ** e * 2.0 ** -24, (t, lane, p, j)
+    # the two readings of field 5 use the exponent: 0x0400 = 2^-14, 0x0800 = 2^-13
+    assert _f16(0x0400) == 2.0 ** -14 and _f16(0x0800) == 2.0 ** -13
 
 
 # ---------------------------------------------------------------- decode operand
 
-def test_decode_operand_range_and_precision():
+def _operand_case():
     rng = np.random.default_rng(13)
-    xr = (rng.standard_normal((3, 2048)) * np.array([[1e-3], [1.0], [3e4]])).astype(np.float32)
+    xr = (rng.standard_normal((4, 2048)) * np.array([[1e-3], [1.0], [3e4], [2.0]])
+          ).astype(np.float32)
     xr[1, 1024:] = 0.0                                  # an all-zero block
-    vals, inv = O.decode_operand(xr)
+    xr[3, 5] = 900.0                                    # one large value
+    return xr
+
+
+def test_decode_operand_scaling_and_precision():
+    xr = _operand_case()
+    xh, aux = O.decode_operand(xr)
+    k = xr.shape[1]
+    j = (np.arange(k) % 128) // 16
+    e = np.where(j < 6, j, j - 6)
+    fold = aux[::8, 16:20].T                             # [m, block]: 2^(12 - sh)
+    sh = 12 - np.log2(fold.astype(np.float64))
+    assert np.all(sh == np.round(sh))
+    shk = np.repeat(sh, 1024, axis=1) - 2 * e[None, :]
+    # fp16 cast matches torch's (library) round-to-nearest-even cast of the exact product
+    scaled = (xr.astype(np.float64) * 2.0 ** shk).astype(np.float32)
+    ref = torch.from_numpy(scaled).to(torch.float16).numpy()
+    assert np.array_equal(xh.view(np.uint16), ref.view(np.uint16))
+    # undoing the per-step power of four, each nonzero block's largest magnitude
+    # lands in [2^14, 2^15)
+    xs = xh.astype(np.float64) * 4.0 ** e[None, :]
+    bm = np.abs(xs).reshape(4, 2, 1024).max(axis=2)
+    for m in range(4):
+        for b in range(2):
+            if np.abs(xr[m, b * 1024:(b + 1) * 1024]).max() > 0:
+                assert 2 ** 14 <= bm[m, b] < 2 ** 15
+    back = xh.astype(np.float64) * 2.0 ** (-shk)
+    # fp16 relative rounding, plus half the subnormal spacing where xh is subnormal
+    assert np.all(np.abs(back - xr) <= np.abs(xr) * 2.0 ** -11 + 2.0 ** (-25 - shk))
+
+
+def test_decode_operand_group_offsets_exact_sum_and_padding():
+    xr = _operand_case()
+    xh, aux = O.decode_operand(xr)
+    m, k = xr.shape
+    assert aux.shape == (k // 128, 32) and aux.dtype == np.float32
+    assert not aux[:, m:16].any() and not aux[:, 16 + m:].any()
+    j = (np.arange(k) % 128) // 16
+    e = np.where(j < 6, j, j - 6)
+    for mm in range(m):
+        for g in range(k // 128):
+            terms = [Fraction(float(xh[mm, kk])) * Fraction(2) ** int(2 * e[kk] - 24)
+                     for kk in range(128 * g, 128 * g + 128)]
+            exact = sum(terms)
+            bound = sum(abs(t) for t in terms) * Fraction(8, 2 ** 24)
+            assert abs(Fraction(float(aux[g, mm])) - exact) <= bound, (mm, g)
+
+
+def _emulated_gemv(packed, n, k, xh, aux, m):
+    """The decode arithmetic read straight from the packed bytes and the
+    operand, in fp64: y = 2^12 sum_b fold[b] sum_{g in b} s (sum_k A B - X)."""
+    codes, scales = O.unpack_weights(packed, n, k)
+    g_count = k // 128
+    j = (np.arange(k) % 128) // 16
+    e = np.where(j < 6, j, j - 6)
+    a = (codes.astype(np.float64) + 1.0) * 4.0 ** e[None, :] * 2.0 ** -24     # A fragment values
+    y = np.zeros((m, n))
+    for g in range(g_count):
+        cols = slice(128 * g, 128 * g + 128)
+        d = xh[:, cols].astype(np.float64) @ a[:, cols].T - aux[g, :m][:, None].astype(np.float64)
+        y += (d * scales[:, g].astype(np.float64)[None, :]) * aux[g, 16:16 + m][:, None]
+    return y * 2.0 ** 12
+
+
+def test_decode_arithmetic_reproduces_the_layer():
+    """The fields as A fragments, the operand as B, the group offsets and the
+    fold factors together give the exact layer (fp64 emulation of the GEMV's
+    arithmetic, no fp32 rounding) within the fp16 rounding of the operand; a
+    wrong power of four for steps 6 and 7, or a missing offset, does not."""
+    rng = np.random.default_rng(14)
+    n, k, m = 64, 2048, 3
+    codes = rng.integers(-1, 2, (n, k)).astype(np.int8)
+    scales = (0.02 * np.abs(rng.standard_normal((n, k // 128))) + 1e-3).astype(np.float16)
+    x = rng.standard_normal((m, k)).astype(np.float32)
+    exact = O.linear_f64(x, codes, scales)
+    packed = O.pack_weights(codes, scales)
+    xh, aux = O.decode_operand(O.fwht_f32(x))
+    y = _emulated_gemv(packed, n, k, xh, aux, m)
+    assert O.rel_frobenius(y, exact) < 6e-4           # fp16 rounding of the operand: ~2.5e-4
+    bad = aux.copy()
+    bad[:, :m] = 0.0                                 # offsets dropped
+    assert O.rel_frobenius(_emulated_gemv(packed, n, k, xh, bad, m), exact) > 0.5
+    wrong = xh.copy()                                # steps 6, 7 read with 4^6, 4^7
+    cols = ((np.arange(k) % 128) // 16) >= 6
+    wrong[:, cols] = (wrong[:, cols].astype(np.float32) / np.float32(4096)).astype(np.float16)
+    assert O.rel_frobenius(_emulated_gemv(packed, n, k, wrong, aux, m), exact) > 0.1
+
+
+def test_f16_operand_range_and_precision():
+    xr = _operand_case()
+    vals, inv = O.f16_operand(xr)
     # fp16 cast matches torch's (library) round-to-nearest-even cast
     f = (1.0 / inv).astype(np.float32)
-    scaled = (xr.reshape(3, 2, 1024) * f[:, :, None]).reshape(3, 2048).astype(np.float32)
+    scaled = (xr.reshape(4, 2, 1024) * f[:, :, None]).reshape(4, 2048).astype(np.float32)
     ref = torch.from_numpy(scaled).to(torch.float16).numpy()
     assert np.array_equal(vals.view(np.uint16), ref.view(np.uint16))
-    # each nonzero block's largest magnitude lands in [2^14, 2^15)
-    bm = np.abs(vals.astype(np.float32)).reshape(3, 2, 1024).max(axis=2)
-    for m in range(3):
+    bm = np.abs(vals.astype(np.float32)).reshape(4, 2, 1024).max(axis=2)
+    for m in range(4):
         for b in range(2):
             if np.abs(xr[m, b * 1024:(b + 1) * 1024]).max() > 0:
                 assert 2 ** 14 <= bm[m, b] < 2 ** 15
