@@ -190,8 +190,7 @@ class DecodeRunner:
         self.ms = [x.shape[0] for x in xs_host]
         self.x = [x.cuda() for x in xs_host]
         self.xh = [torch.empty((m, self.k), dtype=torch.float16, device="cuda") for m in self.ms]
-        self.xs = [torch.empty((m, self.k // 1024), dtype=torch.float32, device="cuda")
-                   for m in self.ms]
+        self.xs = [B.decode_aux(self.k) for m in self.ms]
         self.y = [torch.empty((m, self.n), dtype=torch.bfloat16, device="cuda") for m in self.ms]
         self.ws = []
         for m in self.ms:
@@ -262,8 +261,8 @@ TRAFFIC_GEMM_I8_GATEUP_M2048 = 380_628_736 + 120_762_112   # gemm_i8_kernel, M =
 
 def _gemv_algorithmic_bytes(m, n, k):
     """Bytes one GEMV launch must move: codes + scales + the fp16 activation
-    operand + per-block factors + bf16 output."""
-    return n * k // 4 + n * (k // 128) * 2 + 2 * m * k + m * (k // 1024) * 4 + m * n * 2
+    operand + its 128-byte group records + bf16 output."""
+    return n * k // 4 + n * (k // 128) * 2 + 2 * m * k + (k // 128) * 128 + m * n * 2
 
 
 def run_decode(args, rank, ws, local):
@@ -399,7 +398,7 @@ def run_prefill(args, local, m=2048):
 
         xh = torch.empty((m, layer.k), dtype=torch.float16, device="cuda")
         xs = torch.empty((m, layer.k // 1024), dtype=torch.float32, device="cuda")
-        B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_DECODE, xh, xs, st)
+        B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_F16, xh, xs, st)
 
         def fp16_only():
             B.tern_gemm_prefill_fp16(xh, xs, w_h, m, layer.n, layer.k, y, wsd, nbd, st)
@@ -572,7 +571,7 @@ def run_decode_configs(args, local, shapes=(I.DOWN, I.QKV), ms=(1, 4, 8, 16)):
             for m in ms:
                 x = _activations(shp, m, seed=120 + m).cuda()
                 xh = torch.empty((m, shp.k), dtype=torch.float16, device="cuda")
-                xs = torch.empty((m, shp.k // 1024), dtype=torch.float32, device="cuda")
+                xs = B.decode_aux(shp.k)
                 y = torch.empty((m, shp.n), dtype=torch.bfloat16, device="cuda")
                 nb = B.tern_workspace_bytes(B.TERN_OP_GEMV, m, shp.n, shp.k)
                 ws = B.Workspace().get(nb)
@@ -642,7 +641,7 @@ def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 8, 16), prefill_ms=(128
         for m in decode_ms:
             xs_in = [_activations(shp, m, seed=900 + si).cuda() for si, shp in enumerate(shapes)]
             xh = [torch.empty((m, shp.k), dtype=torch.float16, device="cuda") for shp in shapes]
-            sc = [torch.empty((m, shp.k // 1024), dtype=torch.float32, device="cuda") for shp in shapes]
+            sc = [B.decode_aux(shp.k) for shp in shapes]
             ys = [torch.empty((m, shp.n), dtype=torch.bfloat16, device="cuda") for shp in shapes]
             wss = [B.Workspace().get(B.tern_workspace_bytes(B.TERN_OP_GEMV, m, shp.n, shp.k))
                    for shp in shapes]

@@ -75,8 +75,8 @@ int tern_version(void);
 /* ------------------------------------------------------------------------
  * Packed weight format (defined by this library; the page does not give one)
  *
- * 2-bit field: high bit = negative, low bit = nonzero.  +1 -> 0b01,
- * -1 -> 0b11, 0 -> 0b00 (0b10 also reads as 0 and is never written).
+ * 2-bit field: u = code + 1 (-1 -> 0b00, 0 -> 0b01, +1 -> 0b10; 0b11 is
+ * never written).
  *
  * Rows are padded with zero codes and zero scales to Np512 = N rounded up to
  * a multiple of 512.  `packed` is a sequence of 17408-byte units, unit
@@ -85,17 +85,19 @@ int tern_version(void);
  *   bytes [0, 16384):      codes, 32 tiles of 16 rows.  Tile t (rows
  *       512 rb + 16 t ..) starts at byte 512 t; slot L (0..31) of the tile,
  *       bytes 512 t + 16 L .. + 15, holds four little-endian 32-bit words
- *       w_0..w_3.  With r = L / 4, c = L % 4, word i and field e (0..7),
- *       jj = e / 4, p = e % 4, j = 2 i + jj:
- *         bits 2e..2e+1 of w_i:      code(row, k),
- *         bits 16+2e..17+2e of w_i:  code(row, k + 1),
+ *       w_0..w_3.  With r = L / 4, c = L % 4, word p and field j (0..7):
+ *         bits 2j..2j+1 of w_p:      u(row, k),
+ *         bits 16+2j..17+2j of w_p:  u(row, k + 1),
  *       with row = 512 rb + 16 t + r + 8 (p % 2),
  *            k   = 128 g + 16 j + 2 c + 8 (p / 2);
  *   bytes [16384, 17408):  fp16 scales: tile t at 16384 + 32 t holds 8 pairs
  *       (s[512 rb + 16 t + r][g], s[512 rb + 16 t + r + 8][g]), r = 0..7.
- * Read as fp16 pairs, (w_i << (14 - 2e)) & 0xC000C000 is
- * (2 code(row, k), 2 code(row, k + 1)) (0x4000 = 2.0, 0xC000 = -2.0): register
- * p of the A fragment of an m16n8k16 tensor-core MMA for k16 step j.
+ * Word p is register p of the A fragment of a 16 x 16 tensor-core tile for
+ * every k16 step j of the group: w_p & (0x00030003 << 2j) for j < 6, and
+ * (w_p >> 12) & (0x00030003 << 2(j - 6)) for j = 6, 7, read as an fp16 pair,
+ * is (u(row, k), u(row, k + 1)) * 4^e * 2^-24 with e = j (j < 6) or j - 6
+ * (a subnormal for e <= 4; the two lowest exponent bits, 2^-14 and 2^-13,
+ * for e = 5): one AND per register.
  * ---------------------------------------------------------------------- */
 
 /* Bytes of `packed` for an N x K weight: ceil(N/512) * (K/128) * 17408. */
@@ -136,25 +138,38 @@ tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, in
  *
  *   x      bf16 [M][K]
  *   mode   TERN_FWHT_F32:    out = float xr[M][K]; out_scale unused (may be NULL)
- *          TERN_FWHT_DECODE: out = fp16 [M][K], the decode operand:
- *                 fp16_rn(xr[m,k] * F[m,b]) with the power of two
- *                 F[m,b] = 2^min(14 - E, 126), E = (biased exponent field
- *                 of the fp32 value max_{k in block b} |xr[m,k]|) - 127,
- *                 i.e. floor(log2(absmax)) for a normal absmax, so the
- *                 block's largest magnitude lands in [2^14, 2^15) and no
- *                 fp16 overflow is possible; out_scale = float [M][B]
- *                 holding 1 / F[m,b] (exact)
+ *          TERN_FWHT_DECODE: the decode GEMV's operand, M <= 16.  With
+ *                 sh[m,b] = min(14 - E, 126), E = (biased exponent field of
+ *                 the fp32 value max_{k in block b} |xr[m,k]|) - 127 (so
+ *                 2^sh puts the block's largest magnitude in [2^14, 2^15))
+ *                 and, for column k in k16 step j = (k % 128) / 16,
+ *                 e = j (j < 6) or j - 6 (the power of four the packed field
+ *                 of that step carries):
+ *                 out = fp16 [M][K], fp16_rn(xr[m,k] * 2^(sh - 2e));
+ *                 out_scale = float aux[G][32], one 128-byte record per
+ *                 128-group g: aux[g][m] = the fp32 sum over k in g of
+ *                 out[m,k] * 2^(2e - 24) (every term exact; the 8
+ *                 consecutive columns 8q .. 8q + 7 left to right, then the
+ *                 16 partial sums by a butterfly p[q] += p[q ^ s],
+ *                 s = 1, 2, 4, 8), aux[g][16 + m] = 2^(12 - sh) of the block
+ *                 holding g; both 0 for m >= M.  The GEMV subtracts aux[g][m]
+ *                 from each tensor-core group sum (the fields hold code + 1)
+ *                 and multiplies each block's sum by aux[g][16 + m]
+ *          TERN_FWHT_F16:    out = fp16 [M][K], the fp16 prefill variant's
+ *                 operand: fp16_rn(xr[m,k] * 2^sh[m,b]); out_scale = float
+ *                 [M][B] holding 2^-sh[m,b] (exact); any M
  *          TERN_FWHT_I8:     out = fp16 [M][K] holding xq in [-127,127];
  *                 out_scale = float tscale[M]:
  *                 a = max_k |xr[m,k]|, tscale = a/127 (fp32),
  *                 xq = clamp(rint(xr / tscale), -127, 127) (fp32 division,
  *                 half to even); a == 0 gives xq = 0 and tscale = 0.
  * Requirements: K % 1024 == 0, K <= 65536 (K <= 32768 in TERN_FWHT_I8 mode),
- * M >= 0; `sign` may be unaligned.
+ * M >= 0 (M <= 16 in TERN_FWHT_DECODE mode); `sign` may be unaligned.
  * ---------------------------------------------------------------------- */
 #define TERN_FWHT_F32 0
 #define TERN_FWHT_DECODE 1
 #define TERN_FWHT_I8 2
+#define TERN_FWHT_F16 3
 tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign,
                             int mode, void* out, float* out_scale, void* stream);
 
@@ -194,7 +209,8 @@ tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_
  *   zeros into xr[:, 1024 blk + 512 .. 1024 blk + 1023].
  * tern_quant_rotated -- quantise rotated fp32 activations xr [M][K]
  *   (K % 1024 == 0) exactly as tern_fwht_quant does after its rotation:
- *   mode TERN_FWHT_DECODE (fp16 + per-block factors) or TERN_FWHT_I8 (xq +
+ *   mode TERN_FWHT_DECODE (the decode GEMV's operand, M <= 16),
+ *   TERN_FWHT_F16 (fp16 + per-block factors) or TERN_FWHT_I8 (xq +
  *   per-token tscale).  After a K split each rank quantises its own padded
  *   shard (per-token int8 scales are the rank's own).
  * ---------------------------------------------------------------------- */
@@ -210,11 +226,15 @@ tern_status tern_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, 
  * tern_gemv_decode -- decode GEMV for 1 <= M <= 16 tokens:
  *     y[m,n] = bf16_rn( sum_g s[n,g] * sum_{k in g} code[n,k] * xr[m,k] )
  * computed from the packed weights and the TERN_FWHT_DECODE operand with fp16
- * tensor-core products (2 code times the fp16 activation, exact) and fp32
- * accumulation.  Every weight byte is read once for all M tokens.
+ * tensor-core products (the field read u * 4^e * 2^-24 times the operand,
+ * exact) and fp32 accumulation; each group's sum starts at minus its offset
+ * (the fields hold code + 1), is scaled by the group's scale, each block's
+ * sum by its fold factor, and the total by 2^12 before the bf16 rounding.
+ * Every weight byte is read once for all M tokens.
  *
  *   packed                  from tern_pack (this layer's N, K)
- *   xh, xs                  from tern_fwht_quant(mode = TERN_FWHT_DECODE)
+ *   xh, xs                  from tern_fwht_quant(mode = TERN_FWHT_DECODE):
+ *                           fp16 [M][K] and the float aux [K/128][32] records
  *   y                       bf16 [M][N]
  *   ws, ws_bytes            workspace of at least
  *                           tern_workspace_bytes(TERN_OP_GEMV, M, N, K) bytes,
@@ -365,15 +385,15 @@ tern_status tern_gemm_prefill_packed(const uint16_t* xq, const float* tscale,
  * On sm_103a the int8 values of section 4 already run on the f16 tensor
  * kind (there is no tcgen05 int8 kind), so an fp16 GEMM costs the same MMA
  * time; it keeps the scales exact instead of rounding them to q, and the
- * activations at the decode operand's precision instead of per-token int8.
+ * activations at fp16 precision (TERN_FWHT_F16) instead of per-token int8.
  *
  * tern_expand_fp16 -- w_h fp16 [N][K] = code[n,k] * s[n, k/128] (exact).
  *   codes int8 [N][K], scales fp16 [N][G].  Requirements: K % 1024 == 0,
  *   K <= 65536, N * K < 2^34.
  * tern_gemm_prefill_fp16 --
  *     y[m,n] = bf16_rn( sum_b xs[m,b] * sum_{k in block b} xh[m,k] w_h[n,k] )
- *   with xh fp16 [M][K] and xs fp32 [M][K/1024] the decode operand of
- *   tern_fwht_quant(TERN_FWHT_DECODE) (any M), each block's sum accumulated
+ *   with xh fp16 [M][K] and xs fp32 [M][K/1024] the fp16 operand of
+ *   tern_fwht_quant(TERN_FWHT_F16) (any M), each block's sum accumulated
  *   in fp32 by the tensor cores and the blocks added in fp32 in order.
  *   y bf16 [M][N].  ws: optional workspace as for tern_gemm_prefill_int8
  *   (TERN_OP_GEMM); a split call adds fp32 slice sums in slice order, so

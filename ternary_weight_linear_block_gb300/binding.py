@@ -33,6 +33,7 @@ TERN_NOALLOC_SCRATCH_BYTES = 24 << 20     # include/tern.h, tern_gemv_decode_noa
 TERN_FWHT_F32 = 0
 TERN_FWHT_DECODE = 1
 TERN_FWHT_I8 = 2
+TERN_FWHT_F16 = 3
 TERN_OP_GEMV = 1
 TERN_OP_GEMM = 2
 TERN_OP_GEMM_PACKED = 3
@@ -283,6 +284,12 @@ def pack_layer(codes: torch.Tensor, scales: torch.Tensor, decode: bool = True,
     return PackedLayer(n, k, packed, q, rs, wq)
 
 
+def decode_aux(k: int, device="cuda") -> torch.Tensor:
+    """The float [K/128][32] group records of the decode operand
+    (TERN_FWHT_DECODE's out_scale)."""
+    return torch.empty((k // 128, 32), dtype=torch.float32, device=device)
+
+
 def fwht(x: torch.Tensor, mode: int, sign: torch.Tensor | None = None, stream=None):
     """Rotation (+ quantisation) of bf16 activations [M,K]; returns (out, out_scale)."""
     _need(x, torch.bfloat16, "x")
@@ -291,6 +298,9 @@ def fwht(x: torch.Tensor, mode: int, sign: torch.Tensor | None = None, stream=No
     if mode == TERN_FWHT_F32:
         out, sc = torch.empty((m, k), dtype=torch.float32, device=dev), None
     elif mode == TERN_FWHT_DECODE:
+        out = torch.empty((m, k), dtype=torch.float16, device=dev)
+        sc = decode_aux(k, dev)
+    elif mode == TERN_FWHT_F16:
         out = torch.empty((m, k), dtype=torch.float16, device=dev)
         sc = torch.empty((m, k // 1024), dtype=torch.float32, device=dev)
     else:
@@ -379,7 +389,7 @@ class _DecodeCall:
             self.x = torch.empty((m, layer.k), dtype=torch.bfloat16, device=device)
             self.y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=device)
         self.xh = torch.empty((m, layer.k), dtype=torch.float16, device=device)
-        self.xs = torch.empty((m, layer.k // 1024), dtype=torch.float32, device=device)
+        self.xs = decode_aux(layer.k, device)
         nb = tern_workspace_bytes(TERN_OP_GEMV, m, layer.n, layer.k)
         self.ws = Workspace(device).get(nb)
 
@@ -480,12 +490,12 @@ def expand_fp16(codes: torch.Tensor, scales: torch.Tensor, stream=None) -> torch
 
 def prefill_fp16(w_h: torch.Tensor, x: torch.Tensor, y: torch.Tensor | None = None, sign=None,
                  stream=None, ws: Workspace | None = None) -> torch.Tensor:
-    """fp16 prefill variant: rotation to the decode operand (fp16 + per-block
+    """fp16 prefill variant: rotation to the fp16 operand (fp16 + per-block
     factors), then one tensor-core GEMM against w_h with the factors applied
     per 1024-block in the epilogue."""
     m = x.shape[0]
     n, k = w_h.shape
-    xh, xs = fwht(x, TERN_FWHT_DECODE, sign, stream)
+    xh, xs = fwht(x, TERN_FWHT_F16, sign, stream)
     if y is None:
         y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
     nb = tern_workspace_bytes(TERN_OP_GEMM, m, n, k)

@@ -17,7 +17,7 @@ namespace {
 
 using namespace fwht;
 
-// Modes F32 and DECODE: one warp per (token, block).
+// Modes F32, F16 and DECODE: one warp per (token, block).
 template <int MODE>
 __global__ void __launch_bounds__(128) fwht_block_kernel(const uint16_t* __restrict__ x, int M,
                                                          int K, const int8_t* __restrict__ sign,
@@ -43,14 +43,16 @@ __global__ void __launch_bounds__(128) fwht_block_kernel(const uint16_t* __restr
       p[0] = make_float4(v[ih][0], v[ih][1], v[ih][2], v[ih][3]);
       p[1] = make_float4(v[ih][4], v[ih][5], v[ih][6], v[ih][7]);
     }
-  } else {
+  } else if (MODE == TERN_FWHT_F16) {
     float f, finv;
-    decode_factor(v, f, finv);
+    f16_factor(v, f, finv);
     __half* o = static_cast<__half*>(out) + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock;
 #pragma unroll
     for (int ih = 0; ih < 4; ++ih)
-      *reinterpret_cast<uint4*>(o + ih * 256 + lane * 8) = decode_pack8(v, ih, f);
+      *reinterpret_cast<uint4*>(o + ih * 256 + lane * 8) = f16_pack8(v, ih, f);
     if (lane == 0) out_scale[static_cast<long>(m) * B + b] = finv;
+  } else {
+    decode_store(v, lane, m, b, M, K, static_cast<__half*>(out), out_scale);
   }
 }
 
@@ -190,11 +192,13 @@ __global__ void __launch_bounds__(256) fwht_combine_kernel(
   reinterpret_cast<float4*>(o + 512)[qd] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// Quantisation of already rotated fp32 activations to the GEMV's decode
-// operand (one warp per (token, block), the scaling of the rotation kernel).
-__global__ void __launch_bounds__(128) quant_decode_kernel(const float* __restrict__ xr, int M,
-                                                           int K, __half* __restrict__ out,
-                                                           float* __restrict__ out_scale) {
+// Already rotated fp32 activations -> the GEMV's decode operand (DECODE) or
+// the fp16 operand (F16), with the rotation kernel's arithmetic; one warp per
+// (token, block).
+template <int MODE>
+__global__ void __launch_bounds__(128) quant_block_kernel(const float* __restrict__ xr, int M,
+                                                          int K, __half* __restrict__ out,
+                                                          float* __restrict__ out_scale) {
   const int lane = threadIdx.x & 31;
   const int B = K / kHBlock;
   const long wid = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -212,12 +216,16 @@ __global__ void __launch_bounds__(128) quant_decode_kernel(const float* __restri
     v[ih][0] = p0.x; v[ih][1] = p0.y; v[ih][2] = p0.z; v[ih][3] = p0.w;
     v[ih][4] = p1.x; v[ih][5] = p1.y; v[ih][6] = p1.z; v[ih][7] = p1.w;
   }
+  if (MODE == TERN_FWHT_DECODE) {
+    decode_store(v, lane, m, b, M, K, out, out_scale);
+    return;
+  }
   float f, finv;
-  decode_factor(v, f, finv);
+  f16_factor(v, f, finv);
   __half* o = out + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock;
 #pragma unroll
   for (int ih = 0; ih < 4; ++ih)
-    *reinterpret_cast<uint4*>(o + ih * 256 + lane * 8) = decode_pack8(v, ih, f);
+    *reinterpret_cast<uint4*>(o + ih * 256 + lane * 8) = f16_pack8(v, ih, f);
   if (lane == 0) out_scale[static_cast<long>(m) * B + b] = finv;
 }
 
@@ -292,9 +300,12 @@ cudaError_t launch_quant_rotated(const float* xr, int64_t M, int64_t K, int mode
     return launch(quant_i8_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, st, xr,
                   static_cast<int>(M), static_cast<int>(K), static_cast<__half*>(out), out_scale);
   const long warps = M * (K / kHBlock);
-  return launch(quant_decode_kernel, dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128), 0,
-                st, xr, static_cast<int>(M), static_cast<int>(K), static_cast<__half*>(out),
-                out_scale);
+  const dim3 grid(static_cast<unsigned>((warps + 3) / 4));
+  if (mode == TERN_FWHT_DECODE)
+    return launch(quant_block_kernel<TERN_FWHT_DECODE>, grid, dim3(128), 0, st, xr,
+                  static_cast<int>(M), static_cast<int>(K), static_cast<__half*>(out), out_scale);
+  return launch(quant_block_kernel<TERN_FWHT_F16>, grid, dim3(128), 0, st, xr,
+                static_cast<int>(M), static_cast<int>(K), static_cast<__half*>(out), out_scale);
 }
 
 cudaError_t launch_fwht(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign, int mode,
@@ -313,6 +324,9 @@ cudaError_t launch_fwht(const uint16_t* x, int64_t M, int64_t K, const int8_t* s
   const dim3 grid(static_cast<unsigned>((warps + 3) / 4));
   if (mode == TERN_FWHT_F32)
     return launch(fwht_block_kernel<TERN_FWHT_F32>, grid, dim3(128), 0, st, x, m, k, sign, out,
+                  out_scale);
+  if (mode == TERN_FWHT_F16)
+    return launch(fwht_block_kernel<TERN_FWHT_F16>, grid, dim3(128), 0, st, x, m, k, sign, out,
                   out_scale);
   return launch(fwht_block_kernel<TERN_FWHT_DECODE>, grid, dim3(128), 0, st, x, m, k, sign, out,
                 out_scale);

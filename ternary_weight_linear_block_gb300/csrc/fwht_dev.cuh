@@ -159,10 +159,11 @@ __device__ __forceinline__ float warp_max(float a) {
 }
 
 
-// Decode operand of one rotated block: the power-of-two factor F with
-// max|xr * F| in [2^14, 2^15) (F = 2^min(14 - E, 126), E the exponent of the
-// block's absmax), returned with its exact inverse; xr * F rounds to fp16.
-__device__ __forceinline__ void decode_factor(const float (&v)[4][8], float& f, float& finv) {
+// fp16 operand of one rotated block (the fp16 prefill variant's operand):
+// the power-of-two factor F with max|xr * F| in [2^14, 2^15)
+// (F = 2^min(14 - E, 126), E the exponent of the block's absmax), returned
+// with its exact inverse; xr * F rounds to fp16.
+__device__ __forceinline__ int block_shift(const float (&v)[4][8]) {
   float amax = 0.f;
 #pragma unroll
   for (int ih = 0; ih < 4; ++ih)
@@ -170,13 +171,19 @@ __device__ __forceinline__ void decode_factor(const float (&v)[4][8], float& f, 
     for (int il = 0; il < 8; ++il) amax = fmaxf(amax, fabsf(v[ih][il]));
   amax = warp_max(amax);
   const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;
-  const int sh = min(14 - e, 126);                 // >= -114, so 2^sh is a normal float
-  f = __uint_as_float(static_cast<uint32_t>(sh + 127) << 23);
-  finv = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+  return min(14 - e, 126);                         // >= -114
+}
+__device__ __forceinline__ float pow2f(int e) {    // 2^e for -126 <= e <= 127
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+__device__ __forceinline__ void f16_factor(const float (&v)[4][8], float& f, float& finv) {
+  const int sh = block_shift(v);
+  f = pow2f(sh);
+  finv = pow2f(-sh);
 }
 
-// fp16 (xr * F) of the 8 elements ih*256 + lane*8 + 0..7, packed as a uint4.
-__device__ __forceinline__ uint4 decode_pack8(const float (&v)[4][8], int ih, float f) {
+// fp16 (xr * f) of the 8 elements ih*256 + lane*8 + 0..7, packed as a uint4.
+__device__ __forceinline__ uint4 f16_pack8(const float (&v)[4][8], int ih, float f) {
   uint32_t w[4];
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
@@ -184,6 +191,79 @@ __device__ __forceinline__ uint4 decode_pack8(const float (&v)[4][8], int ih, fl
     w[t] = *reinterpret_cast<uint32_t*>(&h2);
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---------------------------------------------------------------- decode operand
+// The decode GEMV's operand (include/tern.h, TERN_FWHT_DECODE).  Lane l's 8
+// elements ih*256 + l*8 + 0..7 lie in 128-group 2 ih + l / 16 of the block and
+// in its k16 step j = (l % 16) / 2, whose packed field carries the power of
+// four e(j) = j (j < 6) or j - 6.  The operand is fp16(xr * 2^(sh - 2e)); the
+// group offset is the fp32 sum of fp16 value * 2^(2e - 24): each lane's 8
+// terms left to right, then the 16 lanes of the group by a butterfly
+// (xor 1, 2, 4, 8); the block's fold factor is 2^(12 - sh).
+__device__ __forceinline__ int lane_step_exp(int lane) {
+  const int j = (lane & 15) >> 1;
+  return j < 6 ? j : j - 6;
+}
+
+// The fp16 operand of the lane's 8 elements of register group ih (packed as a
+// uint4) and the lane's partial sum of the group offset.
+__device__ __forceinline__ uint4 decode_pack8(const float (&v)[4][8], int ih, int sh, int e,
+                                              float& part) {
+  const float f = pow2f(sh - 2 * e);               // >= 2^-124: a normal float
+  const float back = pow2f(2 * e - 24);
+  uint32_t w[4];
+  float acc = 0.f;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    __half2 h2 = __floats2half2_rn(__fmul_rn(v[ih][2 * t], f), __fmul_rn(v[ih][2 * t + 1], f));
+    const float2 r = __half22float2(h2);
+    acc = t == 0 ? __fmul_rn(r.x, back) : __fadd_rn(acc, __fmul_rn(r.x, back));
+    acc = __fadd_rn(acc, __fmul_rn(r.y, back));
+    w[t] = *reinterpret_cast<uint32_t*>(&h2);
+  }
+  part = acc;
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The group offset from the lanes' partial sums (every lane of the 16-lane
+// half gets the same value).
+__device__ __forceinline__ float group_offset(float part) {
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) part = __fadd_rn(part, __shfl_xor_sync(kFull, part, o));
+  return part;
+}
+
+// Rotated block (token m, block b) -> the decode operand in global memory:
+// xh [M][K] fp16 and the group records aux [G][32] (offsets of token m at
+// [g][m], the block's fold factor at [g][16 + m]).  The warp of token 0 also
+// writes the zeros of tokens M..15 in the block's 8 records.
+__device__ __forceinline__ void decode_store(const float (&v)[4][8], int lane, int m, int b,
+                                             int M, int K, __half* __restrict__ out,
+                                             float* __restrict__ aux) {
+  const int sh = block_shift(v);
+  const int e = lane_step_exp(lane);
+  __half* o = out + static_cast<long>(m) * K + static_cast<long>(b) * 1024;
+  float* ab = aux + static_cast<long>(b) * 8 * 32;
+#pragma unroll
+  for (int ih = 0; ih < 4; ++ih) {
+    float part;
+    *reinterpret_cast<uint4*>(o + ih * 256 + lane * 8) = decode_pack8(v, ih, sh, e, part);
+    const float x = group_offset(part);
+    if ((lane & 15) == 0) {
+      float* rec = ab + (2 * ih + (lane >> 4)) * 32;
+      rec[m] = x;
+      rec[16 + m] = pow2f(12 - sh);
+    }
+  }
+  if (m == 0)
+    for (int i = lane; i < 8 * 16; i += 32) {
+      const int t = i & 15;
+      if (t >= M) {
+        ab[(i >> 4) * 32 + t] = 0.f;
+        ab[(i >> 4) * 32 + 16 + t] = 0.f;
+      }
+    }
 }
 
 }  // namespace fwht

@@ -478,7 +478,8 @@ __global__ void __launch_bounds__(256)
 // tile's 256 rows into a code ring and TMA-loads the tokens; four expansion
 // warps turn the codes into the exact int8 weight values code * q[n, g],
 // held in fp16 and written in the 128-byte-swizzled K-major layout the MMA
-// reads (the sign trick gives 2 code as fp16, times q/2: both exact).  MMA,
+// reads (a field masked in place reads u * 4^e * 2^-24, u = code + 1; times
+// 2^(15 - 2e), then fma with 512 q and -q, gives code * q; all exact).  MMA,
 // per-1024 chunk int32 conversion and epilogue are those of the kernel above.
 // Warp roles: 0 producer, 1 MMA issuer, 2 TMEM allocator, 3 idle, 4-11
 // epilogue, 12-15 expansion.
@@ -888,12 +889,20 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           c = 0;
           cph ^= 1u;
         }
-        __half2 qh[UPW][2];
+        // code * q from the field u = code + 1 read as u * 4^e * 2^-24 (one
+        // AND): times 2^(15 - 2e) it is u * 2^-9, and fma(u * 2^-9, 512 q, -q)
+        // = (u - 1) q; every step exact in fp16 (512 q <= 65024)
+        uint32_t q512[UPW][2], qneg[UPW][2];
 #pragma unroll
         for (int u = 0; u < UPW; ++u)
 #pragma unroll
-          for (int par = 0; par < 2; ++par)
-            qh[u][par] = __half2half2(__float2half_rn(0.5f * static_cast<float>(qv[u][par])));
+          for (int par = 0; par < 2; ++par) {
+            __half2 a2 = __half2half2(__float2half_rn(512.0f * static_cast<float>(qv[u][par])));
+            __half2 b2 = __half2half2(__float2half_rn(-static_cast<float>(qv[u][par])));
+            q512[u][par] = *reinterpret_cast<uint32_t*>(&a2);
+            qneg[u][par] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+#pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_EXPAND);
@@ -901,21 +910,24 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             break;
           }
           const uint32_t base = smem_base + s * PSTAGE_BYTES + row_off;
+          // this stage holds k16 steps j = 4h .. 4h + 3 of the group; word p is
+          // register p (row parity p % 2, 8-column half p / 2)
 #pragma unroll
-          for (int ii = 0; ii < 2; ++ii) {
-            // words 2h + ii hold k16 steps 4h + 2ii and 4h + 2ii + 1 of the group
+          for (int jl = 0; jl < 4; ++jl) {
+            const int j = 4 * h + jl;
+            const int e = j < 6 ? j : j - 6;
+            const uint32_t mask = 0x00030003u << (2 * e);
+            const uint32_t mul = 0x00010001u * static_cast<uint32_t>((30 - 2 * e) << 10);   // 2^(15-2e)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int chunk = 4 * ii + 2 * (e >> 2) + ((e >> 1) & 1);
-              const int par = e & 1;
+            for (int p = 0; p < 4; ++p) {
+              const int chunk = 2 * jl + (p >> 1);
+              const int par = p & 1;
 #pragma unroll
               for (int u = 0; u < UPW; ++u) {
-                const uint32_t w =
-                    h == 0 ? (ii == 0 ? wv[u].x : wv[u].y) : (ii == 0 ? wv[u].z : wv[u].w);
-                const uint32_t two_code = (w << (14 - 2 * e)) & 0xC000C000u;
-                __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&two_code), qh[u][par]);
-                ptx::st_shared_b32(base + xo[chunk] + 8192u * u + 1024u * par,
-                                   *reinterpret_cast<uint32_t*>(&v));
+                const uint32_t w4[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+                const uint32_t f = (j < 6 ? w4[p] : w4[p] >> 12) & mask;
+                const uint32_t v = ptx::fma_f16x2(ptx::mul_f16x2(f, mul), q512[u][par], qneg[u][par]);
+                ptx::st_shared_b32(base + xo[chunk] + 8192u * u + 1024u * par, v);
               }
             }
           }

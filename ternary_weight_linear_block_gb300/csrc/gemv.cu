@@ -5,7 +5,8 @@
 // stored at 2 bits, one fp16 scale per 128 elements of a row, xr the
 // block-Hadamard-rotated activation.  Section 5 records that an int8 (dp4a)
 // decode kernel added error for a 2% end-to-end gain; here the activations
-// stay in fp16 (per-block power-of-two scaled, see tern_fwht_quant).
+// stay in fp16 (a power of two per block and per k16 step, see
+// tern_fwht_quant).
 //
 // GB300 design.  The layer is one stream of weight bytes; everything else is
 // arranged so that stream runs at HBM speed with few instructions per byte:
@@ -13,20 +14,24 @@
 //   1024 bytes of scales, contiguous in the packed format, fetched by one
 //   bulk copy (L2 evict-first) into a 4-stage shared-memory ring; the
 //   activation tile of the group (16 token rows x 128 k, fp16) arrives by
-//   TMA (128-byte swizzle) into the same stage; token rows >= M are
+//   TMA (128-byte swizzle) into the same stage, with the group's 128-byte
+//   record (token offsets, block fold factors); token rows >= M are
 //   zero-filled by TMA and cost no memory traffic.
-// * 2 code is exact in fp16 and the packed format places each pair of
-//   2-bit fields so that a shift and an and give the fp16 pair
-//   (2 code(k), 2 code(k+1)): 16 codes become two m16n8k16 A fragments.
+// * each 32-bit word of the packed format is one register of an m16n8k16 A
+//   fragment for all 8 k16 steps of the group: one AND (after a shift by 12
+//   for steps 6 and 7) gives the fp16 pair u * 4^e * 2^-24, u = code + 1 (a
+//   subnormal, or the two lowest exponent bits), exactly; the operand carries
+//   4^-e, and each group's accumulator starts at minus the tokens' offset
+//   (the group sum of what u = 1 would give), which leaves sum code * x.
 //   Tokens are the n side of the MMA (one n8 tile for M <= 8, two for
 //   M <= 16), so every weight byte is read once for all M tokens.
 //   (On sm_103a the legacy fp8 mma.sync issues four FMA-pipe instructions
 //   per MMA and tcgen05 costs ~100 cycles per MMA even at N = 16, so the
 //   fp16 mma.sync pipe is the fastest tensor path at this shape.)
 // * sixteen consumer warps each own 32 rows (2 tiles) of a unit: B fragments
-//   come from ldmatrix, A fragments from the unpacked words; per group the
-//   fresh fp32 accumulators are scaled by the row's group scale, and per
-//   1024-block by the block's power-of-two activation factor.
+//   come from ldmatrix, A fragments from the masked words; per group the
+//   fp32 accumulators are scaled by the row's group scale, per 1024-block by
+//   the block's fold factor, and the result by 2^12 before the bf16 rounding.
 // * units are cut into equal contiguous ranges, one per persistent CTA
 //   (stream-K).  A 512-row block finished by one CTA is written directly.  A
 //   block shared by at most 4 CTAs at M <= 8 is summed by its first owner,
@@ -64,7 +69,12 @@ constexpr int TILES = RB / 16;
 constexpr int UNIT_CODE_BYTES = RB * 32;        // 512 rows x 128 codes x 2 bits
 constexpr int UNIT_BYTES = UNIT_CODE_BYTES + TILES * 32;
 constexpr int XTILE_BYTES = 16 * kGroup * 2;    // 16 token rows x 128 k, fp16 (two 64-k boxes)
+constexpr int AUX_BYTES = 128;                  // the group's record: 16 offsets, 16 fold factors
+constexpr int AUX_OFF = XTILE_BYTES + UNIT_BYTES;
+constexpr int STAGE_TX = XTILE_BYTES + UNIT_BYTES + AUX_BYTES;
 constexpr int STAGE_BYTES = 24576;
+// The decode operand's fold factors are 2^(12 - sh): the sums carry 2^-12.
+constexpr float OUT_SCALE = 4096.f;
 // Ring depth: measured on gate/up, down, qkv and o at M = 1-16, four stages
 // beat three, five to nine (eight: 16.60 -> 16.41 us per gate/up launch at
 // M = 4, down 12.61 -> 11.65 us at M = 1).
@@ -92,7 +102,8 @@ constexpr uint32_t WAIT_LIMIT = 1u << 18;
 constexpr uint32_t TAG_TRIES = 1u << 16;
 constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
 
-static_assert(XTILE_BYTES + UNIT_BYTES <= STAGE_BYTES, "stage too small");
+static_assert(STAGE_TX <= STAGE_BYTES, "stage too small");
+static_assert(AUX_OFF % 16 == 0, "bulk copy alignment");
 static_assert(STAGE_BYTES % 1024 == 0 && XTILE_BYTES % 16 == 0, "stage alignment");
 
 enum : unsigned int { ERR_PRODUCER = 1u, ERR_CONSUMER = 2u, ERR_DRAIN = 4u, ERR_REDUCE = 8u };
@@ -132,6 +143,17 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// The first MMA of a group: the accumulator starts at (c0, c1, c0, c1), the
+// two tokens' negated group offsets (every row of the tile shares them).
+__device__ __forceinline__ void mma_f16_init(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1, float c0,
+                                             float c1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%10,%11};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
 
 
 __device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned long long v) {
@@ -169,7 +191,8 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
       const int row = rb * RB + 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
       const int tok = 8 * nt + 2 * cq + (i & 1);
       if (row < N && tok < M)
-        y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(acc[tt][nt][i]);
+        y[static_cast<long>(tok) * N + row] =
+            __float2bfloat16_rn(__fmul_rn(acc[tt][nt][i], OUT_SCALE));
     }
     return;
   }
@@ -258,12 +281,13 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
     const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
     const int row = rb * RB + 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
     const int tok = 8 * nt + 2 * cq + (i & 1);
-    if (row < N && tok < M) y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum[v]);
+    if (row < N && tok < M)
+      y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(__fmul_rn(sum[v], OUT_SCALE));
   }
 }
 
-// Fixup after the GEMV: y[tok][row] = bf16(sum of the slots of the row's
-// block, in slot order) for every row of a block shared by more than
+// Fixup after the GEMV: y[tok][row] = bf16(2^12 x the sum of the slots of
+// the row's block, in slot order) for every row of a block shared by more than
 // tag_slots CTAs.
 // One thread per (block, token, row), consecutive threads on consecutive rows
 // (coalesced); the slot loads of a thread are independent.  The reduction is
@@ -295,37 +319,48 @@ __global__ void __launch_bounds__(FIX_THREADS)
     sum += __uint_as_float(static_cast<unsigned int>(a3));
   }
   for (; sl < nslots; ++sl) sum += __uint_as_float(static_cast<unsigned int>(__ldcg(p + sl * stride)));
-  y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(sum);
+  y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(__fmul_rn(sum, OUT_SCALE));
 }
 
-// The MMAs of one unit for this warp's tiles: codes cv, scale pairs sp and the
-// B fragments bf of the group's 8 k16 steps; the group sums, scaled by the
-// rows' group scales, are added to bacc.
+// The MMAs of one unit for this warp's tiles: codes cv, scale pairs sp, the B
+// fragments bf of the group's 8 k16 steps and the tokens' negated group
+// offsets xo; the group sums, scaled by the rows' group scales, are added to
+// bacc.  Word p of a tile's slot is A-fragment register p for every step j:
+// one AND per register (steps 6 and 7 from the word shifted right by 12)
+// gives the fp16 pair u * 4^e * 2^-24, u = code + 1; the operand carries
+// 4^-e, and each group's accumulator starts at minus the tokens' offset,
+// which removes the "+1" of u.
 template <int NT>
 __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t (&sp)[TPW],
                                           const uint32_t (&bf)[NT][8][2],
-                                          float (&bacc)[TPW][NT][4]) {
+                                          const float (&xo)[NT][2], float (&bacc)[TPW][NT][4]) {
   float d[TPW][NT][4];
+  uint32_t hi[TPW][4];
 #pragma unroll
-  for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) d[tt][nt][q] = 0.f;
+  for (int tt = 0; tt < TPW; ++tt) {
+    hi[tt][0] = cv[tt].x >> 12;
+    hi[tt][1] = cv[tt].y >> 12;
+    hi[tt][2] = cv[tt].z >> 12;
+    hi[tt][3] = cv[tt].w >> 12;
+  }
   // k16 steps outer, tiles inner: the tiles' MMA chains alternate
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
+    const uint32_t mask = 0x00030003u << (2 * (j < 6 ? j : j - 6));
 #pragma unroll
     for (int tt = 0; tt < TPW; ++tt) {
       const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
-      const uint32_t w = w4[j >> 1];
-      const int e0 = (j & 1) * 4;
       uint32_t a[4];
 #pragma unroll
-      for (int p = 0; p < 4; ++p) a[p] = (w << (14 - 2 * (e0 + p))) & 0xC000C000u;
+      for (int p = 0; p < 4; ++p) a[p] = (j < 6 ? w4[p] : hi[tt][p]) & mask;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        mma_f16(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
+      for (int nt = 0; nt < NT; ++nt) {
+        if (j == 0)
+          mma_f16_init(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][0][0], bf[nt][0][1], xo[nt][0],
+                       xo[nt][1]);
+        else
+          mma_f16(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
+      }
     }
   }
 #pragma unroll
@@ -342,8 +377,8 @@ __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t
   }
 }
 
-// End of a 1024-block: acc += bacc * f (f the block's activation factor of
-// the thread's two tokens per n8 tile, times 1/2 for the 2 code reading).
+// End of a 1024-block: acc += bacc * f (f the block's fold factor of the
+// thread's two tokens per n8 tile).
 template <int NT>
 __device__ __forceinline__ void fold_block(float (&acc)[TPW][NT][4], float (&bacc)[TPW][NT][4],
                                            const float (&f)[NT][2]) {
@@ -361,7 +396,7 @@ __device__ __forceinline__ void fold_block(float (&acc)[TPW][NT][4], float (&bac
 template <int NT>
 __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t* __restrict__ packed,
-                const float* __restrict__ xs, int M, int N, int K, __nv_bfloat16* __restrict__ y,
+                const float* __restrict__ aux, int M, int N, int K, __nv_bfloat16* __restrict__ y,
                 unsigned long long* __restrict__ partials, int U, int S) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -373,7 +408,6 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = K / kGroup;
-  const int B = K / kHBlock;
   const int C = gridDim.x;
   const int u0 = static_cast<int>(unit_begin(blockIdx.x, U, C));
   const int u1 = static_cast<int>(unit_begin(blockIdx.x + 1, U, C));
@@ -406,19 +440,20 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
     if (producer) {
       ptx::prefetch_tmap(&tmX);
       for (int i = 0; i < pre; ++i) {
-        ptx::mbar_arrive_expect_tx(&full[i], UNIT_BYTES + XTILE_BYTES);
+        ptx::mbar_arrive_expect_tx(&full[i], STAGE_TX);
         ptx::bulk_load_hint(smem + i * STAGE_BYTES + XTILE_BYTES,
                             packed + static_cast<size_t>(u0 + i) * UNIT_BYTES, UNIT_BYTES,
                             &full[i], pol);
       }
     }
-    pdl_wait();   // activations and xs come from the previous kernel
+    pdl_wait();   // activations and their group records come from the previous kernel
     if (producer) {
       for (int i = 0; i < pre; ++i) {
         const int gi = (u0 + i) % G;
         uint8_t* st = smem + i * STAGE_BYTES;
         ptx::tma_load_2d(st, &tmX, &full[i], gi * kGroup, 0);
         ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[i], gi * kGroup + 64, 0);
+        ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(gi) * 32, AUX_BYTES, &full[i]);
       }
       issued = pre;
     }
@@ -434,11 +469,12 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
     }
     uint8_t* st = smem + s * STAGE_BYTES;
     const int gj = (u0 + j) % G;
-    ptx::mbar_arrive_expect_tx(&full[s], UNIT_BYTES + XTILE_BYTES);
+    ptx::mbar_arrive_expect_tx(&full[s], STAGE_TX);
     ptx::bulk_load_hint(st + XTILE_BYTES, packed + static_cast<size_t>(u0 + j) * UNIT_BYTES,
                         UNIT_BYTES, &full[s], pol);
     ptx::tma_load_2d(st, &tmX, &full[s], gj * kGroup, 0);
     ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[s], gj * kGroup + 64, 0);
+    ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(gj) * 32, AUX_BYTES, &full[s]);
     ++issued;
   };
 
@@ -447,7 +483,7 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
     if (lane == 0) {
       ptx::prefetch_tmap(&tmX);
       for (int i = 0; i < pre; ++i) {
-        ptx::mbar_arrive_expect_tx(&full[i], UNIT_BYTES + XTILE_BYTES);
+        ptx::mbar_arrive_expect_tx(&full[i], STAGE_TX);
         ptx::bulk_load_hint(smem + i * STAGE_BYTES + XTILE_BYTES,
                             packed + static_cast<size_t>(u0 + i) * UNIT_BYTES, UNIT_BYTES, &full[i],
                             pol);
@@ -466,13 +502,14 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[s], UNIT_BYTES + XTILE_BYTES);
+          ptx::mbar_arrive_expect_tx(&full[s], STAGE_TX);
           ptx::bulk_load_hint(st + XTILE_BYTES, packed + static_cast<size_t>(u0 + i) * UNIT_BYTES,
                               UNIT_BYTES, &full[s], pol);
           ++issued;
         }
         ptx::tma_load_2d(st, &tmX, &full[s], g * kGroup, 0);
         ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[s], g * kGroup + 64, 0);
+        ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(g) * 32, AUX_BYTES, &full[s]);
         if (++g == G) g = 0;
       }
       if (!ok) {
@@ -489,7 +526,7 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
     // ------------------------------------------------ consumers
     const int cw = MERGED ? warp : warp - 1;   // owns tiles TPW*cw .. TPW*cw + TPW-1 of each unit
     const int gq = lane >> 2, cq = lane & 3;
-    if constexpr (!MERGED) pdl_wait();   // xs is written by the previous kernel; y / ws may still be read by it
+    if constexpr (!MERGED) pdl_wait();   // y / ws may still be read by the previous kernel
 
     // Per-lane shared-memory offsets, fixed for the whole kernel.  ldmatrix
     // matrix mi = lane / 8 covers (k16 step j0 + mi / 2, 8-wide k half mi % 2),
@@ -546,6 +583,19 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
           sp[tt] = *reinterpret_cast<const uint32_t*>(unit + UNIT_CODE_BYTES + 32 * (TPW * cw + tt) +
                                                       4 * gq);
         }
+        // the group record: offsets of tokens 8 nt + 2 cq + {0,1} (negated:
+        // the accumulators start there) and the block's fold factors
+        float xo[NT][2], fo[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float2 o2 = *reinterpret_cast<const float2*>(st + AUX_OFF + 4 * (8 * nt + 2 * cq));
+          const float2 f2 =
+              *reinterpret_cast<const float2*>(st + AUX_OFF + 64 + 4 * (8 * nt + 2 * cq));
+          xo[nt][0] = -o2.x;
+          xo[nt][1] = -o2.y;
+          fo[nt][0] = f2.x;
+          fo[nt][1] = f2.y;
+        }
         // B fragments: bf[nt][j][0..1] for the 8 k16 steps of the group
         uint32_t bf[NT][8][2];
         const uint32_t xb = smem_base + s * STAGE_BYTES;
@@ -557,20 +607,8 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
                         bf[nt][2 * q + 1][1]);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[s]);
-        unit_math<NT>(cv, sp, bf, bacc);
-        if ((g & 7) == 7 || i + 1 == i_end) {
-          const int blk = g >> 3;
-          float f[NT][2];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int tok = 8 * nt + 2 * cq + h;
-              // 1/2 undoes the 2*code reading of the weights
-              f[nt][h] = tok < M ? 0.5f * __ldg(xs + static_cast<long>(tok) * B + blk) : 0.f;
-            }
-          fold_block<NT>(acc, bacc, f);
-        }
+        unit_math<NT>(cv, sp, bf, xo, bacc);
+        if ((g & 7) == 7 || i + 1 == i_end) fold_block<NT>(acc, bacc, fo);
         ++g;
       }
       if (!alive) break;
@@ -611,14 +649,17 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
 // tern_fwht_quant(TERN_FWHT_DECODE) followed by tern_gemv_decode.
 constexpr int LSTAGES = 8;
 constexpr int LX_BYTES = 80 * 1024;             // resident decode operand (a chunk of groups)
-constexpr int LXS_FLOATS = 16 * 64;             // block factors of 16 tokens x 64 blocks
+constexpr int LXS_FLOATS = 16 * 64;             // fold factors of 16 tokens x 64 blocks
+constexpr int LCHUNK_MAX = 64;                  // groups of one chunk at most
+constexpr int LXO_FLOATS = LCHUNK_MAX * 16;     // group offsets of the chunk's groups x 16 tokens
 constexpr size_t LSMEM_BYTES = static_cast<size_t>(LSTAGES) * UNIT_BYTES + LX_BYTES +
-                               LXS_FLOATS * 4 + 1024 + 256;
+                               (LXS_FLOATS + LXO_FLOATS) * 4 + 1024 + 256;
 static_assert(LSMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 // Groups of one chunk: each 256 bytes per token row.
 __host__ __device__ inline int chunk_groups(int M, int G) {
-  const int cu = (LX_BYTES / M - 16) / 256;
+  int cu = (LX_BYTES / M - 16) / 256;
+  if (cu > LCHUNK_MAX) cu = LCHUNK_MAX;
   return cu < G ? cu : G;
 }
 
@@ -633,7 +674,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* xreg = smem + LSTAGES * UNIT_BYTES;
   float* xs_s = reinterpret_cast<float*>(xreg + LX_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(xs_s + LXS_FLOATS);
+  float* xo_s = xs_s + LXS_FLOATS;
+  uint64_t* full = reinterpret_cast<uint64_t*>(xo_s + LXO_FLOATS);
   uint64_t* empty = full + LSTAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + LSTAGES);
 
@@ -711,8 +753,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t x_base = ptx::smem_u32(xreg);
 
     // Rotate the 1024-blocks holding the groups gs .. gs + ng - 1 (mod G) and
-    // store those groups' decode operand at positions 0 .. ng - 1, and the
-    // blocks' factors (x 1/2 for the 2 code reading) in xs_s[token][block].
+    // store those groups' decode operand at positions 0 .. ng - 1, their
+    // offsets in xo_s[position][token] and the blocks' fold factors in
+    // xs_s[token][block] (the arithmetic of the rotation kernel).
     auto build = [&](int gs, int ng) {
       for (int t = cw; t < M * B; t += CONSUMERS) {
         const int m = t / B, b = t - m * B;
@@ -725,18 +768,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fwht::load_block(x + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock,
                          sign ? sign + static_cast<long>(b) * kHBlock : nullptr, lane, v);
         fwht::fwht_1024(v, lane);
-        float f, finv;
-        fwht::decode_factor(v, f, finv);
+        const int sh = fwht::block_shift(v);
+        const int e = fwht::lane_step_exp(lane);
 #pragma unroll
         for (int ih = 0; ih < 4; ++ih) {
           // lanes 0-15 hold group 2 ih of the block, lanes 16-31 group 2 ih + 1
           const int gg = 8 * b + 2 * ih + (lane >> 4);
           const int pos = (gg - gs + G) % G;
-          const uint4 w = fwht::decode_pack8(v, ih, f);
-          if (pos < ng)
+          float part;
+          const uint4 w = fwht::decode_pack8(v, ih, sh, e, part);
+          const float xoff = fwht::group_offset(part);
+          if (pos < ng) {
             *reinterpret_cast<uint4*>(xreg + m * pitch + pos * 256 + (lane & 15) * 16) = w;
+            if ((lane & 15) == 0) xo_s[pos * 16 + m] = xoff;
+          }
         }
-        if (lane == 0) xs_s[m * 64 + b] = 0.5f * finv;
+        if (lane == 0) xs_s[m * 64 + b] = fwht::pow2f(12 - sh);
       }
     };
 
@@ -783,6 +830,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t bf[NT][8][2];
         const int pos = g >= gs ? g - gs : g + G - gs;
         const uint32_t xb = x_base + pos * 256;
+        float xo[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int tok = 8 * nt + 2 * cq + h;
+            xo[nt][h] = tok < M ? -xo_s[pos * 16 + tok] : 0.f;
+          }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -791,7 +846,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         bf[nt][2 * q + 1][0], bf[nt][2 * q + 1][1]);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[s]);
-        unit_math<NT>(cv, sp, bf, bacc);
+        unit_math<NT>(cv, sp, bf, xo, bacc);
         if ((g & 7) == 7 || i + 1 == n_units) {
           const int blk = g >> 3;
           float f[NT][2];

@@ -16,8 +16,9 @@
 namespace tern {
 namespace {
 
+// The 2-bit field of a code: u = code + 1 (-1 -> 0, 0 -> 1, +1 -> 2).
 __device__ __forceinline__ uint32_t field_of(int8_t c) {
-  return c == 1 ? 1u : (c == -1 ? 3u : 0u);
+  return static_cast<uint32_t>(static_cast<int>(c) + 1) & 3u;
 }
 
 constexpr int kUnitRows = 512;
@@ -43,18 +44,17 @@ __global__ void pack_units_kernel(const int8_t* __restrict__ codes,
     const int g = static_cast<int>(unit % G);
     uint32_t out = 0;
     if (w < 4096) {
-      // tile t, slot L = 4 r + c, word i
-      const int t = w >> 7, lane = (w >> 2) & 31, i = w & 3;
+      // tile t, slot L = 4 r + c, word p (register p of the tile's A fragment)
+      const int t = w >> 7, lane = (w >> 2) & 31, p = w & 3;
       const int r = lane >> 2, c = lane & 3;
+      const long row = rb * kUnitRows + 16 * t + r + 8 * (p & 1);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int jj = e >> 2, p = e & 3;
-        const long row = rb * kUnitRows + 16 * t + r + 8 * (p & 1);
-        if (row >= N) continue;
-        const int k = kGroup * g + 16 * (2 * i + jj) + 2 * c + 8 * (p >> 1);
-        const int8_t* src = codes + row * K + k;
-        out |= field_of(src[0]) << (2 * e);
-        out |= field_of(src[1]) << (16 + 2 * e);
+      for (int j = 0; j < 8; ++j) {
+        // field j: k16 step j; rows past N hold zero codes (u = 1)
+        const int k = kGroup * g + 16 * j + 2 * c + 8 * (p >> 1);
+        const uint32_t u0 = row < N ? field_of(codes[row * K + k]) : 1u;
+        const uint32_t u1 = row < N ? field_of(codes[row * K + k + 1]) : 1u;
+        out |= (u0 << (2 * j)) | (u1 << (16 + 2 * j));
       }
     } else {
       const int j = w - 4096;          // tile t = j / 8, pair gq = j % 8

@@ -132,10 +132,12 @@ tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, in
 tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign,
                             int mode, void* out, float* out_scale, void* stream) {
   if (M < 0 || K < 0) return TERN_ERR_INVALID_ARG;
-  if (mode != TERN_FWHT_F32 && mode != TERN_FWHT_DECODE && mode != TERN_FWHT_I8)
+  if (mode != TERN_FWHT_F32 && mode != TERN_FWHT_DECODE && mode != TERN_FWHT_I8 &&
+      mode != TERN_FWHT_F16)
     return TERN_ERR_INVALID_ARG;
   if (!k_ok(K, mode == TERN_FWHT_I8 ? 32768 : kMaxK)) return TERN_ERR_SHAPE;
   if (M > (int64_t(1) << 31) / K) return TERN_ERR_SHAPE;
+  if (mode == TERN_FWHT_DECODE && M > 16) return TERN_ERR_SHAPE;
   if (M == 0) return TERN_OK;
   if (x == nullptr || out == nullptr) return TERN_ERR_INVALID_ARG;
   if (mode != TERN_FWHT_F32 && out_scale == nullptr) return TERN_ERR_INVALID_ARG;
@@ -183,9 +185,11 @@ tern_status tern_fwht_combine(const float* h_first, const float* h_second, int64
 tern_status tern_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, void* out,
                                float* out_scale, void* stream) {
   if (M < 0 || K < 0) return TERN_ERR_INVALID_ARG;
-  if (mode != TERN_FWHT_DECODE && mode != TERN_FWHT_I8) return TERN_ERR_INVALID_ARG;
+  if (mode != TERN_FWHT_DECODE && mode != TERN_FWHT_I8 && mode != TERN_FWHT_F16)
+    return TERN_ERR_INVALID_ARG;
   if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
   if (M > (int64_t(1) << 31) / K) return TERN_ERR_SHAPE;
+  if (mode == TERN_FWHT_DECODE && M > 16) return TERN_ERR_SHAPE;
   if (M == 0) return TERN_OK;
   if (xr == nullptr || out == nullptr || out_scale == nullptr) return TERN_ERR_INVALID_ARG;
   if (!aligned16(xr) || !aligned16(out) || !aligned16(out_scale)) return TERN_ERR_ALIGN;

@@ -151,7 +151,7 @@ class GpuOps:
     def decode(self, lin: KSplitLinear, xr: torch.Tensor, ws: B.Workspace) -> torch.Tensor:
         m, kp = xr.shape
         xh = torch.empty((m, kp), dtype=torch.float16, device=xr.device)
-        xs = torch.empty((m, kp // HBLOCK), dtype=torch.float32, device=xr.device)
+        xs = B.decode_aux(kp, xr.device)
         B.tern_quant_rotated(xr, m, kp, B.TERN_FWHT_DECODE, xh, xs)
         y = torch.empty((m, lin.n), dtype=torch.bfloat16, device=xr.device)
         nb = B.tern_workspace_bytes(B.TERN_OP_GEMV, m, lin.n, kp)

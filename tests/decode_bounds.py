@@ -6,6 +6,7 @@ wrong 512-row block, a mis-scaled group, a lost partial sum), so the decode
 tests also bound every compared element on its own:
 
     |y[m,n] - yref[m,n]| <= 2^-7 |yref[m,n]| + 2^-7 ||W[n,:] * xr[m,:]||_2
+                            + 2^-18 sum_k |s[n,k/128] xr[m,k]|
 
 with W[n,k] = code[n,k] s[n,k/128], xr the exact rotated activation and
 W[n,:] * xr[m,:] the element-wise product.
@@ -17,8 +18,13 @@ power-of-two scaling: an error of at most 2^-11 |xr[m,k]| per element, zero
 mean and independent across k, so their weighted sum has a standard deviation
 of at most 2^-11 / sqrt(3) ||W[n] * xr[m]||; the second term is 27 of those
 standard deviations (the worst case, all errors aligned, is the
-Cauchy-Schwarz 2^-11 ||W[n]|| ||xr[m]||, far looser).  fp32 accumulation adds
-orders of magnitude less.  A dropped, doubled or mis-scaled 128-group of a
+Cauchy-Schwarz 2^-11 ||W[n]|| ||xr[m]||, far looser).  The packed fields hold
+code + 1, so each group's tensor-core sum carries the sum of the activations
+it multiplies, which the group offset (summed in fp32 by the rotation)
+removes; the two sums round differently, by at most a few dozen fp32 ulps of
+sum_{k in g} |xr[m,k]| per group, scaled by s[n,g]: the third term (64 ulps of
+2^-24).  It is what remains for a row of zero codes, and for random weights it
+is a few percent of the second term.  fp32 accumulation adds less.  A dropped, doubled or mis-scaled 128-group of a
 row moves y[m,n] by about ||W[n,g] * xr[m,g]||, which for the workload widths
 (K <= 17408, 40 to 136 groups) is 10 to 25 times the second term, so such a
 slip fails the bound wherever it lands.
@@ -41,7 +47,9 @@ def check_elementwise(y, yref, codes, scales, x, sign=None, what=""):
     xr = O.rotate_f64(x, sign)
     w = O.dequant_f64(codes, scales)
     prod_norm = np.sqrt((xr * xr) @ (w * w).T)                 # [M][R]
-    bound = 2.0 ** -7 * np.abs(yref) + 2.0 ** -7 * prod_norm
+    s_abs = np.repeat(np.abs(np.asarray(scales, np.float64)), 128, axis=1)   # [R][K]
+    offset_term = np.abs(xr) @ s_abs.T                           # [M][R]
+    bound = 2.0 ** -7 * np.abs(yref) + 2.0 ** -7 * prod_norm + 2.0 ** -18 * offset_term
     err = np.abs(y - yref)
     bad = ~(err <= bound)
     if bad.any():

@@ -98,6 +98,10 @@ def test_fwht_argument_errors(lib):
     assert _st("tern_fwht_quant", None, 4, 1024, None, 0, FAKE, None, None) == 1
     assert _st("tern_fwht_quant", FAKE, 0, 1024, None, 0, FAKE, None, None) == 0
     assert _st("tern_fwht_quant", FAKE, -3, 1024, None, 0, FAKE, None, None) == 1
+    assert _st("tern_fwht_quant", FAKE, 17, 1024, None, 1, FAKE, FAKE, None) == 2  # decode: M <= 16
+    assert _st("tern_fwht_quant", FAKE, 4, 1024, None, 3, FAKE, None, None) == 1   # fp16: no scale out
+    assert _st("tern_quant_rotated", FAKE, 17, 1024, 1, FAKE, FAKE, None) == 2
+    assert _st("tern_quant_rotated", FAKE, 4, 1024, 0, FAKE, FAKE, None) == 1      # no f32 mode
 
 
 def test_gemv_argument_errors(lib):
@@ -283,6 +287,6 @@ def test_binding_constants_match_the_header():
         m = re.search(r"\b%s = (\d+)" % name, text)
         assert m and int(m.group(1)) == getattr(B, name), name
     for name in ("TERN_OP_GEMV", "TERN_OP_GEMM", "TERN_OP_GEMM_PACKED", "TERN_FWHT_F32",
-                 "TERN_FWHT_DECODE", "TERN_FWHT_I8"):
+                 "TERN_FWHT_DECODE", "TERN_FWHT_I8", "TERN_FWHT_F16"):
         m = re.search(r"#define %s (\d+)" % name, text)
         assert m and int(m.group(1)) == getattr(B, name), name

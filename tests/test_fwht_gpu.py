@@ -28,6 +28,9 @@ def _run(xd, m, k, mode, sign=None):
         out, sc = poison(torch.empty((m, k), dtype=torch.float32, device=dev)), None
     elif mode == B.TERN_FWHT_DECODE:
         out = poison(torch.empty((m, k), dtype=torch.float16, device=dev))
+        sc = poison(B.decode_aux(k, dev))
+    elif mode == B.TERN_FWHT_F16:
+        out = poison(torch.empty((m, k), dtype=torch.float16, device=dev))
         sc = poison(torch.empty((m, k // 1024), dtype=torch.float32, device=dev))
     else:
         out = poison(torch.empty((m, k), dtype=torch.float16, device=dev))
@@ -48,11 +51,31 @@ def test_fwht_f32_bitwise(m, k, frac, mult):
 
 @pytest.mark.parametrize("m,k,frac,mult", CASES)
 def test_fwht_decode_operand_bitwise(m, k, frac, mult):
+    """The decode operand (per-step scaled fp16) and its group records
+    (offsets, fold factors, zeros for tokens M..15) bit for bit, written over
+    a poisoned buffer."""
     bits, x = I.make_activations(2, m, k, frac, mult)
     out, sc = _run(to_dev_bf16(bits), m, k, B.TERN_FWHT_DECODE)
-    vals, inv = O.decode_operand(O.fwht_f32(x))
+    vals, aux = O.decode_operand(O.fwht_f32(x))
+    assert np.array_equal(f16_bits(out), vals.view(np.uint16))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), aux.view(np.uint32))
+
+
+@pytest.mark.parametrize("m,k,frac,mult", CASES + [(40, 5120, 0.001, 50.0)])
+def test_fwht_f16_operand_bitwise(m, k, frac, mult):
+    bits, x = I.make_activations(2, m, k, frac, mult)
+    out, sc = _run(to_dev_bf16(bits), m, k, B.TERN_FWHT_F16)
+    vals, inv = O.f16_operand(O.fwht_f32(x))
     assert np.array_equal(f16_bits(out), vals.view(np.uint16))
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), inv.view(np.uint32))
+
+
+def test_decode_mode_rejects_more_than_16_tokens():
+    x = torch.zeros((17, 1024), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((17, 1024), dtype=torch.float16, device="cuda")
+    st = B.lib().tern_fwht_quant(x.data_ptr(), 17, 1024, None, B.TERN_FWHT_DECODE,
+                                 out.data_ptr(), B.decode_aux(1024).data_ptr(), None)
+    assert st == 2                                  # TERN_ERR_SHAPE
 
 
 @pytest.mark.parametrize("m,k,frac,mult", CASES + [(64, 17408, 0.001, 50.0), (37, 5120, 0.001, 50.0),
@@ -82,6 +105,10 @@ def test_sign_vector_all_modes():
     out, sc = _run(xd, m, k, B.TERN_FWHT_I8, sd)
     xq, ts = O.quant_tokens(ref)
     assert np.array_equal(out.cpu().float().numpy(), xq.astype(np.float32))
+    out, sc = _run(xd, m, k, B.TERN_FWHT_DECODE, sd)
+    vals, aux = O.decode_operand(ref)
+    assert np.array_equal(f16_bits(out), vals.view(np.uint16))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), aux.view(np.uint32))
     # unaligned sign pointer (the header allows it)
     buf = torch.zeros(k + 1, dtype=torch.int8, device="cuda")
     buf[1:] = sd
@@ -106,7 +133,11 @@ def test_degenerate_inputs():
     ref = O.fwht_f32(xf)
     assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
     out, sc = _run(xd, 6, k, B.TERN_FWHT_DECODE)
-    vals, inv = O.decode_operand(ref)
+    vals, aux = O.decode_operand(ref)
+    assert np.array_equal(f16_bits(out), vals.view(np.uint16))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), aux.view(np.uint32))
+    out, sc = _run(xd, 6, k, B.TERN_FWHT_F16)
+    vals, inv = O.f16_operand(ref)
     assert np.array_equal(f16_bits(out), vals.view(np.uint16))
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), inv.view(np.uint32))
     out, sc = _run(xd, 6, k, B.TERN_FWHT_I8)

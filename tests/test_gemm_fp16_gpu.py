@@ -27,7 +27,7 @@ def _lib():
 
 def _operand_ref(x, codes, scales):
     """fp64 of the variant's arithmetic on its exact fp16 operands."""
-    xh, inv = O.decode_operand(O.fwht_f32(x))
+    xh, inv = O.f16_operand(O.fwht_f32(x))
     m, k = xh.shape
     xe = (xh.astype(np.float64).reshape(m, k // 1024, 1024) *
           inv.astype(np.float64)[:, :, None]).reshape(m, k)
@@ -109,7 +109,7 @@ def test_split_k_within_rounding(m, n, k):
     scales = I.make_scales(24, n, k)
     bits, x = I.make_activations(24, m, k, 0.001, 50.0)
     w_h = B.expand_fp16(to_dev(codes), to_dev(scales))
-    xh, xs = B.fwht(to_dev_bf16(bits), B.TERN_FWHT_DECODE)
+    xh, xs = B.fwht(to_dev_bf16(bits), B.TERN_FWHT_F16)
     y0 = poison(torch.empty((m, n), dtype=torch.bfloat16, device="cuda"))
     y1 = poison(torch.empty((m, n), dtype=torch.bfloat16, device="cuda"))
     B.tern_gemm_prefill_fp16(xh, xs, w_h, m, n, k, y0)

@@ -93,13 +93,16 @@ def test_special_weights():
     scales = I.make_scales(9, n, k)
     codes = np.zeros((n, k), np.int8)
     y = _decode(_layer(codes, scales), bits, m)
-    assert not y.any()                      # all-zero codes -> exact zeros
+    # all-zero codes: only the rounding left by the group offsets' cancellation
+    check_elementwise(y, np.zeros((m, n)), codes, scales, x, what="zero codes")
+    assert np.abs(y).max() < 1e-3 * np.abs(O.rotate_f64(x)).max()
     codes[5, 1300] = -1                     # a single nonzero code
     y = _decode(_layer(codes, scales), bits, m)
+    ref = O.linear_f64(x, codes, scales)
+    check_elementwise(y, ref, codes, scales, x, what="one code")
     xr = O.rotate_f64(x)
     want = -float(scales[5, 1300 // 128]) * xr[:, 1300]
-    assert np.allclose(y[:, 5], want, rtol=2 ** -8, atol=0)
-    assert not np.delete(y, 5, axis=1).any()
+    assert np.allclose(y[:, 5], want, rtol=2 ** -7, atol=1e-4)
 
 
 def test_workspace_after_a_gemm_is_cleaned():

@@ -87,12 +87,12 @@ def test_sign_vector():
 
 def test_quant_rotated_matches_fwht_quant():
     """Quantising the rotated values separately gives the rotation kernel's
-    own decode operand and int8 output bit for bit."""
+    own decode operand, fp16 operand and int8 output bit for bit."""
     m, k = 7, 5120
     bits, x = I.make_activations(62, m, k, 0.001, 50.0)
     xb = to_dev_bf16(bits)
     xr, _ = B.fwht(xb, B.TERN_FWHT_F32)
-    for mode in (B.TERN_FWHT_DECODE, B.TERN_FWHT_I8):
+    for mode in (B.TERN_FWHT_DECODE, B.TERN_FWHT_F16, B.TERN_FWHT_I8):
         out, sc = B.fwht(xb, mode)
         out2 = torch.empty_like(out)
         sc2 = torch.empty_like(sc)
