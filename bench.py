@@ -261,8 +261,8 @@ TRAFFIC_GEMM_I8_GATEUP_M2048 = 380_628_736 + 120_762_112   # gemm_i8_kernel, M =
 
 def _gemv_algorithmic_bytes(m, n, k):
     """Bytes one GEMV launch must move: codes + scales + the fp16 activation
-    operand + its 128-byte group records + bf16 output."""
-    return n * k // 4 + n * (k // 128) * 2 + 2 * m * k + (k // 128) * 128 + m * n * 2
+    operand + its 192-byte group records + bf16 output."""
+    return n * k // 4 + n * (k // 128) * 2 + 2 * m * k + (k // 128) * 192 + m * n * 2
 
 
 def run_decode(args, rank, ws, local):
@@ -847,6 +847,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--no-decode-configs", action="store_true",
+                    help="skip the down / qkv decode configurations (for profiling)")
     ap.add_argument("--stack-layers", type=int, default=64,
                     help="layers of the linear stack section (64 = the 27B model's stack)")
     ap.add_argument("--stack-only", action="store_true",
@@ -875,7 +877,7 @@ def main():
     line, layers = run_decode(args, rank, ws, local)
     del layers
     torch.cuda.empty_cache()
-    if rank == 0:
+    if rank == 0 and not args.no_decode_configs:
         line["decode_configs"] = run_decode_configs(args, local)
     if not args.no_prefill:
         line["prefill"] = run_prefill(args, local)

@@ -146,15 +146,17 @@ tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, in
  *                 e = j (j < 6) or j - 6 (the power of four the packed field
  *                 of that step carries):
  *                 out = fp16 [M][K], fp16_rn(xr[m,k] * 2^(sh - 2e));
- *                 out_scale = float aux[G][32], one 128-byte record per
- *                 128-group g: aux[g][m] = the fp32 sum over k in g of
+ *                 out_scale = float aux[G][48], one 192-byte record per
+ *                 128-group g.  With X[g,m] = the fp32 sum over k in g of
  *                 out[m,k] * 2^(2e - 24) (every term exact; the 8
  *                 consecutive columns 8q .. 8q + 7 left to right, then the
  *                 16 partial sums by a butterfly p[q] += p[q ^ s],
- *                 s = 1, 2, 4, 8), aux[g][16 + m] = 2^(12 - sh) of the block
- *                 holding g; both 0 for m >= M.  The GEMV subtracts aux[g][m]
- *                 from each tensor-core group sum (the fields hold code + 1)
- *                 and multiplies each block's sum by aux[g][16 + m]
+ *                 s = 1, 2, 4, 8) and 0 for m >= M: aux[g][4i .. 4i + 3] =
+ *                 (0 - X[g,2i], 0 - X[g,2i+1], 0 - X[g,2i], 0 - X[g,2i+1])
+ *                 for i = 0..7 (fp32; the tensor core's accumulator quad:
+ *                 the fields hold code + 1, so each group sum starts at minus
+ *                 the offset), aux[g][32 + m] = 2^(12 - sh) of the block
+ *                 holding g (0 for m >= M), the block's fold factor
  *          TERN_FWHT_F16:    out = fp16 [M][K], the fp16 prefill variant's
  *                 operand: fp16_rn(xr[m,k] * 2^sh[m,b]); out_scale = float
  *                 [M][B] holding 2^-sh[m,b] (exact); any M
@@ -234,7 +236,7 @@ tern_status tern_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, 
  *
  *   packed                  from tern_pack (this layer's N, K)
  *   xh, xs                  from tern_fwht_quant(mode = TERN_FWHT_DECODE):
- *                           fp16 [M][K] and the float aux [K/128][32] records
+ *                           fp16 [M][K] and the float aux [K/128][48] records
  *   y                       bf16 [M][N]
  *   ws, ws_bytes            workspace of at least
  *                           tern_workspace_bytes(TERN_OP_GEMV, M, N, K) bytes,

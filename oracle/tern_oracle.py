@@ -508,24 +508,27 @@ def decode_operand(xr):
     For token m, 1024-block b (F = 2^sh, _block_shift) and column k of k16
     step j (e = e(j), see the packed format):
       xh[m, k] = fp16_rn(xr[m, k] * 2^(sh - 2e))      (the fp32 product is exact)
-    and per 128-group g, a 32-float record aux[g]:
-      aux[g][m]      = X[g, m] = the fp32 sum over k in g of xh[m, k] * 2^(2e - 24)
-                       (each term exact), added in this order: the eight
-                       consecutive columns 8q .. 8q + 7 of the group left to
-                       right (q = 0..15), then the sixteen partial sums by a
-                       butterfly tree, p[q] <- p[q] + p[q ^ s] for s = 1, 2, 4, 8;
-      aux[g][16 + m] = 2^(12 - sh) of the block holding g;
-      both 0 for m >= M.
+    and per 128-group g a 48-float record aux[g]:
+      X[g, m] = the fp32 sum over k in g of xh[m, k] * 2^(2e - 24) (each term
+                exact), added in this order: the eight consecutive columns
+                8q .. 8q + 7 of the group left to right (q = 0..15), then the
+                sixteen partial sums by a butterfly tree,
+                p[q] <- p[q] + p[q ^ s] for s = 1, 2, 4, 8;
+      aux[g][4 i .. 4 i + 3] = (-X[g, 2i], -X[g, 2i+1], -X[g, 2i], -X[g, 2i+1])
+                for i = 0..7 (the tensor core's accumulator starts there),
+                each computed as 0 - X in fp32 (+0 where X is 0);
+      aux[g][32 + m] = 2^(12 - sh) of the block holding g;
+      X and the fold factor are 0 for m >= M.
     A field read u * 4^e * 2^-24 times xh[m, k] is u * xh * 2^(2e - 24), so the
     tensor core's group sum minus X is sum_k code * xr * 2^(sh - 24) (up to
     rounding); times the block's 2^(12 - sh) that is 2^-12 sum_k code * xr.
-    Returns (fp16 [M, K], float32 [G, 32]).
+    Returns (fp16 [M, K], float32 [G, 48]).
     """
     xr = np.asarray(xr, dtype=np.float32)
     m, k = xr.shape
     if m > 16:
         raise ValueError("the decode operand holds at most 16 tokens")
-    nb, g_count = k // HBLOCK, k // GROUP
+    g_count = k // GROUP
     sh = _block_shift(xr)                                             # [m, nb]
     e = _k_exponents(k)                                               # [k]
     shk = np.repeat(sh, HBLOCK, axis=1) - 2 * e[None, :]              # [m, k]
@@ -540,8 +543,23 @@ def decode_operand(xr):
     idx = np.arange(16)
     for sft in (1, 2, 4, 8):
         p = (p + p[..., idx ^ sft]).astype(np.float32)
-    aux = np.zeros((g_count, 32), dtype=np.float32)
-    aux[:, :m] = p[:, :, 0].T
+    x16 = np.zeros((g_count, 16), dtype=np.float32)
+    x16[:, :m] = p[:, :, 0].T
+    aux = np.zeros((g_count, 48), dtype=np.float32)
+    pairs = x16.reshape(g_count, 8, 2)
+    aux[:, :32] = -np.concatenate([pairs, pairs], axis=2).reshape(g_count, 32)
+    aux[:, :32] += np.float32(0.0)                                    # 0 - X: -0 becomes +0
     fold = np.ldexp(np.float32(1.0), 12 - sh).astype(np.float32)      # [m, nb]
-    aux[:, 16:16 + m] = np.repeat(fold, HBLOCK // GROUP, axis=1).T
+    aux[:, 32:32 + m] = np.repeat(fold, HBLOCK // GROUP, axis=1).T
     return xh, aux
+
+
+def decode_offsets(aux):
+    """The group offsets X[g, m] (16 tokens) of a decode operand record."""
+    aux = np.asarray(aux, dtype=np.float32)
+    return -aux[:, 0:32].reshape(-1, 8, 4)[:, :, :2].reshape(-1, 16)
+
+
+def decode_folds(aux):
+    """The fold factors [g, m] (16 tokens) of a decode operand record."""
+    return np.asarray(aux, dtype=np.float32)[:, 32:48]

@@ -285,9 +285,9 @@ def pack_layer(codes: torch.Tensor, scales: torch.Tensor, decode: bool = True,
 
 
 def decode_aux(k: int, device="cuda") -> torch.Tensor:
-    """The float [K/128][32] group records of the decode operand
+    """The float [K/128][48] group records of the decode operand
     (TERN_FWHT_DECODE's out_scale)."""
-    return torch.empty((k // 128, 32), dtype=torch.float32, device=device)
+    return torch.empty((k // 128, 48), dtype=torch.float32, device=device)
 
 
 def fwht(x: torch.Tensor, mode: int, sign: torch.Tensor | None = None, stream=None):

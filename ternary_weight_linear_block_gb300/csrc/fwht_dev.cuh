@@ -235,33 +235,40 @@ __device__ __forceinline__ float group_offset(float part) {
 }
 
 // Rotated block (token m, block b) -> the decode operand in global memory:
-// xh [M][K] fp16 and the group records aux [G][32] (offsets of token m at
-// [g][m], the block's fold factor at [g][16 + m]).  The warp of token 0 also
-// writes the zeros of tokens M..15 in the block's 8 records.
+// xh [M][K] fp16 and the 48-float group records aux [G][48]: the negated
+// offsets as the tensor core's accumulator quads (0 - X of tokens 2i and
+// 2i + 1 at [g][4i], [g][4i + 1] and again at [g][4i + 2], [g][4i + 3]) and
+// the block's fold factor of token m at [g][32 + m].  The warp of token 0
+// also writes the zeros of tokens M..15 in the block's 8 records.
 __device__ __forceinline__ void decode_store(const float (&v)[4][8], int lane, int m, int b,
                                              int M, int K, __half* __restrict__ out,
                                              float* __restrict__ aux) {
   const int sh = block_shift(v);
   const int e = lane_step_exp(lane);
   __half* o = out + static_cast<long>(m) * K + static_cast<long>(b) * 1024;
-  float* ab = aux + static_cast<long>(b) * 8 * 32;
+  float* ab = aux + static_cast<long>(b) * 8 * 48;
+  const int qi = 4 * (m >> 1) + (m & 1);
 #pragma unroll
   for (int ih = 0; ih < 4; ++ih) {
     float part;
     *reinterpret_cast<uint4*>(o + ih * 256 + lane * 8) = decode_pack8(v, ih, sh, e, part);
-    const float x = group_offset(part);
+    const float x = __fsub_rn(0.f, group_offset(part));
     if ((lane & 15) == 0) {
-      float* rec = ab + (2 * ih + (lane >> 4)) * 32;
-      rec[m] = x;
-      rec[16 + m] = pow2f(12 - sh);
+      float* rec = ab + (2 * ih + (lane >> 4)) * 48;
+      rec[qi] = x;
+      rec[qi + 2] = x;
+      rec[32 + m] = pow2f(12 - sh);
     }
   }
   if (m == 0)
     for (int i = lane; i < 8 * 16; i += 32) {
       const int t = i & 15;
       if (t >= M) {
-        ab[(i >> 4) * 32 + t] = 0.f;
-        ab[(i >> 4) * 32 + 16 + t] = 0.f;
+        float* rec = ab + (i >> 4) * 48;
+        const int q = 4 * (t >> 1) + (t & 1);
+        rec[q] = 0.f;
+        rec[q + 2] = 0.f;
+        rec[32 + t] = 0.f;
       }
     }
 }

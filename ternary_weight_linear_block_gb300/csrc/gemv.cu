@@ -14,8 +14,9 @@
 //   1024 bytes of scales, contiguous in the packed format, fetched by one
 //   bulk copy (L2 evict-first) into a 4-stage shared-memory ring; the
 //   activation tile of the group (16 token rows x 128 k, fp16) arrives by
-//   TMA (128-byte swizzle) into the same stage, with the group's 128-byte
-//   record (token offsets, block fold factors); token rows >= M are
+//   TMA (128-byte swizzle) into the same stage, with the group's 192-byte
+//   record (negated token offsets as accumulator quads, block fold
+//   factors); token rows >= M are
 //   zero-filled by TMA and cost no memory traffic.
 // * each 32-bit word of the packed format is one register of an m16n8k16 A
 //   fragment for all 8 k16 steps of the group: one AND (after a shift by 12
@@ -69,7 +70,7 @@ constexpr int TILES = RB / 16;
 constexpr int UNIT_CODE_BYTES = RB * 32;        // 512 rows x 128 codes x 2 bits
 constexpr int UNIT_BYTES = UNIT_CODE_BYTES + TILES * 32;
 constexpr int XTILE_BYTES = 16 * kGroup * 2;    // 16 token rows x 128 k, fp16 (two 64-k boxes)
-constexpr int AUX_BYTES = 128;                  // the group's record: 16 offsets, 16 fold factors
+constexpr int AUX_BYTES = 192;                  // the group's record: 8 offset quads, 16 fold factors
 constexpr int AUX_OFF = XTILE_BYTES + UNIT_BYTES;
 constexpr int STAGE_TX = XTILE_BYTES + UNIT_BYTES + AUX_BYTES;
 constexpr int STAGE_BYTES = 24576;
@@ -143,16 +144,44 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// The first MMA of a group: the accumulator starts at (c0, c1, c0, c1), the
-// two tokens' negated group offsets (every row of the tile shares them).
+// The first MMA of a group: the accumulator starts at the quad c, the two
+// tokens' negated group offsets (every row of the tile shares them).
 __device__ __forceinline__ void mma_f16_init(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                             uint32_t a3, uint32_t b0, uint32_t b1, float c0,
-                                             float c1) {
+                                             uint32_t a3, uint32_t b0, uint32_t b1,
+                                             const float4& c) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%11,%10,%11};\n"
+      "{%8,%9}, {%10,%11,%12,%13};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z),
+        "f"(c.w));
+}
+
+// Shared-memory loads at 32-bit shared addresses (the stage contents arrive
+// by the async proxy; the loads follow the barrier wait that covers them).
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds_v4f(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float2 lds_v2f(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
 }
 
 
@@ -333,7 +362,7 @@ __global__ void __launch_bounds__(FIX_THREADS)
 template <int NT>
 __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t (&sp)[TPW],
                                           const uint32_t (&bf)[NT][8][2],
-                                          const float (&xo)[NT][2], float (&bacc)[TPW][NT][4]) {
+                                          const float4 (&xo)[NT], float (&bacc)[TPW][NT][4]) {
   float d[TPW][NT][4];
   uint32_t hi[TPW][4];
 #pragma unroll
@@ -356,8 +385,7 @@ __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         if (j == 0)
-          mma_f16_init(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][0][0], bf[nt][0][1], xo[nt][0],
-                       xo[nt][1]);
+          mma_f16_init(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][0][0], bf[nt][0][1], xo[nt]);
         else
           mma_f16(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
       }
@@ -453,7 +481,7 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
         uint8_t* st = smem + i * STAGE_BYTES;
         ptx::tma_load_2d(st, &tmX, &full[i], gi * kGroup, 0);
         ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[i], gi * kGroup + 64, 0);
-        ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(gi) * 32, AUX_BYTES, &full[i]);
+        ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(gi) * 48, AUX_BYTES, &full[i]);
       }
       issued = pre;
     }
@@ -474,7 +502,7 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
                         UNIT_BYTES, &full[s], pol);
     ptx::tma_load_2d(st, &tmX, &full[s], gj * kGroup, 0);
     ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[s], gj * kGroup + 64, 0);
-    ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(gj) * 32, AUX_BYTES, &full[s]);
+    ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(gj) * 48, AUX_BYTES, &full[s]);
     ++issued;
   };
 
@@ -509,7 +537,7 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
         }
         ptx::tma_load_2d(st, &tmX, &full[s], g * kGroup, 0);
         ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[s], g * kGroup + 64, 0);
-        ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(g) * 32, AUX_BYTES, &full[s]);
+        ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(g) * 48, AUX_BYTES, &full[s]);
         if (++g == G) g = 0;
       }
       if (!ok) {
@@ -542,6 +570,12 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
         const int chunk = 2 * (j & 3) + (mi & 1);
         bf_off[nt][q] = (j >> 2) * (XTILE_BYTES / 2) + row * 128 + ((chunk ^ (row & 7)) << 4);
       }
+    // the warp's two tiles' code slots, their scale pairs, the record's
+    // offset quads and fold factors of tokens 8 nt + 2 cq + {0, 1}
+    const uint32_t code_off = XTILE_BYTES + 512 * (TPW * cw) + 16 * lane;
+    const uint32_t sp_off = XTILE_BYTES + UNIT_CODE_BYTES + 32 * (TPW * cw) + 4 * gq;
+    const uint32_t xo_off = AUX_OFF + 16 * cq;
+    const uint32_t fo_off = AUX_OFF + 128 + 8 * cq;
     const uint32_t smem_base = ptx::smem_u32(smem);
 
     float acc[TPW][NT][4], bacc[TPW][NT][4];
@@ -553,6 +587,8 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
         for (int i = 0; i < 4; ++i) acc[tt][nt][i] = bacc[tt][nt][i] = 0.f;
 
     int rb = u0 / G, g = u0 % G, seg_g0 = g;
+    int s = 0;               // ring stage of unit i
+    uint32_t ph = 0;         // its phase
 
     // The CTA's units form segments, one per row block they touch; the hot
     // loop runs over the units of one segment and the segment's end (direct
@@ -566,47 +602,42 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
           if (lane == 0 && prod_ok && i >= 1 && i + STAGES - 1 < n_units) produce(i + STAGES - 1);
           __syncwarp();
         }
-        const int s = i % STAGES;
-        const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
         if (!ptx::mbar_wait_warp(&full[s], ph, abort_flag, WAIT_LIMIT)) {
           if (!*abort_flag) fail(abort_flag, ERR_CONSUMER);
           alive = false;
           break;
         }
-        const uint8_t* st = smem + s * STAGE_BYTES;
-        const uint8_t* unit = st + XTILE_BYTES;
+        const uint32_t st = smem_base + s * STAGE_BYTES;
         uint4 cv[TPW];
         uint32_t sp[TPW];
 #pragma unroll
         for (int tt = 0; tt < TPW; ++tt) {
-          cv[tt] = *reinterpret_cast<const uint4*>(unit + 512 * (TPW * cw + tt) + 16 * lane);
-          sp[tt] = *reinterpret_cast<const uint32_t*>(unit + UNIT_CODE_BYTES + 32 * (TPW * cw + tt) +
-                                                      4 * gq);
+          cv[tt] = lds_v4(st + code_off + 512 * tt);
+          sp[tt] = lds_u32(st + sp_off + 32 * tt);
         }
-        // the group record: offsets of tokens 8 nt + 2 cq + {0,1} (negated:
-        // the accumulators start there) and the block's fold factors
-        float xo[NT][2], fo[NT][2];
+        float4 xo[NT];
+        float fo[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float2 o2 = *reinterpret_cast<const float2*>(st + AUX_OFF + 4 * (8 * nt + 2 * cq));
-          const float2 f2 =
-              *reinterpret_cast<const float2*>(st + AUX_OFF + 64 + 4 * (8 * nt + 2 * cq));
-          xo[nt][0] = -o2.x;
-          xo[nt][1] = -o2.y;
+          xo[nt] = lds_v4f(st + xo_off + 64 * nt);
+          const float2 f2 = lds_v2f(st + fo_off + 32 * nt);
           fo[nt][0] = f2.x;
           fo[nt][1] = f2.y;
         }
         // B fragments: bf[nt][j][0..1] for the 8 k16 steps of the group
         uint32_t bf[NT][8][2];
-        const uint32_t xb = smem_base + s * STAGE_BYTES;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            ldmatrix_x4(xb + bf_off[nt][q], bf[nt][2 * q][0], bf[nt][2 * q][1], bf[nt][2 * q + 1][0],
+            ldmatrix_x4(st + bf_off[nt][q], bf[nt][2 * q][0], bf[nt][2 * q][1], bf[nt][2 * q + 1][0],
                         bf[nt][2 * q + 1][1]);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[s]);
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
         unit_math<NT>(cv, sp, bf, xo, bacc);
         if ((g & 7) == 7 || i + 1 == i_end) fold_block<NT>(acc, bacc, fo);
         ++g;
@@ -830,14 +861,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t bf[NT][8][2];
         const int pos = g >= gs ? g - gs : g + G - gs;
         const uint32_t xb = x_base + pos * 256;
-        float xo[NT][2];
+        float4 xo[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int tok = 8 * nt + 2 * cq + h;
-            xo[nt][h] = tok < M ? -xo_s[pos * 16 + tok] : 0.f;
-          }
+        for (int nt = 0; nt < NT; ++nt) {
+          const int tok = 8 * nt + 2 * cq;
+          const float x0 = tok < M ? __fsub_rn(0.f, xo_s[pos * 16 + tok]) : 0.f;
+          const float x1 = tok + 1 < M ? __fsub_rn(0.f, xo_s[pos * 16 + tok + 1]) : 0.f;
+          xo[nt] = make_float4(x0, x1, x0, x1);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

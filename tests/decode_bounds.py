@@ -82,6 +82,7 @@ def emulate_decode(codes, scales, x, sign=None):
     packed = O.pack_weights(codes, scales)
     c2, s2 = O.unpack_weights(packed, n, k)
     xh, aux = O.decode_operand(O.fwht_f32(np.asarray(x, np.float32), sign))
+    off, fold = O.decode_offsets(aux), O.decode_folds(aux)
     m = xh.shape[0]
     j = (np.arange(k) % 128) // 16
     e = np.where(j < 6, j, j - 6)
@@ -89,6 +90,6 @@ def emulate_decode(codes, scales, x, sign=None):
     y = np.zeros((m, n))
     for g in range(k // 128):
         cols = slice(128 * g, 128 * g + 128)
-        d = xh[:, cols].astype(np.float64) @ a[:, cols].T - aux[g, :m][:, None].astype(np.float64)
-        y += (d * s2[:, g].astype(np.float64)[None, :]) * aux[g, 16:16 + m][:, None]
+        d = xh[:, cols].astype(np.float64) @ a[:, cols].T - off[g, :m][:, None].astype(np.float64)
+        y += (d * s2[:, g].astype(np.float64)[None, :]) * fold[g, :m][:, None]
     return O.bf16_round((y * 2.0 ** 12).astype(np.float32)).astype(np.float64)

@@ -389,7 +389,7 @@ def test_decode_operand_scaling_and_precision():
     k = xr.shape[1]
     j = (np.arange(k) % 128) // 16
     e = np.where(j < 6, j, j - 6)
-    fold = aux[::8, 16:20].T                             # [m, block]: 2^(12 - sh)
+    fold = O.decode_folds(aux)[::8, :4].T                # [m, block]: 2^(12 - sh)
     sh = 12 - np.log2(fold.astype(np.float64))
     assert np.all(sh == np.round(sh))
     shk = np.repeat(sh, 1024, axis=1) - 2 * e[None, :]
@@ -414,8 +414,13 @@ def test_decode_operand_group_offsets_exact_sum_and_padding():
     xr = _operand_case()
     xh, aux = O.decode_operand(xr)
     m, k = xr.shape
-    assert aux.shape == (k // 128, 32) and aux.dtype == np.float32
-    assert not aux[:, m:16].any() and not aux[:, 16 + m:].any()
+    assert aux.shape == (k // 128, 48) and aux.dtype == np.float32
+    off, fold = O.decode_offsets(aux), O.decode_folds(aux)
+    assert not off[:, m:].any() and not fold[:, m:].any()
+    # the accumulator quads: (-X[2i], -X[2i+1], -X[2i], -X[2i+1]), +0 for a zero offset
+    q = aux[:, :32].reshape(-1, 8, 4)
+    assert np.array_equal(q[:, :, :2].view(np.uint32), q[:, :, 2:].view(np.uint32))
+    assert not np.signbit(aux[:, :32][aux[:, :32] == 0]).any()
     j = (np.arange(k) % 128) // 16
     e = np.where(j < 6, j, j - 6)
     for mm in range(m):
@@ -424,7 +429,7 @@ def test_decode_operand_group_offsets_exact_sum_and_padding():
                      for kk in range(128 * g, 128 * g + 128)]
             exact = sum(terms)
             bound = sum(abs(t) for t in terms) * Fraction(8, 2 ** 24)
-            assert abs(Fraction(float(aux[g, mm])) - exact) <= bound, (mm, g)
+            assert abs(Fraction(float(off[g, mm])) - exact) <= bound, (mm, g)
 
 
 def _emulated_gemv(packed, n, k, xh, aux, m):
@@ -438,8 +443,9 @@ def _emulated_gemv(packed, n, k, xh, aux, m):
     y = np.zeros((m, n))
     for g in range(g_count):
         cols = slice(128 * g, 128 * g + 128)
-        d = xh[:, cols].astype(np.float64) @ a[:, cols].T - aux[g, :m][:, None].astype(np.float64)
-        y += (d * scales[:, g].astype(np.float64)[None, :]) * aux[g, 16:16 + m][:, None]
+        d = xh[:, cols].astype(np.float64) @ a[:, cols].T - \
+            O.decode_offsets(aux)[g, :m][:, None].astype(np.float64)
+        y += (d * scales[:, g].astype(np.float64)[None, :]) * O.decode_folds(aux)[g, :m][:, None]
     return y * 2.0 ** 12
 
 
@@ -459,7 +465,7 @@ def test_decode_arithmetic_reproduces_the_layer():
     y = _emulated_gemv(packed, n, k, xh, aux, m)
     assert O.rel_frobenius(y, exact) < 6e-4           # fp16 rounding of the operand: ~2.5e-4
     bad = aux.copy()
-    bad[:, :m] = 0.0                                 # offsets dropped
+    bad[:, :32] = 0.0                                # offsets dropped
     assert O.rel_frobenius(_emulated_gemv(packed, n, k, xh, bad, m), exact) > 0.5
     wrong = xh.copy()                                # steps 6, 7 read with 4^6, 4^7
     cols = ((np.arange(k) % 128) // 16) >= 6
