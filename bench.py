@@ -211,6 +211,16 @@ class DecodeRunner:
             B.tern_gemv_decode(layer.packed, self.xh[b], self.xs[b], m, self.n, self.k, self.y[b],
                                self.ws[b], self.ws[b].numel(), st)
 
+    def step_fused(self):
+        """The same decode pass with the rotation folded into the GEMV
+        (tern_linear_decode, one launch per batch)."""
+        st = self.stream.cuda_stream
+        for b, m in enumerate(self.ms):
+            layer = self.layers[self.i % len(self.layers)]
+            self.i += 1
+            B.tern_linear_decode(self.x[b], None, layer.packed, m, self.n, self.k, self.y[b],
+                                 self.ws[b], self.ws[b].numel(), st)
+
     def gemv_only(self, b):
         st = self.stream.cuda_stream
         m = self.ms[b]
@@ -290,6 +300,11 @@ def run_decode(args, rank, ws, local):
         kernel_launches = max(200, args.steps)
         tk = _time_region(lambda: run.gemv_only(kb), kernel_launches, stream, 1)
         gemv_us = tk / kernel_launches * 1e6
+        # the fused path (rotation inside the GEMV), same steps
+        for _ in range(args.warmup):
+            run.step_fused()
+        fused_steps = max(200, args.steps)
+        tf = _time_region(run.step_fused, fused_steps, stream, 1)
 
         # end to end through the public API (B.DecodeStepGraph): every step
         # copies the batches' pinned host activations in, rotates, multiplies
@@ -347,6 +362,10 @@ def run_decode(args, rank, ws, local):
                 "ms_per_step": round(te2e / e2e_steps * 1e3, 4),
                 "transfer": ("kernels read x from and write y to pinned host memory in place"
                              if plans[0].zero_copy else "memcpy nodes in the step's graph")},
+        "fused_step": {"what": "rotation folded into the GEMV (tern_linear_decode), one launch "
+                                "per batch, the same weights and batches",
+                       "value": round(bytes_step * fused_steps / tf / 1e9, 1), "unit": "GB/s",
+                       "ms_per_step": round(tf / fused_steps * 1e3, 5)},
         "gpu_launches": run.launches_per_step() * args.steps,
         "clocks": clocks,
     }

@@ -55,6 +55,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <utility>
+
 #include "fwht_dev.cuh"
 #include "sm100_ptx.cuh"
 #include "tern_internal.cuh"
@@ -144,44 +146,56 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// The first MMA of a group: the accumulator starts at the quad c, the two
-// tokens' negated group offsets (every row of the tile shares them).
-__device__ __forceinline__ void mma_f16_init(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                             uint32_t a3, uint32_t b0, uint32_t b1,
-                                             const float4& c) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%11,%12,%13};\n"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z),
-        "f"(c.w));
-}
-
 // Shared-memory loads at 32-bit shared addresses (the stage contents arrive
 // by the async proxy; the loads follow the barrier wait that covers them).
+template <int OFF = 0>
 __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
   uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+%5];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
+               : "r"(a), "n"(OFF));
   return v;
 }
-__device__ __forceinline__ float4 lds_v4f(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(a));
-  return v;
+// (a volatile load: each tile's accumulator quad is loaded into registers of
+// its own, so the MMAs accumulate in place)
+template <int OFF = 0>
+__device__ __forceinline__ void lds_v4f(uint32_t a, float (&v)[4]) {
+  asm volatile("ld.volatile.shared.v4.f32 {%0,%1,%2,%3}, [%4+%5];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+               : "r"(a), "n"(OFF));
 }
+template <int OFF = 0>
 __device__ __forceinline__ float2 lds_v2f(uint32_t a) {
   float2 v;
-  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2+%3];" : "=f"(v.x), "=f"(v.y) : "r"(a), "n"(OFF));
   return v;
 }
+template <int OFF = 0>
 __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
   uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF));
   return v;
+}
+template <int OFF = 0>
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4+%5];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a), "n"(OFF));
+}
+
+// The loads of one unit for a warp's TPW tiles, at compile-time offsets from
+// three per-lane base addresses: code slots (512 bytes apart), scale pairs
+// (32 bytes apart) and, for each tile, the record's offset quad of n8 tile nt
+// (64 bytes apart) as the tile's initial accumulators.
+template <int NT, size_t... T>
+__device__ __forceinline__ void load_tiles(uint32_t a_code, uint32_t a_sp, uint32_t a_rec,
+                                           uint4 (&cv)[TPW], uint32_t (&sp)[TPW],
+                                           float (&d)[TPW][NT][4], std::index_sequence<T...>) {
+  ((cv[T] = lds_v4<512 * static_cast<int>(T)>(a_code)), ...);
+  ((sp[T] = lds_u32<32 * static_cast<int>(T)>(a_sp)), ...);
+  (lds_v4f<0>(a_rec, d[T][0]), ...);
+  if constexpr (NT == 2) (lds_v4f<64>(a_rec, d[T][NT - 1]), ...);
 }
 
 
@@ -351,19 +365,18 @@ __global__ void __launch_bounds__(FIX_THREADS)
   y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(__fmul_rn(sum, OUT_SCALE));
 }
 
-// The MMAs of one unit for this warp's tiles: codes cv, scale pairs sp, the B
-// fragments bf of the group's 8 k16 steps and the tokens' negated group
-// offsets xo; the group sums, scaled by the rows' group scales, are added to
-// bacc.  Word p of a tile's slot is A-fragment register p for every step j:
+// The MMAs of one unit for this warp's tiles: codes cv, scale pairs sp and the
+// B fragments bf of the group's 8 k16 steps accumulate into d, which arrives
+// holding the tokens' negated group offsets; the group sums, scaled by the
+// rows' group scales, are added to bacc.  Word p of a tile's slot is A-fragment register p for every step j:
 // one AND per register (steps 6 and 7 from the word shifted right by 12)
 // gives the fp16 pair u * 4^e * 2^-24, u = code + 1; the operand carries
 // 4^-e, and each group's accumulator starts at minus the tokens' offset,
 // which removes the "+1" of u.
 template <int NT>
 __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t (&sp)[TPW],
-                                          const uint32_t (&bf)[NT][8][2],
-                                          const float4 (&xo)[NT], float (&bacc)[TPW][NT][4]) {
-  float d[TPW][NT][4];
+                                          const uint32_t (&bf)[NT][8][2], float (&d)[TPW][NT][4],
+                                          float (&bacc)[TPW][NT][4]) {
   uint32_t hi[TPW][4];
 #pragma unroll
   for (int tt = 0; tt < TPW; ++tt) {
@@ -383,12 +396,8 @@ __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t
 #pragma unroll
       for (int p = 0; p < 4; ++p) a[p] = (j < 6 ? w4[p] : hi[tt][p]) & mask;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (j == 0)
-          mma_f16_init(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][0][0], bf[nt][0][1], xo[nt]);
-        else
-          mma_f16(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
-      }
+      for (int nt = 0; nt < NT; ++nt)
+        mma_f16(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
     }
   }
 #pragma unroll
@@ -574,8 +583,7 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
     // offset quads and fold factors of tokens 8 nt + 2 cq + {0, 1}
     const uint32_t code_off = XTILE_BYTES + 512 * (TPW * cw) + 16 * lane;
     const uint32_t sp_off = XTILE_BYTES + UNIT_CODE_BYTES + 32 * (TPW * cw) + 4 * gq;
-    const uint32_t xo_off = AUX_OFF + 16 * cq;
-    const uint32_t fo_off = AUX_OFF + 128 + 8 * cq;
+    const uint32_t rec_off = AUX_OFF + 16 * cq;    // offset quads; fold factors at + 128 - 8 cq
     const uint32_t smem_base = ptx::smem_u32(smem);
 
     float acc[TPW][NT][4], bacc[TPW][NT][4];
@@ -608,37 +616,40 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
           break;
         }
         const uint32_t st = smem_base + s * STAGE_BYTES;
+        const uint32_t a_code = st + code_off, a_sp = st + sp_off, a_rec = st + rec_off;
         uint4 cv[TPW];
         uint32_t sp[TPW];
-#pragma unroll
-        for (int tt = 0; tt < TPW; ++tt) {
-          cv[tt] = lds_v4(st + code_off + 512 * tt);
-          sp[tt] = lds_u32(st + sp_off + 32 * tt);
-        }
-        float4 xo[NT];
+        float d[TPW][NT][4];       // each tile's accumulators start at the offset quad
+        load_tiles<NT>(a_code, a_sp, a_rec, cv, sp, d, std::make_index_sequence<TPW>{});
         float fo[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          xo[nt] = lds_v4f(st + xo_off + 64 * nt);
-          const float2 f2 = lds_v2f(st + fo_off + 32 * nt);
-          fo[nt][0] = f2.x;
-          fo[nt][1] = f2.y;
+        {
+          const float2 f2 = lds_v2f<0>(a_rec + 128 - 8 * cq);
+          fo[0][0] = f2.x;
+          fo[0][1] = f2.y;
         }
-        // B fragments: bf[nt][j][0..1] for the 8 k16 steps of the group
+        if constexpr (NT == 2) {
+          const float2 f2 = lds_v2f<32>(a_rec + 128 - 8 * cq);
+          fo[NT - 1][0] = f2.x;
+          fo[NT - 1][1] = f2.y;
+        }
+        // B fragments: bf[nt][j][0..1] for the 8 k16 steps of the group; the
+        // steps 4..7 lie XTILE_BYTES / 2 after steps 0..3
         uint32_t bf[NT][8][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            ldmatrix_x4(st + bf_off[nt][q], bf[nt][2 * q][0], bf[nt][2 * q][1], bf[nt][2 * q + 1][0],
-                        bf[nt][2 * q + 1][1]);
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t b0 = st + bf_off[nt][0], b1 = st + bf_off[nt][1];
+          ldsm_x4<0>(b0, bf[nt][0][0], bf[nt][0][1], bf[nt][1][0], bf[nt][1][1]);
+          ldsm_x4<0>(b1, bf[nt][2][0], bf[nt][2][1], bf[nt][3][0], bf[nt][3][1]);
+          ldsm_x4<XTILE_BYTES / 2>(b0, bf[nt][4][0], bf[nt][4][1], bf[nt][5][0], bf[nt][5][1]);
+          ldsm_x4<XTILE_BYTES / 2>(b1, bf[nt][6][0], bf[nt][6][1], bf[nt][7][0], bf[nt][7][1]);
+        }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[s]);
         if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
         }
-        unit_math<NT>(cv, sp, bf, xo, bacc);
+        unit_math<NT>(cv, sp, bf, d, bacc);
         if ((g & 7) == 7 || i + 1 == i_end) fold_block<NT>(acc, bacc, fo);
         ++g;
       }
@@ -861,13 +872,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t bf[NT][8][2];
         const int pos = g >= gs ? g - gs : g + G - gs;
         const uint32_t xb = x_base + pos * 256;
-        float4 xo[NT];
+        float d[TPW][NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int tok = 8 * nt + 2 * cq;
           const float x0 = tok < M ? __fsub_rn(0.f, xo_s[pos * 16 + tok]) : 0.f;
           const float x1 = tok + 1 < M ? __fsub_rn(0.f, xo_s[pos * 16 + tok + 1]) : 0.f;
-          xo[nt] = make_float4(x0, x1, x0, x1);
+#pragma unroll
+          for (int tt = 0; tt < TPW; ++tt) {
+            d[tt][nt][0] = d[tt][nt][2] = x0;
+            d[tt][nt][1] = d[tt][nt][3] = x1;
+          }
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -877,7 +892,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         bf[nt][2 * q + 1][0], bf[nt][2 * q + 1][1]);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[s]);
-        unit_math<NT>(cv, sp, bf, xo, bacc);
+        unit_math<NT>(cv, sp, bf, d, bacc);
         if ((g & 7) == 7 || i + 1 == n_units) {
           const int blk = g >> 3;
           float f[NT][2];
