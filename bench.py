@@ -372,6 +372,112 @@ def run_decode(args, rank, ws, local):
     return out, layers
 
 
+# ---------------------------------------------------------------- split layer (--split)
+
+SPLIT_LAYERS = (I.GATE_UP, I.DOWN)
+
+
+def split_shard(split, layer, world, rank, codes, scales, pack=True):
+    """This rank's part of one layer: its output rows (split "n", column
+    parallel) or its input columns (split "k", row parallel with the page's
+    half-block exchange), packed for decode (pack=False keeps the codes and
+    scales for a reference compute)."""
+    from ternary_weight_linear_block_gb300 import tp as TP
+    if split == "n":
+        plan = TP.nsplit_plan(layer.n, world, rank)
+        return TP.NSplitLinear(plan, codes[plan.n0:plan.n1].contiguous(),
+                               scales[plan.n0:plan.n1].contiguous(), decode=True, prefill=False,
+                               pack=pack)
+    plan = TP.ksplit_plan(layer.k, world, rank)
+    return TP.KSplitLinear(plan, codes[:, plan.k0:plan.k1].contiguous(),
+                           scales[:, plan.k0 // 128:plan.k1 // 128].contiguous(), decode=True,
+                           prefill=False, expand=False, pack=pack)
+
+
+def split_forward(split, lin, x, world, group=None, ops=None, local=None):
+    """One decode forward of a split layer on this rank: x is the whole input
+    [M, K]; returns the whole output (split "n": the all-gathered rows; split
+    "k": the all-reduced sum of the ranks' partials).  With one rank there is
+    no collective."""
+    from ternary_weight_linear_block_gb300 import tp as TP
+    if split == "n":
+        if world == 1:
+            return (local or TP.nsplit_local)(lin, x)
+        return TP.nsplit_forward(lin, x, group=group, local=local)
+    xs = x[:, lin.plan.k0:lin.plan.k1].contiguous()
+    if world == 1:
+        xr, h = TP.local_phase(lin, xs, ops=ops)
+        return TP.finish_phase(lin, xr, [h], "decode", ops)
+    return TP.forward(lin, xs, group=group, mode="decode", ops=ops)
+
+
+def split_value(whole_bytes_per_step, steps, t_max):
+    """Strong scaling: the whole layers' weight bytes per step (each step
+    processes every layer once, however it is split) over the slowest rank's
+    time."""
+    return whole_bytes_per_step * steps / t_max / 1e9
+
+
+def run_split(args, rank, ws, local):
+    """Decode of gate/up and down split over the ranks (tensor parallel), both
+    batches (M = 1 and 4) per step; weights rotate over shard copies larger
+    than L2 on every rank; NCCL collectives in the data path."""
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    split = args.split
+    with torch.cuda.stream(stream):
+        g = torch.Generator(device="cuda")
+        shards = {}
+        copies = {}
+        for layer in SPLIT_LAYERS:
+            shard_bytes = B.tern_packed_bytes(layer.n, layer.k) // ws
+            copies[layer.name] = max(2, int(np.ceil(2 * L2_BYTES / max(shard_bytes, 1))) + 1)
+            shards[layer.name] = []
+            for c in range(copies[layer.name]):
+                g.manual_seed(4242 + c)            # the same layer on every rank
+                codes = (torch.randint(0, 3, (layer.n, layer.k), dtype=torch.int8, device="cuda",
+                                       generator=g) - 1).to(torch.int8)
+                scales = (0.02 * torch.randn((layer.n, layer.k // 128), device="cuda",
+                                             generator=g).abs() + 1e-3).to(torch.float16)
+                shards[layer.name].append(split_shard(split, layer, ws, rank, codes, scales))
+                del codes, scales
+        xs = {(layer.name, m): _activations(layer, m, seed=500 + m).cuda()
+              for layer in SPLIT_LAYERS for m in DECODE_MS}
+        it = [0]
+
+        def step():
+            for layer in SPLIT_LAYERS:
+                lin = shards[layer.name][it[0] % copies[layer.name]]
+                for m in DECODE_MS:
+                    split_forward(split, lin, xs[(layer.name, m)], ws)
+            it[0] += 1
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        t = _time_region(step, args.steps, stream, ws, lead_cycles=0)
+        t = _max_over_ranks(t, ws)
+        B.tern_check(stream)
+    whole = sum(B.tern_packed_bytes(l.n, l.k) for l in SPLIT_LAYERS) * len(DECODE_MS)
+    how = ("column-parallel N split: each rank its output rows, one all-gather"
+           if split == "n" else
+           "row-parallel K split: each rank its input columns, half-block all-gather "
+           "+ all-reduce of the partial outputs")
+    return {
+        "metric": METRIC, "value": round(split_value(whole, args.steps, t), 1), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None,
+        "dtype": "f16 products (code x fp16 activations), f32 accumulate",
+        "data": "synthetic (seeded uniform ternary codes, |N(0,1)|-based fp16 g128 scales, "
+                "bf16 N(0,1) activations with 0.1% outlier channels x50)",
+        "config": {"workload": "decode gate/up 5120->34816 and down 17408->5120, split over "
+                               "the GPUs", "M": list(DECODE_MS),
+                   "parallelism": f"tp{ws} {how}",
+                   "l2": "inputs larger than L2: each rank's shards rotate over copies"},
+        "gpu_launches": None}
+
+
 def run_prefill(args, local, m=2048):
     """Prefill int8 path through gate/up 5120->34816 at M tokens: the rotation
     with per-token int8 quantisation, then the exact int8 GEMM (int8 values,
@@ -572,9 +678,9 @@ def run_prefill_configs(args, local, configs=((I.GATE_UP, 512), (I.DOWN, 512), (
     return out
 
 
-def run_decode_configs(args, local, shapes=(I.DOWN, I.QKV), ms=(1, 4, 8, 16)):
-    """The decode configurations of down 17408->5120 and qkv 5120->10240 at
-    M = 1, 4, 8 and 16: a step of rotation + GEMV (+ fixup), and the GEMV
+def run_decode_configs(args, local, shapes=(I.DOWN, I.QKV, I.O_PROJ), ms=(1, 4, 8, 16)):
+    """The decode configurations of down 17408->5120, qkv 5120->10240 and o
+    5120->5120 at M = 1, 4, 8 and 16: a step of rotation + GEMV (+ fixup), and the GEMV
     alone, each call streaming the next of several weight copies that
     together exceed L2 by more than 3x."""
     torch.cuda.set_device(local)
@@ -612,7 +718,7 @@ def run_decode_configs(args, local, shapes=(I.DOWN, I.QKV), ms=(1, 4, 8, 16)):
                 ts = _time_region(step, reps, stream, 1) / reps
                 tg = _time_region(gemv, reps, stream, 1) / reps
                 B.tern_check(stream)
-                out.append({"workload": f"decode {shp.name}, M={m}",
+                out.append({"workload": f"decode {shp.name}, M={m}", "shape": shp.name, "M": m,
                             "weight_GBps": round(wbytes / ts / 1e9, 1),
                             "pct_hbm_peak": round(100 * wbytes / ts / 1e9 / hbm_peak, 1),
                             "step_us": round(ts * 1e6, 2), "gemv_us": round(tg * 1e6, 2),
@@ -779,6 +885,79 @@ def _oracle_rate_one_core(budget_s):
         return None
 
 
+_SHAPES = {l.name: l for l in (I.TINY, I.GATE_UP, I.DOWN, I.QKV, I.O_PROJ)}
+
+
+def _oracle_config_rate(kind, shape_name, m, rows, budget_s):
+    """The oracle on a seeded row sample of one configuration, repeated for
+    about budget_s seconds.  kind "decode": O1 (fp64 dense reference), rate in
+    weight bytes per second of the sampled rows; kind "prefill": O2 (the
+    int8 path), rate in int8 ops (2 M rows K) per second."""
+    from oracle import tern_oracle as O
+    layer = _SHAPES[shape_name]
+    d = I.make_layer(layer, m, seed=5, n=rows)
+    work = (rows * layer.k // 4 + rows * (layer.k // 128) * 2) if kind == "decode" \
+        else 2.0 * m * rows * layer.k
+    fn = (lambda: O.linear_f64(d.x, d.codes, d.scales)) if kind == "decode" \
+        else (lambda: O.linear_int8(d.x, d.codes, d.scales))
+    fn()                                   # warm (the dense H cache, allocator)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return work * reps / dt, reps, dt
+
+
+def _one_core(fn_name, fn_args, budget_s):
+    """bench.<fn_name>(*fn_args) in a child process whose BLAS libraries start
+    with one thread (their thread count is fixed when numpy loads)."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "r = bench.%s(*%r); print(json.dumps([r[0], r[1], r[2]]))" % (ROOT, fn_name, fn_args))
+    try:
+        p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=budget_s + 120)
+        return tuple(json.loads(p.stdout.strip().splitlines()[-1]))
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
+def _host_cores():
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        blas = max((i.get("num_threads", 1) for i in threadpool_info()), default=cores)
+        cores = min(cores, blas)
+    except ImportError:
+        pass
+    return cores
+
+
+def config_cpu_baseline(kind, layer, m, rows, budget_s=1.5, one_core_s=1.0):
+    """The oracle beside one GPU configuration, on the host's cores and on one."""
+    rate, reps, dt = _oracle_config_rate(kind, layer.name, m, rows, budget_s)
+    unit, scale = ("GB/s", 1e9) if kind == "decode" else ("TOPS", 1e12)
+    out = {"value": round(rate / scale, 6), "unit": unit, "cores": _host_cores(), "kind": "oracle",
+           "sample": f"{'fp64 dense oracle (O1)' if kind == 'decode' else 'int8-path oracle (O2)'} "
+                     f"on {rows} of {layer.n} rows of {layer.name}, M={m}, "
+                     f"{reps} repetitions in {dt:.1f} s"}
+    if one_core_s > 0:
+        r1 = _one_core("_oracle_config_rate", [kind, layer.name, m, rows, one_core_s], one_core_s)
+        if r1 is not None:
+            out["one_core"] = {"value": round(r1[0] / scale, 6), "unit": unit, "cores": 1,
+                               "sample": f"the same sample, {r1[1]} repetitions in {r1[2]:.1f} s"}
+    return out
+
+
 def run_cpu_baseline(args, budget_s=15.0, one_core_s=5.0):
     """The oracle (fp64 dense reference) timed on a bounded sample of the
     workload, on the host's cores, and (one_core_s > 0) on one core."""
@@ -866,6 +1045,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--split", choices=["n", "k"], default=None,
+                    help="split gate/up and down over the GPUs (tensor parallel) instead of "
+                         "running independent replicas")
     ap.add_argument("--no-decode-configs", action="store_true",
                     help="skip the down / qkv decode configurations (for profiling)")
     ap.add_argument("--stack-layers", type=int, default=64,
@@ -888,6 +1070,14 @@ def main():
         if rank == 0:
             BUILD.build()
         _barrier(ws)
+    if args.split:
+        line = run_split(args, rank, ws, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     if args.stack_only:
         if rank == 0:
             print(json.dumps({"stack": run_stack(args, local, n_layers=args.stack_layers)}),
@@ -896,16 +1086,38 @@ def main():
     line, layers = run_decode(args, rank, ws, local)
     del layers
     torch.cuda.empty_cache()
+    cpu = not args.no_cpu_baseline and ws == 1 and rank == 0
     if rank == 0 and not args.no_decode_configs:
         line["decode_configs"] = run_decode_configs(args, local)
+        if cpu:
+            for e in line["decode_configs"]:
+                e["cpu_baseline"] = config_cpu_baseline(
+                    "decode", _SHAPES[e["shape"]], e["M"], rows=256, budget_s=1.0,
+                    one_core_s=1.0 if e["M"] == 4 else 0)
     if not args.no_prefill:
         line["prefill"] = run_prefill(args, local)
+        if cpu:
+            line["prefill"]["cpu_baseline"] = config_cpu_baseline(
+                "prefill", I.GATE_UP, 512, rows=64, budget_s=2.0, one_core_s=1.5)
         if rank == 0:
             line["prefill"]["other_configs"] = run_prefill_configs(args, local)
     if not args.no_prefill and rank == 0:
         line["mid_m"] = run_mid_m(args, local)
     if not args.no_stack and rank == 0:
         line["stack"] = run_stack(args, local, n_layers=args.stack_layers)
+        if cpu:
+            # each distinct shape's oracle rate at M = 1, times the layers
+            secs = 0.0
+            for shp in I.STACK_LAYERS:
+                r = config_cpu_baseline("decode", shp, 1, rows=256, budget_s=1.0, one_core_s=0)
+                secs += B.tern_packed_bytes(shp.n, shp.k) / (r["value"] * 1e9)
+            secs *= args.stack_layers
+            line["stack"]["cpu_baseline"] = {
+                "value": round(line["stack"]["packed_bytes"] / secs / 1e9, 6), "unit": "GB/s",
+                "ms_per_step": round(secs * 1e3, 1), "cores": _host_cores(), "kind": "oracle",
+                "sample": "fp64 dense oracle (O1) at M=1 on 256 rows of each of the four linear "
+                          "shapes, its per-byte rate applied to each shape's weights, times "
+                          f"{args.stack_layers} layers"}
     if rank == 0:
         if not args.no_cpu_baseline and ws == 1:
             line["cpu_baseline"] = run_cpu_baseline(args)

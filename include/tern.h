@@ -259,6 +259,31 @@ tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const fl
                              size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * tern_gemv_decode_f32 -- the same decode GEMV from fp32 rotated activations:
+ *     y[m,n] = bf16_rn( sum_g s[n,g] * sum_{k in g} code[n,k] * xr[m,k] )
+ * Page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2", section "前提".
+ * The call first forms the decode operand from xr exactly as
+ * tern_quant_rotated(TERN_FWHT_DECODE) does (into the workspace), then runs
+ * tern_gemv_decode on it: results are bit-identical to those two calls.
+ *
+ *   packed                  from tern_pack (this layer's N, K)
+ *   xr                      float [M][K], the rotated activations (for
+ *                           example tern_fwht_quant(TERN_FWHT_F32) output)
+ *   y                       bf16 [M][N]
+ *   ws, ws_bytes            workspace of at least
+ *                           tern_workspace_bytes(TERN_OP_GEMV_F32, M, N, K)
+ *                           bytes, 16-byte aligned, zero-filled before its
+ *                           first use (tern_workspace_init); its first
+ *                           tern_workspace_bytes(TERN_OP_GEMV, M, N, K) bytes
+ *                           are the GEMV's and are left zero-filled again by
+ *                           every call, the rest holds the operand.
+ * Requirements and errors as for tern_gemv_decode.
+ * ---------------------------------------------------------------------- */
+tern_status tern_gemv_decode_f32(const uint8_t* packed, const float* xr, int64_t M, int64_t N,
+                                 int64_t K, uint16_t* y, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/* ------------------------------------------------------------------------
  * tern_linear_decode -- the layer's whole decode path in one launch:
  *     y = tern_gemv_decode(tern_fwht_quant(x, sign, TERN_FWHT_DECODE))
  * Page "RTX 5070 x2 ... Ternary-Bonsai-2-27B on vLLM TP=2", section "前提"
@@ -412,6 +437,7 @@ tern_status tern_gemm_prefill_fp16(const uint16_t* xh, const float* xs, const ui
 #define TERN_OP_GEMV 1
 #define TERN_OP_GEMM 2
 #define TERN_OP_GEMM_PACKED 3
+#define TERN_OP_GEMV_F32 4
 size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
 /* 1 if the GPU current on this thread can load and store `host` directly
  * at that same address -- a pinned host buffer mapped into the device's
@@ -426,7 +452,8 @@ int tern_host_accessible(const void* host);
  * (0 for an empty call or an unknown op): for TERN_OP_GEMV the GEMV kernel,
  * plus the fixup kernel when a 512-row block is shared by more CTAs than the
  * GEMV sums in place (tern_gemv_decode, tern_linear_decode and
- * tern_gemv_decode_noalloc launch the same count); for TERN_OP_GEMM the
+ * tern_gemv_decode_noalloc launch the same count); for TERN_OP_GEMV_F32 one
+ * more (the operand's quantisation kernel); for TERN_OP_GEMM the
  * int8 (or fp16) GEMM, plus its finishing kernel when it is given the
  * workspace and splits K; for TERN_OP_GEMM_PACKED the GEMM, plus the
  * rescale kernel when its tiles are split along K.  Host-only; launch

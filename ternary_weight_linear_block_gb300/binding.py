@@ -37,6 +37,7 @@ TERN_FWHT_F16 = 3
 TERN_OP_GEMV = 1
 TERN_OP_GEMM = 2
 TERN_OP_GEMM_PACKED = 3
+TERN_OP_GEMV_F32 = 4
 STATUS_NAMES = {0: "TERN_OK", 1: "TERN_ERR_INVALID_ARG", 2: "TERN_ERR_SHAPE", 3: "TERN_ERR_ALIGN",
                 4: "TERN_ERR_UNSUPPORTED", 5: "TERN_ERR_CUDA", 6: "TERN_ERR_WORKSPACE",
                 7: "TERN_ERR_TIMEOUT"}
@@ -69,6 +70,7 @@ _SIGS = {
     "tern_selftest_wait": (ctypes.c_int, [ctypes.c_uint32, _p]),
     "tern_gemv_decode_noalloc": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
     "tern_linear_decode": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
+    "tern_gemv_decode_f32": (ctypes.c_int, [_p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
 }
 
 _lib = None
@@ -226,6 +228,11 @@ def tern_selftest_wait(polls: int, stream=None):
     """Launch the bounded-wait self-test (a wait that gives up after ``polls``
     polls); the next tern_check raises TERN_ERR_TIMEOUT."""
     return _call("tern_selftest_wait", polls, _stream(stream))
+
+
+def tern_gemv_decode_f32(packed, xr, m, n, k, y, ws, ws_bytes, stream=None):
+    return _call("tern_gemv_decode_f32", _ptr(packed), _ptr(xr), m, n, k, _ptr(y), _ptr(ws),
+                 ws_bytes, _stream(stream))
 
 
 def tern_linear_decode(x, sign, packed, m, n, k, y, ws, ws_bytes, stream=None):

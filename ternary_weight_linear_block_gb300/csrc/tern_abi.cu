@@ -38,6 +38,20 @@ tern_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TERN_OK : TERN_
 
 bool k_ok(int64_t K, int64_t kmax) { return K > 0 && K % kHBlock == 0 && K <= kmax; }
 
+// Workspace of tern_gemv_decode_f32: the GEMV's partial sums (zero between
+// calls), then the decode operand formed from xr (fp16 [M][K], records
+// [G][48]), each part 256-byte aligned.
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+size_t gemv_f32_xh_offset(int64_t M, int64_t N, int64_t K) {
+  return align256(gemv_workspace_bytes(M, N, K));
+}
+size_t gemv_f32_aux_offset(int64_t M, int64_t N, int64_t K) {
+  return gemv_f32_xh_offset(M, N, K) + align256(static_cast<size_t>(M) * K * 2);
+}
+size_t gemv_f32_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return gemv_f32_aux_offset(M, N, K) + static_cast<size_t>(K / kGroup) * 192;
+}
+
 }  // namespace
 
 extern "C" {
@@ -66,6 +80,7 @@ size_t tern_packed_bytes(int64_t N, int64_t K) {
 size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == TERN_OP_GEMV) return gemv_workspace_bytes(M, N, K);
+  if (op == TERN_OP_GEMV_F32) return M <= 16 ? gemv_f32_workspace_bytes(M, N, K) : 0;
   if (op == TERN_OP_GEMM_PACKED) return gemm_packed_workspace_bytes(M, N, K);
   if (op == TERN_OP_GEMM) return gemm_dense_workspace_bytes(M, N, K);
   return 0;
@@ -100,6 +115,7 @@ int tern_host_accessible(const void* host) {
 int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == TERN_OP_GEMV) return gemv_needs_fixup(M, N, K) ? 2 : 1;
+  if (op == TERN_OP_GEMV_F32) return gemv_needs_fixup(M, N, K) ? 3 : 2;
   if (op == TERN_OP_GEMM) return dense_splits(M, N, K) > 1 ? 2 : 1;
   if (op == TERN_OP_GEMM_PACKED) return packed_splits(M, N, K) > 1 ? 2 : 1;
   return 0;
@@ -215,6 +231,28 @@ tern_status tern_gemv_decode(const uint8_t* packed, const uint16_t* xh, const fl
   if (!aligned16(ws)) return TERN_ERR_ALIGN;
   if (!device_supported()) return TERN_ERR_UNSUPPORTED;
   return from_cuda(launch_gemv(packed, xh, xs, M, N, K, y, ws, static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_gemv_decode_f32(const uint8_t* packed, const float* xr, int64_t M, int64_t N,
+                                 int64_t K, uint16_t* y, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
+  if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
+  if (M > 16) return TERN_ERR_SHAPE;
+  if (N > (int64_t(1) << 30) / (K / 16)) return TERN_ERR_SHAPE;
+  if (M == 0 || N == 0) return TERN_OK;
+  if (packed == nullptr || xr == nullptr || y == nullptr) return TERN_ERR_INVALID_ARG;
+  if (!aligned16(packed) || !aligned16(xr) || !aligned16(y)) return TERN_ERR_ALIGN;
+  if (ws == nullptr || ws_bytes < gemv_f32_workspace_bytes(M, N, K)) return TERN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint16_t* xh = reinterpret_cast<uint16_t*>(base + gemv_f32_xh_offset(M, N, K));
+  float* aux = reinterpret_cast<float*>(base + gemv_f32_aux_offset(M, N, K));
+  const cudaError_t e = launch_quant_rotated(xr, M, K, TERN_FWHT_DECODE, xh, aux, st);
+  if (e != cudaSuccess) return TERN_ERR_CUDA;
+  return from_cuda(launch_gemv(packed, xh, aux, M, N, K, y, ws, st));
 }
 
 tern_status tern_linear_decode(const uint16_t* x, const int8_t* sign, const uint8_t* packed,

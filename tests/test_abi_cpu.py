@@ -115,6 +115,18 @@ def test_gemv_argument_errors(lib):
     assert _st("tern_gemv_decode", *args(ws_b=ws - 1)) == 6
     assert _st("tern_gemv_decode", *args(ws_ptr=None)) == 6
     assert _st("tern_gemv_decode", *args(m=0)) == 0
+    # the fp32-input sibling: a larger workspace (GEMV part, then the operand)
+    wf = B.tern_workspace_bytes(B.TERN_OP_GEMV_F32, 4, 256, 1024)
+    assert wf >= ws + 4 * 1024 * 2 + 8 * 192
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMV_F32, 17, 256, 1024) == 0
+    f32 = lambda m=4, k=1024, xr=FAKE, ws_b=wf, y=FAKE: (FAKE, xr, m, 256, k, y, FAKE, ws_b, None)
+    assert _st("tern_gemv_decode_f32", *f32(m=17)) == 2
+    assert _st("tern_gemv_decode_f32", *f32(k=1536)) == 2
+    assert _st("tern_gemv_decode_f32", *f32(xr=None)) == 1
+    assert _st("tern_gemv_decode_f32", *f32(xr=FAKE + 4)) == 3
+    assert _st("tern_gemv_decode_f32", *f32(ws_b=ws)) == 6
+    assert _st("tern_gemv_decode_f32", *f32(m=0)) == 0
+    assert _st("tern_gemv_decode_f32", *f32()) == 4            # valid, but no GPU here
 
 
 def test_gemm_argument_errors(lib):

@@ -169,3 +169,28 @@ def test_repack_in_place_then_decode_on_the_same_stream():
     B.tern_check()
     for it, y in enumerate(ys):
         assert torch.equal(y, ref[it % 2]), f"call {it} saw other weights"
+
+
+@pytest.mark.parametrize("layer,m", [(I.TINY, 3), (I.QKV, 4), (I.DOWN, 16), (I.GATE_UP, 1)])
+def test_f32_input_entry_point(layer, m):
+    """tern_gemv_decode_f32 (fp32 rotated activations in, the operand formed
+    in the workspace) is bit-identical to rotation -> tern_gemv_decode, and
+    within the decode tolerance of the oracle."""
+    d = I.make_layer(layer, m, seed=21)
+    lay = _layer(d.codes, d.scales)
+    x = to_dev_bf16(d.x_bits)
+    want = bf16_to_f32(B.decode(lay, x, B.Workspace()))
+    xr, _ = B.fwht(x, B.TERN_FWHT_F32)
+    n, k = layer.n, layer.k
+    ws = B.Workspace()
+    for _ in range(2):                       # twice: the GEMV part is left zero-filled
+        buf = ws.get(B.tern_workspace_bytes(B.TERN_OP_GEMV_F32, m, n, k))
+        y = poison(torch.empty((m, n), dtype=torch.bfloat16, device="cuda"))
+        B.tern_gemv_decode_f32(lay.packed, xr, m, n, k, y, buf, buf.numel())
+        B.tern_check()
+        got = bf16_to_f32(y)
+        assert np.array_equal(got, want)
+    rows = np.arange(n) if n <= 512 else block_sample_rows(n, seed=3, extra=128)
+    ref = O.linear_f64(d.x, d.codes[rows], d.scales[rows])
+    assert O.rel_frobenius(got[:, rows], ref) <= TOL
+    check_elementwise(got[:, rows], ref, d.codes[rows], d.scales[rows], d.x, what="f32 entry")
