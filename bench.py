@@ -493,7 +493,7 @@ def run_prefill(args, local, m=2048):
                                generator=g) - 1).to(torch.int8)
         scales = (0.02 * torch.randn((layer.n, layer.k // 128), device="cuda", generator=g).abs()
                   + 1e-3).to(torch.float16)
-        lay = B.pack_layer(codes, scales, decode=True, prefill=True)
+        lay = B.pack_layer(codes, scales, decode=True, prefill=True, int8=True)
         w_h = B.expand_fp16(codes, scales)
         del codes, scales
         x = _activations(layer, m, seed=77).cuda()
@@ -506,12 +506,12 @@ def run_prefill(args, local, m=2048):
         wsd = B.Workspace().scratch(nbd) if nbd else None
 
         def step():
-            B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_I8, xq, ts, st)
-            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y, None,
+            B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_I8H, xq, ts, st)
+            B.tern_gemm_prefill_int8h(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y, None,
                                      wsd, nbd, stream=st)
 
         def gemm_only():
-            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y, None,
+            B.tern_gemm_prefill_int8h(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y, None,
                                      wsd, nbd, stream=st)
 
         nbp = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, layer.n, layer.k)
@@ -520,6 +520,20 @@ def run_prefill(args, local, m=2048):
         def packed_only():
             B.tern_gemm_prefill_packed(xq, ts, lay.packed, lay.q, lay.rscale, m, layer.n,
                                        layer.k, y, None, wsp, nbp, stream=st)
+
+        # the int8-typed boundary: int8 xq and W_int8, widened in the workspace per call
+        xq8 = torch.empty((m, layer.k), dtype=torch.int8, device="cuda")
+        nb8 = B.tern_workspace_bytes(B.TERN_OP_GEMM_INT8, m, layer.n, layer.k)
+        ws8 = B.Workspace().scratch(nb8)
+
+        def int8_step():
+            B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_I8, xq8, ts, st)
+            B.tern_gemm_prefill_int8(xq8, ts, lay.w_int8, lay.rscale, m, layer.n, layer.k, y,
+                                     None, ws8, nb8, stream=st)
+
+        def int8_only():
+            B.tern_gemm_prefill_int8(xq8, ts, lay.w_int8, lay.rscale, m, layer.n, layer.k, y,
+                                     None, ws8, nb8, stream=st)
 
         xh = torch.empty((m, layer.k), dtype=torch.float16, device="cuda")
         xs = torch.empty((m, layer.k // 1024), dtype=torch.float32, device="cuda")
@@ -532,20 +546,24 @@ def run_prefill(args, local, m=2048):
             step()
             packed_only()
             fp16_only()
+            int8_step()
         torch.cuda.synchronize()
         n = 20
         t = _time_region(step, n, stream, 1)
         tg = _time_region(gemm_only, n, stream, 1)
         tp = _time_region(packed_only, n, stream, 1)
         th = _time_region(fp16_only, n, stream, 1)
+        t8 = _time_region(int8_step, n, stream, 1)
+        tg8 = _time_region(int8_only, n, stream, 1)
         B.tern_check(stream)
     ops = 2.0 * m * layer.n * layer.k
-    del lay, w_h
+    del lay, w_h, ws8
     torch.cuda.empty_cache()
     return {"metric": "prefill int8 TOPS (2*M*N*K / step time)", "value": round(ops * n / t / 1e12, 1),
             "unit": "TOPS", "workload": f"prefill gate/up 5120->34816, M={m}",
             "ms_per_step": round(t / n * 1e3, 4),
-            "roofline": {"bound": "tensor", "kernel": "tern_gemm_prefill_int8",
+            "roofline": {"bound": "tensor",
+                         "kernel": "tern_gemm_prefill_int8h (W_int8 held in fp16)",
                          "achieved": round(ops * n / tg / 1e12, 1), "peak": tc_peak,
                          "unit": "TFLOP/s", "frac": round(ops * n / tg / 1e12 / tc_peak, 4),
                          "avg_launch_us": round(tg / n * 1e6, 2),
@@ -561,6 +579,13 @@ def run_prefill(args, local, m=2048):
                        "avg_launch_us": round(tp / n * 1e6, 2),
                        "weight_bytes": layer.n * layer.k // 4 + layer.n * (layer.k // 128) * 3,
                        "expanded_weight_bytes": layer.n * layer.k * 2},
+            "int8_typed": {"kernel": "tern_gemm_prefill_int8 (int8 xq and W_int8; both "
+                                     "widened to fp16 in the workspace on every call)",
+                           "achieved": round(ops * n / tg8 / 1e12, 1), "unit": "TFLOP/s",
+                           "frac": round(ops * n / tg8 / 1e12 / tc_peak, 4),
+                           "avg_call_us": round(tg8 / n * 1e6, 2),
+                           "ms_per_step": round(t8 / n * 1e3, 4),
+                           "vs_fp16_held": round(tg / tg8, 4)},
             "fp16_variant": {"kernel": "tern_gemm_prefill_fp16 (decode operand x fp16 code*s, "
                                        "no int8 quantisation)",
                              "achieved": round(ops * n / th / 1e12, 1), "unit": "TFLOP/s",
@@ -602,7 +627,7 @@ def run_mid_m(args, local, ms=(32, 64, 128, 256, 512)):
                 def expanded():
                     l = lays[i[0] % copies]
                     i[0] += 1
-                    B.tern_gemm_prefill_int8(xq, ts, l.w_q, l.rscale, m, shp.n, shp.k, y, None,
+                    B.tern_gemm_prefill_int8h(xq, ts, l.w_q, l.rscale, m, shp.n, shp.k, y, None,
                                              wse, nbe, stream=st)
 
                 for f in (packed, expanded):
@@ -644,11 +669,11 @@ def run_prefill_configs(args, local, configs=((I.GATE_UP, 512), (I.DOWN, 512), (
             wsp = B.Workspace().scratch(nbp) if nbp else None
 
             def gemm():
-                B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y,
+                B.tern_gemm_prefill_int8h(xq, ts, lay.w_q, lay.rscale, m, layer.n, layer.k, y,
                                          None, wsd, nbd, stream=st)
 
             def step():
-                B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_I8, xq, ts, st)
+                B.tern_fwht_quant(x, m, layer.k, None, B.TERN_FWHT_I8H, xq, ts, st)
                 gemm()
 
             def packed():
@@ -814,14 +839,14 @@ def run_stack(args, local, n_layers=64, decode_ms=(1, 4, 8, 16), prefill_ms=(128
             def prefill_step(packed=False):
                 for row in layers:
                     for si, (shp, lay) in enumerate(zip(shapes, row)):
-                        B.tern_fwht_quant(xs_in[si], m, shp.k, None, B.TERN_FWHT_I8, xq[si],
+                        B.tern_fwht_quant(xs_in[si], m, shp.k, None, B.TERN_FWHT_I8H, xq[si],
                                           ts[si], st)
                         if packed:
                             B.tern_gemm_prefill_packed(xq[si], ts[si], lay.packed, lay.q,
                                                        lay.rscale, m, shp.n, shp.k, ys[si], None,
                                                        wsp, nbs[si], stream=st)
                         else:
-                            B.tern_gemm_prefill_int8(xq[si], ts[si], lay.w_q, lay.rscale, m,
+                            B.tern_gemm_prefill_int8h(xq[si], ts[si], lay.w_q, lay.rscale, m,
                                                      shp.n, shp.k, ys[si], None, wse, nbe[si],
                                                      stream=st)
 

@@ -115,15 +115,21 @@ size_t tern_packed_bytes(int64_t N, int64_t K);
  *   q              int8 [N][G]: rint((127*s)/smax) in fp32, half to even,
  *                  smax[n] = max_g |s[n,g]|; a zero row gives q = 0
  *   rscale         fp32 [N]: smax/127 (0 for a zero row)
- *   w_q            fp16 [N][K]: the exact int8 weight code*q[n,k/128], held in
- *                  fp16 (every integer in [-127,127] is exact in fp16) because
- *                  the sm_103a tensor cores multiply it exactly on the f16 path
- *                  and offer no fast int8 path; needs q and rscale non-NULL.
+ *   w_int8         int8 [N][K]: the exact int8 weight code*q[n,k/128] (section 4:
+ *                  it fits int8 exactly); needs q and rscale non-NULL.
  *                  q and rscale must be both NULL or both non-NULL.
  * Requirements: K % 1024 == 0, 1 <= K <= 65536, N >= 0.
  */
 tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
-                      uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q, void* stream);
+                      uint8_t* packed, int8_t* q, float* rscale, int8_t* w_int8, void* stream);
+
+/* tern_widen_int8 -- int8 [rows][cols] -> the same integers held in fp16
+ * (exact), the operand format of the sm_103a tensor cores' f16 kind (the
+ * chip has no tcgen05 int8 kind).  Used at load time for the fp16-held
+ * weight of tern_gemm_prefill_int8h.  Requirements: cols % 16 == 0;
+ * rows * cols < 2^40. */
+tern_status tern_widen_int8(const int8_t* src, int64_t rows, int64_t cols, uint16_t* dst,
+                            void* stream);
 
 /* ------------------------------------------------------------------------
  * tern_fwht_quant -- block Hadamard rotation of the activations (page
@@ -160,18 +166,20 @@ tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, in
  *          TERN_FWHT_F16:    out = fp16 [M][K], the fp16 prefill variant's
  *                 operand: fp16_rn(xr[m,k] * 2^sh[m,b]); out_scale = float
  *                 [M][B] holding 2^-sh[m,b] (exact); any M
- *          TERN_FWHT_I8:     out = fp16 [M][K] holding xq in [-127,127];
- *                 out_scale = float tscale[M]:
+ *          TERN_FWHT_I8:     out = int8 xq [M][K]; out_scale = float tscale[M]:
  *                 a = max_k |xr[m,k]|, tscale = a/127 (fp32),
  *                 xq = clamp(rint(xr / tscale), -127, 127) (fp32 division,
  *                 half to even); a == 0 gives xq = 0 and tscale = 0.
- * Requirements: K % 1024 == 0, K <= 65536 (K <= 32768 in TERN_FWHT_I8 mode),
+ *          TERN_FWHT_I8H:    the same xq held in fp16 [M][K] (exact), the
+ *                 operand of tern_gemm_prefill_int8h and _packed.
+ * Requirements: K % 1024 == 0, K <= 65536 (K <= 32768 in the two int8 modes),
  * M >= 0 (M <= 16 in TERN_FWHT_DECODE mode); `sign` may be unaligned.
  * ---------------------------------------------------------------------- */
 #define TERN_FWHT_F32 0
 #define TERN_FWHT_DECODE 1
 #define TERN_FWHT_I8 2
 #define TERN_FWHT_F16 3
+#define TERN_FWHT_I8H 4
 tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign,
                             int mode, void* out, float* out_scale, void* stream);
 
@@ -212,8 +220,8 @@ tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_
  * tern_quant_rotated -- quantise rotated fp32 activations xr [M][K]
  *   (K % 1024 == 0) exactly as tern_fwht_quant does after its rotation:
  *   mode TERN_FWHT_DECODE (the decode GEMV's operand, M <= 16),
- *   TERN_FWHT_F16 (fp16 + per-block factors) or TERN_FWHT_I8 (xq +
- *   per-token tscale).  After a K split each rank quantises its own padded
+ *   TERN_FWHT_F16 (fp16 + per-block factors), TERN_FWHT_I8 (int8 xq +
+ *   per-token tscale) or TERN_FWHT_I8H (the same xq held in fp16).  After a K split each rank quantises its own padded
  *   shard (per-token int8 scales are the rank's own).
  * ---------------------------------------------------------------------- */
 tern_status tern_fwht_shard(const uint16_t* x, int64_t M, int64_t Kr, int lead, int trail,
@@ -342,13 +350,37 @@ tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uint16_t* xh, 
  * tern_gemm_prefill_int8 -- the int8 prefill GEMM of page section 4:
  *     acc[m,n] = sum_k xq[m,k] * W_int8[n,k]            (exact int32)
  *     y[m,n]   = bf16_rn(((float)acc[m,n] * tscale[m]) * rscale[n])
- * The operands hold int8 values in fp16 (see tern_pack / tern_fwht_quant);
- * the tcgen05 tensor cores multiply them exactly and the kernel keeps every
- * fp32 partial sum below 2^24 (1024-wide chunks, then int32), so acc is
- * bit-exact.
+ * on int8 operands.  sm_103a's tensor cores have no int8 kind, so the call
+ * holds both operands' integers in fp16 in its workspace (exact), then runs
+ * the tcgen05 GEMM of tern_gemm_prefill_int8h on them; the f16 kind
+ * multiplies them exactly and the kernel keeps every fp32 partial sum below
+ * 2^24 (1024-wide chunks, then int32), so acc is bit-exact.
  *
- *   xq      fp16 [M][K] (TERN_FWHT_I8 output), tscale fp32 [M]
- *   w_q     fp16 [N][K] (tern_pack output),    rscale fp32 [N]
+ *   xq      int8 [M][K] (TERN_FWHT_I8 output), tscale fp32 [M]
+ *   w_int8  int8 [N][K] (tern_pack output),    rscale fp32 [N]
+ *   y       bf16 [M][N]
+ *   acc     int32 [M][N] or NULL
+ *   ws      device workspace (any contents) of at least
+ *           tern_workspace_bytes(TERN_OP_GEMM_INT8, M, N, K) bytes: the two
+ *           fp16 operand copies, then the K-split pieces of
+ *           tern_gemm_prefill_int8h.  It is required.
+ * Requirements and errors as for tern_gemm_prefill_int8h (TERN_ERR_WORKSPACE
+ * for a missing or small workspace).  A caller that keeps the fp16-held
+ * weight (tern_widen_int8, twice the bytes) saves the weight's widening on
+ * every call by calling tern_gemm_prefill_int8h directly.
+ * ---------------------------------------------------------------------- */
+tern_status tern_gemm_prefill_int8(const int8_t* xq, const float* tscale, const int8_t* w_int8,
+                                   const float* rscale, int64_t M, int64_t N, int64_t K,
+                                   uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* ------------------------------------------------------------------------
+ * tern_gemm_prefill_int8h -- the same GEMM on the int8 integers held in fp16
+ * (tcgen05.mma kind::f16, TMA-fed, TMEM accumulators, fused rescale):
+ *
+ *   xq      fp16 [M][K] holding xq (TERN_FWHT_I8H output), tscale fp32 [M]
+ *   w_q     fp16 [N][K] holding W_int8 (tern_widen_int8 of tern_pack's
+ *           w_int8), rscale fp32 [N]
  *   y       bf16 [M][N]
  *   acc     int32 [M][N] or NULL
  *   ws      optional device workspace (any contents) of
@@ -365,10 +397,10 @@ tern_status tern_gemv_decode_noalloc(const uint8_t* packed, const uint16_t* xh, 
  * Device-side waits are bounded; a wait that gives up makes the call's
  * outputs undefined and is reported by tern_check().
  * ---------------------------------------------------------------------- */
-tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
-                                   const float* rscale, int64_t M, int64_t N, int64_t K,
-                                   uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
-                                   void* stream);
+tern_status tern_gemm_prefill_int8h(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
+                                    const float* rscale, int64_t M, int64_t N, int64_t K,
+                                    uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
+                                    void* stream);
 
 /* ------------------------------------------------------------------------
  * tern_gemm_prefill_packed -- the same int8 prefill GEMM (page section 4)
@@ -385,7 +417,7 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
  * per token block, so mid-size M costs the packed bytes instead of the
  * 2-byte expanded weight.
  *
- *   xq      fp16 [M][K] (TERN_FWHT_I8 output), tscale fp32 [M]
+ *   xq      fp16 [M][K] holding xq (TERN_FWHT_I8H output), tscale fp32 [M]
  *   packed  tern_pack's `packed` output (tern_packed_bytes(N, K) bytes)
  *   q       int8 [N][G] and rscale fp32 [N] (tern_pack outputs)
  *   y       bf16 [M][N]
@@ -438,6 +470,7 @@ tern_status tern_gemm_prefill_fp16(const uint16_t* xh, const float* xs, const ui
 #define TERN_OP_GEMM 2
 #define TERN_OP_GEMM_PACKED 3
 #define TERN_OP_GEMV_F32 4
+#define TERN_OP_GEMM_INT8 5
 size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
 /* 1 if the GPU current on this thread can load and store `host` directly
  * at that same address -- a pinned host buffer mapped into the device's
@@ -454,8 +487,9 @@ int tern_host_accessible(const void* host);
  * GEMV sums in place (tern_gemv_decode, tern_linear_decode and
  * tern_gemv_decode_noalloc launch the same count); for TERN_OP_GEMV_F32 one
  * more (the operand's quantisation kernel); for TERN_OP_GEMM the
- * int8 (or fp16) GEMM, plus its finishing kernel when it is given the
- * workspace and splits K; for TERN_OP_GEMM_PACKED the GEMM, plus the
+ * int8h (or fp16) GEMM, plus its finishing kernel when it is given the
+ * workspace and splits K; for TERN_OP_GEMM_INT8 two more (the operands'
+ * widening); for TERN_OP_GEMM_PACKED the GEMM, plus the
  * rescale kernel when its tiles are split along K.  Host-only; launch
  * counting for CUDA-graph sizing and profiling. */
 int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K);

@@ -34,10 +34,12 @@ TERN_FWHT_F32 = 0
 TERN_FWHT_DECODE = 1
 TERN_FWHT_I8 = 2
 TERN_FWHT_F16 = 3
+TERN_FWHT_I8H = 4
 TERN_OP_GEMV = 1
 TERN_OP_GEMM = 2
 TERN_OP_GEMM_PACKED = 3
 TERN_OP_GEMV_F32 = 4
+TERN_OP_GEMM_INT8 = 5
 STATUS_NAMES = {0: "TERN_OK", 1: "TERN_ERR_INVALID_ARG", 2: "TERN_ERR_SHAPE", 3: "TERN_ERR_ALIGN",
                 4: "TERN_ERR_UNSUPPORTED", 5: "TERN_ERR_CUDA", 6: "TERN_ERR_WORKSPACE",
                 7: "TERN_ERR_TIMEOUT"}
@@ -62,8 +64,11 @@ _SIGS = {
                                        _p]),
     "tern_fwht_combine": (ctypes.c_int, [_p, _p, _i64, ctypes.c_int, _p, _i64, _i64, _p]),
     "tern_quant_rotated": (ctypes.c_int, [_p, _i64, _i64, ctypes.c_int, _p, _p, _p]),
+    "tern_widen_int8": (ctypes.c_int, [_p, _i64, _i64, _p, _p]),
     "tern_gemm_prefill_int8": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _p, _sz,
                                               _p]),
+    "tern_gemm_prefill_int8h": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _p, _sz,
+                                               _p]),
     "tern_gemm_prefill_packed": (ctypes.c_int, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _p,
                                                 _p, _sz, _p]),
     "tern_check": (ctypes.c_int, [_p]),
@@ -160,9 +165,13 @@ def tern_workspace_init(ws, nbytes: int | None = None, stream=None):
     return _call("tern_workspace_init", _ptr(ws), nb, _stream(stream))
 
 
-def tern_pack(codes, scales, n, k, packed, q, rscale, w_q, stream=None):
+def tern_pack(codes, scales, n, k, packed, q, rscale, w_int8, stream=None):
     return _call("tern_pack", _ptr(codes), _ptr(scales), n, k, _ptr(packed), _ptr(q),
-                 _ptr(rscale), _ptr(w_q), _stream(stream))
+                 _ptr(rscale), _ptr(w_int8), _stream(stream))
+
+
+def tern_widen_int8(src, rows, cols, dst, stream=None):
+    return _call("tern_widen_int8", _ptr(src), rows, cols, _ptr(dst), _stream(stream))
 
 
 def tern_fwht_quant(x, m, k, sign, mode, out, out_scale, stream=None):
@@ -175,10 +184,16 @@ def tern_gemv_decode(packed, xh, xs, m, n, k, y, ws, ws_bytes, stream=None):
                  ws_bytes, _stream(stream))
 
 
-def tern_gemm_prefill_int8(xq, tscale, w_q, rscale, m, n, k, y, acc=None, ws=None, ws_bytes=0,
-                           stream=None):
-    return _call("tern_gemm_prefill_int8", _ptr(xq), _ptr(tscale), _ptr(w_q), _ptr(rscale), m, n,
-                 k, _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream))
+def tern_gemm_prefill_int8(xq, tscale, w_int8, rscale, m, n, k, y, acc=None, ws=None,
+                           ws_bytes=0, stream=None):
+    return _call("tern_gemm_prefill_int8", _ptr(xq), _ptr(tscale), _ptr(w_int8), _ptr(rscale), m,
+                 n, k, _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def tern_gemm_prefill_int8h(xq, tscale, w_q, rscale, m, n, k, y, acc=None, ws=None, ws_bytes=0,
+                            stream=None):
+    return _call("tern_gemm_prefill_int8h", _ptr(xq), _ptr(tscale), _ptr(w_q), _ptr(rscale), m,
+                 n, k, _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream))
 
 
 def tern_gemm_prefill_packed(xq, tscale, packed, q, rscale, m, n, k, y, acc=None, ws=None,
@@ -261,7 +276,8 @@ class PackedLayer:
     packed: torch.Tensor | None         # uint8, codes + scales in 17408-byte units
     q: torch.Tensor | None              # int8 [N, G]
     rscale: torch.Tensor | None         # float32 [N]
-    w_q: torch.Tensor | None            # float16 [N, K]
+    w_q: torch.Tensor | None            # float16 [N, K] holding W_int8 (exact)
+    w_int8: torch.Tensor | None = None  # int8 [N, K]
 
     @property
     def weight_bytes(self) -> int:
@@ -270,25 +286,32 @@ class PackedLayer:
 
 
 def pack_layer(codes: torch.Tensor, scales: torch.Tensor, decode: bool = True,
-               prefill: bool = True, expand: bool = True, stream=None) -> PackedLayer:
+               prefill: bool = True, expand: bool = True, int8: bool = False,
+               stream=None) -> PackedLayer:
     """Run tern_pack on device codes (int8 [N,K]) and scales (fp16 [N,G]).
     ``decode`` keeps the packed 2-bit units, ``prefill`` the scale split
-    (q, rscale) and, with ``expand``, the expanded int8 weight w_q; without
-    w_q, prefill reads the packed units (tern_gemm_prefill_packed)."""
+    (q, rscale); with ``expand`` the layer also keeps W_int8 held in fp16
+    (w_q, tern_widen_int8 of tern_pack's int8 weight), the operand of
+    tern_gemm_prefill_int8h, and with ``int8`` the int8 weight itself
+    (w_int8, for tern_gemm_prefill_int8).  Without either, prefill reads
+    the packed units (tern_gemm_prefill_packed)."""
     _need(codes, torch.int8, "codes")
     _need(scales, torch.float16, "scales")
     n, k = codes.shape
     dev = codes.device
-    packed = q = rs = wq = None
+    packed = q = rs = wq = w8 = None
     if decode:
         packed = torch.empty(tern_packed_bytes(n, k), dtype=torch.uint8, device=dev)
     if prefill:
         q = torch.empty((n, k // 128), dtype=torch.int8, device=dev)
         rs = torch.empty(n, dtype=torch.float32, device=dev)
-        if expand:
-            wq = torch.empty((n, k), dtype=torch.float16, device=dev)
-    tern_pack(codes, scales, n, k, packed, q, rs, wq, stream)
-    return PackedLayer(n, k, packed, q, rs, wq)
+        if expand or int8:
+            w8 = torch.empty((n, k), dtype=torch.int8, device=dev)
+    tern_pack(codes, scales, n, k, packed, q, rs, w8, stream)
+    if expand and w8 is not None:
+        wq = torch.empty((n, k), dtype=torch.float16, device=dev)
+        tern_widen_int8(w8, n, k, wq, stream)
+    return PackedLayer(n, k, packed, q, rs, wq, w8 if int8 else None)
 
 
 def decode_aux(k: int, device="cuda") -> torch.Tensor:
@@ -311,7 +334,8 @@ def fwht(x: torch.Tensor, mode: int, sign: torch.Tensor | None = None, stream=No
         out = torch.empty((m, k), dtype=torch.float16, device=dev)
         sc = torch.empty((m, k // 1024), dtype=torch.float32, device=dev)
     else:
-        out = torch.empty((m, k), dtype=torch.float16, device=dev)
+        dt = torch.int8 if mode == TERN_FWHT_I8 else torch.float16
+        out = torch.empty((m, k), dtype=dt, device=dev)
         sc = torch.empty(m, dtype=torch.float32, device=dev)
     tern_fwht_quant(x, m, k, sign, mode, out, sc, stream)
     return out, sc
@@ -515,26 +539,36 @@ def prefill(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,
             acc: torch.Tensor | None = None, sign=None, stream=None,
             from_packed: bool | None = None, ws: Workspace | None = None) -> torch.Tensor:
     """Prefill forward: rotation + per-token int8 quantisation, then the int8
-    GEMM, on the expanded weight w_q or (``from_packed``; the default when
-    the layer holds no w_q) straight from the packed units.  Both GEMMs give
-    bit-identical results."""
+    GEMM -- straight from the packed units (``from_packed``; the default when
+    the layer holds no expanded weight), on the fp16-held weight w_q, or on
+    the int8 weight w_int8 (int8-typed operands, tern_gemm_prefill_int8).
+    All three give bit-identical results."""
     m = x.shape[0]
     if from_packed is None:
-        from_packed = layer.w_q is None
-    xq, ts = fwht(x, TERN_FWHT_I8, sign, stream)
+        from_packed = layer.w_q is None and layer.w_int8 is None
+    ws = ws or Workspace(x.device)
     if y is None:
         y = torch.empty((m, layer.n), dtype=torch.bfloat16, device=x.device)
-    if from_packed:
-        nb = tern_workspace_bytes(TERN_OP_GEMM_PACKED, m, layer.n, layer.k)
-        buf = (ws or Workspace(x.device)).scratch(nb, stream) if nb > 0 else None
-        tern_gemm_prefill_packed(xq, ts, layer.packed, layer.q, layer.rscale, m, layer.n,
-                                 layer.k, y, acc, buf, 0 if buf is None else buf.numel(),
-                                 stream=stream)
-    else:
-        nb = tern_workspace_bytes(TERN_OP_GEMM, m, layer.n, layer.k)
-        buf = (ws or Workspace(x.device)).scratch(nb, stream) if nb > 0 else None
-        tern_gemm_prefill_int8(xq, ts, layer.w_q, layer.rscale, m, layer.n, layer.k, y, acc,
-                               buf, nb, stream=stream)
+    if from_packed or layer.w_q is not None:
+        xq, ts = fwht(x, TERN_FWHT_I8H, sign, stream)
+        op = TERN_OP_GEMM_PACKED if from_packed else TERN_OP_GEMM
+        nb = tern_workspace_bytes(op, m, layer.n, layer.k)
+        buf = ws.scratch(nb, stream) if nb > 0 else None
+        nb = 0 if buf is None else buf.numel()
+        if from_packed:
+            tern_gemm_prefill_packed(xq, ts, layer.packed, layer.q, layer.rscale, m, layer.n,
+                                     layer.k, y, acc, buf, nb, stream=stream)
+        else:
+            tern_gemm_prefill_int8h(xq, ts, layer.w_q, layer.rscale, m, layer.n, layer.k, y, acc,
+                                    buf, nb, stream=stream)
+        return y
+    if layer.w_int8 is None:
+        raise ValueError("prefill needs packed units, w_q or w_int8")
+    xq, ts = fwht(x, TERN_FWHT_I8, sign, stream)
+    nb = tern_workspace_bytes(TERN_OP_GEMM_INT8, m, layer.n, layer.k)
+    buf = ws.scratch(nb, stream)
+    tern_gemm_prefill_int8(xq, ts, layer.w_int8, layer.rscale, m, layer.n, layer.k, y, acc, buf,
+                           buf.numel(), stream=stream)
     return y
 
 
@@ -553,6 +587,7 @@ def forward(layer: PackedLayer, x: torch.Tensor, y: torch.Tensor | None = None,
         return decode(layer, x, ws, y=y, sign=sign, stream=stream)
     if layer.q is None:
         raise ValueError("prefill needs the layer packed with prefill=True (q, rscale)")
-    from_packed = layer.packed is not None and (layer.w_q is None or m <= 256)
+    from_packed = layer.packed is not None and (
+        (layer.w_q is None and layer.w_int8 is None) or m <= 256)
     return prefill(layer, x, y=y, sign=sign, stream=stream, from_packed=from_packed, ws=ws)
 

@@ -61,10 +61,40 @@ __global__ void __launch_bounds__(128) fwht_block_kernel(const uint16_t* __restr
 // token's absmax, then quantises and writes its own block: no shared-memory
 // copy of the token, and every warp loads at once.  Launch bounds: up to 18
 // blocks (K <= 18432) two CTAs per SM (registers capped at 56), else one.
-template <int MAX_THREADS, int MIN_CTAS>
+// The quantised values of 8 consecutive elements: int8 (TERN_FWHT_I8), or the
+// same integers held in fp16 (TERN_FWHT_I8H, the tensor cores' operand).
+__device__ __forceinline__ void store_q8(int8_t* p, const float (&q)[8]) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int t = 0; t < 8; ++t)
+    w[t >> 2] |= (static_cast<uint32_t>(static_cast<int>(q[t])) & 0xffu) << (8 * (t & 3));
+  *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+}
+__device__ __forceinline__ void store_q8(__half* p, const float (&q)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    __half2 h2 = __floats2half2_rn(q[2 * t], q[2 * t + 1]);   // integers in [-127,127]: exact
+    w[t] = *reinterpret_cast<uint32_t*>(&h2);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void store_q4(int8_t* p, const float (&q)[4]) {
+  uint32_t w = 0u;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) w |= (static_cast<uint32_t>(static_cast<int>(q[t])) & 0xffu) << (8 * t);
+  *reinterpret_cast<uint32_t*>(p) = w;
+}
+__device__ __forceinline__ void store_q4(__half* p, const float (&q)[4]) {
+  __half2 a = __floats2half2_rn(q[0], q[1]), b = __floats2half2_rn(q[2], q[3]);
+  *reinterpret_cast<uint2*>(p) =
+      make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+}
+
+template <int MAX_THREADS, int MIN_CTAS, typename OutT>
 __global__ void __launch_bounds__(MAX_THREADS, MIN_CTAS)
     fwht_i8_reg_kernel(const uint16_t* __restrict__ x, int M, int K,
-                       const int8_t* __restrict__ sign, __half* __restrict__ xq,
+                       const int8_t* __restrict__ sign, OutT* __restrict__ xq,
                        float* __restrict__ tscale) {
   __shared__ float red[32];
   const int lane = threadIdx.x & 31;
@@ -90,21 +120,14 @@ __global__ void __launch_bounds__(MAX_THREADS, MIN_CTAS)
   const float ts = __fdiv_rn(a, 127.0f);
   const bool nz = ts > 0.f;
   if (threadIdx.x == 0) tscale[m] = nz ? ts : 0.f;
-  __half* ob = xq + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock;
+  OutT* ob = xq + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock;
 #pragma unroll
   for (int ih = 0; ih < 4; ++ih) {
-    uint32_t w[4];
+    float qv[8];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      float q0 = 0.f, q1 = 0.f;
-      if (nz) {
-        q0 = fminf(fmaxf(rintf(__fdiv_rn(v[ih][2 * t], ts)), -127.f), 127.f);
-        q1 = fminf(fmaxf(rintf(__fdiv_rn(v[ih][2 * t + 1], ts)), -127.f), 127.f);
-      }
-      __half2 h2 = __floats2half2_rn(q0, q1);   // integers in [-127,127]: exact
-      w[t] = *reinterpret_cast<uint32_t*>(&h2);
-    }
-    *reinterpret_cast<uint4*>(ob + ih * 256 + lane * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int t = 0; t < 8; ++t)
+      qv[t] = nz ? fminf(fmaxf(rintf(__fdiv_rn(v[ih][t], ts)), -127.f), 127.f) : 0.f;
+    store_q8(ob + ih * 256 + lane * 8, qv);
   }
 }
 
@@ -231,8 +254,9 @@ __global__ void __launch_bounds__(128) quant_block_kernel(const float* __restric
 
 // Per-token int8 quantisation of already rotated fp32 activations (the
 // arithmetic of fwht_i8_reg_kernel); one CTA per token, two passes over the row.
+template <typename OutT>
 __global__ void __launch_bounds__(256) quant_i8_kernel(const float* __restrict__ xr, int M, int K,
-                                                       __half* __restrict__ xq,
+                                                       OutT* __restrict__ xq,
                                                        float* __restrict__ tscale) {
   __shared__ float red[8];
   const int lane = threadIdx.x & 31;
@@ -255,22 +279,15 @@ __global__ void __launch_bounds__(256) quant_i8_kernel(const float* __restrict__
   const float ts = __fdiv_rn(a, 127.0f);
   const bool nz = ts > 0.f;
   if (threadIdx.x == 0) tscale[m] = nz ? ts : 0.f;
-  __half* om = xq + static_cast<long>(m) * K;
+  OutT* om = xq + static_cast<long>(m) * K;
   for (int i = threadIdx.x * 4; i < K; i += 256 * 4) {
     const float4 p = reinterpret_cast<const float4*>(xm + i)[0];
     const float vv[4] = {p.x, p.y, p.z, p.w};
-    uint32_t w[2];
+    float qv[4];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      float q0 = 0.f, q1 = 0.f;
-      if (nz) {
-        q0 = fminf(fmaxf(rintf(__fdiv_rn(vv[2 * t], ts)), -127.f), 127.f);
-        q1 = fminf(fmaxf(rintf(__fdiv_rn(vv[2 * t + 1], ts)), -127.f), 127.f);
-      }
-      __half2 h2 = __floats2half2_rn(q0, q1);
-      w[t] = *reinterpret_cast<uint32_t*>(&h2);
-    }
-    *reinterpret_cast<uint2*>(om + i) = make_uint2(w[0], w[1]);
+    for (int t = 0; t < 4; ++t)
+      qv[t] = nz ? fminf(fmaxf(rintf(__fdiv_rn(vv[t], ts)), -127.f), 127.f) : 0.f;
+    store_q4(om + i, qv);
   }
 }
 
@@ -297,7 +314,10 @@ cudaError_t launch_fwht_combine(const float* h_first, const float* h_second, int
 cudaError_t launch_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, void* out,
                                  float* out_scale, cudaStream_t st) {
   if (mode == TERN_FWHT_I8)
-    return launch(quant_i8_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, st, xr,
+    return launch(quant_i8_kernel<int8_t>, dim3(static_cast<unsigned>(M)), dim3(256), 0, st, xr,
+                  static_cast<int>(M), static_cast<int>(K), static_cast<int8_t*>(out), out_scale);
+  if (mode == TERN_FWHT_I8H)
+    return launch(quant_i8_kernel<__half>, dim3(static_cast<unsigned>(M)), dim3(256), 0, st, xr,
                   static_cast<int>(M), static_cast<int>(K), static_cast<__half*>(out), out_scale);
   const long warps = M * (K / kHBlock);
   const dim3 grid(static_cast<unsigned>((warps + 3) / 4));
@@ -311,14 +331,19 @@ cudaError_t launch_quant_rotated(const float* xr, int64_t M, int64_t K, int mode
 cudaError_t launch_fwht(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign, int mode,
                         void* out, float* out_scale, cudaStream_t st) {
   const int m = static_cast<int>(M), k = static_cast<int>(K);
-  if (mode == TERN_FWHT_I8) {
-    // the entry point admits K <= 32768 in this mode: at most 32 warps
+  if (mode == TERN_FWHT_I8 || mode == TERN_FWHT_I8H) {
+    // the entry point admits K <= 32768 in these modes: at most 32 warps
     const unsigned threads = static_cast<unsigned>(32 * (K / kHBlock));
-    if (K <= 18 * kHBlock)
-      return launch(fwht_i8_reg_kernel<576, 2>, dim3(m), dim3(threads), 0, st, x, m, k, sign,
-                    static_cast<__half*>(out), out_scale);
-    return launch(fwht_i8_reg_kernel<1024, 1>, dim3(m), dim3(threads), 0, st, x, m, k, sign,
-                  static_cast<__half*>(out), out_scale);
+    const bool small = K <= 18 * kHBlock;
+    if (mode == TERN_FWHT_I8)
+      return small ? launch(fwht_i8_reg_kernel<576, 2, int8_t>, dim3(m), dim3(threads), 0, st, x,
+                            m, k, sign, static_cast<int8_t*>(out), out_scale)
+                   : launch(fwht_i8_reg_kernel<1024, 1, int8_t>, dim3(m), dim3(threads), 0, st,
+                            x, m, k, sign, static_cast<int8_t*>(out), out_scale);
+    return small ? launch(fwht_i8_reg_kernel<576, 2, __half>, dim3(m), dim3(threads), 0, st, x, m,
+                          k, sign, static_cast<__half*>(out), out_scale)
+                 : launch(fwht_i8_reg_kernel<1024, 1, __half>, dim3(m), dim3(threads), 0, st, x,
+                          m, k, sign, static_cast<__half*>(out), out_scale);
   }
   const long warps = M * (K / kHBlock);
   const dim3 grid(static_cast<unsigned>((warps + 3) / 4));

@@ -7,7 +7,8 @@
 // section 4 (q[n,g] = round(127 s[n,g] / smax[n]); W_int8[n,k] =
 // code[n,k] q[n,k/128] fits int8 exactly).  Expanding the weights to int8
 // once here, instead of on every prefill step, removes the run-time weight
-// expansion that section 6 measures at 31 of 83 ms of ternary-linear time.
+// expansion that section 6 measures at 31 of 83 ms of ternary-linear time;
+// widen_kernel holds int8 values in fp16 for the tensor cores' f16 kind.
 // The packed unit format is defined in include/tern.h.
 #include <cuda_fp16.h>
 
@@ -90,9 +91,10 @@ __global__ void scale_decomp_kernel(const uint16_t* __restrict__ scales, int N, 
   if (lane == 0) rscale[row] = smax > 0.f ? __fdiv_rn(smax, 127.0f) : 0.f;
 }
 
-// One thread per 8 consecutive elements of a row: w_q = code * q (exact in fp16).
-__global__ void wq_kernel(const int8_t* __restrict__ codes, const int8_t* __restrict__ q, int N,
-                          int K, __half* __restrict__ wq, long n_vec) {
+// One thread per 8 consecutive elements of a row: W_int8 = code * q, exact in
+// int8 (|code q| <= 127).
+__global__ void w8_kernel(const int8_t* __restrict__ codes, const int8_t* __restrict__ q, int N,
+                          int K, int8_t* __restrict__ w8, long n_vec) {
   pdl_wait();
   pdl_launch_dependents();
   const int G = K / kGroup;
@@ -101,17 +103,32 @@ __global__ void wq_kernel(const int8_t* __restrict__ codes, const int8_t* __rest
     const long e0 = vi * 8;
     const long row = e0 / K;
     const int k = static_cast<int>(e0 % K);
-    const float qq = static_cast<float>(q[row * G + k / kGroup]);
+    const int qq = q[row * G + k / kGroup];
     const uint2 cw = *reinterpret_cast<const uint2*>(codes + e0);
+    const int8_t* cb = reinterpret_cast<const int8_t*>(&cw);
+    int8_t v[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) v[t] = static_cast<int8_t>(cb[t] * qq);
+    *reinterpret_cast<uint2*>(w8 + e0) = *reinterpret_cast<const uint2*>(v);
+  }
+}
+
+// One thread per 8 consecutive int8 values: the same integers held in fp16
+// (exact), the operand format of the tensor-core GEMM.
+__global__ void widen_kernel(const int8_t* __restrict__ src, __half* __restrict__ dst, long n_vec) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (long vi = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; vi < n_vec;
+       vi += static_cast<long>(gridDim.x) * blockDim.x) {
+    const uint2 cw = *reinterpret_cast<const uint2*>(src + vi * 8);
     const int8_t* cb = reinterpret_cast<const int8_t*>(&cw);
     uint32_t w[4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      __half2 h = __floats2half2_rn(static_cast<float>(cb[2 * t]) * qq,
-                                    static_cast<float>(cb[2 * t + 1]) * qq);
+      __half2 h = __floats2half2_rn(static_cast<float>(cb[2 * t]), static_cast<float>(cb[2 * t + 1]));
       w[t] = *reinterpret_cast<uint32_t*>(&h);
     }
-    *reinterpret_cast<uint4*>(wq + e0) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(dst + vi * 8) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -154,8 +171,14 @@ cudaError_t launch_expand_fp16(const int8_t* codes, const uint16_t* scales, int6
                 reinterpret_cast<__half*>(w_h), n_vec);
 }
 
+cudaError_t launch_widen_int8(const int8_t* src, int64_t count, uint16_t* dst, cudaStream_t st) {
+  const long n_vec = count / 8;
+  return launch(widen_kernel, dim3(grid_for(n_vec, 256)), dim3(256), 0, st, src,
+                reinterpret_cast<__half*>(dst), n_vec);
+}
+
 cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
-                        uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q,
+                        uint8_t* packed, int8_t* q, float* rscale, int8_t* w_int8,
                         cudaStream_t st) {
   const int n = static_cast<int>(N), k = static_cast<int>(K), G = static_cast<int>(K / kGroup);
   cudaError_t e = cudaSuccess;
@@ -169,10 +192,10 @@ cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, 
     e = launch(scale_decomp_kernel, dim3(static_cast<unsigned>((N + 7) / 8)), dim3(256), 0, st,
                scales, n, G, q, rscale);
     if (e != cudaSuccess) return e;
-    if (w_q != nullptr) {
+    if (w_int8 != nullptr) {
       const long n_vec = N * K / 8;
-      e = launch(wq_kernel, dim3(grid_for(n_vec, 256)), dim3(256), 0, st, codes,
-                 static_cast<const int8_t*>(q), n, k, reinterpret_cast<__half*>(w_q), n_vec);
+      e = launch(w8_kernel, dim3(grid_for(n_vec, 256)), dim3(256), 0, st, codes,
+                 static_cast<const int8_t*>(q), n, k, w_int8, n_vec);
     }
   }
   return e;

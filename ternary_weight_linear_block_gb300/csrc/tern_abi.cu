@@ -51,6 +51,17 @@ size_t gemv_f32_aux_offset(int64_t M, int64_t N, int64_t K) {
 size_t gemv_f32_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return gemv_f32_aux_offset(M, N, K) + static_cast<size_t>(K / kGroup) * 192;
 }
+// Workspace of tern_gemm_prefill_int8: the fp16-held xq, the fp16-held
+// weight, then the K-split pieces of the GEMM, each part 256-byte aligned.
+size_t gemm_int8_w_offset(int64_t M, int64_t N, int64_t K) {
+  return align256(static_cast<size_t>(M) * K * 2);
+}
+size_t gemm_int8_split_offset(int64_t M, int64_t N, int64_t K) {
+  return gemm_int8_w_offset(M, N, K) + align256(static_cast<size_t>(N) * K * 2);
+}
+size_t gemm_int8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return gemm_int8_split_offset(M, N, K) + gemm_dense_workspace_bytes(M, N, K);
+}
 
 }  // namespace
 
@@ -81,6 +92,7 @@ size_t tern_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == TERN_OP_GEMV) return gemv_workspace_bytes(M, N, K);
   if (op == TERN_OP_GEMV_F32) return M <= 16 ? gemv_f32_workspace_bytes(M, N, K) : 0;
+  if (op == TERN_OP_GEMM_INT8) return gemm_int8_workspace_bytes(M, N, K);
   if (op == TERN_OP_GEMM_PACKED) return gemm_packed_workspace_bytes(M, N, K);
   if (op == TERN_OP_GEMM) return gemm_dense_workspace_bytes(M, N, K);
   return 0;
@@ -117,6 +129,7 @@ int tern_kernel_launches(int op, int64_t M, int64_t N, int64_t K) {
   if (op == TERN_OP_GEMV) return gemv_needs_fixup(M, N, K) ? 2 : 1;
   if (op == TERN_OP_GEMV_F32) return gemv_needs_fixup(M, N, K) ? 3 : 2;
   if (op == TERN_OP_GEMM) return dense_splits(M, N, K) > 1 ? 2 : 1;
+  if (op == TERN_OP_GEMM_INT8) return dense_splits(M, N, K) > 1 ? 4 : 3;
   if (op == TERN_OP_GEMM_PACKED) return packed_splits(M, N, K) > 1 ? 2 : 1;
   return 0;
 }
@@ -128,7 +141,7 @@ tern_status tern_workspace_init(void* ws, size_t bytes, void* stream) {
 }
 
 tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
-                      uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q, void* stream) {
+                      uint8_t* packed, int8_t* q, float* rscale, int8_t* w_q, void* stream) {
   if (N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
   if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
   if ((q == nullptr) != (rscale == nullptr)) return TERN_ERR_INVALID_ARG;
@@ -145,13 +158,25 @@ tern_status tern_pack(const int8_t* codes, const uint16_t* scales, int64_t N, in
                                static_cast<cudaStream_t>(stream)));
 }
 
+tern_status tern_widen_int8(const int8_t* src, int64_t rows, int64_t cols, uint16_t* dst,
+                            void* stream) {
+  if (rows < 0 || cols < 0) return TERN_ERR_INVALID_ARG;
+  if (cols % 16 != 0 || (rows > 0 && cols > (int64_t(1) << 40) / rows)) return TERN_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return TERN_OK;
+  if (src == nullptr || dst == nullptr) return TERN_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  return from_cuda(launch_widen_int8(src, rows * cols, dst, static_cast<cudaStream_t>(stream)));
+}
+
 tern_status tern_fwht_quant(const uint16_t* x, int64_t M, int64_t K, const int8_t* sign,
                             int mode, void* out, float* out_scale, void* stream) {
   if (M < 0 || K < 0) return TERN_ERR_INVALID_ARG;
   if (mode != TERN_FWHT_F32 && mode != TERN_FWHT_DECODE && mode != TERN_FWHT_I8 &&
-      mode != TERN_FWHT_F16)
+      mode != TERN_FWHT_F16 && mode != TERN_FWHT_I8H)
     return TERN_ERR_INVALID_ARG;
-  if (!k_ok(K, mode == TERN_FWHT_I8 ? 32768 : kMaxK)) return TERN_ERR_SHAPE;
+  if (!k_ok(K, (mode == TERN_FWHT_I8 || mode == TERN_FWHT_I8H) ? 32768 : kMaxK))
+    return TERN_ERR_SHAPE;
   if (M > (int64_t(1) << 31) / K) return TERN_ERR_SHAPE;
   if (mode == TERN_FWHT_DECODE && M > 16) return TERN_ERR_SHAPE;
   if (M == 0) return TERN_OK;
@@ -201,7 +226,8 @@ tern_status tern_fwht_combine(const float* h_first, const float* h_second, int64
 tern_status tern_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, void* out,
                                float* out_scale, void* stream) {
   if (M < 0 || K < 0) return TERN_ERR_INVALID_ARG;
-  if (mode != TERN_FWHT_DECODE && mode != TERN_FWHT_I8 && mode != TERN_FWHT_F16)
+  if (mode != TERN_FWHT_DECODE && mode != TERN_FWHT_I8 && mode != TERN_FWHT_F16 &&
+      mode != TERN_FWHT_I8H)
     return TERN_ERR_INVALID_ARG;
   if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
   if (M > (int64_t(1) << 31) / K) return TERN_ERR_SHAPE;
@@ -273,15 +299,23 @@ tern_status tern_linear_decode(const uint16_t* x, const int8_t* sign, const uint
       launch_linear_decode(x, sign, packed, M, N, K, y, ws, static_cast<cudaStream_t>(stream)));
 }
 
-tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
-                                   const float* rscale, int64_t M, int64_t N, int64_t K,
-                                   uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
-                                   void* stream) {
+namespace {
+tern_status gemm_int8_shape(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0) return TERN_ERR_INVALID_ARG;
   if (!k_ok(K, kMaxK)) return TERN_ERR_SHAPE;
   if (N % 16 != 0) return TERN_ERR_SHAPE;
   if (M > (int64_t(1) << 24) || N > (int64_t(1) << 24)) return TERN_ERR_SHAPE;
   if ((M + 127) / 128 * ((N + 255) / 256) >= (int64_t(1) << 31)) return TERN_ERR_SHAPE;  // tile count
+  return TERN_OK;
+}
+}  // namespace
+
+tern_status tern_gemm_prefill_int8h(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
+                                    const float* rscale, int64_t M, int64_t N, int64_t K,
+                                    uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  const tern_status sh = gemm_int8_shape(M, N, K);
+  if (sh != TERN_OK) return sh;
   if (M == 0 || N == 0) return TERN_OK;
   if (xq == nullptr || tscale == nullptr || w_q == nullptr || rscale == nullptr || y == nullptr)
     return TERN_ERR_INVALID_ARG;
@@ -291,6 +325,34 @@ tern_status tern_gemm_prefill_int8(const uint16_t* xq, const float* tscale, cons
   if (!device_supported()) return TERN_ERR_UNSUPPORTED;
   return from_cuda(launch_gemm(xq, tscale, w_q, rscale, M, N, K, y, acc, ws, ws_bytes,
                                static_cast<cudaStream_t>(stream)));
+}
+
+tern_status tern_gemm_prefill_int8(const int8_t* xq, const float* tscale, const int8_t* w_int8,
+                                   const float* rscale, int64_t M, int64_t N, int64_t K,
+                                   uint16_t* y, int32_t* acc, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  const tern_status sh = gemm_int8_shape(M, N, K);
+  if (sh != TERN_OK) return sh;
+  if (M == 0 || N == 0) return TERN_OK;
+  if (xq == nullptr || tscale == nullptr || w_int8 == nullptr || rscale == nullptr ||
+      y == nullptr)
+    return TERN_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(tscale) || !aligned16(w_int8) || !aligned16(rscale) ||
+      !aligned16(y) || (acc && !aligned16(acc)))
+    return TERN_ERR_ALIGN;
+  if (ws == nullptr || ws_bytes < gemm_int8_workspace_bytes(M, N, K)) return TERN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TERN_ERR_ALIGN;
+  if (!device_supported()) return TERN_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint16_t* xh = reinterpret_cast<uint16_t*>(base);
+  uint16_t* wh = reinterpret_cast<uint16_t*>(base + gemm_int8_w_offset(M, N, K));
+  const size_t split_off = gemm_int8_split_offset(M, N, K);
+  cudaError_t e = launch_widen_int8(xq, M * K, xh, st);
+  if (e == cudaSuccess) e = launch_widen_int8(w_int8, N * K, wh, st);
+  if (e != cudaSuccess) return TERN_ERR_CUDA;
+  return from_cuda(launch_gemm(xh, tscale, wh, rscale, M, N, K, y, acc, base + split_off,
+                               ws_bytes - split_off, st));
 }
 
 tern_status tern_gemm_prefill_packed(const uint16_t* xq, const float* tscale,

@@ -73,8 +73,9 @@ cudaError_t launch_fwht_combine(const float* h_first, const float* h_second, int
 cudaError_t launch_quant_rotated(const float* xr, int64_t M, int64_t K, int mode, void* out,
                                  float* out_scale, cudaStream_t st);
 cudaError_t launch_pack(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
-                        uint8_t* packed, int8_t* q, float* rscale, uint16_t* w_q,
+                        uint8_t* packed, int8_t* q, float* rscale, int8_t* w_int8,
                         cudaStream_t st);
+cudaError_t launch_widen_int8(const int8_t* src, int64_t count, uint16_t* dst, cudaStream_t st);
 size_t gemv_packed_bytes(int64_t N, int64_t K);
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
 bool gemv_needs_fixup(int64_t M, int64_t N, int64_t K);

@@ -163,13 +163,13 @@ class GpuOps:
         m, kp = xr.shape
         xq = torch.empty((m, kp), dtype=torch.float16, device=xr.device)
         ts = torch.empty(m, dtype=torch.float32, device=xr.device)
-        B.tern_quant_rotated(xr, m, kp, B.TERN_FWHT_I8, xq, ts)
+        B.tern_quant_rotated(xr, m, kp, B.TERN_FWHT_I8H, xq, ts)
         y = torch.empty((m, lin.n), dtype=torch.bfloat16, device=xr.device)
         lay = lin.layer
         if lay.w_q is not None:
             nb = B.tern_workspace_bytes(B.TERN_OP_GEMM, m, lin.n, kp)
             buf = ws.scratch(nb) if nb else None
-            B.tern_gemm_prefill_int8(xq, ts, lay.w_q, lay.rscale, m, lin.n, kp, y, None, buf, nb)
+            B.tern_gemm_prefill_int8h(xq, ts, lay.w_q, lay.rscale, m, lin.n, kp, y, None, buf, nb)
         else:
             nb = B.tern_workspace_bytes(B.TERN_OP_GEMM_PACKED, m, lin.n, kp)
             buf = ws.scratch(nb) if nb else None

@@ -130,12 +130,33 @@ def test_gemv_argument_errors(lib):
 
 
 def test_gemm_argument_errors(lib):
-    a = lambda m=64, n=256, k=1024, y=FAKE: (FAKE, FAKE, FAKE, FAKE, m, n, k, y, None, None, 0, None)
-    assert _st("tern_gemm_prefill_int8", *a(n=250)) == 2
-    assert _st("tern_gemm_prefill_int8", *a(k=100)) == 2
-    assert _st("tern_gemm_prefill_int8", *a(y=None)) == 1
-    assert _st("tern_gemm_prefill_int8", *a(y=FAKE + 2)) == 3
-    assert _st("tern_gemm_prefill_int8", *a(m=0)) == 0
+    a = lambda m=64, n=256, k=1024, y=FAKE, ws=None, nb=0: (FAKE, FAKE, FAKE, FAKE, m, n, k, y,
+                                                            None, ws, nb, None)
+    for fn in ("tern_gemm_prefill_int8h", "tern_gemm_prefill_int8"):
+        assert _st(fn, *a(n=250)) == 2
+        assert _st(fn, *a(k=100)) == 2
+        assert _st(fn, *a(y=None)) == 1
+        assert _st(fn, *a(y=FAKE + 2)) == 3
+        assert _st(fn, *a(m=0)) == 0
+    # the int8-typed call needs its workspace: both operands widened, then the split pieces
+    nb = B.tern_workspace_bytes(B.TERN_OP_GEMM_INT8, 64, 256, 1024)
+    assert nb >= (64 + 256) * 1024 * 2
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMM_INT8, 2048, 34816, 5120) >= (
+        (2048 + 34816) * 5120 * 2 + B.tern_workspace_bytes(B.TERN_OP_GEMM, 2048, 34816, 5120))
+    assert _st("tern_gemm_prefill_int8", *a()) == B.TERN_ERR_WORKSPACE
+    assert _st("tern_gemm_prefill_int8", *a(ws=FAKE, nb=nb - 1)) == B.TERN_ERR_WORKSPACE
+    assert _st("tern_gemm_prefill_int8", *a(ws=FAKE + 8, nb=nb)) == 3
+    assert B.tern_kernel_launches(B.TERN_OP_GEMM_INT8, 64, 256, 1024) in (3, 4)
+    assert B.tern_kernel_launches(B.TERN_OP_GEMM_INT8, 0, 256, 1024) == 0
+
+
+def test_widen_argument_errors(lib):
+    w = lambda rows=4, cols=32, src=FAKE, dst=FAKE: (src, rows, cols, dst, None)
+    assert _st("tern_widen_int8", *w(rows=-1)) == 1
+    assert _st("tern_widen_int8", *w(cols=24)) == 2
+    assert _st("tern_widen_int8", *w(rows=0, src=None)) == 0
+    assert _st("tern_widen_int8", *w(src=None)) == 1
+    assert _st("tern_widen_int8", *w(dst=FAKE + 2)) == 3
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
@@ -298,7 +319,8 @@ def test_binding_constants_match_the_header():
                  "TERN_ERR_UNSUPPORTED"):
         m = re.search(r"\b%s = (\d+)" % name, text)
         assert m and int(m.group(1)) == getattr(B, name), name
-    for name in ("TERN_OP_GEMV", "TERN_OP_GEMM", "TERN_OP_GEMM_PACKED", "TERN_FWHT_F32",
-                 "TERN_FWHT_DECODE", "TERN_FWHT_I8", "TERN_FWHT_F16"):
+    for name in ("TERN_OP_GEMV", "TERN_OP_GEMM", "TERN_OP_GEMM_PACKED", "TERN_OP_GEMV_F32",
+                 "TERN_OP_GEMM_INT8", "TERN_FWHT_F32", "TERN_FWHT_DECODE", "TERN_FWHT_I8",
+                 "TERN_FWHT_F16", "TERN_FWHT_I8H"):
         m = re.search(r"#define %s (\d+)" % name, text)
         assert m and int(m.group(1)) == getattr(B, name), name

@@ -33,7 +33,8 @@ def _run(xd, m, k, mode, sign=None):
         out = poison(torch.empty((m, k), dtype=torch.float16, device=dev))
         sc = poison(torch.empty((m, k // 1024), dtype=torch.float32, device=dev))
     else:
-        out = poison(torch.empty((m, k), dtype=torch.float16, device=dev))
+        dt = torch.int8 if mode == B.TERN_FWHT_I8 else torch.float16
+        out = poison(torch.empty((m, k), dtype=dt, device=dev))
         sc = poison(torch.empty(m, dtype=torch.float32, device=dev))
     B.tern_fwht_quant(xd, m, k, sign, mode, out, sc)
     torch.cuda.synchronize()
@@ -85,11 +86,16 @@ def test_fwht_i8_bitwise(m, k, frac, mult):
     SM, up to the mode's limit of 32 blocks one; both give the oracle's xq
     and tscale."""
     bits, x = I.make_activations(3, m, k, frac, mult)
-    out, sc = _run(to_dev_bf16(bits), m, k, B.TERN_FWHT_I8)
+    xd = to_dev_bf16(bits)
+    out, sc = _run(xd, m, k, B.TERN_FWHT_I8)
     xq, ts = O.quant_tokens(O.fwht_f32(x))
-    got = out.cpu().float().numpy()
-    assert np.array_equal(got, xq.astype(np.float32))
+    assert out.dtype == torch.int8
+    assert np.array_equal(out.cpu().numpy(), xq.astype(np.int8))
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), ts.view(np.uint32))
+    # the same integers held in fp16, the tensor cores' operand
+    out_h, sc_h = _run(xd, m, k, B.TERN_FWHT_I8H)
+    assert np.array_equal(out_h.cpu().float().numpy(), xq.astype(np.float32))
+    assert torch.equal(sc, sc_h)
 
 
 def test_sign_vector_all_modes():

@@ -92,7 +92,7 @@ def test_quant_rotated_matches_fwht_quant():
     bits, x = I.make_activations(62, m, k, 0.001, 50.0)
     xb = to_dev_bf16(bits)
     xr, _ = B.fwht(xb, B.TERN_FWHT_F32)
-    for mode in (B.TERN_FWHT_DECODE, B.TERN_FWHT_F16, B.TERN_FWHT_I8):
+    for mode in (B.TERN_FWHT_DECODE, B.TERN_FWHT_F16, B.TERN_FWHT_I8, B.TERN_FWHT_I8H):
         out, sc = B.fwht(xb, mode)
         out2 = torch.empty_like(out)
         sc2 = torch.empty_like(sc)
