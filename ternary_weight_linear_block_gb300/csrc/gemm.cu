@@ -52,7 +52,14 @@ constexpr int TMEM_COLS = 512;
 // tern_selftest_wait), so 2^18 polls give up after about one second; a
 // wait of the working kernel lasts microseconds.
 constexpr uint32_t WAIT_LIMIT = 1u << 18;
+// Polls of a polling wait (a test and a 32 ns sleep each) before it gives
+// up: about a second.
+constexpr uint32_t POLL_LIMIT = 1u << 24;
+// Tests of a spinning wait (no sleep) before it gives up: about a second.
+constexpr uint32_t SPIN_LIMIT = 1u << 26;
 constexpr uint32_t IDESC = ptx::idesc_f16_f32(BM, BN);
+// a CTA pair's MMA: 256 rows (128 per CTA) x 256 columns
+constexpr uint32_t IDESC_PAIR = ptx::idesc_f16_f32(256, 256);
 constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
 
 enum : unsigned int {
@@ -481,8 +488,8 @@ __global__ void __launch_bounds__(256)
 // reads (a field masked in place reads u * 4^e * 2^-24, u = code + 1; times
 // 2^(15 - 2e), then fma with 512 q and -q, gives code * q; all exact).  MMA,
 // per-1024 chunk int32 conversion and epilogue are those of the kernel above.
-// Warp roles: 0 producer, 1 MMA issuer, 2 TMEM allocator, 3 idle, 4-11
-// epilogue, 12-15 expansion.
+// Warp roles: 0 producer, 1 MMA issuer, 2 TMEM allocator, 3 relay (pairs;
+// else idle), 4-11 epilogue, 12-15 expansion.
 //
 // Two tile orientations (template WM).  WM = false: tokens on the MMA's M
 // side (128 per tile) and weight rows on its N side (256), for M <= 128
@@ -491,7 +498,24 @@ __global__ void __launch_bounds__(256)
 // tokens instead of 128 -- half the expansion work and half the shared-
 // memory writes per MMA -- while the MMA shape, the stage size (A 16 KB, B
 // 32 KB) and the TMEM buffers stay the same; the accumulator's lanes are
-// then weight rows and its columns tokens.  The 512 threads launch with 128 registers each;
+// then weight rows and its columns tokens.
+//
+// WM = true runs in CTA pairs (PAIR, clusters of two, tcgen05 cta_group::2):
+// a pair tile is 256 weight rows x 256 tokens, each CTA expanding its own 128
+// weight rows and loading its own 128 tokens, and the even CTA issuing one
+// 256 x 256 x 16 MMA per k16 step that reads both CTAs' shared memory and
+// writes both CTAs' tensor memory (each CTA's 128 rows, all 256 token
+// columns).  The tensor cores' operand reads and the token copies per SM are
+// then two thirds of a single CTA's for the same work, which matters because
+// shared-memory bandwidth, not the tensor pipe, bounds the single-CTA kernel:
+// per SM and 64-k stage it carries the 48 KB the MMA reads, the 32 KB of
+// tokens TMA writes, the expansion's 16 KB of stores and the codes.  Each
+// CTA's warp 3 relays "stage s holds my tokens and expanded weights" to the
+// even CTA's pfull[s]; the MMA commits arrive (multicast) on both CTAs'
+// stage-free and accumulator-full barriers; both CTAs' epilogue warps
+// release an accumulator buffer on the even CTA's dempty.  (The even CTA's
+// issuer waiting on its own stage's barriers directly, beside the odd CTA's
+// relay, measured slower: 480 -> 547 us at gate/up M = 2048.)  The 512 threads launch with 128 registers each;
 // the epilogue's 128 int32 sums per thread need more, so the warpgroups
 // re-split the block's registers with setmaxnreg (control 48, epilogue 168,
 // expansion 120 per thread); the launcher refuses to launch unless the kernel
@@ -508,6 +532,8 @@ constexpr int PCSTAGES = 4;
 constexpr int PA_BYTES = BM * BK * 2;    // tokens
 constexpr int PB_BYTES = PBN * BK * 2;   // expanded weights
 constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr int PSTAGES_PAIR = 6;
+constexpr int PSTAGE_BYTES_PAIR = PA_BYTES + PB_BYTES / 2;   // 128 weight rows + 128 tokens
 constexpr int P_THREADS = 512;
 constexpr int P_LAUNCH_REGS = 128;
 constexpr int P_REGS_CONTROL = 48, P_REGS_EPILOGUE = 168, P_REGS_EXPAND = 120;
@@ -515,6 +541,8 @@ constexpr size_t PSMEM_BYTES =
     static_cast<size_t>(PSTAGES) * PSTAGE_BYTES + PCSTAGES * PCODE_BYTES + 1024 + 512;
 static_assert(PSMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(PSTAGE_BYTES % 1024 == 0 && PA_BYTES % 1024 == 0, "stage alignment");
+static_assert(PSTAGES_PAIR * PSTAGE_BYTES_PAIR <= PSTAGES * PSTAGE_BYTES,
+              "pair stages fit the single-CTA stage area");
 static_assert(128 * P_REGS_CONTROL + 256 * P_REGS_EPILOGUE + 128 * P_REGS_EXPAND <=
                   P_THREADS * P_LAUNCH_REGS,
               "register split exceeds the block's launch allocation");
@@ -528,38 +556,56 @@ __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
 }
 
-template <bool WM>
+template <bool WM, bool PAIR>
 __global__ void __launch_bounds__(P_THREADS, 1)
     gemm_packed_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t* __restrict__ packed,
                        const int8_t* __restrict__ q, const float* __restrict__ tscale,
                        const float* __restrict__ rscale, int M, int N, int K,
                        __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out, int S,
                        int32_t* __restrict__ part) {
+  // a pair's stage holds 128 tokens (16 KB) instead of 256, so six stages
+  // fit where a single CTA has four
+  constexpr int NST = PAIR ? PSTAGES_PAIR : PSTAGES;
+  constexpr int SGB = PAIR ? PSTAGE_BYTES_PAIR : PSTAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* scode = smem + PSTAGES * PSTAGE_BYTES;
+  uint8_t* scode = smem + NST * SGB;
   uint64_t* afull = reinterpret_cast<uint64_t*>(scode + PCSTAGES * PCODE_BYTES);
-  uint64_t* wfull = afull + PSTAGES;
-  uint64_t* empty = wfull + PSTAGES;
-  uint64_t* cfull = empty + PSTAGES;
+  uint64_t* wfull = afull + NST;
+  uint64_t* empty = wfull + NST;
+  uint64_t* cfull = empty + NST;
   uint64_t* cempty = cfull + PCSTAGES;
   uint64_t* dfull = cempty + PCSTAGES;
   uint64_t* dempty = dfull + 2;
   uint64_t* done = dempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* pfull = done + 1;   // (pairs) both CTAs' stage ready, in the even CTA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pfull + NST);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  static_assert(!PAIR || WM, "CTA pairs split 256 weight rows x 256 tokens");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   constexpr int TOK = p_tok<WM>(), WROWS = p_wrows<WM>(), CODE_BYTES = p_code_bytes<WM>();
+  // In a pair, each CTA loads half of the tile's tokens (the MMA's N side) and
+  // expands its own 128 weight rows (half of the M side).
+  constexpr int TOK_CTA = PAIR ? TOK / 2 : TOK;
+  constexpr int CTAS = PAIR ? 2 : 1;
+  const int rank = PAIR ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+  const int team = PAIR ? static_cast<int>(ptx::cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int teams = PAIR ? static_cast<int>(ptx::cluster_count_x()) : static_cast<int>(gridDim.x);
   // stage layout: MMA operand A (16 KB) at offset 0, B (32 KB) after it; the
   // tokens are A for WM = false and B for WM = true
   constexpr uint32_t TOK_OFF = WM ? PA_BYTES : 0, W_OFF = WM ? 0 : PA_BYTES;
-  constexpr uint32_t TOK_BYTES = TOK * BK * 2;
+  constexpr uint32_t TOK_BYTES = TOK_CTA * BK * 2;
   const int G = K / kGroup;
+  // stage s free again (in a pair, the even CTA's MMA commit completes it;
+  // the ring keeps these waits off the critical path, so they suspend)
+  auto empty_wait = [&](uint64_t* bar, uint32_t parity) {
+    return ptx::mbar_wait(bar, parity, abort_flag, WAIT_LIMIT);
+  };
   const int m_blocks = (M + TOK - 1) / TOK;   // token blocks (fastest in the tile order)
-  const int tiles = m_blocks * ((N + WROWS - 1) / WROWS);
+  const int tiles = m_blocks * ((N + CTAS * WROWS - 1) / (CTAS * WROWS));
   const int units = tiles * S;   // unit = (tile, K slice of whole 128-groups)
   // the tile and the group range [g0, g1) of a unit; the MMA accumulates it
   // in pieces that end at every 1024-chunk boundary (and at g1), so each
@@ -576,7 +622,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < PSTAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       ptx::mbar_init(&afull[s], 1);
       ptx::mbar_init(&wfull[s], 4);   // one arrival per expansion warp
       ptx::mbar_init(&empty[s], 1);
@@ -587,19 +633,26 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&dfull[b], 1);
-      ptx::mbar_init(&dempty[b], 8);   // one arrival per epilogue warp
+      ptx::mbar_init(&dempty[b], 8 * CTAS);   // one arrival per epilogue warp (of both CTAs)
     }
     ptx::mbar_init(done, 1);
+    for (int s = 0; s < NST; ++s) ptx::mbar_init(&pfull[s], 2);   // one relay per CTA
     *abort_flag = 0;
     ptx::mbar_fence_init();
   }
   if (warp == 2) {
-    ptx::tmem_alloc(tmem_slot, TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) ptx::prefetch_tmap(&tmA);
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();   // both CTAs' barriers exist before any remote arrival
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -614,10 +667,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       uint32_t ph = 0, cph = 0;
       long a_issued = 0, c_issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int u = team; u < units && ok; u += teams) {
         int tile, g0, g1;
         unit_of(u, tile, g0, g1);
-        const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
+        const int n_blk = (tile / m_blocks) * CTAS + rank, m_blk = tile % m_blocks;
         constexpr int PER_UNIT = 512 / WROWS;   // weight blocks per 512-row unit
         const uint8_t* wsrc = packed + static_cast<size_t>(n_blk / PER_UNIT) * G * PUNIT_BYTES +
                               (n_blk % PER_UNIT) * CODE_BYTES;
@@ -636,16 +689,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             cph ^= 1u;
           }
           for (int h = 0; h < 2; ++h) {
-            if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, WAIT_LIMIT)) {
+            if (!empty_wait(&empty[s], ph ^ 1u)) {
               if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
               ok = false;
               break;
             }
             ptx::mbar_arrive_expect_tx(&afull[s], TOK_BYTES);
-            ptx::tma_load_2d(smem + s * PSTAGE_BYTES + TOK_OFF, &tmA, &afull[s],
-                             g * kGroup + h * BK, m_blk * TOK);
+            ptx::tma_load_2d(smem + s * SGB + TOK_OFF, &tmA, &afull[s],
+                             g * kGroup + h * BK, m_blk * TOK + rank * TOK_CTA);
             ++a_issued;
-            if (++s == PSTAGES) {
+            if (++s == NST) {
               s = 0;
               ph ^= 1u;
             }
@@ -654,10 +707,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       }
       if (!ok) {
         // let the copies still in flight land before the CTA exits
-        long back = a_issued < PSTAGES ? a_issued : PSTAGES;
+        long back = a_issued < NST ? a_issued : NST;
         for (long i = 0; i < back; ++i) {
           if (--s < 0) {
-            s = PSTAGES - 1;
+            s = NST - 1;
             ph ^= 1u;
           }
           if (!ptx::mbar_wait_bounded(&afull[s], ph, WAIT_LIMIT)) atomicOr(&g_gemm_error, ERR_DRAIN);
@@ -671,18 +724,23 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           if (!ptx::mbar_wait_bounded(&cfull[c], cph, WAIT_LIMIT)) atomicOr(&g_gemm_error, ERR_DRAIN);
         }
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------- MMA issuer (one thread)
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (one thread; in a pair, the even CTA's, for
+      // both: 256 x 256 x 16 MMAs whose commits arrive in both CTAs)
       int s = 0;
       uint32_t ph = 0;
       uint32_t cc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int u = team; u < units && ok; u += teams) {
         int tile, g0, g1;
         unit_of(u, tile, g0, g1);
         for (int gp = g0; gp < g1 && ok; gp = piece_end(gp, g1), ++cc) {
           const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
-          if (!ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag, WAIT_LIMIT)) {
+          const bool drained = PAIR ? ptx::mbar_spin_cluster(&dempty[buf], dph ^ 1u, abort_flag,
+                                                             SPIN_LIMIT)
+                                    : ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag,
+                                                     WAIT_LIMIT);
+          if (!drained) {
             if (!*abort_flag) fail(abort_flag, ERR_MMA);
             ok = false;
             break;
@@ -691,31 +749,74 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           const uint32_t d_tmem = tmem + buf * BN;
           const int n_stages = 2 * (piece_end(gp, g1) - gp);
           for (int j = 0; j < n_stages; ++j) {
-            if (!ptx::mbar_wait(&afull[s], ph, abort_flag, WAIT_LIMIT) ||
-                !ptx::mbar_wait(&wfull[s], ph, abort_flag, WAIT_LIMIT)) {
+            const bool ready =
+                PAIR ? ptx::mbar_spin_cluster(&pfull[s], ph, abort_flag, SPIN_LIMIT)
+                     : (ptx::mbar_wait(&afull[s], ph, abort_flag, WAIT_LIMIT) &&
+                        ptx::mbar_wait(&wfull[s], ph, abort_flag, WAIT_LIMIT));
+            if (!ready) {
               if (!*abort_flag) fail(abort_flag, ERR_MMA);
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            const uint64_t a0 = ptx::sw128_kmajor_desc(ptx::smem_u32(smem + s * PSTAGE_BYTES));
+            const uint64_t a0 = ptx::sw128_kmajor_desc(ptx::smem_u32(smem + s * SGB));
             const uint64_t b0 =
-                ptx::sw128_kmajor_desc(ptx::smem_u32(smem + s * PSTAGE_BYTES + PA_BYTES));
+                ptx::sw128_kmajor_desc(ptx::smem_u32(smem + s * SGB + PA_BYTES));
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              ptx::mma_f16_ss(d_tmem, a0 + 2u * kk, b0 + 2u * kk, IDESC,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-            ptx::mma_commit(&empty[s]);
-            if (++s == PSTAGES) {
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              if constexpr (PAIR)
+                ptx::mma_f16_ss_pair(d_tmem, a0 + 2u * kk, b0 + 2u * kk, IDESC_PAIR,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+              else
+                ptx::mma_f16_ss(d_tmem, a0 + 2u * kk, b0 + 2u * kk, IDESC,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            if constexpr (PAIR)
+              ptx::mma_commit_pair(&empty[s], 0x3);
+            else
+              ptx::mma_commit(&empty[s]);
+            if (++s == NST) {
               s = 0;
               ph ^= 1u;
             }
           }
-          if (ok) ptx::mma_commit(&dfull[buf]);
+          if (ok) {
+            if constexpr (PAIR)
+              ptx::mma_commit_pair(&dfull[buf], 0x3);
+            else
+              ptx::mma_commit(&dfull[buf]);
+          }
         }
       }
-      ptx::mma_commit(done);
+      if constexpr (PAIR)
+        ptx::mma_commit_pair(done, 0x3);
+      else
+        ptx::mma_commit(done);
       if (!ptx::mbar_wait_bounded(done, 0, WAIT_LIMIT)) atomicOr(&g_gemm_error, ERR_DRAIN);
+    } else if (PAIR && warp == 3 && lane == 0) {
+      // ---------------- relay (pairs): once this CTA's stage holds its tokens
+      // and its expanded weights, one arrival on the even CTA's pfull[s]
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      const uint32_t pf = ptx::mapa_shared(pfull, 0);
+      for (int u = team; u < units && ok; u += teams) {
+        int tile, g0, g1;
+        unit_of(u, tile, g0, g1);
+        for (int j = 0; j < 2 * (g1 - g0); ++j) {
+          if (!ptx::mbar_spin_cluster(&afull[s], ph, abort_flag, SPIN_LIMIT) ||
+              !ptx::mbar_spin_cluster(&wfull[s], ph, abort_flag, SPIN_LIMIT)) {
+            if (!*abort_flag) fail(abort_flag, ERR_MMA);
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_cluster(pf + 8u * static_cast<uint32_t>(s));
+          if (++s == NST) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
     }
     __syncwarp();
   } else if (warp < 12) {
@@ -725,16 +826,17 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const int qd = warp & 3;   // TMEM lane quarter accessible to this warp
     uint32_t cc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    for (int u = team; u < units && ok; u += teams) {
       int tile, g0, g1;
       unit_of(u, tile, g0, g1);
-      const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
+      const int n_blk = (tile / m_blocks) * CTAS + rank, m_blk = tile % m_blocks;
       int32_t sums[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sums[i] = 0;
       for (int gp = g0; gp < g1; gp = piece_end(gp, g1), ++cc) {
         const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
-        if (!ptx::mbar_wait_warp(&dfull[buf], dph, abort_flag, WAIT_LIMIT)) {
+        const bool full = ptx::mbar_wait_warp(&dfull[buf], dph, abort_flag, WAIT_LIMIT);
+        if (!full) {
           if (!*abort_flag) fail(abort_flag, ERR_EPILOGUE);
           ok = false;
           break;
@@ -753,7 +855,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&dempty[buf]);
+        if (lane == 0) {
+          if constexpr (PAIR)
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(&dempty[buf], 0));
+          else
+            ptx::mbar_arrive(&dempty[buf]);
+        }
       }
       if (!ok) break;
       if constexpr (WM) {
@@ -838,23 +945,25 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     // 16 16-row tiles of the half unit; lane = slot L = 4 r + c of the packed
     // format
     const int xw = warp - 12;
-    const int r = lane >> 2, cq = lane & 3;
+    const int r = lane >> 2;
     constexpr int UPW = WROWS / 64;   // tiles of 16 rows per expansion warp
-    // byte offset of (u = 0, row parity 0, chunk 0) inside a weight stage:
-    // row 16 xw + r, 4 c bytes into the 16-byte chunk; u adds 64 rows, the
-    // row parity 8 rows
-    const uint32_t row_off = static_cast<uint32_t>(W_OFF + (16 * xw + r) * 128 + 4 * cq);
-    uint32_t xo[8];
+    // The expanded values of a k16 step leave in one stmatrix.x4: register p
+    // (row parity p % 2, 8-column half p / 2) is matrix p, whose 16-byte rows
+    // lanes 8 p .. 8 p + 7 address.  This lane addresses row 16 xw + ri +
+    // 8 (mi % 2) of its tile, 8-column half mi / 2 (u adds 64 rows).
+    const int mi = lane >> 3, ri = lane & 7;
+    const uint32_t row_off = static_cast<uint32_t>(W_OFF + (16 * xw + ri + 8 * (mi & 1)) * 128);
+    uint32_t xo[4];   // the step jl's 16-byte chunk 2 jl + mi / 2 in the 128-byte swizzle
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) xo[ch] = static_cast<uint32_t>((ch ^ r) << 4);
+    for (int jl = 0; jl < 4; ++jl) xo[jl] = static_cast<uint32_t>(((2 * jl + (mi >> 1)) ^ ri) << 4);
     const uint32_t smem_base = ptx::smem_u32(smem);
     int s = 0, c = 0;
     uint32_t ph = 0, cph = 0;
     bool ok = true;
-    for (int unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
+    for (int unit = team; unit < units && ok; unit += teams) {
       int tile, g0, g1;
       unit_of(unit, tile, g0, g1);
-      const int n_blk = tile / m_blocks;
+      const int n_blk = (tile / m_blocks) * CTAS + rank;
       // q of the thread's 2 UPW rows (slots u, row parities par); rows past N read row 0
       const int8_t* qp[UPW][2];
       bool qv_ok[UPW][2];
@@ -904,12 +1013,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, WAIT_LIMIT)) {
+          if (!empty_wait(&empty[s], ph ^ 1u)) {
             if (!*abort_flag) fail(abort_flag, ERR_EXPAND);
             ok = false;
             break;
           }
-          const uint32_t base = smem_base + s * PSTAGE_BYTES + row_off;
+          const uint32_t base = smem_base + s * SGB + row_off;
           // this stage holds k16 steps j = 4h .. 4h + 3 of the group; word p is
           // register p (row parity p % 2, 8-column half p / 2)
 #pragma unroll
@@ -919,22 +1028,21 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             const uint32_t mask = 0x00030003u << (2 * e);
             const uint32_t mul = 0x00010001u * static_cast<uint32_t>((30 - 2 * e) << 10);   // 2^(15-2e)
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              const int chunk = 2 * jl + (p >> 1);
-              const int par = p & 1;
+            for (int u = 0; u < UPW; ++u) {
+              const uint32_t w4[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+              uint32_t v[4];
 #pragma unroll
-              for (int u = 0; u < UPW; ++u) {
-                const uint32_t w4[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+              for (int p = 0; p < 4; ++p) {
                 const uint32_t f = (j < 6 ? w4[p] : w4[p] >> 12) & mask;
-                const uint32_t v = ptx::fma_f16x2(ptx::mul_f16x2(f, mul), q512[u][par], qneg[u][par]);
-                ptx::st_shared_b32(base + xo[chunk] + 8192u * u + 1024u * par, v);
+                v[p] = ptx::fma_f16x2(ptx::mul_f16x2(f, mul), q512[u][p & 1], qneg[u][p & 1]);
               }
+              ptx::stsm_x4(base + xo[jl] + 8192u * u, v[0], v[1], v[2], v[3]);
             }
           }
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&wfull[s]);
-          if (++s == PSTAGES) {
+          if (++s == NST) {
             s = 0;
             ph ^= 1u;
           }
@@ -946,7 +1054,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if constexpr (PAIR) {
+    // the even CTA's MMAs (which read this CTA's shared memory and write its
+    // tensor memory) are done, and both epilogues have read their columns
+    ptx::cluster_sync();
+    if (warp == 2) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+  } else if (warp == 2) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -1146,20 +1262,24 @@ cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t*
 
 namespace {
 // Tile orientation of the packed GEMM: weight rows on the MMA's M side
-// (256-token tiles) above one 128-token block.
+// (256-token tiles, run by CTA pairs) above one 128-token block.
 bool packed_wm(int64_t M) { return M > BM; }
 
+// Tiles: 128 tokens x 256 weight rows per CTA, or 256 weight rows x 256
+// tokens per CTA pair; a "team" is one CTA or one pair.
 long packed_tiles(int64_t M, int64_t N) {
-  return packed_wm(M) ? ((M + 255) / 256) * ((N + 127) / 128)
+  return packed_wm(M) ? ((M + 255) / 256) * ((N + 255) / 256)
                       : ((M + BM - 1) / BM) * ((N + PBN - 1) / PBN);
 }
+long packed_teams(int64_t M) { return packed_wm(M) ? sm_count() / 2 : sm_count(); }
 }  // namespace
 
 // K slices per tile of the packed GEMM: 1 when the tiles alone fill most of
-// the GPU, else as many slices (of whole 128-groups) as keep one unit per SM.
+// the GPU, else as many slices (of whole 128-groups) as keep one unit per
+// team.
 int packed_splits(int64_t M, int64_t N, int64_t K) {
   const long tiles = packed_tiles(M, N);
-  const long sms = sm_count();
+  const long sms = packed_teams(M);
   if (4 * tiles >= 3 * sms) return 1;
   const long want = sms / tiles;
   const long groups = K / kGroup;
@@ -1179,7 +1299,7 @@ cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const ui
   static std::atomic<int> regs_ok{0};
   if (regs_ok.load(std::memory_order_acquire) == 0) {
     int ok = 1;
-    for (auto* kern : {gemm_packed_kernel<false>, gemm_packed_kernel<true>}) {
+    for (auto* kern : {gemm_packed_kernel<false, false>, gemm_packed_kernel<true, true>}) {
       cudaFuncAttributes fa;
       cudaError_t e = cudaFuncGetAttributes(&fa, kern);
       if (e != cudaSuccess) return e;
@@ -1191,7 +1311,7 @@ cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const ui
   if (regs_ok.load(std::memory_order_acquire) < 0) return cudaErrorNotSupported;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t ea = once_per_device(attr_done, [] {
-    for (auto* kern : {gemm_packed_kernel<false>, gemm_packed_kernel<true>}) {
+    for (auto* kern : {gemm_packed_kernel<false, false>, gemm_packed_kernel<true, true>}) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(PSMEM_BYTES));
       if (e != cudaSuccess) return e;
@@ -1200,16 +1320,32 @@ cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const ui
   });
   if (ea != cudaSuccess) return ea;
   const bool wm = packed_wm(M);
-  CUtensorMap ta;
-  if (!make_map(&ta, xq, M, K, wm ? 256 : BM)) return cudaErrorInvalidValue;
+  CUtensorMap ta;   // token boxes: 64 k x (128 tokens, one CTA's half of a pair tile)
+  if (!make_map(&ta, xq, M, K, BM)) return cudaErrorInvalidValue;
   const int S = packed_splits(M, N, K);
   int32_t* part = S > 1 ? static_cast<int32_t*>(ws) : nullptr;
   const long units = packed_tiles(M, N) * S;
-  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
-  cudaError_t e = launch(wm ? gemm_packed_kernel<true> : gemm_packed_kernel<false>, dim3(grid),
-                         dim3(P_THREADS), PSMEM_BYTES, st, ta, packed, q, tscale, rscale,
-                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                         reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
+  cudaError_t e;
+  if (wm) {
+    // one CTA pair per team, as many as fit on the device at once
+    static std::atomic<long> pairs_cached{0};
+    long pairs = pairs_cached.load(std::memory_order_acquire);
+    if (pairs == 0) {
+      pairs = max_active_clusters(gemm_packed_kernel<true, true>, dim3(P_THREADS), PSMEM_BYTES, 2);
+      if (pairs <= 0) return cudaErrorNotSupported;
+      pairs_cached.store(pairs, std::memory_order_release);
+    }
+    const long teams = units < pairs ? units : pairs;
+    e = launch_cluster(gemm_packed_kernel<true, true>, dim3(static_cast<unsigned>(2 * teams)),
+                       dim3(P_THREADS), PSMEM_BYTES, st, 2u, ta, packed, q, tscale, rscale,
+                       static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                       reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
+  } else {
+    const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
+    e = launch(gemm_packed_kernel<false, false>, dim3(grid), dim3(P_THREADS), PSMEM_BYTES, st, ta,
+               packed, q, tscale, rscale, static_cast<int>(M), static_cast<int>(N),
+               static_cast<int>(K), reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
+  }
   if (e != cudaSuccess || S == 1) return e;
   const long threads = M * N / 8;
   return launch(packed_finalize_kernel, dim3(static_cast<unsigned>((threads + FIN_THREADS - 1) /

@@ -85,6 +85,110 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// ---------------------------------------------------------------- clusters
+// (for kernels launched in clusters of two CTAs that share one tcgen05 MMA)
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; orders the memory operations
+// before it (release) with those after it in the other CTAs (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or
+// a peer's).  Default semantics (release at CTA scope): a cluster-scope
+// release puts a fence in front of every arrival, which was measured to
+// bound a CTA pair's stage rate.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// try_wait for barriers that other CTAs arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63) == 63 && *abort) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t* bar, uint32_t parity,
+                                                       volatile int* abort, uint32_t limit) {
+  const bool ok = mbar_wait_cluster(bar, parity, abort, limit);
+  return __all_sync(0xffffffffu, ok);
+}
+// Non-blocking test, for barriers that other CTAs arrive on.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait by polling (test_wait and a short sleep) for barriers whose phases
+// other SMs complete (a peer CTA's arrival, a pair MMA's multicast commit):
+// a try_wait that suspended the thread was measured to oversleep such
+// completions.  Gives up after `limit` polls (1 << 24: about a second) or
+// when `*abort` becomes nonzero; returns true only when the phase completed.
+__device__ __forceinline__ bool mbar_poll_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort) return false;
+    __nanosleep(32);
+  }
+  return false;
+}
+// The same without the sleep, for a single thread whose only job is to
+// follow the barrier (an MMA issuer, a relay).
+__device__ __forceinline__ bool mbar_spin_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *abort) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ bool mbar_poll_cluster_warp(uint64_t* bar, uint32_t parity,
+                                                       volatile int* abort, uint32_t limit) {
+  const bool ok = mbar_poll_cluster(bar, parity, abort, limit);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1) {
@@ -177,6 +281,43 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
+// The same for a pair of CTAs (cta_group::2): one warp in each CTA of the
+// pair allocates (or frees) the same columns in both CTAs' tensor memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// D (+)= A * B^T over a CTA pair, kind::f16, issued by one thread of the
+// even CTA: A's rows 0..M/2-1 and B's rows 0..N/2-1 come from that CTA's
+// shared memory, the other halves from the odd CTA's at the same offsets;
+// each CTA's tensor memory receives its M/2 rows of D (all N columns).
+__device__ __forceinline__ void mma_f16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier at this shared-memory offset in every CTA of
+// `cta_mask` when the pair MMAs issued so far by this thread finish.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
 // 32 lanes x 32 consecutive 32-bit columns; thread i gets lane (base + i).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
@@ -244,6 +385,15 @@ __device__ __forceinline__ uint32_t fma_f16x2(uint32_t a, uint32_t b, uint32_t c
 }
 __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Four 8x8 b16 matrices from mma-fragment registers: register i of lane l
+// holds row l / 4, columns 2 (l % 4) and + 1 of matrix i; lanes 8 i .. 8 i + 7
+// give the shared addresses of matrix i's rows (16 bytes each).
+__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                        uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

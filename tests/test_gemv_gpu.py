@@ -66,7 +66,7 @@ def test_full_size_sampled_rows(layer, m):
     """Full workload shapes in the benchmarked launch; the oracle computes a
     seeded sample of output rows for all tokens: 512 at random plus two of
     every 512-row block (the GEMV's unit of rows, so every block, every
-    block's owners and every fixup slot are looked at)."""
+    block's owners and every owner's slot are looked at)."""
     d = I.make_layer(layer, m, seed=0)
     y = _decode(_layer(d.codes, d.scales), d.x_bits, m)
     rows = block_sample_rows(layer.n, seed=1)
@@ -78,13 +78,20 @@ def test_full_size_sampled_rows(layer, m):
                       what=f"{layer.name} M={m}")
 
 
-def test_repeat_calls_reuse_workspace():
-    d = I.make_layer(I.QKV, 4, seed=3)
-    layer = _layer(d.codes, d.scales)
+@pytest.mark.parametrize("layer,m", [(I.QKV, 4), (I.DOWN, 1), (I.DOWN, 16), (I.GATE_UP, 8)])
+def test_repeat_calls_reuse_workspace(layer, m):
+    """Repeated calls on one workspace give the same bits, in-kernel sums
+    (gate/up at M <= 8) and fixup shapes alike: the shared blocks' slots are
+    added in slot order, and every call leaves the ready tags at zero, so
+    the next call's first owners wait for fresh words."""
+    d = I.make_layer(layer, m, seed=3)
+    lay = _layer(d.codes, d.scales)
     ws = B.Workspace()
-    y1 = _decode(layer, d.x_bits, 4, ws)
-    y2 = _decode(layer, d.x_bits, 4, ws)
-    assert np.array_equal(y1, y2)          # deterministic; counters were reset
+    ys = [_decode(lay, d.x_bits, m, ws) for _ in range(4)]
+    for y in ys[1:]:
+        assert np.array_equal(y.view(np.uint32), ys[0].view(np.uint32))
+    tags = ws.buf[:B.tern_workspace_bytes(B.TERN_OP_GEMV, m, layer.n, layer.k)]
+    assert not tags.view(torch.int32)[1::2].any()          # the high half of every 64-bit word
 
 
 def test_special_weights():
