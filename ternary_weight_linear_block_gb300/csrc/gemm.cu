@@ -52,15 +52,16 @@ constexpr int TMEM_COLS = 512;
 // tern_selftest_wait), so 2^18 polls give up after about one second; a
 // wait of the working kernel lasts microseconds.
 constexpr uint32_t WAIT_LIMIT = 1u << 18;
-// Polls of a polling wait (a test and a 32 ns sleep each) before it gives
-// up: about a second.
-constexpr uint32_t POLL_LIMIT = 1u << 24;
 // Tests of a spinning wait (no sleep) before it gives up: about a second.
 constexpr uint32_t SPIN_LIMIT = 1u << 26;
 constexpr uint32_t IDESC = ptx::idesc_f16_f32(BM, BN);
 // a CTA pair's MMA: 256 rows (128 per CTA) x 256 columns
 constexpr uint32_t IDESC_PAIR = ptx::idesc_f16_f32(256, 256);
 constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
+// a CTA pair's stage: 128 tokens and 128 weight rows (32 KB), six of them in
+// the single CTA's four-stage area
+constexpr int PAIR_STAGES = 6;
+static_assert(PAIR_STAGES * (A_BYTES + B_BYTES / 2) <= STAGES * STAGE_BYTES, "pair stages fit");
 
 enum : unsigned int {
   ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_EPILOGUE = 4u, ERR_DRAIN = 8u, ERR_EXPAND = 16u,
@@ -84,7 +85,18 @@ __device__ __forceinline__ void fail(volatile int* abort_flag, unsigned int code
 // 1024-chunks (units of work = (tile, slice)); a slice stores its partial
 // sums (int32 or fp32) in its own [128][256] piece of `part`, and a second
 // kernel adds each tile's pieces in slice order and finishes the output.
-template <bool FP, bool SPLIT>
+//
+// PAIR (M > 128): clusters of two CTAs share each 256-token x 256-weight-row
+// tile (tcgen05 cta_group::2).  Each CTA loads its own 128 tokens and 128
+// weight rows (32 KB a stage, six stages), warp 3 relays "stage s landed" to
+// the even CTA's pfull[s], and the even CTA issues 256 x 256 x 16 MMAs whose
+// commits arrive (multicast) on both CTAs' barriers; each CTA's epilogue
+// drains its 128 token rows (all 256 weight columns) and releases the
+// accumulator buffer on the even CTA's dempty.  Per SM this halves the
+// weight copies into shared memory and the tensor cores' reads of them, and
+// shared-memory bandwidth (operand copies in, operand reads out) bounds the
+// single-CTA tile.
+template <bool FP, bool SPLIT, bool PAIR>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const float* __restrict__ tscale,
                                           const float* __restrict__ rscale, int M, int N, int K,
@@ -92,22 +104,30 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                                           int32_t* __restrict__ acc_out, int S_arg,
                                           int full_arg, void* __restrict__ part) {
   const int S = SPLIT ? S_arg : 1;
+  constexpr int NST = PAIR ? PAIR_STAGES : STAGES;
+  constexpr int TM = PAIR ? 2 * BM : BM;              // token rows of a tile
+  constexpr int BB = PAIR ? B_BYTES / 2 : B_BYTES;    // this CTA's weight rows, one stage
+  constexpr int WROWS_CTA = PAIR ? BN / 2 : BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* dfull = empty + STAGES;
+  uint8_t* sB = smem + NST * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * (A_BYTES + BB));
+  uint64_t* empty = full + NST;
+  uint64_t* dfull = empty + NST;
   uint64_t* dempty = dfull + 2;
   uint64_t* done = dempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* pfull = done + 1;   // (pairs) both CTAs' stage landed, in the even CTA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pfull + NST);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_blocks = (M + BM - 1) / BM;
+  const int rank = PAIR ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+  const int team = PAIR ? static_cast<int>(ptx::cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int teams = PAIR ? static_cast<int>(ptx::cluster_count_x()) : static_cast<int>(gridDim.x);
+  const int m_blocks = (M + TM - 1) / TM;
   const int n_blocks = (N + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
   const int chunks = K / KCHUNK;
@@ -134,21 +154,27 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&pfull[s], 2);   // (pairs) one relay arrival per CTA
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&dfull[b], 1);
-      ptx::mbar_init(&dempty[b], 8);   // one arrival per epilogue warp
+      ptx::mbar_init(&dempty[b], PAIR ? 16 : 8);   // one arrival per epilogue warp (of both CTAs)
     }
     ptx::mbar_init(done, 1);
     *abort_flag = 0;
     ptx::mbar_fence_init();
   }
   if (warp == 2) {
-    ptx::tmem_alloc(tmem_slot, TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
@@ -156,6 +182,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();   // both CTAs' barriers exist before any remote arrival
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -169,7 +196,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       uint32_t phase = 0;
       long issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int u = team; u < units && ok; u += teams) {
         int tile, c0, c1, piece;
         unit_of(u, tile, c0, c1, piece);
         const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
@@ -180,11 +207,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-          ptx::tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], ks * BK, m_blk * BM);
-          ptx::tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], ks * BK, n_blk * BN);
+          ptx::mbar_arrive_expect_tx(&full[s], A_BYTES + BB);
+          ptx::tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], ks * BK, m_blk * TM + rank * BM);
+          ptx::tma_load_2d(sB + s * BB, &tmB, &full[s], ks * BK, n_blk * BN + rank * WROWS_CTA);
           ++issued;
-          if (++s == STAGES) {
+          if (++s == NST) {
             s = 0;
             phase ^= 1u;
           }
@@ -192,12 +219,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       }
       if (!ok) {
         // let the copies still in flight land before the CTA exits
-        long back = issued < STAGES ? issued : STAGES;
+        long back = issued < NST ? issued : NST;
         int ss = s;
         uint32_t ph = phase;
         for (long i = 0; i < back; ++i) {
           if (--ss < 0) {
-            ss = STAGES - 1;
+            ss = NST - 1;
             ph ^= 1u;
           }
           if (!ptx::mbar_wait_bounded(&full[ss], ph, WAIT_LIMIT)) atomicOr(&g_gemm_error, ERR_DRAIN);
@@ -206,18 +233,21 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer (one thread)
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (one thread; in a pair, the even CTA's, for both)
       int s = 0;
       uint32_t phase = 0;
       uint32_t cc = 0;   // chunk counter across tiles
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int u = team; u < units && ok; u += teams) {
         int tile, c0, c1, piece;
         unit_of(u, tile, c0, c1, piece);
         for (int c = c0; c < c1 && ok; ++c, ++cc) {
           const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
-          if (!ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag, WAIT_LIMIT)) {
+          const bool drained =
+              PAIR ? ptx::mbar_spin_cluster(&dempty[buf], dph ^ 1u, abort_flag, SPIN_LIMIT)
+                   : ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag, WAIT_LIMIT);
+          if (!drained) {
             if (!*abort_flag) fail(abort_flag, ERR_MMA);
             ok = false;
             break;
@@ -225,30 +255,74 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           ptx::tc_fence_after();
           const uint32_t d_tmem = tmem + buf * BN;
           for (int j = 0; j < kStagesPerChunk; ++j) {
-            if (!ptx::mbar_wait(&full[s], phase, abort_flag, WAIT_LIMIT)) {
+            const bool ready = PAIR ? ptx::mbar_spin_cluster(&pfull[s], phase, abort_flag, SPIN_LIMIT)
+                                    : ptx::mbar_wait(&full[s], phase, abort_flag, WAIT_LIMIT);
+            if (!ready) {
               if (!*abort_flag) fail(abort_flag, ERR_MMA);
               ok = false;
               break;
             }
             ptx::tc_fence_after();
             const uint64_t a0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sA + s * A_BYTES));
-            const uint64_t b0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sB + s * B_BYTES));
+            const uint64_t b0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sB + s * BB));
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              ptx::mma_f16_ss(d_tmem, a0 + 2u * kk, b0 + 2u * kk, IDESC,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-            ptx::mma_commit(&empty[s]);
-            if (++s == STAGES) {
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              if constexpr (PAIR)
+                ptx::mma_f16_ss_pair(d_tmem, a0 + 2u * kk, b0 + 2u * kk, IDESC_PAIR,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+              else
+                ptx::mma_f16_ss(d_tmem, a0 + 2u * kk, b0 + 2u * kk, IDESC,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            if constexpr (PAIR)
+              ptx::mma_commit_pair(&empty[s], 0x3);
+            else
+              ptx::mma_commit(&empty[s]);
+            if (++s == NST) {
               s = 0;
               phase ^= 1u;
             }
           }
-          if (ok) ptx::mma_commit(&dfull[buf]);
+          if (ok) {
+            if constexpr (PAIR)
+              ptx::mma_commit_pair(&dfull[buf], 0x3);
+            else
+              ptx::mma_commit(&dfull[buf]);
+          }
         }
       }
       // every MMA issued by this thread has completed once `done` fires
-      ptx::mma_commit(done);
+      if constexpr (PAIR)
+        ptx::mma_commit_pair(done, 0x3);
+      else
+        ptx::mma_commit(done);
       if (!ptx::mbar_wait_bounded(done, 0, WAIT_LIMIT)) atomicOr(&g_gemm_error, ERR_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    if (PAIR && lane == 0) {
+      // ---------------- relay (pairs): once this CTA's stage has landed, one
+      // arrival on the even CTA's pfull[s]
+      int s = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t pf = ptx::mapa_shared(pfull, 0);
+      for (int u = team; u < units && ok; u += teams) {
+        int tile, c0, c1, piece;
+        unit_of(u, tile, c0, c1, piece);
+        for (int j = 0; j < (c1 - c0) * kStagesPerChunk; ++j) {
+          if (!ptx::mbar_spin_cluster(&full[s], phase, abort_flag, SPIN_LIMIT)) {
+            if (!*abort_flag) fail(abort_flag, ERR_MMA);
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_cluster(pf + 8u * static_cast<uint32_t>(s));
+          if (++s == NST) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+      }
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -257,11 +331,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     const int q = warp & 3;   // TMEM lane quarter accessible to this warp
     uint32_t cc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    for (int u = team; u < units && ok; u += teams) {
       int tile, c0, c1, piece;
       unit_of(u, tile, c0, c1, piece);
       const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
-      const int row = m_blk * BM + 32 * q + lane;
+      const int row = m_blk * TM + rank * BM + 32 * q + lane;
       typename std::conditional<FP, float, int32_t>::type sums[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sums[i] = 0;
@@ -293,16 +367,23 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&dempty[buf]);
+        if (lane == 0) {
+          if constexpr (PAIR)
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(&dempty[buf], 0));
+          else
+            ptx::mbar_arrive(&dempty[buf]);
+        }
       }
       if (!ok) break;
       if (SPLIT && piece >= 0) {
         // one slice of a split tile: its partial sums into the slice's
-        // [128][256] piece of `part`; the finishing kernel adds the pieces
+        // [TM][256] piece of `part` (this CTA's rows of it); the finishing
+        // kernel adds the pieces
         if (row < M) {
           const int n0 = n_blk * BN + wg * 128;
           auto* prow = static_cast<typename std::conditional<FP, float, int32_t>::type*>(part) +
-                       (static_cast<long>(piece) * BM + 32 * q + lane) * BN + wg * 128;
+                       (static_cast<long>(piece) * TM + rank * BM + 32 * q + lane) * BN +
+                       wg * 128;
 #pragma unroll
           for (int j = 0; j < 128; j += 8)
             if (n0 + j < N) {
@@ -376,7 +457,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if constexpr (PAIR) {
+    // the even CTA's MMAs (which read this CTA's shared memory and write its
+    // tensor memory) are done, and both epilogues have read their rows
+    ptx::cluster_sync();
+    if (warp == 2) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+  } else if (warp == 2) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -384,21 +473,21 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 
 // SPLIT = false: one unit per tile (no slice arithmetic in the loops);
 // SPLIT = true: S K slices per tile, partial sums to `part`.
-template <bool SPLIT>
+template <bool SPLIT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float* __restrict__ tscale, const float* __restrict__ rscale, int M,
                    int N, int K, __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out,
                    int S, int full, int32_t* __restrict__ part) {
-  gemm_body<false, SPLIT>(tmA, tmB, tscale, rscale, M, N, K, y, acc_out, S, full, part);
+  gemm_body<false, SPLIT, PAIR>(tmA, tmB, tscale, rscale, M, N, K, y, acc_out, S, full, part);
 }
 
-template <bool SPLIT>
+template <bool SPLIT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const float* __restrict__ xs, int M, int N, int K,
                     __nv_bfloat16* __restrict__ y, int S, int full, float* __restrict__ part) {
-  gemm_body<true, SPLIT>(tmA, tmB, xs, nullptr, M, N, K, y, nullptr, S, full, part);
+  gemm_body<true, SPLIT, PAIR>(tmA, tmB, xs, nullptr, M, N, K, y, nullptr, S, full, part);
 }
 
 // After a split GEMM: for every split tile (tiles full .. tiles-1), add its
@@ -408,25 +497,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 template <bool FP>
 __global__ void __launch_bounds__(256)
     split_finalize_kernel(const void* __restrict__ part, int S, int full, int n_split,
-                          int m_blocks, int M, int N, const float* __restrict__ tscale,
+                          int m_blocks, int tm, int M, int N, const float* __restrict__ tscale,
                           const float* __restrict__ rscale, __nv_bfloat16* __restrict__ y,
                           int32_t* __restrict__ acc_out) {
   pdl_launch_dependents();
   const long i = static_cast<long>(blockIdx.x) * 256 + threadIdx.x;
   constexpr int PER_ROW = BN / 8;
-  const long st = i / (BM * PER_ROW);
-  const int r = static_cast<int>((i / PER_ROW) % BM);
+  const long st = i / (static_cast<long>(tm) * PER_ROW);   // tiles of tm token rows
+  const int r = static_cast<int>((i / PER_ROW) % tm);
   const int c8 = static_cast<int>(i % PER_ROW);
   pdl_wait();   // the GEMM's pieces
   if (st >= n_split) return;
   const int tile = full + static_cast<int>(st);
   const int n_blk = tile / m_blocks, m_blk = tile % m_blocks;
-  const long row = static_cast<long>(m_blk) * BM + r;
+  const long row = static_cast<long>(m_blk) * tm + r;
   const int n = n_blk * BN + c8 * 8;
   if (row >= M || n >= N) return;
   typename std::conditional<FP, float, int>::type a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int sl = 0; sl < S; ++sl) {
-    const long off = ((st * S + sl) * BM + r) * BN + c8 * 8;
+    const long off = ((st * S + sl) * tm + r) * BN + c8 * 8;
     if constexpr (FP) {
       const float* p = static_cast<const float*>(part) + off;
       const float4 a0 = __ldcs(reinterpret_cast<const float4*>(p));
@@ -1154,6 +1243,10 @@ int sm_count() {
   return n;
 }
 
+// Token rows of a dense GEMM tile: 128 for one CTA, 256 for a CTA pair
+// (above one 128-token block).
+long dense_tile_rows(int64_t M) { return M > BM ? 2 * BM : BM; }
+
 }  // namespace
 
 // How the expanded-weight GEMMs cut their work: the first `full` tiles whole,
@@ -1163,18 +1256,20 @@ int sm_count() {
 // writing and reading the partial pieces and a launch for the finishing
 // kernel; a split has to win clearly.
 DensePlan dense_plan(int64_t M, int64_t N, int64_t K) {
-  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const long sms = sm_count();
+  // a team is one SM's CTA, or (M > 128) a CTA pair with twice the tile
+  const long tm = dense_tile_rows(M);
+  const long tiles = ((M + tm - 1) / tm) * ((N + BN - 1) / BN);
+  const long sms = tm == BM ? sm_count() : sm_count() / 2;
   const long chunks = K / KCHUNK;
   const double t_chunk = 5.9e-6, bw = 6.0e12, t_launch = 3e-6;
-  const double piece_bytes = static_cast<double>(BM) * BN * 4;
+  const double piece_bytes = static_cast<double>(tm) * BN * 4;
   auto cost = [&](long full, long S) {
     const long split = tiles - full;
     const long per_cta_whole = (full + sms - 1) / sms;
     const long per_cta_split = (split * S + sms - 1) / sms;
     double t = (static_cast<double>(per_cta_whole) * chunks +
                 static_cast<double>(per_cta_split) * ((chunks + S - 1) / S)) * t_chunk;
-    if (S > 1) t += (2.0 * split * S * piece_bytes + 2.0 * split * BM * BN) / bw + t_launch;
+    if (S > 1) t += (2.0 * split * S * piece_bytes + 2.0 * split * tm * BN) / bw + t_launch;
     return t;
   };
   DensePlan best{1, static_cast<int>(tiles)};
@@ -1200,8 +1295,9 @@ DensePlan dense_plan(int64_t M, int64_t N, int64_t K) {
 size_t gemm_dense_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const DensePlan p = dense_plan(M, N, K);
   if (p.S == 1) return 0;
-  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  return static_cast<size_t>(tiles - p.full) * p.S * BM * BN * 4;
+  const long tm = dense_tile_rows(M);
+  const long tiles = ((M + tm - 1) / tm) * ((N + BN - 1) / BN);
+  return static_cast<size_t>(tiles - p.full) * p.S * tm * BN * 4;
 }
 
 int dense_splits(int64_t M, int64_t N, int64_t K) { return dense_plan(M, N, K).S; }
@@ -1211,7 +1307,8 @@ namespace {
 // workspace, else everything whole.
 DensePlan usable_plan(int64_t M, int64_t N, int64_t K, const void* ws, size_t ws_bytes) {
   const DensePlan p = dense_plan(M, N, K);
-  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const long tm = dense_tile_rows(M);
+  const long tiles = ((M + tm - 1) / tm) * ((N + BN - 1) / BN);
   if (p.S > 1 && (ws == nullptr || ws_bytes < gemm_dense_workspace_bytes(M, N, K)))
     return DensePlan{1, static_cast<int>(tiles)};
   return p;
@@ -1221,25 +1318,61 @@ template <bool FP>
 cudaError_t launch_split_finalize(const void* part, const DensePlan& p, int64_t M, int64_t N,
                                   const float* tscale, const float* rscale, uint16_t* y,
                                   int32_t* acc, cudaStream_t st) {
-  const long m_blocks = (M + BM - 1) / BM;
+  const long tm = dense_tile_rows(M);
+  const long m_blocks = (M + tm - 1) / tm;
   const long tiles = m_blocks * ((N + BN - 1) / BN);
   const long n_split = tiles - p.full;
-  const long threads = n_split * BM * (BN / 8);
+  const long threads = n_split * tm * (BN / 8);
   return launch(split_finalize_kernel<FP>, dim3(static_cast<unsigned>((threads + 255) / 256)),
                 dim3(256), 0, st, part, p.S, p.full, static_cast<int>(n_split),
-                static_cast<int>(m_blocks), static_cast<int>(M), static_cast<int>(N), tscale,
-                rscale, reinterpret_cast<__nv_bfloat16*>(y), acc);
+                static_cast<int>(m_blocks), static_cast<int>(tm), static_cast<int>(M),
+                static_cast<int>(N), tscale, rscale, reinterpret_cast<__nv_bfloat16*>(y), acc);
+}
+
+// Launch one of a dense GEMM's four kernels (split or not, pair or not):
+// pairs run as clusters of two, as many as fit on the device at once.
+template <typename Kern, typename... Args>
+cudaError_t launch_dense(Kern kern, bool pair, long units, cudaStream_t st, Args... args) {
+  if (!pair) {
+    const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
+    return launch(kern, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, args...);
+  }
+  // the number of pairs that fit, queried once per kernel
+  static std::atomic<const void*> keys[4];
+  static std::atomic<int> vals[4];
+  const void* key = reinterpret_cast<const void*>(kern);
+  int pairs = 0;
+  for (int i = 0; i < 4 && pairs == 0; ++i)
+    if (keys[i].load(std::memory_order_acquire) == key) pairs = vals[i].load(std::memory_order_acquire);
+  if (pairs == 0) {
+    pairs = max_active_clusters(kern, dim3(NUM_THREADS), SMEM_BYTES, 2);
+    if (pairs <= 0) return cudaErrorNotSupported;
+    for (int i = 0; i < 4; ++i) {
+      const void* expect = nullptr;
+      if (keys[i].load(std::memory_order_acquire) == key) break;
+      if (vals[i].load(std::memory_order_acquire) == 0) {
+        vals[i].store(pairs, std::memory_order_release);
+        if (keys[i].compare_exchange_strong(expect, key)) break;
+      }
+    }
+  }
+  const long teams = units < pairs ? units : pairs;
+  return launch_cluster(kern, dim3(static_cast<unsigned>(2 * teams)), dim3(NUM_THREADS),
+                        SMEM_BYTES, st, 2u, args...);
 }
 }  // namespace
 
 cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t* w_q,
                         const float* rscale, int64_t M, int64_t N, int64_t K, uint16_t* y,
                         int32_t* acc, void* ws, size_t ws_bytes, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, xq, M, K, BM) || !make_map(&tb, w_q, N, K, BN)) return cudaErrorInvalidValue;
+  const bool pair = dense_tile_rows(M) > BM;
+  CUtensorMap ta, tb;   // token boxes of 128 rows; weight boxes of 256 rows (128 in a pair)
+  if (!make_map(&ta, xq, M, K, BM) || !make_map(&tb, w_q, N, K, pair ? BN / 2 : BN))
+    return cudaErrorInvalidValue;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t ea = once_per_device(attr_done, [] {
-    for (auto* kern : {gemm_i8_kernel<false>, gemm_i8_kernel<true>}) {
+    for (auto* kern : {gemm_i8_kernel<false, false>, gemm_i8_kernel<true, false>,
+                       gemm_i8_kernel<false, true>, gemm_i8_kernel<true, true>}) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_BYTES));
       if (e != cudaSuccess) return e;
@@ -1249,13 +1382,14 @@ cudaError_t launch_gemm(const uint16_t* xq, const float* tscale, const uint16_t*
   if (ea != cudaSuccess) return ea;
   const DensePlan p = usable_plan(M, N, K, ws, ws_bytes);
   int32_t* part = p.S > 1 ? static_cast<int32_t*>(ws) : nullptr;
-  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const long tm = dense_tile_rows(M);
+  const long tiles = ((M + tm - 1) / tm) * ((N + BN - 1) / BN);
   const long units = p.full + (tiles - p.full) * p.S;
-  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
-  cudaError_t e = launch(p.S > 1 ? gemm_i8_kernel<true> : gemm_i8_kernel<false>, dim3(grid),
-                         dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, tscale, rscale,
-                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                         reinterpret_cast<__nv_bfloat16*>(y), acc, p.S, p.full, part);
+  auto* kern = p.S > 1 ? (pair ? gemm_i8_kernel<true, true> : gemm_i8_kernel<true, false>)
+                       : (pair ? gemm_i8_kernel<false, true> : gemm_i8_kernel<false, false>);
+  cudaError_t e = launch_dense(kern, pair, units, st, ta, tb, tscale, rscale, static_cast<int>(M),
+                               static_cast<int>(N), static_cast<int>(K),
+                               reinterpret_cast<__nv_bfloat16*>(y), acc, p.S, p.full, part);
   if (e != cudaSuccess || p.S == 1) return e;
   return launch_split_finalize<false>(part, p, M, N, tscale, rscale, y, acc, st);
 }
@@ -1358,11 +1492,14 @@ cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const ui
 cudaError_t launch_gemm_f16(const uint16_t* xh, const float* xs, const uint16_t* w_h, int64_t M,
                             int64_t N, int64_t K, uint16_t* y, void* ws, size_t ws_bytes,
                             cudaStream_t st) {
+  const bool pair = dense_tile_rows(M) > BM;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, xh, M, K, BM) || !make_map(&tb, w_h, N, K, BN)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, xh, M, K, BM) || !make_map(&tb, w_h, N, K, pair ? BN / 2 : BN))
+    return cudaErrorInvalidValue;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t ea = once_per_device(attr_done, [] {
-    for (auto* kern : {gemm_f16_kernel<false>, gemm_f16_kernel<true>}) {
+    for (auto* kern : {gemm_f16_kernel<false, false>, gemm_f16_kernel<true, false>,
+                       gemm_f16_kernel<false, true>, gemm_f16_kernel<true, true>}) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_BYTES));
       if (e != cudaSuccess) return e;
@@ -1372,13 +1509,14 @@ cudaError_t launch_gemm_f16(const uint16_t* xh, const float* xs, const uint16_t*
   if (ea != cudaSuccess) return ea;
   const DensePlan p = usable_plan(M, N, K, ws, ws_bytes);
   float* part = p.S > 1 ? static_cast<float*>(ws) : nullptr;
-  const long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const long tm = dense_tile_rows(M);
+  const long tiles = ((M + tm - 1) / tm) * ((N + BN - 1) / BN);
   const long units = p.full + (tiles - p.full) * p.S;
-  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
-  cudaError_t e = launch(p.S > 1 ? gemm_f16_kernel<true> : gemm_f16_kernel<false>, dim3(grid),
-                         dim3(NUM_THREADS), SMEM_BYTES, st, ta, tb, xs, static_cast<int>(M),
-                         static_cast<int>(N), static_cast<int>(K),
-                         reinterpret_cast<__nv_bfloat16*>(y), p.S, p.full, part);
+  auto* kern = p.S > 1 ? (pair ? gemm_f16_kernel<true, true> : gemm_f16_kernel<true, false>)
+                       : (pair ? gemm_f16_kernel<false, true> : gemm_f16_kernel<false, false>);
+  cudaError_t e = launch_dense(kern, pair, units, st, ta, tb, xs, static_cast<int>(M),
+                               static_cast<int>(N), static_cast<int>(K),
+                               reinterpret_cast<__nv_bfloat16*>(y), p.S, p.full, part);
   if (e != cudaSuccess || p.S == 1) return e;
   return launch_split_finalize<true>(part, p, M, N, nullptr, nullptr, y, nullptr, st);
 }
