@@ -201,13 +201,16 @@ class DecodeRunner:
         self.i = 0
 
     def step(self):
-        """One decode pass per batch; each batch streams the next weight copy."""
+        """One decode pass per batch; each batch streams the next weight copy.
+        The batches are independent, so their rotations are issued first and
+        overlap each other; then the GEMVs run back to back."""
         st = self.stream.cuda_stream
+        for b, m in enumerate(self.ms):
+            B.tern_fwht_quant(self.x[b], m, self.k, None, B.TERN_FWHT_DECODE, self.xh[b],
+                              self.xs[b], st)
         for b, m in enumerate(self.ms):
             layer = self.layers[self.i % len(self.layers)]
             self.i += 1
-            B.tern_fwht_quant(self.x[b], m, self.k, None, B.TERN_FWHT_DECODE, self.xh[b],
-                              self.xs[b], st)
             B.tern_gemv_decode(layer.packed, self.xh[b], self.xs[b], m, self.n, self.k, self.y[b],
                                self.ws[b], self.ws[b].numel(), st)
 

@@ -424,7 +424,8 @@ class _DecodeCall:
         nb = tern_workspace_bytes(TERN_OP_GEMV, m, layer.n, layer.k)
         self.ws = Workspace(device).get(nb)
 
-    def body(self):
+    def first(self):
+        """The input's copy (if any) and the rotation (the fused call: all of it)."""
         lay, m = self.layer, self.m
         st = torch.cuda.current_stream().cuda_stream
         if not self.zero_copy:
@@ -435,8 +436,14 @@ class _DecodeCall:
                                self.ws.numel(), st)
         else:
             tern_fwht_quant(x, m, lay.k, self.sign, TERN_FWHT_DECODE, self.xh, self.xs, st)
-            tern_gemv_decode(lay.packed, self.xh, self.xs, m, lay.n, lay.k, y, self.ws,
-                             self.ws.numel(), st)
+
+    def second(self):
+        """The GEMV (two-call form) and the output's copy (if any)."""
+        lay, m = self.layer, self.m
+        st = torch.cuda.current_stream().cuda_stream
+        if not self.fused:
+            tern_gemv_decode(lay.packed, self.xh, self.xs, m, lay.n, lay.k, self.y.data_ptr(),
+                             self.ws, self.ws.numel(), st)
         if not self.zero_copy:
             self.y_host.copy_(self.y, non_blocking=True)
 
@@ -455,7 +462,11 @@ class DecodeStepGraph:
     Where the GPU can address the pinned buffers directly
     (tern_host_accessible, e.g. over NVLink-C2C on Grace-Blackwell) the
     rotation reads x from host memory and the GEMV writes y into it, with no
-    copy (``zero_copy=None`` chooses; True forces it, False uses copies)."""
+    copy (``zero_copy=None`` chooses; True forces it, False uses copies).
+
+    Every call reads its own host input, so the calls are independent: the
+    graph issues all the rotations first (they overlap one another) and then
+    the GEMVs back to back."""
 
     def __init__(self, entries, sign: torch.Tensor | None = None, fused: bool = False,
                  device="cuda", zero_copy: bool | None = None):
@@ -472,7 +483,9 @@ class DecodeStepGraph:
 
     def _body(self):
         for c in self.calls:
-            c.body()
+            c.first()
+        for c in self.calls:
+            c.second()
 
     def launch(self):
         """Replay on the current stream without waiting."""
