@@ -52,8 +52,6 @@ constexpr int TMEM_COLS = 512;
 // tern_selftest_wait), so 2^18 polls give up after about one second; a
 // wait of the working kernel lasts microseconds.
 constexpr uint32_t WAIT_LIMIT = 1u << 18;
-// Tests of a spinning wait (no sleep) before it gives up: about a second.
-constexpr uint32_t SPIN_LIMIT = 1u << 26;
 constexpr uint32_t IDESC = ptx::idesc_f16_f32(BM, BN);
 // a CTA pair's MMA: 256 rows (128 per CTA) x 256 columns
 constexpr uint32_t IDESC_PAIR = ptx::idesc_f16_f32(256, 256);
@@ -244,10 +242,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         unit_of(u, tile, c0, c1, piece);
         for (int c = c0; c < c1 && ok; ++c, ++cc) {
           const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
-          const bool drained =
-              PAIR ? ptx::mbar_spin_cluster(&dempty[buf], dph ^ 1u, abort_flag, SPIN_LIMIT)
-                   : ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag, WAIT_LIMIT);
-          if (!drained) {
+          if (!ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_MMA);
             ok = false;
             break;
@@ -255,9 +250,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           ptx::tc_fence_after();
           const uint32_t d_tmem = tmem + buf * BN;
           for (int j = 0; j < kStagesPerChunk; ++j) {
-            const bool ready = PAIR ? ptx::mbar_spin_cluster(&pfull[s], phase, abort_flag, SPIN_LIMIT)
-                                    : ptx::mbar_wait(&full[s], phase, abort_flag, WAIT_LIMIT);
-            if (!ready) {
+            // (pairs: the even CTA waits until both CTAs' stage has landed)
+            if (!ptx::mbar_wait(PAIR ? &pfull[s] : &full[s], phase, abort_flag, WAIT_LIMIT)) {
               if (!*abort_flag) fail(abort_flag, ERR_MMA);
               ok = false;
               break;
@@ -311,7 +305,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         int tile, c0, c1, piece;
         unit_of(u, tile, c0, c1, piece);
         for (int j = 0; j < (c1 - c0) * kStagesPerChunk; ++j) {
-          if (!ptx::mbar_spin_cluster(&full[s], phase, abort_flag, SPIN_LIMIT)) {
+          if (!ptx::mbar_wait(&full[s], phase, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_MMA);
             ok = false;
             break;
@@ -825,11 +819,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         unit_of(u, tile, g0, g1);
         for (int gp = g0; gp < g1 && ok; gp = piece_end(gp, g1), ++cc) {
           const uint32_t buf = cc & 1u, dph = (cc >> 1) & 1u;
-          const bool drained = PAIR ? ptx::mbar_spin_cluster(&dempty[buf], dph ^ 1u, abort_flag,
-                                                             SPIN_LIMIT)
-                                    : ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag,
-                                                     WAIT_LIMIT);
-          if (!drained) {
+          if (!ptx::mbar_wait(&dempty[buf], dph ^ 1u, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_MMA);
             ok = false;
             break;
@@ -839,7 +829,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           const int n_stages = 2 * (piece_end(gp, g1) - gp);
           for (int j = 0; j < n_stages; ++j) {
             const bool ready =
-                PAIR ? ptx::mbar_spin_cluster(&pfull[s], ph, abort_flag, SPIN_LIMIT)
+                PAIR ? ptx::mbar_wait(&pfull[s], ph, abort_flag, WAIT_LIMIT)
                      : (ptx::mbar_wait(&afull[s], ph, abort_flag, WAIT_LIMIT) &&
                         ptx::mbar_wait(&wfull[s], ph, abort_flag, WAIT_LIMIT));
             if (!ready) {
@@ -893,8 +883,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         int tile, g0, g1;
         unit_of(u, tile, g0, g1);
         for (int j = 0; j < 2 * (g1 - g0); ++j) {
-          if (!ptx::mbar_spin_cluster(&afull[s], ph, abort_flag, SPIN_LIMIT) ||
-              !ptx::mbar_spin_cluster(&wfull[s], ph, abort_flag, SPIN_LIMIT)) {
+          if (!ptx::mbar_wait(&afull[s], ph, abort_flag, WAIT_LIMIT) ||
+              !ptx::mbar_wait(&wfull[s], ph, abort_flag, WAIT_LIMIT)) {
             if (!*abort_flag) fail(abort_flag, ERR_MMA);
             ok = false;
             break;
