@@ -376,7 +376,9 @@ tern_status tern_gemm_prefill_int8(const int8_t* xq, const float* tscale, const 
 
 /* ------------------------------------------------------------------------
  * tern_gemm_prefill_int8h -- the same GEMM on the int8 integers held in fp16
- * (tcgen05.mma kind::f16, TMA-fed, TMEM accumulators, fused rescale):
+ * (tcgen05.mma kind::f16, TMA-fed, TMEM accumulators, fused rescale).  Tiles
+ * are 128 tokens x 256 weight rows per CTA up to M = 128; above, 256 tokens x
+ * 256 weight rows per cluster of two CTAs sharing each MMA (cta_group::2):
  *
  *   xq      fp16 [M][K] holding xq (TERN_FWHT_I8H output), tscale fp32 [M]
  *   w_q     fp16 [N][K] holding W_int8 (tern_widen_int8 of tern_pack's
@@ -385,12 +387,13 @@ tern_status tern_gemm_prefill_int8(const int8_t* xq, const float* tscale, const 
  *   acc     int32 [M][N] or NULL
  *   ws      optional device workspace (any contents) of
  *           tern_workspace_bytes(TERN_OP_GEMM, M, N, K) bytes.  With it, a
- *           call whose 128 x 256 tiles fill the GPU unevenly splits K in
- *           slices of whole 1024-chunks -- in every tile, or only in the
- *           tiles of the last, partial wave, as a cost model picks: the
- *           slices' exact int32 partial sums go to [128][256] pieces in ws
- *           and a second kernel adds them and rescales (same results bit
- *           for bit).  With NULL (or less) the call runs unsplit.  A split call leaves partial sums
+ *           call whose tiles fill the GPU unevenly splits K in slices of
+ *           whole 1024-chunks -- in every tile, or only in the tiles of the
+ *           last, partial wave, as a cost model picks: the slices' exact
+ *           int32 partial sums go to one piece per tile and slice in ws
+ *           ([128][256], or [256][256] for the pairs' tiles) and a second
+ *           kernel adds them and rescales (same results bit for bit).  With
+ *           NULL (or less) the call runs unsplit.  A split call leaves partial sums
  *           in ws: a buffer also used as a tern_gemv_decode workspace must
  *           be zero-filled again (tern_workspace_init) before that call.
  * Requirements: K % 1024 == 0, K <= 65536, M >= 0, N % 16 == 0, N >= 0.
@@ -411,8 +414,9 @@ tern_status tern_gemm_prefill_int8h(const uint16_t* xq, const float* tscale, con
  *     acc[m,n]    = sum_k xq[m,k] * W_int8[n,k]  (exact int32)
  *     y[m,n]      = bf16_rn(((float)acc[m,n] * tscale[m]) * rscale[n])
  * Results are bit-identical to tern_gemm_prefill_int8 on the same layer.
- * Tiles: 128 tokens x 256 weight rows up to M = 128; above, 256 tokens x
- * 128 weight rows (the weights on the MMA's M side, so each expanded weight
+ * Tiles: 128 tokens x 256 weight rows up to M = 128; above, 256 weight rows
+ * x 256 tokens per cluster of two CTAs (cta_group::2; the weights on the
+ * MMA's M side, each CTA expanding its 128 rows, so each expanded weight
  * serves 256 tokens).  The weights are read at 2 bits each (plus q) once
  * per token block, so mid-size M costs the packed bytes instead of the
  * 2-byte expanded weight.
