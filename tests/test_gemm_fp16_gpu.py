@@ -58,7 +58,7 @@ def test_tiny_layer(m):
 
 
 @pytest.mark.parametrize("m,n,k", [(300, 272, 2048), (129, 528, 3072), (257, 1040, 5120),
-                                   (40, 256, 17408)])
+                                   (40, 256, 17408), (130, 16, 1024)])
 def test_ragged_shapes(m, n, k):
     codes = I.make_codes(17, n, k)
     scales = I.make_scales(17, n, k)

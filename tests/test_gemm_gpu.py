@@ -70,9 +70,12 @@ def test_tiny_layer(m, typed):
 
 
 @pytest.mark.parametrize("m,n,k", [(300, 272, 2048), (129, 528, 3072), (64, 256, 1024),
-                                   (257, 1040, 5120)])
+                                   (257, 1040, 5120), (130, 16, 1024), (384, 144, 2048)])
 @pytest.mark.parametrize("typed", [False, True])
 def test_ragged_shapes(m, n, k, typed):
+    """Ragged M and N on both sides of the switch to CTA pairs (M > 128),
+    including pair tiles whose odd CTA holds no valid weight row (N = 16)
+    or only 16 of its 128 (N = 144)."""
     codes = I.make_codes(11, n, k)
     scales = I.make_scales(11, n, k)
     bits, x = I.make_activations(11, m, k, 0.01, 20.0)

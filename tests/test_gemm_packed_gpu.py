@@ -53,7 +53,8 @@ def test_tiny_layer(m):
 
 
 @pytest.mark.parametrize("m,n,k", [(300, 272, 2048), (129, 528, 3072), (64, 112, 1024),
-                                   (257, 1040, 5120), (31, 1008, 1024), (50, 784, 2048)])
+                                   (257, 1040, 5120), (31, 1008, 1024), (50, 784, 2048),
+                                   (130, 16, 1024), (384, 144, 2048)])
 def test_ragged_shapes(m, n, k):
     codes = I.make_codes(13, n, k)
     scales = I.make_scales(13, n, k)
