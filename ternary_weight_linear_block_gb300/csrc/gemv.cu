@@ -275,7 +275,7 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
   // the other slots in order: all words of a slot are loaded before any is
   // checked, so a slot published long ago costs one memory round trip; a slot
   // not yet complete is retried (bounded)
-  constexpr int SB = 1;
+  constexpr int SB = 2;   // slots loaded per round (3: more registers, a slower hot loop)
   bool ok = true;
   for (int sl0 = 1; sl0 < nslots && ok; sl0 += SB) {
     unsigned long long w[SB][NV];
