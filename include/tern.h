@@ -428,11 +428,15 @@ tern_status tern_gemm_prefill_int8h(const uint16_t* xq, const float* tscale, con
  *   acc     int32 [M][N] or NULL
  *   ws      device workspace of tern_workspace_bytes(TERN_OP_GEMM_PACKED,
  *           M, N, K) bytes (any contents; NULL when that is 0).  When the
- *           tiles are too few to fill the GPU, each tile's K range is split
- *           in S slices of whole 128-groups whose exact int32 partial sums
- *           go to S planes [M][N] of ws; a second kernel adds the planes
- *           (integer sums: the same result in any order) and applies the
- *           rescale (tern_kernel_launches).  As for tern_gemm_prefill_int8,
+ *           tiles fill the GPU unevenly, K ranges are split in S slices of
+ *           whole 128-groups whose exact int32 partial sums a second kernel
+ *           adds (integer sums: the same result in any order) before the
+ *           rescale (tern_kernel_launches).  Up to 128 tokens, with too few
+ *           tiles for the GPU, every tile is split and the slices' sums go
+ *           to S planes [M][N] of ws; above, the whole waves of pair tiles
+ *           stay whole and only the last, partial wave's tiles (all tiles
+ *           when there are fewer than pairs) are split, one [256][256]
+ *           piece per tile and slice in ws.  As for tern_gemm_prefill_int8,
  *           a split call leaves partial sums in ws.
  * Requirements: K % 1024 == 0, K <= 65536, N % 16 == 0, 0 <= M, N <= 2^24.
  * Device-side waits are bounded; a wait that gives up makes the call's

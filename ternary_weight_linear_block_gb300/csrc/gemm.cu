@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                        const int8_t* __restrict__ q, const float* __restrict__ tscale,
                        const float* __restrict__ rscale, int M, int N, int K,
                        __nv_bfloat16* __restrict__ y, int32_t* __restrict__ acc_out, int S,
-                       int32_t* __restrict__ part) {
+                       int full, int32_t* __restrict__ part) {
   // a pair's stage holds 128 tokens (16 KB) instead of 256, so six stages
   // fit where a single CTA has four
   constexpr int NST = PAIR ? PSTAGES_PAIR : PSTAGES;
@@ -689,15 +689,24 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   };
   const int m_blocks = (M + TOK - 1) / TOK;   // token blocks (fastest in the tile order)
   const int tiles = m_blocks * ((N + CTAS * WROWS - 1) / (CTAS * WROWS));
-  const int units = tiles * S;   // unit = (tile, K slice of whole 128-groups)
+  // units: the first `full` tiles whole, then every later tile in S K
+  // slices of whole 128-groups (S = 1: all whole)
+  const int units = full + (tiles - full) * S;
   // the tile and the group range [g0, g1) of a unit; the MMA accumulates it
   // in pieces that end at every 1024-chunk boundary (and at g1), so each
   // fp32 partial stays exact
   auto unit_of = [&](int u, int& tile, int& g0, int& g1) {
-    tile = u / S;
-    const int sl = u % S;
-    g0 = sl * G / S;
-    g1 = (sl + 1) * G / S;
+    if (u < full) {
+      tile = u;
+      g0 = 0;
+      g1 = G;
+    } else {
+      const int v = u - full;
+      tile = full + v / S;
+      const int sl = v % S;
+      g0 = sl * G / S;
+      g1 = (sl + 1) * G / S;
+    }
   };
   auto piece_end = [&](int gp, int g1) {
     const int e = (gp / 8 + 1) * 8;
@@ -948,11 +957,14 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         const int n = n_blk * WROWS + 32 * qd + lane;
         const int t0 = m_blk * TOK + wg * 128;
         if (n < N) {
-          if (S > 1) {
-            int32_t* pcol = part + static_cast<long>(u % S) * M * N + n;
+          if (u >= full) {
+            // one K slice of a split tile: its exact partial sums go to the
+            // slice's piece [256 tokens][256 weight rows] of `part` (this
+            // CTA's 128 rows), which the finishing kernel adds
+            int32_t* pcol = part + (static_cast<long>(u - full) * TOK + wg * 128) * (CTAS * WROWS) +
+                            rank * WROWS + 32 * qd + lane;
 #pragma unroll
-            for (int j = 0; j < 128; ++j)
-              if (t0 + j < M) pcol[static_cast<long>(t0 + j) * N] = sums[j];
+            for (int j = 0; j < 128; ++j) pcol[j * (CTAS * WROWS)] = sums[j];
           } else {
             const float rs = rscale[n];
 #pragma unroll
@@ -970,7 +982,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         continue;
       }
       const int row = m_blk * BM + 32 * qd + lane;
-      if (S > 1) {
+      if (u >= full) {
         // one K slice of the tile: store its exact partial sums in the
         // slice's plane of the workspace; the rescale kernel adds the planes
         if (row < M) {
@@ -1242,16 +1254,18 @@ long dense_tile_rows(int64_t M) { return M > BM ? 2 * BM : BM; }
 // How the expanded-weight GEMMs cut their work: the first `full` tiles whole,
 // the others (the last, partial wave, or all tiles) in S slices of whole
 // 1024-chunks.  The plan with the least estimated time wins: waves of units
-// x chunks per unit x one tile-chunk (~5.9 us measured on GB300), plus
-// writing and reading the partial pieces and a launch for the finishing
-// kernel; a split has to win clearly.
+// x chunks per unit x one tile-chunk (measured on GB300: ~5.9 us for a
+// CTA's 128 x 256 tile, ~5.2 us for a pair's 256 x 256), plus writing and
+// reading the partial pieces and a launch for the finishing kernel; a split
+// has to win by 1 %.  (Gate/up at M = 2048, 1088 pair tiles on 76 pairs:
+// the last wave's 24 tiles in 3 slices, 387 -> 380 us.)
 DensePlan dense_plan(int64_t M, int64_t N, int64_t K) {
   // a team is one SM's CTA, or (M > 128) a CTA pair with twice the tile
   const long tm = dense_tile_rows(M);
   const long tiles = ((M + tm - 1) / tm) * ((N + BN - 1) / BN);
   const long sms = tm == BM ? sm_count() : sm_count() / 2;
   const long chunks = K / KCHUNK;
-  const double t_chunk = 5.9e-6, bw = 6.0e12, t_launch = 3e-6;
+  const double t_chunk = tm == BM ? 5.9e-6 : 5.2e-6, bw = 6.0e12, t_launch = 3e-6;
   const double piece_bytes = static_cast<double>(tm) * BN * 4;
   auto cost = [&](long full, long S) {
     const long split = tiles - full;
@@ -1267,7 +1281,7 @@ DensePlan dense_plan(int64_t M, int64_t N, int64_t K) {
   auto consider = [&](long full, long S) {
     if (S < 2 || S > chunks || full >= tiles) return;
     const double t = cost(full, S);
-    if (t < 0.97 * best_t) {
+    if (t < 0.99 * best_t) {
       best_t = t;
       best = DensePlan{static_cast<int>(S), static_cast<int>(full)};
     }
@@ -1398,21 +1412,56 @@ long packed_tiles(int64_t M, int64_t N) {
 long packed_teams(int64_t M) { return packed_wm(M) ? sm_count() / 2 : sm_count(); }
 }  // namespace
 
-// K slices per tile of the packed GEMM: 1 when the tiles alone fill most of
-// the GPU, else as many slices (of whole 128-groups) as keep one unit per
-// team.
-int packed_splits(int64_t M, int64_t N, int64_t K) {
+namespace {
+struct PackedPlan {
+  int S;      // K slices per split tile (1: nothing split)
+  int full;   // tiles computed whole, before the split ones
+};
+
+// How the packed GEMM cuts its work.  Up to 128 tokens (one CTA per tile):
+// whole tiles when they fill most of the GPU, else every tile in as many K
+// slices of whole 128-groups as keep one unit per CTA (partial sums in S
+// planes [M][N]).  CTA pairs: like the expanded GEMMs, the whole waves of
+// tiles whole and the tiles of the last, partial wave (all tiles when there
+// are fewer than pairs) in S slices, if the estimate is at least 1 % shorter:
+// waves x 128-groups per unit x one tile-group (~0.80 us measured), plus
+// the pieces' traffic and the finishing kernel's launch.
+PackedPlan packed_plan(int64_t M, int64_t N, int64_t K) {
   const long tiles = packed_tiles(M, N);
-  const long sms = packed_teams(M);
-  if (4 * tiles >= 3 * sms) return 1;
-  const long want = sms / tiles;
+  const long teams = packed_teams(M);
   const long groups = K / kGroup;
-  return static_cast<int>(want < groups ? want : groups);
+  if (!packed_wm(M)) {
+    if (4 * tiles >= 3 * teams) return PackedPlan{1, static_cast<int>(tiles)};
+    const long want = teams / tiles;
+    return PackedPlan{static_cast<int>(want < groups ? want : groups), 0};
+  }
+  const double t_group = 0.80e-6, bw = 6.0e12, t_launch = 3e-6;
+  const double piece_bytes = 256.0 * 256 * 4;
+  const long full = tiles / teams * teams, rest = tiles - full;
+  const double whole = static_cast<double>((tiles + teams - 1) / teams * groups) * t_group;
+  PackedPlan best{1, static_cast<int>(tiles)};
+  double best_t = whole;
+  for (long S = 2; rest > 0 && S <= groups && S <= 64; ++S) {
+    const long rounds = (rest * S + teams - 1) / teams;
+    const double t = static_cast<double>(full / teams * groups + rounds * ((groups + S - 1) / S)) *
+                         t_group +
+                     (2.0 * rest * S * piece_bytes + 2.0 * rest * 256 * 256) / bw + t_launch;
+    if (t < 0.99 * whole && t < best_t) {
+      best_t = t;
+      best = PackedPlan{static_cast<int>(S), static_cast<int>(full)};
+    }
+  }
+  return best;
 }
+}  // namespace
+
+int packed_splits(int64_t M, int64_t N, int64_t K) { return packed_plan(M, N, K).S; }
 
 size_t gemm_packed_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  const int S = packed_splits(M, N, K);
-  return S > 1 ? static_cast<size_t>(S) * M * N * sizeof(int32_t) : 0;
+  const PackedPlan p = packed_plan(M, N, K);
+  if (p.S == 1) return 0;
+  if (!packed_wm(M)) return static_cast<size_t>(p.S) * M * N * sizeof(int32_t);
+  return static_cast<size_t>(packed_tiles(M, N) - p.full) * p.S * 256 * 256 * sizeof(int32_t);
 }
 
 cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const uint8_t* packed,
@@ -1446,9 +1495,11 @@ cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const ui
   const bool wm = packed_wm(M);
   CUtensorMap ta;   // token boxes: 64 k x (128 tokens, one CTA's half of a pair tile)
   if (!make_map(&ta, xq, M, K, BM)) return cudaErrorInvalidValue;
-  const int S = packed_splits(M, N, K);
+  const PackedPlan p = packed_plan(M, N, K);
+  const int S = p.S;
   int32_t* part = S > 1 ? static_cast<int32_t*>(ws) : nullptr;
-  const long units = packed_tiles(M, N) * S;
+  const long tiles = packed_tiles(M, N);
+  const long units = p.full + (tiles - p.full) * S;
   cudaError_t e;
   if (wm) {
     // one CTA pair per team, as many as fit on the device at once
@@ -1463,14 +1514,26 @@ cudaError_t launch_gemm_packed(const uint16_t* xq, const float* tscale, const ui
     e = launch_cluster(gemm_packed_kernel<true, true>, dim3(static_cast<unsigned>(2 * teams)),
                        dim3(P_THREADS), PSMEM_BYTES, st, 2u, ta, packed, q, tscale, rscale,
                        static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                       reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
+                       reinterpret_cast<__nv_bfloat16*>(y), acc, S, p.full, part);
   } else {
     const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
     e = launch(gemm_packed_kernel<false, false>, dim3(grid), dim3(P_THREADS), PSMEM_BYTES, st, ta,
                packed, q, tscale, rscale, static_cast<int>(M), static_cast<int>(N),
-               static_cast<int>(K), reinterpret_cast<__nv_bfloat16*>(y), acc, S, part);
+               static_cast<int>(K), reinterpret_cast<__nv_bfloat16*>(y), acc, S, p.full, part);
   }
   if (e != cudaSuccess || S == 1) return e;
+  if (wm) {
+    // the split tiles' pieces, [256 tokens][256 weight rows] each: the
+    // expanded GEMMs' finishing kernel (same tile order and epilogue)
+    const long m_blocks = (M + 255) / 256;
+    const long n_split = tiles - p.full;
+    const long threads = n_split * 256 * (BN / 8);
+    return launch(split_finalize_kernel<false>,
+                  dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256), 0, st,
+                  static_cast<const void*>(part), S, p.full, static_cast<int>(n_split),
+                  static_cast<int>(m_blocks), 256, static_cast<int>(M), static_cast<int>(N),
+                  tscale, rscale, reinterpret_cast<__nv_bfloat16*>(y), acc);
+  }
   const long threads = M * N / 8;
   return launch(packed_finalize_kernel, dim3(static_cast<unsigned>((threads + FIN_THREADS - 1) /
                                                                    FIN_THREADS)),

@@ -49,7 +49,9 @@ def test_kernel_launch_counts(lib):
     G = B.TERN_OP_GEMV
     assert B.tern_kernel_launches(G, 0, 34816, 5120) == 0
     assert B.tern_kernel_launches(99, 4, 34816, 5120) == 0
-    assert B.tern_kernel_launches(B.TERN_OP_GEMM, 2048, 34816, 5120) == 1
+    # 1088 gate/up pair tiles on 76 pairs: the last wave's tiles split along K,
+    # finished by a second kernel
+    assert B.tern_kernel_launches(B.TERN_OP_GEMM, 2048, 34816, 5120) == 2
     # gate/up: 68 blocks x 40 groups over 152 CTAs (17.9 units each): a block
     # has at most 4 owners, summed in place at M <= 8; any sharing at M > 8
     assert B.tern_kernel_launches(G, 1, 34816, 5120) == 1
@@ -61,11 +63,15 @@ def test_kernel_launch_counts(lib):
     assert B.tern_kernel_launches(G, 16, 152 * 512, 1024) == 1
     # one block of 8 groups split over 8 CTAs
     assert B.tern_kernel_launches(G, 16, 512, 1024) == 2
-    # the packed GEMM: 16 x 136 tiles fill the GPU; down at 128 tokens has
-    # 20 tiles, split along K (a second, rescale kernel and an int32 workspace)
+    # the packed GEMM: 8 x 136 pair tiles on 76 pairs, the last wave's 24
+    # tiles split in 3 K slices (a second kernel adds the [256][256] int32
+    # pieces); down at 128 tokens has 20 CTA tiles, all split along K
     P = B.TERN_OP_GEMM_PACKED
-    assert B.tern_kernel_launches(P, 2048, 34816, 5120) == 1
-    assert B.tern_workspace_bytes(P, 2048, 34816, 5120) == 0
+    assert B.tern_kernel_launches(P, 2048, 34816, 5120) == 2
+    assert B.tern_workspace_bytes(P, 2048, 34816, 5120) == 24 * 3 * 256 * 256 * 4
+    # gate/up at 512 tokens: 272 tiles, kept whole
+    assert B.tern_kernel_launches(P, 512, 34816, 5120) == 1
+    assert B.tern_workspace_bytes(P, 512, 34816, 5120) == 0
     assert B.tern_kernel_launches(P, 128, 5120, 17408) == 2
     # 20 tiles -> 7 slices of whole 128-groups (140 units), one int32 plane each
     assert B.tern_workspace_bytes(P, 128, 5120, 17408) == 7 * 128 * 5120 * 4
@@ -235,8 +241,12 @@ def test_fp16_variant_argument_errors(lib):
     # the expanded GEMMs' optional split: 20 tiles of down at 128 tokens
     assert B.tern_workspace_bytes(B.TERN_OP_GEMM, 128, 5120, 17408) > 0
     assert B.tern_kernel_launches(B.TERN_OP_GEMM, 128, 5120, 17408) == 2
-    assert B.tern_workspace_bytes(B.TERN_OP_GEMM, 2048, 34816, 5120) == 0
-    assert B.tern_kernel_launches(B.TERN_OP_GEMM, 2048, 34816, 5120) == 1
+    # ... and the last wave of gate/up at 2048 tokens (24 of 76 pairs busy)
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMM, 2048, 34816, 5120) > 0
+    assert B.tern_kernel_launches(B.TERN_OP_GEMM, 2048, 34816, 5120) == 2
+    # o at 512 tokens: 40 pair tiles, one wave, kept whole
+    assert B.tern_workspace_bytes(B.TERN_OP_GEMM, 512, 5120, 5120) == 0
+    assert B.tern_kernel_launches(B.TERN_OP_GEMM, 512, 5120, 5120) == 1
 
 
 def test_host_accessible_query(lib):

@@ -136,12 +136,14 @@ def test_full_size_sampled(layer, m):
 
 
 @pytest.mark.parametrize("m,n,k", [(100, 512, 5120), (128, 5120, 17408), (40, 10240, 5120),
-                                   (300, 512, 5120)])
+                                   (300, 512, 5120), (512, 10240, 5120)])
 def test_split_k_with_and_without_acc(m, n, k):
-    """Few tiles: each tile's K range is split in slices whose exact int32
-    partial sums are added by a second kernel; y is the same with or without
-    acc.  The last shape has more than 128 tokens, so its tiles hold 128
-    weight rows x 256 tokens (weights on the MMA's M side)."""
+    """Tiles that fill the GPU unevenly: K ranges split in slices whose exact
+    int32 partial sums a second kernel adds; y is the same with or without
+    acc.  Above 128 tokens the tiles are CTA pairs' 256 weight rows x 256
+    tokens: with fewer tiles than pairs every tile is split (300 tokens), with
+    more the whole waves stay whole and only the last wave's tiles are split
+    (512 x 10240: 76 tiles whole, 4 in slices)."""
     assert B.tern_kernel_launches(B.TERN_OP_GEMM_PACKED, m, n, k) == 2
     codes = I.make_codes(31, n, k)
     scales = I.make_scales(31, n, k)
