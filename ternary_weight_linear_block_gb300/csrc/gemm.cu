@@ -508,23 +508,30 @@ __global__ void __launch_bounds__(256)
   const int n = n_blk * BN + c8 * 8;
   if (row >= M || n >= N) return;
   typename std::conditional<FP, float, int>::type a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int sl = 0; sl < S; ++sl) {
-    const long off = ((st * S + sl) * tm + r) * BN + c8 * 8;
-    if constexpr (FP) {
-      const float* p = static_cast<const float*>(part) + off;
-      const float4 a0 = __ldcs(reinterpret_cast<const float4*>(p));
-      const float4 a1 = __ldcs(reinterpret_cast<const float4*>(p + 4));
-      a[0] = __fadd_rn(a[0], a0.x); a[1] = __fadd_rn(a[1], a0.y);
-      a[2] = __fadd_rn(a[2], a0.z); a[3] = __fadd_rn(a[3], a0.w);
-      a[4] = __fadd_rn(a[4], a1.x); a[5] = __fadd_rn(a[5], a1.y);
-      a[6] = __fadd_rn(a[6], a1.z); a[7] = __fadd_rn(a[7], a1.w);
-    } else {
-      const int32_t* p = static_cast<const int32_t*>(part) + off;
-      const int4 a0 = __ldcs(reinterpret_cast<const int4*>(p));
-      const int4 a1 = __ldcs(reinterpret_cast<const int4*>(p + 4));
-      a[0] += a0.x; a[1] += a0.y; a[2] += a0.z; a[3] += a0.w;
-      a[4] += a1.x; a[5] += a1.y; a[6] += a1.z; a[7] += a1.w;
-    }
+  // four slices' loads in flight before their adds (in slice order)
+  for (int sl0 = 0; sl0 < S; sl0 += 4) {
+    int4 v[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (sl0 + u < S) {
+        const int4* p = static_cast<const int4*>(part) +
+                        (((st * S + sl0 + u) * tm + r) * BN + c8 * 8) / 4;
+        v[u][0] = __ldcs(p);
+        v[u][1] = __ldcs(p + 1);
+      }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (sl0 + u < S) {
+        const int w[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
+                          v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if constexpr (FP)
+            a[i] = __fadd_rn(a[i], __int_as_float(w[i]));
+          else
+            a[i] += w[i];
+        }
+      }
   }
   uint32_t out[4];
   if constexpr (FP) {
@@ -1177,12 +1184,22 @@ __global__ void __launch_bounds__(FIN_THREADS)
   pdl_wait();   // the GEMM's partial sums
   if (row >= M) return;
   int aa[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int sl = 0; sl < S; ++sl) {
-    const int32_t* p = part + (static_cast<long>(sl) * M + row) * N + n;
-    const int4 a0 = __ldcs(reinterpret_cast<const int4*>(p));
-    const int4 a1 = __ldcs(reinterpret_cast<const int4*>(p + 4));
-    aa[0] += a0.x; aa[1] += a0.y; aa[2] += a0.z; aa[3] += a0.w;
-    aa[4] += a1.x; aa[5] += a1.y; aa[6] += a1.z; aa[7] += a1.w;
+  for (int sl0 = 0; sl0 < S; sl0 += 4) {   // four planes' loads in flight
+    int4 v[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (sl0 + u < S) {
+        const int4* p = reinterpret_cast<const int4*>(
+            part + (static_cast<long>(sl0 + u) * M + row) * N + n);
+        v[u][0] = __ldcs(p);
+        v[u][1] = __ldcs(p + 1);
+      }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (sl0 + u < S) {
+        aa[0] += v[u][0].x; aa[1] += v[u][0].y; aa[2] += v[u][0].z; aa[3] += v[u][0].w;
+        aa[4] += v[u][1].x; aa[5] += v[u][1].y; aa[6] += v[u][1].z; aa[7] += v[u][1].w;
+      }
   }
   const float4 r0 = __ldg(reinterpret_cast<const float4*>(rscale + n));
   const float4 r1 = __ldg(reinterpret_cast<const float4*>(rscale + n + 4));
