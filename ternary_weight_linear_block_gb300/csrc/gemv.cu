@@ -693,12 +693,13 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
 // rotates again for each chunk.  Results are bit-identical to
 // tern_fwht_quant(TERN_FWHT_DECODE) followed by tern_gemv_decode.
 constexpr int LSTAGES = 8;
-constexpr int LX_BYTES = 80 * 1024;             // resident decode operand (a chunk of groups)
-constexpr int LXS_FLOATS = 16 * 64;             // fold factors of 16 tokens x 64 blocks
+constexpr int LX_BYTES = 76 * 1024;             // resident decode operand (a chunk of groups)
 constexpr int LCHUNK_MAX = 64;                  // groups of one chunk at most
-constexpr int LXO_FLOATS = LCHUNK_MAX * 16;     // group offsets of the chunk's groups x 16 tokens
-constexpr size_t LSMEM_BYTES = static_cast<size_t>(LSTAGES) * UNIT_BYTES + LX_BYTES +
-                               (LXS_FLOATS + LXO_FLOATS) * 4 + 1024 + 256;
+// one group record per chunk position, laid out like the rotation kernel's
+// (negated offset quads of 16 tokens, then their block's fold factors)
+constexpr int LREC_BYTES = LCHUNK_MAX * AUX_BYTES;
+constexpr size_t LSMEM_BYTES = static_cast<size_t>(LSTAGES) * UNIT_BYTES + LX_BYTES + LREC_BYTES +
+                               1024 + 256;
 static_assert(LSMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 // Groups of one chunk: each 256 bytes per token row.
@@ -718,9 +719,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* xreg = smem + LSTAGES * UNIT_BYTES;
-  float* xs_s = reinterpret_cast<float*>(xreg + LX_BYTES);
-  float* xo_s = xs_s + LXS_FLOATS;
-  uint64_t* full = reinterpret_cast<uint64_t*>(xo_s + LXO_FLOATS);
+  float* rec_s = reinterpret_cast<float*>(xreg + LX_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(rec_s + LREC_BYTES / 4);
   uint64_t* empty = full + LSTAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + LSTAGES);
 
@@ -796,11 +796,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     const uint32_t smem_base = ptx::smem_u32(smem);
     const uint32_t x_base = ptx::smem_u32(xreg);
+    const uint32_t rec_base = ptx::smem_u32(rec_s);
 
     // Rotate the 1024-blocks holding the groups gs .. gs + ng - 1 (mod G) and
-    // store those groups' decode operand at positions 0 .. ng - 1, their
-    // offsets in xo_s[position][token] and the blocks' fold factors in
-    // xs_s[token][block] (the arithmetic of the rotation kernel).
+    // store those groups' decode operand at positions 0 .. ng - 1 and their
+    // group records at the same positions (the arithmetic and the record
+    // layout of the rotation kernel: the negated offsets as the tensor
+    // core's accumulator quads, then the block's fold factor per token).
     auto build = [&](int gs, int ng) {
       for (int t = cw; t < M * B; t += CONSUMERS) {
         const int m = t / B, b = t - m * B;
@@ -815,6 +817,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fwht::fwht_1024(v, lane);
         const int sh = fwht::block_shift(v);
         const int e = fwht::lane_step_exp(lane);
+        const float fold = fwht::pow2f(12 - sh);
+        const int qi = 4 * (m >> 1) + (m & 1);
 #pragma unroll
         for (int ih = 0; ih < 4; ++ih) {
           // lanes 0-15 hold group 2 ih of the block, lanes 16-31 group 2 ih + 1
@@ -822,15 +826,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int pos = (gg - gs + G) % G;
           float part;
           const uint4 w = fwht::decode_pack8(v, ih, sh, e, part);
-          const float xoff = fwht::group_offset(part);
+          const float xoff = __fsub_rn(0.f, fwht::group_offset(part));
           if (pos < ng) {
             *reinterpret_cast<uint4*>(xreg + m * pitch + pos * 256 + (lane & 15) * 16) = w;
-            if ((lane & 15) == 0) xo_s[pos * 16 + m] = xoff;
+            if ((lane & 15) == 0) {
+              float* rec = rec_s + pos * (AUX_BYTES / 4);
+              rec[qi] = xoff;
+              rec[qi + 2] = xoff;
+              rec[32 + m] = fold;
+            }
           }
         }
-        if (lane == 0) xs_s[m * 64 + b] = fwht::pow2f(12 - sh);
       }
     };
+
+    // the records' entries of tokens M .. 15 stay zero (offsets and fold
+    // factors), as in the rotation kernel's records
+    for (int i = threadIdx.x - 32; i < LREC_BYTES / 4; i += 32 * CONSUMERS) rec_s[i] = 0.f;
+    ptx::named_sync(1, 32 * CONSUMERS);
+
+    // Per-lane shared-memory offsets, fixed for the whole kernel (as in the
+    // GEMV): the warp's two tiles' code slots and scale pairs in a stage,
+    // and the record's offset quads and fold factors of tokens 8 nt + 2 cq +
+    // {0, 1}.
+    const uint32_t code_off = 512 * (TPW * cw) + 16 * lane;
+    const uint32_t sp_off = UNIT_CODE_BYTES + 32 * (TPW * cw) + 4 * gq;
+    const uint32_t rec_off = 16 * cq;
 
     float acc[TPW][NT][4], bacc[TPW][NT][4];
 #pragma unroll
@@ -841,6 +862,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < 4; ++i) acc[tt][nt][i] = bacc[tt][nt][i] = 0.f;
 
     int rb = u0 / G, g = u0 % G, seg_g0 = g, gs = g;
+    int s = 0;               // ring stage of unit i
+    uint32_t ph = 0;         // its phase
     bool alive = true;
     int c_end = 0;
     for (int i = 0; alive && i < n_units;) {
@@ -856,37 +879,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int seg_stop = i + (G - g);
       const int stop = seg_stop < c_end ? seg_stop : c_end;
       for (; i < stop; ++i) {
-        const int s = i % LSTAGES;
-        const uint32_t ph = static_cast<uint32_t>(i / LSTAGES) & 1u;
         if (!ptx::mbar_wait_warp(&full[s], ph, abort_flag, WAIT_LIMIT)) {
           if (!*abort_flag) fail(abort_flag, ERR_CONSUMER);
           alive = false;
           break;
         }
-        const uint8_t* unit = smem + s * UNIT_BYTES;
+        const uint32_t st = smem_base + s * UNIT_BYTES;
+        const int pos = g >= gs ? g - gs : g + G - gs;
+        const uint32_t a_rec = rec_base + pos * AUX_BYTES + rec_off;
         uint4 cv[TPW];
         uint32_t sp[TPW];
-#pragma unroll
-        for (int tt = 0; tt < TPW; ++tt) {
-          cv[tt] = *reinterpret_cast<const uint4*>(unit + 512 * (TPW * cw + tt) + 16 * lane);
-          sp[tt] = *reinterpret_cast<const uint32_t*>(unit + UNIT_CODE_BYTES + 32 * (TPW * cw + tt) +
-                                                      4 * gq);
+        float d[TPW][NT][4];       // each tile's accumulators start at the offset quad
+        load_tiles<NT>(st + code_off, st + sp_off, a_rec, cv, sp, d,
+                       std::make_index_sequence<TPW>{});
+        float fo[NT][2];
+        {
+          const float2 f2 = lds_v2f<0>(a_rec + 128 - 8 * cq);
+          fo[0][0] = f2.x;
+          fo[0][1] = f2.y;
+        }
+        if constexpr (NT == 2) {
+          const float2 f2 = lds_v2f<32>(a_rec + 128 - 8 * cq);
+          fo[NT - 1][0] = f2.x;
+          fo[NT - 1][1] = f2.y;
         }
         uint32_t bf[NT][8][2];
-        const int pos = g >= gs ? g - gs : g + G - gs;
         const uint32_t xb = x_base + pos * 256;
-        float d[TPW][NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int tok = 8 * nt + 2 * cq;
-          const float x0 = tok < M ? __fsub_rn(0.f, xo_s[pos * 16 + tok]) : 0.f;
-          const float x1 = tok + 1 < M ? __fsub_rn(0.f, xo_s[pos * 16 + tok + 1]) : 0.f;
-#pragma unroll
-          for (int tt = 0; tt < TPW; ++tt) {
-            d[tt][nt][0] = d[tt][nt][2] = x0;
-            d[tt][nt][1] = d[tt][nt][3] = x1;
-          }
-        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -895,19 +913,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         bf[nt][2 * q + 1][0], bf[nt][2 * q + 1][1]);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[s]);
-        unit_math<NT>(cv, sp, bf, d, bacc);
-        if ((g & 7) == 7 || i + 1 == n_units) {
-          const int blk = g >> 3;
-          float f[NT][2];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int tok = 8 * nt + 2 * cq + h;
-              f[nt][h] = tok < M ? xs_s[tok * 64 + blk] : 0.f;
-            }
-          fold_block<NT>(acc, bacc, f);
+        if (++s == LSTAGES) {
+          s = 0;
+          ph ^= 1u;
         }
+        unit_math<NT>(cv, sp, bf, d, bacc);
+        if ((g & 7) == 7 || i + 1 == n_units) fold_block<NT>(acc, bacc, fo);
         ++g;
       }
       if (!alive) break;
