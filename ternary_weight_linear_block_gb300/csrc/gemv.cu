@@ -339,6 +339,14 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
 // (coalesced); the slot loads of a thread are independent.  The reduction is
 // spread over the whole GPU instead of the blocks' owners.
 constexpr int FIX_THREADS = 256;
+// BATCH slots' loads go out before their adds (in slot order), so a row of
+// S slots costs ceil(S / BATCH) memory round trips; the value is the low
+// 32-bit word of each 64-bit slot word.  The launcher takes BATCH = 16 for
+// the blocks with more than 8 owners at M >= 8 and 8 otherwise: measured
+// on GB300, 16 (48 registers) is faster where there are many slots and many
+// tokens, 8 (32 registers) at M <= 4 and on the large grids with few slots
+// (gate/up at M = 16).
+template <int BATCH>
 __global__ void __launch_bounds__(FIX_THREADS)
     fixup_kernel(const unsigned long long* __restrict__ partials, __nv_bfloat16* __restrict__ y,
                  int M, int N, int G, int U, int C, int S, int tag) {
@@ -352,19 +360,19 @@ __global__ void __launch_bounds__(FIX_THREADS)
   const long row = static_cast<long>(rb) * RB + rin;
   pdl_wait();   // the GEMV's partial sums
   if (nslots <= tag || row >= N) return;
-  const unsigned long long* p = partials + (static_cast<long>(rb) * S * M + tok) * RB + rin;
-  const long stride = static_cast<long>(M) * RB;   // one slot
+  const unsigned int* p =
+      reinterpret_cast<const unsigned int*>(partials + (static_cast<long>(rb) * S * M + tok) * RB + rin);
+  const long stride = 2l * M * RB;   // one slot, in 32-bit words
   float sum = 0.f;
-  int sl = 0;
-  for (; sl + 4 <= nslots; sl += 4) {
-    const unsigned long long a0 = __ldcg(p + (sl + 0) * stride), a1 = __ldcg(p + (sl + 1) * stride);
-    const unsigned long long a2 = __ldcg(p + (sl + 2) * stride), a3 = __ldcg(p + (sl + 3) * stride);
-    sum += __uint_as_float(static_cast<unsigned int>(a0));
-    sum += __uint_as_float(static_cast<unsigned int>(a1));
-    sum += __uint_as_float(static_cast<unsigned int>(a2));
-    sum += __uint_as_float(static_cast<unsigned int>(a3));
+  for (int sl = 0; sl < nslots; sl += BATCH) {
+    unsigned int a[BATCH];
+#pragma unroll
+    for (int j = 0; j < BATCH; ++j)
+      if (sl + j < nslots) a[j] = __ldcg(p + (sl + j) * stride);
+#pragma unroll
+    for (int j = 0; j < BATCH; ++j)
+      if (sl + j < nslots) sum += __uint_as_float(a[j]);
   }
-  for (; sl < nslots; ++sl) sum += __uint_as_float(static_cast<unsigned int>(__ldcg(p + sl * stride)));
   y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(__fmul_rn(sum, OUT_SCALE));
 }
 
@@ -1037,7 +1045,8 @@ cudaError_t launch_fixup(const GemvPlan& p, unsigned long long* partials, __nv_b
   if (p.S <= tag) return cudaSuccess;
   const long threads = static_cast<long>(p.RBn) * M * RB;
   const dim3 grid(static_cast<unsigned>((threads + FIX_THREADS - 1) / FIX_THREADS));
-  return launch(fixup_kernel, grid, dim3(FIX_THREADS), 0, st,
+  auto* kern = (M >= 8 && p.S > 8) ? fixup_kernel<16> : fixup_kernel<8>;
+  return launch(kern, grid, dim3(FIX_THREADS), 0, st,
                 static_cast<const unsigned long long*>(partials), y, M, N, G, p.U, p.C, p.S, tag);
 }
 
