@@ -202,31 +202,38 @@ __device__ __forceinline__ void load_tiles(uint32_t a_code, uint32_t a_sp, uint3
 }
 
 
-__device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ void st_word(unsigned int* p, unsigned int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned int ld_word(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+// A published partial sum: its fp32 bits, with +0.0 sent as -0.0, so that a
+// word is nonzero exactly when it has been published (adding -0.0 instead
+// of +0.0 changes at most the sign of a zero sum).
+__device__ __forceinline__ unsigned int published(float v) {
+  const unsigned int b = __float_as_uint(v);
+  return b != 0u ? b : 0x80000000u;
 }
 
 // A segment [ga, gb) of row block rb ends.  A row block finished by one CTA
 // is written directly.  A block shared by at most tag_slots CTAs is summed by
 // its first owner, which in stream-K order finishes the block last: every
-// other owner publishes its 32 rows per warp as tagged 64-bit words
-// (value | 1 << 32) in its slot, with no fence and no atomic (each word is
-// single-copy atomic, so a set tag vouches for the value beside it), and the
-// first owner reads them, adds them in slot order, writes y and clears the
-// tags.  A block with more owners would load its first owner with too many
-// slots: there every owner stores its words untagged (tag 0) and the fixup
-// kernel adds them across the whole GPU after the GEMV.  Between calls every
-// word of the workspace has tag 0.
+// other owner publishes its 32 rows per warp as 32-bit words in its slot
+// (published(): never zero), with no fence and no atomic (each word is
+// single-copy atomic, so a nonzero word is the whole value), and the first
+// owner reads them, adds them in slot order, writes y and zeroes them.  A
+// block with more owners would load its first owner with too many slots:
+// there every owner stores its words and the fixup kernel adds them across
+// the whole GPU after the GEMV, and zeroes them.  Between calls every word
+// of the workspace is zero.
 template <int NT>
 __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int ga, int gb, int rb,
                                          int G, int U, int C, int S, int M, int N, int cw,
                                          int lane, __nv_bfloat16* __restrict__ y,
-                                         unsigned long long* __restrict__ partials,
+                                         unsigned int* __restrict__ partials,
                                          volatile int* abort_flag) {
   const int gq = lane >> 2, cq = lane & 3;
   constexpr int NV = TPW * NT * 4;
@@ -246,57 +253,56 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
   const int slot = static_cast<int>(blockIdx.x) - first;
   const int nslots = owner32(rb * G + G - 1, U, C) - first + 1;
   if (NT == 2 || nslots > tag_slots<NT>()) {
-    unsigned long long* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
+    unsigned int* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
       const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
       const int tok = 8 * nt + 2 * cq + (i & 1);
-      if (tok < M) __stcg(base + tok * RB + rin, static_cast<unsigned long long>(__float_as_uint(acc[tt][nt][i])));
+      if (tok < M) __stcg(base + tok * RB + rin, __float_as_uint(acc[tt][nt][i]));
     }
     return;
   }
   if (slot != 0) {
-    unsigned long long* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
+    unsigned int* base = partials + (static_cast<long>(rb) * S + slot) * M * RB;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
       const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
       const int tok = 8 * nt + 2 * cq + (i & 1);
-      if (tok < M)
-        st_tagged(base + tok * RB + rin,
-                  (1ull << 32) | __float_as_uint(acc[tt][nt][i]));
+      if (tok < M) st_word(base + tok * RB + rin, published(acc[tt][nt][i]));
     }
     return;
   }
   float sum[NV];
 #pragma unroll
   for (int v = 0; v < NV; ++v) sum[v] = acc[v / (NT * 4)][(v / 4) % NT][v % 4];
-  // the other slots in order: all words of a slot are loaded before any is
-  // checked, so a slot published long ago costs one memory round trip; a slot
-  // not yet complete is retried (bounded)
-  constexpr int SB = 2;   // slots loaded per round (3: more registers, a slower hot loop)
+  // the other slots in order, SB at a time: all words of a round are loaded
+  // before any is checked, so slots published long ago cost one memory round
+  // trip; a slot not yet complete is loaded again (bounded).  Measured with
+  // 32-bit words: SB = 2 beats loading all three other slots at once at
+  // every M (gate/up 14.56 -> 14.35 us at M = 4, 14.24 -> 13.81 at M = 1).
+  constexpr int SB = 2;
   bool ok = true;
   for (int sl0 = 1; sl0 < nslots && ok; sl0 += SB) {
-    unsigned long long w[SB][NV];
+    unsigned int w[SB][NV];
     for (uint32_t tries = 0;; ++tries) {
       bool ready = true;
 #pragma unroll
       for (int sb = 0; sb < SB; ++sb) {
-        const unsigned long long* base =
-            partials + (static_cast<long>(rb) * S + sl0 + sb) * M * RB;
+        const unsigned int* base = partials + (static_cast<long>(rb) * S + sl0 + sb) * M * RB;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
           const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
           const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
           const int tok = 8 * nt + 2 * cq + (i & 1);
-          w[sb][v] = (sl0 + sb < nslots && tok < M) ? ld_tagged(base + tok * RB + rin) : (1ull << 32);
+          w[sb][v] = (sl0 + sb < nslots && tok < M) ? ld_word(base + tok * RB + rin) : 1u;
         }
       }
 #pragma unroll
       for (int sb = 0; sb < SB; ++sb)
 #pragma unroll
-        for (int v = 0; v < NV; ++v) ready = ready && (w[sb][v] >> 32) == 1ull;
+        for (int v = 0; v < NV; ++v) ready = ready && w[sb][v] != 0u;
       if (__all_sync(0xffffffffu, ready)) break;
       if (tries >= TAG_TRIES || *abort_flag) {
         if (lane == 0) fail(abort_flag, ERR_REDUCE);
@@ -308,16 +314,16 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
     if (!ok) break;
 #pragma unroll
     for (int sb = 0; sb < SB; ++sb) {
-#pragma unroll
-      for (int v = 0; v < NV; ++v) sum[v] += __uint_as_float(static_cast<unsigned int>(w[sb][v]));
       if (sl0 + sb >= nslots) continue;
-      unsigned long long* base = partials + (static_cast<long>(rb) * S + sl0 + sb) * M * RB;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) sum[v] += __uint_as_float(w[sb][v]);
+      unsigned int* base = partials + (static_cast<long>(rb) * S + sl0 + sb) * M * RB;
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         const int tt = v / (NT * 4), nt = (v / 4) % NT, i = v % 4;
         const int rin = 16 * (TPW * cw + tt) + gq + 8 * (i >> 1);
         const int tok = 8 * nt + 2 * cq + (i & 1);
-        if (tok < M) st_tagged(base + tok * RB + rin, 0ull);
+        if (tok < M) st_word(base + tok * RB + rin, 0u);
       }
     }
   }
@@ -340,16 +346,15 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
 // spread over the whole GPU instead of the blocks' owners.
 constexpr int FIX_THREADS = 256;
 // BATCH slots' loads go out before their adds (in slot order), so a row of
-// S slots costs ceil(S / BATCH) memory round trips; the value is the low
-// 32-bit word of each 64-bit slot word.  The launcher takes BATCH = 16 for
+// S slots costs ceil(S / BATCH) memory round trips.  The launcher takes BATCH = 16 for
 // the blocks with more than 8 owners at M >= 8 and 8 otherwise: measured
 // on GB300, 16 (48 registers) is faster where there are many slots and many
 // tokens, 8 (32 registers) at M <= 4 and on the large grids with few slots
 // (gate/up at M = 16).
 template <int BATCH>
 __global__ void __launch_bounds__(FIX_THREADS)
-    fixup_kernel(const unsigned long long* __restrict__ partials, __nv_bfloat16* __restrict__ y,
-                 int M, int N, int G, int U, int C, int S, int tag) {
+    fixup_kernel(unsigned int* __restrict__ partials, __nv_bfloat16* __restrict__ y, int M, int N,
+                 int G, int U, int C, int S, int tag) {
   pdl_launch_dependents();
   const int t = static_cast<int>(blockIdx.x) * FIX_THREADS + threadIdx.x;
   const int rin = t % RB;
@@ -360,9 +365,8 @@ __global__ void __launch_bounds__(FIX_THREADS)
   const long row = static_cast<long>(rb) * RB + rin;
   pdl_wait();   // the GEMV's partial sums
   if (nslots <= tag || row >= N) return;
-  const unsigned int* p =
-      reinterpret_cast<const unsigned int*>(partials + (static_cast<long>(rb) * S * M + tok) * RB + rin);
-  const long stride = 2l * M * RB;   // one slot, in 32-bit words
+  unsigned int* p = partials + (static_cast<long>(rb) * S * M + tok) * RB + rin;
+  const long stride = static_cast<long>(M) * RB;   // one slot
   float sum = 0.f;
   for (int sl = 0; sl < nslots; sl += BATCH) {
     unsigned int a[BATCH];
@@ -373,6 +377,9 @@ __global__ void __launch_bounds__(FIX_THREADS)
     for (int j = 0; j < BATCH; ++j)
       if (sl + j < nslots) sum += __uint_as_float(a[j]);
   }
+  // the workspace is zero again after the call (the words' values are in
+  // registers by now, so the stores do not wait on the loads)
+  for (int sl = 0; sl < nslots; ++sl) __stcg(p + sl * stride, 0u);
   y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(__fmul_rn(sum, OUT_SCALE));
 }
 
@@ -445,7 +452,7 @@ template <int NT>
 __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t* __restrict__ packed,
                 const float* __restrict__ aux, int M, int N, int K, __nv_bfloat16* __restrict__ y,
-                unsigned long long* __restrict__ partials, int U, int S) {
+                unsigned int* __restrict__ partials, int U, int S) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -721,7 +728,7 @@ template <int NT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     linear_kernel(const uint16_t* __restrict__ x, const int8_t* __restrict__ sign,
                   const uint8_t* __restrict__ packed, int M, int N, int K,
-                  __nv_bfloat16* __restrict__ y, unsigned long long* __restrict__ partials, int U,
+                  __nv_bfloat16* __restrict__ y, unsigned int* __restrict__ partials, int U,
                   int S) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1005,7 +1012,7 @@ EncodeTiledFn encode_fn() {
 
 template <int NT>
 cudaError_t launch_nt(const CUtensorMap& tm, const uint8_t* packed, const float* xs, int M, int N,
-                      int K, __nv_bfloat16* y, unsigned long long* partials,
+                      int K, __nv_bfloat16* y, unsigned int* partials,
                       const GemvPlan& p, cudaStream_t st) {
   static std::atomic<unsigned long long> attr_done{0};
   const cudaError_t e = once_per_device(attr_done, [] {
@@ -1028,7 +1035,7 @@ size_t gemv_packed_bytes(int64_t N, int64_t K) {
 // call leaves all tags at 0.
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const GemvPlan p = make_plan(N, K, sm_count());
-  return static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(unsigned long long);
+  return static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(unsigned int);
 }
 
 // Whether a call at this shape ends with the fixup kernel: some row block is
@@ -1039,7 +1046,7 @@ bool gemv_needs_fixup(int64_t M, int64_t N, int64_t K) {
 }
 
 // The fixup kernel over every (block, token, row), when some block is shared.
-cudaError_t launch_fixup(const GemvPlan& p, unsigned long long* partials, __nv_bfloat16* y, int M,
+cudaError_t launch_fixup(const GemvPlan& p, unsigned int* partials, __nv_bfloat16* y, int M,
                          int N, int G, cudaStream_t st) {
   const int tag = M <= 8 ? tag_slots<1>() : tag_slots<2>();
   if (p.S <= tag) return cudaSuccess;
@@ -1047,13 +1054,13 @@ cudaError_t launch_fixup(const GemvPlan& p, unsigned long long* partials, __nv_b
   const dim3 grid(static_cast<unsigned>((threads + FIX_THREADS - 1) / FIX_THREADS));
   auto* kern = (M >= 8 && p.S > 8) ? fixup_kernel<16> : fixup_kernel<8>;
   return launch(kern, grid, dim3(FIX_THREADS), 0, st,
-                static_cast<const unsigned long long*>(partials), y, M, N, G, p.U, p.C, p.S, tag);
+                partials, y, M, N, G, p.U, p.C, p.S, tag);
 }
 
 cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* xs, int64_t M,
                         int64_t N, int64_t K, uint16_t* y, void* ws, cudaStream_t st) {
   const GemvPlan p = make_plan(N, K, sm_count());
-  auto* partials = static_cast<unsigned long long*>(ws);
+  auto* partials = static_cast<unsigned int*>(ws);
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   // the fp16 activations [M][K]; boxes of 64 k x 16 token rows
@@ -1077,7 +1084,7 @@ cudaError_t launch_gemv(const uint8_t* packed, const uint16_t* xh, const float* 
 namespace {
 template <int NT>
 cudaError_t launch_linear_nt(const uint16_t* x, const int8_t* sign, const uint8_t* packed, int M,
-                             int N, int K, __nv_bfloat16* y, unsigned long long* partials,
+                             int N, int K, __nv_bfloat16* y, unsigned int* partials,
                              const GemvPlan& p, cudaStream_t st) {
   static std::atomic<unsigned long long> attr_done{0};
   const cudaError_t e = once_per_device(attr_done, [] {
@@ -1094,7 +1101,7 @@ cudaError_t launch_linear_decode(const uint16_t* x, const int8_t* sign, const ui
                                  int64_t M, int64_t N, int64_t K, uint16_t* y, void* ws,
                                  cudaStream_t st) {
   const GemvPlan p = make_plan(N, K, sm_count());
-  auto* partials = static_cast<unsigned long long*>(ws);
+  auto* partials = static_cast<unsigned int*>(ws);
   auto* yy = reinterpret_cast<__nv_bfloat16*>(y);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   const cudaError_t e = M <= 8 ? launch_linear_nt<1>(x, sign, packed, m, n, k, yy, partials, p, st)

@@ -82,16 +82,17 @@ def test_full_size_sampled_rows(layer, m):
 def test_repeat_calls_reuse_workspace(layer, m):
     """Repeated calls on one workspace give the same bits, in-kernel sums
     (gate/up at M <= 8) and fixup shapes alike: the shared blocks' slots are
-    added in slot order, and every call leaves the ready tags at zero, so
-    the next call's first owners wait for fresh words."""
+    added in slot order, and every call leaves every word of the workspace
+    zero (a nonzero word is a published partial sum), so the next call's
+    first owners wait for fresh words."""
     d = I.make_layer(layer, m, seed=3)
     lay = _layer(d.codes, d.scales)
     ws = B.Workspace()
     ys = [_decode(lay, d.x_bits, m, ws) for _ in range(4)]
     for y in ys[1:]:
         assert np.array_equal(y.view(np.uint32), ys[0].view(np.uint32))
-    tags = ws.buf[:B.tern_workspace_bytes(B.TERN_OP_GEMV, m, layer.n, layer.k)]
-    assert not tags.view(torch.int32)[1::2].any()          # the high half of every 64-bit word
+    words = ws.buf[:B.tern_workspace_bytes(B.TERN_OP_GEMV, m, layer.n, layer.k)]
+    assert not words.any()
 
 
 def test_special_weights():
@@ -113,8 +114,8 @@ def test_special_weights():
 
 
 def test_workspace_after_a_gemm_is_cleaned():
-    """A Workspace a split GEMM used holds partial sums; words whose high half
-    is 1 would pass for the GEMV's ready tags.  Poison it that way through
+    """A Workspace a split GEMM used holds partial sums; nonzero words would
+    pass for the GEMV's published partial sums.  Poison it that way through
     ``scratch`` (as a GEMM may leave it): the next decode through ``get``
     zero-fills it first, so the in-kernel reduction (one launch, row blocks
     shared by up to four CTAs at M = 1) matches a fresh workspace bit for
@@ -128,7 +129,7 @@ def test_workspace_after_a_gemm_is_cleaned():
     want = _decode(layer, bits, m)
     ws = B.Workspace()
     buf = ws.scratch(B.tern_workspace_bytes(B.TERN_OP_GEMM, 512, 5120, 17408))
-    buf.view(torch.int64).fill_((1 << 32) | 0x3F800000)   # tag 1, value 1.0f
+    buf.view(torch.int32).fill_(0x3F800000)               # 1.0f in every word
     got = _decode(layer, bits, m, ws)
     assert np.array_equal(got, want)
     rows = block_sample_rows(n, seed=2, extra=256)
