@@ -228,8 +228,9 @@ def tern_quant_rotated(xr, m, k, mode, out, out_scale, stream=None):
 
 def tern_check(stream=None):
     """Synchronise and report bounded-wait timeouts.  After a timeout the
-    decode GEMV may have left ready tags in its workspace, so every live
-    ``Workspace`` is marked dirty (its next ``get`` zero-fills it again)."""
+    decode GEMV may have left published partial sums (nonzero words) in its
+    workspace, so every live ``Workspace`` is marked dirty (its next ``get``
+    zero-fills it again)."""
     st = lib().tern_check(_stream(stream))
     if st == TERN_ERR_TIMEOUT:
         for w in list(_WORKSPACES):

@@ -36,11 +36,12 @@
 // * units are cut into equal contiguous ranges, one per persistent CTA
 //   (stream-K).  A 512-row block finished by one CTA is written directly.  A
 //   block shared by at most 4 CTAs at M <= 8 is summed by its first owner,
-//   which in this order reaches it last, from tagged 64-bit words the other
-//   owners publish without fences or atomics; otherwise (more owners: small
-//   N, large K; or M > 8) the block gets untagged partial sums that a small
-//   fixup kernel, launched right after (programmatic launch), adds in slot
-//   order across the whole GPU, so no block's first owner reads many slots.  The segment's end
+//   which in this order reaches it last, from 32-bit words the other owners
+//   publish without fences or atomics (a nonzero word is a published value);
+//   otherwise (more owners: small N, large K; or M > 8) the block's partial
+//   sums go to a small fixup kernel, launched right after (programmatic
+//   launch), which adds them in slot order across the whole GPU, so no
+//   block's first owner reads many slots.  The segment's end
 //   runs outside the per-unit loop, which keeps the hot loop's registers for
 //   the hot loop.
 // * the weight copies do not depend on the previous kernel, so the producer
@@ -1030,9 +1031,8 @@ size_t gemv_packed_bytes(int64_t N, int64_t K) {
   return static_cast<size_t>((N + RB - 1) / RB) * static_cast<size_t>(K / kGroup) * UNIT_BYTES;
 }
 
-// Workspace: 64-bit partial-sum words [RBn][S][M][512] of row blocks shared
-// by several CTAs (value in the low half, ready tag in the high half); every
-// call leaves all tags at 0.
+// Workspace: 32-bit partial-sum words [RBn][S][M][512] of row blocks shared
+// by several CTAs (nonzero once published); every call leaves them all 0.
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const GemvPlan p = make_plan(N, K, sm_count());
   return static_cast<size_t>(p.RBn) * p.S * M * RB * sizeof(unsigned int);

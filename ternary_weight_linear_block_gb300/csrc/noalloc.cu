@@ -19,7 +19,7 @@
 // cached address.  All calls share the one
 // array and it keeps the last call's contents, so each call zero-fills the
 // part it uses on its stream before the kernel (a call that gave up waiting
-// may have left ready tags set); calls that overlap on the GPU (for example
+// may have left published words set); calls that overlap on the GPU (for example
 // on two streams) race on the array.
 #include "tern_internal.cuh"
 

@@ -284,7 +284,7 @@ def test_workspace_zero_fills_for_the_gemv_after_a_gemm(monkeypatch):
 
 def test_a_timeout_marks_every_workspace_dirty(monkeypatch):
     """After tern_check reports a bounded wait that gave up, the GEMV may have
-    left ready tags in its workspace: every live Workspace's next ``get``
+    left published partial sums in its workspace: every live Workspace's next ``get``
     zero-fills again (host logic; tern_check and the fill are faked)."""
     fills = []
 
