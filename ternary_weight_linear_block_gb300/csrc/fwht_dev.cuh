@@ -69,14 +69,16 @@ __device__ __forceinline__ void fwht_1024(float (&v)[4][8], int lane) {
 #pragma unroll
   for (int s = 0; s < 5; ++s) {
     const int lm = 1 << s;
-    const bool upper = (lane & lm) != 0;
+    // lower lane: u + v (own + partner); upper lane: u - v (partner - own),
+    // both as one fma with the lane's sign (a product by +-1 is exact and
+    // the fma rounds once: the same result, signed zeros included)
+    const float sg = (lane & lm) != 0 ? -1.f : 1.f;
 #pragma unroll
     for (int ih = 0; ih < 4; ++ih)
 #pragma unroll
       for (int il = 0; il < 8; ++il) {
-        float p = __shfl_xor_sync(kFull, v[ih][il], lm);
-        // lower lane: u + v (own + partner); upper lane: u - v (partner - own)
-        v[ih][il] = upper ? __fsub_rn(p, v[ih][il]) : __fadd_rn(v[ih][il], p);
+        const float p = __shfl_xor_sync(kFull, v[ih][il], lm);
+        v[ih][il] = __fmaf_rn(v[ih][il], sg, p);
       }
   }
   // stages 8, 9: across the 4 register groups
@@ -139,13 +141,13 @@ __device__ __forceinline__ void fwht_512_unscaled(float (&v)[2][8], int lane) {
 #pragma unroll
   for (int s = 0; s < 5; ++s) {
     const int lm = 1 << s;
-    const bool upper = (lane & lm) != 0;
+    const float sg = (lane & lm) != 0 ? -1.f : 1.f;   // as in fwht_1024
 #pragma unroll
     for (int ih = 0; ih < 2; ++ih)
 #pragma unroll
       for (int il = 0; il < 8; ++il) {
-        float p = __shfl_xor_sync(kFull, v[ih][il], lm);
-        v[ih][il] = upper ? __fsub_rn(p, v[ih][il]) : __fadd_rn(v[ih][il], p);
+        const float p = __shfl_xor_sync(kFull, v[ih][il], lm);
+        v[ih][il] = __fmaf_rn(v[ih][il], sg, p);
       }
   }
 #pragma unroll
