@@ -347,11 +347,15 @@ __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int 
 // spread over the whole GPU instead of the blocks' owners.
 constexpr int FIX_THREADS = 256;
 // BATCH slots' loads go out before their adds (in slot order), so a row of
-// S slots costs ceil(S / BATCH) memory round trips.  The launcher takes BATCH = 16 for
-// the blocks with more than 8 owners at M >= 8 and 8 otherwise: measured
-// on GB300, 16 (48 registers) is faster where there are many slots and many
-// tokens, 8 (32 registers) at M <= 4 and on the large grids with few slots
-// (gate/up at M = 16).
+// S slots costs ceil(S / BATCH) memory round trips.  The launcher takes
+// BATCH = 16 (52 registers) when some block has more than 8 owners and the
+// grid has more CTAs than the GPU has SMs, and 8 (32 registers) otherwise.
+// Measured on GB300, GEMV + fixup per call: with at most one fixup CTA per SM
+// the 8-slot batch is faster even at 16 slots (down 17408->5120 at M = 1-7:
+// 10.6-10.9 against 11.5-11.7 us); past one per SM the 16-slot batch is
+// (qkv 5120->10240 at M = 4-8: 8.9-9.1 against 9.6-10.4 us; down and o at
+// M = 8: 11.5 against 12.8 us, 7.9 against 8.7 us).  With 8 slots or fewer
+// one 8-slot round covers them (gate/up at M = 16: 26.3 against 27.6 us).
 template <int BATCH>
 __global__ void __launch_bounds__(FIX_THREADS)
     fixup_kernel(unsigned int* __restrict__ partials, __nv_bfloat16* __restrict__ y, int M, int N,
@@ -1052,7 +1056,8 @@ cudaError_t launch_fixup(const GemvPlan& p, unsigned int* partials, __nv_bfloat1
   if (p.S <= tag) return cudaSuccess;
   const long threads = static_cast<long>(p.RBn) * M * RB;
   const dim3 grid(static_cast<unsigned>((threads + FIX_THREADS - 1) / FIX_THREADS));
-  auto* kern = (M >= 8 && p.S > 8) ? fixup_kernel<16> : fixup_kernel<8>;
+  const bool wide = p.S > 8 && grid.x > static_cast<unsigned>(sm_count());
+  auto* kern = wide ? fixup_kernel<16> : fixup_kernel<8>;
   return launch(kern, grid, dim3(FIX_THREADS), 0, st,
                 partials, y, M, N, G, p.U, p.C, p.S, tag);
 }
