@@ -47,9 +47,11 @@
 // * the weight copies do not depend on the previous kernel, so the producer
 //   issues the first ring of them before the programmatic launch wait, and
 //   every CTA lets the next kernel launch as soon as it starts.
-// * the producer is a warp of its own at M <= 8; at M > 8 it is lane 0 of
-//   consumer warp 0, so that the 512-thread block leaves the two token
-//   tiles' accumulators enough registers (see gemv_merged).
+// * the producer is a warp of its own.  At M > 8 each group's sums are
+//   scaled straight into the accumulators (group scale times the block's
+//   power-of-two fold factor), so that the two token tiles fit the 544-thread
+//   block's registers; at M <= 8 a block's group sums are folded once per
+//   1024-block (see unit_math_direct).
 // All barrier and tag waits are bounded; a wait that gives up sets an error
 // word that tern_check() reports (the workspace must then be re-initialised).
 #include <cuda.h>
@@ -86,16 +88,10 @@ constexpr int STAGES = 4;
 constexpr int CONSUMERS = 16;                   // consumer warps
 constexpr int TPW = TILES / CONSUMERS;          // tiles per consumer warp (2)
 constexpr int NUM_THREADS = 32 * (1 + CONSUMERS);   // a producer warp + the consumers
-// The GEMV's block: at M <= 8 (one n8 token tile) a producer warp and the 16
-// consumer warps; at M > 8 the producer thread is lane 0 of consumer warp 0,
-// so that 512 threads leave the larger accumulators their registers (ptxas
-// holds a 544-thread block to 96 registers per thread, a 512-thread one to
-// 128).  Measured on gate/up: a merged producer costs M = 4 2.5 us per launch,
-// a 96-register M = 16 kernel spills.
-template <int NT> constexpr bool gemv_merged() { return NT == 2; }
-template <int NT> constexpr int gemv_threads() {
-  return gemv_merged<NT>() ? 32 * CONSUMERS : NUM_THREADS;
-}
+// Both token widths run a producer warp and the 16 consumer warps (544
+// threads; the per-SMSP register file holds such a block to 96 registers per
+// thread).  At M > 8 the two n8 token tiles' accumulators fit that only
+// without the per-block sums (see unit_math_direct).
 // Polls of a bounded barrier wait before it gives up: a poll that finds the
 // phase incomplete suspends for about 3.8 us on GB300 (measured with
 // tern_selftest_wait), so 2^18 polls give up after about one second; a
@@ -437,6 +433,55 @@ __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t
   }
 }
 
+// The same MMAs with the group sums scaled straight into acc: the scale of
+// a row's group times the block's fold factor of a token (a power of two, so
+// the product is exact).  The M > 8 kernels use it: without the per-block
+// sums bacc the two token tiles' accumulators fit a 544-thread block's 96
+// registers, which gives them a producer warp of their own (measured on
+// GB300 against a producer thread inside consumer warp 0: gate/up at M = 16
+// 26.3 -> 23.6 us, down 14.8 -> 13.9 us).  At M <= 8 the per-block fold
+// stays: its extra multiply per group cost gate/up 0.6-1.2 us there.
+template <int NT>
+__device__ __forceinline__ void unit_math_direct(const uint4 (&cv)[TPW], const uint32_t (&sp)[TPW],
+                                                 const uint32_t (&bf)[NT][8][2],
+                                                 float (&d)[TPW][NT][4], const float (&f)[NT][2],
+                                                 float (&acc)[TPW][NT][4]) {
+  uint32_t hi[TPW][4];
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt) {
+    hi[tt][0] = cv[tt].x >> 12;
+    hi[tt][1] = cv[tt].y >> 12;
+    hi[tt][2] = cv[tt].z >> 12;
+    hi[tt][3] = cv[tt].w >> 12;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t mask = 0x00030003u << (2 * (j < 6 ? j : j - 6));
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt) {
+      const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
+      uint32_t a[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) a[p] = (j < 6 ? w4[p] : hi[tt][p]) & mask;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_f16(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
+    }
+  }
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt) {
+    uint32_t spv = sp[tt];
+    const float2 s2 = __half22float2(*reinterpret_cast<__half2*>(&spv));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      acc[tt][nt][0] = fmaf(d[tt][nt][0], s2.x * f[nt][0], acc[tt][nt][0]);
+      acc[tt][nt][1] = fmaf(d[tt][nt][1], s2.x * f[nt][1], acc[tt][nt][1]);
+      acc[tt][nt][2] = fmaf(d[tt][nt][2], s2.y * f[nt][0], acc[tt][nt][2]);
+      acc[tt][nt][3] = fmaf(d[tt][nt][3], s2.y * f[nt][1], acc[tt][nt][3]);
+    }
+  }
+}
+
 // End of a 1024-block: acc += bacc * f (f the block's fold factor of the
 // thread's two tokens per n8 tile).
 template <int NT>
@@ -454,7 +499,7 @@ __device__ __forceinline__ void fold_block(float (&acc)[TPW][NT][4], float (&bac
 }
 
 template <int NT>
-__global__ void __launch_bounds__(gemv_threads<NT>(), 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t* __restrict__ packed,
                 const float* __restrict__ aux, int M, int N, int K, __nv_bfloat16* __restrict__ y,
                 unsigned int* __restrict__ partials, int U, int S) {
@@ -487,58 +532,10 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
   // Lane 0 of warp 0 produces: it issues the first STAGES units (the weights
   // before the programmatic launch wait, which they do not depend on, the
   // activation tiles after it), then refills each stage once every consumer
-  // warp has released it -- in its own loop when warp 0 is a producer warp,
-  // or (MERGED) at the top of consumer iteration i, with unit i + STAGES - 1
-  // into the stage unit i - 1 used.
-  constexpr bool MERGED = gemv_merged<NT>();
-  const bool producer = warp == 0 && lane == 0;
+  // warp has released it.
   const uint64_t pol = ptx::l2_policy_evict_first();
   const int pre = n_units < STAGES ? n_units : STAGES;
-  int issued = 0;          // units whose copies lane 0 of warp 0 issued
-  bool prod_ok = true;
-  if constexpr (MERGED) {
-    if (producer) {
-      ptx::prefetch_tmap(&tmX);
-      for (int i = 0; i < pre; ++i) {
-        ptx::mbar_arrive_expect_tx(&full[i], STAGE_TX);
-        ptx::bulk_load_hint(smem + i * STAGE_BYTES + XTILE_BYTES,
-                            packed + static_cast<size_t>(u0 + i) * UNIT_BYTES, UNIT_BYTES,
-                            &full[i], pol);
-      }
-    }
-    pdl_wait();   // activations and their group records come from the previous kernel
-    if (producer) {
-      for (int i = 0; i < pre; ++i) {
-        const int gi = (u0 + i) % G;
-        uint8_t* st = smem + i * STAGE_BYTES;
-        ptx::tma_load_2d(st, &tmX, &full[i], gi * kGroup, 0);
-        ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[i], gi * kGroup + 64, 0);
-        ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(gi) * 48, AUX_BYTES, &full[i]);
-      }
-      issued = pre;
-    }
-  }
-  // unit j into its stage, after the stage's previous unit was released
-  auto produce = [&](int j) {
-    const int s = j % STAGES;
-    const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1u;
-    if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, WAIT_LIMIT)) {
-      if (!*abort_flag) fail(abort_flag, ERR_PRODUCER);
-      prod_ok = false;
-      return;
-    }
-    uint8_t* st = smem + s * STAGE_BYTES;
-    const int gj = (u0 + j) % G;
-    ptx::mbar_arrive_expect_tx(&full[s], STAGE_TX);
-    ptx::bulk_load_hint(st + XTILE_BYTES, packed + static_cast<size_t>(u0 + j) * UNIT_BYTES,
-                        UNIT_BYTES, &full[s], pol);
-    ptx::tma_load_2d(st, &tmX, &full[s], gj * kGroup, 0);
-    ptx::tma_load_2d(st + XTILE_BYTES / 2, &tmX, &full[s], gj * kGroup + 64, 0);
-    ptx::bulk_load(st + AUX_OFF, aux + static_cast<size_t>(gj) * 48, AUX_BYTES, &full[s]);
-    ++issued;
-  };
-
-  if (!MERGED && warp == 0) {
+  if (warp == 0) {
     // ------------------------------------------------ producer warp
     if (lane == 0) {
       ptx::prefetch_tmap(&tmX);
@@ -550,7 +547,7 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
       }
       pdl_wait();   // the activations are written by the previous kernel
       int g = u0 % G;
-      issued = pre;
+      int issued = pre;   // units whose weight copies are issued
       bool ok = true;
       for (int i = 0; i < n_units; ++i) {
         const int s = i % STAGES;
@@ -584,9 +581,9 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
     __syncwarp();
   } else {
     // ------------------------------------------------ consumers
-    const int cw = MERGED ? warp : warp - 1;   // owns tiles TPW*cw .. TPW*cw + TPW-1 of each unit
+    const int cw = warp - 1;   // owns tiles TPW*cw .. TPW*cw + TPW-1 of each unit
     const int gq = lane >> 2, cq = lane & 3;
-    if constexpr (!MERGED) pdl_wait();   // y / ws may still be read by the previous kernel
+    pdl_wait();   // y / ws may still be read by the previous kernel
 
     // Per-lane shared-memory offsets, fixed for the whole kernel.  ldmatrix
     // matrix mi = lane / 8 covers (k16 step j0 + mi / 2, 8-wide k half mi % 2),
@@ -629,10 +626,6 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
       const int seg_len = (n_units - i < G - g) ? n_units - i : G - g;
       const int i_end = i + seg_len;
       for (; i < i_end; ++i) {
-        if (MERGED && warp == 0) {
-          if (lane == 0 && prod_ok && i >= 1 && i + STAGES - 1 < n_units) produce(i + STAGES - 1);
-          __syncwarp();
-        }
         if (!ptx::mbar_wait_warp(&full[s], ph, abort_flag, WAIT_LIMIT)) {
           if (!*abort_flag) fail(abort_flag, ERR_CONSUMER);
           alive = false;
@@ -672,8 +665,12 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
           s = 0;
           ph ^= 1u;
         }
-        unit_math<NT>(cv, sp, bf, d, bacc);
-        if ((g & 7) == 7 || i + 1 == i_end) fold_block<NT>(acc, bacc, fo);
+        if constexpr (NT == 1) {
+          unit_math<NT>(cv, sp, bf, d, bacc);
+          if ((g & 7) == 7 || i + 1 == i_end) fold_block<NT>(acc, bacc, fo);
+        } else {
+          unit_math_direct<NT>(cv, sp, bf, d, fo, acc);
+        }
         ++g;
       }
       if (!alive) break;
@@ -689,14 +686,6 @@ __global__ void __launch_bounds__(gemv_threads<NT>(), 1)
       ++rb;
     }
     __syncwarp();
-  }
-  if (MERGED && producer && (!prod_ok || *abort_flag)) {
-    // let every copy still in flight land before the CTA exits
-    for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i) {
-      const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
-      if (!ptx::mbar_wait_bounded(&full[i % STAGES], ph, WAIT_LIMIT))
-        atomicOr(&g_gemv_error, ERR_DRAIN);
-    }
   }
   __syncthreads();
 }
@@ -937,8 +926,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           s = 0;
           ph ^= 1u;
         }
-        unit_math<NT>(cv, sp, bf, d, bacc);
-        if ((g & 7) == 7 || i + 1 == n_units) fold_block<NT>(acc, bacc, fo);
+        if constexpr (NT == 1) {
+          unit_math<NT>(cv, sp, bf, d, bacc);
+          if ((g & 7) == 7 || i + 1 == n_units) fold_block<NT>(acc, bacc, fo);
+        } else {
+          unit_math_direct<NT>(cv, sp, bf, d, fo, acc);
+        }
         ++g;
       }
       if (!alive) break;
@@ -1025,7 +1018,7 @@ cudaError_t launch_nt(const CUtensorMap& tm, const uint8_t* packed, const float*
                                 static_cast<int>(SMEM_BYTES));
   });
   if (e != cudaSuccess) return e;
-  return launch(gemv_kernel<NT>, dim3(p.C), dim3(gemv_threads<NT>()), SMEM_BYTES, st, tm, packed, xs, M,
+  return launch(gemv_kernel<NT>, dim3(p.C), dim3(NUM_THREADS), SMEM_BYTES, st, tm, packed, xs, M,
                 N, K, y, partials, p.U, p.S);
 }
 
