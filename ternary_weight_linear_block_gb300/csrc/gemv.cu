@@ -225,7 +225,10 @@ __device__ __forceinline__ unsigned int published(float v) {
 // block with more owners would load its first owner with too many slots:
 // there every owner stores its words and the fixup kernel adds them across
 // the whole GPU after the GEMV, and zeroes them.  Between calls every word
-// of the workspace is zero.
+// of the workspace is zero.  The first owner's wait needs its co-owners (the
+// next CTAs in launch order) resident with it: the grid is at most one CTA
+// per SM and one CTA fits an SM; where the GPU cannot hold the whole grid
+// the bounded wait gives up and the call reports a timeout.
 template <int NT>
 __device__ __forceinline__ void end_segment(const float (&acc)[TPW][NT][4], int ga, int gb, int rb,
                                          int G, int U, int C, int S, int M, int N, int cw,
