@@ -268,7 +268,7 @@ def _time_region(fn, steps, stream, ws, lead_cycles=2_000_000):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the timed kernels at the bench's shapes, from one ncu capture on GB300 of
 # the current kernels; they change only when a kernel changes.
-TRAFFIC_GEMV_GATEUP_M4 = 47_480_064 + 6_144           # gemv_kernel<1>, 5120 -> 34816, M = 4
+TRAFFIC_GEMV_GATEUP_M4 = 47_464_192 + 2_048           # gemv_kernel<1>, 5120 -> 34816, M = 4
 TRAFFIC_GEMM_I8_GATEUP_M2048 = 402_740_992 + 130_555_392   # gemm_i8_kernel (CTA pairs, last wave split), M = 2048
 
 
