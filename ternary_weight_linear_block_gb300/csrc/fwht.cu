@@ -121,12 +121,32 @@ __global__ void __launch_bounds__(MAX_THREADS, MIN_CTAS)
   const bool nz = ts > 0.f;
   if (threadIdx.x == 0) tscale[m] = nz ? ts : 0.f;
   OutT* ob = xq + static_cast<long>(m) * K + static_cast<long>(b) * kHBlock;
+  // The code of an element is rint(v / ts) with the quotient correctly
+  // rounded.  The product p = v * (1 / ts), each factor rounded once, lies
+  // within |v / ts| * 2^-23 <= 127.5 * 2^-23 < 2^-16 of the exact quotient
+  // (|v| <= a = 127 ts up to rounding), and the rounded quotient within
+  // 2^-18 of it.  So where p is farther than 2^-15 from every half-integer,
+  // rint(p) is the code; a chunk where some lane's element comes nearer
+  // (a tie or next to one) takes the division.  A token whose reciprocal
+  // scale overflows (subnormal ts) takes the division everywhere.
+  const float r = __fdiv_rn(1.0f, ts);
+  const bool fast = nz && r <= 3.0e38f;
 #pragma unroll
   for (int ih = 0; ih < 4; ++ih) {
     float qv[8];
+    bool near = !fast;
 #pragma unroll
-    for (int t = 0; t < 8; ++t)
-      qv[t] = nz ? fminf(fmaxf(rintf(__fdiv_rn(v[ih][t], ts)), -127.f), 127.f) : 0.f;
+    for (int t = 0; t < 8; ++t) {
+      const float pv = __fmul_rn(v[ih][t], r);
+      qv[t] = rintf(pv);
+      near = near || __fsub_rn(0.5f, fabsf(__fsub_rn(pv, qv[t]))) < 0x1p-15f;
+    }
+    if (__any_sync(0xffffffffu, near)) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) qv[t] = nz ? rintf(__fdiv_rn(v[ih][t], ts)) : 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) qv[t] = fminf(fmaxf(qv[t], -127.f), 127.f);
     store_q8(ob + ih * 256 + lane * 8, qv);
   }
 }
