@@ -387,18 +387,15 @@ __global__ void __launch_bounds__(FIX_THREADS)
   y[static_cast<long>(tok) * N + row] = __float2bfloat16_rn(__fmul_rn(sum, OUT_SCALE));
 }
 
-// The MMAs of one unit for this warp's tiles: codes cv, scale pairs sp and the
-// B fragments bf of the group's 8 k16 steps accumulate into d, which arrives
-// holding the tokens' negated group offsets; the group sums, scaled by the
-// rows' group scales, are added to bacc.  Word p of a tile's slot is A-fragment register p for every step j:
-// one AND per register (steps 6 and 7 from the word shifted right by 12)
-// gives the fp16 pair u * 4^e * 2^-24, u = code + 1; the operand carries
-// 4^-e, and each group's accumulator starts at minus the tokens' offset,
-// which removes the "+1" of u.
+// The MMAs of one unit for this warp's tiles: codes cv and the B fragments bf
+// of the group's 8 k16 steps accumulate into d, which arrives holding the
+// tokens' negated group offsets.  Word p of a tile's slot is A-fragment
+// register p for every step j: one AND per register (steps 6 and 7 from the
+// word shifted right by 12) gives the fp16 pair u * 4^e * 2^-24, u = code +
+// 1; the operand carries 4^-e, and the offset start removes the "+1" of u.
 template <int NT>
-__device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t (&sp)[TPW],
-                                          const uint32_t (&bf)[NT][8][2], float (&d)[TPW][NT][4],
-                                          float (&bacc)[TPW][NT][4]) {
+__device__ __forceinline__ void unit_mma(const uint4 (&cv)[TPW], const uint32_t (&bf)[NT][8][2],
+                                         float (&d)[TPW][NT][4]) {
   uint32_t hi[TPW][4];
 #pragma unroll
   for (int tt = 0; tt < TPW; ++tt) {
@@ -422,6 +419,15 @@ __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t
         mma_f16(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
     }
   }
+}
+
+// One unit at M <= 8: the group sums, scaled by the rows' group scales sp,
+// are added to the 1024-block's sums bacc (folded into acc once per block).
+template <int NT>
+__device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t (&sp)[TPW],
+                                          const uint32_t (&bf)[NT][8][2], float (&d)[TPW][NT][4],
+                                          float (&bacc)[TPW][NT][4]) {
+  unit_mma<NT>(cv, bf, d);
 #pragma unroll
   for (int tt = 0; tt < TPW; ++tt) {
     uint32_t spv = sp[tt];
@@ -436,8 +442,8 @@ __device__ __forceinline__ void unit_math(const uint4 (&cv)[TPW], const uint32_t
   }
 }
 
-// The same MMAs with the group sums scaled straight into acc: the scale of
-// a row's group times the block's fold factor of a token (a power of two, so
+// One unit with the group sums scaled straight into acc: the scale of a
+// row's group times the block's fold factor of a token (a power of two, so
 // the product is exact).  The M > 8 kernels use it: without the per-block
 // sums bacc the two token tiles' accumulators fit a 544-thread block's 96
 // registers, which gives them a producer warp of their own (measured on
@@ -449,28 +455,7 @@ __device__ __forceinline__ void unit_math_direct(const uint4 (&cv)[TPW], const u
                                                  const uint32_t (&bf)[NT][8][2],
                                                  float (&d)[TPW][NT][4], const float (&f)[NT][2],
                                                  float (&acc)[TPW][NT][4]) {
-  uint32_t hi[TPW][4];
-#pragma unroll
-  for (int tt = 0; tt < TPW; ++tt) {
-    hi[tt][0] = cv[tt].x >> 12;
-    hi[tt][1] = cv[tt].y >> 12;
-    hi[tt][2] = cv[tt].z >> 12;
-    hi[tt][3] = cv[tt].w >> 12;
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t mask = 0x00030003u << (2 * (j < 6 ? j : j - 6));
-#pragma unroll
-    for (int tt = 0; tt < TPW; ++tt) {
-      const uint32_t w4[4] = {cv[tt].x, cv[tt].y, cv[tt].z, cv[tt].w};
-      uint32_t a[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) a[p] = (j < 6 ? w4[p] : hi[tt][p]) & mask;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        mma_f16(d[tt][nt], a[0], a[1], a[2], a[3], bf[nt][j][0], bf[nt][j][1]);
-    }
-  }
+  unit_mma<NT>(cv, bf, d);
 #pragma unroll
   for (int tt = 0; tt < TPW; ++tt) {
     uint32_t spv = sp[tt];
